@@ -1,0 +1,412 @@
+"""Pins of the CPU oracle to facts fixed outside of it (no GPU needed).
+
+Each test names the passage of "Вечная математика TurboQuant"
+(blog.sergeynikolenko.ru/?p=11266) or the textbook fact it checks.  A plausible
+slip in the oracle (dropped term, wrong sign, transposed operand, off-by-one
+index) breaks at least one of them.
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+from scipy import integrate, special, stats
+
+import oracle as O
+import synthetic
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _paper():
+    with open(os.path.join(GOLDEN, "paper_values.json")) as f:
+        return json.load(f)
+
+
+# ---------------------------------------------------------------- random numbers
+def test_splitmix64_known_answers():
+    # Published SplitMix64 reference outputs for seed 0.
+    z = O.splitmix64(0, 3)
+    assert [int(v) for v in z] == [0xE220A8397B1DCDAF, 0x6E789E6AA1B965F4, 0x06C45D188009454F]
+
+
+def test_box_muller_is_standard_normal():
+    g = O.gaussian_matrix(12345, 512, 512).ravel()
+    n = g.size
+    assert abs(g.mean()) < 4.0 / math.sqrt(n)
+    assert abs(g.var() - 1.0) < 4.0 * math.sqrt(2.0 / n)
+    assert stats.kstest(g, "norm").pvalue > 1e-3
+
+
+def test_streams_are_independent():
+    # Π and S must come from different draws (community finding #3 on the page).
+    assert O.PI_STREAM_TAG != O.S_STREAM_TAG
+    a = O.gaussian_matrix(7 ^ O.PI_STREAM_TAG, 64, 64).ravel()
+    b = O.gaussian_matrix(7 ^ O.S_STREAM_TAG, 64, 64).ravel()
+    assert abs(np.corrcoef(a, b)[0, 1]) < 4.0 / 64
+
+
+# ---------------------------------------------------------------- Шаг 1: rotation
+@pytest.mark.parametrize("d", [4, 8, 32, 64, 128, 256])
+def test_rotation_is_orthogonal_qr_factor(d):
+    Pi = O.rotation_matrix(d, seed=11)
+    assert np.max(np.abs(Pi.T @ Pi - np.eye(d))) <= 1e-12
+    # Π is the Q factor of the Gaussian draw with a positive-diagonal R: ΠᵀG is
+    # upper triangular with positive diagonal.
+    G = O.gaussian_matrix(11 ^ O.PI_STREAM_TAG, d, d)
+    R = Pi.T @ G
+    assert np.max(np.abs(np.tril(R, -1))) <= 1e-10
+    assert np.all(np.diag(R) > 0)
+
+
+def test_rotation_maps_basis_vector_to_column():
+    # y = Π x̂: the rotated coordinates of e_0 are the first column of Π.
+    p = O.make_params(32, 2, "mse", seed=3)
+    x = np.zeros((1, 32))
+    x[0, 0] = 2.5
+    out = O.quantize(p, x)
+    assert np.allclose(out["y_unit"][0], p.Pi[:, 0], atol=1e-15)
+    assert out["norm"][0] == np.float32(2.5)
+
+
+# ---------------------------------------------------------------- Lemma: f_X
+@pytest.mark.parametrize("d", [4, 8, 64, 128])
+def test_density_normalised_and_moments(d):
+    tot, _ = integrate.quad(lambda x: O.coord_density(x, d), -1, 1, epsabs=0, epsrel=1e-12, limit=200)
+    assert abs(tot - 1.0) < 1e-10
+    # E[X²] = 1/d for a coordinate of a uniform unit vector
+    m2, _ = integrate.quad(lambda x: x * x * O.coord_density(x, d), -1, 1, epsabs=0, epsrel=1e-12, limit=200)
+    assert abs(m2 - 1.0 / d) < 1e-10 / d
+    assert abs(O.coord_cdf(0.0, d) - 0.5) < 1e-15
+    lo, hi = -0.05, 0.13
+    m1, _ = integrate.quad(lambda x: x * O.coord_density(x, d), lo, hi, epsabs=0, epsrel=1e-12)
+    assert abs(O.cell_first_moment(lo, hi, d) - m1) < 1e-12
+    m0, _ = integrate.quad(lambda x: O.coord_density(x, d), lo, hi, epsabs=0, epsrel=1e-12)
+    assert abs(O.cell_mass(lo, hi, d) - m0) < 1e-12
+
+
+def test_density_matches_sphere_samples():
+    # Lemma: a coordinate of a uniform unit vector follows f_X.
+    d = 16
+    x = synthetic.unit_rows(200000, d, seed=5)[:, 0]
+    assert stats.kstest(x, lambda v: O.coord_cdf(v, d)).pvalue > 1e-3
+
+
+# ---------------------------------------------------------------- Шаг 2: Lloyd–Max
+@pytest.mark.parametrize("d", [8, 64, 128, 256])
+def test_b1_centroid_closed_form(d):
+    # b = 1: boundary 0, centroid = E[X | X > 0] = 2∫₀¹ x f_X = Γ(d/2)/(√π Γ((d+1)/2)).
+    c, t = O.lloyd_max_codebook(d, 2)
+    c1 = math.exp(math.lgamma(d / 2) - 0.5 * math.log(math.pi) - math.lgamma((d + 1) / 2))
+    assert abs(c[1] - c1) <= 1e-12 * c1 and abs(c[0] + c1) <= 1e-12 * c1
+    assert t[0] == 0.0
+    assert abs(O.mse_distortion_theory(d, 2) - (1.0 - d * c1 * c1)) < 1e-12
+
+
+def test_page_gaussian_limit_centroids():
+    pv = _paper()["centroids_gaussian_limit"]
+    d = 128
+    c, _ = O.lloyd_max_codebook(d, 2)
+    assert abs(c[1] * math.sqrt(d) - pv["b1_times_sqrt_d"][0]) < 2.0 / d  # O(1/d) finite-d gap
+    c, _ = O.lloyd_max_codebook(d, 4)
+    pos = np.sort(c[c > 0]) * math.sqrt(d)
+    assert np.all(np.abs(pos / np.array(pv["b2_times_sqrt_d"]) - 1.0) < 0.01)
+
+
+def test_max_1960_gaussian_table_at_large_d():
+    # As d grows f_X(√d·) tends to N(0,1); the codebook tends to Max's (1960)
+    # Gaussian Lloyd–Max levels (4 significant digits in that table).
+    table = {4: [0.4528, 1.510], 8: [0.2451, 0.7560, 1.344, 2.152],
+             16: [0.1284, 0.3881, 0.6568, 0.9424, 1.256, 1.618, 2.069, 2.733]}
+    d = 1 << 14
+    for L, ref in table.items():
+        c, _ = O.lloyd_max_codebook(d, L)
+        pos = np.sort(c[c > 0]) * math.sqrt(d)
+        assert np.all(np.abs(pos - np.array(ref)) < 1.5e-3 + 5e-5 * np.array(ref)), (L, pos)
+
+
+@pytest.mark.parametrize("d,L", [(8, 4), (8, 8), (128, 2), (128, 4), (128, 8), (128, 16), (256, 16)])
+def test_lloyd_fixed_point_by_quadrature(d, L):
+    # Both optimality conditions of Шаг 2, checked with adaptive quadrature of f_X
+    # (independent of the incomplete-beta CDF and the closed-form moment).
+    c, t = O.lloyd_max_codebook(d, L)
+    assert np.all(np.diff(c) > 0)
+    assert np.allclose(t, 0.5 * (c[:-1] + c[1:]), rtol=0, atol=0)
+    edges = np.concatenate(([-1.0], t, [1.0]))
+    for i in range(L):
+        m0, _ = integrate.quad(lambda x: O.coord_density(x, d), edges[i], edges[i + 1], epsabs=0, epsrel=1e-13, limit=400)
+        m1, _ = integrate.quad(lambda x: x * O.coord_density(x, d), edges[i], edges[i + 1], epsabs=0, epsrel=1e-13, limit=400)
+        assert abs(m1 / m0 - c[i]) <= 1e-10 * abs(c[i])
+    # symmetric law → symmetric codebook
+    assert np.max(np.abs(c + c[::-1])) < 1e-13
+
+
+# ---------------------------------------------------------------- Theorem 1 (mse)
+@pytest.mark.parametrize("b", [1, 2, 3, 4])
+def test_dmse_identity_and_page_table(b):
+    d = 128
+    p = O.make_params(d, b, "mse", seed=21)
+    X = synthetic.unit_rows(1 << 14, d, seed=100 + b)
+    q = O.quantize(p, X)
+    Xt = O.dequantize(p, q["idx"], q["norm"])
+    err = np.sum((X - Xt) ** 2, axis=1)
+    theory = O.mse_distortion_theory(d, 1 << b)
+    se = err.std() / math.sqrt(err.size)
+    # exact identity D_mse = d·C(f_X, b) from the proof sketch of Theorem 1
+    assert abs(err.mean() - theory) < 4 * se + 1e-6
+    # the page's table (its b=3 entry 0.030 reads low against the integral ≈0.034)
+    tab = _paper()["dmse_table"]["value"][b - 1]
+    assert abs(theory / tab - 1.0) < (0.15 if b == 3 else 0.05)
+    # Shannon lower bound (≥ 4^-b up to 1 − O(1/d)) and the Theorem 1 upper bound
+    # C·4^-b with C = √3·π/2 (the page's "≤ 2.7× Shannon"; see paper_values.json)
+    const = _paper()["theorem1_constant"]["value"]
+    assert abs(const - math.sqrt(3) * math.pi / 2) < 1e-9
+    assert theory >= 4.0 ** -b * (1 - 2.0 / d)
+    assert theory <= const * 4.0 ** -b
+    # the page's lower-bound row is 4^-b
+    assert abs(_paper()["shannon_lower_bound"]["value"][b - 1] - 4.0 ** -b) < 1e-4
+
+
+def test_dmse_scales_with_norm():
+    # Шаг 0: the norm is split off, so distortion scales with ‖x‖².
+    d = 64
+    p = O.make_params(d, 2, "mse", seed=4)
+    X = synthetic.unit_rows(4096, d, seed=8)
+    a = O.dequantize(p, **{k: O.quantize(p, X)[k] for k in ("idx", "norm")})
+    b = O.dequantize(p, **{k: O.quantize(p, 7.0 * X)[k] for k in ("idx", "norm")})
+    assert np.allclose(b, 7.0 * a, rtol=1e-6)
+
+
+def test_mse_bias_b1_over_random_rotations():
+    # «Проблема смещения»: at b = 1 the mse quantizer shrinks inner products by a
+    # factor → 2/π.  Exact finite-d factor: E_Π[x̃] = d·c₁²·x for unit x.
+    d, M = 32, 4000
+    rng = np.random.default_rng(0)
+    x = synthetic.unit_rows(1, d, seed=1)
+    y = rng.standard_normal((1, d))
+    vals = []
+    for s in range(M):
+        p = O.make_params(d, 1, "mse", seed=1000 + s)
+        q = O.quantize(p, x)
+        vals.append(float((O.dequantize(p, q["idx"], q["norm"]) @ y.T)[0, 0]))
+    vals = np.array(vals)
+    c1 = math.exp(math.lgamma(d / 2) - 0.5 * math.log(math.pi) - math.lgamma((d + 1) / 2))
+    expect = d * c1 * c1 * (x @ y.T).item()
+    assert abs(vals.mean() - expect) < 4 * vals.std() / math.sqrt(M)
+    assert abs(d * c1 * c1 - 2 / math.pi) < 1.0 / d
+
+
+# ---------------------------------------------------------------- QJL / Theorem 2 (prod)
+def _prod_samples(d, b, M, x, y, seed0):
+    vals = []
+    for s in range(M):
+        p = O.make_params(d, b, "prod", seed=seed0 + s)
+        q = O.quantize(p, x)
+        xt = O.dequantize(p, q["idx"], q["norm"], q["z"], q["rnorm"])
+        vals.append(float((xt @ y.T)[0, 0]))
+    return np.array(vals)
+
+
+@pytest.mark.parametrize("b", [1, 2, 3])
+def test_prod_unbiased(b):
+    d, M = 32, 3000
+    x = synthetic.unit_rows(1, d, seed=2)
+    y = np.random.default_rng(3).standard_normal((1, d))
+    vals = _prod_samples(d, b, M, x, y, seed0=50000 * b)
+    truth = (x @ y.T).item()
+    assert abs(vals.mean() - truth) < 4 * vals.std() / math.sqrt(M)
+
+
+def test_prod_b1_variance_exact():
+    # b = 1 is pure QJL on r = x: Var = ((π/2)‖y‖² − ⟨x,y⟩²)/d (the QJL lemma's proof).
+    d, M = 32, 6000
+    x = synthetic.unit_rows(1, d, seed=4)
+    y = np.random.default_rng(5).standard_normal((1, d))
+    vals = _prod_samples(d, 1, M, x, y, seed0=7)
+    expect = ((math.pi / 2) * (y @ y.T).item() - (x @ y.T).item() ** 2) / d
+    assert abs(vals.var() / expect - 1.0) < 0.1
+
+
+@pytest.mark.parametrize("b", [2, 3, 4])
+def test_prod_distortion_below_theorem2_table(b):
+    # D_prod ≤ (π/2)·‖y‖²·D_mse(b−1)/d (Theorem 2 proof), which is the page's table.
+    d, n = 128, 8192
+    p = O.make_params(d, b, "prod", seed=31)
+    X = synthetic.unit_rows(n, d, seed=200 + b)
+    Y = np.random.default_rng(9).standard_normal((n, d))
+    q = O.quantize(p, X)
+    Xt = O.dequantize(p, q["idx"], q["norm"], q["z"], q["rnorm"])
+    err = np.sum(Y * (X - Xt), axis=1) ** 2 * d / np.sum(Y * Y, axis=1)
+    bound = math.pi / 2 * O.mse_distortion_theory(d, 1 << (b - 1))
+    se = err.std() / math.sqrt(n)
+    assert err.mean() <= bound + 4 * se
+    assert err.mean() >= 0.5 * bound
+    tab = _paper()["dprod_table"]["value"][b - 1]
+    assert abs(bound / tab - 1.0) < (0.15 if b == 4 else 0.05)
+
+
+def test_prod_residual_norm_matches_mse_distortion():
+    # E‖r‖² = D_mse(b−1) for the unit-scale residual.
+    d, b = 128, 3
+    p = O.make_params(d, b, "prod", seed=12)
+    X = synthetic.unit_rows(8192, d, seed=13)
+    rn = O.quantize(p, X)["rnorm"].astype(np.float64)
+    theory = O.mse_distortion_theory(d, 1 << (b - 1))
+    assert abs(np.mean(rn ** 2) - theory) < 4 * np.std(rn ** 2) / math.sqrt(rn.size)
+
+
+# ---------------------------------------------------------------- nearest centroid
+@pytest.mark.parametrize("d,b", [(4, 1), (4, 2), (4, 3), (8, 1), (8, 2)])
+def test_bucketize_is_brute_force_nearest_codeword(d, b):
+    p = O.make_params(d, b, "mse", seed=5)
+    X = synthetic.unit_rows(64, d, seed=6)
+    q = O.quantize(p, X)
+    L = 1 << b
+    combos = np.array(list(itertools.product(range(L), repeat=d)))
+    words = p.centroids[combos]                       # all L^d codewords
+    for i in range(X.shape[0]):
+        dist = np.sum((q["y_unit"][i][None, :] - words) ** 2, axis=1)
+        assert np.array_equal(combos[np.argmin(dist)], q["idx"][i])
+        per = np.argmin(np.abs(q["y_unit"][i][:, None] - p.centroids[None, :]), axis=1)
+        assert np.array_equal(per, q["idx"][i])
+
+
+def test_zero_row_convention():
+    p = O.make_params(16, 3, "prod", seed=1)
+    q = O.quantize(p, np.zeros((2, 16)))
+    assert np.all(q["idx"] == 0) and np.all(q["z"] == 1)
+    assert np.all(q["norm"] == 0) and np.all(q["rnorm"] == 0)
+    assert np.all(O.dequantize(p, q["idx"], q["norm"], q["z"], q["rnorm"]) == 0)
+
+
+# ---------------------------------------------------------------- packed layout
+def test_pack_golden_bytes():
+    with open(os.path.join(GOLDEN, "pack_layout.txt")) as f:
+        lines = [ln.split("#")[0].split() for ln in f if ln.strip() and not ln.startswith("#")]
+    assert len(lines) == 5
+    for tok in lines:
+        kind, b = tok[0], int(tok[1])
+        vals = tok[2:10]
+        expect = bytes(int(h, 16) for h in tok[10:])
+        if kind == "codes":
+            got = O.pack_codes(np.array([[int(v) for v in vals]]), b)
+            assert got.tobytes() == expect
+            assert np.array_equal(O.unpack_codes(got, 8, b)[0], [int(v) for v in vals])
+        else:
+            z = np.array([[int(v) for v in vals]])
+            got = O.pack_signs(z)
+            assert got.tobytes() == expect
+            assert np.array_equal(O.unpack_signs(got, 8)[0], z[0])
+
+
+@pytest.mark.parametrize("d", [8, 32, 128, 256])
+@pytest.mark.parametrize("b", [1, 2, 3, 4])
+def test_pack_roundtrip(d, b):
+    idx = np.random.default_rng(d * 10 + b).integers(0, 1 << b, size=(17, d))
+    packed = O.pack_codes(idx, b)
+    assert packed.shape == (17, b * d // 8)
+    assert np.array_equal(O.unpack_codes(packed, d, b), idx)
+
+
+# ---------------------------------------------------------------- attention
+def _tiny_cache(B=2, Hkv=2, T=5, d=8, bk=3, bv=2, seed=0):
+    pk = O.make_params(d, bk, "prod", seed=seed + 1)
+    pv = O.make_params(d, bv, "mse", seed=seed + 2)
+    rng = np.random.default_rng(seed)
+    K = rng.standard_normal((B * Hkv * T, d))
+    V = rng.standard_normal((B * Hkv * T, d))
+    return pk, pv, O.quantize(pk, K), O.quantize(pv, V)
+
+
+def test_attention_zero_query_is_mean_of_values():
+    B, Hq, Hkv, T, d = 2, 4, 2, 5, 8
+    pk, pv, kq, vq = _tiny_cache(B, Hkv, T, d)
+    lens = [3, 5]
+    out, _ = O.decode_attention(pk, pv, np.zeros((B, Hq, d)), kq, vq, lens, Hkv, T)
+    Vt = O.dequantize(pv, vq["idx"], vq["norm"]).reshape(B, Hkv, T, d)
+    for b in range(B):
+        for h in range(Hq):
+            assert np.allclose(out[b, h], Vt[b, h // 2, : lens[b]].mean(axis=0), atol=1e-14)
+
+
+def test_attention_single_token_and_empty():
+    B, Hq, Hkv, T, d = 2, 4, 2, 5, 8
+    pk, pv, kq, vq = _tiny_cache(B, Hkv, T, d, seed=3)
+    q = np.random.default_rng(1).standard_normal((B, Hq, d))
+    out, sc = O.decode_attention(pk, pv, q, kq, vq, [1, 0], Hkv, T)
+    Vt = O.dequantize(pv, vq["idx"], vq["norm"]).reshape(B, Hkv, T, d)
+    for h in range(Hq):
+        assert np.allclose(out[0, h], Vt[0, h // 2, 0], atol=1e-14)
+        assert np.all(out[1, h] == 0)
+    assert np.all(np.isnan(sc[1]))
+
+
+def test_attention_brute_force_loops():
+    B, Hq, Hkv, T, d = 2, 4, 2, 5, 8
+    pk, pv, kq, vq = _tiny_cache(B, Hkv, T, d, seed=5)
+    q = np.random.default_rng(2).standard_normal((B, Hq, d))
+    lens = [4, 5]
+    scale = 0.37
+    out, sc = O.decode_attention(pk, pv, q, kq, vq, lens, Hkv, T, scale=scale)
+
+    def deq(p, rows, r):
+        v = [0.0] * d
+        for i in range(d):
+            acc = 0.0
+            for j in range(d):
+                acc += p.Pi[j][i] * p.centroids[rows["idx"][r][j]]
+            if p.variant == "prod":
+                qj = 0.0
+                for j in range(d):
+                    qj += p.S[j][i] * rows["z"][r][j]
+                acc += math.sqrt(math.pi / 2) / d * float(rows["rnorm"][r]) * qj
+            v[i] = float(rows["norm"][r]) * acc
+        return v
+
+    for b in range(B):
+        for h in range(Hq):
+            kv = h // (Hq // Hkv)
+            s = []
+            for t in range(lens[b]):
+                k = deq(pk, kq, (b * Hkv + kv) * T + t)
+                s.append(scale * sum(q[b, h, i] * k[i] for i in range(d)))
+            m = max(s)
+            w = [math.exp(v - m) for v in s]
+            tot = sum(w)
+            o = [0.0] * d
+            for t in range(lens[b]):
+                v = deq(pv, vq, (b * Hkv + kv) * T + t)
+                for i in range(d):
+                    o[i] += w[t] / tot * v[i]
+            assert np.allclose(sc[b, h, : lens[b]], s, atol=1e-12)
+            assert np.allclose(out[b, h], o, atol=1e-12)
+
+
+def test_attention_gqa_grouping_is_contiguous():
+    # Query head h reads KV head h // (Hq/Hkv): make KV head 1's values constant.
+    B, Hq, Hkv, T, d = 1, 4, 2, 6, 8
+    pk, pv, kq, vq = _tiny_cache(B, Hkv, T, d, seed=9)
+    for key in ("idx", "norm"):
+        vq[key][T:2 * T] = vq[key][T]
+    q = np.random.default_rng(4).standard_normal((B, Hq, d))
+    out, _ = O.decode_attention(pk, pv, q, kq, vq, [T], Hkv, T)
+    v1 = O.dequantize(pv, vq["idx"][T:T + 1], vq["norm"][T:T + 1])[0]
+    assert np.allclose(out[0, 2], v1, atol=1e-14) and np.allclose(out[0, 3], v1, atol=1e-14)
+    assert not np.allclose(out[0, 1], v1, atol=1e-3)
+
+
+def test_rotated_domain_score_identity():
+    # ⟨q, x̃⟩ = ‖x‖(⟨Πq, c[idx]⟩ + γ‖r‖⟨Sq, z⟩): the identity a decoder that never
+    # leaves the rotated domain relies on (dequantization rule + ⟨q, Sᵀz⟩ = ⟨Sq, z⟩).
+    B, Hq, Hkv, T, d = 1, 2, 1, 7, 8
+    pk, pv, kq, vq = _tiny_cache(B, Hkv, T, d, seed=11)
+    q = np.random.default_rng(6).standard_normal((B, Hq, d))
+    _, sc = O.decode_attention(pk, pv, q, kq, vq, [T], Hkv, T, scale=1.0)
+    for h in range(Hq):
+        qp = pk.Pi @ q[0, h]
+        qs = pk.S @ q[0, h]
+        s = kq["norm"].astype(np.float64) * (pk.centroids[kq["idx"]] @ qp
+                                             + pk.gamma * kq["rnorm"].astype(np.float64) * (kq["z"] @ qs))
+        assert np.allclose(sc[0, h], s, atol=1e-12)
