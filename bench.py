@@ -1,0 +1,538 @@
+#!/usr/bin/env python3
+"""Benchmark of the TurboQuant hot path on B300: quantize K and V of one layer
+into the packed cache, then one decode-attention step over that cache.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--no-e2e] [--no-cpu-baseline]
+
+Prints ONE JSON line on rank 0.  The metric is
+the algorithmic HBM traffic of the whole step (bytes the packed format forces
+every implementation to move) divided by the device time of the step, in GB/s;
+quantize Mrows/s and decode GB/s are reported alongside.  Inputs are synthetic
+and resident in HBM; L2 is flushed (a 256 MiB write) before every timed step.
+Under torchrun each rank runs the same per-GPU workload on its own device
+(weak scaling; no data-path collective) and the slowest rank's time is used.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import synthetic  # noqa: E402
+
+L2_FLUSH_BYTES = 256 << 20
+# Kernel launches per library call (quantize: 1; decode: query prep, split, merge).
+LAUNCHES = {"quantize": 1, "decode": 3}
+# The arithmetic the path computes in.
+DTYPE_LABEL = "f32"
+QUANT_SOURCES = ["kv_cache_vector_18_b300/csrc/tq_quantize.cu"]
+
+
+# ----------------------------------------------------------------------------- ranks
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def init_dist(world: int, backend: str):
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+
+
+def barrier(world: int):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    if world == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(value: float, world: int, device=None) -> float:
+    if world == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.SUM)
+    return float(t.item())
+
+
+def aggregate_throughput(units_per_rank: float, seconds_per_rank: float, world: int, device=None) -> float:
+    """Whole-job throughput: all units processed by all ranks / the slowest rank's time."""
+    total = sum_over_ranks(units_per_rank, world, device)
+    slowest = max_over_ranks(seconds_per_rank, world, device)
+    return total / slowest if slowest > 0 else float("nan")
+
+
+# ----------------------------------------------------------------------------- workload
+def workload_spec(name: str) -> dict:
+    w = dict(synthetic.WORKLOADS[name])
+    if name == "llama70b_layer_kv_quant":
+        return dict(name=name, B=1, Hq=w["hq"], Hkv=w["heads"], T=w["tokens"], d=w["d"],
+                    k_bits=w["bits"], k_variant=w["variant"], v_bits=w["bits"], v_variant=w["variant"],
+                    dist="outliers", lens=None)
+    if name == "decode_131k":
+        return dict(name=name, B=w["B"], Hq=w["Hq"], Hkv=w["Hkv"], T=w["T"], d=w["d"], k_bits=w["k_bits"],
+                    k_variant=w["k_variant"], v_bits=w["v_bits"], v_variant=w["v_variant"], dist="gauss", lens=None)
+    if name == "batched_decode_32k":
+        return dict(name=name, B=w["B"], Hq=w["Hq"], Hkv=w["Hkv"], T=w["T"], d=w["d"], k_bits=w["k_bits"],
+                    k_variant=w["k_variant"], v_bits=w["v_bits"], v_variant=w["v_variant"], dist="t",
+                    lens=(w["lo"], w["T"]))
+    raise ValueError(name)
+
+
+def make_inputs(spec: dict):
+    """Host tensors (bf16) for K, V [B, Hkv, T, d], q [B, Hq, d] and int32 lengths."""
+    B, Hkv, T, d, Hq = spec["B"], spec["Hkv"], spec["T"], spec["d"], spec["Hq"]
+    if spec["dist"] == "outliers":
+        ch = synthetic.outlier_channels(d, 4, seed=4)
+        K = synthetic.kv_with_outliers(B * Hkv, T, d, seed=0, channels=ch).reshape(B, Hkv, T, d)
+        V = synthetic.kv_with_outliers(B * Hkv, T, d, seed=1, channels=ch).reshape(B, Hkv, T, d)
+    elif spec["dist"] == "t":
+        K = synthetic.student_t_unit_var((B, Hkv, T, d), seed=0)
+        V = synthetic.student_t_unit_var((B, Hkv, T, d), seed=1)
+    else:
+        K = synthetic.gaussian((B, Hkv, T, d), seed=0)
+        V = synthetic.gaussian((B, Hkv, T, d), seed=1)
+    q = synthetic.gaussian((B, Hq, d), seed=2)
+    if spec["lens"] is None:
+        lens = torch.full((B,), T, dtype=torch.int32)
+    else:
+        lens = synthetic.seq_lens_uniform(B, spec["lens"][0], spec["lens"][1], seed=3)
+    return K, V, q, lens
+
+
+def row_bytes(bits: int, variant: str, d: int) -> int:
+    b_m = bits if variant == "mse" else bits - 1
+    return b_m * d // 8 + 4 + ((d // 8 + 4) if variant == "prod" else 0)
+
+
+def traffic_model(spec: dict, lens) -> dict:
+    """Algorithmic bytes: what the packed format forces any implementation to move."""
+    d, B, Hkv, T, Hq = spec["d"], spec["B"], spec["Hkv"], spec["T"], spec["Hq"]
+    n_rows = B * Hkv * T
+    krb, vrb = row_bytes(spec["k_bits"], spec["k_variant"], d), row_bytes(spec["v_bits"], spec["v_variant"], d)
+    qk = n_rows * (2 * d + krb)
+    qv = n_rows * (2 * d + vrb)
+    ctx = int(sum(int(x) for x in lens)) * Hkv
+    dec = ctx * (krb + vrb) + B * Hq * d * 2 + B * Hq * d * 4
+    return dict(n_rows=n_rows, quant_k=qk, quant_v=qv, decode=dec, total=qk + qv + dec,
+                krb=krb, vrb=vrb, ctx_rows=ctx)
+
+
+# ----------------------------------------------------------------------------- clocks
+REASONS = [(0x4, "sw_power_cap"), (0x8, "hw_slowdown"), (0x20, "sw_thermal_slowdown"),
+           (0x40, "hw_thermal_slowdown"), (0x80, "hw_power_brake_slowdown"), (0x2, "applications_clocks_setting"),
+           (0x10, "sync_boost"), (0x100, "display_clock_setting")]
+
+
+class ClockSampler:
+    """Samples the SM clock and clock-event reasons while the timed loop runs:
+    NVML through pynvml when importable, else `nvidia-smi -lms` in the background."""
+
+    def __init__(self, device_index: int, period_s: float = 0.002):
+        self.samples, self.reasons, self.max_mhz = [], 0, None
+        self.period = period_s
+        self.mode = None
+        self.err = ""
+        self.dev = device_index
+        try:
+            import pynvml as N
+            N.nvmlInit()
+            self.N = N
+            self.h = self._handle(N, device_index)
+            self.max_mhz = N.nvmlDeviceGetMaxClockInfo(self.h, N.NVML_CLOCK_SM)
+            self.mode = "nvml"
+        except Exception as e:  # pragma: no cover - depends on the box
+            self.err = repr(e)
+            self.mode = "smi"
+
+    @staticmethod
+    def _uuid(device_index):
+        try:
+            u = str(torch.cuda.get_device_properties(device_index).uuid)
+            return u if u.startswith("GPU-") else "GPU-" + u
+        except Exception:
+            return None
+
+    def _handle(self, N, device_index):
+        u = self._uuid(device_index)
+        if u is not None:
+            try:
+                return N.nvmlDeviceGetHandleByUUID(u)
+            except Exception:
+                pass
+        return N.nvmlDeviceGetHandleByIndex(device_index)
+
+    def _run_nvml(self):
+        N = self.N
+        fn = getattr(N, "nvmlDeviceGetCurrentClocksEventReasons", None) or N.nvmlDeviceGetCurrentClocksThrottleReasons
+        while not self._stop.is_set():
+            try:
+                self.samples.append(N.nvmlDeviceGetClockInfo(self.h, N.NVML_CLOCK_SM))
+                self.reasons |= int(fn(self.h))
+            except Exception:
+                pass
+            time.sleep(self.period)
+
+    def __enter__(self):
+        self._stop = threading.Event()
+        if self.mode == "nvml":
+            self._t = threading.Thread(target=self._run_nvml, daemon=True)
+            self._t.start()
+        else:
+            import subprocess
+            sel = self._uuid(self.dev) or str(self.dev)
+            try:
+                self._p = subprocess.Popen(
+                    ["nvidia-smi", "-i", sel, "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active",
+                     "--format=csv,noheader,nounits", "-lms", "20"],
+                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                time.sleep(0.3)  # let the first samples arrive before the loop starts
+            except Exception as e:
+                self._p = None
+                self.err += " " + repr(e)
+        return self
+
+    def __exit__(self, *a):
+        if self.mode == "nvml":
+            self._stop.set()
+            self._t.join()
+        elif getattr(self, "_p", None) is not None:
+            self._p.terminate()
+            try:
+                out, _ = self._p.communicate(timeout=5)
+            except Exception:
+                self._p.kill()
+                out = ""
+            for ln in out.splitlines():
+                parts = [x.strip() for x in ln.split(",")]
+                try:
+                    self.samples.append(float(parts[0]))
+                    self.max_mhz = float(parts[1])
+                    self.reasons |= int(parts[2], 16)
+                except Exception:
+                    continue
+
+    def summary(self) -> dict:
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "note": self.err or "no samples"}
+        return {"sm_mhz": float(statistics.median(self.samples)), "sm_max_mhz": float(self.max_mhz),
+                "reasons": [n for bit, n in REASONS if self.reasons & bit], "samples": len(self.samples),
+                "via": self.mode}
+
+
+# ----------------------------------------------------------------------------- helpers
+def load_peaks() -> dict:
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"], "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "source": "fallback"}
+
+
+def source_hash(paths) -> str:
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel_key: str, src_hash: str, rows_per_launch: int):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on this source."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f)[kernel_key]
+    except Exception:
+        return None
+    if rec.get("source_hash") != src_hash:
+        return None
+    return rec["dram_bytes_per_row"] * rows_per_launch
+
+
+def blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i["num_threads"] for i in threadpool_info() if i.get("user_api") == "blas"]
+        return int(max(n)) if n else 1
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# ----------------------------------------------------------------------------- oracle timing
+def oracle_sample_run(spec, K, V, q, lens, rows: int, tokens: int, params):
+    """The oracle as it stands on a bounded sample of the workload: quantize ``rows``
+    K rows and V rows, then decode attention over the first ``tokens`` tokens of
+    every (batch, KV head).  Returns the algorithmic bytes of the sample."""
+    import oracle as O
+    pk, pv = params
+    d = spec["d"]
+    Kr = K.reshape(-1, d)
+    Vr = V.reshape(-1, d)
+    O.quantize(pk, Kr[:rows].double().numpy())
+    O.quantize(pv, Vr[:rows].double().numpy())
+    B, Hkv, Hq = spec["B"], spec["Hkv"], spec["Hq"]
+    Ks = K[:, :, :tokens].reshape(-1, d).double().numpy()
+    Vs = V[:, :, :tokens].reshape(-1, d).double().numpy()
+    kq = O.quantize(pk, Ks)
+    vq = O.quantize(pv, Vs)
+    sl = [min(int(x), tokens) for x in lens]
+    O.decode_attention(pk, pv, q.double().numpy(), kq, vq, sl, Hkv, tokens)
+    krb, vrb = row_bytes(spec["k_bits"], spec["k_variant"], d), row_bytes(spec["v_bits"], spec["v_variant"], d)
+    qbytes = rows * (2 * d + krb) + rows * (2 * d + vrb)
+    dbytes = sum(sl) * Hkv * (krb + vrb) + B * Hq * d * 6
+    return qbytes + dbytes, 2 * rows
+
+
+def oracle_params(spec):
+    import oracle as O
+    return (O.make_params(spec["d"], spec["k_bits"], spec["k_variant"], 10),
+            O.make_params(spec["d"], spec["v_bits"], spec["v_variant"], 11))
+
+
+def cpu_baseline(spec, K, V, q, lens, seconds: float = 12.0) -> dict:
+    params = oracle_params(spec)
+    rows, tokens = 4096, 1024
+    oracle_sample_run(spec, K, V, q, lens, 256, 64, params)  # warm caches / BLAS threads
+    t0 = time.perf_counter()
+    nbytes = nrows = reps = 0
+    while time.perf_counter() - t0 < seconds:
+        b, r = oracle_sample_run(spec, K, V, q, lens, rows, tokens, params)
+        nbytes += b
+        nrows += r
+        reps += 1
+    dt = time.perf_counter() - t0
+    return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": blas_threads(), "kind": "oracle",
+            "sample": f"{reps} x (quantize {rows} K + {rows} V rows, decode over the first {tokens} tokens of "
+                      f"all {spec['B']}x{spec['Hkv']} KV heads, {spec['Hq']} query heads); "
+                      f"{dt:.1f} s; float64 NumPy",
+            "quantize_mrows_s": nrows / dt / 1e6}
+
+
+# ----------------------------------------------------------------------------- reference arm
+def run_reference(args, spec):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    K, V, q, lens = make_inputs(spec)
+    params = oracle_params(spec)
+    t0 = time.perf_counter()
+    oracle_sample_run(spec, K, V, q, lens, 512, 128, params)
+    per_unit = time.perf_counter() - t0
+    budget = max(0.5, min(5.0, 150.0 / max(1, args.steps + args.warmup)))
+    scale = max(1.0, budget / max(per_unit, 1e-3))
+    rows, tokens = int(512 * scale), int(128 * scale)
+    rows = min(rows, spec["B"] * spec["Hkv"] * spec["T"])
+    tokens = min(tokens, spec["T"])
+    for _ in range(args.warmup):
+        oracle_sample_run(spec, K, V, q, lens, rows, tokens, params)
+    nbytes = 0
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        b, _r = oracle_sample_run(spec, K, V, q, lens, rows, tokens, params)
+        nbytes += b
+    dt = time.perf_counter() - t0
+    value = nbytes / dt / 1e9
+    line = {"metric": METRIC, "value": value, "unit": "GB/s", "impl": "reference", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / max(args.steps, 1) * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_block(spec),
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": blas_threads(), "kind": "oracle",
+                             "sample": f"per step: quantize {rows} K + {rows} V rows, decode over the first "
+                                       f"{tokens} tokens of every KV head; float64 NumPy"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+METRIC = "compressed-KV decode attention GB/s and quantize Mrows/s, % of B300 HBM peak"
+
+
+def config_block(spec) -> dict:
+    return {"workload": spec["name"], "batch": spec["B"], "kv_heads": spec["Hkv"], "q_heads": spec["Hq"],
+            "tokens": spec["T"], "d": spec["d"], "k": f"{spec['k_variant']} b={spec['k_bits']}",
+            "v": f"{spec['v_variant']} b={spec['v_bits']}",
+            "step": "tq_quantize(K) + tq_quantize(V) + tq_decode_attention over the packed cache",
+            "l2": f"flushed by a {L2_FLUSH_BYTES >> 20} MiB write before every timed step",
+            "inputs": "resident in HBM (value); pinned host buffers (e2e)"}
+
+
+# ----------------------------------------------------------------------------- our arm
+def run_ours(args, spec):
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    import kv_cache_vector_18_b300 as tq
+
+    K, V, q, lens = make_inputs(spec)
+    d, B, Hq, Hkv, T = spec["d"], spec["B"], spec["Hq"], spec["Hkv"], spec["T"]
+    tm = traffic_model(spec, lens.tolist())
+    kq = tq.Quantizer(d, spec["k_bits"], spec["k_variant"], seed=10)
+    vq = tq.Quantizer(d, spec["v_bits"], spec["v_variant"], seed=11)
+    Kd, Vd, qd, ld = K.to(dev).reshape(-1, d), V.to(dev).reshape(-1, d), q.to(dev), lens.to(dev)
+    kc, vc = kq.empty_planes(tm["n_rows"]), vq.empty_planes(tm["n_rows"])
+    ws = torch.empty(tq.decode_workspace_bytes(kq, vq, B, Hq, Hkv, T), dtype=torch.uint8, device=dev)
+    out = torch.empty((B, Hq, d), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record()
+        kq.quantize(Kd, out=kc)
+        if ev is not None:
+            ev[1].record()
+        vq.quantize(Vd, out=vc)
+        if ev is not None:
+            ev[2].record()
+        tq.decode_attention(kq, vq, qd, kc, vc, ld, Hkv, T, workspace=ws, out=out)
+        if ev is not None:
+            ev[3].record()
+
+    for _ in range(max(args.warmup, 0)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    with sampler:
+        wall0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.zero_()
+            step(evs[i])
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+    barrier(world)
+    qk = [e[0].elapsed_time(e[1]) for e in evs]
+    qv = [e[1].elapsed_time(e[2]) for e in evs]
+    dc = [e[2].elapsed_time(e[3]) for e in evs]
+    step_ms = [e[0].elapsed_time(e[3]) for e in evs]
+    t_local = sum(step_ms) / 1e3
+    t_step = max_over_ranks(t_local, world, dev)
+    value = aggregate_throughput(tm["total"] * args.steps, t_local, world, dev) / 1e9
+    quant_s = (sum(qk) + sum(qv)) / 1e3
+    quant_mrows = aggregate_throughput(2 * tm["n_rows"] * args.steps, quant_s, world, dev) / 1e6
+    dec_gbs = aggregate_throughput(tm["decode"] * args.steps, sum(dc) / 1e3, world, dev) / 1e9
+
+    peaks = load_peaks()
+    # dominant kernel: the quantize launch (one per tq_quantize call)
+    q_launch_ms = statistics.mean(qk + qv)
+    bytes_per_launch = (tm["quant_k"] + tm["quant_v"]) / 2
+    achieved = bytes_per_launch / (q_launch_ms / 1e3) / 1e9
+    src = source_hash(QUANT_SOURCES)
+    traffic = recorded_traffic(f"quantize_{spec['k_variant']}_b{spec['k_bits']}_d{d}", src, tm["n_rows"])
+    roofline = {"kernel": "tq_quantize", "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                "peak_source": peaks["source"], "bytes_per_launch": bytes_per_launch,
+                "launch_ms": q_launch_ms, "source_hash": src,
+                "decode_frac": dec_gbs / peaks["hbm_gbs"]}
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = measure_e2e(args, spec, tq, kq, vq, K, V, q, ld, kc, vc, ws, out, tm, dev, world)
+
+    line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": t_step / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": DTYPE_LABEL,
+            "data": "synthetic (seeded NumPy draws, bf16)", "config": config_block(spec),
+            "quantize_mrows_s": quant_mrows, "decode_gbs": dec_gbs,
+            "pct_hbm_peak": value / peaks["hbm_gbs"] * 100.0,
+            "pct_nominal_8tbs": value / 8000.0 * 100.0,
+            "bytes_per_step": tm["total"],
+            "gpu_launches": args.steps * (2 * LAUNCHES["quantize"] + LAUNCHES["decode"]),
+            "clocks": sampler.summary(), "wall_s_timed_loop": wall, "roofline": roofline, "e2e": e2e}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(spec, K, V, q, lens.tolist())
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def measure_e2e(args, spec, tq, kq, vq, K, V, q, ld, kc, vc, ws, out, tm, dev, world):
+    """Same metric through the public API with host buffers: pinned H2D of the
+    step's K, V and q, the three library calls, D2H of the packed planes and
+    the attention output, all inside the timed region."""
+    d, Hkv, T = spec["d"], spec["Hkv"], spec["T"]
+    Kh, Vh, qh = K.reshape(-1, d).pin_memory(), V.reshape(-1, d).pin_memory(), q.pin_memory()
+    Kd = torch.empty_like(Kh, device=dev)
+    Vd = torch.empty_like(Vh, device=dev)
+    qd = torch.empty_like(qh, device=dev)
+    host_planes = [{k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in p.items()} for p in (kc, vc)]
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = Kh.numel() * Kh.element_size() + Vh.numel() * Vh.element_size() + qh.numel() * qh.element_size()
+    d2h = sum(v.numel() * v.element_size() for p in (kc, vc) for v in p.values()) + out.numel() * 4
+
+    def e2e_step():
+        Kd.copy_(Kh, non_blocking=True)
+        Vd.copy_(Vh, non_blocking=True)
+        qd.copy_(qh, non_blocking=True)
+        kq.quantize(Kd, out=kc)
+        vq.quantize(Vd, out=vc)
+        tq.decode_attention(kq, vq, qd, kc, vc, ld, Hkv, T, workspace=ws, out=out)
+        for hp, p in zip(host_planes, (kc, vc)):
+            for k in p:
+                hp[k].copy_(p[k], non_blocking=True)
+        out_h.copy_(out, non_blocking=True)
+
+    n = max(3, min(args.steps, 50))
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    e0.record()
+    for _ in range(n):
+        e2e_step()
+    e1.record()
+    torch.cuda.synchronize()
+    secs = e0.elapsed_time(e1) / 1e3
+    value = aggregate_throughput(tm["total"] * n, secs, world, dev) / 1e9
+    return {"value": value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
+            "ms_per_step": secs / n * 1e3}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="llama70b_layer_kv_quant",
+                    choices=["llama70b_layer_kv_quant", "decode_131k", "batched_decode_32k"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    spec = workload_spec(args.workload)
+    if args.impl == "reference":
+        return run_reference(args, spec)
+    return run_ours(args, spec)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,175 @@
+/*
+ * tq.h — C ABI of the TurboQuant KV-cache codec and compressed-cache decode
+ * attention for NVIDIA B300 (sm_103a).
+ *
+ * Method: "Вечная математика TurboQuant: как сжать KV-кэш до предела Шеннона"
+ * (blog.sergeynikolenko.ru/?p=11266).  Section names below are that page's:
+ *   «Шаг 0» norm split, «Шаг 1» random rotation Π, «Шаг 2» Lloyd–Max codebook
+ *   and nearest-centroid indices, «QJL» 1-bit sketch sign(S·x) with dequantizer
+ *   √(π/2)/d·Sᵀz, «Собственно TurboQuant» (prod: (b−1)-bit mse + QJL of the
+ *   residual, storing sign(S·r) and ‖r‖), Theorem 2 (the prod map).
+ * The decode-attention consumer is the "custom attention kernel" the
+ * nahornyi.ai commentary says the prod variant needs.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Return value: TQ_OK (0) or a negative TQ_E* code; tq_last_error() gives a
+ *   thread-local message for the last failure on the calling thread.  No C++
+ *   exception crosses this boundary and no kernel traps: invalid arguments are
+ *   rejected on the host before any launch.
+ * - "device pointer" arguments must point to memory of the current CUDA device
+ *   (cudaMalloc / torch allocations) and be 16-byte aligned, else TQ_EALIGN or
+ *   TQ_EINVAL.  The caller owns every buffer passed in; the library allocates
+ *   device memory only inside tq_init and frees it in tq_destroy.
+ * - `stream` is a cudaStream_t (NULL = legacy default stream).  All compute calls
+ *   are asynchronous on that stream; they return after enqueueing.
+ * - A handle may be used from several threads for compute calls concurrently;
+ *   tq_destroy must not race with any other call on that handle.
+ *
+ * Packed cache planes (layout owned by this library; the pages leave it open)
+ * --------------------------------------------------------------------------
+ * For a handle with head dimension d, bits b and variant v, let b_m = b (mse) or
+ * b − 1 (prod).  A row of the cache is stored across up to four planes, each a
+ * dense array of n_rows equal-sized records (record i at byte i·record_bytes):
+ *   codes : b_m·d/8 bytes.  Code j (the centroid index of rotated coordinate j)
+ *           occupies bits [j·b_m, (j+1)·b_m) of the record, least significant
+ *           bit first; bit k of the record is bit (k mod 8) of byte (k div 8).
+ *   signs : d/8 bytes (prod only).  Bit i (same bit order) is 1 iff the QJL
+ *           sign of coordinate i of S·r is +1 (sign(0) = +1).
+ *   norm  : float32 ‖x‖₂ of the input row («Шаг 0»).
+ *   rnorm : float32 ‖r‖₂ of the residual of the unit-norm row (prod only).
+ * A zero input row is stored as norm 0, codes 0, signs all +1, rnorm 0.
+ * Decode attention expects the K and V rows of a batch ordered [B][Hkv][T_max].
+ */
+#ifndef TQ_H
+#define TQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define TQ_OK 0
+#define TQ_EINVAL (-1)        /* bad argument value or shape                       */
+#define TQ_EUNSUPPORTED (-2)  /* valid but not implemented (e.g. d not in range)   */
+#define TQ_EALIGN (-3)        /* pointer or stride not 16-byte aligned             */
+#define TQ_ECUDA (-4)         /* CUDA runtime/driver error (message has details)   */
+#define TQ_ENOMEM (-5)        /* device allocation failed in tq_init               */
+#define TQ_EWORKSPACE (-6)    /* workspace smaller than tq_decode_workspace_bytes  */
+
+enum { TQ_MSE = 0, TQ_PROD = 1 };
+enum { TQ_BF16 = 0, TQ_F32 = 1 };
+
+typedef struct tq_ctx* tq_handle;
+
+/* Device pointers to the planes of n_rows packed rows (see above).  signs and
+ * rnorm are ignored (may be NULL) for an mse handle; codes is ignored when
+ * b_m = 0 (prod with b = 1). */
+typedef struct {
+    uint8_t* codes;
+    uint8_t* signs;
+    float* norm;
+    float* rnorm;
+} tq_planes;
+
+/*
+ * tq_init — build one quantizer: Π, S, the Lloyd–Max codebook and its decision
+ * boundaries, all determined by (d, bits, variant, seed), and upload them to the
+ * current CUDA device.
+ *   «Шаг 1»: Π = Q·diag(sign(R_ii)) for G = QR, G a d×d matrix of i.i.d. N(0,1)
+ *            draws (SplitMix64 stream seed ⊕ 0x5049524F54415445, uniform
+ *            (z>>11)·2⁻⁵³, Box–Muller on consecutive pairs, row-major fill).
+ *   «QJL»:   S, d×d i.i.d. N(0,1) from the stream seed ⊕ 0x514A4C534B455443
+ *            (prod only; independent of Π).
+ *   «Шаг 2»: Lloyd–Max codebook with 2^b_m levels for the exact coordinate law
+ *            f_X(x) = Γ(d/2)/(√π Γ((d−1)/2))·(1−x²)^((d−3)/2) on [−1, 1];
+ *            boundaries are midpoints of neighbouring centroids.
+ * d: multiple of 32 in [32, 256].  bits: 1..4 (mse), 1..4 (prod; b = 1 stores
+ * signs only).  variant: TQ_MSE or TQ_PROD.  On success *out owns device memory
+ * until tq_destroy.  Synchronous (blocks on the uploads).
+ */
+int tq_init(int d, int bits, int variant, uint64_t seed, tq_handle* out);
+
+/* Free everything tq_init allocated.  NULL is accepted. */
+int tq_destroy(tq_handle h);
+
+/* Record sizes in bytes of the codes and signs planes (0 when absent). */
+int tq_row_bytes(tq_handle h, int* code_bytes, int* sign_bytes);
+
+/*
+ * Host-only construction of the same parameters tq_init uploads, in float64,
+ * without touching any GPU (for inspection and tests).  Arrays are caller-owned:
+ * Pi [d·d] row-major (y = Π·x), S [d·d] row-major (may be NULL; ignored for mse),
+ * centroids [2^b_m] ascending, bounds [2^b_m − 1] ascending (NULL allowed).
+ */
+int tq_build_params_host(int d, int bits, int variant, uint64_t seed,
+                         double* Pi, double* S, double* centroids, double* bounds);
+
+/* Host copies of a handle's float64 parameters (same layout as above). */
+int tq_get_params(tq_handle h, double* Pi, double* S, double* centroids, double* bounds);
+
+/*
+ * tq_quantize — quantize n_rows rows of x into the packed planes.
+ * «Шаг 0»–«Шаг 2» (mse); «Собственно TurboQuant» for prod.  Per row x:
+ *   norm = ‖x‖₂;  y = Π·x;  code_j = #{k : t_k·norm < y_j} (ties → lower code);
+ *   prod: e = y/norm − c[code] (the residual r = Πᵀe in the rotated frame),
+ *         rnorm = ‖e‖₂, sign bit i = [(S·r)_i ≥ 0] computed as (S·Πᵀ·e)_i.
+ * x: device pointer to n_rows rows of d elements of x_dtype (TQ_BF16 or
+ *    TQ_F32), row i starting x_row_stride elements after row i−1
+ *    (x_row_stride ≥ d; x_row_stride·element size a multiple of 16 bytes).
+ * out: planes with room for n_rows records.  n_rows = 0 is a no-op.
+ */
+int tq_quantize(tq_handle h, const void* x, int x_dtype, int64_t n_rows,
+                int64_t x_row_stride, tq_planes out, void* stream);
+
+/*
+ * tq_dequantize — Q⁻¹ of «Шаг 2» plus, for prod, the QJL reconstruction:
+ *   x̃ = norm·(Πᵀ·c[code] + √(π/2)/d·rnorm·Sᵀ·z),  z_i = ±1 from the sign bits.
+ * y: device pointer to n_rows·d contiguous elements of y_dtype (TQ_F32 or
+ *    TQ_BF16).
+ */
+int tq_dequantize(tq_handle h, tq_planes in, int64_t n_rows, void* y, int y_dtype,
+                  void* stream);
+
+/*
+ * Size in bytes of the device workspace tq_decode_attention needs for these
+ * shapes on the current device (the split count depends on the SM count).
+ */
+int tq_decode_workspace_bytes(tq_handle hk, tq_handle hv, int B, int Hq, int Hkv,
+                              int T_max, size_t* bytes);
+
+/*
+ * tq_decode_attention — one decode query per (batch, query head) attending over
+ * the compressed cache, never materialising dequantized rows:
+ *   q′ = Π_k·q, q″ = S_k·q                     (query rotated once)
+ *   s_t = scale·norm_t·(⟨q′, c_k[code_t]⟩ + √(π/2)/d·rnorm_t·⟨q″, z_t⟩)
+ *        (= scale·⟨q, k̃_t⟩ by the dequantization rule and ⟨q, Sᵀz⟩ = ⟨Sq, z⟩)
+ *   p = softmax(s over t < seq_lens[b]);  o = Π_vᵀ·Σ_t p_t·vnorm_t·c_v[code_t]
+ *   (values accumulated in the rotated frame; Πᵀ applied once at the end).
+ * Query head h reads KV head h / (Hq/Hkv); Hq must be a multiple of Hkv
+ * (Hq ≤ 4096).  hk and hv must share d.
+ * q: device [B, Hq, d] of q_dtype (TQ_F32 or TQ_BF16), contiguous.
+ * kc, vc: planes holding B·Hkv·T_max rows each, ordered [B][Hkv][T_max].
+ * seq_lens: device int32 [B], each in [0, T_max]; an empty context gives o = 0.
+ * scale: softmax scale; ≤ 0 selects 1/√d.
+ * out: device float32 [B, Hq, d].
+ * scores_out: NULL, or device float32 [B, Hq, T_max] receiving the pre-softmax
+ *    s_t for t < seq_lens[b] (entries past the length are not written).
+ * workspace: device buffer of at least tq_decode_workspace_bytes(...) bytes.
+ */
+int tq_decode_attention(tq_handle hk, tq_handle hv, const void* q, int q_dtype,
+                        tq_planes kc, tq_planes vc, const int32_t* seq_lens,
+                        int B, int Hq, int Hkv, int T_max, float scale,
+                        float* out, float* scores_out,
+                        void* workspace, size_t ws_bytes, void* stream);
+
+/* Message for the last error on this thread ("" if none). */
+const char* tq_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TQ_H */

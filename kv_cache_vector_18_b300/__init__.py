@@ -1,0 +1,171 @@
+"""TurboQuant KV-cache codec and compressed-cache decode attention on B300.
+
+Thin Python binding over the C ABI of ``libtq.so`` (include/tq.h).  It only
+marshals arguments: every step of quantization, dequantization and attention
+runs in the library's CUDA kernels.  PyTorch provides device memory and streams.
+There is no CPU fallback: without the built library, importing the compute
+entry points raises ImportError.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+
+import numpy as np
+import torch
+
+from . import _lib
+from ._lib import TQ_BF16, TQ_F32, TQ_MSE, TQ_PROD, TQError, check
+
+__all__ = ["Quantizer", "decode_attention", "decode_workspace_bytes", "build_params_host", "TQError",
+           "library_path"]
+
+_VARIANTS = {"mse": TQ_MSE, "prod": TQ_PROD}
+_DTYPES = {torch.bfloat16: TQ_BF16, torch.float32: TQ_F32}
+
+
+def library_path() -> str:
+    return _lib.LIB_PATH
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def build_params_host(d: int, bits: int, variant: str = "mse", seed: int = 0) -> dict:
+    """Float64 Π, S, centroids and boundaries exactly as tq_init builds them (host only, no GPU)."""
+    L = _lib.lib()
+    b_m = bits if variant == "mse" else bits - 1
+    Pi = np.zeros(d * d)
+    S = np.zeros(d * d)
+    c = np.zeros(1 << b_m)
+    t = np.zeros(max((1 << b_m) - 1, 1))
+    dp = ctypes.POINTER(ctypes.c_double)
+    check(L.tq_build_params_host(d, bits, _VARIANTS[variant], seed, Pi.ctypes.data_as(dp),
+                                 S.ctypes.data_as(dp), c.ctypes.data_as(dp), t.ctypes.data_as(dp)))
+    out = {"Pi": Pi.reshape(d, d), "centroids": c, "bounds": t[: (1 << b_m) - 1]}
+    if variant == "prod":
+        out["S"] = S.reshape(d, d)
+    return out
+
+
+class Quantizer:
+    """One TurboQuant quantizer (tq_init handle) on the current CUDA device."""
+
+    def __init__(self, d: int, bits: int, variant: str = "mse", seed: int = 0):
+        L = _lib.lib()
+        h = ctypes.c_void_p()
+        check(L.tq_init(d, bits, _VARIANTS[variant], seed, ctypes.byref(h)))
+        self._h = h
+        self.d, self.bits, self.variant, self.seed = d, bits, variant, seed
+        self.b_mse = bits if variant == "mse" else bits - 1
+        cb, sb = ctypes.c_int(), ctypes.c_int()
+        check(L.tq_row_bytes(h, ctypes.byref(cb), ctypes.byref(sb)))
+        self.code_bytes, self.sign_bytes = cb.value, sb.value
+        self.device = torch.cuda.current_device()
+
+    @property
+    def handle(self) -> ctypes.c_void_p:
+        return self._h
+
+    def close(self) -> None:
+        if getattr(self, "_h", None) is not None and self._h.value:
+            _lib.lib().tq_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def params(self) -> dict:
+        d, lv = self.d, 1 << self.b_mse
+        Pi, S, c, t = np.zeros(d * d), np.zeros(d * d), np.zeros(lv), np.zeros(max(lv - 1, 1))
+        dp = ctypes.POINTER(ctypes.c_double)
+        check(_lib.lib().tq_get_params(self._h, Pi.ctypes.data_as(dp), S.ctypes.data_as(dp),
+                                       c.ctypes.data_as(dp), t.ctypes.data_as(dp)))
+        out = {"Pi": Pi.reshape(d, d), "centroids": c, "bounds": t[: lv - 1]}
+        if self.variant == "prod":
+            out["S"] = S.reshape(d, d)
+        return out
+
+    def empty_planes(self, n_rows: int, device=None) -> dict:
+        """Allocate packed planes for n_rows rows (see include/tq.h for the layout)."""
+        dev = device if device is not None else torch.device("cuda", self.device)
+        p = {"codes": torch.empty((n_rows, self.code_bytes), dtype=torch.uint8, device=dev),
+             "norm": torch.empty((n_rows,), dtype=torch.float32, device=dev)}
+        if self.variant == "prod":
+            p["signs"] = torch.empty((n_rows, self.sign_bytes), dtype=torch.uint8, device=dev)
+            p["rnorm"] = torch.empty((n_rows,), dtype=torch.float32, device=dev)
+        return p
+
+    @staticmethod
+    def planes_struct(p: dict) -> _lib.Planes:
+        return _lib.Planes(_ptr(p.get("codes")) if p.get("codes") is not None and p["codes"].numel() else None,
+                           _ptr(p.get("signs")), _ptr(p.get("norm")), _ptr(p.get("rnorm")))
+
+    def quantize(self, x: torch.Tensor, out: dict | None = None, stream=None) -> dict:
+        """tq_quantize over the rows of x ([..., d], bf16 or fp32, on the device)."""
+        if x.dim() < 2:
+            raise ValueError("x must have shape [..., d]")
+        x2 = x.reshape(-1, x.shape[-1])
+        n = x2.shape[0]
+        if out is None:
+            out = self.empty_planes(n, x.device)
+        if n == 0:
+            return out
+        if x2.stride(-1) != 1:
+            raise ValueError("x rows must be contiguous")
+        check(_lib.lib().tq_quantize(self._h, _ptr(x2), _DTYPES[x.dtype], n, x2.stride(0),
+                                     self.planes_struct(out), _stream(stream)))
+        return out
+
+    def dequantize(self, planes: dict, n_rows: int | None = None, dtype=torch.float32, stream=None) -> torch.Tensor:
+        n = planes["norm"].shape[0] if n_rows is None else n_rows
+        y = torch.empty((n, self.d), dtype=dtype, device=planes["norm"].device)
+        check(_lib.lib().tq_dequantize(self._h, self.planes_struct(planes), n, _ptr(y), _DTYPES[dtype],
+                                       _stream(stream)))
+        return y
+
+
+def decode_workspace_bytes(kq: Quantizer, vq: Quantizer, B: int, Hq: int, Hkv: int, T_max: int) -> int:
+    n = ctypes.c_size_t()
+    check(_lib.lib().tq_decode_workspace_bytes(kq.handle, vq.handle, B, Hq, Hkv, T_max, ctypes.byref(n)))
+    return n.value
+
+
+def decode_attention(kq: Quantizer, vq: Quantizer, q: torch.Tensor, kcache: dict, vcache: dict,
+                     seq_lens: torch.Tensor, Hkv: int, T_max: int, scale: float | None = None,
+                     return_scores: bool = False, workspace: torch.Tensor | None = None,
+                     out: torch.Tensor | None = None, stream=None):
+    """tq_decode_attention.  q: [B, Hq, d] (bf16/fp32), caches hold B·Hkv·T_max rows
+    ordered [B][Hkv][T_max], seq_lens: int32 [B] on the device.  Returns out
+    [B, Hq, d] fp32 (and the pre-softmax scores [B, Hq, T_max] when asked)."""
+    B, Hq, d = q.shape
+    if not q.is_contiguous():
+        raise ValueError("q must be contiguous")
+    if seq_lens.dtype != torch.int32:
+        raise ValueError("seq_lens must be int32")
+    need = decode_workspace_bytes(kq, vq, B, Hq, Hkv, T_max)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty((B, Hq, d), dtype=torch.float32, device=q.device)
+    scores = torch.full((B, Hq, T_max), float("nan"), dtype=torch.float32, device=q.device) if return_scores else None
+    check(_lib.lib().tq_decode_attention(
+        kq.handle, vq.handle, _ptr(q), _DTYPES[q.dtype], Quantizer.planes_struct(kcache),
+        Quantizer.planes_struct(vcache), _ptr(seq_lens), B, Hq, Hkv, T_max,
+        float(scale) if scale is not None else 0.0, _ptr(out), _ptr(scores), _ptr(workspace),
+        workspace.numel(), _stream(stream)))
+    return (out, scores) if return_scores else out
+
+
+def default_scale(d: int) -> float:
+    return 1.0 / math.sqrt(d)

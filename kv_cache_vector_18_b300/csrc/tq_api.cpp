@@ -1,0 +1,280 @@
+// C ABI entry points of libtq: argument validation, parameter upload, dispatch
+// to the kernel launchers.  Declarations and contracts are in include/tq.h.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <new>
+
+#include "tq_internal.h"
+
+namespace tq {
+
+static thread_local char g_err[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+    return fail(TQ_ECUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+int check_device_ptr(const void* p, const char* name, bool required) {
+    if (p == nullptr) {
+        if (required) return fail(TQ_EINVAL, "%s is NULL", name);
+        return TQ_OK;
+    }
+    if (((uintptr_t)p & 15u) != 0) return fail(TQ_EALIGN, "%s is not 16-byte aligned", name);
+    cudaPointerAttributes attr;
+    cudaError_t e = cudaPointerGetAttributes(&attr, p);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(TQ_EINVAL, "%s is not a CUDA pointer (%s)", name, cudaGetErrorName(e));
+    }
+    if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged)
+        return fail(TQ_EINVAL, "%s is not device memory", name);
+    int dev = -1;
+    cudaGetDevice(&dev);
+    if (attr.device != dev) return fail(TQ_EINVAL, "%s lives on device %d, current is %d", name, attr.device, dev);
+    return TQ_OK;
+}
+
+namespace {
+
+// float → bfloat16 bits, round to nearest even (finite inputs).
+uint16_t f32_to_bf16(float f) {
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    uint32_t lsb = (u >> 16) & 1u;
+    u += 0x7FFFu + lsb;
+    return (uint16_t)(u >> 16);
+}
+
+int upload(const std::vector<float>& host, float** dev) {
+    cudaError_t e = cudaMalloc((void**)dev, host.size() * sizeof(float));
+    if (e != cudaSuccess) {
+        *dev = nullptr;
+        cudaGetLastError();
+        return fail(TQ_ENOMEM, "cudaMalloc of %zu bytes failed", host.size() * sizeof(float));
+    }
+    e = cudaMemcpy(*dev, host.data(), host.size() * sizeof(float), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy (parameter upload)");
+    return TQ_OK;
+}
+
+void free_device(tq_ctx* h) {
+    float** ptrs[] = {&h->dp.Pi, &h->dp.PiT, &h->dp.S, &h->dp.ST, &h->dp.TT};
+    for (float** p : ptrs) {
+        if (*p) cudaFree(*p);
+        *p = nullptr;
+    }
+}
+
+int upload_params(tq_ctx* h) {
+    const HostParams& hp = h->hp;
+    const int d = hp.d;
+    std::vector<float> a((size_t)d * d), b((size_t)d * d);
+    for (int j = 0; j < d; ++j)
+        for (int i = 0; i < d; ++i) {
+            a[(size_t)j * d + i] = (float)hp.Pi[(size_t)j * d + i];
+            b[(size_t)i * d + j] = (float)hp.Pi[(size_t)j * d + i];
+        }
+    int rc = upload(a, &h->dp.Pi);
+    if (rc == TQ_OK) rc = upload(b, &h->dp.PiT);
+    if (rc == TQ_OK && hp.variant == TQ_PROD) {
+        for (int j = 0; j < d; ++j)
+            for (int i = 0; i < d; ++i) {
+                a[(size_t)j * d + i] = (float)hp.S[(size_t)j * d + i];
+                b[(size_t)i * d + j] = (float)hp.S[(size_t)j * d + i];
+            }
+        rc = upload(a, &h->dp.S);
+        if (rc == TQ_OK) rc = upload(b, &h->dp.ST);
+        if (rc == TQ_OK) {
+            // T = S Πᵀ, stored transposed: TT[j*d+i] = T_ij = Σ_k S_ik Π_jk
+            for (int i = 0; i < d; ++i)
+                for (int j = 0; j < d; ++j) {
+                    double acc = 0.0;
+                    for (int k = 0; k < d; ++k) acc += hp.S[(size_t)i * d + k] * hp.Pi[(size_t)j * d + k];
+                    a[(size_t)j * d + i] = (float)acc;
+                }
+            rc = upload(a, &h->dp.TT);
+        }
+    }
+    return rc;
+}
+
+int validate_handle(tq_handle h, const char* name) {
+    if (h == nullptr) return fail(TQ_EINVAL, "%s handle is NULL", name);
+    int dev = -1;
+    cudaGetDevice(&dev);
+    if (dev != h->device) return fail(TQ_EINVAL, "%s handle was created on device %d, current is %d", name, h->device, dev);
+    return TQ_OK;
+}
+
+int check_planes(const tq_ctx& h, const tq_planes& p, const char* what) {
+    char nm[64];
+    int rc;
+    if (h.code_bytes > 0) {
+        snprintf(nm, sizeof nm, "%s.codes", what);
+        if ((rc = check_device_ptr(p.codes, nm, true)) != TQ_OK) return rc;
+    }
+    snprintf(nm, sizeof nm, "%s.norm", what);
+    if ((rc = check_device_ptr(p.norm, nm, true)) != TQ_OK) return rc;
+    if (h.hp.variant == TQ_PROD) {
+        snprintf(nm, sizeof nm, "%s.signs", what);
+        if ((rc = check_device_ptr(p.signs, nm, true)) != TQ_OK) return rc;
+        snprintf(nm, sizeof nm, "%s.rnorm", what);
+        if ((rc = check_device_ptr(p.rnorm, nm, true)) != TQ_OK) return rc;
+    }
+    return TQ_OK;
+}
+
+}  // namespace
+}  // namespace tq
+
+using namespace tq;
+
+extern "C" {
+
+const char* tq_last_error(void) { return g_err; }
+
+int tq_build_params_host(int d, int bits, int variant, uint64_t seed, double* Pi, double* S,
+                         double* centroids, double* bounds) {
+    HostParams hp;
+    int rc = build_host_params(d, bits, variant, seed, &hp);
+    if (rc != TQ_OK) return rc;
+    if (Pi) memcpy(Pi, hp.Pi.data(), hp.Pi.size() * sizeof(double));
+    if (S && variant == TQ_PROD) memcpy(S, hp.S.data(), hp.S.size() * sizeof(double));
+    if (centroids) memcpy(centroids, hp.centroids.data(), hp.centroids.size() * sizeof(double));
+    if (bounds && !hp.bounds.empty()) memcpy(bounds, hp.bounds.data(), hp.bounds.size() * sizeof(double));
+    g_err[0] = 0;
+    return TQ_OK;
+}
+
+int tq_init(int d, int bits, int variant, uint64_t seed, tq_handle* out) {
+    if (out == nullptr) return fail(TQ_EINVAL, "out is NULL");
+    *out = nullptr;
+    tq_ctx* h = new (std::nothrow) tq_ctx();
+    if (!h) return fail(TQ_ENOMEM, "host allocation failed");
+    int rc = build_host_params(d, bits, variant, seed, &h->hp);
+    if (rc != TQ_OK) {
+        delete h;
+        return rc;
+    }
+    cudaError_t e = cudaGetDevice(&h->device);
+    if (e != cudaSuccess) {
+        delete h;
+        return cuda_fail(e, "cudaGetDevice");
+    }
+    h->code_bytes = h->hp.b_mse * d / 8;
+    h->sign_bytes = variant == TQ_PROD ? d / 8 : 0;
+    h->gamma = (float)(sqrt(M_PI / 2.0) / d);
+    memset(&h->cb, 0, sizeof(h->cb));
+    h->cb.levels = h->hp.levels;
+    for (int i = 0; i < h->hp.levels; ++i) h->cb.c[i] = (float)h->hp.centroids[i];
+    for (int i = 0; i + 1 < h->hp.levels; ++i) h->cb.t[i] = (float)h->hp.bounds[i];
+    rc = upload_params(h);
+    if (rc != TQ_OK) {
+        free_device(h);
+        delete h;
+        return rc;
+    }
+    *out = h;
+    g_err[0] = 0;
+    return TQ_OK;
+}
+
+int tq_destroy(tq_handle h) {
+    if (h == nullptr) return TQ_OK;
+    free_device(h);
+    delete h;
+    return TQ_OK;
+}
+
+int tq_row_bytes(tq_handle h, int* code_bytes, int* sign_bytes) {
+    if (h == nullptr) return fail(TQ_EINVAL, "handle is NULL");
+    if (code_bytes) *code_bytes = h->code_bytes;
+    if (sign_bytes) *sign_bytes = h->sign_bytes;
+    return TQ_OK;
+}
+
+int tq_get_params(tq_handle h, double* Pi, double* S, double* centroids, double* bounds) {
+    if (h == nullptr) return fail(TQ_EINVAL, "handle is NULL");
+    const HostParams& hp = h->hp;
+    if (Pi) memcpy(Pi, hp.Pi.data(), hp.Pi.size() * sizeof(double));
+    if (S && hp.variant == TQ_PROD) memcpy(S, hp.S.data(), hp.S.size() * sizeof(double));
+    if (centroids) memcpy(centroids, hp.centroids.data(), hp.centroids.size() * sizeof(double));
+    if (bounds && !hp.bounds.empty()) memcpy(bounds, hp.bounds.data(), hp.bounds.size() * sizeof(double));
+    return TQ_OK;
+}
+
+int tq_quantize(tq_handle h, const void* x, int x_dtype, int64_t n_rows, int64_t x_row_stride,
+                tq_planes out, void* stream) {
+    int rc = validate_handle(h, "quantizer");
+    if (rc != TQ_OK) return rc;
+    if (n_rows < 0) return fail(TQ_EINVAL, "n_rows=%lld is negative", (long long)n_rows);
+    if (x_dtype != TQ_BF16 && x_dtype != TQ_F32) return fail(TQ_EINVAL, "x_dtype=%d invalid", x_dtype);
+    if (n_rows == 0) return TQ_OK;
+    const int d = h->hp.d;
+    const int es = x_dtype == TQ_BF16 ? 2 : 4;
+    if (x_row_stride < d) return fail(TQ_EINVAL, "x_row_stride=%lld < d=%d", (long long)x_row_stride, d);
+    if ((x_row_stride * es) % 16 != 0) return fail(TQ_EALIGN, "x_row_stride*elem_size must be a multiple of 16 bytes");
+    if ((rc = check_device_ptr(x, "x", true)) != TQ_OK) return rc;
+    if ((rc = check_planes(*h, out, "out")) != TQ_OK) return rc;
+    return launch_quantize(*h, x, x_dtype, n_rows, x_row_stride, out, (cudaStream_t)stream);
+}
+
+int tq_dequantize(tq_handle h, tq_planes in, int64_t n_rows, void* y, int y_dtype, void* stream) {
+    int rc = validate_handle(h, "quantizer");
+    if (rc != TQ_OK) return rc;
+    if (n_rows < 0) return fail(TQ_EINVAL, "n_rows=%lld is negative", (long long)n_rows);
+    if (y_dtype != TQ_BF16 && y_dtype != TQ_F32) return fail(TQ_EINVAL, "y_dtype=%d invalid", y_dtype);
+    if (n_rows == 0) return TQ_OK;
+    if ((rc = check_device_ptr(y, "y", true)) != TQ_OK) return rc;
+    if ((rc = check_planes(*h, in, "in")) != TQ_OK) return rc;
+    return launch_dequantize(*h, in, n_rows, y, y_dtype, (cudaStream_t)stream);
+}
+
+int tq_decode_workspace_bytes(tq_handle hk, tq_handle hv, int B, int Hq, int Hkv, int T_max, size_t* bytes) {
+    if (bytes == nullptr) return fail(TQ_EINVAL, "bytes is NULL");
+    int rc = validate_handle(hk, "key");
+    if (rc == TQ_OK) rc = validate_handle(hv, "value");
+    if (rc != TQ_OK) return rc;
+    DecodeShape plan;
+    return decode_plan(*hk, *hv, B, Hq, Hkv, T_max, &plan, bytes);
+}
+
+int tq_decode_attention(tq_handle hk, tq_handle hv, const void* q, int q_dtype, tq_planes kc,
+                        tq_planes vc, const int32_t* seq_lens, int B, int Hq, int Hkv, int T_max,
+                        float scale, float* out, float* scores_out, void* workspace, size_t ws_bytes,
+                        void* stream) {
+    int rc = validate_handle(hk, "key");
+    if (rc == TQ_OK) rc = validate_handle(hv, "value");
+    if (rc != TQ_OK) return rc;
+    if (q_dtype != TQ_BF16 && q_dtype != TQ_F32) return fail(TQ_EINVAL, "q_dtype=%d invalid", q_dtype);
+    DecodeShape plan;
+    size_t need = 0;
+    if ((rc = decode_plan(*hk, *hv, B, Hq, Hkv, T_max, &plan, &need)) != TQ_OK) return rc;
+    if (B == 0 || Hq == 0) return TQ_OK;
+    if (ws_bytes < need) return fail(TQ_EWORKSPACE, "workspace of %zu bytes < required %zu", ws_bytes, need);
+    if ((rc = check_device_ptr(q, "q", true)) != TQ_OK) return rc;
+    if ((rc = check_device_ptr(seq_lens, "seq_lens", true)) != TQ_OK) return rc;
+    if ((rc = check_device_ptr(out, "out", true)) != TQ_OK) return rc;
+    if ((rc = check_device_ptr(scores_out, "scores_out", false)) != TQ_OK) return rc;
+    if ((rc = check_device_ptr(workspace, "workspace", true)) != TQ_OK) return rc;
+    if (T_max > 0) {
+        if ((rc = check_planes(*hk, kc, "kc")) != TQ_OK) return rc;
+        if ((rc = check_planes(*hv, vc, "vc")) != TQ_OK) return rc;
+    }
+    if (scale <= 0.f) scale = (float)(1.0 / sqrt((double)hk->hp.d));
+    return launch_decode(*hk, *hv, plan, q, q_dtype, kc, vc, seq_lens, scale, out, scores_out, workspace,
+                         (cudaStream_t)stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,83 @@
+// Internal declarations shared by the host API and the CUDA kernels of libtq.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+#include <vector>
+
+#include "tq.h"
+
+namespace tq {
+
+constexpr int kMaxLevels = 16;   // 2^b_m with b_m <= 4
+constexpr int kMinD = 32;
+constexpr int kMaxD = 256;
+constexpr int kMaxGroup = 16;    // query heads per KV head
+
+// Codebook passed by value to kernels (lives in the kernel-parameter bank).
+struct Codebook {
+    float c[kMaxLevels];       // centroids, unit-sphere scale, ascending
+    float t[kMaxLevels - 1];   // decision boundaries (midpoints), ascending
+    int levels;                // 2^b_m
+};
+
+// Float64 parameters of one quantizer, as built on the host.
+struct HostParams {
+    int d = 0, bits = 0, variant = 0, b_mse = 0, levels = 0;
+    uint64_t seed = 0;
+    std::vector<double> Pi;         // [d*d] row-major, y = Pi x
+    std::vector<double> S;          // [d*d] row-major (prod)
+    std::vector<double> centroids;  // [levels]
+    std::vector<double> bounds;     // [levels-1]
+};
+
+// Device copies of the matrices in the layouts each kernel reads.
+struct DeviceParams {
+    float* Pi = nullptr;    // [d*d]  Pi[j*d+i] = Π_ji   (column reads over i)
+    float* PiT = nullptr;   // [d*d]  PiT[i*d+j] = Π_ji  (row reads over j)
+    float* S = nullptr;     // [d*d]  S[j*d+i] = S_ji    (prod)
+    float* ST = nullptr;    // [d*d]  ST[i*d+j] = S_ji   (prod)
+    float* TT = nullptr;    // [d*d]  TT[j*d+i] = (S Πᵀ)_ij  (prod)
+};
+
+}  // namespace tq
+
+struct tq_ctx {
+    tq::HostParams hp;
+    tq::DeviceParams dp;
+    tq::Codebook cb;
+    int device = 0;
+    int code_bytes = 0;
+    int sign_bytes = 0;
+    float gamma = 0.f;  // √(π/2)/d
+};
+
+namespace tq {
+
+// Error reporting (thread-local message, returns the code for chaining).
+int fail(int code, const char* fmt, ...);
+int cuda_fail(cudaError_t e, const char* what);
+int check_device_ptr(const void* p, const char* name, bool required);
+
+// Host parameter construction (tq_params.cpp).
+int build_host_params(int d, int bits, int variant, uint64_t seed, HostParams* out);
+
+// Kernel launchers (one per .cu file).  Arguments are validated by the caller.
+int launch_quantize(const tq_ctx& h, const void* x, int x_dtype, int64_t n_rows,
+                    int64_t x_row_stride, const tq_planes& out, cudaStream_t s);
+int launch_dequantize(const tq_ctx& h, const tq_planes& in, int64_t n_rows, void* y,
+                      int y_dtype, cudaStream_t s);
+
+struct DecodeShape {
+    int B, Hq, Hkv, T_max, d, G, n_splits, chunk;
+};
+int decode_plan(const tq_ctx& hk, const tq_ctx& hv, int B, int Hq, int Hkv, int T_max,
+                DecodeShape* plan, size_t* ws_bytes);
+int launch_decode(const tq_ctx& hk, const tq_ctx& hv, const DecodeShape& plan, const void* q,
+                  int q_dtype, const tq_planes& kc, const tq_planes& vc,
+                  const int32_t* seq_lens, float scale, float* out, float* scores_out,
+                  void* workspace, cudaStream_t s);
+
+}  // namespace tq

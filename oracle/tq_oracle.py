@@ -62,7 +62,7 @@ __all__ = [
     "PI_STREAM_TAG", "S_STREAM_TAG", "splitmix64", "uniform01", "gaussian_matrix",
     "rotation_matrix", "qjl_matrix", "coord_density_const", "coord_density",
     "coord_cdf", "cell_mass", "cell_first_moment", "lloyd_max_codebook",
-    "mse_distortion_theory", "Params", "make_params", "quantize", "pack_codes",
+    "mse_distortion_theory", "Params", "make_params", "quantize", "qjl_of_residual", "pack_codes",
     "unpack_codes", "pack_signs", "unpack_signs", "dequantize", "decode_attention",
     "code_bytes_per_row", "sign_bytes_per_row",
 ]
@@ -279,15 +279,24 @@ def quantize(p: Params, X) -> dict:
     idx[~nz] = 0
     out = {"idx": idx.astype(np.int64), "norm": norm.astype(np.float32), "y_unit": y}
     if p.variant == "prod":
-        x_mse = p.centroids[idx] @ p.Pi                  # Q_mse⁻¹: Πᵀ c[idx], row form
-        r = xhat - x_mse                                 # residual r = x − Q_mse⁻¹(Q_mse(x))
-        r[~nz] = 0.0
-        sr = r @ p.S.T                                   # S r
-        z = np.where(sr >= 0.0, 1, -1).astype(np.int8)   # sign, with sign(0) = +1
-        out["z"] = z
-        out["rnorm"] = np.sqrt(np.sum(r * r, axis=1)).astype(np.float32)
-        out["sr"] = sr
+        out.update(qjl_of_residual(p, X, out["idx"]))
     return out
+
+
+def qjl_of_residual(p: Params, X, idx) -> dict:
+    """«Собственно TurboQuant» steps 2–3 for given mse indices: residual
+    r = x̂ − Q_mse⁻¹(idx) = x̂ − Πᵀc[idx], then store sign(S·r) and ‖r‖."""
+    X = np.asarray(X, dtype=np.float64)
+    norm = np.sqrt(np.sum(X * X, axis=1))
+    nz = norm > 0
+    xhat = np.zeros_like(X)
+    xhat[nz] = X[nz] / norm[nz, None]
+    x_mse = p.centroids[np.asarray(idx)] @ p.Pi          # Q_mse⁻¹: rows of (Πᵀ c[idx])ᵀ
+    r = xhat - x_mse                                     # residual r = x − Q_mse⁻¹(Q_mse(x))
+    r[~nz] = 0.0
+    sr = r @ p.S.T                                       # S r
+    z = np.where(sr >= 0.0, 1, -1).astype(np.int8)       # sign, with sign(0) = +1
+    return {"z": z, "rnorm": np.sqrt(np.sum(r * r, axis=1)).astype(np.float32), "sr": sr}
 
 
 def pack_codes(idx, b_mse: int) -> np.ndarray:

@@ -1,0 +1,75 @@
+"""C ABI checks that need no GPU: the library loads, exports every declared
+symbol, and builds the same parameters as the oracle on the host."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle as O
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_symbols():
+    syms = set()
+    for name in os.listdir(os.path.join(ROOT, "include")):
+        if name.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", name)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            syms |= set(re.findall(r"\b(tq_\w+)\s*\(", text))
+    return syms
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from kv_cache_vector_18_b300 import _lib
+    return _lib.lib()
+
+
+def test_library_exports_every_declared_symbol(lib):
+    syms = _declared_symbols()
+    assert {"tq_init", "tq_quantize", "tq_dequantize", "tq_decode_attention"} <= syms
+    for s in sorted(syms):
+        assert hasattr(lib, s), s
+
+
+def test_binding_declares_every_symbol():
+    from kv_cache_vector_18_b300 import _lib
+    assert _declared_symbols() == set(_lib.EXPORTED)
+
+
+@pytest.mark.parametrize("d,b,v", [(32, 1, "mse"), (64, 2, "prod"), (128, 3, "mse"), (128, 3, "prod"),
+                                   (128, 4, "prod"), (256, 4, "mse"), (96, 2, "mse"), (128, 1, "prod")])
+def test_host_params_match_oracle(d, b, v):
+    import kv_cache_vector_18_b300 as tq
+    got = tq.build_params_host(d, b, v, seed=1234)
+    p = O.make_params(d, b, v, 1234)
+    assert np.max(np.abs(got["Pi"] - p.Pi)) <= 1e-12
+    assert np.max(np.abs(got["centroids"] - p.centroids)) <= 1e-12
+    assert np.max(np.abs(got["bounds"] - p.bounds), initial=0.0) <= 1e-12
+    if v == "prod":
+        assert np.max(np.abs(got["S"] - p.S)) <= 1e-12
+
+
+def test_host_params_reject_bad_shapes(lib):
+    from kv_cache_vector_18_b300 import _lib
+    dp = ctypes.POINTER(ctypes.c_double)
+    buf = np.zeros(256 * 256)
+    p = buf.ctypes.data_as(dp)
+    assert lib.tq_build_params_host(33, 2, 0, 0, p, p, p, p) == _lib.TQ_EUNSUPPORTED
+    assert lib.tq_build_params_host(512, 2, 0, 0, p, p, p, p) == _lib.TQ_EUNSUPPORTED
+    assert lib.tq_build_params_host(128, 5, 0, 0, p, p, p, p) == _lib.TQ_EUNSUPPORTED
+    assert lib.tq_build_params_host(128, 0, 1, 0, p, p, p, p) == _lib.TQ_EUNSUPPORTED
+    assert lib.tq_build_params_host(128, 2, 2, 0, p, p, p, p) == _lib.TQ_EINVAL
+    assert b"variant" in lib.tq_last_error()
+
+
+def test_seed_changes_rotation_and_sketch():
+    import kv_cache_vector_18_b300 as tq
+    a = tq.build_params_host(64, 2, "prod", seed=1)
+    b = tq.build_params_host(64, 2, "prod", seed=2)
+    assert np.max(np.abs(a["Pi"] - b["Pi"])) > 0.1 and np.max(np.abs(a["S"] - b["S"])) > 0.1
+    # Π and S drawn from independent streams of the same seed
+    assert abs(np.corrcoef(a["Pi"].ravel(), a["S"].ravel())[0, 1]) < 0.1

@@ -1,0 +1,128 @@
+"""CUDA quantize / dequantize vs the oracle, through the C ABI (needs a GPU)."""
+import numpy as np
+import pytest
+import torch
+
+import synthetic
+from _parity import check_dequant, check_quantize, f64, oracle_params
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tq():
+    import kv_cache_vector_18_b300 as m
+    return m
+
+
+@pytest.mark.parametrize("variant", ["mse", "prod"])
+@pytest.mark.parametrize("bits", [1, 2, 3, 4])
+@pytest.mark.parametrize("d", [32, 64, 128, 256])
+def test_quantize_dequantize_parity(tq, d, bits, variant):
+    n = 1000  # several 128-row tiles and a ragged tail
+    qz = tq.Quantizer(d, bits, variant, seed=1000 + d + bits)
+    x = synthetic.gaussian((n, d), seed=d * 10 + bits, dtype="bf16").cuda()
+    planes = qz.quantize(x)
+    y = qz.dequantize(planes)
+    torch.cuda.synchronize()
+    p = oracle_params(qz)
+    X = f64(x)
+    check_quantize(p, X, planes)
+    check_dequant(p, planes, y)
+
+
+@pytest.mark.parametrize("variant", ["mse", "prod"])
+def test_fp32_input(tq, variant):
+    qz = tq.Quantizer(128, 2, variant, seed=5)
+    x = synthetic.gaussian((4096, 128), seed=0, dtype="f32").cuda()
+    planes = qz.quantize(x)
+    torch.cuda.synchronize()
+    check_quantize(oracle_params(qz), f64(x), planes)
+
+
+@pytest.mark.parametrize("n", [1, 127, 128, 129, 255, 4097])
+def test_ragged_row_counts(tq, n):
+    qz = tq.Quantizer(128, 3, "prod", seed=3)
+    x = synthetic.gaussian((n, 128), seed=n, dtype="bf16").cuda()
+    planes = qz.quantize(x)
+    y = qz.dequantize(planes)
+    torch.cuda.synchronize()
+    p = oracle_params(qz)
+    check_quantize(p, f64(x), planes)
+    check_dequant(p, planes, y)
+
+
+def test_zero_rows_and_strided_input(tq):
+    qz = tq.Quantizer(64, 3, "prod", seed=9)
+    base = synthetic.gaussian((300, 128), seed=4, dtype="bf16").cuda()
+    base[7] = 0
+    base[200] = 0
+    x = base[:, :64]  # row stride 128 elements
+    planes = qz.quantize(x)
+    torch.cuda.synchronize()
+    p = oracle_params(qz)
+    check_quantize(p, f64(x), planes)
+    codes = planes["codes"].cpu().numpy()
+    assert np.all(codes[7] == 0) and np.all(planes["signs"].cpu().numpy()[7] == 255)
+    assert planes["norm"][200].item() == 0 and planes["rnorm"][200].item() == 0
+    y = qz.dequantize(planes)
+    assert torch.all(y[7] == 0)
+
+
+def test_outlier_channels_and_heavy_tails(tq):
+    ch = synthetic.outlier_channels(128, 4, seed=4)
+    x = synthetic.kv_with_outliers(2, 1024, 128, seed=0, channels=ch).reshape(-1, 128).cuda()
+    t = synthetic.student_t_unit_var((2048, 128), seed=3).cuda()
+    for data in (x, t):
+        qz = tq.Quantizer(128, 3, "mse", seed=10)
+        planes = qz.quantize(data)
+        torch.cuda.synchronize()
+        check_quantize(oracle_params(qz), f64(data), planes)
+
+
+def test_empty_and_bf16_dequant(tq):
+    qz = tq.Quantizer(128, 4, "mse", seed=2)
+    x = synthetic.gaussian((0, 128), seed=1).cuda()
+    planes = qz.quantize(x)
+    assert planes["norm"].numel() == 0
+    x = synthetic.gaussian((257, 128), seed=1).cuda()
+    planes = qz.quantize(x)
+    y32 = qz.dequantize(planes)
+    y16 = qz.dequantize(planes, dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert torch.allclose(y16.float(), y32, rtol=1e-2, atol=1e-2)
+
+
+def test_params_match_oracle(tq):
+    for d, b, v in [(128, 3, "prod"), (256, 4, "mse"), (64, 1, "prod")]:
+        qz = tq.Quantizer(d, b, v, seed=77)
+        got = qz.params()
+        p = oracle_params(qz)
+        assert np.max(np.abs(got["Pi"] - p.Pi)) <= 1e-12
+        assert np.max(np.abs(got["centroids"] - p.centroids)) <= 1e-12
+        if v == "prod":
+            assert np.max(np.abs(got["S"] - p.S)) <= 1e-12
+
+
+def test_abi_rejects_bad_arguments(tq):
+    from kv_cache_vector_18_b300 import _lib
+    qz = tq.Quantizer(128, 3, "mse", seed=1)
+    x = torch.zeros((16, 128), dtype=torch.bfloat16, device="cuda")
+    planes = qz.empty_planes(16)
+    L = _lib.lib()
+    st = qz.planes_struct(planes)
+    # host pointer instead of device memory
+    hx = torch.zeros((16, 128), dtype=torch.bfloat16)
+    assert L.tq_quantize(qz.handle, hx.data_ptr(), 0, 16, 128, st, None) == _lib.TQ_EINVAL
+    # misaligned pointer
+    assert L.tq_quantize(qz.handle, x.data_ptr() + 2, 0, 15, 128, st, None) == _lib.TQ_EALIGN
+    # stride smaller than d, bad dtype, negative rows
+    assert L.tq_quantize(qz.handle, x.data_ptr(), 0, 16, 64, st, None) == _lib.TQ_EINVAL
+    assert L.tq_quantize(qz.handle, x.data_ptr(), 7, 16, 128, st, None) == _lib.TQ_EINVAL
+    assert L.tq_quantize(qz.handle, x.data_ptr(), 0, -1, 128, st, None) == _lib.TQ_EINVAL
+    # missing plane
+    bad = _lib.Planes(planes["codes"].data_ptr(), None, None, None)
+    assert L.tq_quantize(qz.handle, x.data_ptr(), 0, 16, 128, bad, None) == _lib.TQ_EINVAL
+    assert L.tq_quantize(None, x.data_ptr(), 0, 16, 128, st, None) == _lib.TQ_EINVAL
+    assert len(L.tq_last_error()) > 0
+    torch.cuda.synchronize()

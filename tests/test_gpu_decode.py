@@ -1,0 +1,111 @@
+"""CUDA decode attention over the packed cache vs the oracle (needs a GPU).
+
+The oracle gets the GPU's own packed cache (unpacked) so that the comparison
+checks the attention path alone; the codec itself is checked in test_gpu_codec.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import synthetic
+from _parity import check_attention, f64, oracle_params, planes_to_oracle_rows
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tq():
+    import kv_cache_vector_18_b300 as m
+    return m
+
+
+def _run(tq, B, Hq, Hkv, T, d, kb, kv, vb, vv, lens, seed=0, dist="gauss", needle=None, q_dtype="bf16",
+         scale=None, return_scores=False):
+    gen = synthetic.gaussian if dist == "gauss" else synthetic.student_t_unit_var
+    K = gen((B, Hkv, T, d), seed=seed + 1)
+    V = gen((B, Hkv, T, d), seed=seed + 2)
+    q = gen((B, Hq, d), seed=seed + 3, dtype=q_dtype)
+    if needle is not None:
+        K = synthetic.plant_needles(K, q, needle["pos"], needle["strength"], Hq // Hkv)
+    kq = tq.Quantizer(d, kb, kv, seed=seed + 11)
+    vq = tq.Quantizer(d, vb, vv, seed=seed + 12)
+    kc = kq.quantize(K.cuda().reshape(-1, d))
+    vc = vq.quantize(V.cuda().reshape(-1, d))
+    sl = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    res = tq.decode_attention(kq, vq, q.cuda(), kc, vc, sl, Hkv, T, scale=scale, return_scores=return_scores)
+    torch.cuda.synchronize()
+    pk, pv = oracle_params(kq), oracle_params(vq)
+    ref_out, ref_sc = O.decode_attention(pk, pv, f64(q), planes_to_oracle_rows(pk, kc),
+                                         planes_to_oracle_rows(pv, vc), lens, Hkv, T, scale=scale)
+    if return_scores:
+        out, sc = res
+        return f64(out), ref_out, f64(sc), ref_sc
+    return f64(res), ref_out
+
+
+@pytest.mark.parametrize("kv,kb", [("prod", 3), ("mse", 3), ("prod", 4), ("mse", 2), ("prod", 1)])
+@pytest.mark.parametrize("vv,vb", [("mse", 3), ("mse", 2), ("prod", 3)])
+def test_decode_variants(tq, kv, kb, vv, vb):
+    g, r = _run(tq, B=2, Hq=8, Hkv=2, T=700, d=128, kb=kb, kv=kv, vb=vb, vv=vv, lens=[700, 333], seed=kb * 7 + vb)
+    check_attention(g, r)
+
+
+@pytest.mark.parametrize("d", [32, 64, 256])
+def test_decode_head_dims(tq, d):
+    g, r = _run(tq, B=1, Hq=4, Hkv=1, T=513, d=d, kb=3, kv="prod", vb=3, vv="mse", lens=[513], seed=d)
+    check_attention(g, r)
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(1, 1), (16, 1), (32, 8), (12, 4)])
+def test_decode_group_sizes(tq, Hq, Hkv):
+    g, r = _run(tq, B=1, Hq=Hq, Hkv=Hkv, T=300, d=128, kb=4, kv="prod", vb=2, vv="mse", lens=[300], seed=Hq)
+    check_attention(g, r)
+
+
+def test_decode_edge_lengths(tq):
+    # empty context, one token, a partial chunk, full capacity
+    g, r = _run(tq, B=4, Hq=8, Hkv=2, T=1000, d=128, kb=3, kv="prod", vb=3, vv="mse", lens=[0, 1, 65, 1000])
+    check_attention(g, r)
+    assert np.all(g[0] == 0)
+
+
+def test_decode_needle(tq):
+    # planted keys aligned with the query make the softmax peak, so 2e-3 max-abs bites
+    g, r = _run(tq, B=1, Hq=8, Hkv=1, T=4096, d=128, kb=3, kv="prod", vb=3, vv="mse", lens=[4096],
+                needle={"pos": [17, 2500], "strength": 40.0}, seed=5)
+    check_attention(g, r)
+    assert np.max(np.abs(r)) > 0.2  # the needle dominates
+
+
+def test_decode_heavy_tailed_fp32_query_and_scale(tq):
+    g, r = _run(tq, B=2, Hq=4, Hkv=2, T=400, d=128, kb=4, kv="prod", vb=2, vv="mse", lens=[400, 250],
+                dist="t", q_dtype="f32", scale=0.2, seed=8)
+    check_attention(g, r)
+
+
+def test_scores_output_small_config(tq):
+    # 64 fp32 queries scored against 4096 keys (mse b=2, d=128)
+    g, r, gs, rs = _run(tq, B=1, Hq=64, Hkv=1, T=4096, d=128, kb=2, kv="mse", vb=2, vv="mse", lens=[4096],
+                        q_dtype="f32", return_scores=True, seed=0)
+    check_attention(g, r)
+    assert np.max(np.abs(gs - rs)) <= 1e-3 * max(1.0, np.max(np.abs(rs)))
+
+
+def test_decode_workspace_too_small(tq):
+    from kv_cache_vector_18_b300 import _lib
+    kq = tq.Quantizer(128, 3, "prod", seed=1)
+    vq = tq.Quantizer(128, 3, "mse", seed=2)
+    K = synthetic.gaussian((256, 128), seed=1).cuda()
+    kc, vc = kq.quantize(K), vq.quantize(K)
+    q = synthetic.gaussian((1, 8, 128), seed=2).cuda()
+    sl = torch.tensor([256], dtype=torch.int32, device="cuda")
+    need = tq.decode_workspace_bytes(kq, vq, 1, 8, 1, 256)
+    ws = torch.empty(need // 2, dtype=torch.uint8, device="cuda")
+    with pytest.raises(tq.TQError) as e:
+        tq.decode_attention(kq, vq, q, kc, vc, sl, 1, 256, workspace=ws)
+    assert e.value.code == _lib.TQ_EWORKSPACE
+    with pytest.raises(tq.TQError):
+        tq.decode_attention(kq, vq, q, kc, vc, sl, 3, 256)  # Hq not a multiple of Hkv
