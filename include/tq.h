@@ -165,6 +165,33 @@ int tq_decode_attention(tq_handle hk, tq_handle hv, const void* q, int q_dtype,
                         float* out, float* scores_out,
                         void* workspace, size_t ws_bytes, void* stream);
 
+/*
+ * tq_decode_attention_noalloc — the same computation and arguments as
+ * tq_decode_attention, minus the workspace.  It is for callers that cannot call
+ * cudaMalloc or hand over a buffer: a serving loop whose device memory is wholly
+ * pre-reserved by another allocator (a new allocation could fail or stall the
+ * stream), or a thin foreign-language binding that holds stream handles but no
+ * device allocator.  The paper has no counterpart; this is a deployment variant.
+ *
+ * Scratch: one file-scope device array of TQ_NOALLOC_WORKSPACE_BYTES (4 MiB),
+ * held by every GPU that loads the library until process exit.  Shapes whose
+ * tq_decode_workspace_bytes exceeds it are rejected with TQ_EWORKSPACE before any
+ * launch.  The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress with that device current); make that first call before
+ * any stream capture.  The call allocates nothing: no cudaMalloc, cudaFree or
+ * allocating library routine.
+ * Every call on a device shares the one array and it keeps the last call's
+ * contents (nothing in it needs clearing: each call writes all it reads).
+ * Calls that overlap on the GPU — on different streams, or from several host
+ * threads without ordering — race on it and give undefined results; serialise
+ * them, e.g. on one stream.
+ */
+#define TQ_NOALLOC_WORKSPACE_BYTES (4u << 20)
+int tq_decode_attention_noalloc(tq_handle hk, tq_handle hv, const void* q, int q_dtype,
+                                tq_planes kc, tq_planes vc, const int32_t* seq_lens,
+                                int B, int Hq, int Hkv, int T_max, float scale,
+                                float* out, float* scores_out, void* stream);
+
 /* Message for the last error on this thread ("" if none). */
 const char* tq_last_error(void);
 
