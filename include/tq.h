@@ -166,6 +166,15 @@ int tq_decode_attention(tq_handle hk, tq_handle hv, const void* q, int q_dtype,
                         void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * Read (and, when clear ≠ 0, reset) the handle's device status word.  Kernels
+ * never spin without bound: a pipeline wait that exceeds its time limit records
+ * a non-zero code there and the kernel returns early (its outputs are then
+ * undefined).  0 means no such event.  Synchronises the calling thread with the
+ * device.
+ */
+int tq_device_status(tq_handle h, int* status, int clear);
+
+/*
  * tq_decode_attention_noalloc — the same computation and arguments as
  * tq_decode_attention, minus the workspace.  It is for callers that cannot call
  * cudaMalloc or hand over a buffer: a serving loop whose device memory is wholly

@@ -96,6 +96,12 @@ class Quantizer:
             out["S"] = S.reshape(d, d)
         return out
 
+    def device_status(self, clear: bool = True) -> int:
+        """Non-zero when a kernel pipeline wait timed out since the last clear."""
+        st = ctypes.c_int()
+        check(_lib.lib().tq_device_status(self._h, ctypes.byref(st), int(clear)))
+        return st.value
+
     def empty_planes(self, n_rows: int, device=None) -> dict:
         """Allocate packed planes for n_rows rows (see include/tq.h for the layout)."""
         dev = device if device is not None else torch.device("cuda", self.device)

@@ -7,6 +7,8 @@
 
 #include <new>
 
+#include <cudaTypedefs.h>
+
 #include "tq_internal.h"
 
 namespace tq {
@@ -74,6 +76,49 @@ void free_device(tq_ctx* h) {
         if (*p) cudaFree(*p);
         *p = nullptr;
     }
+    if (h->dp.Pi_hi) cudaFree(h->dp.Pi_hi);
+    if (h->dp.Pi_lo) cudaFree(h->dp.Pi_lo);
+    if (h->dp.status) cudaFree(h->dp.status);
+    h->dp.Pi_hi = h->dp.Pi_lo = nullptr;
+    h->dp.status = nullptr;
+}
+
+int upload_u16(const std::vector<uint16_t>& host, uint16_t** dev) {
+    cudaError_t e = cudaMalloc((void**)dev, host.size() * sizeof(uint16_t));
+    if (e != cudaSuccess) {
+        *dev = nullptr;
+        cudaGetLastError();
+        return fail(TQ_ENOMEM, "cudaMalloc of %zu bytes failed", host.size() * sizeof(uint16_t));
+    }
+    e = cudaMemcpy(*dev, host.data(), host.size() * sizeof(uint16_t), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy (parameter upload)");
+    return TQ_OK;
+}
+
+float bf16_bits_to_f32(uint16_t b) {
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+// Π = Π_hi + Π_lo in bf16 for the tensor-core rotation, plus their TMA maps.
+int upload_tensor_core_params(tq_ctx* h) {
+    const int d = h->hp.d;
+    std::vector<uint16_t> hi((size_t)d * d), lo((size_t)d * d);
+    for (size_t k = 0; k < hi.size(); ++k) {
+        const double v = h->hp.Pi[k];
+        hi[k] = f32_to_bf16((float)v);
+        lo[k] = f32_to_bf16((float)(v - (double)bf16_bits_to_f32(hi[k])));
+    }
+    int rc = upload_u16(hi, &h->dp.Pi_hi);
+    if (rc == TQ_OK) rc = upload_u16(lo, &h->dp.Pi_lo);
+    if (rc != TQ_OK) return rc;
+    if (d % 64 == 0) {
+        rc = encode_tmap_bf16_2d(&h->dp.tm_pi_hi, h->dp.Pi_hi, d, d, (uint64_t)d * 2, 64, d);
+        if (rc == TQ_OK) rc = encode_tmap_bf16_2d(&h->dp.tm_pi_lo, h->dp.Pi_lo, d, d, (uint64_t)d * 2, 64, d);
+    }
+    return rc;
 }
 
 int upload_params(tq_ctx* h) {
@@ -106,6 +151,16 @@ int upload_params(tq_ctx* h) {
             rc = upload(a, &h->dp.TT);
         }
     }
+    if (rc == TQ_OK) rc = upload_tensor_core_params(h);
+    if (rc == TQ_OK) {
+        cudaError_t e = cudaMalloc((void**)&h->dp.status, sizeof(int));
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return fail(TQ_ENOMEM, "cudaMalloc of the status word failed");
+        }
+        e = cudaMemset(h->dp.status, 0, sizeof(int));
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemset (status word)");
+    }
     return rc;
 }
 
@@ -136,6 +191,31 @@ int check_planes(const tq_ctx& h, const tq_planes& p, const char* what) {
 }
 
 }  // namespace
+
+int encode_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                        uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer) {
+    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    if (encode == nullptr) {
+        cudaDriverEntryPointQueryResult q;
+        void* fn = nullptr;
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr) {
+            cudaGetLastError();
+            return fail(TQ_ECUDA, "cuTensorMapEncodeTiled entry point unavailable");
+        }
+        encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {row_stride_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(TQ_ECUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+    return TQ_OK;
+}
+
 }  // namespace tq
 
 using namespace tq;
@@ -172,6 +252,10 @@ int tq_init(int d, int bits, int variant, uint64_t seed, tq_handle* out) {
         delete h;
         return cuda_fail(e, "cudaGetDevice");
     }
+    if ((e = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device)) != cudaSuccess) {
+        delete h;
+        return cuda_fail(e, "cudaDeviceGetAttribute(SM count)");
+    }
     h->code_bytes = h->hp.b_mse * d / 8;
     h->sign_bytes = variant == TQ_PROD ? d / 8 : 0;
     h->gamma = (float)(sqrt(M_PI / 2.0) / d);
@@ -201,6 +285,19 @@ int tq_row_bytes(tq_handle h, int* code_bytes, int* sign_bytes) {
     if (h == nullptr) return fail(TQ_EINVAL, "handle is NULL");
     if (code_bytes) *code_bytes = h->code_bytes;
     if (sign_bytes) *sign_bytes = h->sign_bytes;
+    return TQ_OK;
+}
+
+int tq_device_status(tq_handle h, int* status, int clear) {
+    int rc = validate_handle(h, "quantizer");
+    if (rc != TQ_OK) return rc;
+    if (status == nullptr) return fail(TQ_EINVAL, "status is NULL");
+    cudaError_t e = cudaMemcpy(status, h->dp.status, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the status word");
+    if (clear && *status != 0) {
+        e = cudaMemset(h->dp.status, 0, sizeof(int));
+        if (e != cudaSuccess) return cuda_fail(e, "clearing the status word");
+    }
     return TQ_OK;
 }
 

@@ -1,6 +1,7 @@
 // Internal declarations shared by the host API and the CUDA kernels of libtq.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -40,6 +41,12 @@ struct DeviceParams {
     float* S = nullptr;     // [d*d]  S[j*d+i] = S_ji    (prod)
     float* ST = nullptr;    // [d*d]  ST[i*d+j] = S_ji   (prod)
     float* TT = nullptr;    // [d*d]  TT[j*d+i] = (S Πᵀ)_ij  (prod)
+    // Tensor-core operands: Π = Π_hi + Π_lo as two bf16 matrices, row-major [j][i].
+    uint16_t* Pi_hi = nullptr;
+    uint16_t* Pi_lo = nullptr;
+    CUtensorMap tm_pi_hi;   // TMA maps over Pi_hi / Pi_lo, box {64, d}, 128-byte swizzle
+    CUtensorMap tm_pi_lo;
+    int* status = nullptr;  // device word: 0, or the code of a bounded wait that expired
 };
 
 }  // namespace tq
@@ -49,6 +56,7 @@ struct tq_ctx {
     tq::DeviceParams dp;
     tq::Codebook cb;
     int device = 0;
+    int num_sms = 0;
     int code_bytes = 0;
     int sign_bytes = 0;
     float gamma = 0.f;  // √(π/2)/d
@@ -64,7 +72,15 @@ int check_device_ptr(const void* p, const char* name, bool required);
 // Host parameter construction (tq_params.cpp).
 int build_host_params(int d, int bits, int variant, uint64_t seed, HostParams* out);
 
+// 2-D bf16 TMA map: `inner` contiguous elements per row, `outer` rows `row_stride_bytes` apart,
+// box {box_inner, box_outer}, 128-byte swizzle, out-of-range elements read as zero.
+int encode_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                        uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer);
+
 // Kernel launchers (one per .cu file).  Arguments are validated by the caller.
+bool quantize_tc_supported(const tq_ctx& h, int x_dtype);
+int launch_quantize_tc(const tq_ctx& h, const void* x, int64_t n_rows, int64_t x_row_stride,
+                       const tq_planes& out, cudaStream_t s);
 int launch_quantize(const tq_ctx& h, const void* x, int x_dtype, int64_t n_rows,
                     int64_t x_row_stride, const tq_planes& out, cudaStream_t s);
 int launch_dequantize(const tq_ctx& h, const tq_planes& in, int64_t n_rows, void* y,

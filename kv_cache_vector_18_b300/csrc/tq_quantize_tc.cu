@@ -1,0 +1,260 @@
+// tq_quantize on the 5th-generation tensor cores (tcgen05 + TMA + TMEM), for
+// bf16 rows and the mse variant («Шаг 0»–«Шаг 2»).
+//
+// Per 128-row tile: Y = X·Πᵀ as two bf16 MMAs into one fp32 TMEM accumulator,
+// Π = Π_hi + Π_lo (Π_hi = bf16(Π), Π_lo = bf16(Π − Π_hi)), so the rotation is
+// accurate to ~2⁻¹⁷ relative while the inputs stay exact bf16.  The epilogue
+// reads the accumulator row per thread, takes ‖y‖ = ‖x‖ (Π orthogonal), counts
+// the norm-scaled Lloyd–Max boundaries below each y_j and packs b-bit codes.
+//
+// Persistent CTAs (one per SM) with warp roles:
+//   warp 0      TMA producer: Π_hi/Π_lo once, then X tiles into a STAGES ring
+//   warp 1      TMEM owner and single-thread MMA issuer (two accumulators)
+//   warps 2..9  two epilogue warpgroups, one per TMEM accumulator
+#include "tq_common.cuh"
+#include "tq_sm100.cuh"
+
+namespace tq {
+namespace {
+
+using namespace sm100;
+
+constexpr int kTile = 128;        // rows per tile (MMA M)
+constexpr int kKC = 64;           // K elements per 128-byte swizzle chunk
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 32 * (2 + kEpiWarps);
+
+template <int D>
+struct TcCfg {
+    static constexpr int kChunks = D / kKC;
+    static constexpr int kStageBytes = kTile * D * 2;
+    static constexpr int kChunkBytesA = kTile * 128;  // one 64-column chunk of a tile
+    static constexpr int kChunkBytesB = D * 128;      // one 64-column chunk of Π
+    static constexpr int kPiBytes = D * D * 2;
+    static constexpr int kStages = D == 64 ? 8 : 4;
+    static constexpr uint32_t kTmemCols = 2 * D < 32 ? 32 : 2 * D;
+    static constexpr size_t kBarOffset = 2 * (size_t)kPiBytes + (size_t)kStages * kStageBytes;
+    static constexpr size_t kSmemBytes = kBarOffset + 256 + 1024;  // barriers + alignment slack
+};
+
+template <int D, int BM>
+__global__ void __launch_bounds__(kThreads, 1)
+quantize_mse_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_pi_hi,
+                       const __grid_constant__ CUtensorMap tm_pi_lo, int64_t n_rows, Codebook cb,
+                       uint8_t* __restrict__ codes, float* __restrict__ norm_out, int* __restrict__ status) {
+    using C = TcCfg<D>;
+    constexpr int L = 1 << BM;
+    constexpr int P = L / 2 - 1;          // positive decision boundaries
+    constexpr int WORDS = BM * D / 32;    // packed 32-bit words per row
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* pi_hi = smem;
+    uint8_t* pi_lo = smem + C::kPiBytes;
+    uint8_t* stages = smem + 2 * C::kPiBytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
+    uint64_t* full = bars;                      // [kStages]
+    uint64_t* empty = bars + C::kStages;        // [kStages]
+    uint64_t* tfull = empty + C::kStages;       // [2]
+    uint64_t* tempty = tfull + 2;               // [2]
+    uint64_t* pi_full = tempty + 2;
+    uint64_t* drain = pi_full + 1;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t ntiles = (n_rows + kTile - 1) / kTile;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&tfull[a], 1);
+            mbar_init(&tempty[a], 128);
+        }
+        mbar_init(pi_full, 1);
+        mbar_init(drain, 1);
+        fence_barrier_init();
+    }
+    if (warp == 1) tmem_alloc(tmem_holder, C::kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------------------ producer
+        prefetch_tensormap(&tm_x);
+        prefetch_tensormap(&tm_pi_hi);
+        prefetch_tensormap(&tm_pi_lo);
+        mbar_arrive_expect_tx(pi_full, 2 * C::kPiBytes);
+        for (int c = 0; c < C::kChunks; ++c) {
+            tma_load_2d(pi_hi + c * C::kChunkBytesB, &tm_pi_hi, pi_full, c * kKC, 0);
+            tma_load_2d(pi_lo + c * C::kChunkBytesB, &tm_pi_lo, pi_full, c * kKC, 0);
+        }
+        int64_t i = 0;
+        for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++i) {
+            const int s = (int)(i % C::kStages);
+            const int64_t u = i / C::kStages;
+            if (u > 0 && !mbar_wait(&empty[s], (uint32_t)((u - 1) & 1), status, 1)) break;
+            mbar_arrive_expect_tx(&full[s], C::kStageBytes);
+            uint8_t* st = stages + (size_t)s * C::kStageBytes;
+            for (int c = 0; c < C::kChunks; ++c)
+                tma_load_2d(st + c * C::kChunkBytesA, &tm_x, &full[s], c * kKC, (int)(tile * kTile));
+        }
+        // Every load issued must have landed before the CTA may exit.
+        const int64_t issued = i;
+        for (int64_t k = (issued > C::kStages ? issued - C::kStages : 0); k < issued; ++k)
+            mbar_wait(&full[k % C::kStages], (uint32_t)((k / C::kStages) & 1), status, 2);
+        mbar_wait(pi_full, 0, status, 2);
+    } else if (warp == 1 && lane == 0) {
+        // ------------------------------------------------------------ MMA issuer
+        constexpr uint32_t idesc = idesc_bf16_f32(kTile, D);
+        bool ok = mbar_wait(pi_full, 0, status, 3);
+        tc_fence_after();
+        const uint32_t a_base = smem_u32(stages), hi_base = smem_u32(pi_hi), lo_base = smem_u32(pi_lo);
+        int64_t i = 0;
+        for (int64_t tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x, ++i) {
+            const int s = (int)(i % C::kStages);
+            const int acc = (int)(i & 1);
+            const int64_t ua = i >> 1;
+            if (!(ok = mbar_wait(&full[s], (uint32_t)((i / C::kStages) & 1), status, 4))) break;
+            if (ua > 0 && !(ok = mbar_wait(&tempty[acc], (uint32_t)((ua - 1) & 1), status, 5))) break;
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + (uint32_t)(acc * D);
+            const uint32_t a_stage = a_base + (uint32_t)(s * C::kStageBytes);
+#pragma unroll
+            for (int pass = 0; pass < 2; ++pass) {
+                const uint32_t b_base = pass == 0 ? hi_base : lo_base;
+#pragma unroll
+                for (int c = 0; c < C::kChunks; ++c)
+#pragma unroll
+                    for (int kk = 0; kk < kKC / 16; ++kk) {
+                        const uint64_t ad = smem_desc(a_stage + c * C::kChunkBytesA + kk * 32, 1024, 2);
+                        const uint64_t bd = smem_desc(b_base + c * C::kChunkBytesB + kk * 32, 1024, 2);
+                        mma_f16_ss(d_tmem, ad, bd, idesc, (pass | c | kk) != 0);
+                    }
+            }
+            mma_commit(&empty[s]);
+            mma_commit(&tfull[acc]);
+        }
+        mma_commit(drain);
+        mbar_wait(drain, 0, status, 6);
+    } else if (warp >= 2) {
+        // ------------------------------------------------------------ epilogue
+        const int wg = (warp - 2) >> 2;                 // accumulator served
+        const int quad = warp & 3;                      // TMEM lane quadrant of this warp
+        const int r_local = quad * 32 + lane;
+        float tpos[P > 0 ? P : 1];
+#pragma unroll
+        for (int p = 0; p < P; ++p) tpos[p] = cb.t[L / 2 + p];
+        const uint32_t taddr0 = tmem_base + (uint32_t)(wg * D) + ((uint32_t)(quad * 32) << 16);
+        int64_t j = 0;
+        for (int64_t tile = blockIdx.x + (int64_t)wg * gridDim.x; tile < ntiles; tile += 2 * (int64_t)gridDim.x, ++j) {
+            if (!mbar_wait(&tfull[wg], (uint32_t)(j & 1), status, 7)) break;
+            tc_fence_after();
+            uint32_t r[32];
+            float ss = 0.f;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                tmem_ld32(taddr0 + c * 32, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int k = 0; k < 32; ++k) ss = fmaf(__uint_as_float(r[k]), __uint_as_float(r[k]), ss);
+            }
+            const float n = sqrtf(ss);
+            float thr[P > 0 ? P : 1];
+#pragma unroll
+            for (int p = 0; p < P; ++p) thr[p] = n * tpos[p];
+            uint32_t words[WORDS];
+#pragma unroll
+            for (int w = 0; w < WORDS; ++w) words[w] = 0u;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                tmem_ld32(taddr0 + c * 32, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                    const float v = __uint_as_float(r[k]);
+                    const float a = fabsf(v);
+                    uint32_t base = (uint32_t)(L / 2 - 1);
+#pragma unroll
+                    for (int p = 0; p < P; ++p) base -= (a > thr[p]) ? 1u : 0u;
+                    const uint32_t code = base ^ ((v > 0.f) ? (uint32_t)(L - 1) : 0u);
+                    const int bit = k * BM;
+                    const int w = c * BM + (bit >> 5), sh = bit & 31;
+                    words[w] |= code << sh;
+                    if (sh + BM > 32) words[w + 1] |= code >> (32 - sh);
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&tempty[wg]);
+            const int64_t row = tile * kTile + r_local;
+            if (row < n_rows) {
+                uint8_t* dst = codes + row * (int64_t)(WORDS * 4);
+                if constexpr ((WORDS % 4) == 0) {
+#pragma unroll
+                    for (int w = 0; w < WORDS; w += 4)
+                        *reinterpret_cast<uint4*>(dst + 4 * w) = make_uint4(words[w], words[w + 1], words[w + 2], words[w + 3]);
+                } else {
+#pragma unroll
+                    for (int w = 0; w < WORDS; w += 2)
+                        *reinterpret_cast<uint2*>(dst + 4 * w) = make_uint2(words[w], words[w + 1]);
+                }
+                norm_out[row] = n;
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, C::kTmemCols);
+    }
+}
+
+template <int D, int BM>
+int launch_tc(const tq_ctx& h, const CUtensorMap& tm_x, int64_t n_rows, const tq_planes& out, cudaStream_t s) {
+    using C = TcCfg<D>;
+    auto fn = quantize_mse_tc_kernel<D, BM>;
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemBytes);
+    if (e != cudaSuccess) return cuda_fail(e, "quantize smem attribute");
+    const int64_t ntiles = (n_rows + kTile - 1) / kTile;
+    const int grid = (int)(ntiles < h.num_sms ? ntiles : h.num_sms);
+    fn<<<grid, kThreads, C::kSmemBytes, s>>>(tm_x, h.dp.tm_pi_hi, h.dp.tm_pi_lo, n_rows, h.cb, out.codes, out.norm,
+                                             h.dp.status);
+    e = cudaGetLastError();
+    return e == cudaSuccess ? TQ_OK : cuda_fail(e, "tensor-core quantize launch");
+}
+
+template <int D>
+int launch_tc_d(const tq_ctx& h, const CUtensorMap& tm_x, int64_t n_rows, const tq_planes& out, cudaStream_t s) {
+    switch (h.hp.b_mse) {
+        case 1: return launch_tc<D, 1>(h, tm_x, n_rows, out, s);
+        case 2: return launch_tc<D, 2>(h, tm_x, n_rows, out, s);
+        case 3: return launch_tc<D, 3>(h, tm_x, n_rows, out, s);
+        case 4: return launch_tc<D, 4>(h, tm_x, n_rows, out, s);
+        default: return fail(TQ_EUNSUPPORTED, "b_m=%d", h.hp.b_mse);
+    }
+}
+
+}  // namespace
+
+bool quantize_tc_supported(const tq_ctx& h, int x_dtype) {
+    return x_dtype == TQ_BF16 && h.hp.variant == TQ_MSE && (h.hp.d == 64 || h.hp.d == 128) &&
+           h.dp.Pi_hi != nullptr && h.num_sms > 0;
+}
+
+int launch_quantize_tc(const tq_ctx& h, const void* x, int64_t n_rows, int64_t stride, const tq_planes& out,
+                       cudaStream_t s) {
+    CUtensorMap tm_x;
+    int rc = encode_tmap_bf16_2d(&tm_x, x, (uint64_t)h.hp.d, (uint64_t)n_rows, (uint64_t)stride * 2, kKC, kTile);
+    if (rc != TQ_OK) return rc;
+    switch (h.hp.d) {
+        case 64: return launch_tc_d<64>(h, tm_x, n_rows, out, s);
+        case 128: return launch_tc_d<128>(h, tm_x, n_rows, out, s);
+        default: return fail(TQ_EUNSUPPORTED, "tensor-core quantize: d=%d", h.hp.d);
+    }
+}
+
+}  // namespace tq

@@ -29,6 +29,7 @@ def test_quantize_dequantize_parity(tq, d, bits, variant):
     X = f64(x)
     check_quantize(p, X, planes)
     check_dequant(p, planes, y)
+    assert qz.device_status() == 0
 
 
 @pytest.mark.parametrize("variant", ["mse", "prod"])
@@ -126,3 +127,23 @@ def test_abi_rejects_bad_arguments(tq):
     assert L.tq_quantize(None, x.data_ptr(), 0, 16, 128, st, None) == _lib.TQ_EINVAL
     assert len(L.tq_last_error()) > 0
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("bits", [1, 2, 3, 4])
+def test_tensor_core_path_many_tiles(tq, d, bits):
+    # enough rows for several tiles per CTA on every SM, plus a ragged tail
+    n = 148 * 128 * 3 + 77
+    qz = tq.Quantizer(d, bits, "mse", seed=7 + bits)
+    x = synthetic.gaussian((n, d), seed=bits + d).cuda()
+    planes = qz.quantize(x)
+    torch.cuda.synchronize()
+    assert qz.device_status() == 0
+    rows = np.concatenate([np.arange(0, 300), np.arange(n - 300, n),
+                           np.random.default_rng(0).choice(n, 3000, replace=False)])
+    check_quantize(oracle_params(qz), f64(x), planes, rows=rows)
+    # repeat into the same planes: results must be identical
+    codes0 = planes["codes"].clone()
+    qz.quantize(x, out=planes)
+    torch.cuda.synchronize()
+    assert torch.equal(codes0, planes["codes"])
