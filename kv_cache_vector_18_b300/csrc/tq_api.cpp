@@ -7,6 +7,7 @@
 
 #include <new>
 
+#include <cuda_fp16.h>
 #include <cudaTypedefs.h>
 
 #include "tq_internal.h"
@@ -48,6 +49,31 @@ int check_device_ptr(const void* p, const char* name, bool required) {
 }
 
 namespace {
+
+// Scale σ ∈ [1, 2) for the f16 centroid tables of the tensor-core decode: the
+// tables hold f16(σ·c_k) and the kernels divide σ back out in f32.  Choosing σ
+// so that every σ·c_k lands close to an f16 value removes most of the rounding
+// of the centroids (2^-12 relative at σ = 1), which the softmax would amplify.
+float centroid_table_scale(const Codebook& cb) {
+    float best_s = 1.f;
+    double best_err = 1e30;
+    for (int i = 0; i < (1 << 16); ++i) {
+        const float sc = 1.f + (float)i / 65536.f;
+        double err = 0.0;
+        for (int k = 0; k < cb.levels; ++k) {
+            const float v = sc * cb.c[k];
+            if (v == 0.f) continue;
+            const float r = __half2float(__float2half_rn(v));
+            const double e = fabs((double)r - (double)v) / fabs((double)v);
+            if (e > err) err = e;
+        }
+        if (err < best_err) {
+            best_err = err;
+            best_s = sc;
+        }
+    }
+    return best_s;
+}
 
 // float → bfloat16 bits, round to nearest even (finite inputs).
 uint16_t f32_to_bf16(float f) {
@@ -263,6 +289,7 @@ int tq_init(int d, int bits, int variant, uint64_t seed, tq_handle* out) {
     h->cb.levels = h->hp.levels;
     for (int i = 0; i < h->hp.levels; ++i) h->cb.c[i] = (float)h->hp.centroids[i];
     for (int i = 0; i + 1 < h->hp.levels; ++i) h->cb.t[i] = (float)h->hp.bounds[i];
+    h->cb.lut_scale = centroid_table_scale(h->cb);
     rc = upload_params(h);
     if (rc != TQ_OK) {
         free_device(h);

@@ -7,9 +7,12 @@
 //
 // Three launches: query prep, split-K flash-decoding over token chunks with an
 // online softmax per split, and a merge that combines the splits and un-rotates.
+// For d = 128 the split step runs on the tensor cores (tq_decode_mma.cuh); the
+// CUDA-core split kernel below serves every other head dimension.
 #include <math.h>
 
 #include "tq_common.cuh"
+#include "tq_decode_args.h"
 
 namespace tq {
 namespace {
@@ -20,7 +23,7 @@ constexpr int kMinChunk = 64;
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct WsLayout {
-    size_t qr, qs, pm, pl, pacc, pacc2, total;
+    size_t qr, qs, pm, pl, pacc, pacc2, cnt, total;
 };
 
 WsLayout ws_layout(const DecodeShape& p, bool vprod) {
@@ -39,6 +42,8 @@ WsLayout ws_layout(const DecodeShape& p, bool vprod) {
     off = align256(off + heads * p.n_splits * p.d * 4);
     w.pacc2 = off;
     if (vprod) off = align256(off + heads * p.n_splits * p.d * 4);
+    w.cnt = off;  // one ticket per (batch, KV head, head block): at most B·Hq
+    off = align256(off + heads * 4);
     w.total = off;
     return w;
 }
@@ -46,9 +51,12 @@ WsLayout ws_layout(const DecodeShape& p, bool vprod) {
 template <int D, bool KPROD, typename TQ>
 __global__ void query_prep_kernel(const TQ* __restrict__ q, const float* __restrict__ PiT,
                                   const float* __restrict__ ST, int Hq, float* __restrict__ qr,
-                                  float* __restrict__ qs) {
+                                  float* __restrict__ qs, int* __restrict__ cnt, int ncnt) {
     __shared__ float qv[D];
     const int h = blockIdx.x, b = blockIdx.y, j = threadIdx.x;
+    // zero the split-merge tickets of this call
+    const int gt = (blockIdx.y * gridDim.x + blockIdx.x) * blockDim.x + threadIdx.x;
+    if (gt < ncnt) cnt[gt] = 0;
     const size_t base = ((size_t)b * Hq + h) * D;
     qv[j] = load_elem(q + base + j);
     __syncthreads();
@@ -60,29 +68,6 @@ __global__ void query_prep_kernel(const TQ* __restrict__ q, const float* __restr
     qr[base + j] = a;
     if constexpr (KPROD) qs[base + j] = c;
 }
-
-struct SplitArgs {
-    const uint8_t* kcodes;
-    const uint8_t* ksigns;
-    const float* knorm;
-    const float* krnorm;
-    const uint8_t* vcodes;
-    const uint8_t* vsigns;
-    const float* vnorm;
-    const float* vrnorm;
-    const int32_t* seq_lens;
-    const float* qr;
-    const float* qs;
-    float* pm;
-    float* pl;
-    float* pacc;
-    float* pacc2;
-    float* scores;
-    Codebook kcb, vcb;
-    int kb, vb;  // b_m of keys / values
-    float kgamma, vgamma, scale;
-    int B, Hq, Hkv, T_max, G, n_splits, chunk, n_hblocks;
-};
 
 template <int D, bool KPROD, bool VPROD>
 __global__ void __launch_bounds__(kSplitWarps * 32)
@@ -257,6 +242,32 @@ __global__ void decode_merge_kernel(const float* __restrict__ pm, const float* _
     out[head * D + j] = r;
 }
 
+// The tensor-core split kernel is written for d = 128 (the head dimension of
+// every workload this library is tuned for).
+constexpr bool use_mma_split(int d) { return d == mmadec::D128; }
+
+int launch_split_mma_any(const SplitArgs& a, dim3 grid, int kb, bool kp, int vb, bool vp, cudaStream_t s) {
+    using namespace mmadec;
+    if (kp) {
+        switch (kb) {
+            case 0: return launch_for_k<0, true>(a, grid, vb, vp, s);
+            case 1: return launch_for_k<1, true>(a, grid, vb, vp, s);
+            case 2: return launch_for_k<2, true>(a, grid, vb, vp, s);
+            case 3: return launch_for_k<3, true>(a, grid, vb, vp, s);
+            default: break;
+        }
+    } else {
+        switch (kb) {
+            case 1: return launch_for_k<1, false>(a, grid, vb, vp, s);
+            case 2: return launch_for_k<2, false>(a, grid, vb, vp, s);
+            case 3: return launch_for_k<3, false>(a, grid, vb, vp, s);
+            case 4: return launch_for_k<4, false>(a, grid, vb, vp, s);
+            default: break;
+        }
+    }
+    return fail(TQ_EUNSUPPORTED, "tensor-core decode: key b_m=%d", kb);
+}
+
 template <int D>
 int launch_d(const tq_ctx& hk, const tq_ctx& hv, const DecodeShape& p, const void* q, int q_dtype,
              const tq_planes& kc, const tq_planes& vc, const int32_t* seq_lens, float scale, float* out,
@@ -266,19 +277,9 @@ int launch_d(const tq_ctx& hk, const tq_ctx& hv, const DecodeShape& p, const voi
     char* ws = static_cast<char*>(workspace);
     float* qr = reinterpret_cast<float*>(ws + w.qr);
     float* qs = reinterpret_cast<float*>(ws + w.qs);
+    int* cnt = reinterpret_cast<int*>(ws + w.cnt);
     dim3 pg(p.Hq, p.B);
-    if (q_dtype == TQ_F32) {
-        auto qp = static_cast<const float*>(q);
-        if (kprod) query_prep_kernel<D, true><<<pg, D, 0, s>>>(qp, hk.dp.PiT, hk.dp.ST, p.Hq, qr, qs);
-        else query_prep_kernel<D, false><<<pg, D, 0, s>>>(qp, hk.dp.PiT, hk.dp.ST, p.Hq, qr, qs);
-    } else {
-        auto qp = static_cast<const __nv_bfloat16*>(q);
-        if (kprod) query_prep_kernel<D, true><<<pg, D, 0, s>>>(qp, hk.dp.PiT, hk.dp.ST, p.Hq, qr, qs);
-        else query_prep_kernel<D, false><<<pg, D, 0, s>>>(qp, hk.dp.PiT, hk.dp.ST, p.Hq, qr, qs);
-    }
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_fail(e, "query prep launch");
-
+    cudaError_t e = cudaSuccess;
     SplitArgs a;
     a.kcodes = kc.codes; a.ksigns = kc.signs; a.knorm = kc.norm; a.krnorm = kc.rnorm;
     a.vcodes = vc.codes; a.vsigns = vc.signs; a.vnorm = vc.norm; a.vrnorm = vc.rnorm;
@@ -292,6 +293,30 @@ int launch_d(const tq_ctx& hk, const tq_ctx& hv, const DecodeShape& p, const voi
     a.kgamma = hk.gamma; a.vgamma = hv.gamma; a.scale = scale;
     a.B = p.B; a.Hq = p.Hq; a.Hkv = p.Hkv; a.T_max = p.T_max; a.G = p.G;
     a.n_splits = p.n_splits; a.chunk = p.chunk;
+    a.cnt = cnt; a.vPi = hv.dp.Pi; a.vS = hv.dp.S; a.out = out;
+    a.q = q; a.q_f32 = q_dtype == TQ_F32; a.kPi = hk.dp.Pi; a.kS = hk.dp.S;
+    if (use_mma_split(D)) {
+        // query rotation, split and merge all happen in the split kernel
+        a.n_hblocks = (p.G + mmadec::kHeadsPerCta - 1) / mmadec::kHeadsPerCta;
+        e = cudaMemsetAsync(cnt, 0, (size_t)p.B * p.Hq * sizeof(int), s);
+        if (e != cudaSuccess) return cuda_fail(e, "clearing the split tickets");
+        return launch_split_mma_any(a, dim3(p.n_splits, p.Hkv * a.n_hblocks, p.B), hk.hp.b_mse, kprod, hv.hp.b_mse,
+                                    vprod, s);
+    }
+
+    // CUDA-core path: query prep (which also clears the tickets), split, merge
+    if (q_dtype == TQ_F32) {
+        auto qp = static_cast<const float*>(q);
+        if (kprod) query_prep_kernel<D, true><<<pg, D, 0, s>>>(qp, hk.dp.PiT, hk.dp.ST, p.Hq, qr, qs, cnt, (int)((size_t)p.B * p.Hq));
+        else query_prep_kernel<D, false><<<pg, D, 0, s>>>(qp, hk.dp.PiT, hk.dp.ST, p.Hq, qr, qs, cnt, (int)((size_t)p.B * p.Hq));
+    } else {
+        auto qp = static_cast<const __nv_bfloat16*>(q);
+        if (kprod) query_prep_kernel<D, true><<<pg, D, 0, s>>>(qp, hk.dp.PiT, hk.dp.ST, p.Hq, qr, qs, cnt, (int)((size_t)p.B * p.Hq));
+        else query_prep_kernel<D, false><<<pg, D, 0, s>>>(qp, hk.dp.PiT, hk.dp.ST, p.Hq, qr, qs, cnt, (int)((size_t)p.B * p.Hq));
+    }
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "query prep launch");
+
     a.n_hblocks = (p.G + kMaxGroup - 1) / kMaxGroup;
     const int gmax = p.G < kMaxGroup ? p.G : kMaxGroup;
     const size_t smem = sizeof(float) * ((size_t)gmax * D * (2 + kSplitWarps * (vprod ? 2 : 1)) + 2 * kSplitWarps * gmax);
@@ -331,18 +356,18 @@ int decode_plan(const tq_ctx& hk, const tq_ctx& hv, int B, int Hq, int Hkv, int 
     const int G = Hq / Hkv;
     if (Hq > 4096) return fail(TQ_EUNSUPPORTED, "Hq=%d > 4096", Hq);
     if ((int64_t)B * Hkv * T_max > (int64_t)1 << 40) return fail(TQ_EINVAL, "cache too large");
-    int dev = 0, sms = 148;
-    cudaGetDevice(&dev);
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-        cudaGetLastError();
-        sms = 148;
-    }
+    const int sms = hk.num_sms > 0 ? hk.num_sms : 148;
     DecodeShape p;
     p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.T_max = T_max; p.d = hk.hp.d; p.G = G;
-    const int64_t units = (int64_t)(B > 0 ? B : 1) * Hkv;
-    int64_t want = (2 * (int64_t)sms + units - 1) / units;
+    const int hper = use_mma_split(p.d) ? mmadec::kHeadsPerCta : kMaxGroup;
+    const int64_t units = (int64_t)(B > 0 ? B : 1) * Hkv * ((G + hper - 1) / hper);
+    // CUDA-core path: two CTAs per SM; tensor-core path: one 16-warp CTA per SM,
+    // and no more CTAs than SMs so that every split runs in the same wave.
+    int64_t want = use_mma_split(p.d) ? (int64_t)sms * mmadec::ctas_per_sm(hv.hp.variant == TQ_PROD) / units
+                                      : (2 * (int64_t)sms + units - 1) / units;
     int64_t max_splits = (T_max + kMinChunk - 1) / kMinChunk;
     if (max_splits < 1) max_splits = 1;
+    if (use_mma_split(p.d) && want > mmadec::kMaxSplitsMerged) want = mmadec::kMaxSplitsMerged;
     if (want > max_splits) want = max_splits;
     if (want < 1) want = 1;
     int64_t chunk = (T_max + want - 1) / want;

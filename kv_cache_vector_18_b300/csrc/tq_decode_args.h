@@ -1,0 +1,57 @@
+// Arguments of the split-K decode kernels (CUDA-core and tensor-core), shared
+// by tq_decode.cu and the tensor-core instantiation files.
+#pragma once
+
+#include "tq_internal.h"
+
+namespace tq {
+
+// Device pointers and shapes one split launch needs (see include/tq.h).
+struct SplitArgs {
+    const uint8_t* kcodes;
+    const uint8_t* ksigns;
+    const float* knorm;
+    const float* krnorm;
+    const uint8_t* vcodes;
+    const uint8_t* vsigns;
+    const float* vnorm;
+    const float* vrnorm;
+    const int32_t* seq_lens;
+    const float* qr;
+    const float* qs;
+    float* pm;
+    float* pl;
+    float* pacc;
+    float* pacc2;
+    float* scores;
+    Codebook kcb, vcb;
+    int kb, vb;  // b_m of keys / values
+    float kgamma, vgamma, scale;
+    int B, Hq, Hkv, T_max, G, n_splits, chunk, n_hblocks;
+    // Fused merge (tensor-core path): one ticket counter per (batch, KV head,
+    // head block), zeroed by the query-prep launch; the last split CTA of a group
+    // combines the partials and writes out = Π_vᵀ·acc/l (+ S_vᵀ·acc2/l).
+    int* cnt;
+    const float* vPi;  // Π_v row-major [d][d]
+    const float* vS;   // S_v row-major [d][d] (prod values)
+    float* out;        // [B, Hq, d]
+    // Query rotation inside the split kernel (tensor-core path): q′ = Π_k·q, q″ = S_k·q.
+    const void* q;     // [B, Hq, d], bf16 or f32
+    int q_f32;
+    const float* kPi;  // Π_k row-major [d][d]
+    const float* kS;   // S_k row-major [d][d] (prod keys)
+};
+
+namespace mmadec {
+// Tensor-core split kernel for d = 128, keys (kb, kprod) fixed per instantiation
+// file, values dispatched at run time.  Heads are processed 8 per CTA.
+constexpr int kHeadsPerCta = 8;
+constexpr int D128 = 128;
+constexpr int kMaxSplitsMerged = 256;  // splits the last CTA of a group can merge
+// resident split CTAs per SM of the tensor-core decode kernel (one 16- or 8-warp CTA)
+constexpr int ctas_per_sm(bool /*vprod*/) { return 1; }
+template <int KB, bool KP>
+int launch_for_k(const SplitArgs& a, dim3 grid, int vb, bool vp, cudaStream_t s);
+}  // namespace mmadec
+
+}  // namespace tq

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <string>
 #include <vector>
 
@@ -22,6 +23,7 @@ struct Codebook {
     float c[kMaxLevels];       // centroids, unit-sphere scale, ascending
     float t[kMaxLevels - 1];   // decision boundaries (midpoints), ascending
     int levels;                // 2^b_m
+    float lut_scale;           // σ ∈ [1, 2): f16(σ·c_k) is within ~1e-4 relative of σ·c_k for every k
 };
 
 // Float64 parameters of one quantizer, as built on the host.
@@ -69,6 +71,20 @@ int fail(int code, const char* fmt, ...);
 int cuda_fail(cudaError_t e, const char* what);
 int check_device_ptr(const void* p, const char* name, bool required);
 
+// Raise a kernel's dynamic shared-memory limit on the current device once (the
+// attribute persists for the process).  `done` is the caller's per-kernel
+// bitmask of device ordinals already configured.
+inline int ensure_smem_attr(std::atomic<uint64_t>& done, const void* fn, int bytes, const char* what) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const uint64_t bit = 1ull << (dev & 63);
+    if (done.load(std::memory_order_relaxed) & bit) return TQ_OK;
+    const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return cuda_fail(e, what);
+    done.fetch_or(bit, std::memory_order_relaxed);
+    return TQ_OK;
+}
+
 // Host parameter construction (tq_params.cpp).
 int build_host_params(int d, int bits, int variant, uint64_t seed, HostParams* out);
 
@@ -78,7 +94,7 @@ int encode_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint
                         uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer);
 
 // Kernel launchers (one per .cu file).  Arguments are validated by the caller.
-bool quantize_tc_supported(const tq_ctx& h, int x_dtype);
+bool quantize_tc_supported(const tq_ctx& h, int x_dtype, int64_t n_rows);
 int launch_quantize_tc(const tq_ctx& h, const void* x, int64_t n_rows, int64_t x_row_stride,
                        const tq_planes& out, cudaStream_t s);
 int launch_quantize(const tq_ctx& h, const void* x, int x_dtype, int64_t n_rows,

@@ -189,6 +189,11 @@ quantize_mse_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
             }
             tc_fence_before();
             mbar_arrive(&tempty[wg]);
+            if (n == 0.f) {
+                // A zero row stores codes 0 (the sign test above would give L/2 − 1).
+#pragma unroll
+                for (int w = 0; w < WORDS; ++w) words[w] = 0u;
+            }
             const int64_t row = tile * kTile + r_local;
             if (row < n_rows) {
                 uint8_t* dst = codes + row * (int64_t)(WORDS * 4);
@@ -217,13 +222,14 @@ template <int D, int BM>
 int launch_tc(const tq_ctx& h, const CUtensorMap& tm_x, int64_t n_rows, const tq_planes& out, cudaStream_t s) {
     using C = TcCfg<D>;
     auto fn = quantize_mse_tc_kernel<D, BM>;
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemBytes);
-    if (e != cudaSuccess) return cuda_fail(e, "quantize smem attribute");
+    static std::atomic<uint64_t> smem_set{0};
+    const int rc = ensure_smem_attr(smem_set, (const void*)fn, (int)C::kSmemBytes, "quantize smem attribute");
+    if (rc != TQ_OK) return rc;
     const int64_t ntiles = (n_rows + kTile - 1) / kTile;
     const int grid = (int)(ntiles < h.num_sms ? ntiles : h.num_sms);
     fn<<<grid, kThreads, C::kSmemBytes, s>>>(tm_x, h.dp.tm_pi_hi, h.dp.tm_pi_lo, n_rows, h.cb, out.codes, out.norm,
                                              h.dp.status);
-    e = cudaGetLastError();
+    const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? TQ_OK : cuda_fail(e, "tensor-core quantize launch");
 }
 
@@ -240,9 +246,10 @@ int launch_tc_d(const tq_ctx& h, const CUtensorMap& tm_x, int64_t n_rows, const 
 
 }  // namespace
 
-bool quantize_tc_supported(const tq_ctx& h, int x_dtype) {
+bool quantize_tc_supported(const tq_ctx& h, int x_dtype, int64_t n_rows) {
+    // TMA row coordinates are 32-bit signed: the last tile must start below 2^31.
     return x_dtype == TQ_BF16 && h.hp.variant == TQ_MSE && (h.hp.d == 64 || h.hp.d == 128) &&
-           h.dp.Pi_hi != nullptr && h.num_sms > 0;
+           h.dp.Pi_hi != nullptr && h.num_sms > 0 && n_rows < ((int64_t)1 << 31) - kTile;
 }
 
 int launch_quantize_tc(const tq_ctx& h, const void* x, int64_t n_rows, int64_t stride, const tq_planes& out,
