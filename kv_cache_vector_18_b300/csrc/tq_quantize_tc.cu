@@ -7,10 +7,18 @@
 // reads the accumulator row per thread, takes ‖y‖ = ‖x‖ (Π orthogonal), counts
 // the norm-scaled Lloyd–Max boundaries below each y_j and packs b-bit codes.
 //
+// Epilogue arithmetic runs on the FP32 pipe, two coordinates per packed f32x2
+// instruction where the operation allows it: with c = K/‖y‖² (K = 2^62), the
+// test |y_j| > ‖y‖·t_p is the saturated step sat(y_j·(c·y_j) − K·t_p²) ∈ {0, 1}
+// (one FFMA.SAT each; the exact product makes fractional values need a relative
+// tie below 1e-16), the code is (L/2 − ½) ± (count + ½) with the sign of y_j put
+// in by one bit operation, and codes are packed by exact float FMAs
+// acc += code·2^(b·i), 16 or 24 bits per accumulator.
+//
 // Persistent CTAs (one per SM) with warp roles:
 //   warp 0      TMA producer: Π_hi/Π_lo once, then X tiles into a STAGES ring
-//   warp 1      TMEM owner and single-thread MMA issuer (two accumulators)
-//   warps 2..9  two epilogue warpgroups, one per TMEM accumulator
+//   warp 1      TMEM owner and single-thread MMA issuer (three accumulators)
+//   warps 2..13 three epilogue warpgroups, one per TMEM accumulator
 #include "tq_common.cuh"
 #include "tq_sm100.cuh"
 
@@ -19,9 +27,35 @@ namespace {
 
 using namespace sm100;
 
+// Packed FP32 pair arithmetic (two lanes per instruction on the FP32 pipe).
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_split(uint64_t x, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(x));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 constexpr int kTile = 128;        // rows per tile (MMA M)
 constexpr int kKC = 64;           // K elements per 128-byte swizzle chunk
-constexpr int kEpiWarps = 8;
+constexpr int kAcc = 3;           // TMEM accumulators = epilogue warpgroups (14 warps: 128 registers each)
+constexpr int kEpiWarps = 4 * kAcc;
 constexpr int kThreads = 32 * (2 + kEpiWarps);
 
 template <int D>
@@ -32,7 +66,8 @@ struct TcCfg {
     static constexpr int kChunkBytesB = D * 128;      // one 64-column chunk of Π
     static constexpr int kPiBytes = D * D * 2;
     static constexpr int kStages = D == 64 ? 8 : 4;
-    static constexpr uint32_t kTmemCols = 2 * D < 32 ? 32 : 2 * D;
+    // allocation: the power of two ≥ kAcc·D columns (≤ 512)
+    static constexpr uint32_t kTmemCols = kAcc * D <= 32 ? 32 : (kAcc * D <= 64 ? 64 : (kAcc * D <= 128 ? 128 : (kAcc * D <= 256 ? 256 : 512)));
     static constexpr size_t kBarOffset = 2 * (size_t)kPiBytes + (size_t)kStages * kStageBytes;
     static constexpr size_t kSmemBytes = kBarOffset + 256 + 1024;  // barriers + alignment slack
 };
@@ -54,10 +89,10 @@ quantize_mse_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
     uint64_t* full = bars;                      // [kStages]
     uint64_t* empty = bars + C::kStages;        // [kStages]
-    uint64_t* tfull = empty + C::kStages;       // [2]
-    uint64_t* tempty = tfull + 2;               // [2]
-    uint64_t* pi_full = tempty + 2;
-    uint64_t* drain = pi_full + 1;
+    uint64_t* tfull = empty + C::kStages;       // [kAcc]
+    uint64_t* tempty = tfull + kAcc;            // [kAcc]
+    uint64_t* pi_full = tempty + kAcc;
+    uint64_t* drain = pi_full + 1;  // barrier region: 2·kStages + 2·kAcc + 2 ≤ 26 words
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -68,7 +103,7 @@ quantize_mse_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
-        for (int a = 0; a < 2; ++a) {
+        for (int a = 0; a < kAcc; ++a) {
             mbar_init(&tfull[a], 1);
             mbar_init(&tempty[a], 128);
         }
@@ -116,8 +151,8 @@ quantize_mse_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
         int64_t i = 0;
         for (int64_t tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x, ++i) {
             const int s = (int)(i % C::kStages);
-            const int acc = (int)(i & 1);
-            const int64_t ua = i >> 1;
+            const int acc = (int)(i % kAcc);
+            const int64_t ua = i / kAcc;
             if (!(ok = mbar_wait(&full[s], (uint32_t)((i / C::kStages) & 1), status, 4))) break;
             if (ua > 0 && !(ok = mbar_wait(&tempty[acc], (uint32_t)((ua - 1) & 1), status, 5))) break;
             tc_fence_after();
@@ -142,72 +177,114 @@ quantize_mse_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
         mbar_wait(drain, 0, status, 6);
     } else if (warp >= 2) {
         // ------------------------------------------------------------ epilogue
+        constexpr int GB = BM == 3 ? 24 : 16;  // bits per float packing group
+        constexpr int GC = GB / BM;            // codes per group
+        constexpr int NG = 32 / GC;            // groups per 32-code TMEM chunk
+        constexpr float kAcc0 = (float)(1u << (GB - 1)) - 0.5f;  // Σ_i (L/2 − ½)·2^(b·i)
         const int wg = (warp - 2) >> 2;                 // accumulator served
         const int quad = warp & 3;                      // TMEM lane quadrant of this warp
         const int r_local = quad * 32 + lane;
-        float tpos[P > 0 ? P : 1];
+        float t2[P > 0 ? P : 1];                        // squared positive boundaries
 #pragma unroll
-        for (int p = 0; p < P; ++p) tpos[p] = cb.t[L / 2 + p];
+        for (int p = 0; p < P; ++p) t2[p] = cb.t[L / 2 + p] * cb.t[L / 2 + p];
         const uint32_t taddr0 = tmem_base + (uint32_t)(wg * D) + ((uint32_t)(quad * 32) << 16);
         int64_t j = 0;
-        for (int64_t tile = blockIdx.x + (int64_t)wg * gridDim.x; tile < ntiles; tile += 2 * (int64_t)gridDim.x, ++j) {
+        for (int64_t tile = blockIdx.x + (int64_t)wg * gridDim.x; tile < ntiles;
+             tile += (int64_t)kAcc * gridDim.x, ++j) {
             if (!mbar_wait(&tfull[wg], (uint32_t)(j & 1), status, 7)) break;
             tc_fence_after();
-            uint32_t r[32];
-            float ss = 0.f;
+            // pass 1: ‖y‖², two 32-column TMEM loads in flight per wait
+            uint32_t r[2][32];
+            uint64_t ss2 = 0ull;
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                tmem_ld32(taddr0 + c * 32, r);
-                tmem_wait_ld();
+            for (int c = 0; c < D / 32; c += 2) {
+                tmem_ld32(taddr0 + c * 32, r[0]);
+                tmem_ld32(taddr0 + (c + 1) * 32, r[1]);
+                tmem_wait_ld(r[0]);
+                tmem_wait_ld(r[1]);
 #pragma unroll
-                for (int k = 0; k < 32; ++k) ss = fmaf(__uint_as_float(r[k]), __uint_as_float(r[k]), ss);
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int k = 0; k < 32; k += 2) {
+                        const uint64_t v2 = f2(__uint_as_float(r[h][k]), __uint_as_float(r[h][k + 1]));
+                        ss2 = fma2(v2, v2, ss2);
+                    }
             }
+            float ssa, ssb;
+            f2_split(ss2, ssa, ssb);
+            const float ss = ssa + ssb;
             const float n = sqrtf(ss);
-            float thr[P > 0 ? P : 1];
+            // c = K/‖y‖² with K = 2^62, lowered for rows so small that c would overflow
+            const float cs = ss >= 0x1p-38f ? __fdividef(0x1p62f, ss) : 0x1p100f;
+            const float kr = cs * ss;
+            const uint64_t cs2 = f2(cs, cs);
+            float kt2[P > 0 ? P : 1];
 #pragma unroll
-            for (int p = 0; p < P; ++p) thr[p] = n * tpos[p];
-            uint32_t words[WORDS];
-#pragma unroll
-            for (int w = 0; w < WORDS; ++w) words[w] = 0u;
+            for (int p = 0; p < P; ++p) kt2[p] = -kr * t2[p];
+            const int64_t row = tile * kTile + r_local;
+            const bool live = row < n_rows;
+            // a zero row stores codes 0 (the sign test would give L/2)
+            const uint32_t keep = n == 0.f ? 0u : 0xffffffffu;
+            uint8_t* dst = codes + row * (int64_t)(WORDS * 4);
+            // pass 2: chunk c + 1 is loaded while chunk c is bucketized
+            tmem_ld32(taddr0, r[0]);
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
-                tmem_ld32(taddr0 + c * 32, r);
-                tmem_wait_ld();
+                tmem_wait_ld(r[c & 1]);
+                if (c + 1 < D / 32) tmem_ld32(taddr0 + (c + 1) * 32, r[(c + 1) & 1]);
+                const uint32_t* rc = r[c & 1];
+                // codes of coordinate pairs (k, k+1); each group keeps an even and an
+                // odd partial sum (both exact integers) in one packed accumulator
+                uint64_t acc[NG];
 #pragma unroll
-                for (int k = 0; k < 32; ++k) {
-                    const float v = __uint_as_float(r[k]);
-                    const float a = fabsf(v);
-                    uint32_t base = (uint32_t)(L / 2 - 1);
+                for (int gi = 0; gi < NG; ++gi) acc[gi] = f2(kAcc0, 0.f);
 #pragma unroll
-                    for (int p = 0; p < P; ++p) base -= (a > thr[p]) ? 1u : 0u;
-                    const uint32_t code = base ^ ((v > 0.f) ? (uint32_t)(L - 1) : 0u);
-                    const int bit = k * BM;
-                    const int w = c * BM + (bit >> 5), sh = bit & 31;
-                    words[w] |= code << sh;
-                    if (sh + BM > 32) words[w + 1] |= code >> (32 - sh);
+                for (int k = 0; k < 32; k += 2) {
+                    const float va = __uint_as_float(rc[k]), vb = __uint_as_float(rc[k + 1]);
+                    uint64_t cnt2 = f2(0.5f, 0.5f);
+                    if constexpr (P > 0) {
+                        float wa, wb;
+                        f2_split(mul2(f2(va, vb), cs2), wa, wb);
+#pragma unroll
+                        for (int p = 0; p < P; ++p)
+                            cnt2 = add2(cnt2, f2(__saturatef(fmaf(va, wa, kt2[p])), __saturatef(fmaf(vb, wb, kt2[p]))));
+                    }
+                    float ca, cb;
+                    f2_split(cnt2, ca, cb);
+                    const float sa = __uint_as_float(__float_as_uint(ca) | (__float_as_uint(va) & 0x80000000u));
+                    const float sb = __uint_as_float(__float_as_uint(cb) | (__float_as_uint(vb) & 0x80000000u));
+                    acc[k / GC] = fma2(f2(sa, sb),
+                                       f2((float)(1u << (BM * (k % GC))), (float)(1u << (BM * ((k + 1) % GC)))),
+                                       acc[k / GC]);
+                }
+                // the chunk's 32 codes are BM consecutive words of the row: store them now
+                uint32_t cw[BM];
+#pragma unroll
+                for (int w = 0; w < BM; ++w) cw[w] = 0u;
+#pragma unroll
+                for (int gi = 0; gi < NG; ++gi) {
+                    float ea, eb;
+                    f2_split(acc[gi], ea, eb);
+                    const uint32_t gbits = __float2uint_rn(ea + eb);
+                    const int bit = gi * GB, w = bit >> 5, sh = bit & 31;
+                    cw[w] |= gbits << sh;
+                    if (sh + GB > 32) cw[w + 1] |= gbits >> (32 - sh);
+                }
+                if (live) {
+                    uint8_t* cd = dst + c * (BM * 4);
+                    if constexpr (BM == 4) {
+                        *reinterpret_cast<uint4*>(cd) = make_uint4(cw[0] & keep, cw[1] & keep, cw[2] & keep, cw[3] & keep);
+                    } else if constexpr (BM == 2) {
+                        *reinterpret_cast<uint2*>(cd) = make_uint2(cw[0] & keep, cw[1] & keep);
+                    } else {
+#pragma unroll
+                        for (int w = 0; w < BM; ++w) reinterpret_cast<uint32_t*>(cd)[w] = cw[w] & keep;
+                    }
                 }
             }
             tc_fence_before();
             mbar_arrive(&tempty[wg]);
-            if (n == 0.f) {
-                // A zero row stores codes 0 (the sign test above would give L/2 − 1).
-#pragma unroll
-                for (int w = 0; w < WORDS; ++w) words[w] = 0u;
-            }
-            const int64_t row = tile * kTile + r_local;
-            if (row < n_rows) {
-                uint8_t* dst = codes + row * (int64_t)(WORDS * 4);
-                if constexpr ((WORDS % 4) == 0) {
-#pragma unroll
-                    for (int w = 0; w < WORDS; w += 4)
-                        *reinterpret_cast<uint4*>(dst + 4 * w) = make_uint4(words[w], words[w + 1], words[w + 2], words[w + 3]);
-                } else {
-#pragma unroll
-                    for (int w = 0; w < WORDS; w += 2)
-                        *reinterpret_cast<uint2*>(dst + 4 * w) = make_uint2(words[w], words[w + 1]);
-                }
-                norm_out[row] = n;
-            }
+            if (live) norm_out[row] = n;
         }
     }
     tc_fence_before();
