@@ -40,6 +40,8 @@ LAUNCHES = {"quantize": 1, "decode": 3}
 # The arithmetic the path computes in.
 DTYPE_LABEL = "f32"
 QUANT_SOURCES = ["kv_cache_vector_18_b300/csrc/tq_quantize_tc.cu", "kv_cache_vector_18_b300/csrc/tq_sm100.cuh"]
+DECODE_SOURCES = ["kv_cache_vector_18_b300/csrc/tq_decode_mma.cuh", "kv_cache_vector_18_b300/csrc/tq_decode_args.h",
+                  "kv_cache_vector_18_b300/csrc/tq_decode.cu"]
 
 
 # ----------------------------------------------------------------------------- ranks
@@ -280,8 +282,9 @@ def source_hash(paths) -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel_key: str, src_hash: str, rows_per_launch: int):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on this source."""
+def recorded_traffic(kernel_key: str, src_hash: str, units_per_launch: int):
+    """DRAM bytes per launch from the committed ncu summary (bytes per row or per
+    token-head, scaled to this launch), if it was taken on this source."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             rec = json.load(f)[kernel_key]
@@ -289,7 +292,7 @@ def recorded_traffic(kernel_key: str, src_hash: str, rows_per_launch: int):
         return None
     if rec.get("source_hash") != src_hash:
         return None
-    return rec["dram_bytes_per_row"] * rows_per_launch
+    return rec["dram_bytes_per_unit"] * units_per_launch
 
 
 def blas_threads() -> int:
@@ -455,7 +458,7 @@ def run_ours(args, spec):
         # The SM clock idles far below its maximum and takes a sustained load to
         # ramp up; keep the device busy for at least WARM_SECONDS (and W steps)
         # right up to the timed loop so that no idle gap precedes it.
-        warm_steps = keep_busy(lambda: (flush.zero_(), [g.replay() for g in graphs]), args.warmup, WARM_SECONDS)
+        warm_steps = keep_busy(lambda: (flush.zero_(), [g.replay() for g in graphs]), args.warmup, args.warm_seconds)
         barrier(world)
         wall0 = time.perf_counter()
         for i in range(args.steps):
@@ -485,8 +488,16 @@ def run_ours(args, spec):
     roofline = {"kernel": "tq_quantize", "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
                 "peak_source": peaks["source"], "bytes_per_launch": bytes_per_launch,
-                "launch_ms": q_launch_ms, "source_hash": src,
-                "decode_frac": dec_gbs / peaks["hbm_gbs"]}
+                "launch_ms": q_launch_ms, "source_hash": src}
+    # the decode launch (same peak): algorithmic bytes are the packed planes read
+    dsrc = source_hash(DECODE_SOURCES)
+    d_launch_ms = statistics.mean(dc)
+    d_key = f"decode_{spec['k_variant']}_b{spec['k_bits']}_{spec['v_variant']}_b{spec['v_bits']}_d{d}"
+    roofline_decode = {"kernel": "tq_decode_attention", "bound": "hbm",
+                       "achieved": tm["decode"] / (d_launch_ms / 1e3) / 1e9, "peak": peaks["hbm_gbs"],
+                       "unit": "GB/s", "frac": tm["decode"] / (d_launch_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
+                       "traffic": recorded_traffic(d_key, dsrc, tm["ctx_rows"]), "peak_source": peaks["source"],
+                       "bytes_per_launch": tm["decode"], "launch_ms": d_launch_ms, "source_hash": dsrc}
 
     e2e = None
     if not args.no_e2e:
@@ -501,10 +512,11 @@ def run_ours(args, spec):
             "pct_nominal_8tbs": value / 8000.0 * 100.0,
             "bytes_per_step": tm["total"],
             "gpu_launches": args.steps * (2 * LAUNCHES["quantize"] + LAUNCHES["decode"]),
-            "clocks": sampler.summary(), "wall_s_timed_loop": wall, "roofline": roofline, "e2e": e2e,
+            "clocks": sampler.summary(), "wall_s_timed_loop": wall, "roofline": roofline,
+            "roofline_decode": roofline_decode, "e2e": e2e,
             "timing": "CUDA events around CUDA-graph replays of each library call (one graph per call, "
                       "captured through the public API), after >= %.1f s of back-to-back warm-up (%d steps)"
-                      % (WARM_SECONDS, warm_steps),
+                      % (args.warm_seconds, warm_steps),
             "host_us_per_direct_call": {"quantize_k": host_us[0], "quantize_v": host_us[1], "decode": host_us[2]}}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(spec, K, V, q, lens.tolist())
@@ -542,7 +554,7 @@ def measure_e2e(args, spec, tq, kq, vq, K, V, q, ld, kc, vc, ws, out, tm, dev, w
         out_h.copy_(out, non_blocking=True)
 
     n = max(3, min(args.steps, 50))
-    keep_busy(e2e_step, 3, WARM_SECONDS)
+    keep_busy(e2e_step, 3, args.warm_seconds)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     e0.record()
@@ -566,6 +578,8 @@ def main(argv=None):
                     choices=["llama70b_layer_kv_quant", "decode_131k", "batched_decode_32k"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--warm-seconds", type=float, default=WARM_SECONDS,
+                    help="minimum back-to-back warm-up before timing (0 for profiler launch lists)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
