@@ -344,17 +344,6 @@ __device__ __forceinline__ void stage_tile(uint32_t dst, const Slab& s, int tb, 
     stage_rows4(dst + ST::kVN, s.vn, tb, rows, lane);
 }
 
-// Words of tokens g and g + 8 (lane c's runs) and their norms, from a staged tile.
-template <int KB, bool KP, int VB, bool VP>
-struct Raw {
-    uint32_t kw[2][KB > 0 ? KB : 1];
-    uint32_t ks[2];
-    float kn[2], krn[2];
-    uint32_t vw[2][VB > 0 ? VB : 1];
-    uint32_t vs[2];
-    float vn[2], vrn[2];
-};
-
 template <int NW>
 __device__ __forceinline__ void read_words(uint32_t* w, const unsigned char* p) {
     if constexpr (NW == 1) {
@@ -377,26 +366,6 @@ __device__ __forceinline__ void read_words(uint32_t* w, const unsigned char* p) 
     }
 }
 
-template <int KB, bool KP, int VB, bool VP>
-__device__ __forceinline__ void read_tile(Raw<KB, KP, VB, VP>& r, const unsigned char* st, int g, int c) {
-    using ST = Stage<KB, KP, VB, VP>;
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const int t = g + 8 * i;
-        if constexpr (KB > 0) read_words<KB>(r.kw[i], st + ST::kKC + t * ST::kRK + c * (KB * 4));
-        if constexpr (KP) {
-            r.ks[i] = *reinterpret_cast<const uint32_t*>(st + ST::kKS + t * 16 + c * 4);
-            r.krn[i] = *reinterpret_cast<const float*>(st + ST::kKR + t * 4);
-        }
-        r.kn[i] = *reinterpret_cast<const float*>(st + ST::kKN + t * 4);
-        if constexpr (VB > 0) read_words<VB>(r.vw[i], st + ST::kVC + t * ST::kRV + c * (VB * 4));
-        if constexpr (VP) {
-            r.vs[i] = *reinterpret_cast<const uint32_t*>(st + ST::kVS + t * 16 + c * 4);
-            r.vrn[i] = *reinterpret_cast<const float*>(st + ST::kVR + t * 4);
-        }
-        r.vn[i] = *reinterpret_cast<const float*>(st + ST::kVN + t * 4);
-    }
-}
 
 // Warps per CTA: 16 (two KV tiles of data in flight per warp, one CTA per SM);
 // prod values carry a second accumulator set and run 8 warps with more registers.
@@ -471,30 +440,40 @@ struct Acc {
 };
 
 template <int KB, bool KP, int VB, bool VP>
-__device__ __forceinline__ void step(Acc<VP>& st, const Raw<KB, KP, VB, VP>& r, int tb, int t1,
+__device__ __forceinline__ void step(Acc<VP>& st, const unsigned char* stp, int tb, int t1,
                                      const Decoder<KB>& dk, const Decoder<VB>& dv, const SignDecoder& ds,
                                      const uint32_t (&QK)[kKB][2],
                                      const uint32_t (&QS)[kKB][2], const uint2* qsf, int lane, const float (&fK)[2],
                                      const float (&fS)[2], const SplitArgs& a, size_t head0, int G, int g, int c) {
+    using ST = Stage<KB, KP, VB, VP>;
     const bool vA = tb + g < t1, vB = tb + 8 + g < t1;
+    // staged words are read where they are used, to keep few registers live
+    auto kwords = [&](int i, uint32_t* w) { read_words<KB>(w, stp + ST::kKC + (g + 8 * i) * ST::kRK + c * (KB * 4)); };
+    auto vwords = [&](int i, uint32_t* w) { read_words<VB>(w, stp + ST::kVC + (g + 8 * i) * ST::kRV + c * (VB * 4)); };
+    auto word = [&](int off, int i) { return *reinterpret_cast<const uint32_t*>(stp + off + (g + 8 * i) * 16 + c * 4); };
+    auto norm = [&](int off, int i) { return *reinterpret_cast<const float*>(stp + off + (g + 8 * i) * 4); };
 
     // ---- scores: S1 = K̃·Q′ᵀ (codes), S2 = Z·Q″ᵀ (QJL signs)
     float S1[4] = {0.f, 0.f, 0.f, 0.f}, S2[4] = {0.f, 0.f, 0.f, 0.f};
     if constexpr (KB > 0) {
+        uint32_t kwA[KB], kwB[KB];
+        kwords(0, kwA);
+        kwords(1, kwB);
 #pragma unroll
         for (int kb = 0; kb < kKB; ++kb) {
             uint32_t a0, a1, a2, a3;
-            dk.pairs(r.kw[0], kb, a0, a2);
-            dk.pairs(r.kw[1], kb, a1, a3);
+            dk.pairs(kwA, kb, a0, a2);
+            dk.pairs(kwB, kb, a1, a3);
             mma16816(S1, a0, a1, a2, a3, QK[kb][0], QK[kb][1]);
         }
     }
     if constexpr (KP) {
+        const uint32_t ksA = word(ST::kKS, 0), ksB = word(ST::kKS, 1);
 #pragma unroll
         for (int m = 0; m < kKB / 2; ++m) {
             uint32_t pa[4], pb[4];
-            ds.quad(r.ks[0], m, pa);
-            ds.quad(r.ks[1], m, pb);
+            ds.quad(ksA, m, pa);
+            ds.quad(ksB, m, pb);
             uint2 q0, q1;
             if constexpr (QsInSmem<KP, VP>::value) {
                 q0 = qsf[(2 * m) * 32 + lane];
@@ -509,7 +488,13 @@ __device__ __forceinline__ void step(Acc<VP>& st, const Raw<KB, KP, VB, VP>& r, 
     }
     // C layout: [0] (token g, head 2c) [1] (g, 2c+1) [2] (g+8, 2c) [3] (g+8, 2c+1)
     // z = s·log2e + log2‖v‖ (the exponent of the value weight), −∞ past the chunk
-    const float vnA = fmaxf(r.vn[0], 1e-30f), vnB = fmaxf(r.vn[1], 1e-30f);
+    const float vnA = fmaxf(norm(ST::kVN, 0), 1e-30f), vnB = fmaxf(norm(ST::kVN, 1), 1e-30f);
+    const float knr[2] = {norm(ST::kKN, 0), norm(ST::kKN, 1)};
+    float krr[2] = {0.f, 0.f};
+    if constexpr (KP) {
+        krr[0] = norm(ST::kKR, 0);
+        krr[1] = norm(ST::kKR, 1);
+    }
     const float lvA = lg2(vnA), lvB = lg2(vnB);
     const float rvA = rcp(vnA), rvB = rcp(vnB);
     float z[4];
@@ -517,8 +502,8 @@ __device__ __forceinline__ void step(Acc<VP>& st, const Raw<KB, KP, VB, VP>& r, 
     for (int i = 0; i < 4; ++i) {
         const int tk = i >> 1, e = i & 1;
         float v = fK[e] * S1[i];
-        if constexpr (KP) v = fmaf(fS[e] * r.krn[tk], S2[i], v);
-        z[i] = fmaf(r.kn[tk], v, tk ? lvB : lvA);
+        if constexpr (KP) v = fmaf(fS[e] * krr[tk], S2[i], v);
+        z[i] = fmaf(knr[tk], v, tk ? lvB : lvA);
     }
     if (!vA) z[0] = z[1] = -INFINITY;
     if (!vB) z[2] = z[3] = -INFINITY;
@@ -573,23 +558,27 @@ __device__ __forceinline__ void step(Acc<VP>& st, const Raw<KB, KP, VB, VP>& r, 
 
     // ---- values: Oᵀ += Ṽᵀ·P′ᵀ in the rotated frame
     if constexpr (VB > 0) {
+        uint32_t vwA[VB], vwB[VB];
+        vwords(0, vwA);
+        vwords(1, vwB);
 #pragma unroll
         for (int m = 0; m < kMT; ++m) {
             uint32_t x0, x1, y0, y1;
-            dv.pairs(r.vw[0], m, x0, x1);
-            dv.pairs(r.vw[1], m, y0, y1);
+            dv.pairs(vwA, m, x0, x1);
+            dv.pairs(vwB, m, y0, y1);
             mma16816(st.O[m], mov_trans(x0), mov_trans(x1), mov_trans(y0), mov_trans(y1), PB0, PB1);
         }
     }
     if constexpr (VP) {
-        const float gA = a.vgamma * r.vrn[0], gB = a.vgamma * r.vrn[1];
+        const float gA = a.vgamma * norm(ST::kVR, 0), gB = a.vgamma * norm(ST::kVR, 1);
+        const uint32_t vsA = word(ST::kVS, 0), vsB = word(ST::kVS, 1);
         const uint32_t QB0 = mov_trans(pack_h2(pv[0] * gA, pv[1] * gA));
         const uint32_t QB1 = mov_trans(pack_h2(pv[2] * gB, pv[3] * gB));
 #pragma unroll
         for (int m = 0; m < kMT / 2; ++m) {
             uint32_t pa[4], pb[4];
-            ds.quad(r.vs[0], m, pa);
-            ds.quad(r.vs[1], m, pb);
+            ds.quad(vsA, m, pa);
+            ds.quad(vsB, m, pb);
             mma16816(st.O2[2 * m], mov_trans(pa[0]), mov_trans(pa[1]), mov_trans(pb[0]), mov_trans(pb[1]), QB0, QB1);
             mma16816(st.O2[2 * m + 1], mov_trans(pa[2]), mov_trans(pa[3]), mov_trans(pb[2]), mov_trans(pb[3]), QB0,
                      QB1);
@@ -674,7 +663,6 @@ template <int KB, bool KP, int VB, bool VP>
 __global__ void __launch_bounds__(Warps<VP>::value * 32, 1) decode_split_mma_kernel(const SplitArgs a) {
     using SM = Smem<KB, KP, VB, VP>;
     using ST = Stage<KB, KP, VB, VP>;
-    using R = Raw<KB, KP, VB, VP>;
     constexpr int W = SM::W;
     extern __shared__ __align__(128) unsigned char smem[];
     // main-phase regions start at the first 32 KB-aligned shared address
@@ -826,10 +814,9 @@ __global__ void __launch_bounds__(Warps<VP>::value * 32, 1) decode_split_mma_ker
         cp_async_commit();
         cp_async_wait<1>();
         __syncwarp();
-        R r;
-        read_tile(r, mp + SM::kStage + (size_t)(warp * 2 + slot) * ST::kBytes, g, c);
+        step<KB, KP, VB, VP>(st, mp + SM::kStage + (size_t)(warp * 2 + slot) * ST::kBytes, tb, t1, dk, dv, ds, QK,
+                             QS, qsf, lane, fK, fS, a, head0, G, g, c);
         __syncwarp();  // the slot may be refilled once every lane has read it
-        step<KB, KP, VB, VP>(st, r, tb, t1, dk, dv, ds, QK, QS, qsf, lane, fK, fS, a, head0, G, g, c);
         slot ^= 1;
     }
     cp_async_wait<0>();
