@@ -38,8 +38,8 @@ struct SplitArgs {
     // Query rotation inside the split kernel (tensor-core path): q′ = Π_k·q, q″ = S_k·q.
     const void* q;     // [B, Hq, d], bf16 or f32
     int q_f32;
-    const float* kPi;  // Π_k row-major [d][d]
-    const float* kS;   // S_k row-major [d][d] (prod keys)
+    const float* kPiT;  // Π_kᵀ row-major [d][d]: row i is column i of Π_k
+    const float* kST;   // S_kᵀ row-major [d][d] (prod keys)
 };
 
 namespace mmadec {

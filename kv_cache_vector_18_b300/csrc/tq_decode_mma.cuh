@@ -409,22 +409,24 @@ struct Smem {
     static constexpr size_t kQ = kSzK + kSzV + kSzS;
     static constexpr size_t kQsc = kQ + 2 * kHeads * D * 4;
     static constexpr size_t kQSf = kQsc + 2 * kHeads * 4;
-    static constexpr size_t kQin = kQSf + (KP ? (size_t)kKB * 32 * 8 : 0);  // [kHeads][D] raw queries
+    static constexpr size_t kQin = kQSf + (KP ? (size_t)kKB * 32 * 8 : 0);  // [D][kHeads] raw queries
     static constexpr size_t kStage = (kQin + (size_t)kHeads * D * 4 + 127) & ~(size_t)127;
     static constexpr size_t kMain = kStage + (size_t)W * 2 * Stage<KB, KP, VB, VP>::kBytes;
-    // combine phase (reuses the same bytes): per-warp maxima, sums, accumulators
+    // combine phase (reuses the same bytes): per-warp maxima, sums, weights and
+    // accumulators (the latter in fragment order: [warp][m][i][lane])
     static constexpr size_t kWM = 0;
     static constexpr size_t kWL = kWM + W * kHeads * 4;
-    static constexpr size_t kWO = kWL + W * kHeads * 4;
+    static constexpr size_t kWF = kWL + W * kHeads * 4;
+    static constexpr size_t kWO = kWF + W * kHeads * 4;
     static constexpr size_t kWO2 = kWO + (size_t)W * kHeads * D * 4;
     static constexpr size_t kCombine = kWO2 + (VP ? (size_t)W * kHeads * D * 4 : 0);
     // merge phase of the last CTA of a group (reuses the same bytes again)
     static constexpr int kMaxSplits = kMaxSplitsMerged;
     static constexpr size_t kMW = 0;                                      // [kHeads][kMaxSplits] weights
     static constexpr size_t kML = kMW + (size_t)kHeads * kMaxSplits * 4;  // [kHeads] 1/l
-    static constexpr size_t kMO = kML + kHeads * 4;                       // [2][kHeads][D] merged acc
-    static constexpr size_t kMP = (kMO + 2 * (size_t)kHeads * D * 4 + 15) & ~(size_t)15;  // [D][D] Π_v or S_v
-    static constexpr size_t kMerge = kMP + (size_t)D * D * 4;
+    static constexpr size_t kMO = kML + kHeads * 4;                       // [2][D][kHeads] merged acc
+    static constexpr size_t kMP = (kMO + 2 * (size_t)kHeads * D * 4 + 15) & ~(size_t)15;  // [D][D] Π_v, then S_v
+    static constexpr size_t kMerge = kMP + (VP ? 2 : 1) * (size_t)D * D * 4;
     static constexpr size_t kAlignSlack = kBig - 16;  // the 32 KB-aligned base lies at most this far in
     static constexpr size_t kBytes0 = kMain + kAlignSlack > kCombine ? kMain + kAlignSlack : kCombine;
     static constexpr size_t kBytes = kBytes0 > kMerge ? kBytes0 : kMerge;
@@ -591,11 +593,22 @@ __device__ __forceinline__ void step(Acc<VP>& st, const unsigned char* stp, int 
 template <int KB, bool KP, int VB, bool VP>
 __device__ __forceinline__ void merge_group(const SplitArgs& a, unsigned char* smem, size_t head0, int G) {
     using SM = Smem<KB, KP, VB, VP>;
+    constexpr int NT = SM::W * 32;
     float* wts = reinterpret_cast<float*>(smem + SM::kMW);   // [kHeads][kMaxSplits]
     float* linv = reinterpret_cast<float*>(smem + SM::kML);  // [kHeads]
-    float* mo = reinterpret_cast<float*>(smem + SM::kMO);    // [2][kHeads][D]
+    float* mo = reinterpret_cast<float*>(smem + SM::kMO);    // [2][D][kHeads]
+    float* pis = reinterpret_cast<float*>(smem + SM::kMP);   // [D][D] Π_v, then [D][D] S_v
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ns = a.n_splits;
+    // stage Π_v (and S_v) while the split weights are formed: all loads in flight at once
+#pragma unroll
+    for (int i = threadIdx.x; i < D * D / 4; i += NT)
+        reinterpret_cast<float4*>(pis)[i] = __ldg(reinterpret_cast<const float4*>(a.vPi) + i);
+    if constexpr (VP) {
+#pragma unroll
+        for (int i = threadIdx.x; i < D * D / 4; i += NT)
+            reinterpret_cast<float4*>(pis + D * D)[i] = __ldg(reinterpret_cast<const float4*>(a.vS) + i);
+    }
     if (warp < G) {
         const size_t hs = (head0 + warp) * ns;
         float mx = -INFINITY;
@@ -612,51 +625,45 @@ __device__ __forceinline__ void merge_group(const SplitArgs& a, unsigned char* s
         for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
         if (lane == 0) linv[warp] = l > 0.f ? 1.f / l : 0.f;
     }
-    // stage Π_v while the partials are combined (all loads in flight at once)
-    float* pis = reinterpret_cast<float*>(smem + SM::kMP);  // [D][D]
-    for (int i = threadIdx.x; i < D * D / 4; i += blockDim.x)
-        reinterpret_cast<float4*>(pis)[i] = __ldg(reinterpret_cast<const float4*>(a.vPi) + i);
     __syncthreads();
-    for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
+    // Σ over splits, coalesced over dims; stored dim-major so the mat-vec reads head pairs
+    for (int i = threadIdx.x; i < G * D; i += NT) {
         const int h = i / D, j = i % D;
         const size_t hs = (head0 + h) * ns;
+        const float* w = wts + h * SM::kMaxSplits;
         float o = 0.f, o2 = 0.f;
-#pragma unroll 8
+#pragma unroll 16
         for (int s = 0; s < ns; ++s) {
-            const float f = wts[h * SM::kMaxSplits + s];
-            o = fmaf(f, __ldcg(a.pacc + (hs + s) * D + j), o);
-            if constexpr (VP) o2 = fmaf(f, __ldcg(a.pacc2 + (hs + s) * D + j), o2);
+            o = fmaf(w[s], __ldcg(a.pacc + (hs + s) * D + j), o);
+            if constexpr (VP) o2 = fmaf(w[s], __ldcg(a.pacc2 + (hs + s) * D + j), o2);
         }
-        mo[h * D + j] = o * linv[h];
-        if constexpr (VP) mo[kHeads * D + h * D + j] = o2 * linv[h];
+        mo[j * kHeads + h] = o * linv[h];
+        if constexpr (VP) mo[kHeads * D + j * kHeads + h] = o2 * linv[h];
     }
     __syncthreads();
-    // out_i = Σ_j Π_v[j][i]·o_j (+ S_v[j][i]·o2_j) from shared memory
-    float r[kHeads];
-    const int col = threadIdx.x % D, hg = threadIdx.x / D, ng = blockDim.x / D;  // heads hg, hg + ng, …
-#pragma unroll
-    for (int k = 0; k < kHeads; ++k) r[k] = 0.f;
-    for (int j = 0; j < D; ++j) {
-        const float pij = pis[j * D + col];
-#pragma unroll
-        for (int k = 0; k < kHeads; ++k)
-            if (hg + k * ng < G) r[k] = fmaf(pij, mo[(hg + k * ng) * D + j], r[k]);
-    }
-    if constexpr (VP) {
-        __syncthreads();
-        for (int i = threadIdx.x; i < D * D / 4; i += blockDim.x)
-            reinterpret_cast<float4*>(pis)[i] = __ldg(reinterpret_cast<const float4*>(a.vS) + i);
-        __syncthreads();
+    // out[h][col] = Σ_j Π_v[j][col]·o[j][h] (+ S_v[j][col]·o2[j][h]), two heads per thread
+    const int col = threadIdx.x % D, hp = threadIdx.x / D;
+    for (int h0 = 2 * hp; h0 < G; h0 += 2 * (NT / D)) {
+        float r0 = 0.f, r1 = 0.f;
+#pragma unroll 8
         for (int j = 0; j < D; ++j) {
-            const float sij = pis[j * D + col];
-#pragma unroll
-            for (int k = 0; k < kHeads; ++k)
-                if (hg + k * ng < G) r[k] = fmaf(sij, mo[kHeads * D + (hg + k * ng) * D + j], r[k]);
+            const float p = pis[j * D + col];
+            const float2 m = *reinterpret_cast<const float2*>(mo + j * kHeads + h0);
+            r0 = fmaf(p, m.x, r0);
+            r1 = fmaf(p, m.y, r1);
         }
+        if constexpr (VP) {
+#pragma unroll 8
+            for (int j = 0; j < D; ++j) {
+                const float p = pis[D * D + j * D + col];
+                const float2 m = *reinterpret_cast<const float2*>(mo + kHeads * D + j * kHeads + h0);
+                r0 = fmaf(p, m.x, r0);
+                r1 = fmaf(p, m.y, r1);
+            }
+        }
+        a.out[(head0 + h0) * D + col] = r0;
+        if (h0 + 1 < G) a.out[(head0 + h0 + 1) * D + col] = r1;
     }
-#pragma unroll
-    for (int k = 0; k < kHeads; ++k)
-        if (hg + k * ng < G) a.out[(head0 + hg + k * ng) * D + col] = r[k];
 }
 
 template <int KB, bool KP, int VB, bool VP>
@@ -704,37 +711,41 @@ __global__ void __launch_bounds__(Warps<VP>::value * 32, 1) decode_split_mma_ker
     Decoder<KB>::fill(mp + SM::kTabK, a.kcb);
     Decoder<VB>::fill(mp + SM::kTabV, a.vcb);
     if constexpr (KP || VP) SignDecoder::fill(mp + SM::kTabS);
-    float* qin = reinterpret_cast<float*>(mp + SM::kQin);  // [kHeads][D] raw queries of this head block
+    float* qin = reinterpret_cast<float*>(mp + SM::kQin);  // [D][kHeads] raw queries, dim-major
     for (int i = threadIdx.x; i < kHeads * D; i += blockDim.x) {
-        const int h = i / D;
-        const size_t gi = (head0 + h) * D + (i % D);
+        const int h = i / D, j = i % D;
+        const size_t gi = (head0 + h) * D + j;
         float v = 0.f;
         if (h < G)
             v = a.q_f32 ? __ldg(static_cast<const float*>(a.q) + gi)
                         : __bfloat162float(static_cast<const __nv_bfloat16*>(a.q)[gi]);
-        qin[i] = v;
+        qin[j * kHeads + h] = v;
     }
     __syncthreads();
-    // q′ = Π_k·q (threads 0..D−1, row j of Π_k each) and q″ = S_k·q (threads D..2D−1)
-    if (threadIdx.x < (KP ? 2 : 1) * D) {
-        const int j = threadIdx.x % D;
-        const bool second = threadIdx.x >= D;
-        const float4* row = reinterpret_cast<const float4*>((second ? a.kS : a.kPi) + (size_t)j * D);
-        float4 rv[D / 4];
-#pragma unroll
-        for (int i = 0; i < D / 4; ++i) rv[i] = __ldg(row + i);
-        float acc[kHeads];
-#pragma unroll
-        for (int h = 0; h < kHeads; ++h) acc[h] = 0.f;
-#pragma unroll
-        for (int i = 0; i < D / 4; ++i)
-#pragma unroll
-            for (int h = 0; h < kHeads; ++h) {
-                const float4 x = reinterpret_cast<const float4*>(qin + h * D)[i];
-                acc[h] = fmaf(rv[i].x, x.x, fmaf(rv[i].y, x.y, fmaf(rv[i].z, x.z, fmaf(rv[i].w, x.w, acc[h]))));
+    // q′ = Π_k·q and q″ = S_k·q: one job per (matrix, quad of heads, output dim j);
+    // the job walks i over row i of the transposed matrix, so a warp's loads of
+    // one i are 32 consecutive floats, and reads q_i of its four heads as one float4.
+    {
+        constexpr int kJobs = (KP ? 2 : 1) * (kHeads / 4) * D;
+        for (int job = threadIdx.x; job < kJobs; job += blockDim.x) {
+            const int j = job % D, hq = (job / D) % (kHeads / 4), second = job / (D * (kHeads / 4));
+            const float* MT = (second ? a.kST : a.kPiT) + j;
+            float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+#pragma unroll 32
+            for (int i = 0; i < D; ++i) {
+                const float m = __ldg(MT + (size_t)i * D);
+                const float4 x = *reinterpret_cast<const float4*>(qin + i * kHeads + 4 * hq);
+                acc0 = fmaf(m, x.x, acc0);
+                acc1 = fmaf(m, x.y, acc1);
+                acc2 = fmaf(m, x.z, acc2);
+                acc3 = fmaf(m, x.w, acc3);
             }
-#pragma unroll
-        for (int h = 0; h < kHeads; ++h) qsh[(second ? kHeads * D : 0) + h * D + j] = acc[h];
+            float* o = qsh + (second ? kHeads * D : 0) + (4 * hq) * D + j;
+            o[0] = acc0;
+            o[D] = acc1;
+            o[2 * D] = acc2;
+            o[3 * D] = acc3;
+        }
     }
     __syncthreads();
     if (warp < kHeads) {
@@ -827,10 +838,11 @@ __global__ void __launch_bounds__(Warps<VP>::value * 32, 1) decode_split_mma_ker
 #pragma unroll
         for (int o = 4; o < 32; o <<= 1) st.l[e] += __shfl_xor_sync(0xffffffffu, st.l[e], o);
     __syncthreads();  // tables, queries and rings are dead from here on
-    float* wM = reinterpret_cast<float*>(smem + SM::kWM);    // [warp][head]
-    float* wL = reinterpret_cast<float*>(smem + SM::kWL);    // [warp][head]
-    float* wO = reinterpret_cast<float*>(smem + SM::kWO);    // [warp][head][D]
-    float* wO2 = reinterpret_cast<float*>(smem + SM::kWO2);  // [warp][head][D] (prod values)
+    float* wM = reinterpret_cast<float*>(smem + SM::kWM);    // [warp][head] running maxima
+    float* wL = reinterpret_cast<float*>(smem + SM::kWL);    // [warp][head] sums
+    float* wF = reinterpret_cast<float*>(smem + SM::kWF);    // [warp][head] weights 2^(M_w − max_w M_w)
+    float* wO = reinterpret_cast<float*>(smem + SM::kWO);    // [warp][m][i][lane]
+    float* wO2 = reinterpret_cast<float*>(smem + SM::kWO2);  // [warp][m][i][lane] (prod values)
     if (g == 0) {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
@@ -838,55 +850,54 @@ __global__ void __launch_bounds__(Warps<VP>::value * 32, 1) decode_split_mma_ker
             wL[warp * kHeads + 2 * c + e] = st.l[e];
         }
     }
-    float* myO = wO + warp * kHeads * D;
-    float* myO2 = wO2 + warp * kHeads * D;
+    // accumulators in fragment order: each store is 32 consecutive words
+    constexpr int kFrag = kMT * 4 * 32;
 #pragma unroll
-    for (int m = 0; m < kMT; ++m) {
-        // row g of m-tile m is element (g & 1) of pair 2m of lane-run g >> 1, row g + 8 of pair 2m + 1
-        if constexpr (VB > 0) {
-            const int dA = Decoder<VB>::dim(g >> 1, 2 * m, g & 1), dB = Decoder<VB>::dim(g >> 1, 2 * m + 1, g & 1);
-            myO[(2 * c) * D + dA] = st.O[m][0];
-            myO[(2 * c + 1) * D + dA] = st.O[m][1];
-            myO[(2 * c) * D + dB] = st.O[m][2];
-            myO[(2 * c + 1) * D + dB] = st.O[m][3];
-        } else {
-            const int dA = sign_dim(g >> 1, 2 * m, g & 1), dB = sign_dim(g >> 1, 2 * m + 1, g & 1);
-            myO[(2 * c) * D + dA] = 0.f;
-            myO[(2 * c + 1) * D + dA] = 0.f;
-            myO[(2 * c) * D + dB] = 0.f;
-            myO[(2 * c + 1) * D + dB] = 0.f;
+    for (int m = 0; m < kMT; ++m)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            wO[warp * kFrag + (m * 4 + i) * 32 + lane] = st.O[m][i];
+            if constexpr (VP) wO2[warp * kFrag + (m * 4 + i) * 32 + lane] = st.O2[m][i];
         }
-        if constexpr (VP) {
-            const int sA = sign_dim(g >> 1, 2 * m, g & 1), sB = sign_dim(g >> 1, 2 * m + 1, g & 1);
-            myO2[(2 * c) * D + sA] = st.O2[m][0];
-            myO2[(2 * c + 1) * D + sA] = st.O2[m][1];
-            myO2[(2 * c) * D + sB] = st.O2[m][2];
-            myO2[(2 * c + 1) * D + sB] = st.O2[m][3];
-        }
-    }
     __syncthreads();
-    for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
-        const int h = i / D, j = i % D;
+    if (threadIdx.x < kHeads) {
+        const int h = threadIdx.x;
         float Mx = -INFINITY;
 #pragma unroll
         for (int w = 0; w < W; ++w) Mx = fmaxf(Mx, wM[w * kHeads + h]);
-        float o = 0.f, o2 = 0.f, lsum = 0.f;
-        if (Mx != -INFINITY) {
+        float lsum = 0.f;
 #pragma unroll
-            for (int w = 0; w < W; ++w) {
-                const float f = ex2(wM[w * kHeads + h] - Mx);
-                o = fmaf(f, wO[(w * kHeads + h) * D + j], o);
-                if constexpr (VP) o2 = fmaf(f, wO2[(w * kHeads + h) * D + j], o2);
-                lsum = fmaf(f, wL[w * kHeads + h], lsum);
-            }
+        for (int w = 0; w < W; ++w) {
+            const float f = Mx == -INFINITY ? 0.f : ex2(wM[w * kHeads + h] - Mx);
+            wF[w * kHeads + h] = f;
+            lsum = fmaf(f, wL[w * kHeads + h], lsum);
         }
-        const size_t ps = (head0 + h) * a.n_splits + split;
-        a.pacc[ps * D + j] = o / a.vcb.lut_scale;
-        if constexpr (VP) a.pacc2[ps * D + j] = o2;
-        if (j == 0) {
+        if (h < G) {
+            const size_t ps = (head0 + h) * a.n_splits + split;
             a.pm[ps] = Mx == -INFINITY ? -INFINITY : Mx * kLn2;
             a.pl[ps] = lsum;
         }
+    }
+    __syncthreads();
+    // element (m, i, lane) of the accumulator fragments: head 2c + (i & 1), dim from the
+    // decode map (rows g, g + 8 of m-tile m are element g & 1 of pairs 2m, 2m + 1 of run g >> 1)
+    const float inv_vs = 1.f / a.vcb.lut_scale;
+    for (int f = threadIdx.x; f < kFrag; f += blockDim.x) {
+        const int fl = f & 31, fi = (f >> 5) & 3, fm = f >> 7;
+        const int h = 2 * (fl & 3) + (fi & 1), fg = fl >> 2;
+        if (h >= G) continue;
+        float o = 0.f, o2 = 0.f;
+#pragma unroll
+        for (int w = 0; w < W; ++w) {
+            const float wf = wF[w * kHeads + h];
+            o = fmaf(wf, wO[w * kFrag + f], o);
+            if constexpr (VP) o2 = fmaf(wf, wO2[w * kFrag + f], o2);
+        }
+        const size_t ps = (head0 + h) * a.n_splits + split;
+        const int tau = 2 * fm + (fi >> 1);
+        if constexpr (VB > 0) a.pacc[ps * D + Decoder<VB>::dim(fg >> 1, tau, fg & 1)] = o * inv_vs;
+        else a.pacc[ps * D + sign_dim(fg >> 1, tau, fg & 1)] = 0.f;
+        if constexpr (VP) a.pacc2[ps * D + sign_dim(fg >> 1, tau, fg & 1)] = o2;
     }
 
     // ---- the last CTA of this group to finish merges all of its splits
