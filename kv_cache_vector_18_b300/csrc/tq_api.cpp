@@ -102,10 +102,12 @@ void free_device(tq_ctx* h) {
         if (*p) cudaFree(*p);
         *p = nullptr;
     }
-    if (h->dp.Pi_hi) cudaFree(h->dp.Pi_hi);
-    if (h->dp.Pi_lo) cudaFree(h->dp.Pi_lo);
+    uint16_t** hl[] = {&h->dp.Pi_hi, &h->dp.Pi_lo, &h->dp.T_hi, &h->dp.T_lo};
+    for (uint16_t** p : hl) {
+        if (*p) cudaFree(*p);
+        *p = nullptr;
+    }
     if (h->dp.status) cudaFree(h->dp.status);
-    h->dp.Pi_hi = h->dp.Pi_lo = nullptr;
     h->dp.status = nullptr;
 }
 
@@ -143,6 +145,26 @@ int upload_tensor_core_params(tq_ctx* h) {
     if (d % 64 == 0) {
         rc = encode_tmap_bf16_2d(&h->dp.tm_pi_hi, h->dp.Pi_hi, d, d, (uint64_t)d * 2, 64, d);
         if (rc == TQ_OK) rc = encode_tmap_bf16_2d(&h->dp.tm_pi_lo, h->dp.Pi_lo, d, d, (uint64_t)d * 2, 64, d);
+    }
+    if (rc == TQ_OK && h->hp.variant == TQ_PROD) {
+        // T = S·Πᵀ (T_ij = Σ_k S_ik Π_jk) as f16 hi + lo, row-major [i][j]: the operand of
+        // the QJL sketch s = T·e of the rotated residual e
+        std::vector<uint16_t> thi((size_t)d * d), tlo((size_t)d * d);
+        for (int i = 0; i < d; ++i)
+            for (int j = 0; j < d; ++j) {
+                double acc = 0.0;
+                for (int k = 0; k < d; ++k) acc += h->hp.S[(size_t)i * d + k] * h->hp.Pi[(size_t)j * d + k];
+                const __half vh = __float2half_rn((float)acc);
+                const __half vl = __float2half_rn((float)(acc - (double)__half2float(vh)));
+                thi[(size_t)i * d + j] = __half_as_ushort(vh);
+                tlo[(size_t)i * d + j] = __half_as_ushort(vl);
+            }
+        rc = upload_u16(thi, &h->dp.T_hi);
+        if (rc == TQ_OK) rc = upload_u16(tlo, &h->dp.T_lo);
+        if (rc == TQ_OK && d % 64 == 0) {
+            rc = encode_tmap_f16_2d(&h->dp.tm_t_hi, h->dp.T_hi, d, d, (uint64_t)d * 2, 64, d);
+            if (rc == TQ_OK) rc = encode_tmap_f16_2d(&h->dp.tm_t_lo, h->dp.T_lo, d, d, (uint64_t)d * 2, 64, d);
+        }
     }
     return rc;
 }
@@ -218,8 +240,9 @@ int check_planes(const tq_ctx& h, const tq_planes& p, const char* what) {
 
 }  // namespace
 
-int encode_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
-                        uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer) {
+namespace {
+int encode_tmap_2d(CUtensorMapDataType dtype, CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                   uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer) {
     static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
     if (encode == nullptr) {
         cudaDriverEntryPointQueryResult q;
@@ -235,11 +258,23 @@ int encode_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint
     cuuint64_t strides[1] = {row_stride_bytes};
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+    CUresult r = encode(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(TQ_ECUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
     return TQ_OK;
+}
+}  // namespace
+
+int encode_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                        uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer) {
+    return encode_tmap_2d(CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, map, base, inner, outer, row_stride_bytes, box_inner,
+                          box_outer);
+}
+int encode_tmap_f16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                       uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer) {
+    return encode_tmap_2d(CU_TENSOR_MAP_DATA_TYPE_FLOAT16, map, base, inner, outer, row_stride_bytes, box_inner,
+                          box_outer);
 }
 
 }  // namespace tq

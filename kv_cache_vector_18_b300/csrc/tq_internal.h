@@ -48,6 +48,11 @@ struct DeviceParams {
     uint16_t* Pi_lo = nullptr;
     CUtensorMap tm_pi_hi;   // TMA maps over Pi_hi / Pi_lo, box {64, d}, 128-byte swizzle
     CUtensorMap tm_pi_lo;
+    // prod: T = S·Πᵀ = T_hi + T_lo as two f16 matrices, row-major [i][j], and TMA maps
+    uint16_t* T_hi = nullptr;
+    uint16_t* T_lo = nullptr;
+    CUtensorMap tm_t_hi;
+    CUtensorMap tm_t_lo;
     int* status = nullptr;  // device word: 0, or the code of a bounded wait that expired
 };
 
@@ -92,6 +97,9 @@ int build_host_params(int d, int bits, int variant, uint64_t seed, HostParams* o
 // box {box_inner, box_outer}, 128-byte swizzle, out-of-range elements read as zero.
 int encode_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                         uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer);
+// The same for an f16 matrix.
+int encode_tmap_f16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                       uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer);
 
 // Kernel launchers (one per .cu file).  Arguments are validated by the caller.
 bool quantize_tc_supported(const tq_ctx& h, int x_dtype, int64_t n_rows);

@@ -321,12 +321,422 @@ int launch_tc_d(const tq_ctx& h, const CUtensorMap& tm_x, int64_t n_rows, const 
     }
 }
 
+
+// ---------------------------------------------------------------------------
+// The prod variant («Собственно TurboQuant»): codes with b_m = b − 1 bits as
+// above, plus the QJL sketch of the rotated unit residual e = y/‖y‖ − c[idx]:
+// signs = [T·e ≥ 0] with T = S·Πᵀ, and ‖r‖ = ‖e‖ (Π orthogonal).
+//
+// Per 128-row tile and TMEM slot (2·D columns: Y, later E, then S):
+//   MMA 1  Y = X·Πᵀ (bf16 hi/lo of Π, as above)              → columns [0, D)
+//   epilogue pass 1/2: ‖y‖, codes, and e = y/‖y‖ − c[idx] written back as f16
+//          hi/lo pairs into the Y columns already read (32-dim chunk k: hi in
+//          columns 32k … 32k + 15, lo in 32k + 16 … 32k + 31)
+//   MMA 2  S = E·Tᵀ with A read from tensor memory, three f16 passes
+//          E_hi·T_hi + E_lo·T_hi + E_hi·T_lo (≈2⁻²² relative)   → columns [D, 2D)
+//   epilogue pass 3: sign bits of S.
+// Warps: 0 TMA producer (Π, T once, then X tiles), 1 TMEM owner and MMA issuer,
+// 2..9 two epilogue warpgroups, one per TMEM slot.
+constexpr int kProdSlots = 2;
+constexpr int kProdEpiWarps = 4 * kProdSlots;
+constexpr int kProdThreads = 32 * (2 + kProdEpiWarps);
+
+template <int D>
+struct ProdCfg {
+    static constexpr int kChunks = D / kKC;
+    static constexpr int kStageBytes = kTile * D * 2;
+    static constexpr int kChunkBytesA = kTile * 128;
+    static constexpr int kChunkBytesB = D * 128;
+    static constexpr int kMatBytes = D * D * 2;
+    static constexpr int kStages = D == 64 ? 6 : 3;
+    static constexpr uint32_t kTmemCols = kProdSlots * 2 * D;  // 256 or 512
+    static constexpr size_t kBarOffset = 4 * (size_t)kMatBytes + (size_t)kStages * kStageBytes;
+    static constexpr size_t kSmemBytes = kBarOffset + 256 + 1024;  // barriers + alignment slack
+};
+
+// Positive centroids as a polynomial in the bucket count k ∈ {0 … L/2 − 1}
+// (Newton form through the L/2 points, evaluated exactly enough at the nodes).
+template <int BM>
+struct CentroidPoly {
+    static constexpr int N = BM >= 1 ? (1 << (BM - 1)) : 1;
+    float a[N];
+    __device__ void init(const Codebook& cb) {
+        constexpr int L = 1 << BM;
+        float v[N];
+#pragma unroll
+        for (int k = 0; k < N; ++k) v[k] = BM >= 1 ? cb.c[L / 2 + k] : 0.f;
+        // divided differences on nodes 0, 1, …, N − 1
+#pragma unroll
+        for (int j = 1; j < N; ++j)
+#pragma unroll
+            for (int k = N - 1; k >= j; --k) v[k] = (v[k] - v[k - 1]) / (float)j;
+#pragma unroll
+        for (int k = 0; k < N; ++k) a[k] = v[k];
+    }
+    // value at count x (pairs)
+    __device__ __forceinline__ uint64_t eval2(uint64_t x) const {
+        uint64_t p = f2(a[N - 1], a[N - 1]);
+#pragma unroll
+        for (int k = N - 2; k >= 0; --k) {
+            // p = p·(x − k) + a[k]
+            p = fma2(p, add2(x, f2(-(float)k, -(float)k)), f2(a[k], a[k]));
+        }
+        return p;
+    }
+};
+
+template <int D, int BM>
+__global__ void __launch_bounds__(kProdThreads, 1)
+quantize_prod_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_pi_hi,
+                        const __grid_constant__ CUtensorMap tm_pi_lo, const __grid_constant__ CUtensorMap tm_t_hi,
+                        const __grid_constant__ CUtensorMap tm_t_lo, int64_t n_rows, Codebook cb,
+                        uint8_t* __restrict__ codes, uint8_t* __restrict__ signs, float* __restrict__ norm_out,
+                        float* __restrict__ rnorm_out, int* __restrict__ status) {
+    using C = ProdCfg<D>;
+    constexpr int L = 1 << BM;
+    constexpr int P = BM >= 1 ? L / 2 - 1 : 0;  // positive decision boundaries
+    constexpr int WORDS = BM * D / 32;          // packed code words per row
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* pi_hi = smem;
+    uint8_t* pi_lo = smem + C::kMatBytes;
+    uint8_t* t_hi = smem + 2 * C::kMatBytes;
+    uint8_t* t_lo = smem + 3 * C::kMatBytes;
+    uint8_t* stages = smem + 4 * C::kMatBytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
+    uint64_t* full = bars;                        // [kStages] X tile landed
+    uint64_t* empty = full + C::kStages;          // [kStages] X tile consumed by MMA 1
+    uint64_t* yfull = empty + C::kStages;         // [slots] Y ready
+    uint64_t* efull = yfull + kProdSlots;         // [slots] E written (128 arrivals)
+    uint64_t* sfull = efull + kProdSlots;         // [slots] S ready
+    uint64_t* sfree = sfull + kProdSlots;         // [slots] slot read out (128 arrivals)
+    uint64_t* mat_full = sfree + kProdSlots;
+    uint64_t* drain = mat_full + 1;               // ≤ 2·6 + 8 + 2 = 22 words
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t ntiles = (n_rows + kTile - 1) / kTile;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < kProdSlots; ++a) {
+            mbar_init(&yfull[a], 1);
+            mbar_init(&efull[a], 128);
+            mbar_init(&sfull[a], 1);
+            mbar_init(&sfree[a], 128);
+        }
+        mbar_init(mat_full, 1);
+        mbar_init(drain, 1);
+        fence_barrier_init();
+    }
+    if (warp == 1) tmem_alloc(tmem_holder, C::kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------------------ producer
+        prefetch_tensormap(&tm_x);
+        prefetch_tensormap(&tm_pi_hi);
+        prefetch_tensormap(&tm_pi_lo);
+        prefetch_tensormap(&tm_t_hi);
+        prefetch_tensormap(&tm_t_lo);
+        mbar_arrive_expect_tx(mat_full, 4 * C::kMatBytes);
+        for (int c = 0; c < C::kChunks; ++c) {
+            tma_load_2d(pi_hi + c * C::kChunkBytesB, &tm_pi_hi, mat_full, c * kKC, 0);
+            tma_load_2d(pi_lo + c * C::kChunkBytesB, &tm_pi_lo, mat_full, c * kKC, 0);
+            tma_load_2d(t_hi + c * C::kChunkBytesB, &tm_t_hi, mat_full, c * kKC, 0);
+            tma_load_2d(t_lo + c * C::kChunkBytesB, &tm_t_lo, mat_full, c * kKC, 0);
+        }
+        int64_t i = 0;
+        for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++i) {
+            const int s = (int)(i % C::kStages);
+            const int64_t u = i / C::kStages;
+            if (u > 0 && !mbar_wait(&empty[s], (uint32_t)((u - 1) & 1), status, 11)) break;
+            mbar_arrive_expect_tx(&full[s], C::kStageBytes);
+            uint8_t* st = stages + (size_t)s * C::kStageBytes;
+            for (int c = 0; c < C::kChunks; ++c)
+                tma_load_2d(st + c * C::kChunkBytesA, &tm_x, &full[s], c * kKC, (int)(tile * kTile));
+        }
+        // every load issued must have landed before the CTA may exit
+        const int64_t issued = i;
+        for (int64_t k = (issued > C::kStages ? issued - C::kStages : 0); k < issued; ++k)
+            mbar_wait(&full[k % C::kStages], (uint32_t)((k / C::kStages) & 1), status, 12);
+        mbar_wait(mat_full, 0, status, 12);
+    } else if (warp == 1 && lane == 0) {
+        // ------------------------------------------------------------ MMA issuer
+        constexpr uint32_t idesc1 = idesc_bf16_f32(kTile, D);
+        constexpr uint32_t idesc2 = idesc_f16_f32(kTile, D);
+        bool ok = mbar_wait(mat_full, 0, status, 13);
+        tc_fence_after();
+        const uint32_t a_base = smem_u32(stages), pih = smem_u32(pi_hi), pil = smem_u32(pi_lo);
+        const uint32_t th = smem_u32(t_hi), tl = smem_u32(t_lo);
+        // MMA 2 of tile k: S = E·Tᵀ once the epilogue has written E into the slot
+        auto second = [&](int64_t k) {
+            const int a = (int)(k % kProdSlots);
+            const int64_t ua = k / kProdSlots;
+            if (!(ok = mbar_wait(&efull[a], (uint32_t)(ua & 1), status, 14))) return;
+            tc_fence_after();
+            const uint32_t e_tmem = tmem_base + (uint32_t)(a * 2 * D);
+            const uint32_t s_tmem = e_tmem + (uint32_t)D;
+#pragma unroll
+            for (int pass = 0; pass < 3; ++pass) {
+                const uint32_t b_base = pass == 2 ? tl : th;
+#pragma unroll
+                for (int k16 = 0; k16 < D / 16; ++k16) {
+                    // E_hi of dims 16·k16 … in columns 32·(k16/2) + 8·(k16%2), E_lo 16 columns further
+                    const uint32_t acol = 32 * (k16 >> 1) + 8 * (k16 & 1) + (pass == 1 ? 16 : 0);
+                    const uint64_t bd = smem_desc(b_base + (k16 >> 2) * C::kChunkBytesB + (k16 & 3) * 32, 1024, 2);
+                    mma_f16_ts(s_tmem, e_tmem + acol, bd, idesc2, (pass | k16) != 0);
+                }
+            }
+            mma_commit(&sfull[a]);
+        };
+        int64_t i = 0;
+        for (int64_t tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x, ++i) {
+            const int s = (int)(i % C::kStages);
+            const int a = (int)(i % kProdSlots);
+            const int64_t ua = i / kProdSlots;
+            if (!(ok = mbar_wait(&full[s], (uint32_t)((i / C::kStages) & 1), status, 15))) break;
+            if (ua > 0 && !(ok = mbar_wait(&sfree[a], (uint32_t)((ua - 1) & 1), status, 16))) break;
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + (uint32_t)(a * 2 * D);
+            const uint32_t a_stage = a_base + (uint32_t)(s * C::kStageBytes);
+#pragma unroll
+            for (int pass = 0; pass < 2; ++pass) {
+                const uint32_t b_base = pass == 0 ? pih : pil;
+#pragma unroll
+                for (int c = 0; c < C::kChunks; ++c)
+#pragma unroll
+                    for (int kk = 0; kk < kKC / 16; ++kk) {
+                        const uint64_t ad = smem_desc(a_stage + c * C::kChunkBytesA + kk * 32, 1024, 2);
+                        const uint64_t bd = smem_desc(b_base + c * C::kChunkBytesB + kk * 32, 1024, 2);
+                        mma_f16_ss(d_tmem, ad, bd, idesc1, (pass | c | kk) != 0);
+                    }
+            }
+            mma_commit(&empty[s]);
+            mma_commit(&yfull[a]);
+            if (i > 0) second(i - 1);
+        }
+        if (ok && i > 0) second(i - 1);
+        mma_commit(drain);
+        mbar_wait(drain, 0, status, 17);
+    } else if (warp >= 2) {
+        // ------------------------------------------------------------ epilogue
+        constexpr int GB = BM == 3 ? 24 : 16;  // bits per float packing group
+        constexpr int GC = BM > 0 ? GB / BM : 1;
+        constexpr int NG = BM > 0 ? 32 / GC : 1;
+        constexpr float kAcc0 = (float)(1u << (GB - 1)) - 0.5f;
+        const int wg = (warp - 2) >> 2;     // TMEM slot served
+        const int quad = warp & 3;          // TMEM lane quadrant of this warp
+        const int r_local = quad * 32 + lane;
+        float t2[P > 0 ? P : 1];
+#pragma unroll
+        for (int p = 0; p < P; ++p) t2[p] = cb.t[L / 2 + p] * cb.t[L / 2 + p];
+        CentroidPoly<BM> cp;
+        cp.init(cb);
+        const uint32_t lanebits = (uint32_t)(quad * 32) << 16;
+        const uint32_t ybase = tmem_base + (uint32_t)(wg * 2 * D) + lanebits;
+        const uint32_t sbase = ybase + (uint32_t)D;
+        int64_t j = 0;
+        for (int64_t tile = blockIdx.x + (int64_t)wg * gridDim.x; tile < ntiles;
+             tile += (int64_t)kProdSlots * gridDim.x, ++j) {
+            if (!mbar_wait(&yfull[wg], (uint32_t)(j & 1), status, 18)) break;
+            tc_fence_after();
+            uint32_t r[2][32];
+            // pass 1: ‖y‖²
+            uint64_t ss2 = 0ull;
+#pragma unroll
+            for (int c = 0; c < D / 32; c += 2) {
+                tmem_ld32(ybase + c * 32, r[0]);
+                tmem_ld32(ybase + (c + 1) * 32, r[1]);
+                tmem_wait_ld(r[0]);
+                tmem_wait_ld(r[1]);
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int k = 0; k < 32; k += 2) {
+                        const uint64_t v2 = f2(__uint_as_float(r[h][k]), __uint_as_float(r[h][k + 1]));
+                        ss2 = fma2(v2, v2, ss2);
+                    }
+            }
+            float ssa, ssb;
+            f2_split(ss2, ssa, ssb);
+            const float ss = ssa + ssb;
+            const float n = sqrtf(ss);
+            const float inv = n > 0.f ? 1.f / n : 0.f;
+            const uint64_t inv2 = f2(inv, inv);
+            const float cs = ss >= 0x1p-38f ? __fdividef(0x1p62f, ss) : 0x1p100f;
+            const float kr = cs * ss;
+            const uint64_t cs2 = f2(cs, cs);
+            float kt2[P > 0 ? P : 1];
+#pragma unroll
+            for (int p = 0; p < P; ++p) kt2[p] = -kr * t2[p];
+            const int64_t row = tile * kTile + r_local;
+            const bool live = row < n_rows;
+            const uint32_t keep = n == 0.f ? 0u : 0xffffffffu;
+            uint64_t es2 = 0ull;
+            // pass 2: chunk c + 1 is loaded while chunk c is bucketized and its residual stored
+            tmem_ld32(ybase, r[0]);
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                tmem_wait_ld(r[c & 1]);
+                if (c + 1 < D / 32) tmem_ld32(ybase + (c + 1) * 32, r[(c + 1) & 1]);
+                const uint32_t* rc = r[c & 1];
+                uint64_t acc[NG];
+#pragma unroll
+                for (int gi = 0; gi < NG; ++gi) acc[gi] = f2(kAcc0, 0.f);
+                uint32_t ehi[16], elo[16];
+#pragma unroll
+                for (int k = 0; k < 32; k += 2) {
+                    const float va = __uint_as_float(rc[k]), vb = __uint_as_float(rc[k + 1]);
+                    const uint64_t v2 = f2(va, vb);
+                    uint64_t cnt2 = f2(0.5f, 0.5f);
+                    if constexpr (P > 0) {
+                        float wa, wb;
+                        f2_split(mul2(v2, cs2), wa, wb);
+#pragma unroll
+                        for (int p = 0; p < P; ++p)
+                            cnt2 = add2(cnt2, f2(__saturatef(fmaf(va, wa, kt2[p])), __saturatef(fmaf(vb, wb, kt2[p]))));
+                    }
+                    float ca, cb2;
+                    f2_split(cnt2, ca, cb2);
+                    const uint32_t sga = __float_as_uint(va) & 0x80000000u, sgb = __float_as_uint(vb) & 0x80000000u;
+                    if constexpr (BM > 0) {
+                        const float sa = __uint_as_float(__float_as_uint(ca) | sga);
+                        const float sb = __uint_as_float(__float_as_uint(cb2) | sgb);
+                        acc[k / GC] = fma2(f2(sa, sb),
+                                           f2((float)(1u << (BM * (k % GC))), (float)(1u << (BM * ((k + 1) % GC)))),
+                                           acc[k / GC]);
+                    }
+                    // residual e = y/‖y‖ − sign(y)·c⁺[count] (0 for a zero row)
+                    uint64_t e2 = mul2(v2, inv2);
+                    if constexpr (BM > 0) {
+                        float pa, pb;
+                        f2_split(cp.eval2(add2(cnt2, f2(-0.5f, -0.5f))), pa, pb);
+                        const float qa = n > 0.f ? __uint_as_float(__float_as_uint(pa) ^ sga ^ 0x80000000u) : 0.f;
+                        const float qb = n > 0.f ? __uint_as_float(__float_as_uint(pb) ^ sgb ^ 0x80000000u) : 0.f;
+                        e2 = add2(e2, f2(qa, qb));
+                    }
+                    es2 = fma2(e2, e2, es2);
+                    float ea, eb;
+                    f2_split(e2, ea, eb);
+                    const __half2 hi = __floats2half2_rn(ea, eb);
+                    const float2 hf = __half22float2(hi);
+                    const __half2 lo = __floats2half2_rn(ea - hf.x, eb - hf.y);
+                    ehi[k / 2] = *reinterpret_cast<const uint32_t*>(&hi);
+                    elo[k / 2] = *reinterpret_cast<const uint32_t*>(&lo);
+                }
+                // the residual of these 32 dims replaces their (already read) Y columns
+                tmem_st16(ybase + c * 32, ehi);
+                tmem_st16(ybase + c * 32 + 16, elo);
+                if constexpr (BM > 0) {
+                    uint32_t cw[BM];
+#pragma unroll
+                    for (int w = 0; w < BM; ++w) cw[w] = 0u;
+#pragma unroll
+                    for (int gi = 0; gi < NG; ++gi) {
+                        float ea, eb;
+                        f2_split(acc[gi], ea, eb);
+                        const uint32_t gbits = __float2uint_rn(ea + eb);
+                        const int bit = gi * GB, w = bit >> 5, sh = bit & 31;
+                        cw[w] |= gbits << sh;
+                        if (sh + GB > 32) cw[w + 1] |= gbits >> (32 - sh);
+                    }
+                    if (live) {
+                        uint8_t* cd = codes + row * (int64_t)(WORDS * 4) + c * (BM * 4);
+                        if constexpr (BM == 2) {
+                            *reinterpret_cast<uint2*>(cd) = make_uint2(cw[0] & keep, cw[1] & keep);
+                        } else {
+#pragma unroll
+                            for (int w = 0; w < BM; ++w) reinterpret_cast<uint32_t*>(cd)[w] = cw[w] & keep;
+                        }
+                    }
+                }
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(&efull[wg]);
+            float esa, esb;
+            f2_split(es2, esa, esb);
+            if (live) {
+                norm_out[row] = n;
+                rnorm_out[row] = sqrtf(esa + esb);
+            }
+            // pass 3: sign bits of S = T·e (bit i set ⇔ s_i ≥ 0; −0 counts as +0)
+            if (!mbar_wait(&sfull[wg], (uint32_t)(j & 1), status, 19)) break;
+            tc_fence_after();
+            uint32_t sw[D / 32];
+            tmem_ld32(sbase, r[0]);
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                tmem_wait_ld(r[c & 1]);
+                if (c + 1 < D / 32) tmem_ld32(sbase + (c + 1) * 32, r[(c + 1) & 1]);
+                uint32_t neg = 0u;
+#pragma unroll
+                for (int k = 31; k >= 0; --k)
+                    neg = __funnelshift_l(__float_as_uint(__uint_as_float(r[c & 1][k]) + 0.f), neg, 1);
+                sw[c] = ~neg;
+            }
+            tc_fence_before();
+            mbar_arrive(&sfree[wg]);
+            if (live) {
+                uint32_t* sd = reinterpret_cast<uint32_t*>(signs + row * (int64_t)(D / 8));
+                if constexpr (D == 128) {
+                    *reinterpret_cast<uint4*>(sd) = make_uint4(sw[0], sw[1], sw[2], sw[3]);
+                } else {
+                    *reinterpret_cast<uint2*>(sd) = make_uint2(sw[0], sw[1]);
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, C::kTmemCols);
+    }
+}
+
+template <int D, int BM>
+int launch_prod_tc(const tq_ctx& h, const CUtensorMap& tm_x, int64_t n_rows, const tq_planes& out, cudaStream_t s) {
+    using C = ProdCfg<D>;
+    static_assert(C::kSmemBytes <= 232448, "prod quantize shared memory above the per-CTA limit");
+    auto fn = quantize_prod_tc_kernel<D, BM>;
+    static std::atomic<uint64_t> smem_set{0};
+    const int rc = ensure_smem_attr(smem_set, (const void*)fn, (int)C::kSmemBytes, "prod quantize smem attribute");
+    if (rc != TQ_OK) return rc;
+    const int64_t ntiles = (n_rows + kTile - 1) / kTile;
+    const int grid = (int)(ntiles < h.num_sms ? ntiles : h.num_sms);
+    fn<<<grid, kProdThreads, C::kSmemBytes, s>>>(tm_x, h.dp.tm_pi_hi, h.dp.tm_pi_lo, h.dp.tm_t_hi, h.dp.tm_t_lo,
+                                                 n_rows, h.cb, out.codes, out.signs, out.norm, out.rnorm,
+                                                 h.dp.status);
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? TQ_OK : cuda_fail(e, "tensor-core prod quantize launch");
+}
+
+template <int D>
+int launch_prod_tc_d(const tq_ctx& h, const CUtensorMap& tm_x, int64_t n_rows, const tq_planes& out, cudaStream_t s) {
+    switch (h.hp.b_mse) {
+        case 0: return launch_prod_tc<D, 0>(h, tm_x, n_rows, out, s);
+        case 1: return launch_prod_tc<D, 1>(h, tm_x, n_rows, out, s);
+        case 2: return launch_prod_tc<D, 2>(h, tm_x, n_rows, out, s);
+        case 3: return launch_prod_tc<D, 3>(h, tm_x, n_rows, out, s);
+        default: return fail(TQ_EUNSUPPORTED, "prod b_m=%d", h.hp.b_mse);
+    }
+}
 }  // namespace
 
 bool quantize_tc_supported(const tq_ctx& h, int x_dtype, int64_t n_rows) {
     // TMA row coordinates are 32-bit signed: the last tile must start below 2^31.
-    return x_dtype == TQ_BF16 && h.hp.variant == TQ_MSE && (h.hp.d == 64 || h.hp.d == 128) &&
-           h.dp.Pi_hi != nullptr && h.num_sms > 0 && n_rows < ((int64_t)1 << 31) - kTile;
+    const bool params = h.hp.variant == TQ_MSE ? h.dp.Pi_hi != nullptr
+                                               : (h.dp.Pi_hi != nullptr && h.dp.T_hi != nullptr && h.hp.b_mse <= 3);
+    return x_dtype == TQ_BF16 && (h.hp.d == 64 || h.hp.d == 128) && params && h.num_sms > 0 &&
+           n_rows < ((int64_t)1 << 31) - kTile;
 }
 
 int launch_quantize_tc(const tq_ctx& h, const void* x, int64_t n_rows, int64_t stride, const tq_planes& out,
@@ -334,9 +744,11 @@ int launch_quantize_tc(const tq_ctx& h, const void* x, int64_t n_rows, int64_t s
     CUtensorMap tm_x;
     int rc = encode_tmap_bf16_2d(&tm_x, x, (uint64_t)h.hp.d, (uint64_t)n_rows, (uint64_t)stride * 2, kKC, kTile);
     if (rc != TQ_OK) return rc;
+    const bool prod = h.hp.variant == TQ_PROD;
     switch (h.hp.d) {
-        case 64: return launch_tc_d<64>(h, tm_x, n_rows, out, s);
-        case 128: return launch_tc_d<128>(h, tm_x, n_rows, out, s);
+        case 64: return prod ? launch_prod_tc_d<64>(h, tm_x, n_rows, out, s) : launch_tc_d<64>(h, tm_x, n_rows, out, s);
+        case 128:
+            return prod ? launch_prod_tc_d<128>(h, tm_x, n_rows, out, s) : launch_tc_d<128>(h, tm_x, n_rows, out, s);
         default: return fail(TQ_EUNSUPPORTED, "tensor-core quantize: d=%d", h.hp.d);
     }
 }

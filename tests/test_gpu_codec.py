@@ -129,12 +129,13 @@ def test_abi_rejects_bad_arguments(tq):
     torch.cuda.synchronize()
 
 
+@pytest.mark.parametrize("variant", ["mse", "prod"])
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("bits", [1, 2, 3, 4])
-def test_tensor_core_path_many_tiles(tq, d, bits):
+def test_tensor_core_path_many_tiles(tq, d, bits, variant):
     # enough rows for several tiles per CTA on every SM, plus a ragged tail
     n = 148 * 128 * 3 + 77
-    qz = tq.Quantizer(d, bits, "mse", seed=7 + bits)
+    qz = tq.Quantizer(d, bits, variant, seed=7 + bits)
     x = synthetic.gaussian((n, d), seed=bits + d).cuda()
     planes = qz.quantize(x)
     torch.cuda.synchronize()
@@ -144,6 +145,9 @@ def test_tensor_core_path_many_tiles(tq, d, bits):
     check_quantize(oracle_params(qz), f64(x), planes, rows=rows)
     # repeat into the same planes: results must be identical
     codes0 = planes["codes"].clone()
+    signs0 = planes["signs"].clone() if variant == "prod" else None
     qz.quantize(x, out=planes)
     torch.cuda.synchronize()
     assert torch.equal(codes0, planes["codes"])
+    if variant == "prod":
+        assert torch.equal(signs0, planes["signs"])
