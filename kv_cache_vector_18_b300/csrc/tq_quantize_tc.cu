@@ -336,9 +336,10 @@ int launch_tc_d(const tq_ctx& h, const CUtensorMap& tm_x, int64_t n_rows, const 
 //          E_hi·T_hi + E_lo·T_hi + E_hi·T_lo (≈2⁻²² relative)   → columns [D, 2D)
 //   epilogue pass 3: sign bits of S.
 // Warps: 0 TMA producer (Π, T once, then X tiles), 1 TMEM owner and MMA issuer,
-// 2..9 two epilogue warpgroups, one per TMEM slot.
+// 2..17 four epilogue warpgroups: two per TMEM slot, each taking half of the
+// columns of the slot's 128 rows (the row norms are summed through shared memory).
 constexpr int kProdSlots = 2;
-constexpr int kProdEpiWarps = 4 * kProdSlots;
+constexpr int kProdEpiWarps = 8 * kProdSlots;
 constexpr int kProdThreads = 32 * (2 + kProdEpiWarps);
 
 template <int D>
@@ -348,10 +349,11 @@ struct ProdCfg {
     static constexpr int kChunkBytesA = kTile * 128;
     static constexpr int kChunkBytesB = D * 128;
     static constexpr int kMatBytes = D * D * 2;
-    static constexpr int kStages = D == 64 ? 6 : 3;
+    static constexpr int kStages = D == 64 ? 4 : 2;
     static constexpr uint32_t kTmemCols = kProdSlots * 2 * D;  // 256 or 512
     static constexpr size_t kBarOffset = 4 * (size_t)kMatBytes + (size_t)kStages * kStageBytes;
-    static constexpr size_t kSmemBytes = kBarOffset + 256 + 1024;  // barriers + alignment slack
+    static constexpr size_t kXchOffset = kBarOffset + 256;  // [slot][2 sums][2 halves][128 rows] floats
+    static constexpr size_t kSmemBytes = kXchOffset + (size_t)kProdSlots * 2 * 2 * kTile * 4 + 1024;
 };
 
 // Positive centroids as a polynomial in the bucket count k ∈ {0 … L/2 − 1}
@@ -424,9 +426,9 @@ quantize_prod_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_c
         }
         for (int a = 0; a < kProdSlots; ++a) {
             mbar_init(&yfull[a], 1);
-            mbar_init(&efull[a], 128);
+            mbar_init(&efull[a], 256);
             mbar_init(&sfull[a], 1);
-            mbar_init(&sfree[a], 128);
+            mbar_init(&sfree[a], 256);
         }
         mbar_init(mat_full, 1);
         mbar_init(drain, 1);
@@ -531,42 +533,47 @@ quantize_prod_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_c
         constexpr int GC = BM > 0 ? GB / BM : 1;
         constexpr int NG = BM > 0 ? 32 / GC : 1;
         constexpr float kAcc0 = (float)(1u << (GB - 1)) - 0.5f;
-        const int wg = (warp - 2) >> 2;     // TMEM slot served
-        const int quad = warp & 3;          // TMEM lane quadrant of this warp
+        constexpr int H = D / 2;                // columns per half
+        const int wg = (warp - 2) >> 2;         // 0..3
+        const int slot = wg >> 1, half = wg & 1;
+        const int quad = warp & 3;              // TMEM lane quadrant of this warp
         const int r_local = quad * 32 + lane;
+        float* xch = reinterpret_cast<float*>(smem + C::kXchOffset) + slot * (2 * 2 * kTile);
+        float* xss = xch;                       // [half][row] partial ‖y‖²
+        float* xes = xch + 2 * kTile;           // [half][row] partial ‖e‖²
         float t2[P > 0 ? P : 1];
 #pragma unroll
         for (int p = 0; p < P; ++p) t2[p] = cb.t[L / 2 + p] * cb.t[L / 2 + p];
         CentroidPoly<BM> cp;
         cp.init(cb);
         const uint32_t lanebits = (uint32_t)(quad * 32) << 16;
-        const uint32_t ybase = tmem_base + (uint32_t)(wg * 2 * D) + lanebits;
+        const uint32_t ybase = tmem_base + (uint32_t)(slot * 2 * D + half * H) + lanebits;
         const uint32_t sbase = ybase + (uint32_t)D;
+        auto pair_sync = [&]() { asm volatile("bar.sync %0, 256;" ::"r"(1 + slot) : "memory"); };
         int64_t j = 0;
-        for (int64_t tile = blockIdx.x + (int64_t)wg * gridDim.x; tile < ntiles;
+        for (int64_t tile = blockIdx.x + (int64_t)slot * gridDim.x; tile < ntiles;
              tile += (int64_t)kProdSlots * gridDim.x, ++j) {
-            if (!mbar_wait(&yfull[wg], (uint32_t)(j & 1), status, 18)) break;
+            if (!mbar_wait(&yfull[slot], (uint32_t)(j & 1), status, 18)) break;
             tc_fence_after();
             uint32_t r[2][32];
-            // pass 1: ‖y‖²
+            // pass 1: this half's part of ‖y‖², summed with the other half's
             uint64_t ss2 = 0ull;
 #pragma unroll
-            for (int c = 0; c < D / 32; c += 2) {
-                tmem_ld32(ybase + c * 32, r[0]);
-                tmem_ld32(ybase + (c + 1) * 32, r[1]);
-                tmem_wait_ld(r[0]);
-                tmem_wait_ld(r[1]);
+            for (int c = 0; c < H / 32; ++c) tmem_ld32(ybase + c * 32, r[c & 1]);
 #pragma unroll
-                for (int h = 0; h < 2; ++h)
+            for (int c = 0; c < H / 32; ++c) {
+                tmem_wait_ld(r[c & 1]);
 #pragma unroll
-                    for (int k = 0; k < 32; k += 2) {
-                        const uint64_t v2 = f2(__uint_as_float(r[h][k]), __uint_as_float(r[h][k + 1]));
-                        ss2 = fma2(v2, v2, ss2);
-                    }
+                for (int k = 0; k < 32; k += 2) {
+                    const uint64_t v2 = f2(__uint_as_float(r[c & 1][k]), __uint_as_float(r[c & 1][k + 1]));
+                    ss2 = fma2(v2, v2, ss2);
+                }
             }
             float ssa, ssb;
             f2_split(ss2, ssa, ssb);
-            const float ss = ssa + ssb;
+            xss[half * kTile + r_local] = ssa + ssb;
+            pair_sync();
+            const float ss = xss[r_local] + xss[kTile + r_local];  // same order in both halves
             const float n = sqrtf(ss);
             const float inv = n > 0.f ? 1.f / n : 0.f;
             const uint64_t inv2 = f2(inv, inv);
@@ -579,13 +586,14 @@ quantize_prod_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_c
             const int64_t row = tile * kTile + r_local;
             const bool live = row < n_rows;
             const uint32_t keep = n == 0.f ? 0u : 0xffffffffu;
+            const uint32_t qmask = n > 0.f ? 0xffffffffu : 0u;
             uint64_t es2 = 0ull;
             // pass 2: chunk c + 1 is loaded while chunk c is bucketized and its residual stored
             tmem_ld32(ybase, r[0]);
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
+            for (int c = 0; c < H / 32; ++c) {
                 tmem_wait_ld(r[c & 1]);
-                if (c + 1 < D / 32) tmem_ld32(ybase + (c + 1) * 32, r[(c + 1) & 1]);
+                if (c + 1 < H / 32) tmem_ld32(ybase + (c + 1) * 32, r[(c + 1) & 1]);
                 const uint32_t* rc = r[c & 1];
                 uint64_t acc[NG];
 #pragma unroll
@@ -603,23 +611,21 @@ quantize_prod_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_c
                         for (int p = 0; p < P; ++p)
                             cnt2 = add2(cnt2, f2(__saturatef(fmaf(va, wa, kt2[p])), __saturatef(fmaf(vb, wb, kt2[p]))));
                     }
-                    float ca, cb2;
-                    f2_split(cnt2, ca, cb2);
                     const uint32_t sga = __float_as_uint(va) & 0x80000000u, sgb = __float_as_uint(vb) & 0x80000000u;
+                    uint64_t e2 = mul2(v2, inv2);
                     if constexpr (BM > 0) {
+                        float ca, cb2;
+                        f2_split(cnt2, ca, cb2);
                         const float sa = __uint_as_float(__float_as_uint(ca) | sga);
                         const float sb = __uint_as_float(__float_as_uint(cb2) | sgb);
                         acc[k / GC] = fma2(f2(sa, sb),
                                            f2((float)(1u << (BM * (k % GC))), (float)(1u << (BM * ((k + 1) % GC)))),
                                            acc[k / GC]);
-                    }
-                    // residual e = y/‖y‖ − sign(y)·c⁺[count] (0 for a zero row)
-                    uint64_t e2 = mul2(v2, inv2);
-                    if constexpr (BM > 0) {
+                        // residual e = y/‖y‖ − sign(y)·c⁺[count] (0 for a zero row)
                         float pa, pb;
                         f2_split(cp.eval2(add2(cnt2, f2(-0.5f, -0.5f))), pa, pb);
-                        const float qa = n > 0.f ? __uint_as_float(__float_as_uint(pa) ^ sga ^ 0x80000000u) : 0.f;
-                        const float qb = n > 0.f ? __uint_as_float(__float_as_uint(pb) ^ sgb ^ 0x80000000u) : 0.f;
+                        const float qa = __uint_as_float((__float_as_uint(pa) ^ sga ^ 0x80000000u) & qmask);
+                        const float qb = __uint_as_float((__float_as_uint(pb) ^ sgb ^ 0x80000000u) & qmask);
                         e2 = add2(e2, f2(qa, qb));
                     }
                     es2 = fma2(e2, e2, es2);
@@ -648,7 +654,7 @@ quantize_prod_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_c
                         if (sh + GB > 32) cw[w + 1] |= gbits >> (32 - sh);
                     }
                     if (live) {
-                        uint8_t* cd = codes + row * (int64_t)(WORDS * 4) + c * (BM * 4);
+                        uint8_t* cd = codes + row * (int64_t)(WORDS * 4) + (half * (H / 32) + c) * (BM * 4);
                         if constexpr (BM == 2) {
                             *reinterpret_cast<uint2*>(cd) = make_uint2(cw[0] & keep, cw[1] & keep);
                         } else {
@@ -660,22 +666,24 @@ quantize_prod_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_c
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(&efull[wg]);
+            mbar_arrive(&efull[slot]);
             float esa, esb;
             f2_split(es2, esa, esb);
-            if (live) {
+            xes[half * kTile + r_local] = esa + esb;
+            pair_sync();
+            if (live && half == 0) {
                 norm_out[row] = n;
-                rnorm_out[row] = sqrtf(esa + esb);
+                rnorm_out[row] = sqrtf(xes[r_local] + xes[kTile + r_local]);
             }
-            // pass 3: sign bits of S = T·e (bit i set ⇔ s_i ≥ 0; −0 counts as +0)
-            if (!mbar_wait(&sfull[wg], (uint32_t)(j & 1), status, 19)) break;
+            // pass 3: sign bits of this half of S = T·e (bit i set ⇔ s_i ≥ 0; −0 counts as +0)
+            if (!mbar_wait(&sfull[slot], (uint32_t)(j & 1), status, 19)) break;
             tc_fence_after();
-            uint32_t sw[D / 32];
-            tmem_ld32(sbase, r[0]);
+            uint32_t sw[H / 32];
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
+            for (int c = 0; c < H / 32; ++c) tmem_ld32(sbase + c * 32, r[c & 1]);
+#pragma unroll
+            for (int c = 0; c < H / 32; ++c) {
                 tmem_wait_ld(r[c & 1]);
-                if (c + 1 < D / 32) tmem_ld32(sbase + (c + 1) * 32, r[(c + 1) & 1]);
                 uint32_t neg = 0u;
 #pragma unroll
                 for (int k = 31; k >= 0; --k)
@@ -683,13 +691,13 @@ quantize_prod_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_c
                 sw[c] = ~neg;
             }
             tc_fence_before();
-            mbar_arrive(&sfree[wg]);
+            mbar_arrive(&sfree[slot]);
             if (live) {
-                uint32_t* sd = reinterpret_cast<uint32_t*>(signs + row * (int64_t)(D / 8));
-                if constexpr (D == 128) {
-                    *reinterpret_cast<uint4*>(sd) = make_uint4(sw[0], sw[1], sw[2], sw[3]);
-                } else {
+                uint8_t* sd = signs + row * (int64_t)(D / 8) + half * (H / 8);
+                if constexpr (H == 64) {
                     *reinterpret_cast<uint2*>(sd) = make_uint2(sw[0], sw[1]);
+                } else {
+                    *reinterpret_cast<uint32_t*>(sd) = sw[0];
                 }
             }
         }
