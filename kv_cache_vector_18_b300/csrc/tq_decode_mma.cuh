@@ -409,7 +409,8 @@ struct Smem {
     static constexpr size_t kQ = kSzK + kSzV + kSzS;
     static constexpr size_t kQsc = kQ + 2 * kHeads * D * 4;
     static constexpr size_t kQSf = kQsc + 2 * kHeads * 4;
-    static constexpr size_t kQin = kQSf + (KP ? (size_t)kKB * 32 * 8 : 0);  // [D][kHeads] raw queries
+    static constexpr size_t kQKl = kQSf + (KP ? (size_t)kKB * 32 * 8 : 0);  // [kKB][32] f16 low parts of Q′
+    static constexpr size_t kQin = kQKl + (KB > 0 ? (size_t)kKB * 32 * 8 : 0);  // [D][kHeads] raw queries
     static constexpr size_t kStage = (kQin + (size_t)kHeads * D * 4 + 127) & ~(size_t)127;
     static constexpr size_t kMain = kStage + (size_t)W * 2 * Stage<KB, KP, VB, VP>::kBytes;
     // combine phase (reuses the same bytes): per-warp maxima, sums, weights and
@@ -445,7 +446,8 @@ template <int KB, bool KP, int VB, bool VP>
 __device__ __forceinline__ void step(Acc<VP>& st, const unsigned char* stp, int tb, int t1,
                                      const Decoder<KB>& dk, const Decoder<VB>& dv, const SignDecoder& ds,
                                      const uint32_t (&QK)[kKB][2],
-                                     const uint32_t (&QS)[kKB][2], const uint2* qsf, int lane, const float (&fK)[2],
+                                     const uint32_t (&QS)[kKB][2], const uint2* qsf, const uint2* qkl, int lane,
+                                     const float (&fK)[2],
                                      const float (&fS)[2], const SplitArgs& a, size_t head0, int G, int g, int c) {
     using ST = Stage<KB, KP, VB, VP>;
     const bool vA = tb + g < t1, vB = tb + 8 + g < t1;
@@ -467,6 +469,8 @@ __device__ __forceinline__ void step(Acc<VP>& st, const unsigned char* stp, int 
             dk.pairs(kwA, kb, a0, a2);
             dk.pairs(kwB, kb, a1, a3);
             mma16816(S1, a0, a1, a2, a3, QK[kb][0], QK[kb][1]);
+            const uint2 lo = qkl[kb * 32 + lane];  // Q′ − f16(Q′): the score keeps ~2⁻²² of q′
+            mma16816(S1, a0, a1, a2, a3, lo.x, lo.y);
         }
     }
     if constexpr (KP) {
@@ -678,6 +682,7 @@ __global__ void __launch_bounds__(Warps<VP>::value * 32, 1) decode_split_mma_ker
     float* qsh = reinterpret_cast<float*>(mp + SM::kQ);     // [2][kHeads][D]: q′, q″
     float* qsc = reinterpret_cast<float*>(mp + SM::kQsc);   // [2][kHeads]
     uint2* qsf = reinterpret_cast<uint2*>(mp + SM::kQSf);    // [kKB][32]
+    uint2* qkl = reinterpret_cast<uint2*>(mp + SM::kQKl);    // [kKB][32]
     __shared__ int s_last;
 
     const int hb = blockIdx.y % a.n_hblocks, kvh = blockIdx.y / a.n_hblocks;
@@ -776,14 +781,25 @@ __global__ void __launch_bounds__(Warps<VP>::value * 32, 1) decode_split_mma_ker
 #pragma unroll
         for (int kb = 0; kb < kKB; ++kb) {
 #pragma unroll
+            uint32_t lo[2] = {0u, 0u};
             for (int h = 0; h < 2; ++h) {
                 const int tau = 2 * kb + h;
-                QK[kb][h] = KB > 0 ? pack_h2(q1[Decoder<KB>::dim(c, tau, 0)] * i1, q1[Decoder<KB>::dim(c, tau, 1)] * i1)
-                                   : 0u;
+                if constexpr (KB > 0) {
+                    // f16 high part for the fragment, f16 low part (the rounding error) for a second MMA
+                    const float x0 = q1[Decoder<KB>::dim(c, tau, 0)] * i1, x1 = q1[Decoder<KB>::dim(c, tau, 1)] * i1;
+                    const __half2 hh = __floats2half2_rn(x0, x1);
+                    const float2 hf = __half22float2(hh);
+                    QK[kb][h] = *reinterpret_cast<const uint32_t*>(&hh);
+                    lo[h] = pack_h2(x0 - hf.x, x1 - hf.y);
+                } else {
+                    QK[kb][h] = 0u;
+                }
                 QS[kb][h] = KP ? pack_h2(q2[sign_dim(c, tau, 0)] * i2, q2[sign_dim(c, tau, 1)] * i2) : 0u;
             }
             if constexpr (QsInSmem<KP, VP>::value)
                 if (warp == 0) qsf[kb * 32 + lane] = make_uint2(QS[kb][0], QS[kb][1]);
+            if constexpr (KB > 0)
+                if (warp == 0) qkl[kb * 32 + lane] = make_uint2(lo[0], lo[1]);
         }
     }
     __syncthreads();
@@ -826,7 +842,7 @@ __global__ void __launch_bounds__(Warps<VP>::value * 32, 1) decode_split_mma_ker
         cp_async_wait<1>();
         __syncwarp();
         step<KB, KP, VB, VP>(st, mp + SM::kStage + (size_t)(warp * 2 + slot) * ST::kBytes, tb, t1, dk, dv, ds, QK,
-                             QS, qsf, lane, fK, fS, a, head0, G, g, c);
+                             QS, qsf, qkl, lane, fK, fS, a, head0, G, g, c);
         __syncwarp();  // the slot may be refilled once every lane has read it
         slot ^= 1;
     }

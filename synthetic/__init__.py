@@ -27,6 +27,15 @@ def gaussian(shape, seed: int, dtype: str = "bf16") -> torch.Tensor:
     return _cast(np.random.default_rng(seed).standard_normal(shape, dtype=np.float32), dtype)
 
 
+def gaussian_cuda(shape, seed: int, dtype=torch.bfloat16) -> torch.Tensor:
+    """I.i.d. N(0, 1) drawn on the current CUDA device by a generator seeded with
+    `seed` (for inputs too large to draw on the host; the oracle reads sampled
+    rows of the same tensor)."""
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    return torch.randn(tuple(shape), generator=g, device="cuda", dtype=torch.float32).to(dtype)
+
+
 def student_t_unit_var(shape, seed: int, nu: float = 4.0, dtype: str = "bf16") -> torch.Tensor:
     """Heavy-tailed rows: Student-t with ν degrees of freedom scaled to unit variance
     (variance of t_ν is ν/(ν−2), so ν=4 is scaled by 1/√2)."""
