@@ -356,34 +356,38 @@ struct ProdCfg {
     static constexpr size_t kSmemBytes = kXchOffset + (size_t)kProdSlots * 2 * 2 * kTile * 4 + 1024;
 };
 
-// Positive centroids as a polynomial in the bucket count k ∈ {0 … L/2 − 1}
-// (Newton form through the L/2 points, evaluated exactly enough at the nodes).
+// The positive centroids c⁺_k (k = 0 … L/2 − 1) as a polynomial in the bucket
+// counter value x = k + ½ (what the saturated boundary tests sum to), interpolating
+// the L/2 points and built in double precision, so that a residual takes one packed
+// Horner step per degree.  Coefficients are stored negated and per row multiplied
+// by 0 for a zero row, whose residual must be 0.
 template <int BM>
 struct CentroidPoly {
     static constexpr int N = BM >= 1 ? (1 << (BM - 1)) : 1;
-    float a[N];
+    float m[N];  // −(monomial coefficients), m[0] constant term
     __device__ void init(const Codebook& cb) {
         constexpr int L = 1 << BM;
-        float v[N];
+        double v[N], P[N];
 #pragma unroll
-        for (int k = 0; k < N; ++k) v[k] = BM >= 1 ? cb.c[L / 2 + k] : 0.f;
-        // divided differences on nodes 0, 1, …, N − 1
+        for (int k = 0; k < N; ++k) v[k] = BM >= 1 ? (double)cb.c[L / 2 + k] : 0.0;
+        // Newton divided differences on the nodes k + ½ (unit spacing)
 #pragma unroll
         for (int j = 1; j < N; ++j)
 #pragma unroll
-            for (int k = N - 1; k >= j; --k) v[k] = (v[k] - v[k - 1]) / (float)j;
+            for (int k = N - 1; k >= j; --k) v[k] = (v[k] - v[k - 1]) / (double)j;
+        // expand p(x) = v0 + v1 (x − x0) + v2 (x − x0)(x − x1) + … into monomials
 #pragma unroll
-        for (int k = 0; k < N; ++k) a[k] = v[k];
-    }
-    // value at count x (pairs)
-    __device__ __forceinline__ uint64_t eval2(uint64_t x) const {
-        uint64_t p = f2(a[N - 1], a[N - 1]);
+        for (int k = 0; k < N; ++k) P[k] = 0.0;
+        P[0] = v[N - 1];
 #pragma unroll
-        for (int k = N - 2; k >= 0; --k) {
-            // p = p·(x − k) + a[k]
-            p = fma2(p, add2(x, f2(-(float)k, -(float)k)), f2(a[k], a[k]));
+        for (int j = N - 2; j >= 0; --j) {
+            const double xj = j + 0.5;
+#pragma unroll
+            for (int i = N - 1; i >= 1; --i) P[i] = P[i - 1] - xj * P[i];
+            P[0] = v[j] - xj * P[0];
         }
-        return p;
+#pragma unroll
+        for (int k = 0; k < N; ++k) m[k] = (float)-P[k];
     }
 };
 
@@ -586,7 +590,11 @@ quantize_prod_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_c
             const int64_t row = tile * kTile + r_local;
             const bool live = row < n_rows;
             const uint32_t keep = n == 0.f ? 0u : 0xffffffffu;
-            const uint32_t qmask = n > 0.f ? 0xffffffffu : 0u;
+            // −c⁺ polynomial of this row (all zero for a zero row)
+            const float live_f = n > 0.f ? 1.f : 0.f;
+            uint64_t nc2[CentroidPoly<BM>::N];
+#pragma unroll
+            for (int k = 0; k < CentroidPoly<BM>::N; ++k) nc2[k] = f2(cp.m[k] * live_f, cp.m[k] * live_f);
             uint64_t es2 = 0ull;
             // pass 2: chunk c + 1 is loaded while chunk c is bucketized and its residual stored
             tmem_ld32(ybase, r[0]);
@@ -612,7 +620,7 @@ quantize_prod_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_c
                             cnt2 = add2(cnt2, f2(__saturatef(fmaf(va, wa, kt2[p])), __saturatef(fmaf(vb, wb, kt2[p]))));
                     }
                     const uint32_t sga = __float_as_uint(va) & 0x80000000u, sgb = __float_as_uint(vb) & 0x80000000u;
-                    uint64_t e2 = mul2(v2, inv2);
+                    uint64_t e2;
                     if constexpr (BM > 0) {
                         float ca, cb2;
                         f2_split(cnt2, ca, cb2);
@@ -621,12 +629,16 @@ quantize_prod_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_c
                         acc[k / GC] = fma2(f2(sa, sb),
                                            f2((float)(1u << (BM * (k % GC))), (float)(1u << (BM * ((k + 1) % GC)))),
                                            acc[k / GC]);
-                        // residual e = y/‖y‖ − sign(y)·c⁺[count] (0 for a zero row)
-                        float pa, pb;
-                        f2_split(cp.eval2(add2(cnt2, f2(-0.5f, -0.5f))), pa, pb);
-                        const float qa = __uint_as_float((__float_as_uint(pa) ^ sga ^ 0x80000000u) & qmask);
-                        const float qb = __uint_as_float((__float_as_uint(pb) ^ sgb ^ 0x80000000u) & qmask);
-                        e2 = add2(e2, f2(qa, qb));
+                        // residual e = sign(y)·(|y|/‖y‖ − c⁺(count)) (0 for a zero row)
+                        constexpr int N = CentroidPoly<BM>::N;
+                        uint64_t nc = nc2[N - 1];
+#pragma unroll
+                        for (int q = N - 2; q >= 0; --q) nc = fma2(nc, cnt2, nc2[q]);
+                        float ta, tb;
+                        f2_split(fma2(f2(fabsf(va), fabsf(vb)), inv2, nc), ta, tb);
+                        e2 = f2(__uint_as_float(__float_as_uint(ta) ^ sga), __uint_as_float(__float_as_uint(tb) ^ sgb));
+                    } else {
+                        e2 = mul2(v2, inv2);
                     }
                     es2 = fma2(e2, e2, es2);
                     float ea, eb;
@@ -675,7 +687,7 @@ quantize_prod_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_c
                 norm_out[row] = n;
                 rnorm_out[row] = sqrtf(xes[r_local] + xes[kTile + r_local]);
             }
-            // pass 3: sign bits of this half of S = T·e (bit i set ⇔ s_i ≥ 0; −0 counts as +0)
+            // pass 3: sign bits of this half of S = T·e (bit i set ⇔ s_i ≥ 0)
             if (!mbar_wait(&sfull[slot], (uint32_t)(j & 1), status, 19)) break;
             tc_fence_after();
             uint32_t sw[H / 32];
@@ -684,11 +696,12 @@ quantize_prod_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_c
 #pragma unroll
             for (int c = 0; c < H / 32; ++c) {
                 tmem_wait_ld(r[c & 1]);
+                // sign bits straight from the float sign bits (an exact ±0 needs e = 0,
+                // i.e. a zero row, whose signs are all set below)
                 uint32_t neg = 0u;
 #pragma unroll
-                for (int k = 31; k >= 0; --k)
-                    neg = __funnelshift_l(__float_as_uint(__uint_as_float(r[c & 1][k]) + 0.f), neg, 1);
-                sw[c] = ~neg;
+                for (int k = 31; k >= 0; --k) neg = __funnelshift_l(r[c & 1][k], neg, 1);
+                sw[c] = n > 0.f ? ~neg : 0xffffffffu;
             }
             tc_fence_before();
             mbar_arrive(&sfree[slot]);
