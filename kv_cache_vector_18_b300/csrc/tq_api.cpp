@@ -102,7 +102,7 @@ void free_device(tq_ctx* h) {
         if (*p) cudaFree(*p);
         *p = nullptr;
     }
-    uint16_t** hl[] = {&h->dp.Pi_hi, &h->dp.Pi_lo, &h->dp.T_hi, &h->dp.T_lo};
+    uint16_t** hl[] = {&h->dp.Pi_hi, &h->dp.Pi_lo, &h->dp.S_hi, &h->dp.S_lo, &h->dp.T_hi, &h->dp.T_lo};
     for (uint16_t** p : hl) {
         if (*p) cudaFree(*p);
         *p = nullptr;
@@ -130,17 +130,24 @@ float bf16_bits_to_f32(uint16_t b) {
     return f;
 }
 
-// Π = Π_hi + Π_lo in bf16 for the tensor-core rotation, plus their TMA maps.
+// M = M_hi + M_lo as two bf16 matrices (same row-major layout as M).
+int upload_bf16_split(const std::vector<double>& m, uint16_t** dhi, uint16_t** dlo) {
+    std::vector<uint16_t> hi(m.size()), lo(m.size());
+    for (size_t k = 0; k < m.size(); ++k) {
+        hi[k] = f32_to_bf16((float)m[k]);
+        lo[k] = f32_to_bf16((float)(m[k] - (double)bf16_bits_to_f32(hi[k])));
+    }
+    int rc = upload_u16(hi, dhi);
+    if (rc == TQ_OK) rc = upload_u16(lo, dlo);
+    return rc;
+}
+
+// Π = Π_hi + Π_lo (and S = S_hi + S_lo) in bf16 for the tensor-core kernels, plus
+// the TMA maps over Π_hi / Π_lo.
 int upload_tensor_core_params(tq_ctx* h) {
     const int d = h->hp.d;
-    std::vector<uint16_t> hi((size_t)d * d), lo((size_t)d * d);
-    for (size_t k = 0; k < hi.size(); ++k) {
-        const double v = h->hp.Pi[k];
-        hi[k] = f32_to_bf16((float)v);
-        lo[k] = f32_to_bf16((float)(v - (double)bf16_bits_to_f32(hi[k])));
-    }
-    int rc = upload_u16(hi, &h->dp.Pi_hi);
-    if (rc == TQ_OK) rc = upload_u16(lo, &h->dp.Pi_lo);
+    int rc = upload_bf16_split(h->hp.Pi, &h->dp.Pi_hi, &h->dp.Pi_lo);
+    if (rc == TQ_OK && h->hp.variant == TQ_PROD) rc = upload_bf16_split(h->hp.S, &h->dp.S_hi, &h->dp.S_lo);
     if (rc != TQ_OK) return rc;
     if (d % 64 == 0) {
         rc = encode_tmap_bf16_2d(&h->dp.tm_pi_hi, h->dp.Pi_hi, d, d, (uint64_t)d * 2, 64, d);

@@ -38,8 +38,11 @@ struct SplitArgs {
     // Query rotation inside the split kernel (tensor-core path): q′ = Π_k·q, q″ = S_k·q.
     const void* q;     // [B, Hq, d], bf16 or f32
     int q_f32;
-    const float* kPiT;  // Π_kᵀ row-major [d][d]: row i is column i of Π_k
-    const float* kST;   // S_kᵀ row-major [d][d] (prod keys)
+    // the rotation on the tensor cores: Π_k = hi + lo, S_k = hi + lo, bf16 row-major [j][i]
+    const uint16_t* kPi_hi;
+    const uint16_t* kPi_lo;
+    const uint16_t* kS_hi;
+    const uint16_t* kS_lo;
 };
 
 namespace mmadec {

@@ -63,6 +63,13 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+__device__ __forceinline__ void mma16816_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
 // Transpose of an 8×8 b16 tile held one row-pair per lane (fragment layout).
 __device__ __forceinline__ uint32_t mov_trans(uint32_t x) {
     uint32_t y;
@@ -90,6 +97,17 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
     const __half2 h = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<const uint32_t*>(&h);
 }
+__device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// Rotated queries in shared memory: each head's 128 values as four 32-value
+// chunks padded to 36, so that lane (g, c) reading chunk c of head g with 16-byte
+// loads never collides on a bank with the other lanes of its quarter-warp.
+constexpr int kQChunk = 36;
+constexpr int kQRow = 4 * kQChunk;
+__host__ __device__ constexpr int qidx(int h, int j) { return h * kQRow + (j >> 5) * kQChunk + (j & 31); }
 
 // Bits [bit, bit + NBITS) of the little-endian word run w, returned shifted
 // left by S0 (a byte offset into a table whose entries are 2^S0 bytes apart).
@@ -407,10 +425,10 @@ struct Smem {
     }
     static constexpr size_t kTabK = table_offset(0), kTabV = table_offset(1), kTabS = table_offset(2);
     static constexpr size_t kQ = kSzK + kSzV + kSzS;
-    static constexpr size_t kQsc = kQ + 2 * kHeads * D * 4;
+    static constexpr size_t kQsc = kQ + 2 * kHeads * kQRow * 4;
     static constexpr size_t kQSf = kQsc + 2 * kHeads * 4;
     static constexpr size_t kQKl = kQSf + (KP ? (size_t)kKB * 32 * 8 : 0);  // [kKB][32] f16 low parts of Q′
-    static constexpr size_t kQin = kQKl + (KB > 0 ? (size_t)kKB * 32 * 8 : 0);  // [D][kHeads] raw queries
+    static constexpr size_t kQin = kQKl + (KB > 0 ? (size_t)kKB * 32 * 8 : 0);  // [kHeads][D] raw queries
     static constexpr size_t kStage = (kQin + (size_t)kHeads * D * 4 + 127) & ~(size_t)127;
     static constexpr size_t kMain = kStage + (size_t)W * 2 * Stage<KB, KP, VB, VP>::kBytes;
     // combine phase (reuses the same bytes): per-warp maxima, sums, weights and
@@ -427,7 +445,8 @@ struct Smem {
     static constexpr size_t kML = kMW + (size_t)kHeads * kMaxSplits * 4;  // [kHeads] 1/l
     static constexpr size_t kMO = kML + kHeads * 4;                       // [2][D][kHeads] merged acc
     static constexpr size_t kMP = (kMO + 2 * (size_t)kHeads * D * 4 + 15) & ~(size_t)15;  // [D][D] Π_v, then S_v
-    static constexpr size_t kMerge = kMP + (VP ? 2 : 1) * (size_t)D * D * 4;
+    static constexpr size_t kMQ = kMP + (VP ? 2 : 1) * (size_t)D * D * 4;  // [4][kHeads][D] mat-vec partials
+    static constexpr size_t kMerge = kMQ + 4 * (size_t)kHeads * D * 4;
     static constexpr size_t kAlignSlack = kBig - 16;  // the 32 KB-aligned base lies at most this far in
     static constexpr size_t kBytes0 = kMain + kAlignSlack > kCombine ? kMain + kAlignSlack : kCombine;
     static constexpr size_t kBytes = kBytes0 > kMerge ? kBytes0 : kMerge;
@@ -630,43 +649,72 @@ __device__ __forceinline__ void merge_group(const SplitArgs& a, unsigned char* s
         if (lane == 0) linv[warp] = l > 0.f ? 1.f / l : 0.f;
     }
     __syncthreads();
-    // Σ over splits, coalesced over dims; stored dim-major so the mat-vec reads head pairs
+    // Σ over splits, coalesced over dims (up to 32 splits' loads in flight per
+    // round); stored dim-major so the mat-vec reads the 8 heads of a dim at once
     for (int i = threadIdx.x; i < G * D; i += NT) {
         const int h = i / D, j = i % D;
         const size_t hs = (head0 + h) * ns;
         const float* w = wts + h * SM::kMaxSplits;
         float o = 0.f, o2 = 0.f;
-#pragma unroll 16
-        for (int s = 0; s < ns; ++s) {
-            o = fmaf(w[s], __ldcg(a.pacc + (hs + s) * D + j), o);
-            if constexpr (VP) o2 = fmaf(w[s], __ldcg(a.pacc2 + (hs + s) * D + j), o2);
+        for (int s0 = 0; s0 < ns; s0 += 32) {
+            float v[32], v2[VP ? 32 : 1];
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+                const bool in = s0 + k < ns;
+                v[k] = in ? __ldcg(a.pacc + (hs + s0 + k) * D + j) : 0.f;
+                if constexpr (VP) v2[k] = in ? __ldcg(a.pacc2 + (hs + s0 + k) * D + j) : 0.f;
+            }
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+                const float wk = s0 + k < ns ? w[s0 + k] : 0.f;
+                o = fmaf(wk, v[k], o);
+                if constexpr (VP) o2 = fmaf(wk, v2[k], o2);
+            }
         }
         mo[j * kHeads + h] = o * linv[h];
         if constexpr (VP) mo[kHeads * D + j * kHeads + h] = o2 * linv[h];
     }
+    for (int i = G * D + threadIdx.x; i < kHeads * D; i += NT) {  // heads past G: zero
+        mo[(i % D) * kHeads + i / D] = 0.f;
+        if constexpr (VP) mo[kHeads * D + (i % D) * kHeads + i / D] = 0.f;
+    }
     __syncthreads();
-    // out[h][col] = Σ_j Π_v[j][col]·o[j][h] (+ S_v[j][col]·o2[j][h]), two heads per thread
-    const int col = threadIdx.x % D, hp = threadIdx.x / D;
-    for (int h0 = 2 * hp; h0 < G; h0 += 2 * (NT / D)) {
-        float r0 = 0.f, r1 = 0.f;
-#pragma unroll 8
-        for (int j = 0; j < D; ++j) {
-            const float p = pis[j * D + col];
-            const float2 m = *reinterpret_cast<const float2*>(mo + j * kHeads + h0);
-            r0 = fmaf(p, m.x, r0);
-            r1 = fmaf(p, m.y, r1);
-        }
-        if constexpr (VP) {
-#pragma unroll 8
-            for (int j = 0; j < D; ++j) {
-                const float p = pis[D * D + j * D + col];
-                const float2 m = *reinterpret_cast<const float2*>(mo + kHeads * D + j * kHeads + h0);
-                r0 = fmaf(p, m.x, r0);
-                r1 = fmaf(p, m.y, r1);
+    // out[h][col] = Σ_j Π_v[j][col]·o[j][h] (+ S_v[j][col]·o2[j][h]): thread (col, quarter)
+    // sums its quarter of j for all 8 heads (one matrix load feeds 8 FMAs), then
+    // the four quarters are added
+    float* part = reinterpret_cast<float*>(smem + SM::kMQ);  // [4][kHeads][D]
+    for (int t2 = threadIdx.x; t2 < 4 * D; t2 += NT) {
+        const int col = t2 % D, jq = t2 / D;
+        float r[kHeads];
+#pragma unroll
+        for (int k = 0; k < kHeads; ++k) r[k] = 0.f;
+#pragma unroll
+        for (int mtx = 0; mtx < (VP ? 2 : 1); ++mtx) {
+            const float* P = pis + mtx * D * D;
+            const float* Mo = mo + mtx * kHeads * D;
+#pragma unroll 4
+            for (int j = 32 * jq; j < 32 * jq + 32; ++j) {
+                const float p = P[j * D + col];
+                const float4 m0 = *reinterpret_cast<const float4*>(Mo + j * kHeads);
+                const float4 m1 = *reinterpret_cast<const float4*>(Mo + j * kHeads + 4);
+                r[0] = fmaf(p, m0.x, r[0]);
+                r[1] = fmaf(p, m0.y, r[1]);
+                r[2] = fmaf(p, m0.z, r[2]);
+                r[3] = fmaf(p, m0.w, r[3]);
+                r[4] = fmaf(p, m1.x, r[4]);
+                r[5] = fmaf(p, m1.y, r[5]);
+                r[6] = fmaf(p, m1.z, r[6]);
+                r[7] = fmaf(p, m1.w, r[7]);
             }
         }
-        a.out[(head0 + h0) * D + col] = r0;
-        if (h0 + 1 < G) a.out[(head0 + h0 + 1) * D + col] = r1;
+#pragma unroll
+        for (int k = 0; k < kHeads; ++k) part[(jq * kHeads + k) * D + col] = r[k];
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < G * D; i += NT) {
+        const int h = i / D, col = i % D;
+        a.out[(head0 + h) * D + col] = (part[(0 * kHeads + h) * D + col] + part[(1 * kHeads + h) * D + col]) +
+                                       (part[(2 * kHeads + h) * D + col] + part[(3 * kHeads + h) * D + col]);
     }
 }
 
@@ -679,7 +727,7 @@ __global__ void __launch_bounds__(Warps<VP>::value * 32, 1) decode_split_mma_ker
     // main-phase regions start at the first 32 KB-aligned shared address
     const uint32_t sbase = smem_addr(smem);
     unsigned char* mp = smem + (((sbase + (uint32_t)SM::kBig - 1u) & ~((uint32_t)SM::kBig - 1u)) - sbase);
-    float* qsh = reinterpret_cast<float*>(mp + SM::kQ);     // [2][kHeads][D]: q′, q″
+    float* qsh = reinterpret_cast<float*>(mp + SM::kQ);     // [2][kHeads][kQRow]: q′, q″ (see qidx)
     float* qsc = reinterpret_cast<float*>(mp + SM::kQsc);   // [2][kHeads]
     uint2* qsf = reinterpret_cast<uint2*>(mp + SM::kQSf);    // [kKB][32]
     uint2* qkl = reinterpret_cast<uint2*>(mp + SM::kQKl);    // [kKB][32]
@@ -695,6 +743,19 @@ __global__ void __launch_bounds__(Warps<VP>::value * 32, 1) decode_split_mma_ker
     const int t1 = min(t0 + a.chunk, L);
     const size_t head0 = (size_t)b * a.Hq + (size_t)kvh * a.G + (size_t)hb * kHeads;
     const int64_t rowbase = ((int64_t)b * a.Hkv + kvh) * a.T_max;
+
+    // Π_v (and S_v) of the final merge: one L2 prefetch per 128-byte line, spread
+    // over the CTAs of the grid, kept with the evict-last priority
+    {
+        const int nct = gridDim.x * gridDim.y * gridDim.z;
+        const int cta = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+        constexpr int kLines = D * D * 4 / 128;
+        const int l = cta + nct * (int)threadIdx.x;
+        if (l < (VP ? 2 : 1) * kLines) {
+            const float* p = l < kLines ? a.vPi + 32 * l : a.vS + 32 * (l - kLines);
+            asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(p));
+        }
+    }
 
     Slab sl;
     sl.kc = a.kcodes + (size_t)rowbase * (KB * 16);
@@ -713,43 +774,77 @@ __global__ void __launch_bounds__(Warps<VP>::value * 32, 1) decode_split_mma_ker
     cp_async_commit();
 
     // ---- prologue: decode tables, queries, query scales
+    // raw queries of this head block: loads issued before the table fill, stored after
+    constexpr int NT = W * 32, kQPer = kHeads * D / NT;
+    float qv[kQPer];
+#pragma unroll
+    for (int r = 0; r < kQPer; ++r) {
+        const int i = threadIdx.x + r * NT, h = i / D;
+        const size_t gi = (head0 + h) * D + (i % D);
+        qv[r] = h < G ? (a.q_f32 ? __ldg(static_cast<const float*>(a.q) + gi)
+                                 : __bfloat162float(static_cast<const __nv_bfloat16*>(a.q)[gi]))
+                      : 0.f;
+    }
     Decoder<KB>::fill(mp + SM::kTabK, a.kcb);
     Decoder<VB>::fill(mp + SM::kTabV, a.vcb);
     if constexpr (KP || VP) SignDecoder::fill(mp + SM::kTabS);
-    float* qin = reinterpret_cast<float*>(mp + SM::kQin);  // [D][kHeads] raw queries, dim-major
-    for (int i = threadIdx.x; i < kHeads * D; i += blockDim.x) {
-        const int h = i / D, j = i % D;
-        const size_t gi = (head0 + h) * D + j;
-        float v = 0.f;
-        if (h < G)
-            v = a.q_f32 ? __ldg(static_cast<const float*>(a.q) + gi)
-                        : __bfloat162float(static_cast<const __nv_bfloat16*>(a.q)[gi]);
-        qin[j * kHeads + h] = v;
-    }
+    float* qin = reinterpret_cast<float*>(mp + SM::kQin);  // [kHeads][D]
+#pragma unroll
+    for (int r = 0; r < kQPer; ++r) qin[threadIdx.x + r * NT] = qv[r];
     __syncthreads();
-    // q′ = Π_k·q and q″ = S_k·q: one job per (matrix, quad of heads, output dim j);
-    // the job walks i over row i of the transposed matrix, so a warp's loads of
-    // one i are 32 consecutive floats, and reads q_i of its four heads as one float4.
+    // q′ = Π_k·q and q″ = S_k·q on the tensor cores: D[16 × 8 dims] = A·B with
+    // A = [bf16 hi of the 8 heads' q; bf16 lo] and B = a bf16 half of the matrix,
+    // so q_hi·M + q_lo·M is the sum of rows g and g + 8; hi and lo halves of M
+    // accumulate in the same tile (fp32-level accuracy).  Each warp takes its
+    // 8-dim tiles with all of their loads in flight at once.
     {
-        constexpr int kJobs = (KP ? 2 : 1) * (kHeads / 4) * D;
-        for (int job = threadIdx.x; job < kJobs; job += blockDim.x) {
-            const int j = job % D, hq = (job / D) % (kHeads / 4), second = job / (D * (kHeads / 4));
-            const float* MT = (second ? a.kST : a.kPiT) + j;
-            float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
-#pragma unroll 32
-            for (int i = 0; i < D; ++i) {
-                const float m = __ldg(MT + (size_t)i * D);
-                const float4 x = *reinterpret_cast<const float4*>(qin + i * kHeads + 4 * hq);
-                acc0 = fmaf(m, x.x, acc0);
-                acc1 = fmaf(m, x.y, acc1);
-                acc2 = fmaf(m, x.z, acc2);
-                acc3 = fmaf(m, x.w, acc3);
+        uint32_t A[kKB][4];
+#pragma unroll
+        for (int ks = 0; ks < kKB; ++ks) {
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const float2 x = *reinterpret_cast<const float2*>(qin + g * D + 16 * ks + 2 * c + 8 * hh);
+                const __nv_bfloat162 hi = __floats2bfloat162_rn(x.x, x.y);
+                const float2 hf = __bfloat1622float2(hi);
+                A[ks][2 * hh] = *reinterpret_cast<const uint32_t*>(&hi);
+                A[ks][2 * hh + 1] = pack_bf2(x.x - hf.x, x.y - hf.y);
             }
-            float* o = qsh + (second ? kHeads * D : 0) + (4 * hq) * D + j;
-            o[0] = acc0;
-            o[D] = acc1;
-            o[2 * D] = acc2;
-            o[3 * D] = acc3;
+        }
+        constexpr int kJobs = (KP ? 2 : 1) * (D / 8);
+        constexpr int kPer = (kJobs + W - 1) / W;  // tiles per warp
+        uint32_t bh[kPer][kKB][2], bl[kPer][kKB][2];
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+            const int job = warp + u * W;
+            if (job < kJobs) {
+                const int second = job >= D / 8, j0 = 8 * (job % (D / 8));
+                const uint32_t* Mh = reinterpret_cast<const uint32_t*>(second ? a.kS_hi : a.kPi_hi);
+                const uint32_t* Ml = reinterpret_cast<const uint32_t*>(second ? a.kS_lo : a.kPi_lo);
+                const int row = ((j0 + g) * D + 2 * c) >> 1;  // word index of (j0 + g, 2c)
+#pragma unroll
+                for (int ks = 0; ks < kKB; ++ks) {
+                    bh[u][ks][0] = __ldg(Mh + row + 8 * ks);
+                    bh[u][ks][1] = __ldg(Mh + row + 8 * ks + 4);
+                    bl[u][ks][0] = __ldg(Ml + row + 8 * ks);
+                    bl[u][ks][1] = __ldg(Ml + row + 8 * ks + 4);
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+            const int job = warp + u * W;
+            if (job < kJobs) {
+                const int second = job >= D / 8, j0 = 8 * (job % (D / 8));
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int ks = 0; ks < kKB; ++ks) {
+                    mma16816_bf16(acc, A[ks], bh[u][ks][0], bh[u][ks][1]);
+                    mma16816_bf16(acc, A[ks], bl[u][ks][0], bl[u][ks][1]);
+                }
+                float* o = qsh + (second ? kHeads * kQRow : 0) + qidx(g, j0 + 2 * c);
+                o[0] = acc[0] + acc[2];
+                o[1] = acc[1] + acc[3];
+            }
         }
     }
     __syncthreads();
@@ -757,8 +852,8 @@ __global__ void __launch_bounds__(Warps<VP>::value * 32, 1) decode_split_mma_ker
         // warp w finds max|q′| (and max|q″|) of head w
         float m1 = 0.f, m2 = 0.f;
         for (int j = lane; j < D; j += 32) {
-            m1 = fmaxf(m1, fabsf(qsh[warp * D + j]));
-            if constexpr (KP) m2 = fmaxf(m2, fabsf(qsh[kHeads * D + warp * D + j]));
+            m1 = fmaxf(m1, fabsf(qsh[qidx(warp, j)]));
+            if constexpr (KP) m2 = fmaxf(m2, fabsf(qsh[kHeads * kQRow + qidx(warp, j)]));
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
@@ -776,8 +871,23 @@ __global__ void __launch_bounds__(Warps<VP>::value * 32, 1) decode_split_mma_ker
     uint32_t QK[kKB][2], QS[kKB][2];
     {
         const float i1 = 1.f / qsc[g], i2 = 1.f / qsc[kHeads + g];
-        const float* q1 = qsh + g * D;
-        const float* q2 = qsh + kHeads * D + g * D;
+        // this lane's 32 dims of q′ (and q″): chunk c of head g, eight 16-byte loads
+        float q1[32], q2[32];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const float4 u = *reinterpret_cast<const float4*>(qsh + qidx(g, 32 * c) + 4 * k);
+            q1[4 * k] = u.x;
+            q1[4 * k + 1] = u.y;
+            q1[4 * k + 2] = u.z;
+            q1[4 * k + 3] = u.w;
+            if constexpr (KP) {
+                const float4 v = *reinterpret_cast<const float4*>(qsh + kHeads * kQRow + qidx(g, 32 * c) + 4 * k);
+                q2[4 * k] = v.x;
+                q2[4 * k + 1] = v.y;
+                q2[4 * k + 2] = v.z;
+                q2[4 * k + 3] = v.w;
+            }
+        }
 #pragma unroll
         for (int kb = 0; kb < kKB; ++kb) {
 #pragma unroll
@@ -786,7 +896,7 @@ __global__ void __launch_bounds__(Warps<VP>::value * 32, 1) decode_split_mma_ker
                 const int tau = 2 * kb + h;
                 if constexpr (KB > 0) {
                     // f16 high part for the fragment, f16 low part (the rounding error) for a second MMA
-                    const float x0 = q1[Decoder<KB>::dim(c, tau, 0)] * i1, x1 = q1[Decoder<KB>::dim(c, tau, 1)] * i1;
+                    const float x0 = q1[Decoder<KB>::dim(0, tau, 0)] * i1, x1 = q1[Decoder<KB>::dim(0, tau, 1)] * i1;
                     const __half2 hh = __floats2half2_rn(x0, x1);
                     const float2 hf = __half22float2(hh);
                     QK[kb][h] = *reinterpret_cast<const uint32_t*>(&hh);
@@ -794,7 +904,7 @@ __global__ void __launch_bounds__(Warps<VP>::value * 32, 1) decode_split_mma_ker
                 } else {
                     QK[kb][h] = 0u;
                 }
-                QS[kb][h] = KP ? pack_h2(q2[sign_dim(c, tau, 0)] * i2, q2[sign_dim(c, tau, 1)] * i2) : 0u;
+                QS[kb][h] = KP ? pack_h2(q2[sign_dim(0, tau, 0)] * i2, q2[sign_dim(0, tau, 1)] * i2) : 0u;
             }
             if constexpr (QsInSmem<KP, VP>::value)
                 if (warp == 0) qsf[kb * 32 + lane] = make_uint2(QS[kb][0], QS[kb][1]);

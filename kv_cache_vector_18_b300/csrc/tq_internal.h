@@ -46,6 +46,8 @@ struct DeviceParams {
     // Tensor-core operands: Π = Π_hi + Π_lo as two bf16 matrices, row-major [j][i].
     uint16_t* Pi_hi = nullptr;
     uint16_t* Pi_lo = nullptr;
+    uint16_t* S_hi = nullptr;  // S = S_hi + S_lo, bf16 row-major [j][i] (prod)
+    uint16_t* S_lo = nullptr;
     CUtensorMap tm_pi_hi;   // TMA maps over Pi_hi / Pi_lo, box {64, d}, 128-byte swizzle
     CUtensorMap tm_pi_lo;
     // prod: T = S·Πᵀ = T_hi + T_lo as two f16 matrices, row-major [i][j], and TMA maps
