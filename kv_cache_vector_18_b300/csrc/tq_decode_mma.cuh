@@ -317,6 +317,7 @@ struct Stage {
 
 // Plane pointers of this CTA's (batch, KV head) slab.
 struct Slab {
+    bool a16;  // the slab's norm planes start on a 16-byte boundary
     const uint8_t* kc;
     const uint8_t* ks;
     const float* kn;
@@ -327,39 +328,54 @@ struct Slab {
     const float* vrn;
 };
 
-// Rows [tb, tb + 16) of a plane with `rb`-byte rows (a multiple of 16) into
-// smem at dst; rows at or past `rows` are zero-filled without being read.
-__device__ __forceinline__ void stage_rows16(uint32_t dst, const uint8_t* plane, int rb, int tb, int rows,
-                                             int lane) {
-    for (int k = lane; k < rb; k += 32) {  // 16 rows × rb bytes = rb chunks of 16 bytes
-        const int row = (16 * k) / rb;
-        const bool ok = tb + row < rows;
-        const uint8_t* src = ok ? plane + (size_t)tb * rb + 16 * k : plane;
-        cp_async16(dst + 16 * k, src, ok ? 16u : 0u);
+// Rows [tb, tb + 16) of a plane with RB-byte rows (a multiple of 16) into smem
+// at dst, chunk k of 16 bytes through lane k mod 32.  `src` is the tile's first
+// byte.  A full tile copies without predicates; in the chunk's last tile the
+// rows at or past `rows` (tile-relative) are zero-filled without being read.
+template <int RB>
+__device__ __forceinline__ void stage_rows16(uint32_t dst, const uint8_t* src, bool full, int rows, int lane) {
+#pragma unroll
+    for (int r = 0; r < (RB + 31) / 32; ++r) {
+        const int k = lane + 32 * r;
+        if (RB % 32 == 0 || k < RB) {
+            if (full) {
+                cp_async16(dst + 16 * k, src + 16 * k, 16u);
+            } else {
+                const bool ok = (16 * k) / RB < rows;
+                cp_async16(dst + 16 * k, ok ? src + 16 * k : src, ok ? 16u : 0u);
+            }
+        }
     }
 }
-__device__ __forceinline__ void stage_rows4(uint32_t dst, const float* plane, int tb, int rows, int lane) {
-    if (lane < kTile) {
-        const bool ok = tb + lane < rows;
-        cp_async4(dst + 4 * lane, ok ? plane + tb + lane : plane, ok ? 4u : 0u);
+// A tile of fp32 norms: four 16-byte copies (lanes 0–3) when the tile is full and
+// the plane's rows start on a 16-byte boundary (a16, uniform over the CTA), else
+// one 4-byte copy per row (lanes 0–15).
+__device__ __forceinline__ void stage_rows4(uint32_t dst, const float* src, bool full, bool a16, int rows, int lane) {
+    if (full && a16) {
+        if (lane < 4) cp_async16(dst + 16 * lane, src + 4 * lane, 16u);
+    } else if (lane < kTile) {
+        const bool ok = full || lane < rows;
+        cp_async4(dst + 4 * lane, ok ? src + lane : src, ok ? 4u : 0u);
     }
 }
 
 template <int KB, bool KP, int VB, bool VP>
-__device__ __forceinline__ void stage_tile(uint32_t dst, const Slab& s, int tb, int rows, int lane) {
+__device__ __forceinline__ void stage_tile(uint32_t dst, const Slab& s, int tb, int t1, int lane) {
     using ST = Stage<KB, KP, VB, VP>;
-    if constexpr (KB > 0) stage_rows16(dst + ST::kKC, s.kc, ST::kRK, tb, rows, lane);
+    const bool full = tb + kTile <= t1;
+    const int rows = t1 - tb;
+    if constexpr (KB > 0) stage_rows16<ST::kRK>(dst + ST::kKC, s.kc + (size_t)tb * ST::kRK, full, rows, lane);
     if constexpr (KP) {
-        stage_rows16(dst + ST::kKS, s.ks, 16, tb, rows, lane);
-        stage_rows4(dst + ST::kKR, s.krn, tb, rows, lane);
+        stage_rows16<16>(dst + ST::kKS, s.ks + (size_t)tb * 16, full, rows, lane);
+        stage_rows4(dst + ST::kKR, s.krn + tb, full, s.a16, rows, lane);
     }
-    stage_rows4(dst + ST::kKN, s.kn, tb, rows, lane);
-    if constexpr (VB > 0) stage_rows16(dst + ST::kVC, s.vc, ST::kRV, tb, rows, lane);
+    stage_rows4(dst + ST::kKN, s.kn + tb, full, s.a16, rows, lane);
+    if constexpr (VB > 0) stage_rows16<ST::kRV>(dst + ST::kVC, s.vc + (size_t)tb * ST::kRV, full, rows, lane);
     if constexpr (VP) {
-        stage_rows16(dst + ST::kVS, s.vs, 16, tb, rows, lane);
-        stage_rows4(dst + ST::kVR, s.vrn, tb, rows, lane);
+        stage_rows16<16>(dst + ST::kVS, s.vs + (size_t)tb * 16, full, rows, lane);
+        stage_rows4(dst + ST::kVR, s.vrn + tb, full, s.a16, rows, lane);
     }
-    stage_rows4(dst + ST::kVN, s.vn, tb, rows, lane);
+    stage_rows4(dst + ST::kVN, s.vn + tb, full, s.a16, rows, lane);
 }
 
 template <int NW>
@@ -758,6 +774,7 @@ __global__ void __launch_bounds__(Warps<VP>::value * 32, 1) decode_split_mma_ker
     }
 
     Slab sl;
+    sl.a16 = (rowbase & 3) == 0;
     sl.kc = a.kcodes + (size_t)rowbase * (KB * 16);
     sl.ks = a.ksigns + (size_t)rowbase * 16;
     sl.kn = a.knorm + rowbase;
