@@ -491,6 +491,21 @@ def run_ours(args, spec):
                 "frac": achieved / peaks["hbm_gbs"], "traffic": recorded_traffic(traffic_key, src, units),
                 "peak_source": peaks["source"], "bytes_per_launch": nbytes, "launch_ms": ms, "source_hash": src}
 
+    def tensor_info(spec_bits, variant, rows, ms_list):
+        """Tensor-pipe view of a quantize call: algorithmic flops (2d² per row for
+        the rotation, 4d² with the QJL sketch) and the flops the kernel executes
+        (bf16 hi/lo and f16 hi/lo passes: 2 for mse, 2 + 3 for prod)."""
+        ms = statistics.mean(ms_list)
+        alg = (4 if variant == "prod" else 2) * d * d * rows
+        exe = (5 if variant == "prod" else 2) * 2 * d * d * rows
+        peak = peaks.get("bf16_tflops")
+        out = {"algorithmic_tflops": alg / (ms / 1e3) / 1e12, "executed_tflops": exe / (ms / 1e3) / 1e12,
+               "peak_tflops": peak}
+        if peak:
+            out["frac_algorithmic"] = out["algorithmic_tflops"] / peak
+            out["frac_executed"] = out["executed_tflops"] / peak
+        return out
+
     rl = {
         "quantize_k": hbm_roofline(f"tq_quantize ({spec['k_variant']} b={spec['k_bits']})", qk, tm["quant_k"],
                                    f"quantize_{spec['k_variant']}_b{spec['k_bits']}_d{d}", qsrc, tm["n_rows"]),
@@ -500,6 +515,11 @@ def run_ours(args, spec):
                                f"decode_{spec['k_variant']}_b{spec['k_bits']}_{spec['v_variant']}_b{spec['v_bits']}_d{d}",
                                dsrc, tm["ctx_rows"]),
     }
+    rl["quantize_k"]["tensor"] = tensor_info(spec["k_bits"], spec["k_variant"], tm["n_rows"], qk)
+    rl["quantize_v"]["tensor"] = tensor_info(spec["v_bits"], spec["v_variant"], tm["n_rows"], qv)
+    # score, QJL and value products: 2·d flop each per token-head and query head
+    dec_flops = (3 if spec["k_variant"] == "prod" else 2) * 2 * d * (Hq // Hkv) * tm["ctx_rows"]
+    rl["decode"]["mma_tflops"] = dec_flops / (statistics.mean(dc) / 1e3) / 1e12
     # dominant kernel: calls of the same kernel (K and V quantize with one
     # configuration) are one kernel; the largest total device time wins
     groups = {}

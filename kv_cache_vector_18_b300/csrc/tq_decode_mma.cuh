@@ -812,15 +812,19 @@ __global__ void __launch_bounds__(Warps<VP>::value * 32, 1) decode_split_mma_ker
     // q′ = Π_k·q and q″ = S_k·q on the tensor cores: D[16 × 8 dims] = A·B with
     // A = [bf16 hi of the 8 heads' q; bf16 lo] and B = a bf16 half of the matrix,
     // so q_hi·M + q_lo·M is the sum of rows g and g + 8; hi and lo halves of M
-    // accumulate in the same tile (fp32-level accuracy).  Each warp takes its
-    // 8-dim tiles with all of their loads in flight at once.
+    // accumulate in the same tile (fp32-level accuracy).  The contraction order
+    // is permuted so that in k16 blocks 2p and 2p + 1 lane (g, c) holds the eight
+    // consecutive input dims 32p + 8c … 32p + 8c + 7: its matrix operand is one
+    // 16-byte load of row j0 + g.  Each warp takes its 8-dim tiles with all of
+    // their loads in flight at once.
     {
         uint32_t A[kKB][4];
 #pragma unroll
         for (int ks = 0; ks < kKB; ++ks) {
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
-                const float2 x = *reinterpret_cast<const float2*>(qin + g * D + 16 * ks + 2 * c + 8 * hh);
+                const int d0 = 32 * (ks >> 1) + 8 * c + 4 * (ks & 1) + 2 * hh;
+                const float2 x = *reinterpret_cast<const float2*>(qin + g * D + d0);
                 const __nv_bfloat162 hi = __floats2bfloat162_rn(x.x, x.y);
                 const float2 hf = __bfloat1622float2(hi);
                 A[ks][2 * hh] = *reinterpret_cast<const uint32_t*>(&hi);
@@ -829,21 +833,19 @@ __global__ void __launch_bounds__(Warps<VP>::value * 32, 1) decode_split_mma_ker
         }
         constexpr int kJobs = (KP ? 2 : 1) * (D / 8);
         constexpr int kPer = (kJobs + W - 1) / W;  // tiles per warp
-        uint32_t bh[kPer][kKB][2], bl[kPer][kKB][2];
+        uint4 bh[kPer][kKB / 2], bl[kPer][kKB / 2];  // bf16 dims 32p + 8c … + 7 of row j0 + g
 #pragma unroll
         for (int u = 0; u < kPer; ++u) {
             const int job = warp + u * W;
             if (job < kJobs) {
                 const int second = job >= D / 8, j0 = 8 * (job % (D / 8));
-                const uint32_t* Mh = reinterpret_cast<const uint32_t*>(second ? a.kS_hi : a.kPi_hi);
-                const uint32_t* Ml = reinterpret_cast<const uint32_t*>(second ? a.kS_lo : a.kPi_lo);
-                const int row = ((j0 + g) * D + 2 * c) >> 1;  // word index of (j0 + g, 2c)
+                const uint4* Mh = reinterpret_cast<const uint4*>(second ? a.kS_hi : a.kPi_hi);
+                const uint4* Ml = reinterpret_cast<const uint4*>(second ? a.kS_lo : a.kPi_lo);
+                const int row = ((j0 + g) * D + 8 * c) >> 3;  // 16-byte index of (j0 + g, 8c)
 #pragma unroll
-                for (int ks = 0; ks < kKB; ++ks) {
-                    bh[u][ks][0] = __ldg(Mh + row + 8 * ks);
-                    bh[u][ks][1] = __ldg(Mh + row + 8 * ks + 4);
-                    bl[u][ks][0] = __ldg(Ml + row + 8 * ks);
-                    bl[u][ks][1] = __ldg(Ml + row + 8 * ks + 4);
+                for (int p2 = 0; p2 < kKB / 2; ++p2) {
+                    bh[u][p2] = __ldg(Mh + row + 4 * p2);
+                    bl[u][p2] = __ldg(Ml + row + 4 * p2);
                 }
             }
         }
@@ -855,8 +857,9 @@ __global__ void __launch_bounds__(Warps<VP>::value * 32, 1) decode_split_mma_ker
                 float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int ks = 0; ks < kKB; ++ks) {
-                    mma16816_bf16(acc, A[ks], bh[u][ks][0], bh[u][ks][1]);
-                    mma16816_bf16(acc, A[ks], bl[u][ks][0], bl[u][ks][1]);
+                    const uint4 h = bh[u][ks >> 1], l = bl[u][ks >> 1];
+                    mma16816_bf16(acc, A[ks], (ks & 1) ? h.z : h.x, (ks & 1) ? h.w : h.y);
+                    mma16816_bf16(acc, A[ks], (ks & 1) ? l.z : l.x, (ks & 1) ? l.w : l.y);
                 }
                 float* o = qsh + (second ? kHeads * kQRow : 0) + qidx(g, j0 + 2 * c);
                 o[0] = acc[0] + acc[2];
