@@ -437,40 +437,74 @@ def run_ours(args, spec):
             fn()
         host_us.append((time.perf_counter() - t) / 20 * 1e6)
         torch.cuda.synchronize()
-    # One CUDA graph per library call, captured from the same public API: a replay
-    # issues exactly the library's kernels with no host work in between, so the
-    # events below time the device alone.
-    graphs = []
-    for fn in calls:
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            fn()
-        graphs.append(g)
-    def step(ev):
-        ev[0].record()
-        for i, g in enumerate(graphs):
-            g.replay()
-            ev[i + 1].record()
+    # One CUDA graph per step holding the three library calls back to back (as a
+    # serving loop replays them), captured from the same public API, with event
+    # record nodes between the calls: the replay issues exactly the library's
+    # kernels with no host work in between, the inner events give the per-call
+    # device times and events around each replay the step time.  If event nodes
+    # cannot be captured, one graph per call with events between the replays.
+    cap_ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(calls) + 1)]
+    step_graph, graphs, graph_note = None, [], ""
+    try:
+        sg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(sg):
+            cap_ev[0].record()
+            for i, fn in enumerate(calls):
+                fn()
+                cap_ev[i + 1].record()
+        sg.replay()
+        torch.cuda.synchronize()
+        _ = cap_ev[0].elapsed_time(cap_ev[-1])
+        step_graph = sg
+    except Exception as exc:  # fall back to one graph per call
+        graph_note = f"step graph unavailable ({type(exc).__name__}); "
+        torch.cuda.synchronize()
+        for fn in calls:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                fn()
+            graphs.append(g)
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    def replay_all():
+        if step_graph is not None:
+            step_graph.replay()
+        else:
+            for g in graphs:
+                g.replay()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(args.steps)]
+    per_call = []
     sampler = ClockSampler(local)
     with sampler:
         # The SM clock idles far below its maximum and takes a sustained load to
         # ramp up; keep the device busy for at least WARM_SECONDS (and W steps)
         # right up to the timed loop so that no idle gap precedes it.
-        warm_steps = keep_busy(lambda: (flush.zero_(), [g.replay() for g in graphs]), args.warmup, args.warm_seconds)
+        warm_steps = keep_busy(lambda: (flush.zero_(), replay_all()), args.warmup, args.warm_seconds)
         barrier(world)
         wall0 = time.perf_counter()
         for i in range(args.steps):
             flush.zero_()
-            step(evs[i])
+            ev = evs[i]
+            if step_graph is not None:
+                ev[0].record()
+                step_graph.replay()
+                ev[-1].record()
+                torch.cuda.synchronize()  # the in-graph events are read before the next replay
+                per_call.append([cap_ev[k].elapsed_time(cap_ev[k + 1]) for k in range(len(calls))])
+            else:
+                ev[0].record()
+                for k, g in enumerate(graphs):
+                    g.replay()
+                    ev[k + 1].record()
         torch.cuda.synchronize()
         wall = time.perf_counter() - wall0
     barrier(world)
-    qk = [e[0].elapsed_time(e[1]) for e in evs]
-    qv = [e[1].elapsed_time(e[2]) for e in evs]
-    dc = [e[2].elapsed_time(e[3]) for e in evs]
-    step_ms = [e[0].elapsed_time(e[3]) for e in evs]
+    if step_graph is None:
+        per_call = [[e[k].elapsed_time(e[k + 1]) for k in range(len(calls))] for e in evs]
+    qk = [c[0] for c in per_call]
+    qv = [c[1] for c in per_call]
+    dc = [c[2] for c in per_call]
+    step_ms = [e[0].elapsed_time(e[-1]) for e in evs]
     t_local = sum(step_ms) / 1e3
     t_step = max_over_ranks(t_local, world, dev)
     value = aggregate_throughput(tm["total"] * args.steps, t_local, world, dev) / 1e9
@@ -552,8 +586,11 @@ def run_ours(args, spec):
             "gpu_launches": args.steps * (2 * LAUNCHES["quantize"] + LAUNCHES["decode"]),
             "clocks": sampler.summary(), "wall_s_timed_loop": wall, "roofline": roofline,
             "roofline_decode": roofline_decode, "roofline_per_call": rl, "e2e": e2e,
-            "timing": "CUDA events around CUDA-graph replays of each library call (one graph per call, "
-                      "captured through the public API), after >= %.1f s of back-to-back warm-up (%d steps)"
+            "timing": graph_note + ("one CUDA graph per step holding the three library calls (captured through "
+                                    "the public API); step time from CUDA events around each replay, per-call "
+                                    "times from event nodes inside the graph" if step_graph is not None else
+                                    "CUDA events around CUDA-graph replays of each library call (one graph per call)")
+                      + "; L2 flushed before every step; after >= %.1f s of back-to-back warm-up (%d steps)"
                       % (args.warm_seconds, warm_steps),
             "host_us_per_direct_call": {"quantize_k": host_us[0], "quantize_v": host_us[1], "decode": host_us[2]}}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
