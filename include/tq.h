@@ -175,6 +175,18 @@ int tq_decode_attention(tq_handle hk, tq_handle hv, const void* q, int q_dtype,
 int tq_device_status(tq_handle h, int* status, int clear);
 
 /*
+ * tq_check_wait_timeout — exercise the timeout path that tq_device_status
+ * reports, without faulting or hanging anything.  Enqueues on `stream` one
+ * 32-thread block that waits on a shared-memory mbarrier which nothing
+ * completes, using the same bounded wait as the quantize pipelines but with a
+ * limit of limit_ns nanoseconds (1 ≤ limit_ns ≤ 10⁹, else TQ_EINVAL).  When
+ * the limit expires the block stores `code` (1 ≤ code ≤ 1000, else TQ_EINVAL)
+ * into the handle's status word and returns.  Asynchronous; read the result
+ * with tq_device_status.  No other buffer is touched.
+ */
+int tq_check_wait_timeout(tq_handle h, int code, uint64_t limit_ns, void* stream);
+
+/*
  * tq_decode_attention_noalloc — the same computation and arguments as
  * tq_decode_attention, minus the workspace.  It is for callers that cannot call
  * cudaMalloc or hand over a buffer: a serving loop whose device memory is wholly

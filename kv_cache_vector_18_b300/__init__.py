@@ -102,6 +102,10 @@ class Quantizer:
         check(_lib.lib().tq_device_status(self._h, ctypes.byref(st), int(clear)))
         return st.value
 
+    def check_wait_timeout(self, code: int, limit_ns: int, stream=None) -> None:
+        """Enqueue a block whose bounded wait expires and records `code` (tq_check_wait_timeout)."""
+        check(_lib.lib().tq_check_wait_timeout(self._h, int(code), int(limit_ns), _stream(stream)))
+
     def empty_planes(self, n_rows: int, device=None) -> dict:
         """Allocate packed planes for n_rows rows (see include/tq.h for the layout)."""
         dev = device if device is not None else torch.device("cuda", self.device)

@@ -22,7 +22,7 @@ ERROR_NAMES = {TQ_EINVAL: "TQ_EINVAL", TQ_EUNSUPPORTED: "TQ_EUNSUPPORTED", TQ_EA
 # Every symbol include/tq.h declares, for the export check.
 EXPORTED = ["tq_init", "tq_destroy", "tq_row_bytes", "tq_build_params_host", "tq_get_params",
             "tq_quantize", "tq_dequantize", "tq_decode_workspace_bytes", "tq_decode_attention",
-            "tq_decode_attention_noalloc", "tq_device_status", "tq_last_error"]
+            "tq_decode_attention_noalloc", "tq_device_status", "tq_check_wait_timeout", "tq_last_error"]
 NOALLOC_WORKSPACE_BYTES = 4 << 20
 
 
@@ -63,6 +63,7 @@ def lib() -> ctypes.CDLL:
     L.tq_decode_attention_noalloc.argtypes = [vp, vp, vp, i32, Planes, Planes, vp, i32, i32, i32, i32,
                                               ctypes.c_float, vp, vp, vp]
     L.tq_device_status.argtypes = [vp, ctypes.POINTER(i32), i32]
+    L.tq_check_wait_timeout.argtypes = [vp, i32, u64, vp]
     L.tq_last_error.restype = ctypes.c_char_p
     for name in EXPORTED:
         if name != "tq_last_error":

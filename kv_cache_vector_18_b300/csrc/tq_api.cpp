@@ -370,6 +370,14 @@ int tq_device_status(tq_handle h, int* status, int clear) {
     return TQ_OK;
 }
 
+int tq_check_wait_timeout(tq_handle h, int code, uint64_t limit_ns, void* stream) {
+    int rc = validate_handle(h, "quantizer");
+    if (rc != TQ_OK) return rc;
+    if (code < 1 || code > 1000) return fail(TQ_EINVAL, "code must be in [1, 1000]");
+    if (limit_ns < 1 || limit_ns > 1000000000ull) return fail(TQ_EINVAL, "limit_ns must be in [1, 1e9]");
+    return launch_expire_wait(*h, code, limit_ns, (cudaStream_t)stream);
+}
+
 int tq_get_params(tq_handle h, double* Pi, double* S, double* centroids, double* bounds) {
     if (h == nullptr) return fail(TQ_EINVAL, "handle is NULL");
     const HostParams& hp = h->hp;

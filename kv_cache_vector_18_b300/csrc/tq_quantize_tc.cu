@@ -750,7 +750,27 @@ int launch_prod_tc_d(const tq_ctx& h, const CUtensorMap& tm_x, int64_t n_rows, c
         default: return fail(TQ_EUNSUPPORTED, "prod b_m=%d", h.hp.b_mse);
     }
 }
+// One CTA whose pipeline wait nothing completes: the bounded wait gives up after
+// limit_ns, records `code` in the status word and the kernel returns.  It checks
+// the failure path of every pipeline in this file without faulting anything.
+__global__ void expire_wait_kernel(int* status, int code, uint64_t limit_ns) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) mbar_wait(&bar, 0, status, code, limit_ns);
+    __syncthreads();
+}
+
 }  // namespace
+
+int launch_expire_wait(const tq_ctx& h, int code, uint64_t limit_ns, cudaStream_t s) {
+    expire_wait_kernel<<<1, 32, 0, s>>>(h.dp.status, code, limit_ns);
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? TQ_OK : cuda_fail(e, "wait-timeout check launch");
+}
 
 bool quantize_tc_supported(const tq_ctx& h, int x_dtype, int64_t n_rows) {
     // TMA row coordinates are 32-bit signed: the last tile must start below 2^31.

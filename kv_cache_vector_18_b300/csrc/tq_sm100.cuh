@@ -60,18 +60,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
 }
 
 // Wait for the phase of `bar` with the given parity to complete, at most
-// kWaitLimitNs.  On timeout stores `code` into *status and returns false.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status, int code) {
+// limit_ns.  On timeout stores `code` into *status and returns false.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status, int code,
+                                          uint64_t limit_ns) {
     const uint32_t a = smem_u32(bar);
     if (mbar_try_wait(a, parity)) return true;
     const uint64_t t0 = globaltimer();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(a, parity)) return true;
-        if ((it & 255u) == 0 && globaltimer() - t0 > kWaitLimitNs) {
+        if ((it & 255u) == 0 && globaltimer() - t0 > limit_ns) {
             atomicExch(status, code);
             return false;
         }
     }
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status, int code) {
+    return mbar_wait(bar, parity, status, code, kWaitLimitNs);
 }
 
 // 2-D tiled TMA load of box {x: inner, y: outer} at coordinates (x, y) into

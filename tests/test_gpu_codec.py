@@ -129,6 +129,38 @@ def test_abi_rejects_bad_arguments(tq):
     torch.cuda.synchronize()
 
 
+def test_bounded_wait_timeout_reports_status(tq):
+    # A block waits on an mbarrier that nothing completes.  The bounded wait (the one
+    # every quantize pipeline stage uses) gives up after 50 ms, records the code in the
+    # status word and returns; the context stays usable and later work is unaffected.
+    from kv_cache_vector_18_b300 import _lib
+    qz = tq.Quantizer(128, 3, "mse", seed=3)
+    assert qz.device_status() == 0
+    L = _lib.lib()
+    assert L.tq_check_wait_timeout(qz.handle, 0, 50_000_000, None) == _lib.TQ_EINVAL
+    assert L.tq_check_wait_timeout(qz.handle, 99, 0, None) == _lib.TQ_EINVAL
+    assert L.tq_check_wait_timeout(qz.handle, 99, 2_000_000_000, None) == _lib.TQ_EINVAL
+    assert L.tq_check_wait_timeout(None, 99, 50_000_000, None) == _lib.TQ_EINVAL
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    qz.check_wait_timeout(99, 50_000_000)
+    t1.record()
+    torch.cuda.synchronize()
+    assert 45.0 <= t0.elapsed_time(t1) < 1000.0
+    assert qz.device_status(clear=False) == 99
+    assert qz.device_status(clear=True) == 99
+    assert qz.device_status() == 0
+    # the handle still quantizes correctly after the timeout
+    n = 148 * 128 + 33
+    x = synthetic.gaussian((n, 128), seed=5).cuda()
+    planes = qz.quantize(x)
+    torch.cuda.synchronize()
+    assert qz.device_status() == 0
+    rows = np.concatenate([np.arange(0, 200), np.arange(n - 200, n)])
+    check_quantize(oracle_params(qz), f64(x), planes, rows=rows)
+
+
 @pytest.mark.parametrize("variant", ["mse", "prod"])
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("bits", [1, 2, 3, 4])
