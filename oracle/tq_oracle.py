@@ -13,6 +13,10 @@ splitmix64 / gaussian_matrix   pinned: SplitMix64 known-answer outputs for seed 
                                Box-Muller sample moments and a KS test vs N(0,1).
 rotation_matrix (Π)            pinned: orthogonality to 1e-12; sign convention
                                diag(R) > 0 checked against a re-factorisation.
+hadamard_matrix /              pinned: H equals scipy.linalg.hadamard; Π x equals an
+hadamard_rotation (Π_H)        in-place butterfly transform of σ∘x over √d; one-hot
+                               rows give the closed-form b = 1 distortion
+                               (1 − √d·c₁)²; Gaussian rows keep D_mse = d·C(f_X,b).
 coord_density / cdf / moment   pinned: density integrates to 1 (quadrature), the
                                b=1 centroid equals the closed form
                                Γ(d/2)/(√π Γ((d+1)/2)), Gaussian limit at large d.
@@ -42,6 +46,12 @@ Readings where the page is silent (each also listed in the design doc)
   matrices filled row-major.  Stream seeds: seed ⊕ PI_STREAM_TAG for Π,
   seed ⊕ S_STREAM_TAG for S.
 * Π = Q·diag(sign(R_ii)) from G = QR (makes Π Haar-distributed).
+* Walsh–Hadamard option (community finding #3 names WHT for the MSE stage and an
+  independent transform for QJL, without defining the randomisation): the
+  standard randomised Hadamard transform Π_H = H_d·diag(σ)/√d, H_d the Sylvester
+  (natural-order) Hadamard matrix, σ_i = +1 if u_i < ½ else −1 with u_i the i-th
+  uniform of stream seed ⊕ WHT_STREAM_TAG.  d must be a power of two.  S stays
+  Gaussian from its own stream.
 * Codebook uses the exact coordinate law f_X, not its N(0, 1/d) limit.
 * Ties y_j = t_k go to the lower index; sign(0) = +1; a zero row stores norm 0,
   codes 0, signs +1, residual norm 0 (dequantizes to 0).
@@ -60,7 +70,8 @@ from scipy import special
 
 __all__ = [
     "PI_STREAM_TAG", "S_STREAM_TAG", "splitmix64", "uniform01", "gaussian_matrix",
-    "rotation_matrix", "qjl_matrix", "coord_density_const", "coord_density",
+    "WHT_STREAM_TAG", "ROTATIONS", "rotation_matrix", "hadamard_matrix", "hadamard_signs",
+    "hadamard_rotation", "qjl_matrix", "coord_density_const", "coord_density",
     "coord_cdf", "cell_mass", "cell_first_moment", "lloyd_max_codebook",
     "mse_distortion_theory", "Params", "make_params", "quantize", "qjl_of_residual", "pack_codes",
     "unpack_codes", "pack_signs", "unpack_signs", "dequantize", "decode_attention",
@@ -72,6 +83,8 @@ GOLDEN64 = 0x9E3779B97F4A7C15
 # Independent streams for the rotation and the QJL matrix (arbitrary distinct tags).
 PI_STREAM_TAG = 0x5049524F54415445  # "PIROTATE"
 S_STREAM_TAG = 0x514A4C534B455443  # "QJLSKETC"
+WHT_STREAM_TAG = 0x5748545349474E53  # "WHTSIGNS": the ±1 diagonal of the Hadamard rotation
+ROTATIONS = ("qr", "hadamard")
 
 
 # ----------------------------------------------------------------------------
@@ -127,6 +140,26 @@ def rotation_matrix(d: int, seed: int) -> np.ndarray:
     s = np.sign(np.diag(R))
     s[s == 0] = 1.0
     return Q * s[None, :]
+
+
+def hadamard_matrix(d: int) -> np.ndarray:
+    """Sylvester Hadamard matrix H_d (natural order): H_1 = [1], H_2m = [[H, H], [H, −H]]."""
+    assert d >= 1 and d & (d - 1) == 0, "d must be a power of two"
+    H = np.ones((1, 1))
+    while H.shape[0] < d:
+        H = np.block([[H, H], [H, -H]])
+    return H
+
+
+def hadamard_signs(d: int, seed: int) -> np.ndarray:
+    """Random ±1 diagonal σ of the Hadamard rotation: σ_i = +1 iff u_i < ½."""
+    u = uniform01(seed ^ WHT_STREAM_TAG, d)
+    return np.where(u < 0.5, 1.0, -1.0)
+
+
+def hadamard_rotation(d: int, seed: int) -> np.ndarray:
+    """Randomised Walsh–Hadamard rotation Π_H = H_d·diag(σ)/√d (orthogonal)."""
+    return hadamard_matrix(d) * hadamard_signs(d, seed)[None, :] / math.sqrt(d)
 
 
 def qjl_matrix(d: int, seed: int) -> np.ndarray:
@@ -215,8 +248,9 @@ def mse_distortion_theory(d: int, levels: int) -> float:
 class Params:
     """Everything a TurboQuant quantizer is determined by: (d, b, variant, seed)."""
 
-    def __init__(self, d, bits, variant, seed, Pi, S, centroids, bounds):
+    def __init__(self, d, bits, variant, seed, Pi, S, centroids, bounds, rotation="qr"):
         self.d = d
+        self.rotation = rotation  # "qr" (Шаг 1) or "hadamard"
         self.bits = bits
         self.variant = variant  # "mse" or "prod"
         self.seed = seed
@@ -232,16 +266,16 @@ class Params:
 _CODEBOOK_CACHE: dict = {}
 
 
-def make_params(d: int, bits: int, variant: str, seed: int) -> Params:
-    assert variant in ("mse", "prod")
+def make_params(d: int, bits: int, variant: str, seed: int, rotation: str = "qr") -> Params:
+    assert variant in ("mse", "prod") and rotation in ROTATIONS
     b_mse = bits if variant == "mse" else bits - 1
     key = (d, 1 << b_mse)
     if key not in _CODEBOOK_CACHE:
         _CODEBOOK_CACHE[key] = lloyd_max_codebook(d, 1 << b_mse)
     c, t = _CODEBOOK_CACHE[key]
-    Pi = rotation_matrix(d, seed)
+    Pi = rotation_matrix(d, seed) if rotation == "qr" else hadamard_rotation(d, seed)
     S = qjl_matrix(d, seed) if variant == "prod" else None
-    return Params(d, bits, variant, seed, Pi, S, c.copy(), t.copy())
+    return Params(d, bits, variant, seed, Pi, S, c.copy(), t.copy(), rotation)
 
 
 def code_bytes_per_row(p: Params) -> int:

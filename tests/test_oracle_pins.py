@@ -143,6 +143,105 @@ def test_lloyd_fixed_point_by_quadrature(d, L):
     assert np.max(np.abs(c + c[::-1])) < 1e-13
 
 
+# ---------------------------------------------------------------- Walsh–Hadamard rotation
+# Community finding #3 on the page: a Walsh–Hadamard transform for the MSE stage,
+# with an independent random transform for QJL.
+@pytest.mark.parametrize("d", [1, 2, 4, 8, 32, 64, 128, 256])
+def test_hadamard_matrix_is_sylvester(d):
+    from scipy.linalg import hadamard
+    H = O.hadamard_matrix(d)
+    assert np.array_equal(H, hadamard(d).astype(np.float64))
+    assert np.array_equal(H @ H.T, d * np.eye(d))
+
+
+def _fwht(v):
+    # in-place butterflies of the fast Walsh–Hadamard transform (natural order)
+    v = v.copy()
+    n, h = v.shape[-1], 1
+    while h < n:
+        for i in range(0, n, 2 * h):
+            a = v[..., i:i + h].copy()
+            b = v[..., i + h:i + 2 * h].copy()
+            v[..., i:i + h] = a + b
+            v[..., i + h:i + 2 * h] = a - b
+        h *= 2
+    return v
+
+
+@pytest.mark.parametrize("d", [4, 32, 128, 256])
+def test_hadamard_rotation_is_the_fast_transform(d):
+    Pi = O.hadamard_rotation(d, seed=17)
+    assert np.max(np.abs(Pi.T @ Pi - np.eye(d))) <= 1e-13
+    assert np.max(np.abs(np.abs(Pi) - 1 / math.sqrt(d))) <= 1e-15
+    sig = O.hadamard_signs(d, seed=17)
+    assert set(np.unique(sig)) <= {-1.0, 1.0}
+    X = np.random.default_rng(d).standard_normal((5, d))
+    p = O.make_params(d, 2, "mse", seed=17, rotation="hadamard")
+    assert p.rotation == "hadamard"
+    y = O.quantize(p, X)["y_unit"] * np.linalg.norm(X, axis=1, keepdims=True)
+    assert np.max(np.abs(y - _fwht(X * sig) / math.sqrt(d))) <= 1e-12
+
+
+def test_hadamard_signs_balanced_and_independent():
+    s = np.concatenate([O.hadamard_signs(256, seed=k) for k in range(64)])
+    assert abs(s.mean()) < 4.0 / math.sqrt(s.size)
+    # its own stream: not a function of Π's or S's draws
+    assert len({O.WHT_STREAM_TAG, O.PI_STREAM_TAG, O.S_STREAM_TAG}) == 3
+    a = O.hadamard_signs(4096, seed=7)
+    b = np.sign(O.gaussian_matrix(7 ^ O.S_STREAM_TAG, 64, 64).ravel())
+    assert abs(np.corrcoef(a, b)[0, 1]) < 4.0 / 64
+
+
+@pytest.mark.parametrize("d", [32, 128])
+@pytest.mark.parametrize("b", [1, 2, 3, 4])
+def test_hadamard_one_hot_rows_closed_form(d, b):
+    # Every coordinate of Π_H·e_k is ±1/√d, so each is quantized to the centroid c*
+    # nearest 1/√d (with the same sign) and x̃ = ‖x‖·√d·c*·e_k: the distortion is
+    # exactly (1 − √d·c*)²; at b = 1, c* = c₁ = Γ(d/2)/(√π Γ((d+1)/2)).
+    p = O.make_params(d, b, "mse", seed=5, rotation="hadamard")
+    c = p.centroids
+    cstar = c[np.argmin(np.abs(c - 1 / math.sqrt(d)))]
+    if b == 1:
+        c1 = math.exp(math.lgamma(d / 2) - 0.5 * math.log(math.pi) - math.lgamma((d + 1) / 2))
+        assert abs(cstar - c1) < 1e-12
+    for k in (0, 1, d // 2 + 3, d - 1):
+        x = np.zeros((1, d))
+        x[0, k] = 3.0
+        q = O.quantize(p, x)
+        xt = O.dequantize(p, q["idx"], q["norm"])
+        expect = np.zeros(d)
+        expect[k] = 3.0 * math.sqrt(d) * cstar
+        assert np.max(np.abs(xt[0] - expect)) < 1e-12
+        assert abs(float(np.sum((x - xt) ** 2)) / 9.0 - (1 - math.sqrt(d) * cstar) ** 2) < 1e-12
+
+
+@pytest.mark.parametrize("b", [1, 2, 3, 4])
+def test_hadamard_dmse_identity_on_gaussian_rows(b):
+    # Π_H is orthogonal, so Π_H·x/‖x‖ is uniform on the sphere for Gaussian x and
+    # the identity D_mse = d·C(f_X, b) holds exactly in expectation.
+    d = 128
+    p = O.make_params(d, b, "mse", seed=22, rotation="hadamard")
+    X = synthetic.unit_rows(1 << 14, d, seed=300 + b)
+    q = O.quantize(p, X)
+    err = np.sum((X - O.dequantize(p, q["idx"], q["norm"])) ** 2, axis=1)
+    theory = O.mse_distortion_theory(d, 1 << b)
+    assert abs(err.mean() - theory) < 4 * err.std() / math.sqrt(err.size) + 1e-6
+
+
+def test_hadamard_prod_unbiased():
+    # QJL's unbiasedness comes from S alone, whatever the orthogonal Π.
+    d, M = 32, 3000
+    x = synthetic.unit_rows(1, d, seed=12)
+    y = np.random.default_rng(13).standard_normal((1, d))
+    vals = []
+    for s in range(M):
+        p = O.make_params(d, 2, "prod", seed=70000 + s, rotation="hadamard")
+        q = O.quantize(p, x)
+        vals.append(float((O.dequantize(p, q["idx"], q["norm"], q["z"], q["rnorm"]) @ y.T)[0, 0]))
+    vals = np.array(vals)
+    assert abs(vals.mean() - (x @ y.T).item()) < 4 * vals.std() / math.sqrt(M)
+
+
 # ---------------------------------------------------------------- Theorem 1 (mse)
 @pytest.mark.parametrize("b", [1, 2, 3, 4])
 def test_dmse_identity_and_page_table(b):
