@@ -331,8 +331,9 @@ def oracle_sample_run(spec, K, V, q, lens, rows: int, tokens: int, params):
 
 def oracle_params(spec):
     import oracle as O
-    return (O.make_params(spec["d"], spec["k_bits"], spec["k_variant"], 10),
-            O.make_params(spec["d"], spec["v_bits"], spec["v_variant"], 11))
+    rot = spec.get("rotation", "qr")
+    return (O.make_params(spec["d"], spec["k_bits"], spec["k_variant"], 10, rot),
+            O.make_params(spec["d"], spec["v_bits"], spec["v_variant"], 11, rot))
 
 
 def cpu_baseline(spec, K, V, q, lens, seconds: float = 12.0) -> dict:
@@ -396,7 +397,7 @@ METRIC = "compressed-KV decode attention GB/s and quantize Mrows/s, % of B300 HB
 def config_block(spec) -> dict:
     return {"workload": spec["name"], "batch": spec["B"], "kv_heads": spec["Hkv"], "q_heads": spec["Hq"],
             "tokens": spec["T"], "d": spec["d"], "k": f"{spec['k_variant']} b={spec['k_bits']}",
-            "v": f"{spec['v_variant']} b={spec['v_bits']}",
+            "v": f"{spec['v_variant']} b={spec['v_bits']}", "rotation": spec.get("rotation", "qr"),
             "step": "tq_quantize(K) + tq_quantize(V) + tq_decode_attention over the packed cache",
             "l2": f"flushed by a {L2_FLUSH_BYTES >> 20} MiB write before every timed step",
             "inputs": "resident in HBM (value); pinned host buffers (e2e)"}
@@ -413,8 +414,9 @@ def run_ours(args, spec):
     K, V, q, lens = make_inputs(spec)
     d, B, Hq, Hkv, T = spec["d"], spec["B"], spec["Hq"], spec["Hkv"], spec["T"]
     tm = traffic_model(spec, lens.tolist())
-    kq = tq.Quantizer(d, spec["k_bits"], spec["k_variant"], seed=10)
-    vq = tq.Quantizer(d, spec["v_bits"], spec["v_variant"], seed=11)
+    rot = spec.get("rotation", "qr")
+    kq = tq.Quantizer(d, spec["k_bits"], spec["k_variant"], seed=10, rotation=rot)
+    vq = tq.Quantizer(d, spec["v_bits"], spec["v_variant"], seed=11, rotation=rot)
     Kd, Vd, qd, ld = K.to(dev).reshape(-1, d), V.to(dev).reshape(-1, d), q.to(dev), lens.to(dev)
     kc, vc = kq.empty_planes(tm["n_rows"]), vq.empty_planes(tm["n_rows"])
     ws = torch.empty(tq.decode_workspace_bytes(kq, vq, B, Hq, Hkv, T), dtype=torch.uint8, device=dev)
@@ -527,11 +529,13 @@ def run_ours(args, spec):
 
     def tensor_info(spec_bits, variant, rows, ms_list):
         """Tensor-pipe view of a quantize call: algorithmic flops (2d² per row for
-        the rotation, 4d² with the QJL sketch) and the flops the kernel executes
-        (bf16 hi/lo and f16 hi/lo passes: 2 for mse, 2 + 3 for prod)."""
+        the rotation, or d·log2(d) butterfly additions for the Hadamard one, plus
+        2d² for the QJL sketch) and the flops the kernel executes (bf16 hi/lo passes
+        for Π, one ±1 pass for the Hadamard matrix, 3 f16 passes for the sketch)."""
         ms = statistics.mean(ms_list)
-        alg = (4 if variant == "prod" else 2) * d * d * rows
-        exe = (5 if variant == "prod" else 2) * 2 * d * d * rows
+        had = rot == "hadamard"
+        alg = ((d * int(math.log2(d))) if had else 2 * d * d) * rows + (2 * d * d * rows if variant == "prod" else 0)
+        exe = ((1 if had else 2) + (3 if variant == "prod" else 0)) * 2 * d * d * rows
         peak = peaks.get("bf16_tflops")
         out = {"algorithmic_tflops": alg / (ms / 1e3) / 1e12, "executed_tflops": exe / (ms / 1e3) / 1e12,
                "peak_tflops": peak}
@@ -540,11 +544,12 @@ def run_ours(args, spec):
             out["frac_executed"] = out["executed_tflops"] / peak
         return out
 
+    wht = "_wht" if rot == "hadamard" else ""
     rl = {
         "quantize_k": hbm_roofline(f"tq_quantize ({spec['k_variant']} b={spec['k_bits']})", qk, tm["quant_k"],
-                                   f"quantize_{spec['k_variant']}_b{spec['k_bits']}_d{d}", qsrc, tm["n_rows"]),
+                                   f"quantize_{spec['k_variant']}_b{spec['k_bits']}_d{d}{wht}", qsrc, tm["n_rows"]),
         "quantize_v": hbm_roofline(f"tq_quantize ({spec['v_variant']} b={spec['v_bits']})", qv, tm["quant_v"],
-                                   f"quantize_{spec['v_variant']}_b{spec['v_bits']}_d{d}", qsrc, tm["n_rows"]),
+                                   f"quantize_{spec['v_variant']}_b{spec['v_bits']}_d{d}{wht}", qsrc, tm["n_rows"]),
         "decode": hbm_roofline("tq_decode_attention", dc, tm["decode"],
                                f"decode_{spec['k_variant']}_b{spec['k_bits']}_{spec['v_variant']}_b{spec['v_bits']}_d{d}",
                                dsrc, tm["ctx_rows"]),
@@ -651,6 +656,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama70b_layer_kv_quant",
                     choices=["llama70b_layer_kv_quant", "decode_131k", "batched_decode_32k"])
+    ap.add_argument("--rotation", choices=["qr", "hadamard"], default="qr",
+                    help="rotation of both quantizers (hadamard: randomised Walsh-Hadamard)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--warm-seconds", type=float, default=WARM_SECONDS,
@@ -659,6 +666,7 @@ def main(argv=None):
     if args.warmup < 3:
         args.warmup = 3
     spec = workload_spec(args.workload)
+    spec["rotation"] = args.rotation
     if args.impl == "reference":
         return run_reference(args, spec)
     return run_ours(args, spec)

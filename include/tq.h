@@ -61,6 +61,7 @@ extern "C" {
 
 enum { TQ_MSE = 0, TQ_PROD = 1 };
 enum { TQ_BF16 = 0, TQ_F32 = 1 };
+enum { TQ_ROT_QR = 0, TQ_ROT_HADAMARD = 1 };
 
 typedef struct tq_ctx* tq_handle;
 
@@ -92,6 +93,20 @@ typedef struct {
  */
 int tq_init(int d, int bits, int variant, uint64_t seed, tq_handle* out);
 
+/*
+ * tq_init_ex — tq_init with a choice of rotation.  rotation = TQ_ROT_QR is
+ * tq_init.  rotation = TQ_ROT_HADAMARD replaces «Шаг 1»'s Π by the randomised
+ * Walsh–Hadamard rotation the page's community findings (#3) recommend for the
+ * MSE stage, with QJL on its own independent S as before:
+ *   Π = H_d·diag(σ)/√d,  (H_d)_ji = (−1)^popcount(j AND i)  (natural-order
+ *   Sylvester matrix),  σ_i = +1 if the i-th uniform (z>>11)·2⁻⁵³ of the
+ *   SplitMix64 stream seed ⊕ 0x5748545349474E53 is below ½, else −1.
+ * The Hadamard rotation needs d to be a power of two (32, 64, 128, 256), else
+ * TQ_EUNSUPPORTED; any other rotation value is TQ_EINVAL.  The packed planes,
+ * codebook, S and every other call are unchanged.
+ */
+int tq_init_ex(int d, int bits, int variant, int rotation, uint64_t seed, tq_handle* out);
+
 /* Free everything tq_init allocated.  NULL is accepted. */
 int tq_destroy(tq_handle h);
 
@@ -106,6 +121,10 @@ int tq_row_bytes(tq_handle h, int* code_bytes, int* sign_bytes);
  */
 int tq_build_params_host(int d, int bits, int variant, uint64_t seed,
                          double* Pi, double* S, double* centroids, double* bounds);
+
+/* tq_build_params_host with a rotation argument (as in tq_init_ex). */
+int tq_build_params_host_ex(int d, int bits, int variant, int rotation, uint64_t seed,
+                            double* Pi, double* S, double* centroids, double* bounds);
 
 /* Host copies of a handle's float64 parameters (same layout as above). */
 int tq_get_params(tq_handle h, double* Pi, double* S, double* centroids, double* bounds);

@@ -21,6 +21,7 @@ __all__ = ["Quantizer", "decode_attention", "decode_workspace_bytes", "build_par
            "library_path"]
 
 _VARIANTS = {"mse": TQ_MSE, "prod": TQ_PROD}
+_ROTATIONS = {"qr": _lib.TQ_ROT_QR, "hadamard": _lib.TQ_ROT_HADAMARD}
 _DTYPES = {torch.bfloat16: TQ_BF16, torch.float32: TQ_F32}
 
 
@@ -38,8 +39,8 @@ def _stream(stream) -> int | None:
     return stream.cuda_stream
 
 
-def build_params_host(d: int, bits: int, variant: str = "mse", seed: int = 0) -> dict:
-    """Float64 Π, S, centroids and boundaries exactly as tq_init builds them (host only, no GPU)."""
+def build_params_host(d: int, bits: int, variant: str = "mse", seed: int = 0, rotation: str = "qr") -> dict:
+    """Float64 Π, S, centroids and boundaries exactly as tq_init_ex builds them (host only, no GPU)."""
     L = _lib.lib()
     b_m = bits if variant == "mse" else bits - 1
     Pi = np.zeros(d * d)
@@ -47,8 +48,8 @@ def build_params_host(d: int, bits: int, variant: str = "mse", seed: int = 0) ->
     c = np.zeros(1 << b_m)
     t = np.zeros(max((1 << b_m) - 1, 1))
     dp = ctypes.POINTER(ctypes.c_double)
-    check(L.tq_build_params_host(d, bits, _VARIANTS[variant], seed, Pi.ctypes.data_as(dp),
-                                 S.ctypes.data_as(dp), c.ctypes.data_as(dp), t.ctypes.data_as(dp)))
+    check(L.tq_build_params_host_ex(d, bits, _VARIANTS[variant], _ROTATIONS[rotation], seed, Pi.ctypes.data_as(dp),
+                                    S.ctypes.data_as(dp), c.ctypes.data_as(dp), t.ctypes.data_as(dp)))
     out = {"Pi": Pi.reshape(d, d), "centroids": c, "bounds": t[: (1 << b_m) - 1]}
     if variant == "prod":
         out["S"] = S.reshape(d, d)
@@ -56,14 +57,18 @@ def build_params_host(d: int, bits: int, variant: str = "mse", seed: int = 0) ->
 
 
 class Quantizer:
-    """One TurboQuant quantizer (tq_init handle) on the current CUDA device."""
+    """One TurboQuant quantizer (tq_init_ex handle) on the current CUDA device.
 
-    def __init__(self, d: int, bits: int, variant: str = "mse", seed: int = 0):
+    rotation: "qr" (Π from the QR factor of a Gaussian matrix) or "hadamard"
+    (randomised Walsh–Hadamard, d a power of two).
+    """
+
+    def __init__(self, d: int, bits: int, variant: str = "mse", seed: int = 0, rotation: str = "qr"):
         L = _lib.lib()
         h = ctypes.c_void_p()
-        check(L.tq_init(d, bits, _VARIANTS[variant], seed, ctypes.byref(h)))
+        check(L.tq_init_ex(d, bits, _VARIANTS[variant], _ROTATIONS[rotation], seed, ctypes.byref(h)))
         self._h = h
-        self.d, self.bits, self.variant, self.seed = d, bits, variant, seed
+        self.d, self.bits, self.variant, self.seed, self.rotation = d, bits, variant, seed, rotation
         self.b_mse = bits if variant == "mse" else bits - 1
         cb, sb = ctypes.c_int(), ctypes.c_int()
         check(L.tq_row_bytes(h, ctypes.byref(cb), ctypes.byref(sb)))

@@ -15,12 +15,14 @@ TQ_ENOMEM = -5
 TQ_EWORKSPACE = -6
 TQ_MSE, TQ_PROD = 0, 1
 TQ_BF16, TQ_F32 = 0, 1
+TQ_ROT_QR, TQ_ROT_HADAMARD = 0, 1
 
 ERROR_NAMES = {TQ_EINVAL: "TQ_EINVAL", TQ_EUNSUPPORTED: "TQ_EUNSUPPORTED", TQ_EALIGN: "TQ_EALIGN",
                TQ_ECUDA: "TQ_ECUDA", TQ_ENOMEM: "TQ_ENOMEM", TQ_EWORKSPACE: "TQ_EWORKSPACE"}
 
 # Every symbol include/tq.h declares, for the export check.
-EXPORTED = ["tq_init", "tq_destroy", "tq_row_bytes", "tq_build_params_host", "tq_get_params",
+EXPORTED = ["tq_init", "tq_init_ex", "tq_destroy", "tq_row_bytes", "tq_build_params_host",
+            "tq_build_params_host_ex", "tq_get_params",
             "tq_quantize", "tq_dequantize", "tq_decode_workspace_bytes", "tq_decode_attention",
             "tq_decode_attention_noalloc", "tq_device_status", "tq_check_wait_timeout", "tq_last_error"]
 NOALLOC_WORKSPACE_BYTES = 4 << 20
@@ -51,9 +53,11 @@ def lib() -> ctypes.CDLL:
     vp, i32, i64, u64, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_uint64, ctypes.c_size_t
     dp = ctypes.POINTER(ctypes.c_double)
     L.tq_init.argtypes = [i32, i32, i32, u64, ctypes.POINTER(vp)]
+    L.tq_init_ex.argtypes = [i32, i32, i32, i32, u64, ctypes.POINTER(vp)]
     L.tq_destroy.argtypes = [vp]
     L.tq_row_bytes.argtypes = [vp, ctypes.POINTER(i32), ctypes.POINTER(i32)]
     L.tq_build_params_host.argtypes = [i32, i32, i32, u64, dp, dp, dp, dp]
+    L.tq_build_params_host_ex.argtypes = [i32, i32, i32, i32, u64, dp, dp, dp, dp]
     L.tq_get_params.argtypes = [vp, dp, dp, dp, dp]
     L.tq_quantize.argtypes = [vp, vp, i32, i64, i64, Planes, vp]
     L.tq_dequantize.argtypes = [vp, Planes, i64, vp, i32, vp]

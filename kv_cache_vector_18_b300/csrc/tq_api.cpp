@@ -102,7 +102,7 @@ void free_device(tq_ctx* h) {
         if (*p) cudaFree(*p);
         *p = nullptr;
     }
-    uint16_t** hl[] = {&h->dp.Pi_hi, &h->dp.Pi_lo, &h->dp.S_hi, &h->dp.S_lo, &h->dp.T_hi, &h->dp.T_lo};
+    uint16_t** hl[] = {&h->dp.Pi_hi, &h->dp.Pi_lo, &h->dp.S_hi, &h->dp.S_lo, &h->dp.T_hi, &h->dp.T_lo, &h->dp.Pm};
     for (uint16_t** p : hl) {
         if (*p) cudaFree(*p);
         *p = nullptr;
@@ -152,6 +152,16 @@ int upload_tensor_core_params(tq_ctx* h) {
     if (d % 64 == 0) {
         rc = encode_tmap_bf16_2d(&h->dp.tm_pi_hi, h->dp.Pi_hi, d, d, (uint64_t)d * 2, 64, d);
         if (rc == TQ_OK) rc = encode_tmap_bf16_2d(&h->dp.tm_pi_lo, h->dp.Pi_lo, d, d, (uint64_t)d * 2, 64, d);
+    }
+    if (rc == TQ_OK && h->hp.rotation == TQ_ROT_HADAMARD) {
+        // √d·Π has entries ±1: one exact bf16 operand, one MMA pass
+        std::vector<uint16_t> pm((size_t)d * d);
+        const double sd = sqrt((double)d);
+        for (size_t k = 0; k < pm.size(); ++k) pm[k] = h->hp.Pi[k] * sd > 0.0 ? 0x3F80u : 0xBF80u;
+        rc = upload_u16(pm, &h->dp.Pm);
+        if (rc == TQ_OK && d % 64 == 0) rc = encode_tmap_bf16_2d(&h->dp.tm_pm, h->dp.Pm, d, d, (uint64_t)d * 2, 64, d);
+        h->rot_passes = 1;
+        h->rot_norm_scale = (float)(1.0 / sd);
     }
     if (rc == TQ_OK && h->hp.variant == TQ_PROD) {
         // T = S·Πᵀ (T_ij = Σ_k S_ik Π_jk) as f16 hi + lo, row-major [i][j]: the operand of
@@ -294,8 +304,13 @@ const char* tq_last_error(void) { return g_err; }
 
 int tq_build_params_host(int d, int bits, int variant, uint64_t seed, double* Pi, double* S,
                          double* centroids, double* bounds) {
+    return tq_build_params_host_ex(d, bits, variant, TQ_ROT_QR, seed, Pi, S, centroids, bounds);
+}
+
+int tq_build_params_host_ex(int d, int bits, int variant, int rotation, uint64_t seed, double* Pi, double* S,
+                            double* centroids, double* bounds) {
     HostParams hp;
-    int rc = build_host_params(d, bits, variant, seed, &hp);
+    int rc = build_host_params(d, bits, variant, rotation, seed, &hp);
     if (rc != TQ_OK) return rc;
     if (Pi) memcpy(Pi, hp.Pi.data(), hp.Pi.size() * sizeof(double));
     if (S && variant == TQ_PROD) memcpy(S, hp.S.data(), hp.S.size() * sizeof(double));
@@ -306,11 +321,15 @@ int tq_build_params_host(int d, int bits, int variant, uint64_t seed, double* Pi
 }
 
 int tq_init(int d, int bits, int variant, uint64_t seed, tq_handle* out) {
+    return tq_init_ex(d, bits, variant, TQ_ROT_QR, seed, out);
+}
+
+int tq_init_ex(int d, int bits, int variant, int rotation, uint64_t seed, tq_handle* out) {
     if (out == nullptr) return fail(TQ_EINVAL, "out is NULL");
     *out = nullptr;
     tq_ctx* h = new (std::nothrow) tq_ctx();
     if (!h) return fail(TQ_ENOMEM, "host allocation failed");
-    int rc = build_host_params(d, bits, variant, seed, &h->hp);
+    int rc = build_host_params(d, bits, variant, rotation, seed, &h->hp);
     if (rc != TQ_OK) {
         delete h;
         return rc;

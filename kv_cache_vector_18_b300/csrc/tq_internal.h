@@ -29,6 +29,7 @@ struct Codebook {
 // Float64 parameters of one quantizer, as built on the host.
 struct HostParams {
     int d = 0, bits = 0, variant = 0, b_mse = 0, levels = 0;
+    int rotation = 0;               // TQ_ROT_QR or TQ_ROT_HADAMARD
     uint64_t seed = 0;
     std::vector<double> Pi;         // [d*d] row-major, y = Pi x
     std::vector<double> S;          // [d*d] row-major (prod)
@@ -50,6 +51,10 @@ struct DeviceParams {
     uint16_t* S_lo = nullptr;
     CUtensorMap tm_pi_hi;   // TMA maps over Pi_hi / Pi_lo, box {64, d}, 128-byte swizzle
     CUtensorMap tm_pi_lo;
+    // Hadamard rotation: √d·Π = H·diag(σ) has entries ±1, exact in bf16, so the
+    // quantize contraction takes it in one pass and scales the norm by 1/√d.
+    uint16_t* Pm = nullptr;
+    CUtensorMap tm_pm;
     // prod: T = S·Πᵀ = T_hi + T_lo as two f16 matrices, row-major [i][j], and TMA maps
     uint16_t* T_hi = nullptr;
     uint16_t* T_lo = nullptr;
@@ -69,6 +74,10 @@ struct tq_ctx {
     int code_bytes = 0;
     int sign_bytes = 0;
     float gamma = 0.f;  // √(π/2)/d
+    // rotation operand of the tensor-core quantize kernels: 2 passes (Π_hi, Π_lo) with
+    // norm scale 1, or 1 pass over the ±1 Hadamard matrix with norm scale 1/√d
+    int rot_passes = 2;
+    float rot_norm_scale = 1.f;
 };
 
 namespace tq {
@@ -93,7 +102,7 @@ inline int ensure_smem_attr(std::atomic<uint64_t>& done, const void* fn, int byt
 }
 
 // Host parameter construction (tq_params.cpp).
-int build_host_params(int d, int bits, int variant, uint64_t seed, HostParams* out);
+int build_host_params(int d, int bits, int variant, int rotation, uint64_t seed, HostParams* out);
 
 // 2-D bf16 TMA map: `inner` contiguous elements per row, `outer` rows `row_stride_bytes` apart,
 // box {box_inner, box_outer}, 128-byte swizzle, out-of-range elements read as zero.

@@ -8,6 +8,11 @@
 //   f_X(x) = Γ(d/2)/(√π Γ((d−1)/2))·(1−x²)^((d−3)/2) on [−1, 1] (the Lemma),
 //   alternating "boundaries = midpoints" and "centroids = conditional means".
 //
+// Walsh–Hadamard option (community finding #3 of the page: WHT for the MSE stage,
+//   an independent transform for QJL): Π = H_d·diag(σ)/√d with H_d the natural-
+//   order Hadamard matrix, (H_d)_ji = (−1)^popcount(j & i), and σ_i = +1 iff the
+//   i-th uniform of its own stream is below ½.  S is unchanged.
+//
 // Numerics here are this library's own: Householder QR, and cell integrals by
 // composite Gauss–Legendre quadrature of f_X and x·f_X.
 #include <math.h>
@@ -24,6 +29,7 @@ namespace {
 constexpr uint64_t kGolden = 0x9E3779B97F4A7C15ull;
 constexpr uint64_t kPiStreamTag = 0x5049524F54415445ull;  // "PIROTATE"
 constexpr uint64_t kSStreamTag = 0x514A4C534B455443ull;   // "QJLSKETC"
+constexpr uint64_t kWhtStreamTag = 0x5748545349474E53ull; // "WHTSIGNS"
 
 // SplitMix64 (Steele, Lea & Flood 2014), counter form: output i mixes seed + (i+1)·φ.
 inline uint64_t splitmix64_at(uint64_t seed, uint64_t i) {
@@ -47,6 +53,16 @@ void gaussian_fill(uint64_t seed, size_t n, double* out) {
         double a = 2.0 * M_PI * u2;
         out[2 * k] = r * cos(a);
         if (2 * k + 1 < n) out[2 * k + 1] = r * sin(a);
+    }
+}
+
+// Π_ji = (−1)^popcount(j & i)·σ_i/√d.
+void hadamard_rotation(int d, uint64_t seed, std::vector<double>* Pi) {
+    Pi->assign((size_t)d * d, 0.0);
+    const double s = 1.0 / sqrt((double)d);
+    for (int i = 0; i < d; ++i) {
+        const double sig = uniform_at(seed ^ kWhtStreamTag, (uint64_t)i) < 0.5 ? s : -s;
+        for (int j = 0; j < d; ++j) (*Pi)[(size_t)j * d + i] = (__builtin_popcount((unsigned)(j & i)) & 1) ? -sig : sig;
     }
 }
 
@@ -194,21 +210,29 @@ void cached_codebook(int d, int levels, std::vector<double>* c, std::vector<doub
 
 }  // namespace
 
-int build_host_params(int d, int bits, int variant, uint64_t seed, HostParams* out) {
+int build_host_params(int d, int bits, int variant, int rotation, uint64_t seed, HostParams* out) {
     if (d < kMinD || d > kMaxD || d % 32 != 0)
         return fail(TQ_EUNSUPPORTED, "d=%d unsupported (need a multiple of 32 in [32, 256])", d);
     if (variant != TQ_MSE && variant != TQ_PROD) return fail(TQ_EINVAL, "variant=%d invalid", variant);
+    if (rotation != TQ_ROT_QR && rotation != TQ_ROT_HADAMARD) return fail(TQ_EINVAL, "rotation=%d invalid", rotation);
+    if (rotation == TQ_ROT_HADAMARD && (d & (d - 1)) != 0)
+        return fail(TQ_EUNSUPPORTED, "the Hadamard rotation needs d a power of two (d=%d)", d);
     if (bits < 1 || bits > 4) return fail(TQ_EUNSUPPORTED, "bits=%d unsupported (1..4)", bits);
     HostParams hp;
     hp.d = d;
     hp.bits = bits;
     hp.variant = variant;
     hp.seed = seed;
+    hp.rotation = rotation;
     hp.b_mse = variant == TQ_MSE ? bits : bits - 1;
     hp.levels = 1 << hp.b_mse;
-    std::vector<double> G((size_t)d * d);
-    gaussian_fill(seed ^ kPiStreamTag, G.size(), G.data());
-    rotation_from_gaussian(d, G, &hp.Pi);
+    if (rotation == TQ_ROT_QR) {
+        std::vector<double> G((size_t)d * d);
+        gaussian_fill(seed ^ kPiStreamTag, G.size(), G.data());
+        rotation_from_gaussian(d, G, &hp.Pi);
+    } else {
+        hadamard_rotation(d, seed, &hp.Pi);
+    }
     if (variant == TQ_PROD) {
         hp.S.resize((size_t)d * d);
         gaussian_fill(seed ^ kSStreamTag, hp.S.size(), hp.S.data());

@@ -3,7 +3,10 @@
 //
 // Per 128-row tile: Y = X·Πᵀ as two bf16 MMAs into one fp32 TMEM accumulator,
 // Π = Π_hi + Π_lo (Π_hi = bf16(Π), Π_lo = bf16(Π − Π_hi)), so the rotation is
-// accurate to ~2⁻¹⁷ relative while the inputs stay exact bf16.  The epilogue
+// accurate to ~2⁻¹⁷ relative while the inputs stay exact bf16.  With the
+// Walsh–Hadamard rotation the operand is √d·Π = H·diag(σ), whose ±1 entries are
+// exact in bf16: one MMA gives √d·y exactly up to fp32 accumulation, the
+// codes depend only on y/‖y‖, and the stored norm is scaled by 1/√d.  The epilogue
 // reads the accumulator row per thread, takes ‖y‖ = ‖x‖ (Π orthogonal), counts
 // the norm-scaled Lloyd–Max boundaries below each y_j and packs b-bit codes.
 //
@@ -75,8 +78,9 @@ struct TcCfg {
 template <int D, int BM>
 __global__ void __launch_bounds__(kThreads, 1)
 quantize_mse_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_pi_hi,
-                       const __grid_constant__ CUtensorMap tm_pi_lo, int64_t n_rows, Codebook cb,
-                       uint8_t* __restrict__ codes, float* __restrict__ norm_out, int* __restrict__ status) {
+                       const __grid_constant__ CUtensorMap tm_pi_lo, int64_t n_rows, int npass, float norm_scale,
+                       Codebook cb, uint8_t* __restrict__ codes, float* __restrict__ norm_out,
+                       int* __restrict__ status) {
     using C = TcCfg<D>;
     constexpr int L = 1 << BM;
     constexpr int P = L / 2 - 1;          // positive decision boundaries
@@ -122,10 +126,10 @@ quantize_mse_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
         prefetch_tensormap(&tm_x);
         prefetch_tensormap(&tm_pi_hi);
         prefetch_tensormap(&tm_pi_lo);
-        mbar_arrive_expect_tx(pi_full, 2 * C::kPiBytes);
+        mbar_arrive_expect_tx(pi_full, npass * C::kPiBytes);
         for (int c = 0; c < C::kChunks; ++c) {
             tma_load_2d(pi_hi + c * C::kChunkBytesB, &tm_pi_hi, pi_full, c * kKC, 0);
-            tma_load_2d(pi_lo + c * C::kChunkBytesB, &tm_pi_lo, pi_full, c * kKC, 0);
+            if (npass == 2) tma_load_2d(pi_lo + c * C::kChunkBytesB, &tm_pi_lo, pi_full, c * kKC, 0);
         }
         int64_t i = 0;
         for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++i) {
@@ -160,6 +164,7 @@ quantize_mse_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
             const uint32_t a_stage = a_base + (uint32_t)(s * C::kStageBytes);
 #pragma unroll
             for (int pass = 0; pass < 2; ++pass) {
+                if (pass >= npass) break;
                 const uint32_t b_base = pass == 0 ? hi_base : lo_base;
 #pragma unroll
                 for (int c = 0; c < C::kChunks; ++c)
@@ -284,7 +289,7 @@ quantize_mse_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
             }
             tc_fence_before();
             mbar_arrive(&tempty[wg]);
-            if (live) norm_out[row] = n;
+            if (live) norm_out[row] = n * norm_scale;
         }
     }
     tc_fence_before();
@@ -304,7 +309,9 @@ int launch_tc(const tq_ctx& h, const CUtensorMap& tm_x, int64_t n_rows, const tq
     if (rc != TQ_OK) return rc;
     const int64_t ntiles = (n_rows + kTile - 1) / kTile;
     const int grid = (int)(ntiles < h.num_sms ? ntiles : h.num_sms);
-    fn<<<grid, kThreads, C::kSmemBytes, s>>>(tm_x, h.dp.tm_pi_hi, h.dp.tm_pi_lo, n_rows, h.cb, out.codes, out.norm,
+    const bool one = h.rot_passes == 1;
+    fn<<<grid, kThreads, C::kSmemBytes, s>>>(tm_x, one ? h.dp.tm_pm : h.dp.tm_pi_hi, one ? h.dp.tm_pm : h.dp.tm_pi_lo,
+                                             n_rows, h.rot_passes, h.rot_norm_scale, h.cb, out.codes, out.norm,
                                              h.dp.status);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? TQ_OK : cuda_fail(e, "tensor-core quantize launch");
@@ -395,7 +402,8 @@ template <int D, int BM>
 __global__ void __launch_bounds__(kProdThreads, 1)
 quantize_prod_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_pi_hi,
                         const __grid_constant__ CUtensorMap tm_pi_lo, const __grid_constant__ CUtensorMap tm_t_hi,
-                        const __grid_constant__ CUtensorMap tm_t_lo, int64_t n_rows, Codebook cb,
+                        const __grid_constant__ CUtensorMap tm_t_lo, int64_t n_rows, int npass, float norm_scale,
+                        Codebook cb,
                         uint8_t* __restrict__ codes, uint8_t* __restrict__ signs, float* __restrict__ norm_out,
                         float* __restrict__ rnorm_out, int* __restrict__ status) {
     using C = ProdCfg<D>;
@@ -451,10 +459,10 @@ quantize_prod_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_c
         prefetch_tensormap(&tm_pi_lo);
         prefetch_tensormap(&tm_t_hi);
         prefetch_tensormap(&tm_t_lo);
-        mbar_arrive_expect_tx(mat_full, 4 * C::kMatBytes);
+        mbar_arrive_expect_tx(mat_full, (2 + npass) * C::kMatBytes);
         for (int c = 0; c < C::kChunks; ++c) {
             tma_load_2d(pi_hi + c * C::kChunkBytesB, &tm_pi_hi, mat_full, c * kKC, 0);
-            tma_load_2d(pi_lo + c * C::kChunkBytesB, &tm_pi_lo, mat_full, c * kKC, 0);
+            if (npass == 2) tma_load_2d(pi_lo + c * C::kChunkBytesB, &tm_pi_lo, mat_full, c * kKC, 0);
             tma_load_2d(t_hi + c * C::kChunkBytesB, &tm_t_hi, mat_full, c * kKC, 0);
             tma_load_2d(t_lo + c * C::kChunkBytesB, &tm_t_lo, mat_full, c * kKC, 0);
         }
@@ -514,6 +522,7 @@ quantize_prod_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_c
             const uint32_t a_stage = a_base + (uint32_t)(s * C::kStageBytes);
 #pragma unroll
             for (int pass = 0; pass < 2; ++pass) {
+                if (pass >= npass) break;
                 const uint32_t b_base = pass == 0 ? pih : pil;
 #pragma unroll
                 for (int c = 0; c < C::kChunks; ++c)
@@ -684,7 +693,7 @@ quantize_prod_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_c
             xes[half * kTile + r_local] = esa + esb;
             pair_sync();
             if (live && half == 0) {
-                norm_out[row] = n;
+                norm_out[row] = n * norm_scale;
                 rnorm_out[row] = sqrtf(xes[r_local] + xes[kTile + r_local]);
             }
             // pass 3: sign bits of this half of S = T·e (bit i set ⇔ s_i ≥ 0)
@@ -733,9 +742,10 @@ int launch_prod_tc(const tq_ctx& h, const CUtensorMap& tm_x, int64_t n_rows, con
     if (rc != TQ_OK) return rc;
     const int64_t ntiles = (n_rows + kTile - 1) / kTile;
     const int grid = (int)(ntiles < h.num_sms ? ntiles : h.num_sms);
-    fn<<<grid, kProdThreads, C::kSmemBytes, s>>>(tm_x, h.dp.tm_pi_hi, h.dp.tm_pi_lo, h.dp.tm_t_hi, h.dp.tm_t_lo,
-                                                 n_rows, h.cb, out.codes, out.signs, out.norm, out.rnorm,
-                                                 h.dp.status);
+    const bool one = h.rot_passes == 1;
+    fn<<<grid, kProdThreads, C::kSmemBytes, s>>>(tm_x, one ? h.dp.tm_pm : h.dp.tm_pi_hi, one ? h.dp.tm_pm : h.dp.tm_pi_lo,
+                                                 h.dp.tm_t_hi, h.dp.tm_t_lo, n_rows, h.rot_passes, h.rot_norm_scale,
+                                                 h.cb, out.codes, out.signs, out.norm, out.rnorm, h.dp.status);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? TQ_OK : cuda_fail(e, "tensor-core prod quantize launch");
 }
@@ -774,8 +784,8 @@ int launch_expire_wait(const tq_ctx& h, int code, uint64_t limit_ns, cudaStream_
 
 bool quantize_tc_supported(const tq_ctx& h, int x_dtype, int64_t n_rows) {
     // TMA row coordinates are 32-bit signed: the last tile must start below 2^31.
-    const bool params = h.hp.variant == TQ_MSE ? h.dp.Pi_hi != nullptr
-                                               : (h.dp.Pi_hi != nullptr && h.dp.T_hi != nullptr && h.hp.b_mse <= 3);
+    const bool rot = h.rot_passes == 1 ? h.dp.Pm != nullptr : h.dp.Pi_hi != nullptr;
+    const bool params = h.hp.variant == TQ_MSE ? rot : (rot && h.dp.T_hi != nullptr && h.hp.b_mse <= 3);
     return x_dtype == TQ_BF16 && (h.hp.d == 64 || h.hp.d == 128) && params && h.num_sms > 0 &&
            n_rows < ((int64_t)1 << 31) - kTile;
 }

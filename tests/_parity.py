@@ -36,7 +36,7 @@ def f64(t: torch.Tensor) -> np.ndarray:
 
 
 def oracle_params(qz) -> O.Params:
-    return O.make_params(qz.d, qz.bits, qz.variant, qz.seed)
+    return O.make_params(qz.d, qz.bits, qz.variant, qz.seed, getattr(qz, "rotation", "qr"))
 
 
 def boundary_margin(p: O.Params, y_unit: np.ndarray) -> np.ndarray:

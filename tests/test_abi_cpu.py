@@ -73,3 +73,33 @@ def test_seed_changes_rotation_and_sketch():
     assert np.max(np.abs(a["Pi"] - b["Pi"])) > 0.1 and np.max(np.abs(a["S"] - b["S"])) > 0.1
     # Π and S drawn from independent streams of the same seed
     assert abs(np.corrcoef(a["Pi"].ravel(), a["S"].ravel())[0, 1]) < 0.1
+
+
+@pytest.mark.parametrize("d,b,v", [(32, 1, "mse"), (64, 2, "prod"), (128, 3, "mse"), (128, 3, "prod"),
+                                   (256, 4, "mse"), (128, 1, "prod")])
+def test_host_hadamard_params_match_oracle(d, b, v):
+    # the library builds (H_d)_ji from popcount parity, the oracle by Sylvester recursion
+    import kv_cache_vector_18_b300 as tq
+    got = tq.build_params_host(d, b, v, seed=99, rotation="hadamard")
+    p = O.make_params(d, b, v, 99, rotation="hadamard")
+    assert np.max(np.abs(got["Pi"] - p.Pi)) <= 1e-15
+    assert np.max(np.abs(got["centroids"] - p.centroids)) <= 1e-12
+    if v == "prod":
+        assert np.max(np.abs(got["S"] - p.S)) <= 1e-12
+
+
+def test_host_hadamard_rejects_bad_arguments(lib):
+    from kv_cache_vector_18_b300 import _lib
+    dp = ctypes.POINTER(ctypes.c_double)
+    buf = np.zeros(256 * 256)
+    p = buf.ctypes.data_as(dp)
+    # not a power of two
+    assert lib.tq_build_params_host_ex(96, 2, 0, _lib.TQ_ROT_HADAMARD, 0, p, p, p, p) == _lib.TQ_EUNSUPPORTED
+    assert b"power of two" in lib.tq_last_error()
+    assert lib.tq_build_params_host_ex(128, 2, 0, 2, 0, p, p, p, p) == _lib.TQ_EINVAL
+    assert lib.tq_build_params_host_ex(96, 2, 0, _lib.TQ_ROT_QR, 0, p, p, p, p) == _lib.TQ_OK
+    # the plain entry point is the QR rotation
+    a, b = np.zeros(64 * 64), np.zeros(64 * 64)
+    assert lib.tq_build_params_host(64, 2, 0, 5, a.ctypes.data_as(dp), None, None, None) == _lib.TQ_OK
+    assert lib.tq_build_params_host_ex(64, 2, 0, _lib.TQ_ROT_QR, 5, b.ctypes.data_as(dp), None, None, None) == _lib.TQ_OK
+    assert np.array_equal(a, b)
