@@ -579,6 +579,9 @@ def run_ours(args, spec):
     e2e = None
     if not args.no_e2e:
         e2e = measure_e2e(args, spec, tq, kq, vq, K, V, q, ld, kc, vc, ws, out, tm, dev, world)
+    append = measure_append(tq, kq, vq, qd, kc, vc, ld, spec, ws, out, flush, dev)
+    append["decode_us"] = statistics.mean(dc) * 1e3
+    append["append_overhead_us"] = append["us"] - append["decode_us"]
 
     line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": t_step / args.steps * 1e3, "higher_is_better": True,
@@ -590,7 +593,7 @@ def run_ours(args, spec):
             "bytes_per_step": tm["total"],
             "gpu_launches": args.steps * (2 * LAUNCHES["quantize"] + LAUNCHES["decode"]),
             "clocks": sampler.summary(), "wall_s_timed_loop": wall, "roofline": roofline,
-            "roofline_decode": roofline_decode, "roofline_per_call": rl, "e2e": e2e,
+            "roofline_decode": roofline_decode, "roofline_per_call": rl, "e2e": e2e, "append_step": append,
             "timing": graph_note + ("one CUDA graph per step holding the three library calls (captured through "
                                     "the public API); step time from CUDA events around each replay, per-call "
                                     "times from event nodes inside the graph" if step_graph is not None else
@@ -605,6 +608,42 @@ def run_ours(args, spec):
     if world > 1:
         torch.distributed.destroy_process_group()
     return 0
+
+
+def measure_append(tq, kq, vq, qd, kc, vc, ld, spec, ws, out, flush, dev, reps: int = 200) -> dict:
+    """Device time of one decode step with append (tq_decode_append_attention):
+    the new K and V rows of every slab are quantized into token seq_len − 1 (the
+    lengths are reset to len − 1 before each replay by a 4·B-byte device copy,
+    included in the time), the lengths bumped back to len, and attention runs over
+    the same tokens as the plain decode call.  Runs after the timed loop; it
+    overwrites one cached token per slab."""
+    B, Hkv, d, T = spec["B"], spec["Hkv"], spec["d"], spec["T"]
+    kn = synthetic.gaussian_cuda((B, Hkv, d), seed=20)
+    vn = synthetic.gaussian_cuda((B, Hkv, d), seed=21)
+    la0 = (ld - 1).clamp_min(0).to(torch.int32)
+    la = la0.clone()
+
+    def body():
+        la.copy_(la0)
+        tq.decode_append_attention(kq, vq, qd, kn, vn, kc, vc, la, Hkv, T, workspace=ws, out=out)
+
+    body()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        body()
+    for _ in range(5):
+        g.replay()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for e0, e1 in evs:
+        flush.zero_()
+        e0.record()
+        g.replay()
+        e1.record()
+    torch.cuda.synchronize()
+    us = [e0.elapsed_time(e1) * 1e3 for e0, e1 in evs]
+    return {"us": statistics.mean(us), "reps": reps, "library_launches": 2 + LAUNCHES["decode"],
+            "what": "length reset copy + append (K and V) + length bump + decode, one graph; L2 flushed"}
 
 
 def measure_e2e(args, spec, tq, kq, vq, K, V, q, ld, kc, vc, ws, out, tm, dev, world):

@@ -59,6 +59,10 @@ extern "C" {
 #define TQ_ENOMEM (-5)        /* device allocation failed in tq_init               */
 #define TQ_EWORKSPACE (-6)    /* workspace smaller than tq_decode_workspace_bytes  */
 
+/* Codes in a handle's device status word (tq_device_status) other than the
+ * 1..99 of an expired pipeline wait. */
+#define TQ_STATUS_APPEND_FULL 200  /* an append found its (batch, KV head) slab full */
+
 enum { TQ_MSE = 0, TQ_PROD = 1 };
 enum { TQ_BF16 = 0, TQ_F32 = 1 };
 enum { TQ_ROT_QR = 0, TQ_ROT_HADAMARD = 1 };
@@ -185,11 +189,34 @@ int tq_decode_attention(tq_handle hk, tq_handle hv, const void* q, int q_dtype,
                         void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * tq_decode_append_attention — one decode step that first appends the step's
+ * new key and value rows to the packed cache, then attends over the cache with
+ * them («Шаг 0»–«Шаг 2» and «Собственно TurboQuant» for the new rows, then the
+ * same attention as tq_decode_attention).
+ * k_new, v_new: device [B, Hkv, d] rows of kv_dtype (TQ_BF16 or TQ_F32),
+ *    contiguous.  The row of (b, h) is quantized with hk (resp. hv) into cache
+ *    row (b·Hkv + h)·T_max + seq_lens[b], the next free token of its slab.
+ * seq_lens: device int32 [B], read and written: on entry the tokens already
+ *    cached, on exit one more.  A slab whose length is already T_max (or
+ *    negative) is not written and its length is left as it was; hk's status
+ *    word then holds TQ_STATUS_APPEND_FULL (read it with tq_device_status).
+ * Attention then covers the updated lengths; q, q_dtype, kc, vc, B, Hq, Hkv,
+ * T_max, scale, out and the workspace are as in tq_decode_attention.  Launches
+ * on `stream`: one append (K and V rows together), one length update, then the
+ * decode launches.
+ */
+int tq_decode_append_attention(tq_handle hk, tq_handle hv, const void* q, int q_dtype,
+                               const void* k_new, const void* v_new, int kv_dtype,
+                               tq_planes kc, tq_planes vc, int32_t* seq_lens,
+                               int B, int Hq, int Hkv, int T_max, float scale, float* out,
+                               void* workspace, size_t ws_bytes, void* stream);
+
+/*
  * Read (and, when clear ≠ 0, reset) the handle's device status word.  Kernels
  * never spin without bound: a pipeline wait that exceeds its time limit records
- * a non-zero code there and the kernel returns early (its outputs are then
- * undefined).  0 means no such event.  Synchronises the calling thread with the
- * device.
+ * a non-zero code (1..99) there and the kernel returns early (its outputs are
+ * then undefined); an append into a full slab records TQ_STATUS_APPEND_FULL.
+ * 0 means no such event.  Synchronises the calling thread with the device.
  */
 int tq_device_status(tq_handle h, int* status, int clear);
 

@@ -17,7 +17,7 @@ import torch
 from . import _lib
 from ._lib import TQ_BF16, TQ_F32, TQ_MSE, TQ_PROD, TQError, check
 
-__all__ = ["Quantizer", "decode_attention", "decode_workspace_bytes", "build_params_host", "TQError",
+__all__ = ["Quantizer", "decode_attention", "decode_append_attention", "decode_workspace_bytes", "build_params_host", "TQError",
            "library_path"]
 
 _VARIANTS = {"mse": TQ_MSE, "prod": TQ_PROD}
@@ -180,6 +180,35 @@ def decode_attention(kq: Quantizer, vq: Quantizer, q: torch.Tensor, kcache: dict
         float(scale) if scale is not None else 0.0, _ptr(out), _ptr(scores), _ptr(workspace),
         workspace.numel(), _stream(stream)))
     return (out, scores) if return_scores else out
+
+
+def decode_append_attention(kq: Quantizer, vq: Quantizer, q: torch.Tensor, k_new: torch.Tensor,
+                            v_new: torch.Tensor, kcache: dict, vcache: dict, seq_lens: torch.Tensor, Hkv: int,
+                            T_max: int, scale: float | None = None, workspace: torch.Tensor | None = None,
+                            out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """tq_decode_append_attention.  k_new, v_new: [B, Hkv, d] (bf16/fp32, same dtype)
+    appended at token seq_lens[b] of each (b, KV head) slab; seq_lens (int32 [B] on
+    the device) is incremented in place; returns out [B, Hq, d] fp32 over the
+    updated cache."""
+    B, Hq, d = q.shape
+    for name, t in (("q", q), ("k_new", k_new), ("v_new", v_new)):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if k_new.shape != (B, Hkv, d) or v_new.shape != (B, Hkv, d) or k_new.dtype != v_new.dtype:
+        raise ValueError("k_new and v_new must both be [B, Hkv, d] of one dtype")
+    if seq_lens.dtype != torch.int32:
+        raise ValueError("seq_lens must be int32")
+    need = decode_workspace_bytes(kq, vq, B, Hq, Hkv, T_max)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty((B, Hq, d), dtype=torch.float32, device=q.device)
+    check(_lib.lib().tq_decode_append_attention(
+        kq.handle, vq.handle, _ptr(q), _DTYPES[q.dtype], _ptr(k_new), _ptr(v_new), _DTYPES[k_new.dtype],
+        Quantizer.planes_struct(kcache), Quantizer.planes_struct(vcache), _ptr(seq_lens), B, Hq, Hkv, T_max,
+        float(scale) if scale is not None else 0.0, _ptr(out), _ptr(workspace), workspace.numel(),
+        _stream(stream)))
+    return out
 
 
 def default_scale(d: int) -> float:

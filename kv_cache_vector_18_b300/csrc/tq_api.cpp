@@ -470,4 +470,33 @@ int tq_decode_attention(tq_handle hk, tq_handle hv, const void* q, int q_dtype, 
                          (cudaStream_t)stream);
 }
 
+int tq_decode_append_attention(tq_handle hk, tq_handle hv, const void* q, int q_dtype, const void* k_new,
+                               const void* v_new, int kv_dtype, tq_planes kc, tq_planes vc, int32_t* seq_lens,
+                               int B, int Hq, int Hkv, int T_max, float scale, float* out, void* workspace,
+                               size_t ws_bytes, void* stream) {
+    int rc = validate_handle(hk, "key");
+    if (rc == TQ_OK) rc = validate_handle(hv, "value");
+    if (rc != TQ_OK) return rc;
+    if (q_dtype != TQ_BF16 && q_dtype != TQ_F32) return fail(TQ_EINVAL, "q_dtype=%d invalid", q_dtype);
+    if (kv_dtype != TQ_BF16 && kv_dtype != TQ_F32) return fail(TQ_EINVAL, "kv_dtype=%d invalid", kv_dtype);
+    DecodeShape plan;
+    size_t need = 0;
+    if ((rc = decode_plan(*hk, *hv, B, Hq, Hkv, T_max, &plan, &need)) != TQ_OK) return rc;
+    if (B == 0 || Hq == 0) return TQ_OK;
+    if (T_max <= 0) return fail(TQ_EINVAL, "T_max=%d leaves no room to append", T_max);
+    if (ws_bytes < need) return fail(TQ_EWORKSPACE, "workspace of %zu bytes < required %zu", ws_bytes, need);
+    if ((rc = check_device_ptr(q, "q", true)) != TQ_OK) return rc;
+    if ((rc = check_device_ptr(k_new, "k_new", true)) != TQ_OK) return rc;
+    if ((rc = check_device_ptr(v_new, "v_new", true)) != TQ_OK) return rc;
+    if ((rc = check_device_ptr(seq_lens, "seq_lens", true)) != TQ_OK) return rc;
+    if ((rc = check_device_ptr(out, "out", true)) != TQ_OK) return rc;
+    if ((rc = check_device_ptr(workspace, "workspace", true)) != TQ_OK) return rc;
+    if ((rc = check_planes(*hk, kc, "kc")) != TQ_OK) return rc;
+    if ((rc = check_planes(*hv, vc, "vc")) != TQ_OK) return rc;
+    if (scale <= 0.f) scale = (float)(1.0 / sqrt((double)hk->hp.d));
+    const cudaStream_t s = (cudaStream_t)stream;
+    if ((rc = launch_append(*hk, *hv, k_new, v_new, kv_dtype, B, Hkv, T_max, seq_lens, kc, vc, s)) != TQ_OK) return rc;
+    return launch_decode(*hk, *hv, plan, q, q_dtype, kc, vc, seq_lens, scale, out, nullptr, workspace, s);
+}
+
 }  // extern "C"

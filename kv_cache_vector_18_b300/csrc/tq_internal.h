@@ -115,6 +115,10 @@ int encode_tmap_f16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint6
 // Kernel launchers (one per .cu file).  Arguments are validated by the caller.
 bool quantize_tc_supported(const tq_ctx& h, int x_dtype, int64_t n_rows);
 int launch_expire_wait(const tq_ctx& h, int code, uint64_t limit_ns, cudaStream_t s);
+// Decode-step append (tq_append.cu): quantize the new K and V rows [B·Hkv, d] into
+// the next free token of each (batch, KV head) slab, then bump the lengths.
+int launch_append(const tq_ctx& hk, const tq_ctx& hv, const void* k_new, const void* v_new, int x_dtype, int B,
+                  int Hkv, int T_max, int32_t* lens, const tq_planes& kc, const tq_planes& vc, cudaStream_t s);
 int launch_quantize_tc(const tq_ctx& h, const void* x, int64_t n_rows, int64_t x_row_stride,
                        const tq_planes& out, cudaStream_t s);
 int launch_quantize(const tq_ctx& h, const void* x, int x_dtype, int64_t n_rows,
