@@ -646,6 +646,57 @@ def measure_append(tq, kq, vq, qd, kc, vc, ld, spec, ws, out, flush, dev, reps: 
             "what": "length reset copy + append (K and V) + length bump + decode, one graph; L2 flushed"}
 
 
+def score_quality(tq, d: int, bits: int, variant: str, tau: float, B: int = 4, Hq: int = 64, Hkv: int = 8,
+                  T: int = 4096, seed: int = 0) -> dict:
+    """Attention quality of one key quantizer against exact attention (mse-only
+    versus prod keys at the same bits per coordinate).  Keys, values and queries
+    are N(0, 1) bf16; the softmax scale τ/√d sets how peaked attention is (logit
+    standard deviation ≈ τ).  Scores come from tq_decode_attention (scores_out);
+    exact scores, softmax and outputs from the same bf16 rows in fp32."""
+    dev = torch.device("cuda")
+    K = synthetic.gaussian_cuda((B, Hkv, T, d), seed=seed + 1)
+    V = synthetic.gaussian_cuda((B, Hkv, T, d), seed=seed + 2)
+    q = synthetic.gaussian_cuda((B, Hq, d), seed=seed + 3)
+    kq = tq.Quantizer(d, bits, variant, seed=seed + 11)
+    vq = tq.Quantizer(d, 4, "mse", seed=seed + 12)  # values only feed the unused output
+    kc = kq.quantize(K.reshape(-1, d))
+    vc = vq.quantize(V.reshape(-1, d))
+    lens = torch.full((B,), T, dtype=torch.int32, device=dev)
+    scale = tau / math.sqrt(d)
+    _, sq = tq.decode_attention(kq, vq, q, kc, vc, lens, Hkv, T, scale=scale, return_scores=True)
+    G = Hq // Hkv
+    Kf = K.float().repeat_interleave(G, dim=1)                # [B, Hq, T, d]
+    s = scale * torch.einsum("bhtd,bhd->bht", Kf, q.float())  # exact scores
+    p, pq = torch.softmax(s, -1), torch.softmax(sq, -1)
+    Vf = V.float().repeat_interleave(G, dim=1)
+    o, oq = torch.einsum("bht,bhtd->bhd", p, Vf), torch.einsum("bht,bhtd->bhd", pq, Vf)
+    top1 = (s.argmax(-1) == sq.argmax(-1)).double().mean().item()
+    t5, t5q = s.topk(5, -1).indices, sq.topk(5, -1).indices
+    rec5 = (t5.unsqueeze(-1) == t5q.unsqueeze(-2)).any(-1).double().mean().item()
+    kl = (p * (torch.log(p.clamp_min(1e-30)) - torch.log(pq.clamp_min(1e-30)))).sum(-1).mean().item()
+    out_rel = ((oq - o).norm() / o.norm()).item()
+    sd, sqd = s.double(), sq.double()
+    slope = ((sqd * sd).sum() / (sd * sd).sum()).item()
+    noise = ((sqd - slope * sd).std() / sd.std()).item()
+    return {"d": d, "bits": bits, "keys": variant, "tau": tau, "queries": B * Hq, "tokens": T,
+            "top1": top1, "top5_recall": rec5, "kl": kl, "out_rel_l2": out_rel, "score_slope": slope,
+            "score_noise": noise}
+
+
+def run_score_quality_study(args) -> int:
+    torch.cuda.set_device(0)
+    import kv_cache_vector_18_b300 as tq
+    rows = []
+    for d in (64, 128):
+        for bits in (2, 3, 4):
+            for variant in ("mse", "prod"):
+                for tau in (1.0, 4.0, 8.0):
+                    rows.append(score_quality(tq, d, bits, variant, tau, seed=100 * d + bits))
+    print(json.dumps({"study": "score-quality", "data": "synthetic N(0,1) bf16 keys, values and queries",
+                      "rows": rows}), flush=True)
+    return 0
+
+
 def measure_e2e(args, spec, tq, kq, vq, K, V, q, ld, kc, vc, ws, out, tm, dev, world):
     """Same metric through the public API with host buffers: pinned H2D of the
     step's K, V and q, the three library calls, D2H of the packed planes and
@@ -697,6 +748,8 @@ def main(argv=None):
                     choices=["llama70b_layer_kv_quant", "decode_131k", "batched_decode_32k"])
     ap.add_argument("--rotation", choices=["qr", "hadamard"], default="qr",
                     help="rotation of both quantizers (hadamard: randomised Walsh-Hadamard)")
+    ap.add_argument("--study", choices=["score-quality"], default=None,
+                    help="print a study's JSON line instead of the benchmark (no timing)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--warm-seconds", type=float, default=WARM_SECONDS,
@@ -704,6 +757,8 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
+    if args.study == "score-quality":
+        return run_score_quality_study(args)
     spec = workload_spec(args.workload)
     spec["rotation"] = args.rotation
     if args.impl == "reference":
