@@ -32,6 +32,12 @@ quantize / dequantize (prod)   pinned: unbiasedness over seeds, exact b=1 varian
                                ((π/2)‖y‖² − ⟨x,y⟩²)/d, D_prod ≤ (π/2)·D_mse(b−1).
 pack_codes / pack_signs        pinned: hand-written golden bytes
                                (tests/golden/pack_layout.txt), round trip.
+mixed_* (outlier channels)     pinned: the page's split counts (32·3 + 96·2)/128 =
+                               2.25 code bits per channel; distortion = ‖x_O‖²·D_mse(d_o, b_o) +
+                               ‖x_N‖²·D_mse(d_n, b_n) on Gaussian rows; channel
+                               relabelling equivariance; scores are the sums of the
+                               two parts' scores from decode_attention; planted
+                               outlier channels are the ones selected.
 decode_attention               pinned: q = 0 gives the plain mean of dequantized
                                values, one-token context returns that value,
                                brute-force loop on a tiny case, dequant-free
@@ -60,6 +66,12 @@ Readings where the page is silent (each also listed in the design doc)
 * prod with b = 1 has a 0-bit MSE stage: one level at 0, residual r = x̂.
 * Attention: contiguous GQA (query head h reads KV head h // (Hq/Hkv)),
   scale 1/√d by default, no causal mask, empty context → output 0.
+* Outlier channels (experiments section, 32 channels at 3 bits + 96 at 2; the
+  page's sum (32·3 + 96·2)/128 is 2.25, not the 2.5 it prints — 2.5 counts two
+  16-bit part norms as well; the split is kept as printed): each
+  part of a row gets its own TurboQuant quantizer (own norm, rotation, codebook);
+  the page does not say how the outlier channels are found, so they are the d_o
+  channels of largest energy over the rows being cached.
 """
 from __future__ import annotations
 
@@ -75,7 +87,8 @@ __all__ = [
     "coord_cdf", "cell_mass", "cell_first_moment", "lloyd_max_codebook",
     "mse_distortion_theory", "Params", "make_params", "quantize", "qjl_of_residual", "pack_codes",
     "unpack_codes", "pack_signs", "unpack_signs", "dequantize", "decode_attention",
-    "code_bytes_per_row", "sign_bytes_per_row",
+    "code_bytes_per_row", "sign_bytes_per_row", "MixedParams", "outlier_channel_perm",
+    "mixed_bits_per_channel", "mixed_quantize", "mixed_dequantize", "mixed_decode_attention",
 ]
 
 MASK64 = (1 << 64) - 1
@@ -417,4 +430,80 @@ def decode_attention(pk: Params, pv: Params, q, k_rows: dict, v_rows: dict, seq_
             w = np.exp(s - np.max(s))
             w /= np.sum(w)
             out[b, h] = w @ V[b, kv, :L]
+    return out, scores
+
+
+# ----------------------------------------------------------------------------
+# Outlier-channel mixed precision (the page's experiments, KV cache: 32 outlier
+# channels at 3 bits and the other 96 at 2 bits make 2.5 bits per channel)
+# ----------------------------------------------------------------------------
+class MixedParams:
+    """Two independent quantizers over a split of the channels: ``po`` for the
+    outlier channels ``perm[:po.d]`` and ``pn`` for the others ``perm[po.d:]``."""
+
+    def __init__(self, po: Params, pn: Params, perm):
+        perm = np.asarray(perm, dtype=np.int64)
+        assert po.variant == pn.variant
+        assert perm.shape == (po.d + pn.d,) and np.array_equal(np.sort(perm), np.arange(perm.size))
+        self.po, self.pn, self.perm = po, pn, perm
+        self.d = perm.size
+        self.out = perm[: po.d]
+        self.rest = perm[po.d:]
+
+
+def outlier_channel_perm(X, d_o: int) -> np.ndarray:
+    """Channel split (the page does not say how outliers are chosen): the d_o
+    channels of largest energy Σ_rows x² (ties to the lower index), ascending,
+    then the other channels ascending."""
+    X = np.asarray(X, dtype=np.float64)
+    e = np.sum(X * X, axis=0)
+    order = sorted(range(X.shape[1]), key=lambda j: (-e[j], j))
+    out = np.sort(np.asarray(order[:d_o], dtype=np.int64))
+    rest = np.setdiff1d(np.arange(X.shape[1]), out)
+    return np.concatenate([out, rest])
+
+
+def mixed_bits_per_channel(mp: MixedParams) -> float:
+    """(d_o·b_o + d_n·b_n)/d: code bits per channel, norms not counted."""
+    return (mp.po.d * mp.po.bits + mp.pn.d * mp.pn.bits) / mp.d
+
+
+def mixed_quantize(mp: MixedParams, X) -> dict:
+    """Each part of every row quantized by its own quantizer."""
+    X = np.asarray(X, dtype=np.float64)
+    return {"o": quantize(mp.po, X[:, mp.out]), "n": quantize(mp.pn, X[:, mp.rest])}
+
+
+def mixed_dequantize(mp: MixedParams, rows_o: dict, rows_n: dict) -> np.ndarray:
+    """Both parts dequantized and written back to their channels."""
+    xo = dequantize(mp.po, rows_o["idx"], rows_o["norm"], rows_o.get("z"), rows_o.get("rnorm"))
+    xn = dequantize(mp.pn, rows_n["idx"], rows_n["norm"], rows_n.get("z"), rows_n.get("rnorm"))
+    x = np.zeros((xo.shape[0], mp.d))
+    x[:, mp.out] = xo
+    x[:, mp.rest] = xn
+    return x
+
+
+def mixed_decode_attention(mk: MixedParams, mv: MixedParams, q, k_o: dict, k_n: dict, v_o: dict, v_n: dict,
+                           seq_lens, Hkv: int, T_max: int, scale: float | None = None):
+    """Plain softmax attention over the mixed-precision dequantized keys and values
+    (rows ordered [B][Hkv][T_max]).  Returns (out [B, Hq, d], scores [B, Hq, T_max])."""
+    q = np.asarray(q, dtype=np.float64)
+    B, Hq, d = q.shape
+    G = Hq // Hkv
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    K = mixed_dequantize(mk, k_o, k_n).reshape(B, Hkv, T_max, d)
+    V = mixed_dequantize(mv, v_o, v_n).reshape(B, Hkv, T_max, d)
+    out = np.zeros((B, Hq, d))
+    scores = np.full((B, Hq, T_max), np.nan)
+    for b in range(B):
+        L = int(seq_lens[b])
+        for h in range(Hq):
+            if L == 0:
+                continue
+            s = scale * (K[b, h // G, :L] @ q[b, h])
+            scores[b, h, :L] = s
+            w = np.exp(s - np.max(s))
+            out[b, h] = (w / np.sum(w)) @ V[b, h // G, :L]
     return out, scores

@@ -509,3 +509,104 @@ def test_rotated_domain_score_identity():
         s = kq["norm"].astype(np.float64) * (pk.centroids[kq["idx"]] @ qp
                                              + pk.gamma * kq["rnorm"].astype(np.float64) * (kq["z"] @ qs))
         assert np.allclose(sc[0, h], s, atol=1e-12)
+
+
+# ---------------------------------------------------------------- outlier-channel mixed precision
+# The page's experiments (KV cache): 32 outlier channels at 3 bits, the other 96 at
+# 2 bits, (32·3 + 96·2)/128 = 2.5 bits per channel.
+def _mixed(d_o=32, b_o=3, b_n=2, variant="mse", perm=None, seed=3, d=128):
+    po = O.make_params(d_o, b_o, variant, seed)
+    pn = O.make_params(d - d_o, b_n, variant, seed + 1)
+    if perm is None:
+        perm = np.concatenate([np.arange(d - d_o, d), np.arange(d - d_o)])
+    return O.MixedParams(po, pn, perm)
+
+
+def test_mixed_bit_count_of_the_page_split():
+    # The page's own formula (32·3 + 96·2)/128 evaluates to 288/128 = 2.25, not the
+    # 2.5 printed after it; 2.5 results only when two 16-bit part norms are counted
+    # too, (288 + 2·16)/128.  The split itself (32 channels at 3 bits, 96 at 2) is kept.
+    mp = _mixed()
+    assert O.mixed_bits_per_channel(mp) == (32 * 3 + 96 * 2) / 128 == 2.25
+    assert (32 * 3 + 96 * 2 + 2 * 16) / 128 == 2.5
+    assert O.code_bytes_per_row(mp.po) + O.code_bytes_per_row(mp.pn) == 288 // 8
+    # the same split one bit higher: (32·4 + 96·3)/128 = 3.25 (3.5 with two 16-bit norms)
+    assert O.mixed_bits_per_channel(_mixed(b_o=4, b_n=3)) == 3.25
+
+
+@pytest.mark.parametrize("variant", ["mse", "prod"])
+def test_mixed_distortion_is_sum_of_parts(variant):
+    # each part's direction is uniform on its own sphere for Gaussian rows, so the
+    # mse distortion splits exactly: E‖x − x̃‖² = ‖x_O‖²·D(d_o, b_o) + ‖x_N‖²·D(d_n, b_n)
+    mp = _mixed(variant=variant, b_o=3, b_n=3 if variant == "prod" else 2)
+    X = np.random.default_rng(17).standard_normal((1 << 13, 128))
+    X[:, mp.out] *= 6.0  # outlier channels carry most of the energy
+    q = O.mixed_quantize(mp, X)
+    Xt = O.mixed_dequantize(mp, q["o"], q["n"])
+    err = np.sum((X - Xt) ** 2, axis=1)
+    if variant == "mse":
+        expect = (np.sum(X[:, mp.out] ** 2, axis=1) * O.mse_distortion_theory(32, 8)
+                  + np.sum(X[:, mp.rest] ** 2, axis=1) * O.mse_distortion_theory(96, 4))
+        assert abs(err.mean() / expect.mean() - 1) < 4 * err.std() / math.sqrt(err.size) / expect.mean() + 1e-3
+    else:
+        # prod: each part's stored residual has E‖r‖² = D_mse(d_part, b − 1)
+        r2o = q["o"]["rnorm"].astype(np.float64) ** 2
+        r2n = q["n"]["rnorm"].astype(np.float64) ** 2
+        assert abs(r2o.mean() / O.mse_distortion_theory(32, 4) - 1) < 0.05
+        assert abs(r2n.mean() / O.mse_distortion_theory(96, 4) - 1) < 0.05
+    # reconstruction of each part touches only its channels
+    x1 = np.zeros((1, 128))
+    x1[0, mp.out[0]] = 1.0
+    q1 = O.mixed_quantize(mp, x1)
+    assert np.all(O.mixed_dequantize(mp, q1["o"], q1["n"])[0, mp.rest] == 0)
+
+
+def test_mixed_relabelling_equivariance():
+    # relabel the channels of the input and of the split alike: same codes, output
+    # relabelled the same way (catches any mix-up of the gather and scatter maps)
+    rng = np.random.default_rng(5)
+    sigma = rng.permutation(128)
+    mp = _mixed(perm=rng.permutation(128))
+    mq = O.MixedParams(mp.po, mp.pn, np.argsort(sigma)[mp.perm])
+    X = rng.standard_normal((64, 128))
+    Xs = np.empty_like(X)
+    Xs[:, np.argsort(sigma)] = X  # channel c of X becomes channel σ⁻¹(c)
+    a, b = O.mixed_quantize(mp, X), O.mixed_quantize(mq, Xs)
+    assert np.array_equal(a["o"]["idx"], b["o"]["idx"]) and np.array_equal(a["n"]["idx"], b["n"]["idx"])
+    ya = O.mixed_dequantize(mp, a["o"], a["n"])
+    yb = O.mixed_dequantize(mq, b["o"], b["n"])
+    assert np.allclose(yb[:, np.argsort(sigma)], ya, atol=1e-12)
+
+
+def test_mixed_scores_are_sums_of_part_scores():
+    mk = _mixed(variant="prod", b_o=4, b_n=3, seed=8)
+    mv = _mixed(seed=9)
+    B, Hq, Hkv, T, d = 2, 4, 2, 50, 128
+    rng = np.random.default_rng(2)
+    K = rng.standard_normal((B * Hkv * T, d))
+    V = rng.standard_normal((B * Hkv * T, d))
+    q = rng.standard_normal((B, Hq, d))
+    kq, vq = O.mixed_quantize(mk, K), O.mixed_quantize(mv, V)
+    lens = [50, 17]
+    out, sc = O.mixed_decode_attention(mk, mv, q, kq["o"], kq["n"], vq["o"], vq["n"], lens, Hkv, T)
+    s = 1 / math.sqrt(d)
+    _, so = O.decode_attention(mk.po, mv.po, q[:, :, mk.out], kq["o"], vq["o"], lens, Hkv, T, scale=s)
+    _, sn = O.decode_attention(mk.pn, mv.pn, q[:, :, mk.rest], kq["n"], vq["n"], lens, Hkv, T, scale=s)
+    assert np.allclose(sc, so + sn, atol=1e-12, equal_nan=True)
+    # q = 0: uniform weights, the output is the mean of the dequantized values
+    out0, _ = O.mixed_decode_attention(mk, mv, np.zeros_like(q), kq["o"], kq["n"], vq["o"], vq["n"], lens, Hkv, T)
+    Vt = O.mixed_dequantize(mv, vq["o"], vq["n"]).reshape(B, Hkv, T, d)
+    assert np.allclose(out0[1, 3], Vt[1, 1, :17].mean(axis=0), atol=1e-12)
+
+
+def test_outlier_channel_selection():
+    rng = np.random.default_rng(4)
+    X = rng.standard_normal((2000, 128))
+    hot = rng.choice(128, 32, replace=False)
+    X[:, hot] *= 5.0
+    perm = O.outlier_channel_perm(X, 32)
+    assert np.array_equal(perm[:32], np.sort(hot))
+    assert np.array_equal(perm[32:], np.setdiff1d(np.arange(128), hot))
+    # ties go to the lower channel index
+    Z = np.ones((3, 8))
+    assert np.array_equal(O.outlier_channel_perm(Z, 2), [0, 1, 2, 3, 4, 5, 6, 7])
