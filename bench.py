@@ -683,6 +683,73 @@ def score_quality(tq, d: int, bits: int, variant: str, tau: float, B: int = 4, H
             "score_noise": noise}
 
 
+def run_mixed(args) -> int:
+    """Outlier-channel mixed precision on the Llama-3.1-70B layer: the 32 channels
+    of largest energy at 3 bits and the other 96 at 2 (mse, K and V), chosen by
+    tq_select_outlier_channels from the rows themselves.  Device time per call
+    (CUDA graph per call, L2 flushed before each replay), algorithmic bytes ÷ time,
+    and the distortion against uniform 2- and 3-bit quantizers on the same rows."""
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    import kv_cache_vector_18_b300 as tq
+    spec = workload_spec("llama70b_layer_kv_quant")
+    K, V, q, lens = make_inputs(spec)
+    d, B, Hq, Hkv, T = spec["d"], spec["B"], spec["Hq"], spec["Hkv"], spec["T"]
+    d_o, bo, bn = 32, 3, 2
+    Kd, Vd, qd, ld = K.to(dev).reshape(-1, d), V.to(dev).reshape(-1, d), q.to(dev), lens.to(dev)
+    n = Kd.shape[0]
+    pk, _ = tq.select_outlier_channels(Kd, d_o)
+    pv, _ = tq.select_outlier_channels(Vd, d_o)
+    mk = tq.MixedQuantizer(pk, d_o, bo, bn, "mse", seed_o=10, seed_n=12)
+    mv = tq.MixedQuantizer(pv, d_o, bo, bn, "mse", seed_o=11, seed_n=13)
+    kc, vc = mk.empty_planes(n), mv.empty_planes(n)
+    ws = torch.empty(tq.mixed_decode_workspace_bytes(mk, mv, B, Hq, Hkv, T), dtype=torch.uint8, device=dev)
+    out = torch.empty((B, Hq, d), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    calls = {"quantize_k": lambda: mk.quantize(Kd, out=kc), "quantize_v": lambda: mv.quantize(Vd, out=vc),
+             "decode": lambda: tq.mixed_decode_attention(mk, mv, qd, kc, vc, ld, Hkv, T, workspace=ws, out=out)}
+    for fn in calls.values():
+        fn()
+    torch.cuda.synchronize()
+    rec = (bo * d_o // 8 + 4) + (bn * (d - d_o) // 8 + 4)  # record bytes of both parts
+    nbytes = {"quantize_k": n * (2 * d + rec), "quantize_v": n * (2 * d + rec),
+              "decode": int(lens.sum()) * Hkv * 2 * rec + B * Hq * d * 6}
+    peaks = load_peaks()
+    res = {}
+    for name, fn in calls.items():
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        for _ in range(max(args.warmup, 3)):
+            flush.zero_()
+            g.replay()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(50)]
+        for e0, e1 in evs:
+            flush.zero_()
+            e0.record()
+            g.replay()
+            e1.record()
+        torch.cuda.synchronize()
+        ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs)
+        gbs = nbytes[name] / (ms / 1e3) / 1e9
+        res[name] = {"us": ms * 1e3, "bytes": nbytes[name], "gbs": gbs, "frac": gbs / peaks["hbm_gbs"]}
+    # distortion E‖x − x̃‖²/‖x‖² on the first 65536 K rows: mixed against uniform
+    m = 1 << 16
+    xs = Kd[:m]
+    def dist(y):
+        xf = xs.float()
+        return float((((xf - y.float()) ** 2).sum(1) / (xf ** 2).sum(1)).double().mean())
+    dm = dist(mk.dequantize(mk.quantize(xs)))
+    u2, u3 = tq.Quantizer(d, 2, "mse", seed=10), tq.Quantizer(d, 3, "mse", seed=10)
+    d2, d3 = dist(u2.dequantize(u2.quantize(xs))), dist(u3.dequantize(u3.quantize(xs)))
+    print(json.dumps({"mixed": "outlier channels 32 x 3 bits + 96 x 2 bits, mse, K and V",
+                      "workload": spec["name"], "code_bits_per_channel": (d_o * bo + (d - d_o) * bn) / d,
+                      "record_bytes": rec, "calls": res, "peak_gbs": peaks["hbm_gbs"],
+                      "distortion": {"mixed": dm, "uniform_b2": d2, "uniform_b3": d3},
+                      "timing": "CUDA graph per call, events around 50 replays, L2 flushed before each"}), flush=True)
+    return 0
+
+
 def run_score_quality_study(args) -> int:
     torch.cuda.set_device(0)
     import kv_cache_vector_18_b300 as tq
@@ -750,6 +817,8 @@ def main(argv=None):
                     help="rotation of both quantizers (hadamard: randomised Walsh-Hadamard)")
     ap.add_argument("--study", choices=["score-quality"], default=None,
                     help="print a study's JSON line instead of the benchmark (no timing)")
+    ap.add_argument("--mixed", action="store_true",
+                    help="time outlier-channel mixed precision on the default workload (own JSON line)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--warm-seconds", type=float, default=WARM_SECONDS,
@@ -759,6 +828,8 @@ def main(argv=None):
         args.warmup = 3
     if args.study == "score-quality":
         return run_score_quality_study(args)
+    if args.mixed:
+        return run_mixed(args)
     spec = workload_spec(args.workload)
     spec["rotation"] = args.rotation
     if args.impl == "reference":

@@ -62,6 +62,7 @@ extern "C" {
 /* Codes in a handle's device status word (tq_device_status) other than the
  * 1..99 of an expired pipeline wait. */
 #define TQ_STATUS_APPEND_FULL 200  /* an append found its (batch, KV head) slab full */
+#define TQ_STATUS_BAD_CHANNEL 201  /* a channel permutation entry was outside [0, d) */
 
 enum { TQ_MSE = 0, TQ_PROD = 1 };
 enum { TQ_BF16 = 0, TQ_F32 = 1 };
@@ -187,6 +188,71 @@ int tq_decode_attention(tq_handle hk, tq_handle hv, const void* q, int q_dtype,
                         int B, int Hq, int Hkv, int T_max, float scale,
                         float* out, float* scores_out,
                         void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Outlier-channel mixed precision (the page's experiments, KV cache: "outlier"
+ * channels kept at more bits than the rest, 32 channels at 3 bits and 96 at 2).
+ * A row's d channels are split by a device permutation perm (int32 [d]):
+ * perm[0..d_o) are the outlier channels, perm[d_o..d) the others, each entry in
+ * [0, d) and each channel once.  Each part is an ordinary quantizer handle of its
+ * own dimension (ho: d_o channels, hn: d − d_o; both of one variant), so it has
+ * its own norm, rotation, codebook and packed planes.  A perm entry outside
+ * [0, d) is never dereferenced: it reads or writes channel 0 and the part
+ * handle's status word records TQ_STATUS_BAD_CHANNEL.
+ */
+
+/*
+ * tq_select_outlier_channels — choose the split from the rows to be cached (the
+ * page does not say how outliers are found): energy[j] = Σ_rows x_j² in float64
+ * (device [d], written), and perm = the d_o channels of largest energy (ties to
+ * the lower channel) ascending, then the others ascending (device int32 [d]).
+ * x: device [n_rows, d] with row stride x_row_stride elements (x_dtype TQ_BF16
+ * or TQ_F32).  d: multiple of 32 in [64, 256]; d_o: multiple of 32 in
+ * [32, d − 32].  Energies are accumulated with float64 atomics, so channels
+ * whose energies agree to ~1e-15 relative may be ordered either way.
+ */
+int tq_select_outlier_channels(const void* x, int x_dtype, int64_t n_rows, int64_t x_row_stride, int d,
+                               int d_o, double* energy, int32_t* perm, void* stream);
+
+/*
+ * tq_mixed_quantize — part o of row i (channels perm[0..d_o)) quantized by ho into
+ * record i of out_o, part n (channels perm[d_o..d)) by hn into out_n, exactly as
+ * tq_quantize would quantize the gathered sub-rows.  x: device [n_rows, d], row
+ * stride x_row_stride ≥ d elements (stride·element size a multiple of 16 bytes).
+ */
+int tq_mixed_quantize(tq_handle ho, tq_handle hn, const int32_t* perm, const void* x, int x_dtype,
+                      int64_t n_rows, int64_t x_row_stride, tq_planes out_o, tq_planes out_n,
+                      void* stream);
+
+/*
+ * tq_mixed_dequantize — both parts dequantized (as tq_dequantize) and written to
+ * their channels of y: device [n_rows, d] of y_dtype, contiguous.
+ */
+int tq_mixed_dequantize(tq_handle ho, tq_handle hn, const int32_t* perm, tq_planes in_o, tq_planes in_n,
+                        int64_t n_rows, void* y, int y_dtype, void* stream);
+
+/* Workspace bytes tq_mixed_decode_attention needs for these shapes. */
+int tq_mixed_decode_workspace_bytes(tq_handle hko, tq_handle hkn, tq_handle hvo, tq_handle hvn, int B,
+                                    int Hq, int Hkv, int T_max, size_t* bytes);
+
+/*
+ * tq_mixed_decode_attention — tq_decode_attention over mixed-precision keys and
+ * values: the score of token t is the sum of its parts' scores,
+ *   s_t = scale·Σ_p ‖k_p,t‖(⟨q′_p, c_p[code]⟩ + √(π/2)/d_p·‖r_p,t‖⟨q″_p, z_p,t⟩)
+ * with q′_p = Π_p·q[perm_k part p] (= scale·⟨q, k̃_t⟩ of the mixed dequantized
+ * key), and the output is Σ_t p_t·ṽ_t with each value part rotated back by its
+ * own Πᵀ (+ Sᵀ) once per head and scattered to its channels by perm_v.  Keys
+ * (hko, hkn, perm_k) and values (hvo, hvn, perm_v) may split differently but
+ * must have the same total d (64..256).  Planes kc_o, kc_n, vc_o, vc_n hold
+ * B·Hkv·T_max records each, ordered [B][Hkv][T_max].  Other arguments as
+ * tq_decode_attention; bad perm entries are recorded in hko's status word.
+ */
+int tq_mixed_decode_attention(tq_handle hko, tq_handle hkn, tq_handle hvo, tq_handle hvn,
+                              const int32_t* perm_k, const int32_t* perm_v, const void* q, int q_dtype,
+                              tq_planes kc_o, tq_planes kc_n, tq_planes vc_o, tq_planes vc_n,
+                              const int32_t* seq_lens, int B, int Hq, int Hkv, int T_max, float scale,
+                              float* out, float* scores_out, void* workspace, size_t ws_bytes,
+                              void* stream);
 
 /*
  * tq_decode_append_attention — one decode step that first appends the step's

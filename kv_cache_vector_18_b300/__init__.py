@@ -17,7 +17,8 @@ import torch
 from . import _lib
 from ._lib import TQ_BF16, TQ_F32, TQ_MSE, TQ_PROD, TQError, check
 
-__all__ = ["Quantizer", "decode_attention", "decode_append_attention", "decode_workspace_bytes", "build_params_host", "TQError",
+__all__ = ["Quantizer", "MixedQuantizer", "decode_attention", "decode_append_attention", "mixed_decode_attention",
+           "mixed_decode_workspace_bytes", "select_outlier_channels", "decode_workspace_bytes", "build_params_host", "TQError",
            "library_path"]
 
 _VARIANTS = {"mse": TQ_MSE, "prod": TQ_PROD}
@@ -209,6 +210,90 @@ def decode_append_attention(kq: Quantizer, vq: Quantizer, q: torch.Tensor, k_new
         float(scale) if scale is not None else 0.0, _ptr(out), _ptr(workspace), workspace.numel(),
         _stream(stream)))
     return out
+
+
+def select_outlier_channels(x: torch.Tensor, d_o: int, stream=None):
+    """tq_select_outlier_channels.  x: [n, d] (bf16/fp32, unit stride along d).
+    Returns (perm int32 [d]: the d_o channels of largest energy ascending, then the
+    rest ascending; energy float64 [d])."""
+    n, d = x.shape
+    if x.stride(1) != 1:
+        raise ValueError("x must have unit stride along channels")
+    perm = torch.empty(d, dtype=torch.int32, device=x.device)
+    energy = torch.empty(d, dtype=torch.float64, device=x.device)
+    check(_lib.lib().tq_select_outlier_channels(_ptr(x), _DTYPES[x.dtype], n, x.stride(0), d, d_o, _ptr(energy),
+                                                _ptr(perm), _stream(stream)))
+    return perm, energy
+
+
+class MixedQuantizer:
+    """Outlier-channel mixed precision: channels perm[:d_o] quantized by one handle
+    (bits_o), the others by a second (bits_n), both of one variant; perm is an
+    int32 permutation of range(d) on the device.  Planes come as {"o": …, "n": …}."""
+
+    def __init__(self, perm: torch.Tensor, d_o: int, bits_o: int, bits_n: int, variant: str = "mse",
+                 seed_o: int = 0, seed_n: int = 1, rotation: str = "qr"):
+        if perm.dtype != torch.int32 or perm.dim() != 1 or not perm.is_cuda:
+            raise ValueError("perm must be a 1-D int32 CUDA tensor")
+        self.d = perm.numel()
+        self.perm = perm.contiguous()
+        self.qo = Quantizer(d_o, bits_o, variant, seed=seed_o, rotation=rotation)
+        self.qn = Quantizer(self.d - d_o, bits_n, variant, seed=seed_n, rotation=rotation)
+        self.d_o, self.variant = d_o, variant
+
+    def empty_planes(self, n_rows: int) -> dict:
+        return {"o": self.qo.empty_planes(n_rows), "n": self.qn.empty_planes(n_rows)}
+
+    def quantize(self, x: torch.Tensor, out: dict | None = None, stream=None) -> dict:
+        n, d = x.shape
+        if d != self.d or x.stride(1) != 1:
+            raise ValueError("x must be [n, d] with unit stride along channels")
+        out = out if out is not None else self.empty_planes(n)
+        check(_lib.lib().tq_mixed_quantize(self.qo.handle, self.qn.handle, _ptr(self.perm), _ptr(x),
+                                           _DTYPES[x.dtype], n, x.stride(0), Quantizer.planes_struct(out["o"]),
+                                           Quantizer.planes_struct(out["n"]), _stream(stream)))
+        return out
+
+    def dequantize(self, planes: dict, dtype=torch.float32, stream=None) -> torch.Tensor:
+        n = planes["o"]["norm"].shape[0]
+        y = torch.empty((n, self.d), dtype=dtype, device=self.perm.device)
+        check(_lib.lib().tq_mixed_dequantize(self.qo.handle, self.qn.handle, _ptr(self.perm),
+                                             Quantizer.planes_struct(planes["o"]), Quantizer.planes_struct(planes["n"]),
+                                             n, _ptr(y), _DTYPES[dtype], _stream(stream)))
+        return y
+
+
+def mixed_decode_workspace_bytes(mk: MixedQuantizer, mv: MixedQuantizer, B: int, Hq: int, Hkv: int, T_max: int) -> int:
+    n = ctypes.c_size_t()
+    check(_lib.lib().tq_mixed_decode_workspace_bytes(mk.qo.handle, mk.qn.handle, mv.qo.handle, mv.qn.handle, B, Hq,
+                                                     Hkv, T_max, ctypes.byref(n)))
+    return n.value
+
+
+def mixed_decode_attention(mk: MixedQuantizer, mv: MixedQuantizer, q: torch.Tensor, kcache: dict, vcache: dict,
+                           seq_lens: torch.Tensor, Hkv: int, T_max: int, scale: float | None = None,
+                           return_scores: bool = False, workspace: torch.Tensor | None = None,
+                           out: torch.Tensor | None = None, stream=None):
+    """tq_mixed_decode_attention; arguments as decode_attention with MixedQuantizer
+    handles and {"o", "n"} caches."""
+    B, Hq, d = q.shape
+    if not q.is_contiguous():
+        raise ValueError("q must be contiguous")
+    if seq_lens.dtype != torch.int32:
+        raise ValueError("seq_lens must be int32")
+    need = mixed_decode_workspace_bytes(mk, mv, B, Hq, Hkv, T_max)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty((B, Hq, d), dtype=torch.float32, device=q.device)
+    scores = torch.full((B, Hq, T_max), float("nan"), dtype=torch.float32, device=q.device) if return_scores else None
+    P = Quantizer.planes_struct
+    check(_lib.lib().tq_mixed_decode_attention(
+        mk.qo.handle, mk.qn.handle, mv.qo.handle, mv.qn.handle, _ptr(mk.perm), _ptr(mv.perm), _ptr(q),
+        _DTYPES[q.dtype], P(kcache["o"]), P(kcache["n"]), P(vcache["o"]), P(vcache["n"]), _ptr(seq_lens), B, Hq,
+        Hkv, T_max, float(scale) if scale is not None else 0.0, _ptr(out), _ptr(scores), _ptr(workspace),
+        workspace.numel(), _stream(stream)))
+    return (out, scores) if return_scores else out
 
 
 def default_scale(d: int) -> float:

@@ -17,6 +17,7 @@ TQ_MSE, TQ_PROD = 0, 1
 TQ_BF16, TQ_F32 = 0, 1
 TQ_ROT_QR, TQ_ROT_HADAMARD = 0, 1
 TQ_STATUS_APPEND_FULL = 200
+TQ_STATUS_BAD_CHANNEL = 201
 
 ERROR_NAMES = {TQ_EINVAL: "TQ_EINVAL", TQ_EUNSUPPORTED: "TQ_EUNSUPPORTED", TQ_EALIGN: "TQ_EALIGN",
                TQ_ECUDA: "TQ_ECUDA", TQ_ENOMEM: "TQ_ENOMEM", TQ_EWORKSPACE: "TQ_EWORKSPACE"}
@@ -25,7 +26,9 @@ ERROR_NAMES = {TQ_EINVAL: "TQ_EINVAL", TQ_EUNSUPPORTED: "TQ_EUNSUPPORTED", TQ_EA
 EXPORTED = ["tq_init", "tq_init_ex", "tq_destroy", "tq_row_bytes", "tq_build_params_host",
             "tq_build_params_host_ex", "tq_get_params",
             "tq_quantize", "tq_dequantize", "tq_decode_workspace_bytes", "tq_decode_attention",
-            "tq_decode_attention_noalloc", "tq_decode_append_attention", "tq_device_status", "tq_check_wait_timeout", "tq_last_error"]
+            "tq_decode_attention_noalloc", "tq_decode_append_attention", "tq_select_outlier_channels",
+            "tq_mixed_quantize", "tq_mixed_dequantize", "tq_mixed_decode_workspace_bytes",
+            "tq_mixed_decode_attention", "tq_device_status", "tq_check_wait_timeout", "tq_last_error"]
 NOALLOC_WORKSPACE_BYTES = 4 << 20
 
 
@@ -69,6 +72,12 @@ def lib() -> ctypes.CDLL:
                                               ctypes.c_float, vp, vp, vp]
     L.tq_decode_append_attention.argtypes = [vp, vp, vp, i32, vp, vp, i32, Planes, Planes, vp, i32, i32, i32, i32,
                                              ctypes.c_float, vp, vp, sz, vp]
+    L.tq_select_outlier_channels.argtypes = [vp, i32, i64, i64, i32, i32, vp, vp, vp]
+    L.tq_mixed_quantize.argtypes = [vp, vp, vp, vp, i32, i64, i64, Planes, Planes, vp]
+    L.tq_mixed_dequantize.argtypes = [vp, vp, vp, Planes, Planes, i64, vp, i32, vp]
+    L.tq_mixed_decode_workspace_bytes.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, ctypes.POINTER(sz)]
+    L.tq_mixed_decode_attention.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, Planes, Planes, Planes, Planes, vp,
+                                            i32, i32, i32, i32, ctypes.c_float, vp, vp, vp, sz, vp]
     L.tq_device_status.argtypes = [vp, ctypes.POINTER(i32), i32]
     L.tq_check_wait_timeout.argtypes = [vp, i32, u64, vp]
     L.tq_last_error.restype = ctypes.c_char_p

@@ -470,6 +470,130 @@ int tq_decode_attention(tq_handle hk, tq_handle hv, const void* q, int q_dtype, 
                          (cudaStream_t)stream);
 }
 
+int tq_select_outlier_channels(const void* x, int x_dtype, int64_t n_rows, int64_t x_row_stride, int d, int d_o,
+                               double* energy, int32_t* perm, void* stream) {
+    if (x_dtype != TQ_BF16 && x_dtype != TQ_F32) return fail(TQ_EINVAL, "x_dtype=%d invalid", x_dtype);
+    if (d < 2 * kMinD || d > kMaxD || d % 32 != 0) return fail(TQ_EUNSUPPORTED, "d=%d unsupported (64..256, multiple of 32)", d);
+    if (d_o < kMinD || d_o > d - kMinD || d_o % 32 != 0)
+        return fail(TQ_EINVAL, "d_o=%d must be a multiple of 32 in [32, d − 32]", d_o);
+    if (n_rows < 0) return fail(TQ_EINVAL, "n_rows=%lld is negative", (long long)n_rows);
+    const int es = x_dtype == TQ_BF16 ? 2 : 4;
+    if (x_row_stride < d) return fail(TQ_EINVAL, "x_row_stride=%lld < d=%d", (long long)x_row_stride, d);
+    if ((x_row_stride * es) % 16 != 0) return fail(TQ_EALIGN, "x_row_stride*elem_size must be a multiple of 16 bytes");
+    int rc;
+    if (n_rows > 0 && (rc = check_device_ptr(x, "x", true)) != TQ_OK) return rc;
+    if ((rc = check_device_ptr(energy, "energy", true)) != TQ_OK) return rc;
+    if ((rc = check_device_ptr(perm, "perm", true)) != TQ_OK) return rc;
+    return launch_select_outlier_channels(x, x_dtype, n_rows, x_row_stride, d, d_o, energy, perm,
+                                          (cudaStream_t)stream);
+}
+
+namespace {
+int validate_split(tq_handle ho, tq_handle hn, const char* what) {
+    int rc = validate_handle(ho, what);
+    if (rc == TQ_OK) rc = validate_handle(hn, what);
+    if (rc != TQ_OK) return rc;
+    if (ho->hp.variant != hn->hp.variant) return fail(TQ_EINVAL, "%s parts differ in variant", what);
+    if (ho->hp.d + hn->hp.d > kMaxD) return fail(TQ_EUNSUPPORTED, "%s parts sum to d=%d > %d", what,
+                                                 ho->hp.d + hn->hp.d, kMaxD);
+    return TQ_OK;
+}
+}  // namespace
+
+int tq_mixed_quantize(tq_handle ho, tq_handle hn, const int32_t* perm, const void* x, int x_dtype, int64_t n_rows,
+                      int64_t x_row_stride, tq_planes out_o, tq_planes out_n, void* stream) {
+    int rc = validate_split(ho, hn, "quantizer");
+    if (rc != TQ_OK) return rc;
+    if (n_rows < 0) return fail(TQ_EINVAL, "n_rows=%lld is negative", (long long)n_rows);
+    if (x_dtype != TQ_BF16 && x_dtype != TQ_F32) return fail(TQ_EINVAL, "x_dtype=%d invalid", x_dtype);
+    if (n_rows == 0) return TQ_OK;
+    const int d = ho->hp.d + hn->hp.d;
+    const int es = x_dtype == TQ_BF16 ? 2 : 4;
+    if (x_row_stride < d) return fail(TQ_EINVAL, "x_row_stride=%lld < d=%d", (long long)x_row_stride, d);
+    if ((x_row_stride * es) % 16 != 0) return fail(TQ_EALIGN, "x_row_stride*elem_size must be a multiple of 16 bytes");
+    if ((rc = check_device_ptr(perm, "perm", true)) != TQ_OK) return rc;
+    if ((rc = check_device_ptr(x, "x", true)) != TQ_OK) return rc;
+    if ((rc = check_planes(*ho, out_o, "out_o")) != TQ_OK) return rc;
+    if ((rc = check_planes(*hn, out_n, "out_n")) != TQ_OK) return rc;
+    const cudaStream_t s = (cudaStream_t)stream;
+    rc = launch_quantize_part(*ho, x, x_dtype, n_rows, x_row_stride, perm, d, out_o, s);
+    if (rc == TQ_OK) rc = launch_quantize_part(*hn, x, x_dtype, n_rows, x_row_stride, perm + ho->hp.d, d, out_n, s);
+    return rc;
+}
+
+int tq_mixed_dequantize(tq_handle ho, tq_handle hn, const int32_t* perm, tq_planes in_o, tq_planes in_n,
+                        int64_t n_rows, void* y, int y_dtype, void* stream) {
+    int rc = validate_split(ho, hn, "quantizer");
+    if (rc != TQ_OK) return rc;
+    if (n_rows < 0) return fail(TQ_EINVAL, "n_rows=%lld is negative", (long long)n_rows);
+    if (y_dtype != TQ_BF16 && y_dtype != TQ_F32) return fail(TQ_EINVAL, "y_dtype=%d invalid", y_dtype);
+    if (n_rows == 0) return TQ_OK;
+    const int d = ho->hp.d + hn->hp.d;
+    if ((rc = check_device_ptr(perm, "perm", true)) != TQ_OK) return rc;
+    if ((rc = check_device_ptr(y, "y", true)) != TQ_OK) return rc;
+    if ((rc = check_planes(*ho, in_o, "in_o")) != TQ_OK) return rc;
+    if ((rc = check_planes(*hn, in_n, "in_n")) != TQ_OK) return rc;
+    const cudaStream_t s = (cudaStream_t)stream;
+    rc = launch_dequantize_part(*ho, in_o, n_rows, perm, d, y, y_dtype, s);
+    if (rc == TQ_OK) rc = launch_dequantize_part(*hn, in_n, n_rows, perm + ho->hp.d, d, y, y_dtype, s);
+    return rc;
+}
+
+namespace {
+int mixed_shape(tq_handle hko, tq_handle hkn, tq_handle hvo, tq_handle hvn, int B, int Hq, int Hkv, int T_max,
+                MixedShape* plan, size_t* bytes) {
+    int rc = validate_split(hko, hkn, "key");
+    if (rc == TQ_OK) rc = validate_split(hvo, hvn, "value");
+    if (rc != TQ_OK) return rc;
+    const int d = hko->hp.d + hkn->hp.d;
+    if (hvo->hp.d + hvn->hp.d != d) return fail(TQ_EINVAL, "key d=%d and value d=%d differ", d,
+                                                hvo->hp.d + hvn->hp.d);
+    return mixed_plan(d, hko->num_sms, hvo->hp.variant == TQ_PROD, B, Hq, Hkv, T_max, plan, bytes);
+}
+}  // namespace
+
+int tq_mixed_decode_workspace_bytes(tq_handle hko, tq_handle hkn, tq_handle hvo, tq_handle hvn, int B, int Hq,
+                                    int Hkv, int T_max, size_t* bytes) {
+    if (bytes == nullptr) return fail(TQ_EINVAL, "bytes is NULL");
+    MixedShape plan;
+    return mixed_shape(hko, hkn, hvo, hvn, B, Hq, Hkv, T_max, &plan, bytes);
+}
+
+int tq_mixed_decode_attention(tq_handle hko, tq_handle hkn, tq_handle hvo, tq_handle hvn, const int32_t* perm_k,
+                              const int32_t* perm_v, const void* q, int q_dtype, tq_planes kc_o, tq_planes kc_n,
+                              tq_planes vc_o, tq_planes vc_n, const int32_t* seq_lens, int B, int Hq, int Hkv,
+                              int T_max, float scale, float* out, float* scores_out, void* workspace,
+                              size_t ws_bytes, void* stream) {
+    if (q_dtype != TQ_BF16 && q_dtype != TQ_F32) return fail(TQ_EINVAL, "q_dtype=%d invalid", q_dtype);
+    MixedShape plan;
+    size_t need = 0;
+    int rc = mixed_shape(hko, hkn, hvo, hvn, B, Hq, Hkv, T_max, &plan, &need);
+    if (rc != TQ_OK) return rc;
+    if (B == 0 || Hq == 0) return TQ_OK;
+    if (ws_bytes < need) return fail(TQ_EWORKSPACE, "workspace of %zu bytes < required %zu", ws_bytes, need);
+    if ((rc = check_device_ptr(perm_k, "perm_k", true)) != TQ_OK) return rc;
+    if ((rc = check_device_ptr(perm_v, "perm_v", true)) != TQ_OK) return rc;
+    if ((rc = check_device_ptr(q, "q", true)) != TQ_OK) return rc;
+    if ((rc = check_device_ptr(seq_lens, "seq_lens", true)) != TQ_OK) return rc;
+    if ((rc = check_device_ptr(out, "out", true)) != TQ_OK) return rc;
+    if ((rc = check_device_ptr(scores_out, "scores_out", false)) != TQ_OK) return rc;
+    if ((rc = check_device_ptr(workspace, "workspace", true)) != TQ_OK) return rc;
+    if (T_max > 0) {
+        if ((rc = check_planes(*hko, kc_o, "kc_o")) != TQ_OK) return rc;
+        if ((rc = check_planes(*hkn, kc_n, "kc_n")) != TQ_OK) return rc;
+        if ((rc = check_planes(*hvo, vc_o, "vc_o")) != TQ_OK) return rc;
+        if ((rc = check_planes(*hvn, vc_n, "vc_n")) != TQ_OK) return rc;
+    }
+    if (scale <= 0.f) scale = (float)(1.0 / sqrt((double)plan.d));
+    MixedDecode m;
+    m.hk[0] = hko; m.hk[1] = hkn; m.hv[0] = hvo; m.hv[1] = hvn;
+    m.perm_k = perm_k; m.perm_v = perm_v;
+    m.q = q; m.q_dtype = q_dtype;
+    m.kc[0] = kc_o; m.kc[1] = kc_n; m.vc[0] = vc_o; m.vc[1] = vc_n;
+    m.seq_lens = seq_lens; m.scale = scale; m.out = out; m.scores = scores_out; m.workspace = workspace;
+    return launch_mixed_decode(m, plan, (cudaStream_t)stream);
+}
+
 int tq_decode_append_attention(tq_handle hk, tq_handle hv, const void* q, int q_dtype, const void* k_new,
                                const void* v_new, int kv_dtype, tq_planes kc, tq_planes vc, int32_t* seq_lens,
                                int B, int Hq, int Hkv, int T_max, float scale, float* out, void* workspace,

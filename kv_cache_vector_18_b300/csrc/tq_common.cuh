@@ -27,6 +27,24 @@ __device__ __forceinline__ int bucket_count(const Codebook& cb, float n, float y
     return c;
 }
 
+// Channels of one part of an outlier-channel split: element j of the part is
+// channel ch[j] of a full row of d_full elements (ch == nullptr: channel j, the
+// plain single-part row).  An index outside [0, d_full) is never dereferenced: it
+// maps to channel 0 and records TQ_STATUS_BAD_CHANNEL.
+struct ChannelMap {
+    const int32_t* ch = nullptr;
+    int d_full = 0;
+    int* status = nullptr;
+};
+
+__device__ __forceinline__ int channel_of(const ChannelMap& cm, int j) {
+    if (cm.ch == nullptr) return j;
+    const int c = cm.ch[j];
+    if ((unsigned)c < (unsigned)cm.d_full) return c;
+    atomicExch(cm.status, TQ_STATUS_BAD_CHANNEL);
+    return 0;
+}
+
 // Read code j (b bits, LSB-first bitstream) from a row held as 32-bit words.
 __device__ __forceinline__ int read_code(const uint32_t* w, int j, int b) {
     int bit = j * b;

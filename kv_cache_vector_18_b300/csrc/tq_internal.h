@@ -115,6 +115,34 @@ int encode_tmap_f16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint6
 // Kernel launchers (one per .cu file).  Arguments are validated by the caller.
 bool quantize_tc_supported(const tq_ctx& h, int x_dtype, int64_t n_rows);
 int launch_expire_wait(const tq_ctx& h, int code, uint64_t limit_ns, cudaStream_t s);
+// Outlier-channel mixed precision (tq_quantize.cu, tq_dequantize.cu, tq_mixed.cu):
+// one part of a channel split quantized from / dequantized to full rows of d_full.
+int launch_quantize_part(const tq_ctx& h, const void* x, int x_dtype, int64_t n_rows, int64_t stride,
+                         const int32_t* ch, int d_full, const tq_planes& out, cudaStream_t s);
+int launch_dequantize_part(const tq_ctx& h, const tq_planes& in, int64_t n_rows, const int32_t* ch, int d_full,
+                           void* y, int y_dtype, cudaStream_t s);
+struct MixedShape {
+    int B = 0, Hq = 0, Hkv = 0, T_max = 0, d = 0, G = 0, n_splits = 1, chunk = 64;
+};
+struct MixedDecode {
+    const tq_ctx* hk[2];  // key parts: outlier channels, the rest
+    const tq_ctx* hv[2];
+    const int32_t* perm_k;
+    const int32_t* perm_v;
+    const void* q;
+    int q_dtype;
+    tq_planes kc[2], vc[2];
+    const int32_t* seq_lens;
+    float scale;
+    float* out;
+    float* scores;
+    void* workspace;
+};
+int mixed_plan(int d, int sms, bool vprod, int B, int Hq, int Hkv, int T_max, MixedShape* plan, size_t* ws_bytes);
+int launch_mixed_decode(const MixedDecode& m, const MixedShape& p, cudaStream_t s);
+int launch_select_outlier_channels(const void* x, int x_dtype, int64_t n_rows, int64_t stride, int d, int d_o,
+                                   double* energy, int32_t* perm, cudaStream_t s);
+
 // Decode-step append (tq_append.cu): quantize the new K and V rows [B·Hkv, d] into
 // the next free token of each (batch, KV head) slab, then bump the lengths.
 int launch_append(const tq_ctx& hk, const tq_ctx& hv, const void* k_new, const void* v_new, int x_dtype, int B,

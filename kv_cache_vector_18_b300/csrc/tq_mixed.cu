@@ -1,0 +1,492 @@
+// Outlier-channel mixed precision: every row's d channels split into d_o outlier
+// channels and d − d_o others, each part quantized by its own TurboQuant handle
+// (own norm, rotation and codebook; the page's experiments use 32 channels at 3
+// bits and 96 at 2).  The split is a device permutation perm[d]: perm[0..d_o)
+// are the outlier channels, perm[d_o..d) the rest.
+//
+// Here: choosing the outlier channels (largest energy over the rows to be
+// cached), and split-K decode attention whose keys and values are two-part rows.
+// A token's score is the sum of its parts' scores; values accumulate per part in
+// that part's rotated frame and each part is rotated back and scattered to its
+// channels once per output head.  Lane l of a warp owns positions j = l + 32m of
+// the permuted row; d_o is a multiple of 32, so each slot m lies in one part.
+#include <math.h>
+
+#include "tq_common.cuh"
+
+namespace tq {
+namespace {
+
+constexpr int kWarps = 4;      // warps per split CTA
+constexpr int kMinChunk = 64;  // tokens per split at least
+
+// ---------------------------------------------------------------- outlier channels
+// energy[j] += Σ_rows x_j² over this block's rows, in double.
+template <typename TIn>
+__global__ void channel_energy_kernel(const TIn* __restrict__ x, int64_t n_rows, int64_t stride, int d,
+                                      int64_t rows_per_block, double* __restrict__ energy) {
+    const int j = threadIdx.x;
+    const int64_t r0 = (int64_t)blockIdx.x * rows_per_block;
+    const int64_t r1 = r0 + rows_per_block < n_rows ? r0 + rows_per_block : n_rows;
+    if (j >= d) return;
+    double e = 0.0;
+    for (int64_t r = r0; r < r1; ++r) {
+        const double v = load_elem(x + r * stride + j);
+        e = fma(v, v, e);
+    }
+    atomicAdd(energy + j, e);
+}
+
+// One block of d threads: the d_o channels of largest energy (ties to the lower
+// index) in ascending order, then the others in ascending order.
+__global__ void outlier_perm_kernel(const double* __restrict__ energy, int d, int d_o, int32_t* __restrict__ perm) {
+    __shared__ double e[kMaxD];
+    __shared__ int is_out[kMaxD];
+    const int j = threadIdx.x;
+    if (j < d) e[j] = energy[j];
+    __syncthreads();
+    int rank = 0;
+    if (j < d)
+        for (int k = 0; k < d; ++k) rank += (e[k] > e[j] || (e[k] == e[j] && k < j)) ? 1 : 0;
+    if (j < d) is_out[j] = rank < d_o;
+    __syncthreads();
+    if (j < d) {
+        int before = 0;  // channels of the same class below j
+        for (int k = 0; k < j; ++k) before += is_out[k] == is_out[j] ? 1 : 0;
+        perm[is_out[j] ? before : d_o + before] = j;
+    }
+}
+
+// ---------------------------------------------------------------- decode
+// One part of a split row: its handle's tables and its planes.
+struct Part {
+    const uint8_t* codes;
+    const uint8_t* signs;
+    const float* norm;
+    const float* rnorm;
+    Codebook cb;
+    int b;         // b_m
+    int d;         // channels of the part
+    float gamma;   // √(π/2)/d_part
+};
+
+struct MixedArgs {
+    Part k[2], v[2];         // [0] outlier part, [1] the rest
+    int kdo, vdo;            // d_o of the key and value splits
+    const int32_t* seq_lens;
+    const float* qr;         // [B·Hq][D] rotated query parts, key-permuted positions
+    const float* qs;         // same for S·q (prod keys)
+    float* pm;
+    float* pl;
+    float* pacc;
+    float* pacc2;
+    float* scores;
+    float scale;
+    int B, Hq, Hkv, T_max, G, n_splits, chunk, n_hblocks;
+};
+
+// q′ (and q″ for prod keys) of each key part: position j of part p is
+// Σ_i Π_p[jl][i]·q[perm[off_p + i]] with jl = j − off_p.
+template <int D, typename TQ>
+__global__ void mixed_query_prep_kernel(const TQ* __restrict__ q, const int32_t* __restrict__ perm, int kdo,
+                                        const float* __restrict__ PiT0, const float* __restrict__ ST0,
+                                        const float* __restrict__ PiT1, const float* __restrict__ ST1, int kprod,
+                                        int Hq, float* __restrict__ qr, float* __restrict__ qs, int* __restrict__ status) {
+    __shared__ float qv[D];
+    const int h = blockIdx.x, b = blockIdx.y, j = threadIdx.x;
+    const size_t base = ((size_t)b * Hq + h) * D;
+    ChannelMap cm;
+    cm.ch = perm;
+    cm.d_full = D;
+    cm.status = status;
+    qv[j] = load_elem(q + base + channel_of(cm, j));  // qv in key-permuted order
+    __syncthreads();
+    const bool p0 = j < kdo;
+    const int off = p0 ? 0 : kdo, dp = p0 ? kdo : D - kdo, jl = j - off;
+    const float* PiT = p0 ? PiT0 : PiT1;
+    const float* ST = p0 ? ST0 : ST1;
+    float a = 0.f, c = 0.f;
+    for (int i = 0; i < dp; ++i) {
+        a = fmaf(__ldg(PiT + (size_t)i * dp + jl), qv[off + i], a);
+        if (kprod) c = fmaf(__ldg(ST + (size_t)i * dp + jl), qv[off + i], c);
+    }
+    qr[base + j] = a;
+    if (kprod) qs[base + j] = c;
+}
+
+// Split-K flash decoding over token chunks for two-part keys and values: per
+// (token chunk, KV head, block of ≤ kMaxGroup query heads) an online softmax and
+// per-part value sums, written as one partial (m, l, acc[, acc2]) per head.
+template <int D, bool KPROD, bool VPROD>
+__global__ void __launch_bounds__(kWarps * 32)
+mixed_split_kernel(const MixedArgs a) {
+    constexpr int PER = D / 32;
+    extern __shared__ float sm[];
+    const int hb = blockIdx.y % a.n_hblocks, kvh = blockIdx.y / a.n_hblocks;
+    const int G = min(kMaxGroup, a.G - hb * kMaxGroup);
+    float* qr = sm;                                   // [G][D]
+    float* qs = qr + G * D;                           // [G][D]
+    float* acc = qs + G * D;                          // [warps][G][D]
+    float* acc2 = acc + kWarps * G * D;               // [warps][G][D] (prod values)
+    float* wm = acc2 + (VPROD ? kWarps * G * D : 0);  // [warps][G]
+    float* wl = wm + kWarps * G;                      // [warps][G]
+    __shared__ float cent[4][kMaxLevels];             // key part 0, 1, value part 0, 1
+
+    const int split = blockIdx.x, b = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int L = a.seq_lens[b];
+    L = L < 0 ? 0 : (L > a.T_max ? a.T_max : L);
+    const int t0 = split * a.chunk;
+    const int t1 = min(t0 + a.chunk, L);
+    const size_t head0 = (size_t)b * a.Hq + (size_t)kvh * a.G + (size_t)hb * kMaxGroup;
+
+    for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
+        qr[i] = a.qr[head0 * D + i];
+        if (KPROD) qs[i] = a.qs[head0 * D + i];
+    }
+    for (int i = threadIdx.x; i < kWarps * G * D; i += blockDim.x) {
+        acc[i] = 0.f;
+        if (VPROD) acc2[i] = 0.f;
+    }
+    if (threadIdx.x < kMaxLevels) {
+        const int i = threadIdx.x;
+        cent[0][i] = a.k[0].cb.c[i];
+        cent[1][i] = a.k[1].cb.c[i];
+        cent[2][i] = a.v[0].cb.c[i];
+        cent[3][i] = a.v[1].cb.c[i];
+    }
+    __syncthreads();
+
+    float m_[kMaxGroup], l_[kMaxGroup];
+#pragma unroll
+    for (int h = 0; h < kMaxGroup; ++h) {
+        m_[h] = -INFINITY;
+        l_[h] = 0.f;
+    }
+    float* myacc = acc + warp * G * D;
+    float* myacc2 = acc2 + warp * G * D;
+    // record sizes of the four parts' planes
+    const int kcb0 = a.k[0].b * a.k[0].d / 8, kcb1 = a.k[1].b * a.k[1].d / 8;
+    const int vcb0 = a.v[0].b * a.v[0].d / 8, vcb1 = a.v[1].b * a.v[1].d / 8;
+
+    for (int t = t0 + warp; t < t1; t += kWarps) {
+        const int64_t row = ((int64_t)b * a.Hkv + kvh) * a.T_max + t;
+        float ck[PER], zk[PER], cv[PER], zv[PER];
+#pragma unroll
+        for (int m = 0; m < PER; ++m) {
+            // keys: slot m belongs to part 0 when it lies below d_o
+            {
+                const bool o = 32 * m < a.kdo;
+                const int jl = lane + 32 * m - (o ? 0 : a.kdo);
+                const int bp = o ? a.k[0].b : a.k[1].b;
+                const uint8_t* cp = o ? a.k[0].codes + row * kcb0 : a.k[1].codes + row * kcb1;
+                ck[m] = bp > 0 ? cent[o ? 0 : 1][read_code(reinterpret_cast<const uint32_t*>(cp), jl, bp)] : 0.f;
+                if (KPROD) {
+                    const uint8_t* sp = o ? a.k[0].signs + row * (a.k[0].d / 8) : a.k[1].signs + row * (a.k[1].d / 8);
+                    const uint32_t sw = reinterpret_cast<const uint32_t*>(sp)[jl >> 5];
+                    zk[m] = ((sw >> lane) & 1u) ? 1.f : -1.f;
+                }
+            }
+            {
+                const bool o = 32 * m < a.vdo;
+                const int jl = lane + 32 * m - (o ? 0 : a.vdo);
+                const int bp = o ? a.v[0].b : a.v[1].b;
+                const uint8_t* cp = o ? a.v[0].codes + row * vcb0 : a.v[1].codes + row * vcb1;
+                cv[m] = bp > 0 ? cent[o ? 2 : 3][read_code(reinterpret_cast<const uint32_t*>(cp), jl, bp)] : 0.f;
+                if (VPROD) {
+                    const uint8_t* sp = o ? a.v[0].signs + row * (a.v[0].d / 8) : a.v[1].signs + row * (a.v[1].d / 8);
+                    const uint32_t sw = reinterpret_cast<const uint32_t*>(sp)[jl >> 5];
+                    zv[m] = ((sw >> lane) & 1u) ? 1.f : -1.f;
+                }
+            }
+        }
+        const float kn0 = a.k[0].norm[row], kn1 = a.k[1].norm[row];
+        const float krn0 = KPROD ? a.k[0].gamma * a.k[0].rnorm[row] : 0.f;
+        const float krn1 = KPROD ? a.k[1].gamma * a.k[1].rnorm[row] : 0.f;
+        const float vn0 = a.v[0].norm[row], vn1 = a.v[1].norm[row];
+        const float vrn0 = VPROD ? a.v[0].gamma * a.v[0].rnorm[row] : 0.f;
+        const float vrn1 = VPROD ? a.v[1].gamma * a.v[1].rnorm[row] : 0.f;
+
+        for (int h = 0; h < G; ++h) {
+            // this lane's share of Σ_parts ‖k_p‖·(⟨q′_p, c_p⟩ + γ_p‖r_p‖⟨q″_p, z_p⟩)
+            float part = 0.f;
+#pragma unroll
+            for (int m = 0; m < PER; ++m) {
+                const bool o = 32 * m < a.kdo;
+                float v = qr[h * D + lane + 32 * m] * ck[m];
+                if (KPROD) v = fmaf(o ? krn0 : krn1, qs[h * D + lane + 32 * m] * zk[m], v);
+                part = fmaf(o ? kn0 : kn1, v, part);
+            }
+            const float s = a.scale * warp_sum(part);
+            if (a.scores != nullptr && lane == 0) a.scores[(head0 + h) * a.T_max + t] = s;
+            float mh = m_[0], lh = l_[0];
+#pragma unroll
+            for (int k = 1; k < kMaxGroup; ++k)
+                if (k == h) { mh = m_[k]; lh = l_[k]; }
+            const float mn = fmaxf(mh, s);
+            const float corr = __expf(mh - mn);
+            const float p = __expf(s - mn);
+            lh = fmaf(lh, corr, p);
+#pragma unroll
+            for (int k = 0; k < kMaxGroup; ++k)
+                if (k == h) { m_[k] = mn; l_[k] = lh; }
+#pragma unroll
+            for (int m = 0; m < PER; ++m) {
+                const bool o = 32 * m < a.vdo;
+                const float pv = p * (o ? vn0 : vn1);
+                float* r = myacc + h * D + lane + 32 * m;
+                *r = fmaf(*r, corr, pv * cv[m]);
+                if (VPROD) {
+                    float* r2 = myacc2 + h * D + lane + 32 * m;
+                    *r2 = fmaf(*r2, corr, pv * (o ? vrn0 : vrn1) * zv[m]);
+                }
+            }
+        }
+    }
+    if (lane == 0)
+        for (int h = 0; h < G; ++h) {
+            float mh = m_[0], lh = l_[0];
+#pragma unroll
+            for (int k = 1; k < kMaxGroup; ++k)
+                if (k == h) { mh = m_[k]; lh = l_[k]; }
+            wm[warp * G + h] = mh;
+            wl[warp * G + h] = lh;
+        }
+    __syncthreads();
+
+    // combine the warps of this split and write its partial state
+    for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
+        const int h = i / D;
+        float M = -INFINITY;
+        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wm[w * G + h]);
+        float o = 0.f, o2 = 0.f, l = 0.f;
+        if (M != -INFINITY) {
+            for (int w = 0; w < kWarps; ++w) {
+                const float f = __expf(wm[w * G + h] - M);
+                o = fmaf(f, acc[w * G * D + i], o);
+                if (VPROD) o2 = fmaf(f, acc2[w * G * D + i], o2);
+                l = fmaf(f, wl[w * G + h], l);
+            }
+        }
+        const size_t ps = (head0 + h) * a.n_splits + split;
+        a.pacc[ps * D + (i % D)] = o;
+        if (VPROD) a.pacc2[ps * D + (i % D)] = o2;
+        if (i % D == 0) {
+            a.pm[ps] = M;
+            a.pl[ps] = l;
+        }
+    }
+}
+
+// Combine the splits of one head, rotate each value part back (out = Π_pᵀ·acc_p/l
+// + S_pᵀ·acc2_p/l) and scatter it to its channels.
+template <int D, bool VPROD>
+__global__ void mixed_merge_kernel(const float* __restrict__ pm, const float* __restrict__ pl,
+                                   const float* __restrict__ pacc, const float* __restrict__ pacc2,
+                                   const float* __restrict__ Pi0, const float* __restrict__ S0,
+                                   const float* __restrict__ Pi1, const float* __restrict__ S1, int vdo,
+                                   const int32_t* __restrict__ perm_v, int Hq, int n_splits, float* __restrict__ out,
+                                   int* __restrict__ status) {
+    __shared__ float o1[D], o2[D];
+    const int h = blockIdx.x, b = blockIdx.y, j = threadIdx.x;
+    const size_t head = (size_t)b * Hq + h;
+    float M = -INFINITY;
+    for (int s = 0; s < n_splits; ++s) M = fmaxf(M, pm[head * n_splits + s]);
+    float a = 0.f, c = 0.f, l = 0.f;
+    if (M != -INFINITY) {
+        for (int s = 0; s < n_splits; ++s) {
+            const size_t ps = head * n_splits + s;
+            const float f = __expf(pm[ps] - M);
+            l = fmaf(f, pl[ps], l);
+            a = fmaf(f, pacc[ps * D + j], a);
+            if (VPROD) c = fmaf(f, pacc2[ps * D + j], c);
+        }
+    }
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    o1[j] = a * inv;
+    o2[j] = c * inv;
+    __syncthreads();
+    const bool p0 = j < vdo;
+    const int off = p0 ? 0 : vdo, dp = p0 ? vdo : D - vdo, jl = j - off;
+    const float* Pi = p0 ? Pi0 : Pi1;
+    const float* S = p0 ? S0 : S1;
+    float r = 0.f;
+    for (int k = 0; k < dp; ++k) {
+        r = fmaf(__ldg(Pi + (size_t)k * dp + jl), o1[off + k], r);
+        if (VPROD) r = fmaf(__ldg(S + (size_t)k * dp + jl), o2[off + k], r);
+    }
+    ChannelMap cm;
+    cm.ch = perm_v;
+    cm.d_full = D;
+    cm.status = status;
+    out[head * D + channel_of(cm, j)] = r;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct MixedLayout {
+    size_t qr, qs, pm, pl, pacc, pacc2, total;
+};
+
+MixedLayout mixed_layout(int B, int Hq, int d, int n_splits, bool vprod) {
+    MixedLayout w;
+    const size_t heads = (size_t)B * Hq;
+    size_t off = 0;
+    w.qr = off;
+    off = align256(off + heads * d * 4);
+    w.qs = off;
+    off = align256(off + heads * d * 4);
+    w.pm = off;
+    off = align256(off + heads * n_splits * 4);
+    w.pl = off;
+    off = align256(off + heads * n_splits * 4);
+    w.pacc = off;
+    off = align256(off + heads * n_splits * d * 4);
+    w.pacc2 = off;
+    if (vprod) off = align256(off + heads * n_splits * d * 4);
+    w.total = off > 0 ? off : 256;
+    return w;
+}
+
+void fill_part(Part* p, const tq_ctx& h, const tq_planes& pl) {
+    p->codes = pl.codes;
+    p->signs = pl.signs;
+    p->norm = pl.norm;
+    p->rnorm = pl.rnorm;
+    p->cb = h.cb;
+    p->b = h.hp.b_mse;
+    p->d = h.hp.d;
+    p->gamma = h.gamma;
+}
+
+template <int D>
+int launch_mixed_d(const MixedDecode& m, const MixedShape& p, cudaStream_t s) {
+    const bool kprod = m.hk[0]->hp.variant == TQ_PROD, vprod = m.hv[0]->hp.variant == TQ_PROD;
+    const MixedLayout w = mixed_layout(p.B, p.Hq, D, p.n_splits, vprod);
+    char* ws = static_cast<char*>(m.workspace);
+    MixedArgs a;
+    for (int i = 0; i < 2; ++i) {
+        fill_part(&a.k[i], *m.hk[i], m.kc[i]);
+        fill_part(&a.v[i], *m.hv[i], m.vc[i]);
+    }
+    a.kdo = m.hk[0]->hp.d;
+    a.vdo = m.hv[0]->hp.d;
+    a.seq_lens = m.seq_lens;
+    float* qr = reinterpret_cast<float*>(ws + w.qr);
+    float* qs = reinterpret_cast<float*>(ws + w.qs);
+    a.qr = qr;
+    a.qs = qs;
+    a.pm = reinterpret_cast<float*>(ws + w.pm);
+    a.pl = reinterpret_cast<float*>(ws + w.pl);
+    a.pacc = reinterpret_cast<float*>(ws + w.pacc);
+    a.pacc2 = reinterpret_cast<float*>(ws + w.pacc2);
+    a.scores = m.scores;
+    a.scale = m.scale;
+    a.B = p.B; a.Hq = p.Hq; a.Hkv = p.Hkv; a.T_max = p.T_max; a.G = p.G;
+    a.n_splits = p.n_splits; a.chunk = p.chunk;
+    a.n_hblocks = (p.G + kMaxGroup - 1) / kMaxGroup;
+    int* status = m.hk[0]->dp.status;
+    const dim3 pg(p.Hq, p.B);
+    const tq_ctx& k0 = *m.hk[0];
+    const tq_ctx& k1 = *m.hk[1];
+    if (m.q_dtype == TQ_F32)
+        mixed_query_prep_kernel<D, float><<<pg, D, 0, s>>>(static_cast<const float*>(m.q), m.perm_k, a.kdo, k0.dp.PiT,
+                                                           k0.dp.ST, k1.dp.PiT, k1.dp.ST, kprod, p.Hq, qr, qs, status);
+    else
+        mixed_query_prep_kernel<D, __nv_bfloat16><<<pg, D, 0, s>>>(static_cast<const __nv_bfloat16*>(m.q), m.perm_k,
+                                                                   a.kdo, k0.dp.PiT, k0.dp.ST, k1.dp.PiT, k1.dp.ST,
+                                                                   kprod, p.Hq, qr, qs, status);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "mixed query prep launch");
+
+    const int gmax = p.G < kMaxGroup ? p.G : kMaxGroup;
+    const size_t smem = sizeof(float) * ((size_t)gmax * D * (2 + kWarps * (vprod ? 2 : 1)) + 2 * kWarps * gmax);
+    const dim3 sg(p.n_splits, p.Hkv * a.n_hblocks, p.B);
+#define TQ_MSPLIT(KP, VP)                                                                        \
+    do {                                                                                         \
+        auto fn = mixed_split_kernel<D, KP, VP>;                                                 \
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);   \
+        if (e != cudaSuccess) return cuda_fail(e, "mixed decode smem attribute");               \
+        fn<<<sg, kWarps * 32, smem, s>>>(a);                                                     \
+    } while (0)
+    if (kprod && vprod) TQ_MSPLIT(true, true);
+    else if (kprod) TQ_MSPLIT(true, false);
+    else if (vprod) TQ_MSPLIT(false, true);
+    else TQ_MSPLIT(false, false);
+#undef TQ_MSPLIT
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "mixed decode split launch");
+    const tq_ctx& v0 = *m.hv[0];
+    const tq_ctx& v1 = *m.hv[1];
+    if (vprod)
+        mixed_merge_kernel<D, true><<<pg, D, 0, s>>>(a.pm, a.pl, a.pacc, a.pacc2, v0.dp.Pi, v0.dp.S, v1.dp.Pi, v1.dp.S,
+                                                     a.vdo, m.perm_v, p.Hq, p.n_splits, m.out, status);
+    else
+        mixed_merge_kernel<D, false><<<pg, D, 0, s>>>(a.pm, a.pl, a.pacc, a.pacc2, v0.dp.Pi, v0.dp.S, v1.dp.Pi,
+                                                      v1.dp.S, a.vdo, m.perm_v, p.Hq, p.n_splits, m.out, status);
+    e = cudaGetLastError();
+    return e == cudaSuccess ? TQ_OK : cuda_fail(e, "mixed decode merge launch");
+}
+
+}  // namespace
+
+int mixed_plan(int d, int sms, bool vprod, int B, int Hq, int Hkv, int T_max, MixedShape* plan, size_t* ws_bytes) {
+    if (B < 0 || Hq < 0 || Hkv <= 0 || T_max < 0) return fail(TQ_EINVAL, "negative or zero shape");
+    if (Hq % Hkv != 0) return fail(TQ_EINVAL, "Hq=%d is not a multiple of Hkv=%d", Hq, Hkv);
+    if (Hq > 4096) return fail(TQ_EUNSUPPORTED, "Hq=%d > 4096", Hq);
+    if ((int64_t)B * Hkv * T_max > (int64_t)1 << 40) return fail(TQ_EINVAL, "cache too large");
+    MixedShape p;
+    p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.T_max = T_max; p.d = d; p.G = Hq / Hkv;
+    const int64_t units = (int64_t)(B > 0 ? B : 1) * Hkv * ((p.G + kMaxGroup - 1) / kMaxGroup);
+    int64_t want = (2 * (int64_t)(sms > 0 ? sms : 148) + units - 1) / units;  // two CTAs per SM
+    int64_t max_splits = (T_max + kMinChunk - 1) / kMinChunk;
+    if (max_splits < 1) max_splits = 1;
+    if (want > max_splits) want = max_splits;
+    if (want < 1) want = 1;
+    int64_t chunk = (T_max + want - 1) / want;
+    chunk = (chunk + kMinChunk - 1) / kMinChunk * kMinChunk;
+    if (chunk < kMinChunk) chunk = kMinChunk;
+    p.chunk = (int)chunk;
+    p.n_splits = (int)((T_max + chunk - 1) / chunk);
+    if (p.n_splits < 1) p.n_splits = 1;
+    *plan = p;
+    *ws_bytes = mixed_layout(B, Hq, d, p.n_splits, vprod).total;
+    return TQ_OK;
+}
+
+int launch_mixed_decode(const MixedDecode& m, const MixedShape& p, cudaStream_t s) {
+    switch (p.d) {
+        case 64: return launch_mixed_d<64>(m, p, s);
+        case 96: return launch_mixed_d<96>(m, p, s);
+        case 128: return launch_mixed_d<128>(m, p, s);
+        case 160: return launch_mixed_d<160>(m, p, s);
+        case 192: return launch_mixed_d<192>(m, p, s);
+        case 224: return launch_mixed_d<224>(m, p, s);
+        case 256: return launch_mixed_d<256>(m, p, s);
+        default: return fail(TQ_EUNSUPPORTED, "mixed d=%d", p.d);
+    }
+}
+
+int launch_select_outlier_channels(const void* x, int x_dtype, int64_t n_rows, int64_t stride, int d, int d_o,
+                                   double* energy, int32_t* perm, cudaStream_t s) {
+    cudaError_t e = cudaMemsetAsync(energy, 0, (size_t)d * sizeof(double), s);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the channel energies");
+    if (n_rows > 0) {
+        const int64_t per = 256;
+        int64_t blocks = (n_rows + per - 1) / per;
+        if (blocks > 0x7fffffffLL) return fail(TQ_EINVAL, "n_rows too large");
+        if (x_dtype == TQ_F32)
+            channel_energy_kernel<float><<<(unsigned)blocks, d, 0, s>>>(static_cast<const float*>(x), n_rows, stride,
+                                                                         d, per, energy);
+        else
+            channel_energy_kernel<__nv_bfloat16><<<(unsigned)blocks, d, 0, s>>>(
+                static_cast<const __nv_bfloat16*>(x), n_rows, stride, d, per, energy);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail(e, "channel energy launch");
+    }
+    outlier_perm_kernel<<<1, d, 0, s>>>(energy, d, d_o, perm);
+    e = cudaGetLastError();
+    return e == cudaSuccess ? TQ_OK : cuda_fail(e, "outlier channel launch");
+}
+
+}  // namespace tq

@@ -16,7 +16,7 @@ __global__ void __launch_bounds__(kWarps * 32)
 quantize_rows_kernel(const TIn* __restrict__ x, int64_t n_rows, int64_t stride,
                      const float* __restrict__ PiT, const float* __restrict__ TT, Codebook cb,
                      int b_m, uint8_t* __restrict__ codes, uint8_t* __restrict__ signs,
-                     float* __restrict__ norm_out, float* __restrict__ rnorm_out) {
+                     float* __restrict__ norm_out, float* __restrict__ rnorm_out, ChannelMap cm) {
     constexpr int PER = D / 32;
     __shared__ float xs[kWarps][D];
     __shared__ uint32_t words[kWarps][D * 4 / 32];
@@ -28,7 +28,7 @@ quantize_rows_kernel(const TIn* __restrict__ x, int64_t n_rows, int64_t stride,
     float ss = 0.f;
 #pragma unroll
     for (int m = 0; m < PER; ++m) {
-        float v = load_elem(xr + lane + 32 * m);
+        float v = load_elem(xr + channel_of(cm, lane + 32 * m));
         xs[warp][lane + 32 * m] = v;
         ss = fmaf(v, v, ss);
     }
@@ -99,7 +99,7 @@ quantize_rows_kernel(const TIn* __restrict__ x, int64_t n_rows, int64_t stride,
 
 template <int D>
 int launch_d(const tq_ctx& h, const void* x, int x_dtype, int64_t n_rows, int64_t stride,
-             const tq_planes& out, cudaStream_t s) {
+             const tq_planes& out, cudaStream_t s, ChannelMap cm = ChannelMap()) {
     const int64_t blocks = (n_rows + kWarps - 1) / kWarps;
     if (blocks > 0x7fffffffLL) return fail(TQ_EINVAL, "n_rows too large");
     dim3 grid((unsigned)blocks), block(kWarps * 32);
@@ -108,24 +108,42 @@ int launch_d(const tq_ctx& h, const void* x, int x_dtype, int64_t n_rows, int64_
         auto xp = static_cast<const __nv_bfloat16*>(x);
         if (prod)
             quantize_rows_kernel<D, true><<<grid, block, 0, s>>>(xp, n_rows, stride, h.dp.PiT, h.dp.TT, h.cb, h.hp.b_mse,
-                                                                 out.codes, out.signs, out.norm, out.rnorm);
+                                                                 out.codes, out.signs, out.norm, out.rnorm, cm);
         else
             quantize_rows_kernel<D, false><<<grid, block, 0, s>>>(xp, n_rows, stride, h.dp.PiT, h.dp.TT, h.cb, h.hp.b_mse,
-                                                                  out.codes, out.signs, out.norm, out.rnorm);
+                                                                  out.codes, out.signs, out.norm, out.rnorm, cm);
     } else {
         auto xp = static_cast<const float*>(x);
         if (prod)
             quantize_rows_kernel<D, true><<<grid, block, 0, s>>>(xp, n_rows, stride, h.dp.PiT, h.dp.TT, h.cb, h.hp.b_mse,
-                                                                 out.codes, out.signs, out.norm, out.rnorm);
+                                                                 out.codes, out.signs, out.norm, out.rnorm, cm);
         else
             quantize_rows_kernel<D, false><<<grid, block, 0, s>>>(xp, n_rows, stride, h.dp.PiT, h.dp.TT, h.cb, h.hp.b_mse,
-                                                                  out.codes, out.signs, out.norm, out.rnorm);
+                                                                  out.codes, out.signs, out.norm, out.rnorm, cm);
     }
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? TQ_OK : cuda_fail(e, "quantize launch");
 }
 
 }  // namespace
+
+int launch_quantize_part(const tq_ctx& h, const void* x, int x_dtype, int64_t n_rows, int64_t stride,
+                         const int32_t* ch, int d_full, const tq_planes& out, cudaStream_t s) {
+    ChannelMap cm;
+    cm.ch = ch;
+    cm.d_full = d_full;
+    cm.status = h.dp.status;
+    switch (h.hp.d) {
+        case 32: return launch_d<32>(h, x, x_dtype, n_rows, stride, out, s, cm);
+        case 64: return launch_d<64>(h, x, x_dtype, n_rows, stride, out, s, cm);
+        case 96: return launch_d<96>(h, x, x_dtype, n_rows, stride, out, s, cm);
+        case 128: return launch_d<128>(h, x, x_dtype, n_rows, stride, out, s, cm);
+        case 160: return launch_d<160>(h, x, x_dtype, n_rows, stride, out, s, cm);
+        case 192: return launch_d<192>(h, x, x_dtype, n_rows, stride, out, s, cm);
+        case 224: return launch_d<224>(h, x, x_dtype, n_rows, stride, out, s, cm);
+        default: return fail(TQ_EUNSUPPORTED, "part d=%d", h.hp.d);
+    }
+}
 
 int launch_quantize(const tq_ctx& h, const void* x, int x_dtype, int64_t n_rows, int64_t stride,
                     const tq_planes& out, cudaStream_t s) {

@@ -1,0 +1,161 @@
+"""Outlier-channel mixed precision vs the oracle (needs a GPU).
+
+The page's experiments keep 32 "outlier" channels at 3 bits and the other 96 at
+2 bits.  Each part is an ordinary quantizer of its own dimension over a channel
+permutation; attention sums the parts' scores.  Checked against the oracle's
+mixed_* functions: channel selection, both parts' codes, the scattered
+dequantization, attention outputs and scores, and a bad permutation entry
+turned into a status code.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import synthetic
+from _parity import check_attention, check_dequant, check_quantize, f64, oracle_params, planes_to_oracle_rows
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tq():
+    import kv_cache_vector_18_b300 as m
+    return m
+
+
+def _hot_rows(n, d, hot, seed, dtype="bf16"):
+    X = synthetic.gaussian((n, d), seed=seed, dtype="f32")
+    X[:, torch.as_tensor(hot)] *= 6.0
+    return X.to(torch.bfloat16) if dtype == "bf16" else X
+
+
+def _mixed_params(mq):
+    return O.MixedParams(oracle_params(mq.qo), oracle_params(mq.qn), mq.perm.cpu().numpy())
+
+
+@pytest.mark.parametrize("d,d_o", [(128, 32), (64, 32), (256, 64)])
+def test_outlier_channel_selection(tq, d, d_o):
+    hot = np.random.default_rng(d).choice(d, d_o, replace=False)
+    X = _hot_rows(3000, d, hot, seed=d)
+    perm, energy = tq.select_outlier_channels(X.cuda(), d_o)
+    torch.cuda.synchronize()
+    Xf = f64(X)
+    assert np.allclose(energy.cpu().numpy(), np.sum(Xf * Xf, axis=0), rtol=1e-12)
+    assert np.array_equal(perm.cpu().numpy(), O.outlier_channel_perm(Xf, d_o))
+    assert np.array_equal(perm.cpu().numpy()[:d_o], np.sort(hot))
+
+
+@pytest.mark.parametrize("variant,bo,bn", [("mse", 3, 2), ("mse", 4, 3), ("prod", 3, 2), ("prod", 4, 3)])
+def test_mixed_quantize_dequantize(tq, variant, bo, bn):
+    d, d_o, n = 128, 32, 1500
+    hot = np.random.default_rng(1).choice(d, d_o, replace=False)
+    X = _hot_rows(n, d, hot, seed=2)
+    perm, _ = tq.select_outlier_channels(X.cuda(), d_o)
+    mq = tq.MixedQuantizer(perm, d_o, bo, bn, variant, seed_o=5, seed_n=6)
+    planes = mq.quantize(X.cuda())
+    y = mq.dequantize(planes)
+    torch.cuda.synchronize()
+    assert mq.qo.device_status() == 0 and mq.qn.device_status() == 0
+    mp = _mixed_params(mq)
+    Xf = f64(X)
+    check_quantize(mp.po, Xf[:, mp.out], planes["o"])
+    check_quantize(mp.pn, Xf[:, mp.rest], planes["n"])
+    ro = planes_to_oracle_rows(mp.po, planes["o"])
+    rn = planes_to_oracle_rows(mp.pn, planes["n"])
+    ref = O.mixed_dequantize(mp, ro, rn)
+    rel = np.linalg.norm(f64(y) - ref, axis=1) / np.linalg.norm(ref, axis=1)
+    assert rel.max() <= 1e-4, rel.max()
+    # each part on its own equals the single-part path on the gathered sub-rows
+    sub = X.cuda()[:, perm[:d_o].long()].contiguous()
+    alone = mq.qo.quantize(sub)
+    torch.cuda.synchronize()
+    check_dequant(mp.po, alone, mq.qo.dequantize(alone))
+
+
+def test_mixed_fp32_strided_input(tq):
+    d, d_o = 128, 32
+    perm = torch.as_tensor(np.random.default_rng(3).permutation(d), dtype=torch.int32, device="cuda")
+    base = synthetic.gaussian((700, 256), seed=9, dtype="f32").cuda()
+    x = base[:, 32:160]
+    mq = tq.MixedQuantizer(perm, d_o, 3, 2, "mse", seed_o=1, seed_n=2)
+    planes = mq.quantize(x)
+    torch.cuda.synchronize()
+    mp = _mixed_params(mq)
+    Xf = f64(x)
+    check_quantize(mp.po, Xf[:, mp.out], planes["o"])
+    check_quantize(mp.pn, Xf[:, mp.rest], planes["n"])
+
+
+@pytest.mark.parametrize("d,kdo,vdo,kv,kb,vv,vb", [
+    (128, 32, 32, "mse", (3, 2), "mse", (3, 2)),
+    (128, 32, 64, "prod", (4, 3), "mse", (3, 2)),
+    (128, 64, 32, "prod", (3, 2), "prod", (4, 3)),
+    (64, 32, 32, "mse", (4, 2), "mse", (3, 2)),
+    (256, 64, 96, "mse", (3, 2), "prod", (3, 3)),
+])
+def test_mixed_decode_attention(tq, d, kdo, vdo, kv, kb, vv, vb):
+    B, Hq, Hkv, T = 2, 8, 2, 333
+    lens = [333, 120]
+    rng = np.random.default_rng(d + kdo + vdo)
+    hot_k = rng.choice(d, kdo, replace=False)
+    hot_v = rng.choice(d, vdo, replace=False)
+    K = _hot_rows(B * Hkv * T, d, hot_k, seed=11)
+    V = _hot_rows(B * Hkv * T, d, hot_v, seed=12)
+    q = synthetic.gaussian((B, Hq, d), seed=13)
+    pk, _ = tq.select_outlier_channels(K.cuda(), kdo)
+    pv, _ = tq.select_outlier_channels(V.cuda(), vdo)
+    mk = tq.MixedQuantizer(pk, kdo, kb[0], kb[1], kv, seed_o=21, seed_n=22)
+    mv = tq.MixedQuantizer(pv, vdo, vb[0], vb[1], vv, seed_o=23, seed_n=24)
+    kc, vc = mk.quantize(K.cuda()), mv.quantize(V.cuda())
+    sl = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    out, sc = tq.mixed_decode_attention(mk, mv, q.cuda(), kc, vc, sl, Hkv, T, return_scores=True)
+    torch.cuda.synchronize()
+    assert mk.qo.device_status() == 0
+    a, b = _mixed_params(mk), _mixed_params(mv)
+    ref, ref_sc = O.mixed_decode_attention(
+        a, b, f64(q), planes_to_oracle_rows(a.po, kc["o"]), planes_to_oracle_rows(a.pn, kc["n"]),
+        planes_to_oracle_rows(b.po, vc["o"]), planes_to_oracle_rows(b.pn, vc["n"]), lens, Hkv, T)
+    check_attention(f64(out), ref)
+    g = f64(sc)
+    mask = ~np.isnan(ref_sc)
+    assert np.max(np.abs(g[mask] - ref_sc[mask])) <= 1e-3 * max(1.0, np.max(np.abs(ref_sc[mask])))
+
+
+def test_bad_channel_entry_is_flagged(tq):
+    from kv_cache_vector_18_b300 import _lib
+    d, d_o = 128, 32
+    perm = torch.arange(d, dtype=torch.int32, device="cuda")
+    perm[40] = 1000  # outside [0, d): read as channel 0, flagged, never dereferenced
+    mq = tq.MixedQuantizer(perm, d_o, 3, 2, "mse", seed_o=1, seed_n=2)
+    x = synthetic.gaussian((64, d), seed=1).cuda()
+    mq.quantize(x)
+    torch.cuda.synchronize()
+    assert mq.qo.device_status() == 0
+    assert mq.qn.device_status(clear=True) == _lib.TQ_STATUS_BAD_CHANNEL
+    assert mq.qn.device_status() == 0
+
+
+def test_mixed_rejects_bad_arguments(tq):
+    from kv_cache_vector_18_b300 import _lib
+    L = _lib.lib()
+    perm = torch.arange(128, dtype=torch.int32, device="cuda")
+    a = tq.Quantizer(32, 3, "mse", seed=1)
+    b = tq.Quantizer(96, 2, "prod", seed=2)
+    x = torch.zeros((8, 128), dtype=torch.bfloat16, device="cuda")
+    P = tq.Quantizer.planes_struct
+    pa, pb = a.empty_planes(8), b.empty_planes(8)
+    # parts of different variants
+    assert L.tq_mixed_quantize(a.handle, b.handle, perm.data_ptr(), x.data_ptr(), 0, 8, 128, P(pa), P(pb),
+                               None) == _lib.TQ_EINVAL
+    c = tq.Quantizer(96, 2, "mse", seed=2)
+    pc = c.empty_planes(8)
+    # row stride below d
+    assert L.tq_mixed_quantize(a.handle, c.handle, perm.data_ptr(), x.data_ptr(), 0, 8, 64, P(pa), P(pc),
+                               None) == _lib.TQ_EINVAL
+    assert L.tq_mixed_quantize(a.handle, c.handle, None, x.data_ptr(), 0, 8, 128, P(pa), P(pc),
+                               None) == _lib.TQ_EINVAL
+    e = torch.empty(128, dtype=torch.float64, device="cuda")
+    assert L.tq_select_outlier_channels(x.data_ptr(), 0, 8, 128, 128, 100, e.data_ptr(), perm.data_ptr(),
+                                        None) == _lib.TQ_EINVAL
+    torch.cuda.synchronize()
