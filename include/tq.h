@@ -214,15 +214,25 @@ int tq_decode_attention(tq_handle hk, tq_handle hv, const void* q, int q_dtype,
 int tq_select_outlier_channels(const void* x, int x_dtype, int64_t n_rows, int64_t x_row_stride, int d,
                                int d_o, double* energy, int32_t* perm, void* stream);
 
+/* Bytes of the scratch buffer that lets tq_mixed_quantize use the tensor cores. */
+size_t tq_mixed_quantize_scratch_bytes(void);
+
 /*
  * tq_mixed_quantize — part o of row i (channels perm[0..d_o)) quantized by ho into
  * record i of out_o, part n (channels perm[d_o..d)) by hn into out_n, exactly as
  * tq_quantize would quantize the gathered sub-rows.  x: device [n_rows, d], row
  * stride x_row_stride ≥ d elements (stride·element size a multiple of 16 bytes).
+ * scratch: NULL, or a caller-owned device buffer of scratch_bytes bytes, 256-byte
+ * aligned.  With at least tq_mixed_quantize_scratch_bytes() of it, bf16 rows,
+ * mse parts, d = 128 and d_o ∈ {32, 64} (b_o ≥ b_n), both parts come out of one
+ * tensor-core rotation by M = blockdiag(Π_o, Π_n)·P, whose bf16 halves are built
+ * in the scratch on `stream`; otherwise a CUDA-core kernel per part gathers the
+ * part's channels itself.  The scratch must not be shared by calls that may run
+ * concurrently.
  */
 int tq_mixed_quantize(tq_handle ho, tq_handle hn, const int32_t* perm, const void* x, int x_dtype,
                       int64_t n_rows, int64_t x_row_stride, tq_planes out_o, tq_planes out_n,
-                      void* stream);
+                      void* scratch, size_t scratch_bytes, void* stream);
 
 /*
  * tq_mixed_dequantize — both parts dequantized (as tq_dequantize) and written to

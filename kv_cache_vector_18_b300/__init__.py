@@ -240,6 +240,9 @@ class MixedQuantizer:
         self.qo = Quantizer(d_o, bits_o, variant, seed=seed_o, rotation=rotation)
         self.qn = Quantizer(self.d - d_o, bits_n, variant, seed=seed_n, rotation=rotation)
         self.d_o, self.variant = d_o, variant
+        # scratch for the combined rotation operand of the tensor-core path
+        self.scratch = torch.empty(_lib.lib().tq_mixed_quantize_scratch_bytes(), dtype=torch.uint8,
+                                   device=self.perm.device)
 
     def empty_planes(self, n_rows: int) -> dict:
         return {"o": self.qo.empty_planes(n_rows), "n": self.qn.empty_planes(n_rows)}
@@ -251,7 +254,8 @@ class MixedQuantizer:
         out = out if out is not None else self.empty_planes(n)
         check(_lib.lib().tq_mixed_quantize(self.qo.handle, self.qn.handle, _ptr(self.perm), _ptr(x),
                                            _DTYPES[x.dtype], n, x.stride(0), Quantizer.planes_struct(out["o"]),
-                                           Quantizer.planes_struct(out["n"]), _stream(stream)))
+                                           Quantizer.planes_struct(out["n"]), _ptr(self.scratch), self.scratch.numel(),
+                                           _stream(stream)))
         return out
 
     def dequantize(self, planes: dict, dtype=torch.float32, stream=None) -> torch.Tensor:

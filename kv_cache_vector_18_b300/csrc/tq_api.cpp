@@ -500,8 +500,11 @@ int validate_split(tq_handle ho, tq_handle hn, const char* what) {
 }
 }  // namespace
 
+size_t tq_mixed_quantize_scratch_bytes(void) { return mixed_tc_scratch_bytes(); }
+
 int tq_mixed_quantize(tq_handle ho, tq_handle hn, const int32_t* perm, const void* x, int x_dtype, int64_t n_rows,
-                      int64_t x_row_stride, tq_planes out_o, tq_planes out_n, void* stream) {
+                      int64_t x_row_stride, tq_planes out_o, tq_planes out_n, void* scratch, size_t scratch_bytes,
+                      void* stream) {
     int rc = validate_split(ho, hn, "quantizer");
     if (rc != TQ_OK) return rc;
     if (n_rows < 0) return fail(TQ_EINVAL, "n_rows=%lld is negative", (long long)n_rows);
@@ -515,7 +518,10 @@ int tq_mixed_quantize(tq_handle ho, tq_handle hn, const int32_t* perm, const voi
     if ((rc = check_device_ptr(x, "x", true)) != TQ_OK) return rc;
     if ((rc = check_planes(*ho, out_o, "out_o")) != TQ_OK) return rc;
     if ((rc = check_planes(*hn, out_n, "out_n")) != TQ_OK) return rc;
+    if ((rc = check_device_ptr(scratch, "scratch", false)) != TQ_OK) return rc;
     const cudaStream_t s = (cudaStream_t)stream;
+    if (mixed_quantize_tc_supported(*ho, *hn, x_dtype, n_rows, x_row_stride, scratch, scratch_bytes))
+        return launch_mixed_quantize_tc(*ho, *hn, perm, x, n_rows, x_row_stride, out_o, out_n, scratch, s);
     rc = launch_quantize_part(*ho, x, x_dtype, n_rows, x_row_stride, perm, d, out_o, s);
     if (rc == TQ_OK) rc = launch_quantize_part(*hn, x, x_dtype, n_rows, x_row_stride, perm + ho->hp.d, d, out_n, s);
     return rc;

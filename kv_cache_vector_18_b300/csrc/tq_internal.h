@@ -121,6 +121,14 @@ int launch_quantize_part(const tq_ctx& h, const void* x, int x_dtype, int64_t n_
                          const int32_t* ch, int d_full, const tq_planes& out, cudaStream_t s);
 int launch_dequantize_part(const tq_ctx& h, const tq_planes& in, int64_t n_rows, const int32_t* ch, int d_full,
                            void* y, int y_dtype, cudaStream_t s);
+// Tensor-core mixed quantize (tq_mixed_tc.cu): bf16 rows, mse parts, d = 128,
+// d_o ∈ {32, 64}; scratch holds the combined rotation operand (hi and lo).
+size_t mixed_tc_scratch_bytes();
+bool mixed_quantize_tc_supported(const tq_ctx& ho, const tq_ctx& hn, int x_dtype, int64_t n_rows, int64_t stride,
+                                 const void* scratch, size_t scratch_bytes);
+int launch_mixed_quantize_tc(const tq_ctx& ho, const tq_ctx& hn, const int32_t* perm, const void* x, int64_t n_rows,
+                             int64_t stride, const tq_planes& out_o, const tq_planes& out_n, void* scratch,
+                             cudaStream_t s);
 struct MixedShape {
     int B = 0, Hq = 0, Hkv = 0, T_max = 0, d = 0, G = 0, n_splits = 1, chunk = 64;
 };

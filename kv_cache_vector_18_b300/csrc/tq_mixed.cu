@@ -18,6 +18,8 @@ namespace tq {
 namespace {
 
 constexpr int kWarps = 4;      // warps per split CTA
+// query heads per split CTA: their queries and value sums are held in registers
+__host__ __device__ constexpr int heads_per_cta(int d) { return d <= 128 ? 8 : 4; }
 constexpr int kMinChunk = 64;  // tokens per split at least
 
 // ---------------------------------------------------------------- outlier channels
@@ -106,7 +108,8 @@ __global__ void mixed_query_prep_kernel(const TQ* __restrict__ q, const int32_t*
     const float* PiT = p0 ? PiT0 : PiT1;
     const float* ST = p0 ? ST0 : ST1;
     float a = 0.f, c = 0.f;
-    for (int i = 0; i < dp; ++i) {
+#pragma unroll 16
+    for (int i = 0; i < dp; ++i) {  // unrolled so that the matrix loads go out in batches
         a = fmaf(__ldg(PiT + (size_t)i * dp + jl), qv[off + i], a);
         if (kprod) c = fmaf(__ldg(ST + (size_t)i * dp + jl), qv[off + i], c);
     }
@@ -115,21 +118,22 @@ __global__ void mixed_query_prep_kernel(const TQ* __restrict__ q, const int32_t*
 }
 
 // Split-K flash decoding over token chunks for two-part keys and values: per
-// (token chunk, KV head, block of ≤ kMaxGroup query heads) an online softmax and
-// per-part value sums, written as one partial (m, l, acc[, acc2]) per head.
+// (token chunk, KV head, block of kHB query heads) an online softmax and per-part
+// value sums, written as one partial (m, l, acc[, acc2]) per head.  The block's
+// q′ (and for prod keys q″) and value sums live in registers; a group smaller
+// than kHB pads with zero queries whose results are not written.
 template <int D, bool KPROD, bool VPROD>
-__global__ void __launch_bounds__(kWarps * 32)
+__global__ void __launch_bounds__(kWarps * 32, 3)
 mixed_split_kernel(const MixedArgs a) {
     constexpr int PER = D / 32;
+    constexpr int kHB = heads_per_cta(D);
     extern __shared__ float sm[];
     const int hb = blockIdx.y % a.n_hblocks, kvh = blockIdx.y / a.n_hblocks;
-    const int G = min(kMaxGroup, a.G - hb * kMaxGroup);
-    float* qr = sm;                                   // [G][D]
-    float* qs = qr + G * D;                           // [G][D]
-    float* acc = qs + G * D;                          // [warps][G][D]
-    float* acc2 = acc + kWarps * G * D;               // [warps][G][D] (prod values)
-    float* wm = acc2 + (VPROD ? kWarps * G * D : 0);  // [warps][G]
-    float* wl = wm + kWarps * G;                      // [warps][G]
+    const int G = min(kHB, a.G - hb * kHB);           // live heads of this block
+    float* wacc = sm;                                 // [warps][kHB][D] value sums at the end
+    float* acc2 = wacc + kWarps * kHB * D;            // [warps][kHB][D] (prod values)
+    float* wm = acc2 + (VPROD ? kWarps * kHB * D : 0);  // [warps][kHB]
+    float* wl = wm + kWarps * kHB;                    // [warps][kHB]
     __shared__ float cent[4][kMaxLevels];             // key part 0, 1, value part 0, 1
 
     const int split = blockIdx.x, b = blockIdx.z;
@@ -138,16 +142,10 @@ mixed_split_kernel(const MixedArgs a) {
     L = L < 0 ? 0 : (L > a.T_max ? a.T_max : L);
     const int t0 = split * a.chunk;
     const int t1 = min(t0 + a.chunk, L);
-    const size_t head0 = (size_t)b * a.Hq + (size_t)kvh * a.G + (size_t)hb * kMaxGroup;
+    const size_t head0 = (size_t)b * a.Hq + (size_t)kvh * a.G + (size_t)hb * kHB;
 
-    for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
-        qr[i] = a.qr[head0 * D + i];
-        if (KPROD) qs[i] = a.qs[head0 * D + i];
-    }
-    for (int i = threadIdx.x; i < kWarps * G * D; i += blockDim.x) {
-        acc[i] = 0.f;
-        if (VPROD) acc2[i] = 0.f;
-    }
+    if (VPROD)
+        for (int i = threadIdx.x; i < kWarps * kHB * D; i += blockDim.x) acc2[i] = 0.f;
     if (threadIdx.x < kMaxLevels) {
         const int i = threadIdx.x;
         cent[0][i] = a.k[0].cb.c[i];
@@ -155,16 +153,21 @@ mixed_split_kernel(const MixedArgs a) {
         cent[2][i] = a.v[0].cb.c[i];
         cent[3][i] = a.v[1].cb.c[i];
     }
-    __syncthreads();
-
-    float m_[kMaxGroup], l_[kMaxGroup];
+    float q1[kHB][PER], q2[KPROD ? kHB : 1][PER], acc[kHB][PER], m_[kHB], l_[kHB];
 #pragma unroll
-    for (int h = 0; h < kMaxGroup; ++h) {
+    for (int h = 0; h < kHB; ++h) {
         m_[h] = -INFINITY;
         l_[h] = 0.f;
+#pragma unroll
+        for (int m = 0; m < PER; ++m) {
+            const bool live = h < G;
+            q1[h][m] = live ? a.qr[(head0 + h) * D + lane + 32 * m] : 0.f;
+            if (KPROD) q2[h][m] = live ? a.qs[(head0 + h) * D + lane + 32 * m] : 0.f;
+            acc[h][m] = 0.f;
+        }
     }
-    float* myacc = acc + warp * G * D;
-    float* myacc2 = acc2 + warp * G * D;
+    __syncthreads();
+    float* myacc2 = acc2 + warp * kHB * D;
     // record sizes of the four parts' planes
     const int kcb0 = a.k[0].b * a.k[0].d / 8, kcb1 = a.k[1].b * a.k[1].d / 8;
     const int vcb0 = a.v[0].b * a.v[0].d / 8, vcb1 = a.v[1].b * a.v[1].d / 8;
@@ -206,72 +209,87 @@ mixed_split_kernel(const MixedArgs a) {
         const float vn0 = a.v[0].norm[row], vn1 = a.v[1].norm[row];
         const float vrn0 = VPROD ? a.v[0].gamma * a.v[0].rnorm[row] : 0.f;
         const float vrn1 = VPROD ? a.v[1].gamma * a.v[1].rnorm[row] : 0.f;
-
-        for (int h = 0; h < G; ++h) {
-            // this lane's share of Σ_parts ‖k_p‖·(⟨q′_p, c_p⟩ + γ_p‖r_p‖⟨q″_p, z_p⟩)
-            float part = 0.f;
+        // the key's per-slot factors: ‖k_p‖·c and ‖k_p‖·γ_p‖r_p‖·z
+        float fk[PER], gk[PER];
+#pragma unroll
+        for (int m = 0; m < PER; ++m) {
+            const bool o = 32 * m < a.kdo;
+            fk[m] = (o ? kn0 : kn1) * ck[m];
+            if (KPROD) gk[m] = (o ? kn0 * krn0 : kn1 * krn1) * zk[m];
+        }
+        // every head's score: lane shares, then all heads reduced together
+        float part[kHB];
+#pragma unroll
+        for (int h = 0; h < kHB; ++h) {
+            float s = 0.f;
 #pragma unroll
             for (int m = 0; m < PER; ++m) {
-                const bool o = 32 * m < a.kdo;
-                float v = qr[h * D + lane + 32 * m] * ck[m];
-                if (KPROD) v = fmaf(o ? krn0 : krn1, qs[h * D + lane + 32 * m] * zk[m], v);
-                part = fmaf(o ? kn0 : kn1, v, part);
+                s = fmaf(q1[h][m], fk[m], s);
+                if (KPROD) s = fmaf(q2[h][m], gk[m], s);
             }
-            const float s = a.scale * warp_sum(part);
-            if (a.scores != nullptr && lane == 0) a.scores[(head0 + h) * a.T_max + t] = s;
-            float mh = m_[0], lh = l_[0];
+            part[h] = s;
+        }
 #pragma unroll
-            for (int k = 1; k < kMaxGroup; ++k)
-                if (k == h) { mh = m_[k]; lh = l_[k]; }
-            const float mn = fmaxf(mh, s);
-            const float corr = __expf(mh - mn);
+        for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+            for (int h = 0; h < kHB; ++h) part[h] += __shfl_xor_sync(0xffffffffu, part[h], off);
+        // the value's per-slot factors ‖v_p‖·c and ‖v_p‖·γ_p‖r_p‖·z
+        float fv[PER], gv[PER];
+#pragma unroll
+        for (int m = 0; m < PER; ++m) {
+            const bool o = 32 * m < a.vdo;
+            fv[m] = (o ? vn0 : vn1) * cv[m];
+            if (VPROD) gv[m] = (o ? vn0 * vrn0 : vn1 * vrn1) * zv[m];
+        }
+#pragma unroll
+        for (int h = 0; h < kHB; ++h) {
+            const float s = a.scale * part[h];
+            if (a.scores != nullptr && lane == 0 && h < G) a.scores[(head0 + h) * a.T_max + t] = s;
+            // online softmax (all lanes hold identical values)
+            const float mn = fmaxf(m_[h], s);
+            const float corr = __expf(m_[h] - mn);
             const float p = __expf(s - mn);
-            lh = fmaf(lh, corr, p);
-#pragma unroll
-            for (int k = 0; k < kMaxGroup; ++k)
-                if (k == h) { m_[k] = mn; l_[k] = lh; }
+            l_[h] = fmaf(l_[h], corr, p);
+            m_[h] = mn;
 #pragma unroll
             for (int m = 0; m < PER; ++m) {
-                const bool o = 32 * m < a.vdo;
-                const float pv = p * (o ? vn0 : vn1);
-                float* r = myacc + h * D + lane + 32 * m;
-                *r = fmaf(*r, corr, pv * cv[m]);
+                acc[h][m] = fmaf(acc[h][m], corr, p * fv[m]);
                 if (VPROD) {
                     float* r2 = myacc2 + h * D + lane + 32 * m;
-                    *r2 = fmaf(*r2, corr, pv * (o ? vrn0 : vrn1) * zv[m]);
+                    *r2 = fmaf(*r2, corr, p * gv[m]);
                 }
             }
         }
     }
-    if (lane == 0)
-        for (int h = 0; h < G; ++h) {
-            float mh = m_[0], lh = l_[0];
 #pragma unroll
-            for (int k = 1; k < kMaxGroup; ++k)
-                if (k == h) { mh = m_[k]; lh = l_[k]; }
-            wm[warp * G + h] = mh;
-            wl[warp * G + h] = lh;
+    for (int h = 0; h < kHB; ++h) {
+#pragma unroll
+        for (int m = 0; m < PER; ++m) wacc[(warp * kHB + h) * D + lane + 32 * m] = acc[h][m];
+        if (lane == 0) {
+            wm[warp * kHB + h] = m_[h];
+            wl[warp * kHB + h] = l_[h];
         }
+    }
     __syncthreads();
 
-    // combine the warps of this split and write its partial state
+    // combine the warps of this split and write its partial state (live heads only)
     for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
-        const int h = i / D;
+        const int h = i / D, j = i % D;
         float M = -INFINITY;
-        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wm[w * G + h]);
+        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wm[w * kHB + h]);
         float o = 0.f, o2 = 0.f, l = 0.f;
         if (M != -INFINITY) {
             for (int w = 0; w < kWarps; ++w) {
-                const float f = __expf(wm[w * G + h] - M);
-                o = fmaf(f, acc[w * G * D + i], o);
-                if (VPROD) o2 = fmaf(f, acc2[w * G * D + i], o2);
-                l = fmaf(f, wl[w * G + h], l);
+                const float f = __expf(wm[w * kHB + h] - M);
+                o = fmaf(f, wacc[(w * kHB + h) * D + j], o);
+                if (VPROD) o2 = fmaf(f, acc2[(w * kHB + h) * D + j], o2);
+                l = fmaf(f, wl[w * kHB + h], l);
             }
         }
         const size_t ps = (head0 + h) * a.n_splits + split;
-        a.pacc[ps * D + (i % D)] = o;
-        if (VPROD) a.pacc2[ps * D + (i % D)] = o2;
-        if (i % D == 0) {
+        a.pacc[ps * D + j] = o;
+        if (VPROD) a.pacc2[ps * D + j] = o2;
+        if (j == 0) {
             a.pm[ps] = M;
             a.pl[ps] = l;
         }
@@ -291,9 +309,11 @@ __global__ void mixed_merge_kernel(const float* __restrict__ pm, const float* __
     const int h = blockIdx.x, b = blockIdx.y, j = threadIdx.x;
     const size_t head = (size_t)b * Hq + h;
     float M = -INFINITY;
+#pragma unroll 16
     for (int s = 0; s < n_splits; ++s) M = fmaxf(M, pm[head * n_splits + s]);
     float a = 0.f, c = 0.f, l = 0.f;
     if (M != -INFINITY) {
+#pragma unroll 8
         for (int s = 0; s < n_splits; ++s) {
             const size_t ps = head * n_splits + s;
             const float f = __expf(pm[ps] - M);
@@ -311,6 +331,7 @@ __global__ void mixed_merge_kernel(const float* __restrict__ pm, const float* __
     const float* Pi = p0 ? Pi0 : Pi1;
     const float* S = p0 ? S0 : S1;
     float r = 0.f;
+#pragma unroll 16
     for (int k = 0; k < dp; ++k) {
         r = fmaf(__ldg(Pi + (size_t)k * dp + jl), o1[off + k], r);
         if (VPROD) r = fmaf(__ldg(S + (size_t)k * dp + jl), o2[off + k], r);
@@ -384,7 +405,8 @@ int launch_mixed_d(const MixedDecode& m, const MixedShape& p, cudaStream_t s) {
     a.scale = m.scale;
     a.B = p.B; a.Hq = p.Hq; a.Hkv = p.Hkv; a.T_max = p.T_max; a.G = p.G;
     a.n_splits = p.n_splits; a.chunk = p.chunk;
-    a.n_hblocks = (p.G + kMaxGroup - 1) / kMaxGroup;
+    constexpr int kHB = heads_per_cta(D);
+    a.n_hblocks = (p.G + kHB - 1) / kHB;
     int* status = m.hk[0]->dp.status;
     const dim3 pg(p.Hq, p.B);
     const tq_ctx& k0 = *m.hk[0];
@@ -399,8 +421,7 @@ int launch_mixed_d(const MixedDecode& m, const MixedShape& p, cudaStream_t s) {
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "mixed query prep launch");
 
-    const int gmax = p.G < kMaxGroup ? p.G : kMaxGroup;
-    const size_t smem = sizeof(float) * ((size_t)gmax * D * (2 + kWarps * (vprod ? 2 : 1)) + 2 * kWarps * gmax);
+    const size_t smem = sizeof(float) * ((size_t)kWarps * kHB * D * (vprod ? 2 : 1) + 2 * kWarps * kHB);
     const dim3 sg(p.n_splits, p.Hkv * a.n_hblocks, p.B);
 #define TQ_MSPLIT(KP, VP)                                                                        \
     do {                                                                                         \
@@ -437,8 +458,10 @@ int mixed_plan(int d, int sms, bool vprod, int B, int Hq, int Hkv, int T_max, Mi
     if ((int64_t)B * Hkv * T_max > (int64_t)1 << 40) return fail(TQ_EINVAL, "cache too large");
     MixedShape p;
     p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.T_max = T_max; p.d = d; p.G = Hq / Hkv;
-    const int64_t units = (int64_t)(B > 0 ? B : 1) * Hkv * ((p.G + kMaxGroup - 1) / kMaxGroup);
-    int64_t want = (2 * (int64_t)(sms > 0 ? sms : 148) + units - 1) / units;  // two CTAs per SM
+    const int hb = heads_per_cta(d);
+    const int64_t units = (int64_t)(B > 0 ? B : 1) * Hkv * ((p.G + hb - 1) / hb);
+    // two waves of three 4-warp CTAs per SM
+    int64_t want = (6 * (int64_t)(sms > 0 ? sms : 148) + units - 1) / units;
     int64_t max_splits = (T_max + kMinChunk - 1) / kMinChunk;
     if (max_splits < 1) max_splits = 1;
     if (want > max_splits) want = max_splits;

@@ -73,6 +73,41 @@ def test_mixed_quantize_dequantize(tq, variant, bo, bn):
     check_dequant(mp.po, alone, mq.qo.dequantize(alone))
 
 
+@pytest.mark.parametrize("d_o,bo,bn", [(32, 3, 2), (64, 4, 2), (32, 2, 2), (64, 3, 1)])
+def test_mixed_tensor_core_and_cuda_core_paths(tq, d_o, bo, bn):
+    # bf16 mse rows at d = 128 take the tensor-core path when a scratch is given and
+    # the per-part CUDA-core path without one; both against the oracle, over enough
+    # rows for several tiles per SM, a ragged tail, and rows with one part all zero
+    from kv_cache_vector_18_b300 import _lib
+    d, n = 128, 148 * 128 * 2 + 77
+    hot = np.random.default_rng(d_o + bo).choice(d, d_o, replace=False)
+    X = _hot_rows(n, d, hot, seed=bo * 10 + bn)
+    perm, _ = tq.select_outlier_channels(X.cuda(), d_o)
+    hot_sorted = perm[:d_o].long().cpu()
+    X[5, hot_sorted] = 0                        # outlier part zero
+    rest = torch.as_tensor(np.setdiff1d(np.arange(d), hot_sorted.numpy()))
+    X[n - 3, rest] = 0                          # other part zero
+    X[n - 1] = 0                                # whole row zero
+    mq = tq.MixedQuantizer(perm, d_o, bo, bn, "mse", seed_o=41, seed_n=42)
+    xd = X.cuda()
+    tc = mq.quantize(xd)
+    cc = mq.empty_planes(n)
+    P = tq.Quantizer.planes_struct
+    assert _lib.lib().tq_mixed_quantize(mq.qo.handle, mq.qn.handle, mq.perm.data_ptr(), xd.data_ptr(), 0, n, d,
+                                        P(cc["o"]), P(cc["n"]), None, 0, None) == 0
+    torch.cuda.synchronize()
+    assert mq.qo.device_status() == 0 and mq.qn.device_status() == 0
+    mp = _mixed_params(mq)
+    Xf = f64(X)
+    rows = np.unique(np.concatenate([np.arange(300), np.arange(n - 300, n),
+                                     np.random.default_rng(2).choice(n, 3000, replace=False)]))
+    for planes in (tc, cc):
+        check_quantize(mp.po, Xf[:, mp.out], planes["o"], rows=rows)
+        check_quantize(mp.pn, Xf[:, mp.rest], planes["n"], rows=rows)
+    assert float(tc["o"]["norm"][5]) == 0 and float(tc["n"]["norm"][n - 3]) == 0
+    assert not tc["o"]["codes"][5].any() and not tc["n"]["codes"][n - 1].any()
+
+
 def test_mixed_fp32_strided_input(tq):
     d, d_o = 128, 32
     perm = torch.as_tensor(np.random.default_rng(3).permutation(d), dtype=torch.int32, device="cuda")
@@ -147,14 +182,14 @@ def test_mixed_rejects_bad_arguments(tq):
     pa, pb = a.empty_planes(8), b.empty_planes(8)
     # parts of different variants
     assert L.tq_mixed_quantize(a.handle, b.handle, perm.data_ptr(), x.data_ptr(), 0, 8, 128, P(pa), P(pb),
-                               None) == _lib.TQ_EINVAL
+                               None, 0, None) == _lib.TQ_EINVAL
     c = tq.Quantizer(96, 2, "mse", seed=2)
     pc = c.empty_planes(8)
     # row stride below d
     assert L.tq_mixed_quantize(a.handle, c.handle, perm.data_ptr(), x.data_ptr(), 0, 8, 64, P(pa), P(pc),
-                               None) == _lib.TQ_EINVAL
+                               None, 0, None) == _lib.TQ_EINVAL
     assert L.tq_mixed_quantize(a.handle, c.handle, None, x.data_ptr(), 0, 8, 128, P(pa), P(pc),
-                               None) == _lib.TQ_EINVAL
+                               None, 0, None) == _lib.TQ_EINVAL
     e = torch.empty(128, dtype=torch.float64, device="cuda")
     assert L.tq_select_outlier_channels(x.data_ptr(), 0, 8, 128, 128, 100, e.data_ptr(), perm.data_ptr(),
                                         None) == _lib.TQ_EINVAL
