@@ -103,3 +103,26 @@ def test_host_hadamard_rejects_bad_arguments(lib):
     assert lib.tq_build_params_host(64, 2, 0, 5, a.ctypes.data_as(dp), None, None, None) == _lib.TQ_OK
     assert lib.tq_build_params_host_ex(64, 2, 0, _lib.TQ_ROT_QR, 5, b.ctypes.data_as(dp), None, None, None) == _lib.TQ_OK
     assert np.array_equal(a, b)
+
+
+def test_new_entry_points_reject_bad_arguments_on_the_host(lib):
+    # argument checks run before any CUDA call, so they hold without a GPU
+    from kv_cache_vector_18_b300 import _lib
+    h = ctypes.c_void_p()
+    assert lib.tq_init_ex(128, 3, 0, 7, 0, ctypes.byref(h)) == _lib.TQ_EINVAL       # unknown rotation
+    assert lib.tq_init_ex(96, 3, 0, _lib.TQ_ROT_HADAMARD, 0, ctypes.byref(h)) == _lib.TQ_EUNSUPPORTED
+    assert not h.value
+    assert lib.tq_check_wait_timeout(None, 99, 1000, None) == _lib.TQ_EINVAL
+    assert lib.tq_select_outlier_channels(None, 0, 10, 128, 48, 32, None, None, None) == _lib.TQ_EUNSUPPORTED
+    assert lib.tq_select_outlier_channels(None, 0, 10, 128, 128, 40, None, None, None) == _lib.TQ_EINVAL
+    assert lib.tq_select_outlier_channels(None, 0, 10, 128, 128, 128, None, None, None) == _lib.TQ_EINVAL
+    assert lib.tq_select_outlier_channels(None, 5, 10, 128, 128, 32, None, None, None) == _lib.TQ_EINVAL
+    P = _lib.Planes()
+    assert lib.tq_mixed_quantize(None, None, None, None, 0, 8, 128, P, P, None, 0, None) == _lib.TQ_EINVAL
+    assert lib.tq_mixed_dequantize(None, None, None, P, P, 8, None, 0, None) == _lib.TQ_EINVAL
+    n = ctypes.c_size_t()
+    assert lib.tq_mixed_decode_workspace_bytes(None, None, None, None, 1, 8, 1, 16, ctypes.byref(n)) == _lib.TQ_EINVAL
+    assert lib.tq_decode_append_attention(None, None, None, 0, None, None, 0, P, P, None, 1, 8, 1, 16, 0.0, None,
+                                          None, 0, None) == _lib.TQ_EINVAL
+    assert lib.tq_mixed_quantize_scratch_bytes() == 2 * 128 * 128 * 2
+    assert len(lib.tq_last_error()) > 0
