@@ -123,7 +123,7 @@ __global__ void mixed_query_prep_kernel(const TQ* __restrict__ q, const int32_t*
 // q′ (and for prod keys q″) and value sums live in registers; a group smaller
 // than kHB pads with zero queries whose results are not written.
 template <int D, bool KPROD, bool VPROD>
-__global__ void __launch_bounds__(kWarps * 32, 3)
+__global__ void __launch_bounds__(kWarps * 32, 2)
 mixed_split_kernel(const MixedArgs a) {
     constexpr int PER = D / 32;
     constexpr int kHB = heads_per_cta(D);
@@ -172,43 +172,87 @@ mixed_split_kernel(const MixedArgs a) {
     const int kcb0 = a.k[0].b * a.k[0].d / 8, kcb1 = a.k[1].b * a.k[1].d / 8;
     const int vcb0 = a.v[0].b * a.v[0].d / 8, vcb1 = a.v[1].b * a.v[1].d / 8;
 
-    for (int t = t0 + warp; t < t1; t += kWarps) {
-        const int64_t row = ((int64_t)b * a.Hkv + kvh) * a.T_max + t;
-        float ck[PER], zk[PER], cv[PER], zv[PER];
+    // A token's raw words: for each slot the code word(s) holding its lane's code
+    // and the sign word, for keys and values, and the parts' norms.  The next
+    // token's are loaded while the current one is computed.
+    uint32_t kw[PER][2], ks[PER], vw[PER][2], vs[PER];
+    float nr[8];
+    auto load_raw = [&](int64_t row) {
 #pragma unroll
         for (int m = 0; m < PER; ++m) {
-            // keys: slot m belongs to part 0 when it lies below d_o
             {
                 const bool o = 32 * m < a.kdo;
                 const int jl = lane + 32 * m - (o ? 0 : a.kdo);
                 const int bp = o ? a.k[0].b : a.k[1].b;
-                const uint8_t* cp = o ? a.k[0].codes + row * kcb0 : a.k[1].codes + row * kcb1;
-                ck[m] = bp > 0 ? cent[o ? 0 : 1][read_code(reinterpret_cast<const uint32_t*>(cp), jl, bp)] : 0.f;
+                kw[m][0] = kw[m][1] = 0u;
+                if (bp > 0) {
+                    const uint32_t* w = reinterpret_cast<const uint32_t*>(o ? a.k[0].codes + row * kcb0
+                                                                            : a.k[1].codes + row * kcb1);
+                    const int bit = jl * bp;
+                    kw[m][0] = w[bit >> 5];
+                    if ((bit & 31) + bp > 32) kw[m][1] = w[(bit >> 5) + 1];
+                }
                 if (KPROD) {
                     const uint8_t* sp = o ? a.k[0].signs + row * (a.k[0].d / 8) : a.k[1].signs + row * (a.k[1].d / 8);
-                    const uint32_t sw = reinterpret_cast<const uint32_t*>(sp)[jl >> 5];
-                    zk[m] = ((sw >> lane) & 1u) ? 1.f : -1.f;
+                    ks[m] = reinterpret_cast<const uint32_t*>(sp)[jl >> 5];
                 }
             }
             {
                 const bool o = 32 * m < a.vdo;
                 const int jl = lane + 32 * m - (o ? 0 : a.vdo);
                 const int bp = o ? a.v[0].b : a.v[1].b;
-                const uint8_t* cp = o ? a.v[0].codes + row * vcb0 : a.v[1].codes + row * vcb1;
-                cv[m] = bp > 0 ? cent[o ? 2 : 3][read_code(reinterpret_cast<const uint32_t*>(cp), jl, bp)] : 0.f;
+                vw[m][0] = vw[m][1] = 0u;
+                if (bp > 0) {
+                    const uint32_t* w = reinterpret_cast<const uint32_t*>(o ? a.v[0].codes + row * vcb0
+                                                                            : a.v[1].codes + row * vcb1);
+                    const int bit = jl * bp;
+                    vw[m][0] = w[bit >> 5];
+                    if ((bit & 31) + bp > 32) vw[m][1] = w[(bit >> 5) + 1];
+                }
                 if (VPROD) {
                     const uint8_t* sp = o ? a.v[0].signs + row * (a.v[0].d / 8) : a.v[1].signs + row * (a.v[1].d / 8);
-                    const uint32_t sw = reinterpret_cast<const uint32_t*>(sp)[jl >> 5];
-                    zv[m] = ((sw >> lane) & 1u) ? 1.f : -1.f;
+                    vs[m] = reinterpret_cast<const uint32_t*>(sp)[jl >> 5];
                 }
             }
         }
-        const float kn0 = a.k[0].norm[row], kn1 = a.k[1].norm[row];
-        const float krn0 = KPROD ? a.k[0].gamma * a.k[0].rnorm[row] : 0.f;
-        const float krn1 = KPROD ? a.k[1].gamma * a.k[1].rnorm[row] : 0.f;
-        const float vn0 = a.v[0].norm[row], vn1 = a.v[1].norm[row];
-        const float vrn0 = VPROD ? a.v[0].gamma * a.v[0].rnorm[row] : 0.f;
-        const float vrn1 = VPROD ? a.v[1].gamma * a.v[1].rnorm[row] : 0.f;
+        nr[0] = a.k[0].norm[row];
+        nr[1] = a.k[1].norm[row];
+        nr[2] = a.v[0].norm[row];
+        nr[3] = a.v[1].norm[row];
+        nr[4] = KPROD ? a.k[0].rnorm[row] : 0.f;
+        nr[5] = KPROD ? a.k[1].rnorm[row] : 0.f;
+        nr[6] = VPROD ? a.v[0].rnorm[row] : 0.f;
+        nr[7] = VPROD ? a.v[1].rnorm[row] : 0.f;
+    };
+    const int64_t slab = ((int64_t)b * a.Hkv + kvh) * a.T_max;
+    if (t0 + warp < t1) load_raw(slab + t0 + warp);
+
+    for (int t = t0 + warp; t < t1; t += kWarps) {
+        float ck[PER], zk[PER], cv[PER], zv[PER];
+#pragma unroll
+        for (int m = 0; m < PER; ++m) {
+            {
+                const bool o = 32 * m < a.kdo;
+                const int jl = lane + 32 * m - (o ? 0 : a.kdo);
+                const int bp = o ? a.k[0].b : a.k[1].b;
+                const int code = (int)(__funnelshift_r(kw[m][0], kw[m][1], (jl * bp) & 31) & ((1u << bp) - 1u));
+                ck[m] = bp > 0 ? cent[o ? 0 : 1][code] : 0.f;
+                if (KPROD) zk[m] = ((ks[m] >> lane) & 1u) ? 1.f : -1.f;
+            }
+            {
+                const bool o = 32 * m < a.vdo;
+                const int jl = lane + 32 * m - (o ? 0 : a.vdo);
+                const int bp = o ? a.v[0].b : a.v[1].b;
+                const int code = (int)(__funnelshift_r(vw[m][0], vw[m][1], (jl * bp) & 31) & ((1u << bp) - 1u));
+                cv[m] = bp > 0 ? cent[o ? 2 : 3][code] : 0.f;
+                if (VPROD) zv[m] = ((vs[m] >> lane) & 1u) ? 1.f : -1.f;
+            }
+        }
+        const float kn0 = nr[0], kn1 = nr[1], vn0 = nr[2], vn1 = nr[3];
+        const float krn0 = a.k[0].gamma * nr[4], krn1 = a.k[1].gamma * nr[5];
+        const float vrn0 = a.v[0].gamma * nr[6], vrn1 = a.v[1].gamma * nr[7];
+        // the next token's words are in flight while this one is computed
+        if (t + kWarps < t1) load_raw(slab + t + kWarps);
         // the key's per-slot factors: ‖k_p‖·c and ‖k_p‖·γ_p‖r_p‖·z
         float fk[PER], gk[PER];
 #pragma unroll
@@ -460,8 +504,8 @@ int mixed_plan(int d, int sms, bool vprod, int B, int Hq, int Hkv, int T_max, Mi
     p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.T_max = T_max; p.d = d; p.G = Hq / Hkv;
     const int hb = heads_per_cta(d);
     const int64_t units = (int64_t)(B > 0 ? B : 1) * Hkv * ((p.G + hb - 1) / hb);
-    // two waves of three 4-warp CTAs per SM
-    int64_t want = (6 * (int64_t)(sms > 0 ? sms : 148) + units - 1) / units;
+    // two waves of two resident 4-warp CTAs per SM
+    int64_t want = (4 * (int64_t)(sms > 0 ? sms : 148) + units - 1) / units;
     int64_t max_splits = (T_max + kMinChunk - 1) / kMinChunk;
     if (max_splits < 1) max_splits = 1;
     if (want > max_splits) want = max_splits;
