@@ -126,3 +126,21 @@ def test_new_entry_points_reject_bad_arguments_on_the_host(lib):
                                           None, 0, None) == _lib.TQ_EINVAL
     assert lib.tq_mixed_quantize_scratch_bytes() == 2 * 128 * 128 * 2
     assert len(lib.tq_last_error()) > 0
+
+
+def test_binding_constants_match_the_header():
+    from kv_cache_vector_18_b300 import _lib
+    text = open(os.path.join(ROOT, "include", "tq.h")).read()
+    defines = {m.group(1): int(m.group(2))
+               for m in re.finditer(r"^#define\s+(TQ_\w+)\s+\(?(-?\d+)\)?\s*(?:/\*.*)?$", text, flags=re.M)}
+    assert {"TQ_OK", "TQ_EWORKSPACE", "TQ_STATUS_APPEND_FULL", "TQ_STATUS_BAD_CHANNEL"} <= set(defines)
+    for name, value in defines.items():
+        assert getattr(_lib, name) == value, name
+    assert "#define TQ_NOALLOC_WORKSPACE_BYTES (4u << 20)" in text and _lib.NOALLOC_WORKSPACE_BYTES == 4 << 20
+    enums = {}
+    for body in re.findall(r"enum\s*\{([^}]*)\}", text):
+        for name, value in re.findall(r"(TQ_\w+)\s*=\s*(\d+)", body):
+            enums[name] = int(value)
+    assert {"TQ_MSE", "TQ_PROD", "TQ_BF16", "TQ_F32", "TQ_ROT_QR", "TQ_ROT_HADAMARD"} <= set(enums)
+    for name, value in enums.items():
+        assert getattr(_lib, name) == value, name
