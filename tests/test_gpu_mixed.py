@@ -122,15 +122,16 @@ def test_mixed_fp32_strided_input(tq):
     check_quantize(mp.pn, Xf[:, mp.rest], planes["n"])
 
 
-@pytest.mark.parametrize("d,kdo,vdo,kv,kb,vv,vb", [
-    (128, 32, 32, "mse", (3, 2), "mse", (3, 2)),
-    (128, 32, 64, "prod", (4, 3), "mse", (3, 2)),
-    (128, 64, 32, "prod", (3, 2), "prod", (4, 3)),
-    (64, 32, 32, "mse", (4, 2), "mse", (3, 2)),
-    (256, 64, 96, "mse", (3, 2), "prod", (3, 3)),
+@pytest.mark.parametrize("d,kdo,vdo,kv,kb,vv,vb,Hq", [
+    (128, 32, 32, "mse", (3, 2), "mse", (3, 2), 32),   # 16 query heads per KV head: two head blocks
+    (128, 32, 32, "mse", (3, 2), "mse", (3, 2), 8),
+    (128, 32, 64, "prod", (4, 3), "mse", (3, 2), 8),
+    (128, 64, 32, "prod", (3, 2), "prod", (4, 3), 8),
+    (64, 32, 32, "mse", (4, 2), "mse", (3, 2), 8),
+    (256, 64, 96, "mse", (3, 2), "prod", (3, 3), 24),  # 12 heads per KV head: 3 blocks of 4
 ])
-def test_mixed_decode_attention(tq, d, kdo, vdo, kv, kb, vv, vb):
-    B, Hq, Hkv, T = 2, 8, 2, 333
+def test_mixed_decode_attention(tq, d, kdo, vdo, kv, kb, vv, vb, Hq):
+    B, Hkv, T = 2, 2, 333
     lens = [333, 120]
     rng = np.random.default_rng(d + kdo + vdo)
     hot_k = rng.choice(d, kdo, replace=False)
