@@ -9,7 +9,12 @@
  *   √(π/2)/d·Sᵀz, «Собственно TurboQuant» (prod: (b−1)-bit mse + QJL of the
  *   residual, storing sign(S·r) and ‖r‖), Theorem 2 (the prod map).
  * The decode-attention consumer is the "custom attention kernel" the
- * nahornyi.ai commentary says the prod variant needs.
+ * nahornyi.ai commentary says the prod variant needs.  Also from that page:
+ * «Что сделало сообщество» finding #3 (a Walsh–Hadamard rotation for the MSE
+ * stage with an independent QJL transform: tq_init_ex), and the experiments
+ * section's outlier-channel split (32 channels at 3 bits, 96 at 2: tq_mixed_*).
+ * The decode step with append (tq_decode_append_attention) is this library's
+ * serving entry point; the pages define no such step.
  *
  * Conventions shared by every entry point
  * ---------------------------------------
