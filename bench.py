@@ -5,7 +5,7 @@ into the packed cache, then one decode-attention step over that cache.
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload NAME] [--no-e2e] [--no-cpu-baseline]
 
-Prints ONE JSON line on rank 0 (see DESIGN.md "Measurement").  The metric is
+Prints ONE JSON line on rank 0.  The metric is
 the algorithmic HBM traffic of the whole step (bytes the packed format forces
 every implementation to move) divided by the device time of the step, in GB/s;
 quantize Mrows/s and decode GB/s are reported alongside.  Inputs are synthetic
@@ -38,7 +38,7 @@ WARM_SECONDS = 1.0
 # Kernel launches per library call (quantize: 1; decode: query prep, split, merge).
 LAUNCHES = {"quantize": 1, "decode": 3}
 # The arithmetic the path computes in.
-DTYPE_LABEL = "f32"
+DTYPE_LABEL = "bf16 in, bf16/f16 hi+lo MMA operands, fp32 accumulate and out"
 QUANT_SOURCES = ["kv_cache_vector_18_b300/csrc/tq_quantize_tc.cu", "kv_cache_vector_18_b300/csrc/tq_sm100.cuh"]
 DECODE_SOURCES = ["kv_cache_vector_18_b300/csrc/tq_decode_mma.cuh", "kv_cache_vector_18_b300/csrc/tq_decode_args.h",
                   "kv_cache_vector_18_b300/csrc/tq_decode.cu"]
@@ -103,15 +103,17 @@ def workload_spec(name: str) -> dict:
 
 
 def make_inputs(spec: dict):
-    """Host tensors (bf16) for K, V [B, Hkv, T, d], q [B, Hq, d] and int32 lengths."""
+    """bf16 K, V [B, Hkv, T, d] (host tensors, except the heavy-tailed batched
+    workload's, which are drawn on the device), q [B, Hq, d] and int32 lengths."""
     B, Hkv, T, d, Hq = spec["B"], spec["Hkv"], spec["T"], spec["d"], spec["Hq"]
     if spec["dist"] == "outliers":
         ch = synthetic.outlier_channels(d, 4, seed=4)
         K = synthetic.kv_with_outliers(B * Hkv, T, d, seed=0, channels=ch).reshape(B, Hkv, T, d)
         V = synthetic.kv_with_outliers(B * Hkv, T, d, seed=1, channels=ch).reshape(B, Hkv, T, d)
     elif spec["dist"] == "t":
-        K = synthetic.student_t_unit_var((B, Hkv, T, d), seed=0)
-        V = synthetic.student_t_unit_var((B, Hkv, T, d), seed=1)
+        # 2 x 537 M heavy-tailed values: drawn on the device (a host draw takes minutes)
+        K = synthetic.student_t_unit_var_cuda((B, Hkv, T, d), seed=0)
+        V = synthetic.student_t_unit_var_cuda((B, Hkv, T, d), seed=1)
     else:
         K = synthetic.gaussian((B, Hkv, T, d), seed=0)
         V = synthetic.gaussian((B, Hkv, T, d), seed=1)
@@ -314,11 +316,11 @@ def oracle_sample_run(spec, K, V, q, lens, rows: int, tokens: int, params):
     d = spec["d"]
     Kr = K.reshape(-1, d)
     Vr = V.reshape(-1, d)
-    O.quantize(pk, Kr[:rows].double().numpy())
-    O.quantize(pv, Vr[:rows].double().numpy())
+    O.quantize(pk, Kr[:rows].cpu().double().numpy())
+    O.quantize(pv, Vr[:rows].cpu().double().numpy())
     B, Hkv, Hq = spec["B"], spec["Hkv"], spec["Hq"]
-    Ks = K[:, :, :tokens].reshape(-1, d).double().numpy()
-    Vs = V[:, :, :tokens].reshape(-1, d).double().numpy()
+    Ks = K[:, :, :tokens].reshape(-1, d).cpu().double().numpy()
+    Vs = V[:, :, :tokens].reshape(-1, d).cpu().double().numpy()
     kq = O.quantize(pk, Ks)
     vq = O.quantize(pv, Vs)
     sl = [min(int(x), tokens) for x in lens]
@@ -336,9 +338,7 @@ def oracle_params(spec):
             O.make_params(spec["d"], spec["v_bits"], spec["v_variant"], 11, rot))
 
 
-def cpu_baseline(spec, K, V, q, lens, seconds: float = 12.0) -> dict:
-    params = oracle_params(spec)
-    rows, tokens = 4096, 1024
+def _oracle_rate(spec, K, V, q, lens, params, rows: int, tokens: int, seconds: float):
     oracle_sample_run(spec, K, V, q, lens, 256, 64, params)  # warm caches / BLAS threads
     t0 = time.perf_counter()
     nbytes = nrows = reps = 0
@@ -348,11 +348,29 @@ def cpu_baseline(spec, K, V, q, lens, seconds: float = 12.0) -> dict:
         nrows += r
         reps += 1
     dt = time.perf_counter() - t0
-    return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": blas_threads(), "kind": "oracle",
-            "sample": f"{reps} x (quantize {rows} K + {rows} V rows, decode over the first {tokens} tokens of "
-                      f"all {spec['B']}x{spec['Hkv']} KV heads, {spec['Hq']} query heads); "
-                      f"{dt:.1f} s; float64 NumPy",
-            "quantize_mrows_s": nrows / dt / 1e6}
+    return nbytes / dt / 1e9, nrows / dt / 1e6, reps, dt
+
+
+def cpu_baseline(spec, K, V, q, lens, seconds: float = 12.0, seconds_1core: float = 6.0) -> dict:
+    """The oracle as it stands on this host's cores: all BLAS threads, then one."""
+    params = oracle_params(spec)
+    rows, tokens = 4096, 1024
+    gbs, mrows, reps, dt = _oracle_rate(spec, K, V, q, lens, params, rows, tokens, seconds)
+    out = {"value": gbs, "unit": "GB/s", "cores": blas_threads(), "kind": "oracle",
+           "sample": f"{reps} x (quantize {rows} K + {rows} V rows, decode over the first {tokens} tokens of "
+                     f"all {spec['B']}x{spec['Hkv']} KV heads, {spec['Hq']} query heads); "
+                     f"{dt:.1f} s; float64 NumPy",
+           "quantize_mrows_s": mrows, "host_cpu_count": os.cpu_count(), "blas_threads": blas_threads()}
+    try:
+        from threadpoolctl import threadpool_limits
+        with threadpool_limits(limits=1):
+            g1, m1, r1, d1 = _oracle_rate(spec, K, V, q, lens, params, rows // 4, tokens // 4, seconds_1core)
+        out["one_core"] = {"value": g1, "unit": "GB/s", "quantize_mrows_s": m1, "cores": 1,
+                           "sample": f"{r1} x (quantize {rows // 4} K + {rows // 4} V rows, decode over the first "
+                                     f"{tokens // 4} tokens of every KV head); {d1:.1f} s"}
+    except Exception as exc:  # pragma: no cover - threadpoolctl missing
+        out["one_core"] = {"note": f"unavailable ({type(exc).__name__})"}
+    return out
 
 
 # ----------------------------------------------------------------------------- reference arm
@@ -601,6 +619,8 @@ def run_ours(args, spec):
                       + "; L2 flushed before every step; after >= %.1f s of back-to-back warm-up (%d steps)"
                       % (args.warm_seconds, warm_steps),
             "host_us_per_direct_call": {"quantize_k": host_us[0], "quantize_v": host_us[1], "decode": host_us[2]}}
+    if not args.no_configs and spec["name"] == "llama70b_layer_kv_quant" and spec.get("rotation", "qr") == "qr":
+        line["configs"] = measure_configs(tq, flush, dev, peaks)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(spec, K, V, q, lens.tolist())
     if rank == 0:
@@ -608,6 +628,145 @@ def run_ours(args, spec):
     if world > 1:
         torch.distributed.destroy_process_group()
     return 0
+
+
+def time_call(fn, flush, reps: int = 20, warm: int = 3) -> float:
+    """Mean device time (ms) of one library call: captured once as a CUDA graph
+    through the public API, replayed `reps` times with L2 flushed (a 256 MiB
+    write) before each replay, CUDA events on the launching stream around each."""
+    fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    for _ in range(warm):
+        flush.zero_()
+        g.replay()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for e0, e1 in evs:
+        flush.zero_()
+        e0.record()
+        g.replay()
+        e1.record()
+    torch.cuda.synchronize()
+    return statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs)
+
+
+def _rl(kernel, ms, nbytes, peaks, flops=None, exe_flops=None) -> dict:
+    """Roofline object of one call: algorithmic bytes (and flops) per launch over
+    its mean device time, against the measured HBM copy (and bf16) peaks."""
+    gbs = nbytes / (ms / 1e3) / 1e9
+    out = {"kernel": kernel, "bound": "hbm", "launch_ms": ms, "bytes_per_launch": nbytes, "achieved": gbs,
+           "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"], "peak_source": peaks["source"]}
+    if flops is not None:
+        tf = flops / (ms / 1e3) / 1e12
+        out["tensor"] = {"algorithmic_tflops": tf, "peak_tflops": peaks.get("bf16_tflops"),
+                         "frac_algorithmic": tf / peaks["bf16_tflops"] if peaks.get("bf16_tflops") else None}
+        if exe_flops is not None:
+            te = exe_flops / (ms / 1e3) / 1e12
+            out["tensor"]["executed_tflops"] = te
+            out["tensor"]["frac_executed"] = te / peaks["bf16_tflops"] if peaks.get("bf16_tflops") else None
+    return out
+
+
+def _quant_flops(d: int, variant: str, rows: int, rotation: str = "qr"):
+    """Algorithmic flops of a quantize call (2d² per row for the rotation, 2d² more
+    for the prod sketch) and the flops the tensor-core kernels execute (bf16
+    hi/lo passes for Π, or one ±1 pass for the Hadamard matrix, and 3 f16 passes
+    for the sketch)."""
+    alg = 2 * d * d * rows * (2 if variant == "prod" else 1)
+    exe = ((1 if rotation == "hadamard" else 2) + (3 if variant == "prod" else 0)) * 2 * d * d * rows
+    return alg, exe
+
+
+def measure_configs(tq, flush, dev, peaks, reps: int = 20) -> dict:
+    """Device time and roofline of every library call of the other workloads the
+    metric is quoted on (each call alone, as a CUDA graph, L2 flushed before each
+    replay): the 4096-row fp32 case, the 131072-token decode, the batched decode,
+    and quantize throughput at every point of the bit-width / head-dim sweep."""
+    res = {}
+    # 4096 x 128 fp32 rows, mse b = 2: quantize, dequantize, 64 queries scored against all keys
+    w = synthetic.WORKLOADS["small_mse_b2"]
+    n, d, nq = w["rows"], w["d"], w["queries"]
+    X = synthetic.gaussian((n, d), seed=0, dtype="f32").to(dev)
+    qz = tq.Quantizer(d, w["bits"], w["variant"], seed=0)
+    pl = qz.quantize(X)
+    y = torch.empty((n, d), dtype=torch.float32, device=dev)
+    q = synthetic.gaussian((1, nq, d), seed=1, dtype="f32").to(dev)
+    sl = torch.tensor([n], dtype=torch.int32, device=dev)
+    ws = torch.empty(tq.decode_workspace_bytes(qz, qz, 1, nq, 1, n), dtype=torch.uint8, device=dev)
+    o = torch.empty((1, nq, d), dtype=torch.float32, device=dev)
+    rb = row_bytes(w["bits"], w["variant"], d)
+
+    def dq():
+        from kv_cache_vector_18_b300 import _lib
+        _lib.check(_lib.lib().tq_dequantize(qz.handle, tq.Quantizer.planes_struct(pl), n, y.data_ptr(),
+                                            _lib.TQ_F32, torch.cuda.current_stream().cuda_stream))
+    sc = torch.empty((1, nq, n), dtype=torch.float32, device=dev)
+
+    def sc_call():
+        from kv_cache_vector_18_b300 import _lib
+        _lib.check(_lib.lib().tq_decode_attention(
+            qz.handle, qz.handle, q.data_ptr(), _lib.TQ_F32, tq.Quantizer.planes_struct(pl),
+            tq.Quantizer.planes_struct(pl), sl.data_ptr(), 1, nq, 1, n, 0.0, o.data_ptr(), sc.data_ptr(),
+            ws.data_ptr(), ws.numel(), torch.cuda.current_stream().cuda_stream))
+    a, e = _quant_flops(d, w["variant"], n)
+    res["small_mse_b2"] = {
+        "quantize": _rl("tq_quantize (fp32 rows, mse b=2)", time_call(lambda: qz.quantize(X, out=pl), flush, reps),
+                        n * (4 * d + rb), peaks, a, e),
+        "dequantize": _rl("tq_dequantize (fp32 out)", time_call(dq, flush, reps), n * (rb + 4 * d), peaks),
+        "decode_scores": _rl("tq_decode_attention (64 queries x 4096 keys, scores out)",
+                             time_call(sc_call, flush, reps), 2 * n * rb + nq * d * 8 + nq * n * 4, peaks)}
+    del X, pl, y, ws
+    # the two decode workloads: both quantize calls and the decode
+    for name in ("decode_131k", "batched_decode_32k"):
+        spec = workload_spec(name)
+        K, V, qh, lens = make_inputs(spec)
+        d, B, Hq, Hkv, T = spec["d"], spec["B"], spec["Hq"], spec["Hkv"], spec["T"]
+        tm = traffic_model(spec, lens.tolist())
+        kq = tq.Quantizer(d, spec["k_bits"], spec["k_variant"], seed=10)
+        vq = tq.Quantizer(d, spec["v_bits"], spec["v_variant"], seed=11)
+        Kd, Vd, qd, ld = K.to(dev).reshape(-1, d), V.to(dev).reshape(-1, d), qh.to(dev), lens.to(dev)
+        del K, V
+        kc, vc = kq.empty_planes(tm["n_rows"]), vq.empty_planes(tm["n_rows"])
+        ws = torch.empty(tq.decode_workspace_bytes(kq, vq, B, Hq, Hkv, T), dtype=torch.uint8, device=dev)
+        o = torch.empty((B, Hq, d), dtype=torch.float32, device=dev)
+        ka, ke = _quant_flops(d, spec["k_variant"], tm["n_rows"])
+        va, ve = _quant_flops(d, spec["v_variant"], tm["n_rows"])
+        entry = {
+            "quantize_k": _rl(f"tq_quantize ({spec['k_variant']} b={spec['k_bits']})",
+                              time_call(lambda: kq.quantize(Kd, out=kc), flush, reps), tm["quant_k"], peaks, ka, ke),
+            "quantize_v": _rl(f"tq_quantize ({spec['v_variant']} b={spec['v_bits']})",
+                              time_call(lambda: vq.quantize(Vd, out=vc), flush, reps), tm["quant_v"], peaks, va, ve)}
+        dms = time_call(lambda: tq.decode_attention(kq, vq, qd, kc, vc, ld, Hkv, T, workspace=ws, out=o), flush, reps)
+        entry["decode"] = _rl("tq_decode_attention", dms, tm["decode"], peaks)
+        fl = (3 if spec["k_variant"] == "prod" else 2) * 2 * d * (Hq // Hkv) * tm["ctx_rows"]
+        entry["decode"]["mma_tflops"] = fl / (dms / 1e3) / 1e12
+        entry["decode"]["token_heads"] = tm["ctx_rows"]
+        res[name] = entry
+        del Kd, Vd, kc, vc, ws
+        torch.cuda.empty_cache()
+    # bit-width / head-dim sweep: quantize throughput of 2^20 bf16 N(0,1) rows per point
+    sw = synthetic.WORKLOADS["sweep"]
+    n = sw["rows"]
+    pts = []
+    for dd in sw["d"]:
+        for variant in sw["variants"]:
+            for bits in sw["bits"]:
+                seed = 100 * dd + 10 * bits + (variant == "prod")
+                X = synthetic.gaussian_cuda((n, dd), seed=seed)
+                qz = tq.Quantizer(dd, bits, variant, seed=seed)
+                pl = qz.empty_planes(n)
+                ms = time_call(lambda: qz.quantize(X, out=pl), flush, max(5, reps // 2))
+                a, e = _quant_flops(dd, variant, n)
+                r = _rl(f"tq_quantize ({variant} b={bits}, d={dd})", ms, n * (2 * dd + row_bytes(bits, variant, dd)),
+                        peaks, a, e)
+                r.update({"d": dd, "variant": variant, "bits": bits, "mrows_s": n / (ms / 1e3) / 1e6})
+                pts.append(r)
+                del X, pl, qz
+    res["sweep"] = pts
+    torch.cuda.empty_cache()
+    return res
 
 
 def measure_append(tq, kq, vq, qd, kc, vc, ld, spec, ws, out, flush, dev, reps: int = 200) -> dict:
@@ -769,7 +928,7 @@ def measure_e2e(args, spec, tq, kq, vq, K, V, q, ld, kc, vc, ws, out, tm, dev, w
     step's K, V and q, the three library calls, D2H of the packed planes and
     the attention output, all inside the timed region."""
     d, Hkv, T = spec["d"], spec["Hkv"], spec["T"]
-    Kh, Vh, qh = K.reshape(-1, d).pin_memory(), V.reshape(-1, d).pin_memory(), q.pin_memory()
+    Kh, Vh, qh = K.reshape(-1, d).cpu().pin_memory(), V.reshape(-1, d).cpu().pin_memory(), q.pin_memory()
     Kd = torch.empty_like(Kh, device=dev)
     Vd = torch.empty_like(Vh, device=dev)
     qd = torch.empty_like(qh, device=dev)
@@ -821,6 +980,8 @@ def main(argv=None):
                     help="time outlier-channel mixed precision on the default workload (own JSON line)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-call timing of the other workloads (configs block)")
     ap.add_argument("--warm-seconds", type=float, default=WARM_SECONDS,
                     help="minimum back-to-back warm-up before timing (0 for profiler launch lists)")
     args = ap.parse_args(argv)

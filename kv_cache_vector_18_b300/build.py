@@ -1,6 +1,6 @@
 """Build libtq.so (host C++ + sm_103a CUDA) in-tree with nvcc.
 
-    python -m kv_cache_vector_18_b300.build [--force] [--debug]
+    python -m kv_cache_vector_18_b300.build [--force]
 
 Objects go to ``_build/`` at the repository root; the shared library is written
 next to this file so that it travels with the source tree.
@@ -31,12 +31,9 @@ def _nvcc() -> str:
     raise RuntimeError("nvcc not found")
 
 
-def _flags(debug: bool):
-    f = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
-         "-I", INCLUDE, "-I", CSRC, "--expt-relaxed-constexpr"] + ARCH
-    if debug:
-        f += ["-DTQ_DEBUG=1"]
-    return f
+def _flags():
+    return ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
+            "-I", INCLUDE, "-I", CSRC, "--expt-relaxed-constexpr"] + ARCH
 
 
 def _stale(src: str, obj: str, deps) -> bool:
@@ -46,17 +43,17 @@ def _stale(src: str, obj: str, deps) -> bool:
     return any(os.path.getmtime(p) > t for p in [src] + deps)
 
 
-def build(force: bool = False, debug: bool = False, verbose: bool = False) -> str:
+def build(force: bool = False, verbose: bool = False) -> str:
     os.makedirs(BUILD, exist_ok=True)
     nvcc = _nvcc()
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
     deps = glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(CSRC, "*.cuh")) + \
         glob.glob(os.path.join(INCLUDE, "*.h"))
-    flags = _flags(debug)
+    flags = _flags()
     jobs = []
     objs = []
     for s in srcs:
-        o = os.path.join(BUILD, os.path.basename(s) + (".dbg" if debug else "") + ".o")
+        o = os.path.join(BUILD, os.path.basename(s) + ".o")
         objs.append(o)
         if force or _stale(s, o, deps):
             jobs.append([nvcc, "-c", s, "-o", o] + flags)
@@ -83,8 +80,7 @@ def build(force: bool = False, debug: bool = False, verbose: bool = False) -> st
 if __name__ == "__main__":
     ap = argparse.ArgumentParser()
     ap.add_argument("--force", action="store_true")
-    ap.add_argument("--debug", action="store_true")
     ap.add_argument("-v", "--verbose", action="store_true")
     a = ap.parse_args()
-    print(build(force=a.force, debug=a.debug, verbose=a.verbose))
+    print(build(force=a.force, verbose=a.verbose))
     sys.exit(0)

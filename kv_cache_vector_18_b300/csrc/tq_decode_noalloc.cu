@@ -2,6 +2,7 @@
 // allocate device memory.  The workspace tq_decode_attention asks its caller
 // for lives instead in one file-scope __device__ array of fixed size that every
 // call on a device shares.
+#include <atomic>
 #include <mutex>
 
 #include "tq_internal.h"
@@ -15,23 +16,27 @@ static __device__ __align__(256) unsigned char g_decode_scratch[TQ_NOALLOC_WORKS
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-void* g_scratch_addr[kMaxDevices] = {};
+std::atomic<void*> g_scratch_addr[kMaxDevices] = {};
 
-// Device address of the scratch buffer on the current device (looked up on the
-// first call made with that device current, then cached).
+// Device address of the scratch buffer on the current device.  The first call
+// made with a device current looks it up (under a mutex); later calls read the
+// cached address without taking the lock.
 int scratch_on_current_device(void** out) {
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return tq::cuda_fail(e, "cudaGetDevice");
     if (dev < 0 || dev >= kMaxDevices) return tq::fail(TQ_EUNSUPPORTED, "device ordinal %d >= %d", dev, kMaxDevices);
-    std::lock_guard<std::mutex> lock(g_mu);
-    if (g_scratch_addr[dev] == nullptr) {
-        void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_decode_scratch);
-        if (e != cudaSuccess) return tq::cuda_fail(e, "cudaGetSymbolAddress(decode scratch)");
-        g_scratch_addr[dev] = p;
+    void* p = g_scratch_addr[dev].load(std::memory_order_acquire);
+    if (p == nullptr) {
+        std::lock_guard<std::mutex> lock(g_mu);
+        p = g_scratch_addr[dev].load(std::memory_order_relaxed);
+        if (p == nullptr) {
+            e = cudaGetSymbolAddress(&p, g_decode_scratch);
+            if (e != cudaSuccess) return tq::cuda_fail(e, "cudaGetSymbolAddress(decode scratch)");
+            g_scratch_addr[dev].store(p, std::memory_order_release);
+        }
     }
-    *out = g_scratch_addr[dev];
+    *out = p;
     return TQ_OK;
 }
 

@@ -563,10 +563,26 @@ quantize_prod_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_c
         const uint32_t ybase = tmem_base + (uint32_t)(slot * 2 * D + half * H) + lanebits;
         const uint32_t sbase = ybase + (uint32_t)D;
         auto pair_sync = [&]() { asm volatile("bar.sync %0, 256;" ::"r"(1 + slot) : "memory"); };
+        // Both halves of a slot meet at the named barrier above, so a bounded wait
+        // that gives up must end the loop for all 256 threads at once: each wait's
+        // outcome is AND-reduced over the pair on the same barrier, and the loop is
+        // left only when the reduced result says so.
+        auto pair_all = [&](bool ok) -> bool {
+            uint32_t r;
+            asm volatile(
+                "{\n\t.reg .pred p, q;\n\t"
+                "setp.ne.u32 p, %1, 0;\n\t"
+                "bar.red.and.pred q, %2, 256, p;\n\t"
+                "selp.u32 %0, 1, 0, q;\n\t}\n"
+                : "=r"(r)
+                : "r"((uint32_t)ok), "r"(1 + slot)
+                : "memory");
+            return r != 0;
+        };
         int64_t j = 0;
         for (int64_t tile = blockIdx.x + (int64_t)slot * gridDim.x; tile < ntiles;
              tile += (int64_t)kProdSlots * gridDim.x, ++j) {
-            if (!mbar_wait(&yfull[slot], (uint32_t)(j & 1), status, 18)) break;
+            if (!pair_all(mbar_wait(&yfull[slot], (uint32_t)(j & 1), status, 18))) break;
             tc_fence_after();
             uint32_t r[2][32];
             // pass 1: this half's part of ‖y‖², summed with the other half's
@@ -697,7 +713,7 @@ quantize_prod_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_c
                 rnorm_out[row] = sqrtf(xes[r_local] + xes[kTile + r_local]);
             }
             // pass 3: sign bits of this half of S = T·e (bit i set ⇔ s_i ≥ 0)
-            if (!mbar_wait(&sfull[slot], (uint32_t)(j & 1), status, 19)) break;
+            if (!pair_all(mbar_wait(&sfull[slot], (uint32_t)(j & 1), status, 19))) break;
             tc_fence_after();
             uint32_t sw[H / 32];
 #pragma unroll

@@ -43,8 +43,8 @@ decode_attention               pinned: q = 0 gives the plain mean of dequantized
                                brute-force loop on a tiny case, dequant-free
                                rotated-domain identity of the score.
 
-Readings where the page is silent (each also listed in the design doc)
-------------------------------------------------------------------
+Readings where the page is silent
+---------------------------------
 * "Gaussian" means i.i.d. N(0,1) entries (Шаг 1, QJL).  Π and S come from two
   independent streams (community finding #3 on the page).
 * Random numbers: SplitMix64 (counter form: output i mixes seed + (i+1)·φ64),
@@ -435,7 +435,8 @@ def decode_attention(pk: Params, pv: Params, q, k_rows: dict, v_rows: dict, seq_
 
 # ----------------------------------------------------------------------------
 # Outlier-channel mixed precision (the page's experiments, KV cache: 32 outlier
-# channels at 3 bits and the other 96 at 2 bits make 2.5 bits per channel)
+# channels at 3 bits and the other 96 at 2 bits, (32·3 + 96·2)/128 = 2.25 code
+# bits per channel; the page prints 2.5, which needs two 16-bit part norms)
 # ----------------------------------------------------------------------------
 class MixedParams:
     """Two independent quantizers over a split of the channels: ``po`` for the

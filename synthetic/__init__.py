@@ -6,9 +6,11 @@ dtype with PyTorch's CPU cast.  The pages measure on real Llama KV caches
 (LongBench / Needle-in-a-Haystack); those models and datasets are not available,
 so these shapes and distributions stand in for them.
 
-Every generator returns CPU ``torch`` tensors in the storage dtype; callers copy
-them to the device for the CUDA path and call ``.double().numpy()`` for the
-oracle, so both sides see bit-identical inputs.
+The host generators return CPU ``torch`` tensors in the storage dtype; callers
+copy them to the device for the CUDA path and call ``.double().numpy()`` for the
+oracle, so both sides see bit-identical inputs.  The ``*_cuda`` generators draw
+inputs too large for the host on the device; the oracle then reads sampled rows
+of that same device tensor.
 """
 from __future__ import annotations
 
@@ -41,6 +43,23 @@ def student_t_unit_var(shape, seed: int, nu: float = 4.0, dtype: str = "bf16") -
     (variance of t_ν is ν/(ν−2), so ν=4 is scaled by 1/√2)."""
     a = np.random.default_rng(seed).standard_t(nu, size=shape).astype(np.float64)
     return _cast(a * np.sqrt((nu - 2.0) / nu), dtype)
+
+
+def student_t_unit_var_cuda(shape, seed: int, nu: int = 4, dtype=torch.bfloat16) -> torch.Tensor:
+    """Heavy-tailed rows drawn on the current CUDA device (for inputs too large to
+    draw on the host): Student-t with an integer ν degrees of freedom as
+    z / √(χ²_ν / ν), χ²_ν the sum of ν squared standard normals, scaled by
+    √((ν − 2)/ν) to unit variance; every normal comes from one generator seeded
+    with `seed`."""
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    z = torch.randn(tuple(shape), generator=g, device="cuda", dtype=torch.float32)
+    chi2 = torch.zeros_like(z)
+    for _ in range(int(nu)):
+        e = torch.randn(tuple(shape), generator=g, device="cuda", dtype=torch.float32)
+        chi2.addcmul_(e, e)
+    t = z * torch.rsqrt(chi2 / nu) * float(np.sqrt((nu - 2.0) / nu))
+    return t.to(dtype)
 
 
 def outlier_channels(d: int, count: int, seed: int) -> np.ndarray:

@@ -513,7 +513,7 @@ def test_rotated_domain_score_identity():
 
 # ---------------------------------------------------------------- outlier-channel mixed precision
 # The page's experiments (KV cache): 32 outlier channels at 3 bits, the other 96 at
-# 2 bits, (32·3 + 96·2)/128 = 2.5 bits per channel.
+# 2 bits, (32·3 + 96·2)/128 = 2.25 code bits per channel (the page prints 2.5).
 def _mixed(d_o=32, b_o=3, b_n=2, variant="mse", perm=None, seed=3, d=128):
     po = O.make_params(d_o, b_o, variant, seed)
     pn = O.make_params(d - d_o, b_n, variant, seed + 1)

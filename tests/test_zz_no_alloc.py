@@ -1,9 +1,14 @@
 """tq_decode_attention_noalloc: decode attention whose scratch is a static device
 array inside the library, for callers that cannot allocate device memory (for
 example a serving loop whose memory another allocator has fully reserved, or a
-thin foreign binding with no device allocator).  Checked against
-tq_decode_attention with a caller-owned workspace, on two calls in a row that
-reuse the shared scratch with different shapes.  Collected last on purpose.
+thin foreign binding with no device allocator).
+
+Checked against tq_decode_attention with a caller-owned workspace over a
+sequence of calls that reuse the shared scratch: each call's split partials and
+merge tickets land on bytes an earlier call left behind with another layout —
+including a call whose query is NaN, so that its partials are NaN.  Also checks
+that a warmed-up call leaves the device's free memory unchanged.  Collected last
+on purpose.
 """
 import numpy as np
 import pytest
@@ -26,10 +31,11 @@ def _case(tq, B, Hq, Hkv, T, d, kb, kv, vb, vv, lens, seed):
     return kq, vq, q, kc, vc, sl
 
 
-def _noalloc(tq, kq, vq, q, kc, vc, sl, Hkv, T, scores=False):
+def _noalloc(tq, kq, vq, q, kc, vc, sl, Hkv, T, scores=False, out=None):
     from kv_cache_vector_18_b300 import _lib
     B, Hq, d = q.shape
-    out = torch.full((B, Hq, d), float("nan"), dtype=torch.float32, device="cuda")
+    if out is None:
+        out = torch.full((B, Hq, d), float("nan"), dtype=torch.float32, device="cuda")
     sc = torch.full((B, Hq, T), float("nan"), dtype=torch.float32, device="cuda") if scores else None
     rc = _lib.lib().tq_decode_attention_noalloc(
         kq.handle, vq.handle, q.data_ptr(), _lib.TQ_BF16, tq.Quantizer.planes_struct(kc),
@@ -39,12 +45,30 @@ def _noalloc(tq, kq, vq, q, kc, vc, sl, Hkv, T, scores=False):
     return out, sc
 
 
-def test_noalloc_matches_workspace_entry_point_twice():
+# Run in this order: a many-split layout, then a call whose NaN query leaves NaN
+# partials and used tickets all over the scratch, then layouts whose partials
+# and tickets sit at other offsets (a CUDA-core head dimension, fewer splits, a
+# larger one again).
+CASES = [
+    dict(B=4, Hq=32, Hkv=4, T=3000, d=128, kb=3, kv="prod", vb=3, vv="mse", lens=[3000, 1, 2999, 1500], seed=0),
+    dict(B=2, Hq=16, Hkv=2, T=2000, d=128, kb=3, kv="prod", vb=3, vv="mse", lens=[2000, 777], seed=10, nan=True),
+    dict(B=1, Hq=8, Hkv=1, T=5000, d=64, kb=2, kv="mse", vb=4, vv="mse", lens=[4999], seed=50),
+    dict(B=2, Hq=16, Hkv=2, T=2000, d=128, kb=3, kv="prod", vb=3, vv="mse", lens=[2000, 777], seed=20),
+    dict(B=1, Hq=64, Hkv=8, T=4096, d=128, kb=4, kv="prod", vb=2, vv="mse", lens=[4096], seed=30),
+]
+
+
+def test_noalloc_matches_workspace_entry_point_over_dirty_scratch():
     import kv_cache_vector_18_b300 as tq
-    cases = [dict(B=2, Hq=16, Hkv=2, T=2000, d=128, kb=3, kv="prod", vb=3, vv="mse", lens=[2000, 777], seed=0),
-             dict(B=1, Hq=8, Hkv=1, T=5000, d=64, kb=2, kv="mse", vb=4, vv="mse", lens=[4999], seed=50)]
-    for i, c in enumerate(cases):
+    for i, c in enumerate(CASES):
+        c = dict(c)
+        nan = c.pop("nan", False)
         kq, vq, q, kc, vc, sl = _case(tq, **c)
+        if nan:
+            q = torch.full_like(q, float("nan"))
+            _noalloc(tq, kq, vq, q, kc, vc, sl, c["Hkv"], c["T"])
+            torch.cuda.synchronize()
+            continue
         ref, ref_sc = tq.decode_attention(kq, vq, q, kc, vc, sl, c["Hkv"], c["T"], return_scores=True)
         got, got_sc = _noalloc(tq, kq, vq, q, kc, vc, sl, c["Hkv"], c["T"], scores=True)
         torch.cuda.synchronize()
@@ -55,6 +79,21 @@ def test_noalloc_matches_workspace_entry_point_twice():
         valid = ~np.isnan(rs)
         assert np.array_equal(np.isnan(gs), np.isnan(rs))
         assert np.max(np.abs(gs[valid] - rs[valid])) <= 2e-3
+
+
+def test_noalloc_call_leaves_free_memory_unchanged():
+    import kv_cache_vector_18_b300 as tq
+    kq, vq, q, kc, vc, sl = _case(tq, **{k: v for k, v in CASES[0].items()})
+    out = torch.empty((4, 32, 128), dtype=torch.float32, device="cuda")
+    for _ in range(2):  # warm-up: module loading, first symbol lookup
+        _noalloc(tq, kq, vq, q, kc, vc, sl, 4, 3000, out=out)
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    for _ in range(3):
+        _noalloc(tq, kq, vq, q, kc, vc, sl, 4, 3000, out=out)
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0, f"free device memory changed by {free0 - free1} bytes across no-alloc calls"
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():
