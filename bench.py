@@ -298,11 +298,16 @@ def recorded_traffic(kernel_key: str, src_hash: str, units_per_launch: int):
 
 
 def blas_threads() -> int:
+    """Threads of NumPy's BLAS: threadpoolctl when importable, else the thread
+    count the environment fixes, else one per host core (OpenBLAS's default)."""
     try:
         from threadpoolctl import threadpool_info
         n = [i["num_threads"] for i in threadpool_info() if i.get("user_api") == "blas"]
         return int(max(n)) if n else 1
     except Exception:
+        for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+            if os.environ.get(var, "").isdigit():
+                return int(os.environ[var])
         return os.cpu_count() or 1
 
 
@@ -361,16 +366,34 @@ def cpu_baseline(spec, K, V, q, lens, seconds: float = 12.0, seconds_1core: floa
                      f"all {spec['B']}x{spec['Hkv']} KV heads, {spec['Hq']} query heads); "
                      f"{dt:.1f} s; float64 NumPy",
            "quantize_mrows_s": mrows, "host_cpu_count": os.cpu_count(), "blas_threads": blas_threads()}
-    try:
-        from threadpoolctl import threadpool_limits
-        with threadpool_limits(limits=1):
-            g1, m1, r1, d1 = _oracle_rate(spec, K, V, q, lens, params, rows // 4, tokens // 4, seconds_1core)
-        out["one_core"] = {"value": g1, "unit": "GB/s", "quantize_mrows_s": m1, "cores": 1,
-                           "sample": f"{r1} x (quantize {rows // 4} K + {rows // 4} V rows, decode over the first "
-                                     f"{tokens // 4} tokens of every KV head); {d1:.1f} s"}
-    except Exception as exc:  # pragma: no cover - threadpoolctl missing
-        out["one_core"] = {"note": f"unavailable ({type(exc).__name__})"}
+    out["one_core"] = oracle_one_core(spec["name"], rows // 4, tokens // 4, seconds_1core)
     return out
+
+
+def oracle_one_core(workload: str, rows: int, tokens: int, seconds: float) -> dict:
+    """The same oracle sample on one core: a fresh interpreter whose BLAS and
+    OpenMP pools are limited to one thread before NumPy loads (no GPU use)."""
+    import subprocess
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    code = ("import json, sys; sys.path.insert(0, %r); import bench; "
+            "print(json.dumps(bench._one_core_child(%r, %d, %d, %f)))" % (ROOT, workload, rows, tokens, seconds))
+    try:
+        r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=300)
+        return json.loads(r.stdout.strip().splitlines()[-1])
+    except Exception as exc:  # pragma: no cover - depends on the host
+        return {"note": f"unavailable ({type(exc).__name__})"}
+
+
+def _one_core_child(workload: str, rows: int, tokens: int, seconds: float) -> dict:
+    spec = workload_spec(workload)
+    K, V, q, lens = make_inputs(spec) if spec["dist"] != "t" else (None, None, None, None)
+    if K is None:
+        return {"note": "device-drawn workload; one-core timing runs on the host workloads only"}
+    gbs, mrows, reps, dt = _oracle_rate(spec, K, V, q, lens.tolist(), oracle_params(spec), rows, tokens, seconds)
+    return {"value": gbs, "unit": "GB/s", "quantize_mrows_s": mrows, "cores": 1, "blas_threads": blas_threads(),
+            "sample": f"{reps} x (quantize {rows} K + {rows} V rows, decode over the first {tokens} tokens of "
+                      f"every KV head); {dt:.1f} s"}
 
 
 # ----------------------------------------------------------------------------- reference arm

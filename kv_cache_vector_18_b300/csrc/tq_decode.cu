@@ -295,6 +295,7 @@ int launch_d(const tq_ctx& hk, const tq_ctx& hv, const DecodeShape& p, const voi
     a.n_splits = p.n_splits; a.chunk = p.chunk;
     a.cnt = cnt; a.vPi = hv.dp.Pi; a.vS = hv.dp.S; a.out = out;
     a.q = q; a.q_f32 = q_dtype == TQ_F32; a.kPi_hi = hk.dp.Pi_hi; a.kPi_lo = hk.dp.Pi_lo; a.kS_hi = hk.dp.S_hi; a.kS_lo = hk.dp.S_lo;
+    a.status = hk.dp.status;
     if (use_mma_split(D)) {
         // query rotation, split and merge all happen in the split kernel
         a.n_hblocks = (p.G + mmadec::kHeadsPerCta - 1) / mmadec::kHeadsPerCta;

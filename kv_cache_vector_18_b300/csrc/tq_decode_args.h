@@ -43,6 +43,9 @@ struct SplitArgs {
     const uint16_t* kPi_lo;
     const uint16_t* kS_hi;
     const uint16_t* kS_lo;
+    // the key handle's device status word: a staging wait that gives up records
+    // kDecodeStageTimeout there
+    int* status;
 };
 
 namespace mmadec {
@@ -51,6 +54,7 @@ namespace mmadec {
 constexpr int kHeadsPerCta = 8;
 constexpr int D128 = 128;
 constexpr int kMaxSplitsMerged = 256;  // splits the last CTA of a group can merge
+constexpr int kDecodeStageTimeout = 30;  // status code of an expired tile-staging wait
 // resident split CTAs per SM of the tensor-core decode kernel (one 16- or 8-warp CTA)
 constexpr int ctas_per_sm(bool /*vprod*/) { return 1; }
 template <int KB, bool KP>

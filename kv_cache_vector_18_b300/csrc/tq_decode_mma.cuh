@@ -8,40 +8,46 @@
 // part for prod values), written as one split partial (m, l, acc) per head.
 //
 // Mapping onto mma.sync.m16n8k16 (f16 operands, f32 accumulators), per warp and
-// 16-token step, lane = 4·g + c:
-//   scores  S[16 tokens × 8 heads] = K̃[16 × d] · Q′ᵀ[d × 8]: the A fragment is
-//           decoded in registers straight from the packed codes — lane (g, c)
-//           owns tokens g and g + 8 and the 32 dims [32c, 32c + 32) of each, so
-//           its code bits are one contiguous run of the row.  Four (or two)
-//           consecutive codes index a shared-memory table of f16 centroid pairs;
-//           one byte of QJL sign bits indexes a table of four ±1 pairs.  Table
-//           words are read one 32-bit load per fragment register, so each lands
-//           directly in its MMA operand slot.  Q′ (and Q″ = S·q) are B fragments
-//           whose k order follows the decoded pairs.
-//   values  Oᵀ[d × 8 heads] += Ṽᵀ[d × 16 tokens] · P′ᵀ[16 × 8]: Ṽ is decoded the
-//           same way (token-major pairs) and moved to the dim-major A layout
-//           with movmatrix.trans; P′ leaves the score accumulator in exactly the
-//           layout movmatrix.trans turns into the B fragment.
-// ‖v_t‖ is folded into the softmax exponent (P′_t = 2^(s_t·log2e + log2‖v_t‖ − M)),
-// so the f16 weights stay bounded whatever the value norms; l accumulates
-// P′_t/‖v_t‖ in f32 against the same running maximum M.  M is raised only when a
-// step's exponent exceeds it by more than kSlack, so P′ ≤ 2^kSlack and most
-// steps skip the cross-lane maximum.  Per-head scale factors keep the f16 query
-// fragments in [−1, 1], and the centroid tables hold f16(σ·c) for a per-codebook
-// σ chosen on the host so that the f16 rounding of the centroids — systematic,
-// and amplified by the softmax — nearly vanishes.
+// 16-token step made of two 8-token groups, lane = 4·g + c:
+//   scores  S[16 × 8 tokens] = [Q′_hi; Q′_lo][16 × d] · K̃ᵀ[d × 8 tokens]: the keys
+//           are the B operand, so rows 0–7 (f16 high parts of the 8 heads' q′)
+//           and rows 8–15 (their f16 rounding errors) use the whole M = 16 and
+//           the score keeps ~2⁻²² of q′ at no extra MMA.  Lane (g, c) decodes
+//           token g of the group: for k16 block kb its B fragment is four
+//           consecutive codes of the token's row (one byte at 2 bits: one 64-bit
+//           load from a table of code quads; two code-pair loads at 3 and 4
+//           bits; two bit operations per pair at 1 bit).
+//   QJL     Z·Q″ᵀ in the same orientation, [Q″_hi; Q″_lo] · Zᵀ: one byte of sign
+//           bits gives the ±1 fragments of two k16 blocks through one 128-bit
+//           table load.
+//   values  Oᵀ[d × 8 heads] += Ṽᵀ[d × 16 tokens] · P′ᵀ[16 × 8]: Ṽ is decoded
+//           token-major (code-pair tables) and moved to the dim-major A layout
+//           with movmatrix.trans; P′ leaves the score accumulator already in the
+//           B-fragment layout (lane (g, c): head g, tokens 2c, 2c + 1 of each group).
+// Each lane keeps the online-softmax state of one head (g).  ‖v_t‖ is folded
+// into the softmax exponent (P′_t = 2^(s_t·log2e + log2‖v_t‖ − M)), so the f16
+// weights stay bounded whatever the value norms; l accumulates P′_t/‖v_t‖ in f32
+// against the same running maximum M.  M is raised only when a step's exponent
+// exceeds it by more than kSlack, so P′ ≤ 2^kSlack and most steps skip the
+// cross-lane maximum.  Per-head scale factors keep the f16 query fragments in
+// [−1, 1], and the centroid tables hold f16(σ·c) for a per-codebook σ chosen on
+// the host so that the f16 rounding of the centroids — systematic, and
+// amplified by the softmax — nearly vanishes.
 //
-// Data movement: each warp streams its 16-token tiles of all packed planes into
-// a two-stage shared-memory ring with cp.async (the next tile is in flight while
-// the current one is decoded), so the hot loop reads its operands with short
-// shared-memory loads.  The last CTA of each (batch, KV head, head block) to
-// finish merges every split's partial and applies Π_vᵀ (no merge launch).
+// Data movement: one producer warp streams the chunk's packed planes into a
+// ring of shared-memory stages of 64 tokens with cp.async, each stage
+// completing on a "full" mbarrier; the consumer warps take 16-token tiles of
+// the stages round-robin, read their operands with short shared-memory loads
+// and release each stage on an "empty" mbarrier (every wait is bounded).  The
+// last CTA of each (batch, KV head, head block) to finish merges every split's
+// partial and applies Π_vᵀ (no merge launch).
 #pragma once
 
 #include <math.h>
 
 #include "tq_common.cuh"
 #include "tq_decode_args.h"
+#include "tq_sm100.cuh"
 
 namespace tq {
 namespace mmadec {
@@ -157,41 +163,39 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// ---- per-lane decoders: packed codes → f16 fragment pairs -------------------
-// A lane owns a run of 32 consecutive codes of a row (dims [32c, 32c + 32)).
-// Decoder<B>::pairs(w, kb, p0, p1) yields the two f16 pairs that k16 block kb
-// of an MMA fragment takes from that run (pairs τ = 2kb and 2kb + 1), and
-// Decoder<B>::dim(c, τ, e) is the dim held by element e of pair τ — the Q′
-// fragments and the accumulator rows follow the same map.
-//   B = 1: both codes of a pair are bits τ and τ + 16 of the run's word; the
-//          centroids are ±c₁, so the pair is the constant (−c₁, −c₁) with its
-//          two sign bits flipped where the code bits are set (two ALU ops).
-//   B = 2: a shared-memory table indexed by four adjacent codes (one byte)
-//          whose entry is the two f16 pairs, 16 interleaved copies so that a
-//          warp's lookups never collide on a bank.
-//   B = 3, 4: a shared-memory table of f16 centroid pairs indexed by two
-//          adjacent codes, one copy per lane.
-// (Measured on B300 against register-only variants — byte permutes for B = 2,
-// two bit operations per QJL sign pair — the tables are faster: the integer
-// pipe, not shared memory, is the tighter resource.)
+template <int OFF>
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+    uint2 v;
+    asm("ld.shared.v2.b32 {%0, %1}, [%2+%3];" : "=r"(v.x), "=r"(v.y) : "r"(addr), "n"(OFF));
+    return v;
+}
+
+// A ±1 (or ±c) f16 pair from two bits of w that are 16 apart: bits τ and τ + 16
+// land in the two sign positions and flip the pair `neg` (whose halves are
+// negative) where they are set.
 __device__ __forceinline__ uint32_t flip_pair(uint32_t w, int tau, uint32_t neg) {
     return neg ^ ((w << (15 - tau)) & 0x80008000u);
 }
 
-template <int B>
-struct Decoder {
-    static constexpr bool kQuadTable = B == 2;  // 256 quads × 16 copies × 8 bytes
-    static constexpr bool kTable = B >= 3;
-    static constexpr size_t kTableBytes =
-        kTable ? (size_t)(1 << (2 * B)) * 32 * 4 : (kQuadTable ? (size_t)256 * 16 * 8 : 0);
-    static constexpr int kWords = B > 0 ? B : 1;
-    // per-lane constants
-    uint32_t k0, k1;   // B = 1: (−c₁, −c₁); B = 2: levels (c0, c1), (c2, c3); B ≥ 3: table base | lane offset
-    uint32_t tab;
+constexpr uint32_t kMinusOnePair = 0xBC00BC00u;  // f16 (−1, −1)
 
+// Every table sits at a shared-memory address that is a multiple of its
+// (power-of-two) size, so a lookup address is one OR of the shifted code field
+// with the lane's copy offset and the table base.  Table layouts (σ = the
+// codebook's table scale):
+//   quad (b = 2): entry e (a byte: four 2-bit codes, LSB first) holds the two f16
+//          pairs (σc[e₀], σc[e₁]), (σc[e₂], σc[e₃]) as 8 bytes, 16 copies
+//          (128-byte entries), so a half-warp's 64-bit loads never collide;
+//   pair (b = 3, 4): entry e (two b-bit codes) holds (σc[e₀], σc[e₁]), 32 copies.
+template <int B>
+struct Table {
+    static constexpr bool kQuad = B == 2;
+    static constexpr bool kPair = B >= 3;
+    static constexpr size_t kBytes =
+        kPair ? (size_t)(1 << (2 * B)) * 32 * 4 : (kQuad ? (size_t)256 * 16 * 8 : 0);
     __device__ static void fill(unsigned char* tabp, const Codebook& cb) {
-        if constexpr (kQuadTable) {
-            const float s = cb.lut_scale;
+        const float s = cb.lut_scale;
+        if constexpr (kQuad) {
             for (int i = threadIdx.x; i < 256 * 16; i += blockDim.x) {
                 const uint32_t e = (uint32_t)i >> 4, copy = (uint32_t)i & 15u;
                 uint2 v;
@@ -200,8 +204,7 @@ struct Decoder {
                 *reinterpret_cast<uint2*>(tabp + e * 128u + copy * 8u) = v;
             }
         }
-        if constexpr (kTable) {
-            const float s = cb.lut_scale;
+        if constexpr (kPair) {
             constexpr uint32_t m = (1u << B) - 1u;
             for (int i = threadIdx.x; i < (1 << (2 * B)) * 32; i += blockDim.x) {
                 const uint32_t e = (uint32_t)i >> 5, copy = (uint32_t)i & 31u;
@@ -210,109 +213,147 @@ struct Decoder {
             }
         }
     }
+    // this lane's view of the table (base | copy offset)
+    __device__ static uint32_t lane_base(const unsigned char* tabp, int lane) {
+        return smem_addr(tabp) + (kQuad ? (uint32_t)(lane & 15) * 8u : (uint32_t)lane * 4u);
+    }
+};
+
+// ---- keys: the B operand of the score MMA ------------------------------------
+// Lane (g, c) decodes token g of an 8-token group from its run of 32 codes
+// (dims [32c, 32c + 32), KB words starting at byte 4·KB·c of the row).  For k16
+// block kb the fragment (b0, b1) holds, in MMA k slots 2c, 2c + 1, 2c + 8,
+// 2c + 9, the dims dim(c, kb, 0..3); the Q′ fragments follow the same map.
+//   KB = 1: pairs of bits 16 apart, (2kb, 2kb + 16) and (2kb + 1, 2kb + 17):
+//           the centroids are ±c₁, two bit operations per pair;
+//   KB = 2: byte kb of the run, one 64-bit load from the quad table;
+//   KB = 3, 4: codes 4kb … 4kb + 3 of the run, two loads from the pair table.
+template <int KB>
+struct KDecoder {
+    uint32_t k0;   // KB = 1: (−σc₁, −σc₁)
+    uint32_t tab;  // KB ≥ 2: table base | lane copy offset
     __device__ void init(const Codebook& cb, const unsigned char* tabp, int lane) {
-        const float s = cb.lut_scale;
-        if constexpr (B == 1) {
-            k0 = pack_h2(cb.c[0] * s, cb.c[0] * s);
-        } else if constexpr (kQuadTable) {
-            tab = smem_addr(tabp) + (uint32_t)(lane & 15) * 8u;
-        } else if constexpr (B == 2) {
-            k0 = pack_h2(cb.c[0] * s, cb.c[1] * s);
-            k1 = pack_h2(cb.c[2] * s, cb.c[3] * s);
-        } else if constexpr (kTable) {
-            tab = smem_addr(tabp) + (uint32_t)lane * 4u;
+        if constexpr (KB == 1) k0 = pack_h2(cb.c[0] * cb.lut_scale, cb.c[0] * cb.lut_scale);
+        if constexpr (KB >= 2) tab = Table<KB>::lane_base(tabp, lane);
+    }
+    __device__ __forceinline__ void frag(const uint32_t* w, int kb, uint32_t& b0, uint32_t& b1) const {
+        if constexpr (KB == 1) {
+            b0 = flip_pair(w[0], 2 * kb, k0);
+            b1 = flip_pair(w[0], 2 * kb + 1, k0);
+        } else if constexpr (KB == 2) {
+            const uint2 v = lds64<0>(field_off<8, 7>(w, 8 * kb) | tab);
+            b0 = v.x;
+            b1 = v.y;
+        } else {
+            b0 = lds32(field_off<2 * KB, 7>(w, 4 * KB * kb) | tab);
+            b1 = lds32(field_off<2 * KB, 7>(w, 4 * KB * kb + 2 * KB) | tab);
         }
+    }
+    __host__ __device__ static constexpr int dim(int c, int kb, int e) {
+        return KB == 1 ? 32 * c + 2 * kb + (e >> 1) + 16 * (e & 1) : 32 * c + 4 * kb + e;
+    }
+};
+
+// QJL signs of the keys: word c of a token's sign row holds dims [32c, 32c + 32);
+// byte j of it (eight signs, LSB first) gives the fragments of k16 blocks 2j and
+// 2j + 1 through one 128-bit load from a table whose entry e holds the four f16
+// ±1 pairs of e's bits (0, 1), (2, 3), (4, 5), (6, 7) — (b0, b1) of block 2j,
+// then (b0, b1) of block 2j + 1.  Eight copies (128-byte entries) keep each
+// quarter-warp's loads apart.  Block kb covers dims 32c + 4kb … 32c + 4kb + 3.
+struct KSignTable {
+    static constexpr size_t kBytes = (size_t)256 * 8 * 16;
+    __device__ static void fill(unsigned char* tabp) {
+        for (int i = threadIdx.x; i < 256 * 8; i += blockDim.x) {
+            const uint32_t e = (uint32_t)i >> 3, copy = (uint32_t)i & 7u;
+            uint32_t v[4];
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                const uint32_t lo = (e >> (2 * p)) & 1u ? 0x3C00u : 0xBC00u;
+                const uint32_t hi = (e >> (2 * p + 1)) & 1u ? 0x3C00u : 0xBC00u;
+                v[p] = lo | (hi << 16);
+            }
+            *reinterpret_cast<uint4*>(tabp + e * 128u + copy * 16u) = make_uint4(v[0], v[1], v[2], v[3]);
+        }
+    }
+    __device__ static uint32_t lane_base(const unsigned char* tabp, int lane) {
+        return smem_addr(tabp) + (uint32_t)(lane & 7) * 16u;
+    }
+};
+__host__ __device__ constexpr int ksign_dim(int c, int kb, int e) { return 32 * c + 4 * kb + e; }
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+
+// ---- values: token-major pairs for movmatrix ----------------------------------
+// A lane owns a run of 32 consecutive codes of a row (dims [32c, 32c + 32)).
+// Decoder<B>::pairs(w, m, p0, p1) yields the two f16 pairs that m16 tile m of
+// the value operand takes from that run (pairs τ = 2m and 2m + 1, before the
+// transpose), and Decoder<B>::dim(c, τ, e) is the dim held by element e of pair
+// τ — the accumulator rows follow the same map.
+//   B = 1: both codes of a pair are bits τ and τ + 16 of the run's word (±c₁).
+//   B = 2: byte m of the run, one 64-bit load from the quad table.
+//   B = 3, 4: two adjacent codes per pair, one load each from the pair table.
+template <int B>
+struct Decoder {
+    static constexpr size_t kTableBytes = Table<B>::kBytes;
+    uint32_t k0;
+    uint32_t tab;
+    __device__ void init(const Codebook& cb, const unsigned char* tabp, int lane) {
+        if constexpr (B == 1) k0 = pack_h2(cb.c[0] * cb.lut_scale, cb.c[0] * cb.lut_scale);
+        if constexpr (B >= 2) tab = Table<B>::lane_base(tabp, lane);
     }
     __device__ __forceinline__ void pairs(const uint32_t* w, int kb, uint32_t& p0, uint32_t& p1) const {
         if constexpr (B == 1) {
             p0 = flip_pair(w[0], 2 * kb, k0);
             p1 = flip_pair(w[0], 2 * kb + 1, k0);
-        } else if constexpr (kQuadTable) {
-            const uint32_t a = field_off<8, 7>(w, 8 * kb) | tab;
-            p0 = lds32(a);
-            p1 = lds32o<4>(a);
         } else if constexpr (B == 2) {
-            const int wi = kb >> 2, j = kb & 3;
-            const uint32_t x = (w[wi] >> (2 * j)) & 0x03030303u;  // codes j, j+4, j+8, j+12 in bytes
-            const uint32_t y = x * 0x22u + 0x10101010u;           // byte-permute selectors
-            p0 = __byte_perm(k0, k1, y);
-            p1 = __byte_perm(k0, k1, y >> 16);
+            const uint2 v = lds64<0>(field_off<8, 7>(w, 8 * kb) | tab);
+            p0 = v.x;
+            p1 = v.y;
         } else {
             p0 = lds32(field_off<2 * B, 7>(w, 4 * B * kb) | tab);
             p1 = lds32(field_off<2 * B, 7>(w, 4 * B * kb + 2 * B) | tab);
         }
     }
     __host__ __device__ static constexpr int dim(int c, int tau, int e) {
-        return B == 1 ? 32 * c + tau + 16 * e
-                      : ((B == 2 && !kQuadTable) ? 32 * c + 16 * ((tau >> 1) >> 2) + ((tau >> 1) & 3) + 8 * (tau & 1) +
-                                                       4 * e
-                                                 : 32 * c + 2 * tau + e);
+        return B == 1 ? 32 * c + tau + 16 * e : 32 * c + 2 * tau + e;
     }
 };
 
-constexpr uint32_t kMinusOnePair = 0xBC00BC00u;  // f16 (−1, −1)
-
-// Every table is placed at a shared-memory address that is a multiple of its
-// (power-of-two) size, so a lookup address is one OR of the shifted code field
-// with the lane's copy offset and the table base.
-
-// QJL sign pairs of a lane's 32 sign bits: either two ALU operations per pair
-// (bits τ, τ + 16), or a shared-memory table mapping one byte of sign bits to
-// four ±1 pairs (bits 2τ, 2τ + 1), 8 copies so that lookups never collide.
+// QJL sign pairs of the values (prod values): pair τ of a lane's sign word is
+// bits (τ, τ + 16), two bit operations each; quad(w, m, p) gives pairs 4m … 4m + 3.
 struct SignDecoder {
-    static constexpr bool kTable = true;
-    static constexpr size_t kTableBytes = kTable ? (size_t)256 * 8 * 16 : 0;
-    uint32_t tab;
-    __device__ static void fill(unsigned char* tabp) {
-        if constexpr (kTable) {
-            for (int i = threadIdx.x; i < 256 * 8; i += blockDim.x) {
-                const uint32_t e = (uint32_t)i >> 3, copy = (uint32_t)i & 7u;
-                uint32_t v[4];
-#pragma unroll
-                for (int p = 0; p < 4; ++p) {
-                    const uint32_t lo = (e >> (2 * p)) & 1u ? 0x3C00u : 0xBC00u;
-                    const uint32_t hi = (e >> (2 * p + 1)) & 1u ? 0x3C00u : 0xBC00u;
-                    v[p] = lo | (hi << 16);
-                }
-                *reinterpret_cast<uint4*>(tabp + e * 128u + copy * 16u) = make_uint4(v[0], v[1], v[2], v[3]);
-            }
-        }
-    }
-    __device__ void init(const unsigned char* tabp, int lane) {
-        if constexpr (kTable) tab = smem_addr(tabp) + (uint32_t)(lane & 7) * 16u;
-    }
-    // pairs 4m..4m+3 (k16 blocks 2m and 2m + 1)
     __device__ __forceinline__ void quad(uint32_t w, int m, uint32_t (&p)[4]) const {
-        if constexpr (kTable) {
-            const uint32_t a = field_off<8, 7>(&w, 8 * m) | tab;
-            p[0] = lds32(a);
-            p[1] = lds32o<4>(a);
-            p[2] = lds32o<8>(a);
-            p[3] = lds32o<12>(a);
-        } else {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) p[i] = flip_pair(w, 4 * m + i, kMinusOnePair);
-        }
+        for (int i = 0; i < 4; ++i) p[i] = flip_pair(w, 4 * m + i, kMinusOnePair);
     }
-    __host__ __device__ static constexpr int dim(int c, int tau, int e) {
-        return kTable ? 32 * c + 2 * tau + e : 32 * c + tau + 16 * e;
-    }
+    __host__ __device__ static constexpr int dim(int c, int tau, int e) { return 32 * c + tau + 16 * e; }
 };
 __host__ __device__ constexpr int sign_dim(int c, int tau, int e) { return SignDecoder::dim(c, tau, e); }
 
-// Byte layout of one 16-token tile of every plane in a warp's staging ring.
+// Tokens per stage of the CTA's staging ring (four 16-token tiles), and the
+// most stages a ring holds (it takes what shared memory the tables leave).
+constexpr int kStageRows = 64;
+constexpr int kMaxStages = 12;
+
+// Byte layout of one stage (kStageRows tokens) of every plane: plane by plane,
+// rows in token order, so a 16-token tile of a plane is one contiguous run.
 template <int KB, bool KP, int VB, bool VP>
 struct Stage {
+    static constexpr int R = kStageRows;
     static constexpr int kRK = KB * 16, kRV = VB * 16;  // code bytes per row
     static constexpr int kKC = 0;
-    static constexpr int kKS = kKC + kTile * kRK;
-    static constexpr int kKN = kKS + (KP ? kTile * 16 : 0);
-    static constexpr int kKR = kKN + kTile * 4;
-    static constexpr int kVC = kKR + (KP ? kTile * 4 : 0);
-    static constexpr int kVS = kVC + kTile * kRV;
-    static constexpr int kVN = kVS + (VP ? kTile * 16 : 0);
-    static constexpr int kVR = kVN + kTile * 4;
-    static constexpr int kBytes = kVR + (VP ? kTile * 4 : 0);
+    static constexpr int kKS = kKC + R * kRK;
+    static constexpr int kKN = kKS + (KP ? R * 16 : 0);
+    static constexpr int kKR = kKN + R * 4;
+    static constexpr int kVC = kKR + (KP ? R * 4 : 0);
+    static constexpr int kVS = kVC + R * kRV;
+    static constexpr int kVN = kVS + (VP ? R * 16 : 0);
+    static constexpr int kVR = kVN + R * 4;
+    static constexpr int kBytes = kVR + (VP ? R * 4 : 0);
 };
 
 // Plane pointers of this CTA's (batch, KV head) slab.
@@ -328,54 +369,89 @@ struct Slab {
     const float* vrn;
 };
 
-// Rows [tb, tb + 16) of a plane with RB-byte rows (a multiple of 16) into smem
-// at dst, chunk k of 16 bytes through lane k mod 32.  `src` is the tile's first
-// byte.  A full tile copies without predicates; in the chunk's last tile the
-// rows at or past `rows` (tile-relative) are zero-filled without being read.
-template <int RB>
-__device__ __forceinline__ void stage_rows16(uint32_t dst, const uint8_t* src, bool full, int rows, int lane) {
+// The producer warp's copy of one stage: rows [tb, tb + valid) of every plane of
+// the slab into the stage at dst with per-lane cp.async; rows from `valid` to
+// kStageRows are zero-filled and nothing past the chunk's last token is read.
+template <int RB>  // bytes per row, a multiple of 16
+__device__ __forceinline__ void copy_rows16(uint32_t dst, const uint8_t* src, int valid, int lane) {
+    constexpr int kChunks = kStageRows * RB / 16, kPerRow = RB / 16;
 #pragma unroll
-    for (int r = 0; r < (RB + 31) / 32; ++r) {
-        const int k = lane + 32 * r;
-        if (RB % 32 == 0 || k < RB) {
-            if (full) {
-                cp_async16(dst + 16 * k, src + 16 * k, 16u);
-            } else {
-                const bool ok = (16 * k) / RB < rows;
-                cp_async16(dst + 16 * k, ok ? src + 16 * k : src, ok ? 16u : 0u);
-            }
+    for (int r = 0; r < (kChunks + 31) / 32; ++r) {
+        const int q = lane + 32 * r;
+        if (kChunks % 32 == 0 || q < kChunks) {
+            const bool ok = q / kPerRow < valid;
+            cp_async16(dst + 16 * q, ok ? src + 16 * q : src, ok ? 16u : 0u);
         }
     }
 }
-// A tile of fp32 norms: four 16-byte copies (lanes 0–3) when the tile is full and
-// the plane's rows start on a 16-byte boundary (a16, uniform over the CTA), else
-// one 4-byte copy per row (lanes 0–15).
-__device__ __forceinline__ void stage_rows4(uint32_t dst, const float* src, bool full, bool a16, int rows, int lane) {
-    if (full && a16) {
-        if (lane < 4) cp_async16(dst + 16 * lane, src + 4 * lane, 16u);
-    } else if (lane < kTile) {
-        const bool ok = full || lane < rows;
-        cp_async4(dst + 4 * lane, ok ? src + lane : src, ok ? 4u : 0u);
+// fp32 norms: 16-byte chunks of four rows when the plane's rows start on a
+// 16-byte boundary (a16), else one 4-byte copy per row
+__device__ __forceinline__ void copy_norms(uint32_t dst, const float* src, bool a16, int valid, int lane) {
+    if (a16) {
+        if (lane < kStageRows / 4) {
+            const int n = min(4, max(0, valid - 4 * lane));
+            cp_async16(dst + 16 * lane, n > 0 ? src + 4 * lane : src, 4u * (uint32_t)n);
+        }
+    } else {
+#pragma unroll
+        for (int i = lane; i < kStageRows; i += 32) {
+            const bool ok = i < valid;
+            cp_async4(dst + 4 * i, ok ? src + i : src, ok ? 4u : 0u);
+        }
     }
 }
 
+// Bulk variant (T_max % 4 == 0): rows [tb, tb + min(kStageRows, T_max − tb)) of
+// every plane with one untiled bulk copy each, completing on the stage's full
+// mbarrier.  The row count is a multiple of 4, so every copy is a multiple of 16
+// bytes and starts on a 16-byte boundary; rows past the chunk's end are masked
+// in the step, and nothing past the slab is read.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
 template <int KB, bool KP, int VB, bool VP>
-__device__ __forceinline__ void stage_tile(uint32_t dst, const Slab& s, int tb, int t1, int lane) {
+__device__ __forceinline__ void produce_stage_bulk(uint32_t dst, uint32_t bar, const Slab& s, int tb, int T_max) {
     using ST = Stage<KB, KP, VB, VP>;
-    const bool full = tb + kTile <= t1;
-    const int rows = t1 - tb;
-    if constexpr (KB > 0) stage_rows16<ST::kRK>(dst + ST::kKC, s.kc + (size_t)tb * ST::kRK, full, rows, lane);
+    // bytes of one row over all planes: codes, norms (keys and values), signs and residual norms
+    constexpr uint32_t kRowBytes = ST::kRK + ST::kRV + 8 + (KP ? 20 : 0) + (VP ? 20 : 0);
+    static_assert(kRowBytes * kStageRows == ST::kBytes, "bulk staging must fill the whole stage layout");
+    const uint32_t rows = (uint32_t)min(kStageRows, T_max - tb);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the consumers' reads of the slot come first
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(rows * kRowBytes)
+                 : "memory");
+    if constexpr (KB > 0) bulk_g2s(dst + ST::kKC, s.kc + (size_t)tb * ST::kRK, rows * ST::kRK, bar);
     if constexpr (KP) {
-        stage_rows16<16>(dst + ST::kKS, s.ks + (size_t)tb * 16, full, rows, lane);
-        stage_rows4(dst + ST::kKR, s.krn + tb, full, s.a16, rows, lane);
+        bulk_g2s(dst + ST::kKS, s.ks + (size_t)tb * 16, rows * 16, bar);
+        bulk_g2s(dst + ST::kKR, s.krn + tb, rows * 4, bar);
     }
-    stage_rows4(dst + ST::kKN, s.kn + tb, full, s.a16, rows, lane);
-    if constexpr (VB > 0) stage_rows16<ST::kRV>(dst + ST::kVC, s.vc + (size_t)tb * ST::kRV, full, rows, lane);
+    bulk_g2s(dst + ST::kKN, s.kn + tb, rows * 4, bar);
+    if constexpr (VB > 0) bulk_g2s(dst + ST::kVC, s.vc + (size_t)tb * ST::kRV, rows * ST::kRV, bar);
     if constexpr (VP) {
-        stage_rows16<16>(dst + ST::kVS, s.vs + (size_t)tb * 16, full, rows, lane);
-        stage_rows4(dst + ST::kVR, s.vrn + tb, full, s.a16, rows, lane);
+        bulk_g2s(dst + ST::kVS, s.vs + (size_t)tb * 16, rows * 16, bar);
+        bulk_g2s(dst + ST::kVR, s.vrn + tb, rows * 4, bar);
     }
-    stage_rows4(dst + ST::kVN, s.vn + tb, full, s.a16, rows, lane);
+    bulk_g2s(dst + ST::kVN, s.vn + tb, rows * 4, bar);
+}
+
+template <int KB, bool KP, int VB, bool VP>
+__device__ __forceinline__ void produce_stage(uint32_t dst, const Slab& s, int tb, int valid, int lane) {
+    using ST = Stage<KB, KP, VB, VP>;
+    if constexpr (KB > 0) copy_rows16<ST::kRK>(dst + ST::kKC, s.kc + (size_t)tb * ST::kRK, valid, lane);
+    if constexpr (KP) {
+        copy_rows16<16>(dst + ST::kKS, s.ks + (size_t)tb * 16, valid, lane);
+        copy_norms(dst + ST::kKR, s.krn + tb, s.a16, valid, lane);
+    }
+    copy_norms(dst + ST::kKN, s.kn + tb, s.a16, valid, lane);
+    if constexpr (VB > 0) copy_rows16<ST::kRV>(dst + ST::kVC, s.vc + (size_t)tb * ST::kRV, valid, lane);
+    if constexpr (VP) {
+        copy_rows16<16>(dst + ST::kVS, s.vs + (size_t)tb * 16, valid, lane);
+        copy_norms(dst + ST::kVR, s.vrn + tb, s.a16, valid, lane);
+    }
+    copy_norms(dst + ST::kVN, s.vn + tb, s.a16, valid, lane);
 }
 
 template <int NW>
@@ -401,30 +477,24 @@ __device__ __forceinline__ void read_words(uint32_t* w, const unsigned char* p) 
 }
 
 
-// Warps per CTA: 16 (two KV tiles of data in flight per warp, one CTA per SM);
-// prod values carry a second accumulator set and run 8 warps with more registers.
+// Consumer warps per CTA (one CTA per SM, plus one producer warp): prod values
+// carry a second accumulator set and run fewer warps with more registers.
 template <bool VP>
 struct Warps {
-    static constexpr int value = VP ? 8 : 16;
-};
-
-// The Q″ fragments stay in shared memory (one uint2 per lane and k16 block)
-// when registers are short.
-template <bool KP, bool VP>
-struct QsInSmem {
-    static constexpr bool value = KP && !VP;
+    static constexpr int value = VP ? 7 : 11;
 };
 
 template <int KB, bool KP, int VB, bool VP>
 struct Smem {
-    static constexpr int W = Warps<VP>::value;
-    // main phase: decode tables, queries, query scales, Q″ fragments, staging rings
+    static constexpr int W = Warps<VP>::value;    // consumer warps
+    static constexpr int kThreads = (W + 1) * 32;  // and the producer warp
+    // main phase: decode tables, queries, query scales, staging rings
     // tables (power-of-two sizes) largest first from a 32 KB-aligned base, so that
     // each one starts at a multiple of its own size
-    static constexpr size_t kSzK = Decoder<KB>::kTableBytes, kSzV = Decoder<VB>::kTableBytes;
-    static constexpr size_t kSzS = (KP || VP) ? SignDecoder::kTableBytes : 0;
+    static constexpr size_t kSzK = Table<KB>::kBytes, kSzV = Table<VB>::kBytes;
+    static constexpr size_t kSzS = KP ? KSignTable::kBytes : 0;
     static constexpr size_t kBig = 32768;
-    static constexpr size_t table_offset(int which) {  // 0 = keys, 1 = values, 2 = signs
+    static constexpr size_t table_offset(int which) {  // 0 = keys, 1 = values, 2 = key signs
         const size_t sz[3] = {kSzK, kSzV, kSzS};
         size_t off = 0;
         for (int i = 0; i < 3; ++i)
@@ -442,11 +512,14 @@ struct Smem {
     static constexpr size_t kTabK = table_offset(0), kTabV = table_offset(1), kTabS = table_offset(2);
     static constexpr size_t kQ = kSzK + kSzV + kSzS;
     static constexpr size_t kQsc = kQ + 2 * kHeads * kQRow * 4;
-    static constexpr size_t kQSf = kQsc + 2 * kHeads * 4;
-    static constexpr size_t kQKl = kQSf + (KP ? (size_t)kKB * 32 * 8 : 0);  // [kKB][32] f16 low parts of Q′
-    static constexpr size_t kQin = kQKl + (KB > 0 ? (size_t)kKB * 32 * 8 : 0);  // [kHeads][D] raw queries
+    static constexpr size_t kQin = kQsc + 2 * kHeads * 4;  // [kHeads][D] raw queries
     static constexpr size_t kStage = (kQin + (size_t)kHeads * D * 4 + 127) & ~(size_t)127;
-    static constexpr size_t kMain = kStage + (size_t)W * 2 * Stage<KB, KP, VB, VP>::kBytes;
+    static constexpr size_t kAlignSlack = kBig - 16;  // the 32 KB-aligned base lies at most this far in
+    static constexpr size_t kLimit = 232448 - 2048;   // per-CTA limit less static and reserved bytes
+    static constexpr int kStagesFit = (int)((kLimit - kAlignSlack - kStage) / Stage<KB, KP, VB, VP>::kBytes);
+    static constexpr int kStages = kStagesFit < kMaxStages ? kStagesFit : kMaxStages;
+    static_assert(kStages >= 4, "too few staging stages fit in shared memory");
+    static constexpr size_t kMain = kStage + (size_t)kStages * Stage<KB, KP, VB, VP>::kBytes;
     // combine phase (reuses the same bytes): per-warp maxima, sums, weights and
     // accumulators (the latter in fragment order: [warp][m][i][lane])
     static constexpr size_t kWM = 0;
@@ -463,145 +536,132 @@ struct Smem {
     static constexpr size_t kMP = (kMO + 2 * (size_t)kHeads * D * 4 + 15) & ~(size_t)15;  // [D][D] Π_v, then S_v
     static constexpr size_t kMQ = kMP + (VP ? 2 : 1) * (size_t)D * D * 4;  // [4][kHeads][D] mat-vec partials
     static constexpr size_t kMerge = kMQ + 4 * (size_t)kHeads * D * 4;
-    static constexpr size_t kAlignSlack = kBig - 16;  // the 32 KB-aligned base lies at most this far in
     static constexpr size_t kBytes0 = kMain + kAlignSlack > kCombine ? kMain + kAlignSlack : kCombine;
     static constexpr size_t kBytes = kBytes0 > kMerge ? kBytes0 : kMerge;
 };
 
-// Per-warp running state of the online softmax (heads 2c, 2c+1 of the lane)
-// and the value accumulators.
+// Per-lane running state of the online softmax (head g of the lane; the four
+// lanes of a quad share it) and the value accumulators (heads 2c, 2c + 1).
 template <bool VP>
 struct Acc {
     float O[kMT][4];
     float O2[VP ? kMT : 1][4];
-    float M[2], Mt[2], l[2];
+    float M, Mt, l;
 };
 
-template <int KB, bool KP, int VB, bool VP>
-__device__ __forceinline__ void step(Acc<VP>& st, const unsigned char* stp, int tb, int t1,
-                                     const Decoder<KB>& dk, const Decoder<VB>& dv, const SignDecoder& ds,
-                                     const uint32_t (&QK)[kKB][2],
-                                     const uint32_t (&QS)[kKB][2], const uint2* qsf, const uint2* qkl, int lane,
-                                     const float (&fK)[2],
-                                     const float (&fS)[2], const SplitArgs& a, size_t head0, int G, int g, int c) {
+// One 16-token step of a warp: tokens tb … tb + 15 (FULL: all below t1), rows
+// r0 … r0 + 15 of the stage at stp.  AQ[kb] = [Q′_hi; Q′_lo] fragments of head g,
+// AS[kb] = [Q″_hi; Q″_lo].  Lane (g, c) ends with the weights of head g for tokens 2c, 2c + 1 and
+// 8 + 2c, 9 + 2c, which are the B fragment of the value MMA.
+template <int KB, bool KP, int VB, bool VP, bool FULL>
+__device__ __forceinline__ void step(Acc<VP>& st, const unsigned char* stp, int r0, int tb, int t1,
+                                     const KDecoder<KB>& dk, const Decoder<VB>& dv, const SignDecoder& ds,
+                                     uint32_t stab, const uint32_t (&AQ)[kKB][4], const uint32_t (&AS)[kKB][4],
+                                     float fK, float fS, const SplitArgs& a, size_t head0, int G, int g, int c) {
     using ST = Stage<KB, KP, VB, VP>;
-    const bool vA = tb + g < t1, vB = tb + 8 + g < t1;
-    // staged words are read where they are used, to keep few registers live
-    auto kwords = [&](int i, uint32_t* w) { read_words<KB>(w, stp + ST::kKC + (g + 8 * i) * ST::kRK + c * (KB * 4)); };
-    auto vwords = [&](int i, uint32_t* w) { read_words<VB>(w, stp + ST::kVC + (g + 8 * i) * ST::kRV + c * (VB * 4)); };
-    auto word = [&](int off, int i) { return *reinterpret_cast<const uint32_t*>(stp + off + (g + 8 * i) * 16 + c * 4); };
-    auto norm = [&](int off, int i) { return *reinterpret_cast<const float*>(stp + off + (g + 8 * i) * 4); };
-
-    // ---- scores: S1 = K̃·Q′ᵀ (codes), S2 = Z·Q″ᵀ (QJL signs)
-    float S1[4] = {0.f, 0.f, 0.f, 0.f}, S2[4] = {0.f, 0.f, 0.f, 0.f};
-    if constexpr (KB > 0) {
-        uint32_t kwA[KB], kwB[KB];
-        kwords(0, kwA);
-        kwords(1, kwB);
+    // ---- scores of head g: S1 = [Q′_hi; Q′_lo]·K̃ᵀ (codes), S2 = [Q″_hi; Q″_lo]·Zᵀ (QJL signs)
+    // accumulator of group n: [0] (hi, token 2c) [1] (hi, 2c + 1) [2] (lo, 2c) [3] (lo, 2c + 1)
+    float S1[2][4], S2[2][4];
 #pragma unroll
-        for (int kb = 0; kb < kKB; ++kb) {
-            uint32_t a0, a1, a2, a3;
-            dk.pairs(kwA, kb, a0, a2);
-            dk.pairs(kwB, kb, a1, a3);
-            mma16816(S1, a0, a1, a2, a3, QK[kb][0], QK[kb][1]);
-            const uint2 lo = qkl[kb * 32 + lane];  // Q′ − f16(Q′): the score keeps ~2⁻²² of q′
-            mma16816(S1, a0, a1, a2, a3, lo.x, lo.y);
-        }
-    }
-    if constexpr (KP) {
-        const uint32_t ksA = word(ST::kKS, 0), ksB = word(ST::kKS, 1);
+    for (int n = 0; n < 2; ++n) {
 #pragma unroll
-        for (int m = 0; m < kKB / 2; ++m) {
-            uint32_t pa[4], pb[4];
-            ds.quad(ksA, m, pa);
-            ds.quad(ksB, m, pb);
-            uint2 q0, q1;
-            if constexpr (QsInSmem<KP, VP>::value) {
-                q0 = qsf[(2 * m) * 32 + lane];
-                q1 = qsf[(2 * m + 1) * 32 + lane];
-            } else {
-                q0 = make_uint2(QS[2 * m][0], QS[2 * m][1]);
-                q1 = make_uint2(QS[2 * m + 1][0], QS[2 * m + 1][1]);
+        for (int i = 0; i < 4; ++i) S1[n][i] = S2[n][i] = 0.f;
+        if constexpr (KB > 0) {
+            uint32_t w[KB];
+            read_words<KB>(w, stp + ST::kKC + (r0 + 8 * n + g) * ST::kRK + c * (KB * 4));
+#pragma unroll
+            for (int kb = 0; kb < kKB; ++kb) {
+                uint32_t b0, b1;
+                dk.frag(w, kb, b0, b1);
+                mma16816(S1[n], AQ[kb][0], AQ[kb][1], AQ[kb][2], AQ[kb][3], b0, b1);
             }
-            mma16816(S2, pa[0], pb[0], pa[1], pb[1], q0.x, q0.y);
-            mma16816(S2, pa[2], pb[2], pa[3], pb[3], q1.x, q1.y);
+        }
+        if constexpr (KP) {
+            const uint32_t ws = *reinterpret_cast<const uint32_t*>(stp + ST::kKS + (r0 + 8 * n + g) * 16 + c * 4);
+#pragma unroll
+            for (int j = 0; j < kKB / 2; ++j) {
+                const uint4 f = lds128(field_off<8, 7>(&ws, 8 * j) | stab);
+                mma16816(S2[n], AS[2 * j][0], AS[2 * j][1], AS[2 * j][2], AS[2 * j][3], f.x, f.y);
+                mma16816(S2[n], AS[2 * j + 1][0], AS[2 * j + 1][1], AS[2 * j + 1][2], AS[2 * j + 1][3], f.z, f.w);
+            }
         }
     }
-    // C layout: [0] (token g, head 2c) [1] (g, 2c+1) [2] (g+8, 2c) [3] (g+8, 2c+1)
+    // this lane's tokens: i = 0, 1 → 2c, 2c + 1; i = 2, 3 → 8 + 2c, 9 + 2c
+    auto norms = [&](int off, float (&v)[4]) {
+        const float2 x = *reinterpret_cast<const float2*>(stp + off + 4 * r0 + 8 * c);
+        const float2 y = *reinterpret_cast<const float2*>(stp + off + 4 * r0 + 32 + 8 * c);
+        v[0] = x.x;
+        v[1] = x.y;
+        v[2] = y.x;
+        v[3] = y.y;
+    };
+    float kn[4], vn[4], kr[4];
+    norms(ST::kKN, kn);
+    norms(ST::kVN, vn);
+    if constexpr (KP) norms(ST::kKR, kr);
     // z = s·log2e + log2‖v‖ (the exponent of the value weight), −∞ past the chunk
-    const float vnA = fmaxf(norm(ST::kVN, 0), 1e-30f), vnB = fmaxf(norm(ST::kVN, 1), 1e-30f);
-    const float knr[2] = {norm(ST::kKN, 0), norm(ST::kKN, 1)};
-    float krr[2] = {0.f, 0.f};
-    if constexpr (KP) {
-        krr[0] = norm(ST::kKR, 0);
-        krr[1] = norm(ST::kKR, 1);
-    }
-    const float lvA = lg2(vnA), lvB = lg2(vnB);
-    const float rvA = rcp(vnA), rvB = rcp(vnB);
-    float z[4];
+    float z[4], lv[4], rv[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const int tk = i >> 1, e = i & 1;
-        float v = fK[e] * S1[i];
-        if constexpr (KP) v = fmaf(fS[e] * krr[tk], S2[i], v);
-        z[i] = fmaf(knr[tk], v, tk ? lvB : lvA);
+        const int n = i >> 1, j = i & 1;
+        const float vv = fmaxf(vn[i], 1e-30f);
+        lv[i] = lg2(vv);
+        rv[i] = rcp(vv);
+        float v = fK * (S1[n][j] + S1[n][2 + j]);
+        if constexpr (KP) v = fmaf(fS * kr[i], S2[n][j] + S2[n][2 + j], v);
+        z[i] = fmaf(kn[i], v, lv[i]);
+        if constexpr (!FULL)
+            if (tb + 8 * n + 2 * c + j >= t1) z[i] = -INFINITY;
     }
-    if (!vA) z[0] = z[1] = -INFINITY;
-    if (!vB) z[2] = z[3] = -INFINITY;
-    if (a.scores != nullptr) {
+    if (a.scores != nullptr && g < G) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const int t = tb + g + 8 * (i >> 1), h = 2 * c + (i & 1);
-            if (((i >> 1) ? vB : vA) && h < G)
-                a.scores[(head0 + h) * a.T_max + t] = (z[i] - ((i >> 1) ? lvB : lvA)) * kLn2;
+            const int t = tb + 8 * (i >> 1) + 2 * c + (i & 1);
+            if (FULL || t < t1) a.scores[(head0 + g) * a.T_max + t] = (z[i] - lv[i]) * kLn2;
         }
     }
 
-    // ---- online softmax with a lazily raised maximum
-    const bool raise = fmaxf(z[0], z[2]) > st.Mt[0] || fmaxf(z[1], z[3]) > st.Mt[1];
-    if (__any_sync(0xffffffffu, raise)) {
-        float corr[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            float mx = fmaxf(z[e], z[2 + e]);
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-            const float Mn = fmaxf(st.M[e], mx);
-            corr[e] = ex2(st.M[e] - Mn);  // 0 on the first step (M = −∞)
-            st.M[e] = Mn;
-            st.Mt[e] = Mn + kSlack;
-            st.l[e] *= corr[e];
-        }
+    // ---- online softmax with a lazily raised maximum (head g, shared by the quad)
+    const float zm = fmaxf(fmaxf(z[0], z[1]), fmaxf(z[2], z[3]));
+    if (__any_sync(0xffffffffu, zm > st.Mt)) {
+        float mx = fmaxf(zm, __shfl_xor_sync(0xffffffffu, zm, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const float Mn = fmaxf(st.M, mx);
+        const float corr = Mn == -INFINITY ? 1.f : ex2(st.M - Mn);  // 0 on the first raise (M = −∞)
+        st.M = Mn;
+        st.Mt = Mn + kSlack;
+        st.l *= corr;
+        // the accumulators hold heads 2c and 2c + 1, whose state lives in quads 2c, 2c + 1
+        const float cA = __shfl_sync(0xffffffffu, corr, 8 * c), cB = __shfl_sync(0xffffffffu, corr, 8 * c + 4);
 #pragma unroll
         for (int m = 0; m < kMT; ++m) {
-            st.O[m][0] *= corr[0];
-            st.O[m][1] *= corr[1];
-            st.O[m][2] *= corr[0];
-            st.O[m][3] *= corr[1];
+            st.O[m][0] *= cA;
+            st.O[m][1] *= cB;
+            st.O[m][2] *= cA;
+            st.O[m][3] *= cB;
             if constexpr (VP) {
-                st.O2[m][0] *= corr[0];
-                st.O2[m][1] *= corr[1];
-                st.O2[m][2] *= corr[0];
-                st.O2[m][3] *= corr[1];
+                st.O2[m][0] *= cA;
+                st.O2[m][1] *= cB;
+                st.O2[m][2] *= cA;
+                st.O2[m][3] *= cB;
             }
         }
     }
     float pv[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const int e = i & 1;
-        pv[i] = ex2(z[i] - st.M[e]);
-        st.l[e] = fmaf(pv[i], (i >> 1) ? rvB : rvA, st.l[e]);
+        pv[i] = ex2(z[i] - st.M);
+        st.l = fmaf(pv[i], rv[i], st.l);
     }
-    const uint32_t PB0 = mov_trans(pack_h2(pv[0], pv[1]));
-    const uint32_t PB1 = mov_trans(pack_h2(pv[2], pv[3]));
+    // B fragment of the value MMA: head g, tokens (2c, 2c + 1) and (8 + 2c, 9 + 2c)
+    const uint32_t PB0 = pack_h2(pv[0], pv[1]);
+    const uint32_t PB1 = pack_h2(pv[2], pv[3]);
 
     // ---- values: Oᵀ += Ṽᵀ·P′ᵀ in the rotated frame
     if constexpr (VB > 0) {
         uint32_t vwA[VB], vwB[VB];
-        vwords(0, vwA);
-        vwords(1, vwB);
+        read_words<VB>(vwA, stp + ST::kVC + (r0 + g) * ST::kRV + c * (VB * 4));
+        read_words<VB>(vwB, stp + ST::kVC + (r0 + g + 8) * ST::kRV + c * (VB * 4));
 #pragma unroll
         for (int m = 0; m < kMT; ++m) {
             uint32_t x0, x1, y0, y1;
@@ -611,10 +671,18 @@ __device__ __forceinline__ void step(Acc<VP>& st, const unsigned char* stp, int 
         }
     }
     if constexpr (VP) {
-        const float gA = a.vgamma * norm(ST::kVR, 0), gB = a.vgamma * norm(ST::kVR, 1);
-        const uint32_t vsA = word(ST::kVS, 0), vsB = word(ST::kVS, 1);
-        const uint32_t QB0 = mov_trans(pack_h2(pv[0] * gA, pv[1] * gA));
-        const uint32_t QB1 = mov_trans(pack_h2(pv[2] * gB, pv[3] * gB));
+        float vr[4];
+        norms(ST::kVR, vr);
+        if constexpr (!FULL) {
+            // rows past the chunk may hold anything (bulk staging copies whole tiles)
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                if (tb + 8 * (i >> 1) + 2 * c + (i & 1) >= t1) vr[i] = 0.f;
+        }
+        const uint32_t QB0 = pack_h2(pv[0] * a.vgamma * vr[0], pv[1] * a.vgamma * vr[1]);
+        const uint32_t QB1 = pack_h2(pv[2] * a.vgamma * vr[2], pv[3] * a.vgamma * vr[3]);
+        const uint32_t vsA = *reinterpret_cast<const uint32_t*>(stp + ST::kVS + (r0 + g) * 16 + c * 4);
+        const uint32_t vsB = *reinterpret_cast<const uint32_t*>(stp + ST::kVS + (r0 + g + 8) * 16 + c * 4);
 #pragma unroll
         for (int m = 0; m < kMT / 2; ++m) {
             uint32_t pa[4], pb[4];
@@ -632,7 +700,7 @@ __device__ __forceinline__ void step(Acc<VP>& st, const unsigned char* stp, int 
 template <int KB, bool KP, int VB, bool VP>
 __device__ __forceinline__ void merge_group(const SplitArgs& a, unsigned char* smem, size_t head0, int G) {
     using SM = Smem<KB, KP, VB, VP>;
-    constexpr int NT = SM::W * 32;
+    constexpr int NT = SM::kThreads;
     float* wts = reinterpret_cast<float*>(smem + SM::kMW);   // [kHeads][kMaxSplits]
     float* linv = reinterpret_cast<float*>(smem + SM::kML);  // [kHeads]
     float* mo = reinterpret_cast<float*>(smem + SM::kMO);    // [2][D][kHeads]
@@ -735,7 +803,7 @@ __device__ __forceinline__ void merge_group(const SplitArgs& a, unsigned char* s
 }
 
 template <int KB, bool KP, int VB, bool VP>
-__global__ void __launch_bounds__(Warps<VP>::value * 32, 1) decode_split_mma_kernel(const SplitArgs a) {
+__global__ void __launch_bounds__((Warps<VP>::value + 1) * 32, 1) decode_split_mma_kernel(const SplitArgs a) {
     using SM = Smem<KB, KP, VB, VP>;
     using ST = Stage<KB, KP, VB, VP>;
     constexpr int W = SM::W;
@@ -745,8 +813,6 @@ __global__ void __launch_bounds__(Warps<VP>::value * 32, 1) decode_split_mma_ker
     unsigned char* mp = smem + (((sbase + (uint32_t)SM::kBig - 1u) & ~((uint32_t)SM::kBig - 1u)) - sbase);
     float* qsh = reinterpret_cast<float*>(mp + SM::kQ);     // [2][kHeads][kQRow]: q′, q″ (see qidx)
     float* qsc = reinterpret_cast<float*>(mp + SM::kQsc);   // [2][kHeads]
-    uint2* qsf = reinterpret_cast<uint2*>(mp + SM::kQSf);    // [kKB][32]
-    uint2* qkl = reinterpret_cast<uint2*>(mp + SM::kQKl);    // [kKB][32]
     __shared__ int s_last;
 
     const int hb = blockIdx.y % a.n_hblocks, kvh = blockIdx.y / a.n_hblocks;
@@ -784,30 +850,61 @@ __global__ void __launch_bounds__(Warps<VP>::value * 32, 1) decode_split_mma_ker
     sl.vn = a.vnorm + rowbase;
     sl.vrn = a.vrnorm + rowbase;
 
-    // start streaming this warp's first tile before the prologue
+    // ---- staging ring: warp W produces, warps 0 … W − 1 consume 16-token tiles
     const int ntiles = t1 > t0 ? (t1 - t0 + kTile - 1) / kTile : 0;
-    const uint32_t ring = smem_addr(mp + SM::kStage) + (uint32_t)(warp * 2 * ST::kBytes);
-    if (warp < ntiles) stage_tile<KB, KP, VB, VP>(ring, sl, t0 + warp * kTile, t1, lane);
-    cp_async_commit();
+    const int nstages = (ntiles + kStageRows / kTile - 1) / (kStageRows / kTile);
+    const uint32_t ring = smem_addr(mp + SM::kStage);
+    __shared__ __align__(8) uint64_t s_full[SM::kStages], s_empty[SM::kStages];
+    const bool producer = warp == W;
+    // the producer fills the first stages before the prologue, so that they land
+    // while the tables and queries are prepared
+    // bulk staging when every slab's norm rows start on a 16-byte boundary:
+    // one lane, one copy per plane and stage
+    const bool bulk = (a.T_max & 3) == 0;
+    auto produce = [&](int i) {
+        const int tb = t0 + i * kStageRows;
+        const uint32_t dst = ring + (uint32_t)((i % SM::kStages) * ST::kBytes);
+        const uint32_t bar = smem_addr(&s_full[i % SM::kStages]);
+        if (bulk) {
+            if (lane == 0) produce_stage_bulk<KB, KP, VB, VP>(dst, bar, sl, tb, a.T_max);
+        } else {
+            produce_stage<KB, KP, VB, VP>(dst, sl, tb, t1 - tb, lane);
+            // the stage's full barrier counts one arrival per producer lane, made when
+            // that lane's copies have landed
+            asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+        }
+    };
+    if (producer) {
+        if (lane == 0) {
+            for (int i = 0; i < SM::kStages; ++i) {
+                sm100::mbar_init(&s_full[i], bulk ? 1 : 32);
+                sm100::mbar_init(&s_empty[i], kStageRows / kTile);
+            }
+            sm100::fence_barrier_init();
+        }
+        __syncwarp();
+        for (int i = 0; i < min(nstages, SM::kStages); ++i) produce(i);
+    }
 
     // ---- prologue: decode tables, queries, query scales
     // raw queries of this head block: loads issued before the table fill, stored after
-    constexpr int NT = W * 32, kQPer = kHeads * D / NT;
+    constexpr int NT = SM::kThreads, kQPer = (kHeads * D + NT - 1) / NT;
     float qv[kQPer];
 #pragma unroll
     for (int r = 0; r < kQPer; ++r) {
         const int i = threadIdx.x + r * NT, h = i / D;
         const size_t gi = (head0 + h) * D + (i % D);
-        qv[r] = h < G ? (a.q_f32 ? __ldg(static_cast<const float*>(a.q) + gi)
-                                 : __bfloat162float(static_cast<const __nv_bfloat16*>(a.q)[gi]))
-                      : 0.f;
+        qv[r] = (i < kHeads * D && h < G) ? (a.q_f32 ? __ldg(static_cast<const float*>(a.q) + gi)
+                                                     : __bfloat162float(static_cast<const __nv_bfloat16*>(a.q)[gi]))
+                                          : 0.f;
     }
-    Decoder<KB>::fill(mp + SM::kTabK, a.kcb);
-    Decoder<VB>::fill(mp + SM::kTabV, a.vcb);
-    if constexpr (KP || VP) SignDecoder::fill(mp + SM::kTabS);
+    Table<KB>::fill(mp + SM::kTabK, a.kcb);
+    Table<VB>::fill(mp + SM::kTabV, a.vcb);
+    if constexpr (KP) KSignTable::fill(mp + SM::kTabS);
     float* qin = reinterpret_cast<float*>(mp + SM::kQin);  // [kHeads][D]
 #pragma unroll
-    for (int r = 0; r < kQPer; ++r) qin[threadIdx.x + r * NT] = qv[r];
+    for (int r = 0; r < kQPer; ++r)
+        if (threadIdx.x + r * NT < kHeads * D) qin[threadIdx.x + r * NT] = qv[r];
     __syncthreads();
     // q′ = Π_k·q and q″ = S_k·q on the tensor cores: D[16 × 8 dims] = A·B with
     // A = [bf16 hi of the 8 heads' q; bf16 lo] and B = a bf16 half of the matrix,
@@ -831,12 +928,12 @@ __global__ void __launch_bounds__(Warps<VP>::value * 32, 1) decode_split_mma_ker
                 A[ks][2 * hh + 1] = pack_bf2(x.x - hf.x, x.y - hf.y);
             }
         }
-        constexpr int kJobs = (KP ? 2 : 1) * (D / 8);
-        constexpr int kPer = (kJobs + W - 1) / W;  // tiles per warp
+        constexpr int kJobs = (KP ? 2 : 1) * (D / 8), kAll = W + 1;
+        constexpr int kPer = (kJobs + kAll - 1) / kAll;  // tiles per warp
         uint4 bh[kPer][kKB / 2], bl[kPer][kKB / 2];  // bf16 dims 32p + 8c … + 7 of row j0 + g
 #pragma unroll
         for (int u = 0; u < kPer; ++u) {
-            const int job = warp + u * W;
+            const int job = warp + u * kAll;
             if (job < kJobs) {
                 const int second = job >= D / 8, j0 = 8 * (job % (D / 8));
                 const uint4* Mh = reinterpret_cast<const uint4*>(second ? a.kS_hi : a.kPi_hi);
@@ -851,7 +948,7 @@ __global__ void __launch_bounds__(Warps<VP>::value * 32, 1) decode_split_mma_ker
         }
 #pragma unroll
         for (int u = 0; u < kPer; ++u) {
-            const int job = warp + u * W;
+            const int job = warp + u * kAll;
             if (job < kJobs) {
                 const int second = job >= D / 8, j0 = 8 * (job % (D / 8));
                 float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -887,67 +984,6 @@ __global__ void __launch_bounds__(Warps<VP>::value * 32, 1) decode_split_mma_ker
     }
     __syncthreads();
 
-    // B fragments of Q′ (and Q″) for head g, k order following the decoded pairs.
-    uint32_t QK[kKB][2], QS[kKB][2];
-    {
-        const float i1 = 1.f / qsc[g], i2 = 1.f / qsc[kHeads + g];
-        // this lane's 32 dims of q′ (and q″): chunk c of head g, eight 16-byte loads
-        float q1[32], q2[32];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const float4 u = *reinterpret_cast<const float4*>(qsh + qidx(g, 32 * c) + 4 * k);
-            q1[4 * k] = u.x;
-            q1[4 * k + 1] = u.y;
-            q1[4 * k + 2] = u.z;
-            q1[4 * k + 3] = u.w;
-            if constexpr (KP) {
-                const float4 v = *reinterpret_cast<const float4*>(qsh + kHeads * kQRow + qidx(g, 32 * c) + 4 * k);
-                q2[4 * k] = v.x;
-                q2[4 * k + 1] = v.y;
-                q2[4 * k + 2] = v.z;
-                q2[4 * k + 3] = v.w;
-            }
-        }
-#pragma unroll
-        for (int kb = 0; kb < kKB; ++kb) {
-#pragma unroll
-            uint32_t lo[2] = {0u, 0u};
-            for (int h = 0; h < 2; ++h) {
-                const int tau = 2 * kb + h;
-                if constexpr (KB > 0) {
-                    // f16 high part for the fragment, f16 low part (the rounding error) for a second MMA
-                    const float x0 = q1[Decoder<KB>::dim(0, tau, 0)] * i1, x1 = q1[Decoder<KB>::dim(0, tau, 1)] * i1;
-                    const __half2 hh = __floats2half2_rn(x0, x1);
-                    const float2 hf = __half22float2(hh);
-                    QK[kb][h] = *reinterpret_cast<const uint32_t*>(&hh);
-                    lo[h] = pack_h2(x0 - hf.x, x1 - hf.y);
-                } else {
-                    QK[kb][h] = 0u;
-                }
-                QS[kb][h] = KP ? pack_h2(q2[sign_dim(0, tau, 0)] * i2, q2[sign_dim(0, tau, 1)] * i2) : 0u;
-            }
-            if constexpr (QsInSmem<KP, VP>::value)
-                if (warp == 0) qsf[kb * 32 + lane] = make_uint2(QS[kb][0], QS[kb][1]);
-            if constexpr (KB > 0)
-                if (warp == 0) qkl[kb * 32 + lane] = make_uint2(lo[0], lo[1]);
-        }
-    }
-    __syncthreads();
-    // score factors for this lane's two heads (2c, 2c+1), log2 units
-    const float scale2 = a.scale * kLog2e;
-    float fK[2], fS[2];
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-        fK[e] = scale2 * qsc[2 * c + e] / a.kcb.lut_scale;
-        fS[e] = scale2 * a.kgamma * qsc[kHeads + 2 * c + e];
-    }
-    Decoder<KB> dk;
-    Decoder<VB> dv;
-    dk.init(a.kcb, mp + SM::kTabK, lane);
-    dv.init(a.vcb, mp + SM::kTabV, lane);
-    SignDecoder ds;
-    ds.init(mp + SM::kTabS, lane);
-
     Acc<VP> st;
 #pragma unroll
     for (int m = 0; m < kMT; ++m)
@@ -956,55 +992,118 @@ __global__ void __launch_bounds__(Warps<VP>::value * 32, 1) decode_split_mma_ker
             st.O[m][i] = 0.f;
             if constexpr (VP) st.O2[m][i] = 0.f;
         }
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-        st.M[e] = -INFINITY;
-        st.Mt[e] = -INFINITY;
-        st.l[e] = 0.f;
-    }
+    st.M = -INFINITY;
+    st.Mt = -INFINITY;
+    st.l = 0.f;
 
-    // ---- main loop over this warp's tiles: tile k is staged in ring slot k & 1
-    int slot = 0;
-    for (int tile = warp; tile < ntiles; tile += W) {
-        const int tb = t0 + tile * kTile;
-        if (tile + W < ntiles) stage_tile<KB, KP, VB, VP>(ring + (slot ^ 1) * ST::kBytes, sl, tb + W * kTile, t1, lane);
-        cp_async_commit();
-        cp_async_wait<1>();
-        __syncwarp();
-        step<KB, KP, VB, VP>(st, mp + SM::kStage + (size_t)(warp * 2 + slot) * ST::kBytes, tb, t1, dk, dv, ds, QK,
-                             QS, qsf, qkl, lane, fK, fS, a, head0, G, g, c);
-        __syncwarp();  // the slot may be refilled once every lane has read it
-        slot ^= 1;
+    if (producer) {
+        // ---- producer: refill each stage once its four tiles have been consumed
+        for (int i = SM::kStages; i < nstages; ++i) {
+            const bool ok = sm100::mbar_wait(&s_empty[i % SM::kStages], (uint32_t)((i / SM::kStages - 1) & 1), a.status,
+                                             kDecodeStageTimeout);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            produce(i);
+        }
+        cp_async_wait<0>();  // every copy this warp issued has landed
+    } else {
+        // A fragments of head g: [Q′_hi; Q′_lo] for the codes and [Q″_hi; Q″_lo] for
+        // the QJL signs, k order following the key decoders' dims
+        uint32_t AQ[kKB][4], AS[kKB][4];
+        {
+            const float i1 = 1.f / qsc[g], i2 = 1.f / qsc[kHeads + g];
+            // this lane's 32 dims of q′ (and q″): chunk c of head g, eight 16-byte loads
+            float q1[32], q2[32];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const float4 u = *reinterpret_cast<const float4*>(qsh + qidx(g, 32 * c) + 4 * k);
+                q1[4 * k] = u.x;
+                q1[4 * k + 1] = u.y;
+                q1[4 * k + 2] = u.z;
+                q1[4 * k + 3] = u.w;
+                if constexpr (KP) {
+                    const float4 v = *reinterpret_cast<const float4*>(qsh + kHeads * kQRow + qidx(g, 32 * c) + 4 * k);
+                    q2[4 * k] = v.x;
+                    q2[4 * k + 1] = v.y;
+                    q2[4 * k + 2] = v.z;
+                    q2[4 * k + 3] = v.w;
+                }
+            }
+            // f16 high part of a pair for rows 0–7, its rounding error for rows 8–15
+            auto split = [](float x0, float x1, uint32_t& hi, uint32_t& lo) {
+                const __half2 hh = __floats2half2_rn(x0, x1);
+                const float2 hf = __half22float2(hh);
+                hi = *reinterpret_cast<const uint32_t*>(&hh);
+                lo = pack_h2(x0 - hf.x, x1 - hf.y);
+            };
+#pragma unroll
+            for (int kb = 0; kb < kKB; ++kb) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {  // h = 0: k slots 2c, 2c + 1; h = 1: 2c + 8, 2c + 9
+                    if constexpr (KB > 0)
+                        split(q1[KDecoder<KB>::dim(0, kb, 2 * h)] * i1, q1[KDecoder<KB>::dim(0, kb, 2 * h + 1)] * i1,
+                              AQ[kb][2 * h], AQ[kb][2 * h + 1]);
+                    else
+                        AQ[kb][2 * h] = AQ[kb][2 * h + 1] = 0u;
+                    if constexpr (KP)
+                        split(q2[ksign_dim(0, kb, 2 * h)] * i2, q2[ksign_dim(0, kb, 2 * h + 1)] * i2, AS[kb][2 * h],
+                              AS[kb][2 * h + 1]);
+                    else
+                        AS[kb][2 * h] = AS[kb][2 * h + 1] = 0u;
+                }
+            }
+        }
+        // score factors of head g, log2 units
+        const float scale2 = a.scale * kLog2e;
+        const float fK = scale2 * qsc[g] / a.kcb.lut_scale;
+        const float fS = scale2 * a.kgamma * qsc[kHeads + g];
+        KDecoder<KB> dk;
+        Decoder<VB> dv;
+        dk.init(a.kcb, mp + SM::kTabK, lane);
+        dv.init(a.vcb, mp + SM::kTabV, lane);
+        SignDecoder ds;
+        const uint32_t stab = KP ? KSignTable::lane_base(mp + SM::kTabS, lane) : 0u;
+
+        // ---- consumers: tile t is rows 16·(t mod 4) … of stage t / 4
+        for (int tile = warp; tile < ntiles; tile += W) {
+            const int stage = tile >> 2, slot = stage % SM::kStages;
+            const bool ok = sm100::mbar_wait(&s_full[slot], (uint32_t)((stage / SM::kStages) & 1), a.status,
+                                             kDecodeStageTimeout);
+            if (!__all_sync(0xffffffffu, ok)) break;  // the warp gives up together
+            const int tb = t0 + tile * kTile, r0 = (tile & 3) * kTile;
+            const unsigned char* stp = mp + SM::kStage + (size_t)slot * ST::kBytes;
+            if (tb + kTile <= t1)
+                step<KB, KP, VB, VP, true>(st, stp, r0, tb, t1, dk, dv, ds, stab, AQ, AS, fK, fS, a, head0, G, g, c);
+            else
+                step<KB, KP, VB, VP, false>(st, stp, r0, tb, t1, dk, dv, ds, stab, AQ, AS, fK, fS, a, head0, G, g, c);
+            __syncwarp();  // every lane has read the tile before the stage is released
+            if (lane == 0) sm100::mbar_arrive(&s_empty[slot]);
+        }
     }
-    cp_async_wait<0>();
 
     // ---- combine the warps of this CTA into one split partial per head
-#pragma unroll
-    for (int e = 0; e < 2; ++e)
-#pragma unroll
-        for (int o = 4; o < 32; o <<= 1) st.l[e] += __shfl_xor_sync(0xffffffffu, st.l[e], o);
+    st.l += __shfl_xor_sync(0xffffffffu, st.l, 1);
+    st.l += __shfl_xor_sync(0xffffffffu, st.l, 2);
     __syncthreads();  // tables, queries and rings are dead from here on
     float* wM = reinterpret_cast<float*>(smem + SM::kWM);    // [warp][head] running maxima
     float* wL = reinterpret_cast<float*>(smem + SM::kWL);    // [warp][head] sums
     float* wF = reinterpret_cast<float*>(smem + SM::kWF);    // [warp][head] weights 2^(M_w − max_w M_w)
     float* wO = reinterpret_cast<float*>(smem + SM::kWO);    // [warp][m][i][lane]
     float* wO2 = reinterpret_cast<float*>(smem + SM::kWO2);  // [warp][m][i][lane] (prod values)
-    if (g == 0) {
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            wM[warp * kHeads + 2 * c + e] = st.M[e];
-            wL[warp * kHeads + 2 * c + e] = st.l[e];
-        }
-    }
     // accumulators in fragment order: each store is 32 consecutive words
     constexpr int kFrag = kMT * 4 * 32;
-#pragma unroll
-    for (int m = 0; m < kMT; ++m)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            wO[warp * kFrag + (m * 4 + i) * 32 + lane] = st.O[m][i];
-            if constexpr (VP) wO2[warp * kFrag + (m * 4 + i) * 32 + lane] = st.O2[m][i];
+    if (!producer) {
+        if (c == 0) {
+            wM[warp * kHeads + g] = st.M;
+            wL[warp * kHeads + g] = st.l;
         }
+#pragma unroll
+        for (int m = 0; m < kMT; ++m)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                wO[warp * kFrag + (m * 4 + i) * 32 + lane] = st.O[m][i];
+                if constexpr (VP) wO2[warp * kFrag + (m * 4 + i) * 32 + lane] = st.O2[m][i];
+            }
+    }
     __syncthreads();
     if (threadIdx.x < kHeads) {
         const int h = threadIdx.x;
@@ -1062,11 +1161,12 @@ __global__ void __launch_bounds__(Warps<VP>::value * 32, 1) decode_split_mma_ker
 template <int KB, bool KP, int VB, bool VP>
 int launch_split_mma(const SplitArgs& a, dim3 grid, cudaStream_t s) {
     using SM = Smem<KB, KP, VB, VP>;
+    static_assert(SM::kBytes <= 232448 - 1024, "decode shared memory above the per-CTA limit");
     auto fn = decode_split_mma_kernel<KB, KP, VB, VP>;
     static std::atomic<uint64_t> smem_set{0};
     const int rc = ensure_smem_attr(smem_set, (const void*)fn, (int)SM::kBytes, "decode (tensor-core) smem attribute");
     if (rc != TQ_OK) return rc;
-    fn<<<grid, SM::W * 32, SM::kBytes, s>>>(a);
+    fn<<<grid, SM::kThreads, SM::kBytes, s>>>(a);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? TQ_OK : cuda_fail(e, "decode (tensor-core) split launch");
 }

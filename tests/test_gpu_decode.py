@@ -72,6 +72,24 @@ def test_decode_edge_lengths(tq):
     assert np.all(g[0] == 0)
 
 
+@pytest.mark.parametrize("T,lens", [(701, [701, 333, 1, 0]), (1002, [1002, 999, 16, 17])])
+def test_decode_slabs_not_16_byte_aligned(tq, T, lens):
+    # T_max % 4 != 0: slab norm rows start off 16-byte boundaries, so tiles are
+    # staged by per-lane copies instead of bulk copies; prod values on the second
+    g, r = _run(tq, B=4, Hq=16, Hkv=2, T=T, d=128, kb=3, kv="prod", vb=3, vv="mse" if T == 701 else "prod",
+                lens=lens, seed=T)
+    check_attention(g, r)
+
+
+@pytest.mark.parametrize("vv", ["mse", "prod"])
+def test_decode_bulk_staging_tail_rows(tq, vv):
+    # T_max % 16 == 4: the last tile of a slab copies only 4 rows; lengths end
+    # inside tiles so the rows past each chunk are masked
+    g, r = _run(tq, B=3, Hq=8, Hkv=2, T=1028, d=128, kb=4, kv="prod", vb=2, vv=vv, lens=[1028, 1027, 515],
+                seed=11)
+    check_attention(g, r)
+
+
 def test_decode_needle(tq):
     # planted keys aligned with the query make the softmax peak, so 2e-3 max-abs bites
     g, r = _run(tq, B=1, Hq=8, Hkv=1, T=4096, d=128, kb=3, kv="prod", vb=3, vv="mse", lens=[4096],
