@@ -330,6 +330,289 @@ int launch_tc_d(const tq_ctx& h, const CUtensorMap& tm_x, int64_t n_rows, const 
 
 
 // ---------------------------------------------------------------------------
+// d = 256, mse: Π_hi + Π_lo (256 KB of bf16) do not fit beside the row tiles, so
+// Π is streamed with them.  A stage holds 64-dim chunk c of a 128-row tile and
+// the same 64 columns of Π_hi and Π_lo (all 256 output rows, 128-byte swizzled);
+// per k16 step and pass one N = 256 MMA accumulates Y = X·Πᵀ over the four chunks
+// into one of two 256-column TMEM slots.  Four epilogue warpgroups, two per slot,
+// each take half of the columns; the halves of ‖y‖² meet in shared memory behind
+// a named barrier.  Π is re-read from L2 for every tile: 256 KB per 128 rows,
+// which keeps this path near the tensor and L2 rates rather than HBM's.
+constexpr int k256Stages = 2;
+constexpr int k256EpiWarps = 16;
+constexpr int k256Threads = 32 * (2 + k256EpiWarps);
+
+struct Cfg256 {
+    static constexpr int D = 256;
+    static constexpr int kChunks = D / kKC;                      // 4
+    static constexpr int kXBytes = kTile * 128;                  // 16 KB: 128 rows × 64 bf16
+    static constexpr int kPBytes = D * 128;                      // 32 KB: 256 rows × 64 bf16
+    static constexpr int kStageBytes = kXBytes + 2 * kPBytes;    // 80 KB
+    static constexpr size_t kBarOffset = (size_t)k256Stages * kStageBytes;
+    static constexpr size_t kXchOffset = kBarOffset + 256;      // [slot][half][row] partial ‖y‖²
+    static constexpr size_t kSmemBytes = kXchOffset + (size_t)2 * 2 * kTile * 4 + 1024;
+};
+
+template <int BM>
+__global__ void __launch_bounds__(k256Threads, 1)
+quantize_mse_tc256_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_pi_hi,
+                          const __grid_constant__ CUtensorMap tm_pi_lo, int64_t n_rows, int npass, float norm_scale,
+                          Codebook cb, uint8_t* __restrict__ codes, float* __restrict__ norm_out,
+                          int* __restrict__ status) {
+    using C = Cfg256;
+    constexpr int D = C::D;
+    constexpr int H = D / 2;              // columns per half
+    constexpr int L = 1 << BM;
+    constexpr int P = L / 2 - 1;          // positive decision boundaries
+    constexpr int WORDS = BM * D / 32;    // packed 32-bit words per row
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* stages = smem;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
+    uint64_t* full = bars;                 // [k256Stages] chunk landed
+    uint64_t* empty = full + k256Stages;   // [k256Stages] chunk consumed by the MMAs
+    uint64_t* tfull = empty + k256Stages;  // [2] Y ready
+    uint64_t* tempty = tfull + 2;          // [2] slot read out (256 arrivals)
+    uint64_t* drain = tempty + 2;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t ntiles = (n_rows + kTile - 1) / kTile;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < k256Stages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&tfull[a], 1);
+            mbar_init(&tempty[a], 256);
+        }
+        mbar_init(drain, 1);
+        fence_barrier_init();
+    }
+    if (warp == 1) tmem_alloc(tmem_holder, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------------------ producer
+        prefetch_tensormap(&tm_x);
+        prefetch_tensormap(&tm_pi_hi);
+        prefetch_tensormap(&tm_pi_lo);
+        int64_t q = 0;  // chunks issued
+        bool ok = true;
+        for (int64_t tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
+            for (int c = 0; c < C::kChunks; ++c, ++q) {
+                const int s = (int)(q % k256Stages);
+                const int64_t u = q / k256Stages;
+                if (u > 0 && !(ok = mbar_wait(&empty[s], (uint32_t)((u - 1) & 1), status, 21))) break;
+                uint8_t* st = stages + (size_t)s * C::kStageBytes;
+                mbar_arrive_expect_tx(&full[s], C::kXBytes + npass * C::kPBytes);
+                tma_load_2d(st, &tm_x, &full[s], c * kKC, (int)(tile * kTile));
+                tma_load_2d(st + C::kXBytes, &tm_pi_hi, &full[s], c * kKC, 0);
+                if (npass == 2) tma_load_2d(st + C::kXBytes + C::kPBytes, &tm_pi_lo, &full[s], c * kKC, 0);
+            }
+        }
+        // every load issued must have landed before the CTA may exit
+        for (int64_t k = (q > k256Stages ? q - k256Stages : 0); k < q; ++k)
+            mbar_wait(&full[k % k256Stages], (uint32_t)((k / k256Stages) & 1), status, 22);
+    } else if (warp == 1 && lane == 0) {
+        // ------------------------------------------------------------ MMA issuer
+        constexpr uint32_t idesc = idesc_bf16_f32(kTile, D);
+        const uint32_t base = smem_u32(stages);
+        int64_t q = 0, i = 0;
+        bool ok = true;
+        for (int64_t tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x, ++i) {
+            const int a = (int)(i & 1);
+            const int64_t ua = i >> 1;
+            if (ua > 0 && !(ok = mbar_wait(&tempty[a], (uint32_t)((ua - 1) & 1), status, 23))) break;
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + (uint32_t)(a * D);
+            for (int c = 0; c < C::kChunks; ++c, ++q) {
+                const int s = (int)(q % k256Stages);
+                if (!(ok = mbar_wait(&full[s], (uint32_t)((q / k256Stages) & 1), status, 24))) break;
+                tc_fence_after();
+                const uint32_t st = base + (uint32_t)(s * C::kStageBytes);
+#pragma unroll
+                for (int pass = 0; pass < 2; ++pass) {
+                    if (pass >= npass) break;
+#pragma unroll
+                    for (int kk = 0; kk < kKC / 16; ++kk) {
+                        const uint64_t ad = smem_desc(st + kk * 32, 1024, 2);
+                        const uint64_t bd = smem_desc(st + C::kXBytes + pass * C::kPBytes + kk * 32, 1024, 2);
+                        mma_f16_ss(d_tmem, ad, bd, idesc, (c | kk | pass) != 0);
+                    }
+                }
+                mma_commit(&empty[s]);
+            }
+            if (ok) mma_commit(&tfull[a]);
+        }
+        mma_commit(drain);
+        mbar_wait(drain, 0, status, 25);
+    } else if (warp >= 2) {
+        // ------------------------------------------------------------ epilogue
+        constexpr int GB = BM == 3 ? 24 : 16;  // bits per float packing group
+        constexpr int GC = GB / BM;            // codes per group
+        constexpr int NG = 32 / GC;            // groups per 32-code TMEM chunk
+        constexpr float kAcc0 = (float)(1u << (GB - 1)) - 0.5f;
+        const int wg = (warp - 2) >> 2;        // 0..3
+        const int slot = wg >> 1, half = wg & 1;
+        const int quad = warp & 3;             // TMEM lane quadrant of this warp
+        const int r_local = quad * 32 + lane;
+        float* xss = reinterpret_cast<float*>(smem + C::kXchOffset) + slot * (2 * kTile);  // [half][row]
+        float t2[P > 0 ? P : 1];
+#pragma unroll
+        for (int p = 0; p < P; ++p) t2[p] = cb.t[L / 2 + p] * cb.t[L / 2 + p];
+        const uint32_t ybase = tmem_base + (uint32_t)(slot * D + half * H) + ((uint32_t)(quad * 32) << 16);
+        auto pair_sync = [&]() { asm volatile("bar.sync %0, 256;" ::"r"(1 + slot) : "memory"); };
+        // the two halves of a slot leave the tile loop together when a wait gives up
+        auto pair_all = [&](bool ok) -> bool {
+            uint32_t r;
+            asm volatile(
+                "{\n\t.reg .pred p, q;\n\t"
+                "setp.ne.u32 p, %1, 0;\n\t"
+                "bar.red.and.pred q, %2, 256, p;\n\t"
+                "selp.u32 %0, 1, 0, q;\n\t}\n"
+                : "=r"(r)
+                : "r"((uint32_t)ok), "r"(1 + slot)
+                : "memory");
+            return r != 0;
+        };
+        int64_t j = 0;
+        for (int64_t tile = blockIdx.x + (int64_t)slot * gridDim.x; tile < ntiles; tile += 2 * (int64_t)gridDim.x, ++j) {
+            if (!pair_all(mbar_wait(&tfull[slot], (uint32_t)(j & 1), status, 26))) break;
+            tc_fence_after();
+            uint32_t r[2][32];
+            // pass 1: this half's part of ‖y‖², summed with the other half's
+            uint64_t ss2 = 0ull;
+#pragma unroll
+            for (int c = 0; c < H / 32; c += 2) {
+                tmem_ld32(ybase + c * 32, r[0]);
+                tmem_ld32(ybase + (c + 1) * 32, r[1]);
+                tmem_wait_ld(r[0]);
+                tmem_wait_ld(r[1]);
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int k = 0; k < 32; k += 2) {
+                        const uint64_t v2 = f2(__uint_as_float(r[h][k]), __uint_as_float(r[h][k + 1]));
+                        ss2 = fma2(v2, v2, ss2);
+                    }
+            }
+            float ssa, ssb;
+            f2_split(ss2, ssa, ssb);
+            xss[half * kTile + r_local] = ssa + ssb;
+            pair_sync();
+            const float ss = xss[r_local] + xss[kTile + r_local];  // same order in both halves
+            const float n = sqrtf(ss);
+            const float cs = ss >= 0x1p-38f ? __fdividef(0x1p62f, ss) : 0x1p100f;
+            const float kr = cs * ss;
+            const uint64_t cs2 = f2(cs, cs);
+            float kt2[P > 0 ? P : 1];
+#pragma unroll
+            for (int p = 0; p < P; ++p) kt2[p] = -kr * t2[p];
+            const int64_t row = tile * kTile + r_local;
+            const bool live = row < n_rows;
+            const uint32_t keep = n == 0.f ? 0u : 0xffffffffu;
+            uint8_t* dst = codes + row * (int64_t)(WORDS * 4) + half * (H / 32) * (BM * 4);
+            // pass 2: chunk c + 1 is loaded while chunk c is bucketized
+            tmem_ld32(ybase, r[0]);
+#pragma unroll
+            for (int c = 0; c < H / 32; ++c) {
+                tmem_wait_ld(r[c & 1]);
+                if (c + 1 < H / 32) tmem_ld32(ybase + (c + 1) * 32, r[(c + 1) & 1]);
+                const uint32_t* rc = r[c & 1];
+                uint64_t acc[NG];
+#pragma unroll
+                for (int gi = 0; gi < NG; ++gi) acc[gi] = f2(kAcc0, 0.f);
+#pragma unroll
+                for (int k = 0; k < 32; k += 2) {
+                    const float va = __uint_as_float(rc[k]), vb = __uint_as_float(rc[k + 1]);
+                    uint64_t cnt2 = f2(0.5f, 0.5f);
+                    if constexpr (P > 0) {
+                        float wa, wb;
+                        f2_split(mul2(f2(va, vb), cs2), wa, wb);
+#pragma unroll
+                        for (int p = 0; p < P; ++p)
+                            cnt2 = add2(cnt2, f2(__saturatef(fmaf(va, wa, kt2[p])), __saturatef(fmaf(vb, wb, kt2[p]))));
+                    }
+                    float ca, cb2;
+                    f2_split(cnt2, ca, cb2);
+                    const float sa = __uint_as_float(__float_as_uint(ca) | (__float_as_uint(va) & 0x80000000u));
+                    const float sb = __uint_as_float(__float_as_uint(cb2) | (__float_as_uint(vb) & 0x80000000u));
+                    acc[k / GC] = fma2(f2(sa, sb),
+                                       f2((float)(1u << (BM * (k % GC))), (float)(1u << (BM * ((k + 1) % GC)))),
+                                       acc[k / GC]);
+                }
+                uint32_t cw[BM];
+#pragma unroll
+                for (int w = 0; w < BM; ++w) cw[w] = 0u;
+#pragma unroll
+                for (int gi = 0; gi < NG; ++gi) {
+                    float ea, eb;
+                    f2_split(acc[gi], ea, eb);
+                    const uint32_t gbits = __float2uint_rn(ea + eb);
+                    const int bit = gi * GB, w = bit >> 5, sh = bit & 31;
+                    cw[w] |= gbits << sh;
+                    if (sh + GB > 32) cw[w + 1] |= gbits >> (32 - sh);
+                }
+                if (live) {
+                    uint8_t* cd = dst + c * (BM * 4);
+                    if constexpr (BM == 4) {
+                        *reinterpret_cast<uint4*>(cd) = make_uint4(cw[0] & keep, cw[1] & keep, cw[2] & keep, cw[3] & keep);
+                    } else if constexpr (BM == 2) {
+                        *reinterpret_cast<uint2*>(cd) = make_uint2(cw[0] & keep, cw[1] & keep);
+                    } else {
+#pragma unroll
+                        for (int w = 0; w < BM; ++w) reinterpret_cast<uint32_t*>(cd)[w] = cw[w] & keep;
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&tempty[slot]);
+            if (live && half == 0) norm_out[row] = n * norm_scale;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, 512);
+    }
+}
+
+template <int BM>
+int launch_tc256(const tq_ctx& h, const CUtensorMap& tm_x, int64_t n_rows, const tq_planes& out, cudaStream_t s) {
+    using C = Cfg256;
+    static_assert(C::kSmemBytes <= 232448, "d = 256 quantize shared memory above the per-CTA limit");
+    auto fn = quantize_mse_tc256_kernel<BM>;
+    static std::atomic<uint64_t> smem_set{0};
+    const int rc = ensure_smem_attr(smem_set, (const void*)fn, (int)C::kSmemBytes, "d=256 quantize smem attribute");
+    if (rc != TQ_OK) return rc;
+    const int64_t ntiles = (n_rows + kTile - 1) / kTile;
+    const int grid = (int)(ntiles < h.num_sms ? ntiles : h.num_sms);
+    const bool one = h.rot_passes == 1;
+    fn<<<grid, k256Threads, C::kSmemBytes, s>>>(tm_x, one ? h.dp.tm_pm : h.dp.tm_pi_hi, one ? h.dp.tm_pm : h.dp.tm_pi_lo,
+                                                n_rows, h.rot_passes, h.rot_norm_scale, h.cb, out.codes, out.norm,
+                                                h.dp.status);
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? TQ_OK : cuda_fail(e, "d=256 tensor-core quantize launch");
+}
+
+int launch_tc256_b(const tq_ctx& h, const CUtensorMap& tm_x, int64_t n_rows, const tq_planes& out, cudaStream_t s) {
+    switch (h.hp.b_mse) {
+        case 1: return launch_tc256<1>(h, tm_x, n_rows, out, s);
+        case 2: return launch_tc256<2>(h, tm_x, n_rows, out, s);
+        case 3: return launch_tc256<3>(h, tm_x, n_rows, out, s);
+        case 4: return launch_tc256<4>(h, tm_x, n_rows, out, s);
+        default: return fail(TQ_EUNSUPPORTED, "b_m=%d", h.hp.b_mse);
+    }
+}
+
+// ---------------------------------------------------------------------------
 // The prod variant («Собственно TurboQuant»): codes with b_m = b − 1 bits as
 // above, plus the QJL sketch of the rotated unit residual e = y/‖y‖ − c[idx]:
 // signs = [T·e ≥ 0] with T = S·Πᵀ, and ‖r‖ = ‖e‖ (Π orthogonal).
@@ -802,8 +1085,8 @@ bool quantize_tc_supported(const tq_ctx& h, int x_dtype, int64_t n_rows) {
     // TMA row coordinates are 32-bit signed: the last tile must start below 2^31.
     const bool rot = h.rot_passes == 1 ? h.dp.Pm != nullptr : h.dp.Pi_hi != nullptr;
     const bool params = h.hp.variant == TQ_MSE ? rot : (rot && h.dp.T_hi != nullptr && h.hp.b_mse <= 3);
-    return x_dtype == TQ_BF16 && (h.hp.d == 64 || h.hp.d == 128) && params && h.num_sms > 0 &&
-           n_rows < ((int64_t)1 << 31) - kTile;
+    const bool dim = h.hp.d == 64 || h.hp.d == 128 || (h.hp.d == 256 && h.hp.variant == TQ_MSE);
+    return x_dtype == TQ_BF16 && dim && params && h.num_sms > 0 && n_rows < ((int64_t)1 << 31) - kTile;
 }
 
 int launch_quantize_tc(const tq_ctx& h, const void* x, int64_t n_rows, int64_t stride, const tq_planes& out,
@@ -816,6 +1099,9 @@ int launch_quantize_tc(const tq_ctx& h, const void* x, int64_t n_rows, int64_t s
         case 64: return prod ? launch_prod_tc_d<64>(h, tm_x, n_rows, out, s) : launch_tc_d<64>(h, tm_x, n_rows, out, s);
         case 128:
             return prod ? launch_prod_tc_d<128>(h, tm_x, n_rows, out, s) : launch_tc_d<128>(h, tm_x, n_rows, out, s);
+        case 256:
+            if (!prod) return launch_tc256_b(h, tm_x, n_rows, out, s);
+            return fail(TQ_EUNSUPPORTED, "tensor-core quantize: prod at d=256");
         default: return fail(TQ_EUNSUPPORTED, "tensor-core quantize: d=%d", h.hp.d);
     }
 }
