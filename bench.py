@@ -480,6 +480,22 @@ def run_ours(args, spec):
             fn()
         host_us.append((time.perf_counter() - t) / 20 * 1e6)
         torch.cuda.synchronize()
+    # The same calls straight through the C ABI with their arguments marshalled
+    # once (what a C or C++ caller pays per call: checks, tensor-map encoding, launch).
+    from kv_cache_vector_18_b300 import _lib as _L
+    Lb, strm = _L.lib(), torch.cuda.current_stream().cuda_stream
+    kps, vps = tq.Quantizer.planes_struct(kc), tq.Quantizer.planes_struct(vc)
+    abi = [lambda: Lb.tq_quantize(kq.handle, Kd.data_ptr(), _L.TQ_BF16, tm["n_rows"], d, kps, strm),
+           lambda: Lb.tq_quantize(vq.handle, Vd.data_ptr(), _L.TQ_BF16, tm["n_rows"], d, vps, strm),
+           lambda: Lb.tq_decode_attention(kq.handle, vq.handle, qd.data_ptr(), _L.TQ_BF16, kps, vps, ld.data_ptr(),
+                                          B, Hq, Hkv, T, 0.0, out.data_ptr(), None, ws.data_ptr(), ws.numel(), strm)]
+    abi_us = []
+    for fn in abi:
+        t = time.perf_counter()
+        for _ in range(20):
+            assert fn() == 0
+        abi_us.append((time.perf_counter() - t) / 20 * 1e6)
+        torch.cuda.synchronize()
     # One CUDA graph per step holding the three library calls back to back (as a
     # serving loop replays them), captured from the same public API, with event
     # record nodes between the calls: the replay issues exactly the library's
@@ -641,7 +657,10 @@ def run_ours(args, spec):
                                     "CUDA events around CUDA-graph replays of each library call (one graph per call)")
                       + "; L2 flushed before every step; after >= %.1f s of back-to-back warm-up (%d steps)"
                       % (args.warm_seconds, warm_steps),
-            "host_us_per_direct_call": {"quantize_k": host_us[0], "quantize_v": host_us[1], "decode": host_us[2]}}
+            "host_us_per_direct_call": {"quantize_k": host_us[0], "quantize_v": host_us[1], "decode": host_us[2],
+                                        "via": "Python binding"},
+            "host_us_per_abi_call": {"quantize_k": abi_us[0], "quantize_v": abi_us[1], "decode": abi_us[2],
+                                     "via": "C ABI through ctypes, arguments marshalled once"}}
     if not args.no_configs and spec["name"] == "llama70b_layer_kv_quant" and spec.get("rotation", "qr") == "qr":
         line["configs"] = measure_configs(tq, flush, dev, peaks)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

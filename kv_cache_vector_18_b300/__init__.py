@@ -169,8 +169,8 @@ def decode_attention(kq: Quantizer, vq: Quantizer, q: torch.Tensor, kcache: dict
         raise ValueError("q must be contiguous")
     if seq_lens.dtype != torch.int32:
         raise ValueError("seq_lens must be int32")
-    need = decode_workspace_bytes(kq, vq, B, Hq, Hkv, T_max)
-    if workspace is None:
+    if workspace is None:  # a caller-provided workspace is size-checked by the library
+        need = decode_workspace_bytes(kq, vq, B, Hq, Hkv, T_max)
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
     if out is None:
         out = torch.empty((B, Hq, d), dtype=torch.float32, device=q.device)
@@ -199,8 +199,8 @@ def decode_append_attention(kq: Quantizer, vq: Quantizer, q: torch.Tensor, k_new
         raise ValueError("k_new and v_new must both be [B, Hkv, d] of one dtype")
     if seq_lens.dtype != torch.int32:
         raise ValueError("seq_lens must be int32")
-    need = decode_workspace_bytes(kq, vq, B, Hq, Hkv, T_max)
-    if workspace is None:
+    if workspace is None:  # a caller-provided workspace is size-checked by the library
+        need = decode_workspace_bytes(kq, vq, B, Hq, Hkv, T_max)
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
     if out is None:
         out = torch.empty((B, Hq, d), dtype=torch.float32, device=q.device)

@@ -1059,6 +1059,382 @@ int launch_prod_tc_d(const tq_ctx& h, const CUtensorMap& tm_x, int64_t n_rows, c
         default: return fail(TQ_EUNSUPPORTED, "prod b_m=%d", h.hp.b_mse);
     }
 }
+// ---------------------------------------------------------------------------
+// d = 256, prod: as the d = 256 mse path, Π is streamed with the row chunks, and
+// so is T = SΠᵀ for the sketch.  Tensor memory holds one 512-column slot: Y (and,
+// once read, the residual E as f16 hi/lo) in columns [0, 256), S = E·Tᵀ in
+// [256, 512).  Per tile the ring carries four chunks of (X, Π_hi, Π_lo), then
+// four chunks of (T_hi, T_lo); the MMA issuer runs MMA 1 over the first four,
+// waits for the epilogue to write E, then MMA 2 over the next four (three f16
+// passes, E read from tensor memory).  MMA 1 of the next tile overlaps the sign
+// pass of this one.  Four epilogue warpgroups each take a 64-column quarter of
+// every tile; the quarters' ‖y‖² and ‖e‖² meet in shared memory.
+struct CfgP256 {
+    static constexpr int D = 256;
+    static constexpr int kChunks = D / kKC;                      // 4
+    static constexpr int kXBytes = kTile * 128;                  // 16 KB
+    static constexpr int kPBytes = D * 128;                      // 32 KB
+    static constexpr int kStageBytes = kXBytes + 2 * kPBytes;    // 80 KB
+    static constexpr size_t kBarOffset = (size_t)k256Stages * kStageBytes;
+    static constexpr size_t kXchOffset = kBarOffset + 256;      // [2 sums][4 quarters][row]
+    static constexpr size_t kSmemBytes = kXchOffset + (size_t)2 * 4 * kTile * 4 + 1024;
+};
+
+template <int BM>
+__global__ void __launch_bounds__(k256Threads, 1)
+quantize_prod_tc256_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_pi_hi,
+                           const __grid_constant__ CUtensorMap tm_pi_lo, const __grid_constant__ CUtensorMap tm_t_hi,
+                           const __grid_constant__ CUtensorMap tm_t_lo, int64_t n_rows, int npass, float norm_scale,
+                           Codebook cb, uint8_t* __restrict__ codes, uint8_t* __restrict__ signs,
+                           float* __restrict__ norm_out, float* __restrict__ rnorm_out, int* __restrict__ status) {
+    using C = CfgP256;
+    constexpr int D = C::D;
+    constexpr int Q = D / 4;                    // columns per quarter
+    constexpr int L = 1 << BM;
+    constexpr int P = BM >= 1 ? L / 2 - 1 : 0;  // positive decision boundaries
+    constexpr int WORDS = BM * D / 32;          // packed code words per row
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* stages = smem;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
+    uint64_t* full = bars;                 // [k256Stages] chunk landed
+    uint64_t* empty = full + k256Stages;   // [k256Stages] chunk consumed by the MMAs
+    uint64_t* yfull = empty + k256Stages;  // Y ready
+    uint64_t* efull = yfull + 1;           // E written (512 arrivals)
+    uint64_t* sfull = efull + 1;           // S ready
+    uint64_t* sfree = sfull + 1;           // S read out (512 arrivals)
+    uint64_t* drain = sfree + 1;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t ntiles = (n_rows + kTile - 1) / kTile;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < k256Stages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(yfull, 1);
+        mbar_init(efull, 512);
+        mbar_init(sfull, 1);
+        mbar_init(sfree, 512);
+        mbar_init(drain, 1);
+        fence_barrier_init();
+    }
+    if (warp == 1) tmem_alloc(tmem_holder, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------------------ producer
+        prefetch_tensormap(&tm_x);
+        prefetch_tensormap(&tm_pi_hi);
+        prefetch_tensormap(&tm_pi_lo);
+        prefetch_tensormap(&tm_t_hi);
+        prefetch_tensormap(&tm_t_lo);
+        int64_t q = 0;  // chunks issued
+        bool ok = true;
+        for (int64_t tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
+            for (int c = 0; c < 2 * C::kChunks; ++c, ++q) {
+                const int s = (int)(q % k256Stages);
+                const int64_t u = q / k256Stages;
+                if (u > 0 && !(ok = mbar_wait(&empty[s], (uint32_t)((u - 1) & 1), status, 31))) break;
+                uint8_t* st = stages + (size_t)s * C::kStageBytes;
+                if (c < C::kChunks) {  // X, Π_hi (, Π_lo) of chunk c
+                    mbar_arrive_expect_tx(&full[s], C::kXBytes + npass * C::kPBytes);
+                    tma_load_2d(st, &tm_x, &full[s], c * kKC, (int)(tile * kTile));
+                    tma_load_2d(st + C::kXBytes, &tm_pi_hi, &full[s], c * kKC, 0);
+                    if (npass == 2) tma_load_2d(st + C::kXBytes + C::kPBytes, &tm_pi_lo, &full[s], c * kKC, 0);
+                } else {              // T_hi, T_lo of chunk c − 4
+                    mbar_arrive_expect_tx(&full[s], 2 * C::kPBytes);
+                    tma_load_2d(st + C::kXBytes, &tm_t_hi, &full[s], (c - C::kChunks) * kKC, 0);
+                    tma_load_2d(st + C::kXBytes + C::kPBytes, &tm_t_lo, &full[s], (c - C::kChunks) * kKC, 0);
+                }
+            }
+        }
+        for (int64_t k = (q > k256Stages ? q - k256Stages : 0); k < q; ++k)
+            mbar_wait(&full[k % k256Stages], (uint32_t)((k / k256Stages) & 1), status, 32);
+    } else if (warp == 1 && lane == 0) {
+        // ------------------------------------------------------------ MMA issuer
+        constexpr uint32_t idesc1 = idesc_bf16_f32(kTile, D);
+        constexpr uint32_t idesc2 = idesc_f16_f32(kTile, D);
+        const uint32_t base = smem_u32(stages);
+        const uint32_t y_tmem = tmem_base, s_tmem = tmem_base + (uint32_t)D;
+        int64_t q = 0, i = 0;
+        bool ok = true;
+        for (int64_t tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x, ++i) {
+            // MMA 1: Y = X·Πᵀ into columns [0, D), once the previous tile's MMA 2 (which
+            // reads E from these columns) has completed
+            if (i > 0 && !(ok = mbar_wait(sfull, (uint32_t)((i - 1) & 1), status, 30))) break;
+            for (int c = 0; c < C::kChunks; ++c, ++q) {
+                const int s = (int)(q % k256Stages);
+                if (!(ok = mbar_wait(&full[s], (uint32_t)((q / k256Stages) & 1), status, 33))) break;
+                tc_fence_after();
+                const uint32_t st = base + (uint32_t)(s * C::kStageBytes);
+#pragma unroll
+                for (int pass = 0; pass < 2; ++pass) {
+                    if (pass >= npass) break;
+#pragma unroll
+                    for (int kk = 0; kk < kKC / 16; ++kk) {
+                        const uint64_t ad = smem_desc(st + kk * 32, 1024, 2);
+                        const uint64_t bd = smem_desc(st + C::kXBytes + pass * C::kPBytes + kk * 32, 1024, 2);
+                        mma_f16_ss(y_tmem, ad, bd, idesc1, (c | kk | pass) != 0);
+                    }
+                }
+                mma_commit(&empty[s]);
+            }
+            if (!ok) break;
+            mma_commit(yfull);
+            // MMA 2: S = E·Tᵀ into columns [D, 2D), once the epilogue has written E and
+            // has read the previous tile's S
+            if (!(ok = mbar_wait(efull, (uint32_t)(i & 1), status, 34))) break;
+            if (i > 0 && !(ok = mbar_wait(sfree, (uint32_t)((i - 1) & 1), status, 35))) break;
+            tc_fence_after();
+            for (int c = 0; c < C::kChunks; ++c, ++q) {
+                const int s = (int)(q % k256Stages);
+                if (!(ok = mbar_wait(&full[s], (uint32_t)((q / k256Stages) & 1), status, 36))) break;
+                tc_fence_after();
+                const uint32_t st = base + (uint32_t)(s * C::kStageBytes);
+#pragma unroll
+                for (int pass = 0; pass < 3; ++pass) {
+#pragma unroll
+                    for (int kk = 0; kk < kKC / 16; ++kk) {
+                        const int k16 = 4 * c + kk;
+                        // E_hi of dims 16·k16 … in columns 32·(k16/2) + 8·(k16%2), E_lo 16 columns further
+                        const uint32_t acol = 32 * (k16 >> 1) + 8 * (k16 & 1) + (pass == 1 ? 16 : 0);
+                        const uint64_t bd =
+                            smem_desc(st + C::kXBytes + (pass == 2 ? C::kPBytes : 0) + kk * 32, 1024, 2);
+                        mma_f16_ts(s_tmem, y_tmem + acol, bd, idesc2, (c | kk | pass) != 0);
+                    }
+                }
+                mma_commit(&empty[s]);
+            }
+            if (!ok) break;
+            mma_commit(sfull);
+        }
+        mma_commit(drain);
+        mbar_wait(drain, 0, status, 37);
+    } else if (warp >= 2) {
+        // ------------------------------------------------------------ epilogue
+        constexpr int GB = BM == 3 ? 24 : 16;  // bits per float packing group
+        constexpr int GC = BM > 0 ? GB / BM : 1;
+        constexpr int NG = BM > 0 ? 32 / GC : 1;
+        constexpr float kAcc0 = (float)(1u << (GB - 1)) - 0.5f;
+        const int qtr = (warp - 2) >> 2;        // quarter of the columns: 0..3
+        const int quad = warp & 3;              // TMEM lane quadrant of this warp
+        const int r_local = quad * 32 + lane;
+        float* xss = reinterpret_cast<float*>(smem + C::kXchOffset);  // [quarter][row] partial ‖y‖²
+        float* xes = xss + 4 * kTile;                                   // [quarter][row] partial ‖e‖²
+        float t2[P > 0 ? P : 1];
+#pragma unroll
+        for (int p = 0; p < P; ++p) t2[p] = cb.t[L / 2 + p] * cb.t[L / 2 + p];
+        CentroidPoly<BM> cp;
+        cp.init(cb);
+        const uint32_t lanebits = (uint32_t)(quad * 32) << 16;
+        const uint32_t ybase = tmem_base + (uint32_t)(qtr * Q) + lanebits;
+        const uint32_t sbase = ybase + (uint32_t)D;
+        auto all_sync = [&]() { asm volatile("bar.sync 1, 512;" ::: "memory"); };
+        // the quarters leave the tile loop together when a wait gives up
+        auto all_ok = [&](bool ok) -> bool {
+            uint32_t r;
+            asm volatile(
+                "{\n\t.reg .pred p, q;\n\t"
+                "setp.ne.u32 p, %1, 0;\n\t"
+                "bar.red.and.pred q, 1, 512, p;\n\t"
+                "selp.u32 %0, 1, 0, q;\n\t}\n"
+                : "=r"(r)
+                : "r"((uint32_t)ok)
+                : "memory");
+            return r != 0;
+        };
+        int64_t j = 0;
+        for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++j) {
+            if (!all_ok(mbar_wait(yfull, (uint32_t)(j & 1), status, 38))) break;
+            tc_fence_after();
+            uint32_t r[2][32];
+            // pass 1: this quarter's part of ‖y‖², summed with the other quarters'
+            uint64_t ss2 = 0ull;
+            tmem_ld32(ybase, r[0]);
+            tmem_ld32(ybase + 32, r[1]);
+            tmem_wait_ld(r[0]);
+            tmem_wait_ld(r[1]);
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int k = 0; k < 32; k += 2) {
+                    const uint64_t v2 = f2(__uint_as_float(r[h][k]), __uint_as_float(r[h][k + 1]));
+                    ss2 = fma2(v2, v2, ss2);
+                }
+            float ssa, ssb;
+            f2_split(ss2, ssa, ssb);
+            xss[qtr * kTile + r_local] = ssa + ssb;
+            all_sync();
+            const float ss = (xss[r_local] + xss[kTile + r_local]) + (xss[2 * kTile + r_local] + xss[3 * kTile + r_local]);
+            const float n = sqrtf(ss);
+            const float inv = n > 0.f ? 1.f / n : 0.f;
+            const uint64_t inv2 = f2(inv, inv);
+            const float cs = ss >= 0x1p-38f ? __fdividef(0x1p62f, ss) : 0x1p100f;
+            const float kr = cs * ss;
+            const uint64_t cs2 = f2(cs, cs);
+            float kt2[P > 0 ? P : 1];
+#pragma unroll
+            for (int p = 0; p < P; ++p) kt2[p] = -kr * t2[p];
+            const int64_t row = tile * kTile + r_local;
+            const bool live = row < n_rows;
+            const uint32_t keep = n == 0.f ? 0u : 0xffffffffu;
+            const float live_f = n > 0.f ? 1.f : 0.f;
+            uint64_t nc2[CentroidPoly<BM>::N];
+#pragma unroll
+            for (int k = 0; k < CentroidPoly<BM>::N; ++k) nc2[k] = f2(cp.m[k] * live_f, cp.m[k] * live_f);
+            uint64_t es2 = 0ull;
+            // pass 2: codes and the residual of this quarter's two 32-dim chunks (already in registers)
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const uint32_t* rc = r[c];
+                uint64_t acc[NG];
+#pragma unroll
+                for (int gi = 0; gi < NG; ++gi) acc[gi] = f2(kAcc0, 0.f);
+                uint32_t ehi[16], elo[16];
+#pragma unroll
+                for (int k = 0; k < 32; k += 2) {
+                    const float va = __uint_as_float(rc[k]), vb = __uint_as_float(rc[k + 1]);
+                    const uint64_t v2 = f2(va, vb);
+                    uint64_t cnt2 = f2(0.5f, 0.5f);
+                    if constexpr (P > 0) {
+                        float wa, wb;
+                        f2_split(mul2(v2, cs2), wa, wb);
+#pragma unroll
+                        for (int p = 0; p < P; ++p)
+                            cnt2 = add2(cnt2, f2(__saturatef(fmaf(va, wa, kt2[p])), __saturatef(fmaf(vb, wb, kt2[p]))));
+                    }
+                    const uint32_t sga = __float_as_uint(va) & 0x80000000u, sgb = __float_as_uint(vb) & 0x80000000u;
+                    uint64_t e2;
+                    if constexpr (BM > 0) {
+                        float ca, cb2;
+                        f2_split(cnt2, ca, cb2);
+                        const float sa = __uint_as_float(__float_as_uint(ca) | sga);
+                        const float sb = __uint_as_float(__float_as_uint(cb2) | sgb);
+                        acc[k / GC] = fma2(f2(sa, sb),
+                                           f2((float)(1u << (BM * (k % GC))), (float)(1u << (BM * ((k + 1) % GC)))),
+                                           acc[k / GC]);
+                        // residual e = sign(y)·(|y|/‖y‖ − c⁺(count)) (0 for a zero row)
+                        constexpr int N = CentroidPoly<BM>::N;
+                        uint64_t nc = nc2[N - 1];
+#pragma unroll
+                        for (int qq = N - 2; qq >= 0; --qq) nc = fma2(nc, cnt2, nc2[qq]);
+                        float ta, tb;
+                        f2_split(fma2(f2(fabsf(va), fabsf(vb)), inv2, nc), ta, tb);
+                        e2 = f2(__uint_as_float(__float_as_uint(ta) ^ sga), __uint_as_float(__float_as_uint(tb) ^ sgb));
+                    } else {
+                        e2 = mul2(v2, inv2);
+                    }
+                    es2 = fma2(e2, e2, es2);
+                    float ea, eb;
+                    f2_split(e2, ea, eb);
+                    const __half2 hi = __floats2half2_rn(ea, eb);
+                    const float2 hf = __half22float2(hi);
+                    const __half2 lo = __floats2half2_rn(ea - hf.x, eb - hf.y);
+                    ehi[k / 2] = *reinterpret_cast<const uint32_t*>(&hi);
+                    elo[k / 2] = *reinterpret_cast<const uint32_t*>(&lo);
+                }
+                // the residual of these 32 dims replaces their (already read) Y columns
+                tmem_st16(ybase + c * 32, ehi);
+                tmem_st16(ybase + c * 32 + 16, elo);
+                if constexpr (BM > 0) {
+                    uint32_t cw[BM];
+#pragma unroll
+                    for (int w = 0; w < BM; ++w) cw[w] = 0u;
+#pragma unroll
+                    for (int gi = 0; gi < NG; ++gi) {
+                        float ea, eb;
+                        f2_split(acc[gi], ea, eb);
+                        const uint32_t gbits = __float2uint_rn(ea + eb);
+                        const int bit = gi * GB, w = bit >> 5, sh = bit & 31;
+                        cw[w] |= gbits << sh;
+                        if (sh + GB > 32) cw[w + 1] |= gbits >> (32 - sh);
+                    }
+                    if (live) {
+                        uint8_t* cd = codes + row * (int64_t)(WORDS * 4) + (qtr * (Q / 32) + c) * (BM * 4);
+                        if constexpr (BM == 2) {
+                            *reinterpret_cast<uint2*>(cd) = make_uint2(cw[0] & keep, cw[1] & keep);
+                        } else {
+#pragma unroll
+                            for (int w = 0; w < BM; ++w) reinterpret_cast<uint32_t*>(cd)[w] = cw[w] & keep;
+                        }
+                    }
+                }
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(efull);
+            float esa, esb;
+            f2_split(es2, esa, esb);
+            xes[qtr * kTile + r_local] = esa + esb;
+            all_sync();
+            if (live && qtr == 0) {
+                norm_out[row] = n * norm_scale;
+                rnorm_out[row] = sqrtf((xes[r_local] + xes[kTile + r_local]) + (xes[2 * kTile + r_local] + xes[3 * kTile + r_local]));
+            }
+            // pass 3: sign bits of this quarter of S = T·e (bit i set ⇔ s_i ≥ 0)
+            if (!all_ok(mbar_wait(sfull, (uint32_t)(j & 1), status, 39))) break;
+            tc_fence_after();
+            tmem_ld32(sbase, r[0]);
+            tmem_ld32(sbase + 32, r[1]);
+            tmem_wait_ld(r[0]);
+            tmem_wait_ld(r[1]);
+            tc_fence_before();
+            mbar_arrive(sfree);
+            uint32_t sw[2];
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                uint32_t neg = 0u;
+#pragma unroll
+                for (int k = 31; k >= 0; --k) neg = __funnelshift_l(r[c][k], neg, 1);
+                sw[c] = n > 0.f ? ~neg : 0xffffffffu;
+            }
+            if (live) *reinterpret_cast<uint2*>(signs + row * (int64_t)(D / 8) + qtr * (Q / 8)) = make_uint2(sw[0], sw[1]);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, 512);
+    }
+}
+
+template <int BM>
+int launch_prod_tc256(const tq_ctx& h, const CUtensorMap& tm_x, int64_t n_rows, const tq_planes& out,
+                      cudaStream_t s) {
+    using C = CfgP256;
+    static_assert(C::kSmemBytes <= 232448, "d = 256 prod quantize shared memory above the per-CTA limit");
+    auto fn = quantize_prod_tc256_kernel<BM>;
+    static std::atomic<uint64_t> smem_set{0};
+    const int rc = ensure_smem_attr(smem_set, (const void*)fn, (int)C::kSmemBytes, "d=256 prod quantize smem attribute");
+    if (rc != TQ_OK) return rc;
+    const int64_t ntiles = (n_rows + kTile - 1) / kTile;
+    const int grid = (int)(ntiles < h.num_sms ? ntiles : h.num_sms);
+    const bool one = h.rot_passes == 1;
+    fn<<<grid, k256Threads, C::kSmemBytes, s>>>(tm_x, one ? h.dp.tm_pm : h.dp.tm_pi_hi, one ? h.dp.tm_pm : h.dp.tm_pi_lo,
+                                                h.dp.tm_t_hi, h.dp.tm_t_lo, n_rows, h.rot_passes, h.rot_norm_scale, h.cb,
+                                                out.codes, out.signs, out.norm, out.rnorm, h.dp.status);
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? TQ_OK : cuda_fail(e, "d=256 tensor-core prod quantize launch");
+}
+
+int launch_prod_tc256_b(const tq_ctx& h, const CUtensorMap& tm_x, int64_t n_rows, const tq_planes& out,
+                        cudaStream_t s) {
+    switch (h.hp.b_mse) {
+        case 0: return launch_prod_tc256<0>(h, tm_x, n_rows, out, s);
+        case 1: return launch_prod_tc256<1>(h, tm_x, n_rows, out, s);
+        case 2: return launch_prod_tc256<2>(h, tm_x, n_rows, out, s);
+        case 3: return launch_prod_tc256<3>(h, tm_x, n_rows, out, s);
+        default: return fail(TQ_EUNSUPPORTED, "prod b_m=%d", h.hp.b_mse);
+    }
+}
+
 // One CTA whose pipeline wait nothing completes: the bounded wait gives up after
 // limit_ns, records `code` in the status word and the kernel returns.  It checks
 // the failure path of every pipeline in this file without faulting anything.
@@ -1085,7 +1461,7 @@ bool quantize_tc_supported(const tq_ctx& h, int x_dtype, int64_t n_rows) {
     // TMA row coordinates are 32-bit signed: the last tile must start below 2^31.
     const bool rot = h.rot_passes == 1 ? h.dp.Pm != nullptr : h.dp.Pi_hi != nullptr;
     const bool params = h.hp.variant == TQ_MSE ? rot : (rot && h.dp.T_hi != nullptr && h.hp.b_mse <= 3);
-    const bool dim = h.hp.d == 64 || h.hp.d == 128 || (h.hp.d == 256 && h.hp.variant == TQ_MSE);
+    const bool dim = h.hp.d == 64 || h.hp.d == 128 || h.hp.d == 256;
     return x_dtype == TQ_BF16 && dim && params && h.num_sms > 0 && n_rows < ((int64_t)1 << 31) - kTile;
 }
 
@@ -1100,8 +1476,7 @@ int launch_quantize_tc(const tq_ctx& h, const void* x, int64_t n_rows, int64_t s
         case 128:
             return prod ? launch_prod_tc_d<128>(h, tm_x, n_rows, out, s) : launch_tc_d<128>(h, tm_x, n_rows, out, s);
         case 256:
-            if (!prod) return launch_tc256_b(h, tm_x, n_rows, out, s);
-            return fail(TQ_EUNSUPPORTED, "tensor-core quantize: prod at d=256");
+            return prod ? launch_prod_tc256_b(h, tm_x, n_rows, out, s) : launch_tc256_b(h, tm_x, n_rows, out, s);
         default: return fail(TQ_EUNSUPPORTED, "tensor-core quantize: d=%d", h.hp.d);
     }
 }
