@@ -187,6 +187,10 @@ int tq_decode_workspace_bytes(tq_handle hk, tq_handle hv, int B, int Hq, int Hkv
  * scores_out: NULL, or device float32 [B, Hq, T_max] receiving the pre-softmax
  *    s_t for t < seq_lens[b] (entries past the length are not written).
  * workspace: device buffer of at least tq_decode_workspace_bytes(...) bytes.
+ * Rows of a slab past seq_lens[b] (up to T_max) may be read and are masked;
+ * nothing past a slab's T_max rows is read.  A staging wait of the d = 128
+ * tensor-core kernel that expires records code 30 in hk's status word
+ * (tq_device_status); the outputs of that call are then undefined.
  */
 int tq_decode_attention(tq_handle hk, tq_handle hv, const void* q, int q_dtype,
                         tq_planes kc, tq_planes vc, const int32_t* seq_lens,

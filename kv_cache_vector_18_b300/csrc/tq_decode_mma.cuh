@@ -707,14 +707,15 @@ __device__ __forceinline__ void merge_group(const SplitArgs& a, unsigned char* s
     float* pis = reinterpret_cast<float*>(smem + SM::kMP);   // [D][D] Π_v, then [D][D] S_v
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ns = a.n_splits;
-    // stage Π_v (and S_v) while the split weights are formed: all loads in flight at once
-#pragma unroll
-    for (int i = threadIdx.x; i < D * D / 4; i += NT)
-        reinterpret_cast<float4*>(pis)[i] = __ldg(reinterpret_cast<const float4*>(a.vPi) + i);
-    if constexpr (VP) {
-#pragma unroll
-        for (int i = threadIdx.x; i < D * D / 4; i += NT)
-            reinterpret_cast<float4*>(pis + D * D)[i] = __ldg(reinterpret_cast<const float4*>(a.vS) + i);
+    // stage Π_v (and S_v) with asynchronous copies that land while the split
+    // weights and the split sum are formed
+    {
+        const uint32_t dst = smem_addr(pis);
+        for (int i = threadIdx.x; i < D * D / 4; i += NT) cp_async16(dst + 16u * i, a.vPi + 4 * i, 16u);
+        if constexpr (VP)
+            for (int i = threadIdx.x; i < D * D / 4; i += NT)
+                cp_async16(dst + 16u * (D * D / 4 + i), a.vS + 4 * i, 16u);
+        cp_async_commit();
     }
     if (warp < G) {
         const size_t hs = (head0 + warp) * ns;
@@ -762,6 +763,7 @@ __device__ __forceinline__ void merge_group(const SplitArgs& a, unsigned char* s
         mo[(i % D) * kHeads + i / D] = 0.f;
         if constexpr (VP) mo[kHeads * D + (i % D) * kHeads + i / D] = 0.f;
     }
+    cp_async_wait<0>();  // this thread's part of Π_v has landed
     __syncthreads();
     // out[h][col] = Σ_j Π_v[j][col]·o[j][h] (+ S_v[j][col]·o2[j][h]): thread (col, quarter)
     // sums its quarter of j for all 8 heads (one matrix load feeds 8 FMAs), then
