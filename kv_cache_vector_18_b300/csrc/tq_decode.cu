@@ -19,8 +19,12 @@ namespace {
 
 constexpr int kSplitWarps = 4;
 constexpr int kMinChunk = 64;
+constexpr int64_t kMaxChunk = 8192;
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// d = 128 runs the tensor-core split kernel (tq_decode_mma.cuh)
+constexpr bool use_mma_split(int d) { return d == mmadec::D128; }
 
 struct WsLayout {
     size_t qr, qs, pm, pl, pacc, pacc2, cnt, total;
@@ -244,7 +248,6 @@ __global__ void decode_merge_kernel(const float* __restrict__ pm, const float* _
 
 // The tensor-core split kernel is written for d = 128 (the head dimension of
 // every workload this library is tuned for).
-constexpr bool use_mma_split(int d) { return d == mmadec::D128; }
 
 int launch_split_mma_any(const SplitArgs& a, dim3 grid, int kb, bool kp, int vb, bool vp, cudaStream_t s) {
     using namespace mmadec;
@@ -374,6 +377,17 @@ int decode_plan(const tq_ctx& hk, const tq_ctx& hv, int B, int Hq, int Hkv, int 
     int64_t chunk = (T_max + want - 1) / want;
     chunk = (chunk + kMinChunk - 1) / kMinChunk * kMinChunk;
     if (chunk < kMinChunk) chunk = kMinChunk;
+    // Tensor-core path: a CTA takes at most kMaxChunk tokens, so that a batch of
+    // ragged lengths (unknown on the host) is spread over several waves of CTAs
+    // that the hardware hands out as SMs free up, instead of one CTA per slab
+    // whose longest slab sets the time.  Equal-length workloads already fill one
+    // wave with smaller chunks and are unaffected.
+    if (use_mma_split(p.d) && chunk > kMaxChunk) {
+        // … but never more splits than the last CTA of a group can merge
+        const int64_t floor_chunk = ((T_max + mmadec::kMaxSplitsMerged - 1) / mmadec::kMaxSplitsMerged + kMinChunk - 1) /
+                                    kMinChunk * kMinChunk;
+        chunk = kMaxChunk > floor_chunk ? kMaxChunk : floor_chunk;
+    }
     p.chunk = (int)chunk;
     p.n_splits = (int)((T_max + chunk - 1) / chunk);
     if (p.n_splits < 1) p.n_splits = 1;
