@@ -287,8 +287,10 @@ int tq_mixed_decode_attention(tq_handle hko, tq_handle hkn, tq_handle hvo, tq_ha
  *    word then holds TQ_STATUS_APPEND_FULL (read it with tq_device_status).
  * Attention then covers the updated lengths; q, q_dtype, kc, vc, B, Hq, Hkv,
  * T_max, scale, out and the workspace are as in tq_decode_attention.  Launches
- * on `stream`: one append (K and V rows together), one length update, then the
- * decode launches.
+ * on `stream`: one append (K and V rows together; its last block to finish
+ * updates the lengths and clears the decode's merge tickets), then the decode.
+ * The append counts its finished blocks in a device word of hk, so calls that
+ * share hk must not overlap on the GPU.
  */
 int tq_decode_append_attention(tq_handle hk, tq_handle hv, const void* q, int q_dtype,
                                const void* k_new, const void* v_new, int kv_dtype,

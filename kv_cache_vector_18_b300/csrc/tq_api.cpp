@@ -218,13 +218,14 @@ int upload_params(tq_ctx* h) {
     }
     if (rc == TQ_OK) rc = upload_tensor_core_params(h);
     if (rc == TQ_OK) {
-        cudaError_t e = cudaMalloc((void**)&h->dp.status, sizeof(int));
+        cudaError_t e = cudaMalloc((void**)&h->dp.status, 2 * sizeof(int));
         if (e != cudaSuccess) {
             cudaGetLastError();
             return fail(TQ_ENOMEM, "cudaMalloc of the status word failed");
         }
-        e = cudaMemset(h->dp.status, 0, sizeof(int));
+        e = cudaMemset(h->dp.status, 0, 2 * sizeof(int));
         if (e != cudaSuccess) return cuda_fail(e, "cudaMemset (status word)");
+        h->dp.append_done = h->dp.status + 1;
     }
     return rc;
 }
@@ -625,8 +626,12 @@ int tq_decode_append_attention(tq_handle hk, tq_handle hv, const void* q, int q_
     if ((rc = check_planes(*hv, vc, "vc")) != TQ_OK) return rc;
     if (scale <= 0.f) scale = (float)(1.0 / sqrt((double)hk->hp.d));
     const cudaStream_t s = (cudaStream_t)stream;
-    if ((rc = launch_append(*hk, *hv, k_new, v_new, kv_dtype, B, Hkv, T_max, seq_lens, kc, vc, s)) != TQ_OK) return rc;
-    return launch_decode(*hk, *hv, plan, q, q_dtype, kc, vc, seq_lens, scale, out, nullptr, workspace, s);
+    int n_tickets = 0;
+    int* tickets = decode_tickets(*hv, plan, workspace, &n_tickets);
+    if ((rc = launch_append(*hk, *hv, k_new, v_new, kv_dtype, B, Hkv, T_max, seq_lens, kc, vc, tickets, n_tickets,
+                            s)) != TQ_OK)
+        return rc;
+    return launch_decode(*hk, *hv, plan, q, q_dtype, kc, vc, seq_lens, scale, out, nullptr, workspace, s, true);
 }
 
 }  // extern "C"

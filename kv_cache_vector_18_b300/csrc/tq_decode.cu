@@ -274,7 +274,7 @@ int launch_split_mma_any(const SplitArgs& a, dim3 grid, int kb, bool kp, int vb,
 template <int D>
 int launch_d(const tq_ctx& hk, const tq_ctx& hv, const DecodeShape& p, const void* q, int q_dtype,
              const tq_planes& kc, const tq_planes& vc, const int32_t* seq_lens, float scale, float* out,
-             float* scores, void* workspace, cudaStream_t s) {
+             float* scores, void* workspace, cudaStream_t s, bool tickets_zeroed) {
     const bool kprod = hk.hp.variant == TQ_PROD, vprod = hv.hp.variant == TQ_PROD;
     const WsLayout w = ws_layout(p, vprod);
     char* ws = static_cast<char*>(workspace);
@@ -302,8 +302,10 @@ int launch_d(const tq_ctx& hk, const tq_ctx& hv, const DecodeShape& p, const voi
     if (use_mma_split(D)) {
         // query rotation, split and merge all happen in the split kernel
         a.n_hblocks = (p.G + mmadec::kHeadsPerCta - 1) / mmadec::kHeadsPerCta;
-        e = cudaMemsetAsync(cnt, 0, (size_t)p.B * p.Hq * sizeof(int), s);
-        if (e != cudaSuccess) return cuda_fail(e, "clearing the split tickets");
+        if (!tickets_zeroed) {
+            e = cudaMemsetAsync(cnt, 0, (size_t)p.B * p.Hq * sizeof(int), s);
+            if (e != cudaSuccess) return cuda_fail(e, "clearing the split tickets");
+        }
         return launch_split_mma_any(a, dim3(p.n_splits, p.Hkv * a.n_hblocks, p.B), hk.hp.b_mse, kprod, hv.hp.b_mse,
                                     vprod, s);
     }
@@ -396,18 +398,24 @@ int decode_plan(const tq_ctx& hk, const tq_ctx& hv, int B, int Hq, int Hkv, int 
     return TQ_OK;
 }
 
+int* decode_tickets(const tq_ctx& hv, const DecodeShape& plan, void* workspace, int* count) {
+    const WsLayout w = ws_layout(plan, hv.hp.variant == TQ_PROD);
+    *count = plan.B * plan.Hq;
+    return reinterpret_cast<int*>(static_cast<char*>(workspace) + w.cnt);
+}
+
 int launch_decode(const tq_ctx& hk, const tq_ctx& hv, const DecodeShape& plan, const void* q, int q_dtype,
                   const tq_planes& kc, const tq_planes& vc, const int32_t* seq_lens, float scale, float* out,
-                  float* scores_out, void* workspace, cudaStream_t s) {
+                  float* scores_out, void* workspace, cudaStream_t s, bool tickets_zeroed) {
     switch (plan.d) {
-        case 32: return launch_d<32>(hk, hv, plan, q, q_dtype, kc, vc, seq_lens, scale, out, scores_out, workspace, s);
-        case 64: return launch_d<64>(hk, hv, plan, q, q_dtype, kc, vc, seq_lens, scale, out, scores_out, workspace, s);
-        case 96: return launch_d<96>(hk, hv, plan, q, q_dtype, kc, vc, seq_lens, scale, out, scores_out, workspace, s);
-        case 128: return launch_d<128>(hk, hv, plan, q, q_dtype, kc, vc, seq_lens, scale, out, scores_out, workspace, s);
-        case 160: return launch_d<160>(hk, hv, plan, q, q_dtype, kc, vc, seq_lens, scale, out, scores_out, workspace, s);
-        case 192: return launch_d<192>(hk, hv, plan, q, q_dtype, kc, vc, seq_lens, scale, out, scores_out, workspace, s);
-        case 224: return launch_d<224>(hk, hv, plan, q, q_dtype, kc, vc, seq_lens, scale, out, scores_out, workspace, s);
-        case 256: return launch_d<256>(hk, hv, plan, q, q_dtype, kc, vc, seq_lens, scale, out, scores_out, workspace, s);
+        case 32: return launch_d<32>(hk, hv, plan, q, q_dtype, kc, vc, seq_lens, scale, out, scores_out, workspace, s, tickets_zeroed);
+        case 64: return launch_d<64>(hk, hv, plan, q, q_dtype, kc, vc, seq_lens, scale, out, scores_out, workspace, s, tickets_zeroed);
+        case 96: return launch_d<96>(hk, hv, plan, q, q_dtype, kc, vc, seq_lens, scale, out, scores_out, workspace, s, tickets_zeroed);
+        case 128: return launch_d<128>(hk, hv, plan, q, q_dtype, kc, vc, seq_lens, scale, out, scores_out, workspace, s, tickets_zeroed);
+        case 160: return launch_d<160>(hk, hv, plan, q, q_dtype, kc, vc, seq_lens, scale, out, scores_out, workspace, s, tickets_zeroed);
+        case 192: return launch_d<192>(hk, hv, plan, q, q_dtype, kc, vc, seq_lens, scale, out, scores_out, workspace, s, tickets_zeroed);
+        case 224: return launch_d<224>(hk, hv, plan, q, q_dtype, kc, vc, seq_lens, scale, out, scores_out, workspace, s, tickets_zeroed);
+        case 256: return launch_d<256>(hk, hv, plan, q, q_dtype, kc, vc, seq_lens, scale, out, scores_out, workspace, s, tickets_zeroed);
         default: return fail(TQ_EUNSUPPORTED, "d=%d", plan.d);
     }
 }

@@ -61,6 +61,9 @@ struct DeviceParams {
     CUtensorMap tm_t_hi;
     CUtensorMap tm_t_lo;
     int* status = nullptr;  // device word: 0, or the code of a bounded wait that expired
+    // device word after the status word: blocks of a decode-step append that have
+    // finished (the last one resets it to 0)
+    int* append_done = nullptr;
 };
 
 }  // namespace tq
@@ -152,9 +155,11 @@ int launch_select_outlier_channels(const void* x, int x_dtype, int64_t n_rows, i
                                    double* energy, int32_t* perm, cudaStream_t s);
 
 // Decode-step append (tq_append.cu): quantize the new K and V rows [B·Hkv, d] into
-// the next free token of each (batch, KV head) slab, then bump the lengths.
+// the next free token of each (batch, KV head) slab; the launch's last block then
+// bumps the lengths and zeroes the decode's n_tickets merge tickets (if any).
 int launch_append(const tq_ctx& hk, const tq_ctx& hv, const void* k_new, const void* v_new, int x_dtype, int B,
-                  int Hkv, int T_max, int32_t* lens, const tq_planes& kc, const tq_planes& vc, cudaStream_t s);
+                  int Hkv, int T_max, int32_t* lens, const tq_planes& kc, const tq_planes& vc, int* tickets,
+                  int n_tickets, cudaStream_t s);
 int launch_quantize_tc(const tq_ctx& h, const void* x, int64_t n_rows, int64_t x_row_stride,
                        const tq_planes& out, cudaStream_t s);
 int launch_quantize(const tq_ctx& h, const void* x, int x_dtype, int64_t n_rows,
@@ -167,9 +172,13 @@ struct DecodeShape {
 };
 int decode_plan(const tq_ctx& hk, const tq_ctx& hv, int B, int Hq, int Hkv, int T_max,
                 DecodeShape* plan, size_t* ws_bytes);
+// tickets_zeroed: the merge tickets (decode_tickets) were zeroed by the launch
+// before this one, so the tensor-core path skips its own clearing.
 int launch_decode(const tq_ctx& hk, const tq_ctx& hv, const DecodeShape& plan, const void* q,
                   int q_dtype, const tq_planes& kc, const tq_planes& vc,
                   const int32_t* seq_lens, float scale, float* out, float* scores_out,
-                  void* workspace, cudaStream_t s);
+                  void* workspace, cudaStream_t s, bool tickets_zeroed = false);
+// The merge tickets of a decode workspace: where they lie and how many there are.
+int* decode_tickets(const tq_ctx& hv, const DecodeShape& plan, void* workspace, int* count);
 
 }  // namespace tq
