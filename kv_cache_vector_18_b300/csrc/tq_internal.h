@@ -160,7 +160,7 @@ int launch_select_outlier_channels(const void* x, int x_dtype, int64_t n_rows, i
 int launch_append(const tq_ctx& hk, const tq_ctx& hv, const void* k_new, const void* v_new, int x_dtype, int B,
                   int Hkv, int T_max, int32_t* lens, const tq_planes& kc, const tq_planes& vc, int* tickets,
                   int n_tickets, cudaStream_t s);
-int launch_quantize_tc(const tq_ctx& h, const void* x, int64_t n_rows, int64_t x_row_stride,
+int launch_quantize_tc(const tq_ctx& h, const void* x, int x_dtype, int64_t n_rows, int64_t x_row_stride,
                        const tq_planes& out, cudaStream_t s);
 int launch_quantize(const tq_ctx& h, const void* x, int x_dtype, int64_t n_rows,
                     int64_t x_row_stride, const tq_planes& out, cudaStream_t s);

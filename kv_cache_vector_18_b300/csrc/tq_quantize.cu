@@ -147,7 +147,7 @@ int launch_quantize_part(const tq_ctx& h, const void* x, int x_dtype, int64_t n_
 
 int launch_quantize(const tq_ctx& h, const void* x, int x_dtype, int64_t n_rows, int64_t stride,
                     const tq_planes& out, cudaStream_t s) {
-    if (quantize_tc_supported(h, x_dtype, n_rows)) return launch_quantize_tc(h, x, n_rows, stride, out, s);
+    if (quantize_tc_supported(h, x_dtype, n_rows)) return launch_quantize_tc(h, x, x_dtype, n_rows, stride, out, s);
     switch (h.hp.d) {
         case 32: return launch_d<32>(h, x, x_dtype, n_rows, stride, out, s);
         case 64: return launch_d<64>(h, x, x_dtype, n_rows, stride, out, s);

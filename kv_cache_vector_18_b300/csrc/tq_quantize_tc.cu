@@ -57,31 +57,38 @@ __device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
 
 constexpr int kTile = 128;        // rows per tile (MMA M)
 constexpr int kKC = 64;           // K elements per 128-byte swizzle chunk
-constexpr int kAcc = 3;           // TMEM accumulators = epilogue warpgroups (14 warps: 128 registers each)
-constexpr int kEpiWarps = 4 * kAcc;
-constexpr int kThreads = 32 * (2 + kEpiWarps);
+constexpr int kThreads = 32 * 14;  // 14 warps: 128 registers each
 
-template <int D>
+// F32: fp32 rows.  Four converter warps then load the rows with 16-byte loads and
+// write each value as bf16 hi + lo into two swizzled tiles (x = x_hi + x_lo to
+// ~2⁻¹⁸), and the MMAs take x_hi·Π_hi + x_hi·Π_lo + x_lo·Π_hi (the dropped
+// x_lo·Π_lo is ~2⁻¹⁸ of y); two epilogue warpgroups instead of three.
+template <int D, bool F32 = false>
 struct TcCfg {
     static constexpr int kChunks = D / kKC;
-    static constexpr int kStageBytes = kTile * D * 2;
+    static constexpr int kTileBytes = kTile * D * 2;          // one bf16 tile
+    static constexpr int kStageBytes = (F32 ? 2 : 1) * kTileBytes;
     static constexpr int kChunkBytesA = kTile * 128;  // one 64-column chunk of a tile
     static constexpr int kChunkBytesB = D * 128;      // one 64-column chunk of Π
     static constexpr int kPiBytes = D * D * 2;
-    static constexpr int kStages = D == 64 ? 8 : 4;
+    static constexpr int kStages = F32 ? (D == 64 ? 4 : 2) : (D == 64 ? 8 : 4);
+    static constexpr int kAcc = F32 ? 2 : 3;           // TMEM accumulators = epilogue warpgroups
+    static constexpr int kConvWarp0 = 2 + 4 * kAcc;    // first converter warp (F32)
+    static_assert(32 * (kConvWarp0 + (F32 ? 4 : 0)) == kThreads, "warp roles");
     // allocation: the power of two ≥ kAcc·D columns (≤ 512)
     static constexpr uint32_t kTmemCols = kAcc * D <= 32 ? 32 : (kAcc * D <= 64 ? 64 : (kAcc * D <= 128 ? 128 : (kAcc * D <= 256 ? 256 : 512)));
     static constexpr size_t kBarOffset = 2 * (size_t)kPiBytes + (size_t)kStages * kStageBytes;
     static constexpr size_t kSmemBytes = kBarOffset + 256 + 1024;  // barriers + alignment slack
 };
 
-template <int D, int BM>
+template <int D, int BM, bool F32 = false>
 __global__ void __launch_bounds__(kThreads, 1)
 quantize_mse_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_pi_hi,
                        const __grid_constant__ CUtensorMap tm_pi_lo, int64_t n_rows, int npass, float norm_scale,
                        Codebook cb, uint8_t* __restrict__ codes, float* __restrict__ norm_out,
-                       int* __restrict__ status) {
-    using C = TcCfg<D>;
+                       int* __restrict__ status, const float* __restrict__ xf, int64_t xf_stride) {
+    using C = TcCfg<D, F32>;
+    constexpr int kAcc = C::kAcc;
     constexpr int L = 1 << BM;
     constexpr int P = L / 2 - 1;          // positive decision boundaries
     constexpr int WORDS = BM * D / 32;    // packed 32-bit words per row
@@ -104,7 +111,7 @@ quantize_mse_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
-            mbar_init(&full[s], 1);
+            mbar_init(&full[s], F32 ? 128 : 1);  // the converter threads, or the TMA's expect_tx
             mbar_init(&empty[s], 1);
         }
         for (int a = 0; a < kAcc; ++a) {
@@ -132,7 +139,7 @@ quantize_mse_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
             if (npass == 2) tma_load_2d(pi_lo + c * C::kChunkBytesB, &tm_pi_lo, pi_full, c * kKC, 0);
         }
         int64_t i = 0;
-        for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++i) {
+        for (int64_t tile = blockIdx.x; !F32 && tile < ntiles; tile += gridDim.x, ++i) {
             const int s = (int)(i % C::kStages);
             const int64_t u = i / C::kStages;
             if (u > 0 && !mbar_wait(&empty[s], (uint32_t)((u - 1) & 1), status, 1)) break;
@@ -162,15 +169,19 @@ quantize_mse_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
             tc_fence_after();
             const uint32_t d_tmem = tmem_base + (uint32_t)(acc * D);
             const uint32_t a_stage = a_base + (uint32_t)(s * C::kStageBytes);
+            // passes (A, B): bf16 rows (x, Π_hi), (x, Π_lo); fp32 rows also (x_lo, Π_hi);
+            // the exact ±1 Walsh–Hadamard operand needs no Π_lo pass
 #pragma unroll
-            for (int pass = 0; pass < 2; ++pass) {
-                if (pass >= npass) break;
-                const uint32_t b_base = pass == 0 ? hi_base : lo_base;
+            for (int pass = 0; pass < (F32 ? 3 : 2); ++pass) {
+                const bool pi_lo_pass = pass == 1;
+                if (pi_lo_pass && npass < 2) continue;
+                const uint32_t b_base = pi_lo_pass ? lo_base : hi_base;
+                const uint32_t a_tile = a_stage + (pass == 2 ? (uint32_t)C::kTileBytes : 0u);
 #pragma unroll
                 for (int c = 0; c < C::kChunks; ++c)
 #pragma unroll
                     for (int kk = 0; kk < kKC / 16; ++kk) {
-                        const uint64_t ad = smem_desc(a_stage + c * C::kChunkBytesA + kk * 32, 1024, 2);
+                        const uint64_t ad = smem_desc(a_tile + c * C::kChunkBytesA + kk * 32, 1024, 2);
                         const uint64_t bd = smem_desc(b_base + c * C::kChunkBytesB + kk * 32, 1024, 2);
                         mma_f16_ss(d_tmem, ad, bd, idesc, (pass | c | kk) != 0);
                     }
@@ -180,6 +191,69 @@ quantize_mse_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
         }
         mma_commit(drain);
         mbar_wait(drain, 0, status, 6);
+    } else if (F32 && warp >= C::kConvWarp0) {
+        // ------------------------------------------------------------ converters (fp32 rows)
+        // thread ct takes 16-byte chunks (8 columns) ct, ct + 128, … of the tile; each
+        // becomes 8 bf16 hi and 8 bf16 lo values at the chunk's 128-byte-swizzled
+        // place (row r: 16-byte slot (c8 mod 8) XOR (r mod 8) of its 64-column block)
+        const int ct = threadIdx.x - 32 * C::kConvWarp0;
+        constexpr int CH = D / 8;  // chunks per row
+        constexpr int kRounds = kTile * CH / (128 * 4);
+        auto conv_all = [&](bool ok) -> bool {
+            uint32_t r;
+            asm volatile(
+                "{\n\t.reg .pred p, q;\n\t"
+                "setp.ne.u32 p, %1, 0;\n\t"
+                "bar.red.and.pred q, 1, 128, p;\n\t"
+                "selp.u32 %0, 1, 0, q;\n\t}\n"
+                : "=r"(r)
+                : "r"((uint32_t)ok)
+                : "memory");
+            return r != 0;
+        };
+        int64_t i = 0;
+        for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++i) {
+            const int s = (int)(i % C::kStages);
+            const int64_t u = i / C::kStages;
+            if (u > 0 && !conv_all(mbar_wait(&empty[s], (uint32_t)((u - 1) & 1), status, 8))) break;
+            uint8_t* st = stages + (size_t)s * C::kStageBytes;
+#pragma unroll
+            for (int rd = 0; rd < kRounds; ++rd) {
+                float4 v[4][2];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int q = ct + 128 * (4 * rd + k), r = q / CH, c8 = q % CH;
+                    const int64_t row = tile * kTile + r;
+                    if (row < n_rows) {
+                        const float4* src = reinterpret_cast<const float4*>(xf + row * xf_stride + 8 * c8);
+                        v[k][0] = __ldg(src);
+                        v[k][1] = __ldg(src + 1);
+                    } else {
+                        v[k][0] = v[k][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+                }
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int q = ct + 128 * (4 * rd + k), r = q / CH, c8 = q % CH;
+                    const float xv[8] = {v[k][0].x, v[k][0].y, v[k][0].z, v[k][0].w,
+                                         v[k][1].x, v[k][1].y, v[k][1].z, v[k][1].w};
+                    uint32_t hi[4], lo[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const __nv_bfloat162 h2 = __floats2bfloat162_rn(xv[2 * e], xv[2 * e + 1]);
+                        const float2 hf = __bfloat1622float2(h2);
+                        const __nv_bfloat162 l2 = __floats2bfloat162_rn(xv[2 * e] - hf.x, xv[2 * e + 1] - hf.y);
+                        hi[e] = *reinterpret_cast<const uint32_t*>(&h2);
+                        lo[e] = *reinterpret_cast<const uint32_t*>(&l2);
+                    }
+                    uint8_t* dst = st + (c8 / 8) * C::kChunkBytesA + r * 128 + (((c8 % 8) ^ (r & 7)) << 4);
+                    *reinterpret_cast<uint4*>(dst) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                    *reinterpret_cast<uint4*>(dst + C::kTileBytes) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                }
+            }
+            fence_proxy_async_smem();  // the generic-proxy writes above, before the MMA reads them
+            mbar_arrive(&full[s]);
+        }
     } else if (warp >= 2) {
         // ------------------------------------------------------------ epilogue
         constexpr int GB = BM == 3 ? 24 : 16;  // bits per float packing group
@@ -300,10 +374,11 @@ quantize_mse_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
     }
 }
 
-template <int D, int BM>
-int launch_tc(const tq_ctx& h, const CUtensorMap& tm_x, int64_t n_rows, const tq_planes& out, cudaStream_t s) {
-    using C = TcCfg<D>;
-    auto fn = quantize_mse_tc_kernel<D, BM>;
+template <int D, int BM, bool F32 = false>
+int launch_tc(const tq_ctx& h, const CUtensorMap& tm_x, int64_t n_rows, const tq_planes& out, cudaStream_t s,
+              const float* xf = nullptr, int64_t xf_stride = 0) {
+    using C = TcCfg<D, F32>;
+    auto fn = quantize_mse_tc_kernel<D, BM, F32>;
     static std::atomic<uint64_t> smem_set{0};
     const int rc = ensure_smem_attr(smem_set, (const void*)fn, (int)C::kSmemBytes, "quantize smem attribute");
     if (rc != TQ_OK) return rc;
@@ -312,7 +387,7 @@ int launch_tc(const tq_ctx& h, const CUtensorMap& tm_x, int64_t n_rows, const tq
     const bool one = h.rot_passes == 1;
     fn<<<grid, kThreads, C::kSmemBytes, s>>>(tm_x, one ? h.dp.tm_pm : h.dp.tm_pi_hi, one ? h.dp.tm_pm : h.dp.tm_pi_lo,
                                              n_rows, h.rot_passes, h.rot_norm_scale, h.cb, out.codes, out.norm,
-                                             h.dp.status);
+                                             h.dp.status, xf, xf_stride);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? TQ_OK : cuda_fail(e, "tensor-core quantize launch");
 }
@@ -324,6 +399,21 @@ int launch_tc_d(const tq_ctx& h, const CUtensorMap& tm_x, int64_t n_rows, const 
         case 2: return launch_tc<D, 2>(h, tm_x, n_rows, out, s);
         case 3: return launch_tc<D, 3>(h, tm_x, n_rows, out, s);
         case 4: return launch_tc<D, 4>(h, tm_x, n_rows, out, s);
+        default: return fail(TQ_EUNSUPPORTED, "b_m=%d", h.hp.b_mse);
+    }
+}
+
+// fp32 rows (mse, d = 64 and 128): the rows are read by the kernel's converter
+// warps; the X tensor map is unused
+template <int D>
+int launch_tc_f32_d(const tq_ctx& h, const float* x, int64_t n_rows, int64_t stride, const tq_planes& out,
+                    cudaStream_t s) {
+    const CUtensorMap& none = h.dp.tm_pi_hi;
+    switch (h.hp.b_mse) {
+        case 1: return launch_tc<D, 1, true>(h, none, n_rows, out, s, x, stride);
+        case 2: return launch_tc<D, 2, true>(h, none, n_rows, out, s, x, stride);
+        case 3: return launch_tc<D, 3, true>(h, none, n_rows, out, s, x, stride);
+        case 4: return launch_tc<D, 4, true>(h, none, n_rows, out, s, x, stride);
         default: return fail(TQ_EUNSUPPORTED, "b_m=%d", h.hp.b_mse);
     }
 }
@@ -1462,11 +1552,17 @@ bool quantize_tc_supported(const tq_ctx& h, int x_dtype, int64_t n_rows) {
     const bool rot = h.rot_passes == 1 ? h.dp.Pm != nullptr : h.dp.Pi_hi != nullptr;
     const bool params = h.hp.variant == TQ_MSE ? rot : (rot && h.dp.T_hi != nullptr && h.hp.b_mse <= 3);
     const bool dim = h.hp.d == 64 || h.hp.d == 128 || h.hp.d == 256;
-    return x_dtype == TQ_BF16 && dim && params && h.num_sms > 0 && n_rows < ((int64_t)1 << 31) - kTile;
+    const bool f32 = x_dtype == TQ_F32 && h.hp.variant == TQ_MSE && (h.hp.d == 64 || h.hp.d == 128);
+    return (x_dtype == TQ_BF16 || f32) && dim && params && h.num_sms > 0 && n_rows < ((int64_t)1 << 31) - kTile;
 }
 
-int launch_quantize_tc(const tq_ctx& h, const void* x, int64_t n_rows, int64_t stride, const tq_planes& out,
-                       cudaStream_t s) {
+int launch_quantize_tc(const tq_ctx& h, const void* x, int x_dtype, int64_t n_rows, int64_t stride,
+                       const tq_planes& out, cudaStream_t s) {
+    if (x_dtype == TQ_F32) {
+        const float* xf = static_cast<const float*>(x);
+        return h.hp.d == 64 ? launch_tc_f32_d<64>(h, xf, n_rows, stride, out, s)
+                            : launch_tc_f32_d<128>(h, xf, n_rows, stride, out, s);
+    }
     CUtensorMap tm_x;
     int rc = encode_tmap_bf16_2d(&tm_x, x, (uint64_t)h.hp.d, (uint64_t)n_rows, (uint64_t)stride * 2, kKC, kTile);
     if (rc != TQ_OK) return rc;

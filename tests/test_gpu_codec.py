@@ -183,3 +183,27 @@ def test_tensor_core_path_many_tiles(tq, d, bits, variant):
     assert torch.equal(codes0, planes["codes"])
     if variant == "prod":
         assert torch.equal(signs0, planes["signs"])
+
+
+@pytest.mark.parametrize("rotation", ["qr", "hadamard"])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("bits", [1, 2, 3, 4])
+def test_tensor_core_path_fp32_rows(tq, d, bits, rotation):
+    # fp32 rows on the tensor-core mse path (each row split into bf16 hi + lo on
+    # the device): several tiles per CTA, a ragged tail, a row stride wider than
+    # d and two all-zero rows
+    n = 148 * 128 * 2 + 45
+    qz = tq.Quantizer(d, bits, "mse", seed=31 + bits, rotation=rotation)
+    base = synthetic.student_t_unit_var((n, d + 32), seed=bits * 3 + d, dtype="f32").cuda()
+    base[5] = 0
+    base[n - 1] = 0
+    x = base[:, :d]
+    planes = qz.quantize(x)
+    torch.cuda.synchronize()
+    assert qz.device_status() == 0
+    rows = np.concatenate([np.arange(0, 300), np.arange(n - 300, n),
+                           np.random.default_rng(1).choice(n, 3000, replace=False)])
+    check_quantize(oracle_params(qz), f64(x), planes, rows=rows)
+    codes = planes["codes"].cpu().numpy()
+    assert np.all(codes[5] == 0) and np.all(codes[n - 1] == 0)
+    assert planes["norm"][5].item() == 0
