@@ -39,6 +39,13 @@ WARM_SECONDS = 1.0
 # kernel, which rotates the queries and merges its splits itself, after a
 # memset node that clears its tickets).
 LAUNCHES = {"quantize": 1, "decode": 1}
+
+
+def kv_one_launch(spec) -> bool:
+    """tq_quantize_kv runs K and V in one launch when both are mse with the same
+    d in {64, 128}, bits and rotation (otherwise it makes one launch per side)."""
+    return (spec["k_variant"] == spec["v_variant"] == "mse" and spec["k_bits"] == spec["v_bits"]
+            and spec["d"] in (64, 128))
 # The arithmetic the path computes in.
 DTYPE_LABEL = "bf16 in, bf16/f16 hi+lo MMA operands, fp32 accumulate and out"
 QUANT_SOURCES = ["kv_cache_vector_18_b300/csrc/tq_quantize_tc.cu", "kv_cache_vector_18_b300/csrc/tq_sm100.cuh"]
@@ -441,7 +448,9 @@ def config_block(spec) -> dict:
     return {"workload": spec["name"], "batch": spec["B"], "kv_heads": spec["Hkv"], "q_heads": spec["Hq"],
             "tokens": spec["T"], "d": spec["d"], "k": f"{spec['k_variant']} b={spec['k_bits']}",
             "v": f"{spec['v_variant']} b={spec['v_bits']}", "rotation": spec.get("rotation", "qr"),
-            "step": "tq_quantize(K) + tq_quantize(V) + tq_decode_attention over the packed cache",
+            "step": ("tq_quantize_kv(K, V) (one launch) + tq_decode_attention over the packed cache"
+                     if kv_one_launch(spec) else
+                     "tq_quantize(K) + tq_quantize(V) + tq_decode_attention over the packed cache"),
             "l2": f"flushed by a {L2_FLUSH_BYTES >> 20} MiB write before every timed step",
             "inputs": "resident in HBM (value); pinned host buffers (e2e)"}
 
@@ -466,8 +475,14 @@ def run_ours(args, spec):
     out = torch.empty((B, Hq, d), dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
-    calls = [lambda: kq.quantize(Kd, out=kc), lambda: vq.quantize(Vd, out=vc),
-             lambda: tq.decode_attention(kq, vq, qd, kc, vc, ld, Hkv, T, workspace=ws, out=out)]
+    fused = kv_one_launch(spec)
+    dec_call = lambda: tq.decode_attention(kq, vq, qd, kc, vc, ld, Hkv, T, workspace=ws, out=out)
+    if fused:  # K and V quantized by one library call and one launch
+        names = ["quantize_kv", "decode"]
+        calls = [lambda: tq.quantize_kv(kq, vq, Kd, Vd, k_out=kc, v_out=vc), dec_call]
+    else:
+        names = ["quantize_k", "quantize_v", "decode"]
+        calls = [lambda: kq.quantize(Kd, out=kc), lambda: vq.quantize(Vd, out=vc), dec_call]
     for _ in range(max(args.warmup, 0)):
         flush.zero_()
         for fn in calls:
@@ -487,10 +502,15 @@ def run_ours(args, spec):
     from kv_cache_vector_18_b300 import _lib as _L
     Lb, strm = _L.lib(), torch.cuda.current_stream().cuda_stream
     kps, vps = tq.Quantizer.planes_struct(kc), tq.Quantizer.planes_struct(vc)
-    abi = [lambda: Lb.tq_quantize(kq.handle, Kd.data_ptr(), _L.TQ_BF16, tm["n_rows"], d, kps, strm),
-           lambda: Lb.tq_quantize(vq.handle, Vd.data_ptr(), _L.TQ_BF16, tm["n_rows"], d, vps, strm),
-           lambda: Lb.tq_decode_attention(kq.handle, vq.handle, qd.data_ptr(), _L.TQ_BF16, kps, vps, ld.data_ptr(),
-                                          B, Hq, Hkv, T, 0.0, out.data_ptr(), None, ws.data_ptr(), ws.numel(), strm)]
+    abi_dec = lambda: Lb.tq_decode_attention(kq.handle, vq.handle, qd.data_ptr(), _L.TQ_BF16, kps, vps,
+                                             ld.data_ptr(), B, Hq, Hkv, T, 0.0, out.data_ptr(), None, ws.data_ptr(),
+                                             ws.numel(), strm)
+    if fused:
+        abi = [lambda: Lb.tq_quantize_kv(kq.handle, vq.handle, Kd.data_ptr(), Vd.data_ptr(), _L.TQ_BF16, tm["n_rows"],
+                                         tm["n_rows"], d, d, kps, vps, strm), abi_dec]
+    else:
+        abi = [lambda: Lb.tq_quantize(kq.handle, Kd.data_ptr(), _L.TQ_BF16, tm["n_rows"], d, kps, strm),
+               lambda: Lb.tq_quantize(vq.handle, Vd.data_ptr(), _L.TQ_BF16, tm["n_rows"], d, vps, strm), abi_dec]
     abi_us = []
     for fn in abi:
         t = time.perf_counter()
@@ -562,14 +582,13 @@ def run_ours(args, spec):
     barrier(world)
     if step_graph is None:
         per_call = [[e[k].elapsed_time(e[k + 1]) for k in range(len(calls))] for e in evs]
-    qk = [c[0] for c in per_call]
-    qv = [c[1] for c in per_call]
-    dc = [c[2] for c in per_call]
+    col = {n: [c[k] for c in per_call] for k, n in enumerate(names)}
+    dc = col["decode"]
     step_ms = [e[0].elapsed_time(e[-1]) for e in evs]
     t_local = sum(step_ms) / 1e3
     t_step = max_over_ranks(t_local, world, dev)
     value = aggregate_throughput(tm["total"] * args.steps, t_local, world, dev) / 1e9
-    quant_s = (sum(qk) + sum(qv)) / 1e3
+    quant_s = sum(sum(v) for n, v in col.items() if n != "decode") / 1e3
     quant_mrows = aggregate_throughput(2 * tm["n_rows"] * args.steps, quant_s, world, dev) / 1e6
     dec_gbs = aggregate_throughput(tm["decode"] * args.steps, sum(dc) / 1e3, world, dev) / 1e9
 
@@ -604,17 +623,24 @@ def run_ours(args, spec):
         return out
 
     wht = "_wht" if rot == "hadamard" else ""
-    rl = {
-        "quantize_k": hbm_roofline(f"tq_quantize ({spec['k_variant']} b={spec['k_bits']})", qk, tm["quant_k"],
-                                   f"quantize_{spec['k_variant']}_b{spec['k_bits']}_d{d}{wht}", qsrc, tm["n_rows"]),
-        "quantize_v": hbm_roofline(f"tq_quantize ({spec['v_variant']} b={spec['v_bits']})", qv, tm["quant_v"],
-                                   f"quantize_{spec['v_variant']}_b{spec['v_bits']}_d{d}{wht}", qsrc, tm["n_rows"]),
-        "decode": hbm_roofline("tq_decode_attention", dc, tm["decode"],
-                               f"decode_{spec['k_variant']}_b{spec['k_bits']}_{spec['v_variant']}_b{spec['v_bits']}_d{d}",
-                               dsrc, tm["ctx_rows"]),
-    }
-    rl["quantize_k"]["tensor"] = tensor_info(spec["k_bits"], spec["k_variant"], tm["n_rows"], qk)
-    rl["quantize_v"]["tensor"] = tensor_info(spec["v_bits"], spec["v_variant"], tm["n_rows"], qv)
+    rl = {}
+    if fused:
+        rl["quantize_kv"] = hbm_roofline(
+            f"tq_quantize_kv (mse b={spec['k_bits']}, K and V rows in one launch)", col["quantize_kv"],
+            tm["quant_k"] + tm["quant_v"], f"quantize_mse_b{spec['k_bits']}_d{d}{wht}", qsrc, 2 * tm["n_rows"])
+        rl["quantize_kv"]["tensor"] = tensor_info(spec["k_bits"], "mse", 2 * tm["n_rows"], col["quantize_kv"])
+    else:
+        rl["quantize_k"] = hbm_roofline(f"tq_quantize ({spec['k_variant']} b={spec['k_bits']})", col["quantize_k"],
+                                        tm["quant_k"], f"quantize_{spec['k_variant']}_b{spec['k_bits']}_d{d}{wht}",
+                                        qsrc, tm["n_rows"])
+        rl["quantize_v"] = hbm_roofline(f"tq_quantize ({spec['v_variant']} b={spec['v_bits']})", col["quantize_v"],
+                                        tm["quant_v"], f"quantize_{spec['v_variant']}_b{spec['v_bits']}_d{d}{wht}",
+                                        qsrc, tm["n_rows"])
+        rl["quantize_k"]["tensor"] = tensor_info(spec["k_bits"], spec["k_variant"], tm["n_rows"], col["quantize_k"])
+        rl["quantize_v"]["tensor"] = tensor_info(spec["v_bits"], spec["v_variant"], tm["n_rows"], col["quantize_v"])
+    rl["decode"] = hbm_roofline("tq_decode_attention", dc, tm["decode"],
+                                f"decode_{spec['k_variant']}_b{spec['k_bits']}_{spec['v_variant']}_b{spec['v_bits']}_d{d}",
+                                dsrc, tm["ctx_rows"])
     # score, QJL and value products: 2·d flop each per token-head and query head
     dec_flops = (3 if spec["k_variant"] == "prod" else 2) * 2 * d * (Hq // Hkv) * tm["ctx_rows"]
     rl["decode"]["mma_tflops"] = dec_flops / (statistics.mean(dc) / 1e3) / 1e12
@@ -650,19 +676,17 @@ def run_ours(args, spec):
             "pct_hbm_peak": value / peaks["hbm_gbs"] * 100.0,
             "pct_nominal_8tbs": value / 8000.0 * 100.0,
             "bytes_per_step": tm["total"],
-            "gpu_launches": args.steps * (2 * LAUNCHES["quantize"] + LAUNCHES["decode"]),
+            "gpu_launches": args.steps * ((1 if fused else 2) * LAUNCHES["quantize"] + LAUNCHES["decode"]),
             "clocks": sampler.summary(), "wall_s_timed_loop": wall, "roofline": roofline,
             "roofline_decode": roofline_decode, "roofline_per_call": rl, "e2e": e2e, "append_step": append,
-            "timing": graph_note + ("one CUDA graph per step holding the three library calls (captured through "
+            "timing": graph_note + (f"one CUDA graph per step holding the {len(calls)} library calls (captured through "
                                     "the public API); step time from CUDA events around each replay, per-call "
                                     "times from event nodes inside the graph" if step_graph is not None else
                                     "CUDA events around CUDA-graph replays of each library call (one graph per call)")
                       + "; L2 flushed before every step; after >= %.1f s of back-to-back warm-up (%d steps)"
                       % (args.warm_seconds, warm_steps),
-            "host_us_per_direct_call": {"quantize_k": host_us[0], "quantize_v": host_us[1], "decode": host_us[2],
-                                        "via": "Python binding"},
-            "host_us_per_abi_call": {"quantize_k": abi_us[0], "quantize_v": abi_us[1], "decode": abi_us[2],
-                                     "via": "C ABI through ctypes, arguments marshalled once"}}
+            "host_us_per_direct_call": dict(zip(names, host_us), via="Python binding"),
+            "host_us_per_abi_call": dict(zip(names, abi_us), via="C ABI through ctypes, arguments marshalled once")}
     if not args.no_configs and spec["name"] == "llama70b_layer_kv_quant" and spec.get("rotation", "qr") == "qr":
         line["configs"] = measure_configs(tq, flush, dev, peaks)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -970,7 +994,7 @@ def run_score_quality_study(args) -> int:
 
 def measure_e2e(args, spec, tq, kq, vq, K, V, q, ld, kc, vc, ws, out, tm, dev, world):
     """Same metric through the public API with host buffers: pinned H2D of the
-    step's K, V and q, the three library calls, D2H of the packed planes and
+    step's K, V and q, the step's library calls, D2H of the packed planes and
     the attention output, all inside the timed region."""
     d, Hkv, T = spec["d"], spec["Hkv"], spec["T"]
     Kh, Vh, qh = K.reshape(-1, d).cpu().pin_memory(), V.reshape(-1, d).cpu().pin_memory(), q.pin_memory()
@@ -986,8 +1010,11 @@ def measure_e2e(args, spec, tq, kq, vq, K, V, q, ld, kc, vc, ws, out, tm, dev, w
         Kd.copy_(Kh, non_blocking=True)
         Vd.copy_(Vh, non_blocking=True)
         qd.copy_(qh, non_blocking=True)
-        kq.quantize(Kd, out=kc)
-        vq.quantize(Vd, out=vc)
+        if kv_one_launch(spec):
+            tq.quantize_kv(kq, vq, Kd, Vd, k_out=kc, v_out=vc)
+        else:
+            kq.quantize(Kd, out=kc)
+            vq.quantize(Vd, out=vc)
         tq.decode_attention(kq, vq, qd, kc, vc, ld, Hkv, T, workspace=ws, out=out)
         for hp, p in zip(host_planes, (kc, vc)):
             for k in p:

@@ -154,6 +154,23 @@ int tq_quantize(tq_handle h, const void* x, int x_dtype, int64_t n_rows,
                 int64_t x_row_stride, tq_planes out, void* stream);
 
 /*
+ * tq_quantize_kv — tq_quantize(hk, k, …, k_out) and tq_quantize(hv, v, …, v_out)
+ * in one call: the key and value rows of a decode step or a prefill chunk (the
+ * «KV-кэш» use of the method: K and V are quantized independently, each with
+ * its own handle).  Results are bit-identical to the two separate calls.  When
+ * both handles are mse with the same d ∈ {64, 128}, b and rotation kind, and
+ * the rows are bf16 or fp32, both sides run in ONE launch of the tensor-core
+ * kernel (its CTAs split between K and V in proportion to their rows);
+ * otherwise the call makes the two launches.  Arguments: as tq_quantize for each
+ * side (k_rows / v_rows may differ; either may be 0); both sides share x_dtype.
+ * k_out and v_out must not overlap each other or the inputs.  Errors: as
+ * tq_quantize, checked for both sides before anything is launched.
+ */
+int tq_quantize_kv(tq_handle hk, tq_handle hv, const void* k, const void* v, int x_dtype,
+                   int64_t k_rows, int64_t v_rows, int64_t k_row_stride, int64_t v_row_stride,
+                   tq_planes k_out, tq_planes v_out, void* stream);
+
+/*
  * tq_dequantize — Q⁻¹ of «Шаг 2» plus, for prod, the QJL reconstruction:
  *   x̃ = norm·(Πᵀ·c[code] + √(π/2)/d·rnorm·Sᵀ·z),  z_i = ±1 from the sign bits.
  * y: device pointer to n_rows·d contiguous elements of y_dtype (TQ_F32 or

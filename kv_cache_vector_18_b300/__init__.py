@@ -17,7 +17,7 @@ import torch
 from . import _lib
 from ._lib import TQ_BF16, TQ_F32, TQ_MSE, TQ_PROD, TQError, check
 
-__all__ = ["Quantizer", "MixedQuantizer", "decode_attention", "decode_append_attention", "mixed_decode_attention",
+__all__ = ["Quantizer", "MixedQuantizer", "quantize_kv", "decode_attention", "decode_append_attention", "mixed_decode_attention",
            "mixed_decode_workspace_bytes", "select_outlier_channels", "decode_workspace_bytes", "build_params_host", "TQError",
            "library_path"]
 
@@ -149,6 +149,26 @@ class Quantizer:
         check(_lib.lib().tq_dequantize(self._h, self.planes_struct(planes), n, _ptr(y), _DTYPES[dtype],
                                        _stream(stream)))
         return y
+
+
+def quantize_kv(kq: Quantizer, vq: Quantizer, k: torch.Tensor, v: torch.Tensor, k_out: dict | None = None,
+                v_out: dict | None = None, stream=None) -> tuple[dict, dict]:
+    """tq_quantize_kv: the rows of k with kq and the rows of v with vq in one call
+    (one launch when both are mse with the same d, b and rotation kind).  k and v
+    are [..., d] with the same dtype (bf16 or fp32) on the device."""
+    if k.dtype != v.dtype:
+        raise ValueError("k and v must have the same dtype")
+    k2, v2 = k.reshape(-1, k.shape[-1]), v.reshape(-1, v.shape[-1])
+    nk, nv = k2.shape[0], v2.shape[0]
+    k_out = kq.empty_planes(nk, k.device) if k_out is None else k_out
+    v_out = vq.empty_planes(nv, v.device) if v_out is None else v_out
+    if (nk and k2.stride(-1) != 1) or (nv and v2.stride(-1) != 1):
+        raise ValueError("k and v rows must be contiguous")
+    check(_lib.lib().tq_quantize_kv(kq.handle, vq.handle, _ptr(k2) if nk else None, _ptr(v2) if nv else None,
+                                    _DTYPES[k.dtype], nk, nv, k2.stride(0) if nk else kq.d,
+                                    v2.stride(0) if nv else vq.d, Quantizer.planes_struct(k_out),
+                                    Quantizer.planes_struct(v_out), _stream(stream)))
+    return k_out, v_out
 
 
 def decode_workspace_bytes(kq: Quantizer, vq: Quantizer, B: int, Hq: int, Hkv: int, T_max: int) -> int:

@@ -25,7 +25,7 @@ ERROR_NAMES = {TQ_EINVAL: "TQ_EINVAL", TQ_EUNSUPPORTED: "TQ_EUNSUPPORTED", TQ_EA
 # Every symbol include/tq.h declares, for the export check.
 EXPORTED = ["tq_init", "tq_init_ex", "tq_destroy", "tq_row_bytes", "tq_build_params_host",
             "tq_build_params_host_ex", "tq_get_params",
-            "tq_quantize", "tq_dequantize", "tq_decode_workspace_bytes", "tq_decode_attention",
+            "tq_quantize", "tq_quantize_kv", "tq_dequantize", "tq_decode_workspace_bytes", "tq_decode_attention",
             "tq_decode_attention_noalloc", "tq_decode_append_attention", "tq_select_outlier_channels",
             "tq_mixed_quantize_scratch_bytes", "tq_mixed_quantize", "tq_mixed_dequantize", "tq_mixed_decode_workspace_bytes",
             "tq_mixed_decode_attention", "tq_device_status", "tq_check_wait_timeout", "tq_last_error"]
@@ -64,6 +64,7 @@ def lib() -> ctypes.CDLL:
     L.tq_build_params_host_ex.argtypes = [i32, i32, i32, i32, u64, dp, dp, dp, dp]
     L.tq_get_params.argtypes = [vp, dp, dp, dp, dp]
     L.tq_quantize.argtypes = [vp, vp, i32, i64, i64, Planes, vp]
+    L.tq_quantize_kv.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, i64, Planes, Planes, vp]
     L.tq_dequantize.argtypes = [vp, Planes, i64, vp, i32, vp]
     L.tq_decode_workspace_bytes.argtypes = [vp, vp, i32, i32, i32, i32, ctypes.POINTER(sz)]
     L.tq_decode_attention.argtypes = [vp, vp, vp, i32, Planes, Planes, vp, i32, i32, i32, i32,

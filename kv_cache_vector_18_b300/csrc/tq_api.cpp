@@ -408,9 +408,11 @@ int tq_get_params(tq_handle h, double* Pi, double* S, double* centroids, double*
     return TQ_OK;
 }
 
-int tq_quantize(tq_handle h, const void* x, int x_dtype, int64_t n_rows, int64_t x_row_stride,
-                tq_planes out, void* stream) {
-    int rc = validate_handle(h, "quantizer");
+namespace {
+
+int check_quantize_args(tq_handle h, const void* x, int x_dtype, int64_t n_rows, int64_t x_row_stride,
+                        const tq_planes& out, const char* what) {
+    int rc = validate_handle(h, what);
     if (rc != TQ_OK) return rc;
     if (n_rows < 0) return fail(TQ_EINVAL, "n_rows=%lld is negative", (long long)n_rows);
     if (x_dtype != TQ_BF16 && x_dtype != TQ_F32) return fail(TQ_EINVAL, "x_dtype=%d invalid", x_dtype);
@@ -420,8 +422,31 @@ int tq_quantize(tq_handle h, const void* x, int x_dtype, int64_t n_rows, int64_t
     if (x_row_stride < d) return fail(TQ_EINVAL, "x_row_stride=%lld < d=%d", (long long)x_row_stride, d);
     if ((x_row_stride * es) % 16 != 0) return fail(TQ_EALIGN, "x_row_stride*elem_size must be a multiple of 16 bytes");
     if ((rc = check_device_ptr(x, "x", true)) != TQ_OK) return rc;
-    if ((rc = check_planes(*h, out, "out")) != TQ_OK) return rc;
+    return check_planes(*h, out, "out");
+}
+
+}  // namespace
+
+int tq_quantize(tq_handle h, const void* x, int x_dtype, int64_t n_rows, int64_t x_row_stride,
+                tq_planes out, void* stream) {
+    const int rc = check_quantize_args(h, x, x_dtype, n_rows, x_row_stride, out, "quantizer");
+    if (rc != TQ_OK || n_rows == 0) return rc;
     return launch_quantize(*h, x, x_dtype, n_rows, x_row_stride, out, (cudaStream_t)stream);
+}
+
+int tq_quantize_kv(tq_handle hk, tq_handle hv, const void* k, const void* v, int x_dtype, int64_t k_rows,
+                   int64_t v_rows, int64_t k_row_stride, int64_t v_row_stride, tq_planes k_out, tq_planes v_out,
+                   void* stream) {
+    int rc = check_quantize_args(hk, k, x_dtype, k_rows, k_row_stride, k_out, "key quantizer");
+    if (rc != TQ_OK) return rc;
+    if ((rc = check_quantize_args(hv, v, x_dtype, v_rows, v_row_stride, v_out, "value quantizer")) != TQ_OK) return rc;
+    const cudaStream_t s = (cudaStream_t)stream;
+    if (quantize_pair_tc_supported(*hk, *hv, x_dtype, k_rows, v_rows))
+        return launch_quantize_pair_tc(*hk, k, k_rows, k_row_stride, k_out, *hv, v, v_rows, v_row_stride, v_out,
+                                       x_dtype, s);
+    if (k_rows > 0 && (rc = launch_quantize(*hk, k, x_dtype, k_rows, k_row_stride, k_out, s)) != TQ_OK) return rc;
+    if (v_rows > 0) rc = launch_quantize(*hv, v, x_dtype, v_rows, v_row_stride, v_out, s);
+    return rc;
 }
 
 int tq_dequantize(tq_handle h, tq_planes in, int64_t n_rows, void* y, int y_dtype, void* stream) {

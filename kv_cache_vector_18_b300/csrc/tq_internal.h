@@ -162,6 +162,11 @@ int launch_append(const tq_ctx& hk, const tq_ctx& hv, const void* k_new, const v
                   int n_tickets, cudaStream_t s);
 int launch_quantize_tc(const tq_ctx& h, const void* x, int x_dtype, int64_t n_rows, int64_t x_row_stride,
                        const tq_planes& out, cudaStream_t s);
+// Two mse quantizers (same d ∈ {64, 128}, b, rotation kind) in one tensor-core launch.
+bool quantize_pair_tc_supported(const tq_ctx& ha, const tq_ctx& hb, int x_dtype, int64_t rows_a, int64_t rows_b);
+int launch_quantize_pair_tc(const tq_ctx& ha, const void* xa, int64_t rows_a, int64_t stride_a, const tq_planes& out_a,
+                            const tq_ctx& hb, const void* xb, int64_t rows_b, int64_t stride_b, const tq_planes& out_b,
+                            int x_dtype, cudaStream_t s);
 int launch_quantize(const tq_ctx& h, const void* x, int x_dtype, int64_t n_rows,
                     int64_t x_row_stride, const tq_planes& out, cudaStream_t s);
 int launch_dequantize(const tq_ctx& h, const tq_planes& in, int64_t n_rows, void* y,

@@ -81,14 +81,38 @@ struct TcCfg {
     static constexpr size_t kSmemBytes = kBarOffset + 256 + 1024;  // barriers + alignment slack
 };
 
+// One quantizer's share of an mse launch: its rows (a tensor map for bf16 rows,
+// a pointer for fp32 rows), its rotation operands, codebook and output planes.
+struct TcSide {
+    CUtensorMap tm_x, tm_pi_hi, tm_pi_lo;
+    const float* xf;
+    int64_t xf_stride;
+    int64_t n_rows;
+    float norm_scale;
+    Codebook cb;
+    uint8_t* codes;
+    float* norm_out;
+    int* status;
+};
+
+// CTAs [0, split) quantize side a, CTAs [split, gridDim.x) side b (the K and V
+// rows of one decode step in one launch; a single quantizer passes split =
+// gridDim.x).  Both sides share D, b, the row dtype and the number of Π passes.
 template <int D, int BM, bool F32 = false>
 __global__ void __launch_bounds__(kThreads, 1)
-quantize_mse_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_pi_hi,
-                       const __grid_constant__ CUtensorMap tm_pi_lo, int64_t n_rows, int npass, float norm_scale,
-                       Codebook cb, uint8_t* __restrict__ codes, float* __restrict__ norm_out,
-                       int* __restrict__ status, const float* __restrict__ xf, int64_t xf_stride) {
+quantize_mse_tc_kernel(const __grid_constant__ TcSide side_a, const __grid_constant__ TcSide side_b, int split,
+                       int npass) {
     using C = TcCfg<D, F32>;
     constexpr int kAcc = C::kAcc;
+    const bool on_b = (int)blockIdx.x >= split;
+    const TcSide& sd = on_b ? side_b : side_a;
+    const int cta = on_b ? (int)blockIdx.x - split : (int)blockIdx.x;
+    const int ncta = on_b ? (int)gridDim.x - split : split;
+    const CUtensorMap* tm_x = &sd.tm_x;
+    const CUtensorMap* tm_pi_hi = &sd.tm_pi_hi;
+    const CUtensorMap* tm_pi_lo = &sd.tm_pi_lo;
+    const int64_t n_rows = sd.n_rows;
+    int* const status = sd.status;
     constexpr int L = 1 << BM;
     constexpr int P = L / 2 - 1;          // positive decision boundaries
     constexpr int WORDS = BM * D / 32;    // packed 32-bit words per row
@@ -130,23 +154,23 @@ quantize_mse_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
 
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------------------ producer
-        prefetch_tensormap(&tm_x);
-        prefetch_tensormap(&tm_pi_hi);
-        prefetch_tensormap(&tm_pi_lo);
+        if (!F32) prefetch_tensormap(tm_x);
+        prefetch_tensormap(tm_pi_hi);
+        prefetch_tensormap(tm_pi_lo);
         mbar_arrive_expect_tx(pi_full, npass * C::kPiBytes);
         for (int c = 0; c < C::kChunks; ++c) {
-            tma_load_2d(pi_hi + c * C::kChunkBytesB, &tm_pi_hi, pi_full, c * kKC, 0);
-            if (npass == 2) tma_load_2d(pi_lo + c * C::kChunkBytesB, &tm_pi_lo, pi_full, c * kKC, 0);
+            tma_load_2d(pi_hi + c * C::kChunkBytesB, tm_pi_hi, pi_full, c * kKC, 0);
+            if (npass == 2) tma_load_2d(pi_lo + c * C::kChunkBytesB, tm_pi_lo, pi_full, c * kKC, 0);
         }
         int64_t i = 0;
-        for (int64_t tile = blockIdx.x; !F32 && tile < ntiles; tile += gridDim.x, ++i) {
+        for (int64_t tile = cta; !F32 && tile < ntiles; tile += ncta, ++i) {
             const int s = (int)(i % C::kStages);
             const int64_t u = i / C::kStages;
             if (u > 0 && !mbar_wait(&empty[s], (uint32_t)((u - 1) & 1), status, 1)) break;
             mbar_arrive_expect_tx(&full[s], C::kStageBytes);
             uint8_t* st = stages + (size_t)s * C::kStageBytes;
             for (int c = 0; c < C::kChunks; ++c)
-                tma_load_2d(st + c * C::kChunkBytesA, &tm_x, &full[s], c * kKC, (int)(tile * kTile));
+                tma_load_2d(st + c * C::kChunkBytesA, tm_x, &full[s], c * kKC, (int)(tile * kTile));
         }
         // Every load issued must have landed before the CTA may exit.
         const int64_t issued = i;
@@ -160,7 +184,7 @@ quantize_mse_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
         tc_fence_after();
         const uint32_t a_base = smem_u32(stages), hi_base = smem_u32(pi_hi), lo_base = smem_u32(pi_lo);
         int64_t i = 0;
-        for (int64_t tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x, ++i) {
+        for (int64_t tile = cta; ok && tile < ntiles; tile += ncta, ++i) {
             const int s = (int)(i % C::kStages);
             const int acc = (int)(i % kAcc);
             const int64_t ua = i / kAcc;
@@ -197,6 +221,8 @@ quantize_mse_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
         // becomes 8 bf16 hi and 8 bf16 lo values at the chunk's 128-byte-swizzled
         // place (row r: 16-byte slot (c8 mod 8) XOR (r mod 8) of its 64-column block)
         const int ct = threadIdx.x - 32 * C::kConvWarp0;
+        const float* __restrict__ xf = sd.xf;
+        const int64_t xf_stride = sd.xf_stride;
         constexpr int CH = D / 8;  // chunks per row
         constexpr int kRounds = kTile * CH / (128 * 4);
         auto conv_all = [&](bool ok) -> bool {
@@ -212,7 +238,7 @@ quantize_mse_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
             return r != 0;
         };
         int64_t i = 0;
-        for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++i) {
+        for (int64_t tile = cta; tile < ntiles; tile += ncta, ++i) {
             const int s = (int)(i % C::kStages);
             const int64_t u = i / C::kStages;
             if (u > 0 && !conv_all(mbar_wait(&empty[s], (uint32_t)((u - 1) & 1), status, 8))) break;
@@ -262,14 +288,17 @@ quantize_mse_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
         constexpr float kAcc0 = (float)(1u << (GB - 1)) - 0.5f;  // Σ_i (L/2 − ½)·2^(b·i)
         const int wg = (warp - 2) >> 2;                 // accumulator served
         const int quad = warp & 3;                      // TMEM lane quadrant of this warp
+        const Codebook& cb = sd.cb;
+        uint8_t* const codes = sd.codes;
+        float* const norm_out = sd.norm_out;
+        const float norm_scale = sd.norm_scale;
         const int r_local = quad * 32 + lane;
         float t2[P > 0 ? P : 1];                        // squared positive boundaries
 #pragma unroll
         for (int p = 0; p < P; ++p) t2[p] = cb.t[L / 2 + p] * cb.t[L / 2 + p];
         const uint32_t taddr0 = tmem_base + (uint32_t)(wg * D) + ((uint32_t)(quad * 32) << 16);
         int64_t j = 0;
-        for (int64_t tile = blockIdx.x + (int64_t)wg * gridDim.x; tile < ntiles;
-             tile += (int64_t)kAcc * gridDim.x, ++j) {
+        for (int64_t tile = cta + (int64_t)wg * ncta; tile < ntiles; tile += (int64_t)kAcc * ncta, ++j) {
             if (!mbar_wait(&tfull[wg], (uint32_t)(j & 1), status, 7)) break;
             tc_fence_after();
             // pass 1: ‖y‖², two 32-column TMEM loads in flight per wait
@@ -374,22 +403,52 @@ quantize_mse_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
     }
 }
 
-template <int D, int BM, bool F32 = false>
-int launch_tc(const tq_ctx& h, const CUtensorMap& tm_x, int64_t n_rows, const tq_planes& out, cudaStream_t s,
-              const float* xf = nullptr, int64_t xf_stride = 0) {
+TcSide make_side(const tq_ctx& h, const CUtensorMap* tm_x, const float* xf, int64_t stride, int64_t n_rows,
+                 const tq_planes& out) {
+    TcSide sd;
+    memset(&sd, 0, sizeof(sd));
+    const bool one = h.rot_passes == 1;
+    if (tm_x) sd.tm_x = *tm_x;
+    sd.tm_pi_hi = one ? h.dp.tm_pm : h.dp.tm_pi_hi;
+    sd.tm_pi_lo = one ? h.dp.tm_pm : h.dp.tm_pi_lo;
+    sd.xf = xf;
+    sd.xf_stride = stride;
+    sd.n_rows = n_rows;
+    sd.norm_scale = h.rot_norm_scale;
+    sd.cb = h.cb;
+    sd.codes = out.codes;
+    sd.norm_out = out.norm;
+    sd.status = h.dp.status;
+    return sd;
+}
+
+// One launch over one side, or over two (b != nullptr, both holding rows): the
+// grid's CTAs are divided between the sides in proportion to their tiles.
+template <int D, int BM, bool F32>
+int launch_tc(const TcSide& a, const TcSide* b, int npass, int num_sms, cudaStream_t s) {
     using C = TcCfg<D, F32>;
     auto fn = quantize_mse_tc_kernel<D, BM, F32>;
     static std::atomic<uint64_t> smem_set{0};
     const int rc = ensure_smem_attr(smem_set, (const void*)fn, (int)C::kSmemBytes, "quantize smem attribute");
     if (rc != TQ_OK) return rc;
-    const int64_t ntiles = (n_rows + kTile - 1) / kTile;
-    const int grid = (int)(ntiles < h.num_sms ? ntiles : h.num_sms);
-    const bool one = h.rot_passes == 1;
-    fn<<<grid, kThreads, C::kSmemBytes, s>>>(tm_x, one ? h.dp.tm_pm : h.dp.tm_pi_hi, one ? h.dp.tm_pm : h.dp.tm_pi_lo,
-                                             n_rows, h.rot_passes, h.rot_norm_scale, h.cb, out.codes, out.norm,
-                                             h.dp.status, xf, xf_stride);
+    const int64_t ta = (a.n_rows + kTile - 1) / kTile;
+    const int64_t tb = b ? (b->n_rows + kTile - 1) / kTile : 0;
+    const int64_t tiles = ta + tb;
+    const int grid = (int)(tiles < num_sms ? tiles : num_sms);
+    int split = grid;
+    if (b) {  // both sides hold ≥ 1 tile, so grid ≥ 2
+        const int64_t want = (ta * grid + tiles / 2) / tiles;
+        split = (int)(want < 1 ? 1 : (want > grid - 1 ? grid - 1 : want));
+    }
+    fn<<<grid, kThreads, C::kSmemBytes, s>>>(a, b ? *b : a, split, npass);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? TQ_OK : cuda_fail(e, "tensor-core quantize launch");
+}
+
+template <int D, int BM>
+int launch_tc(const tq_ctx& h, const CUtensorMap& tm_x, int64_t n_rows, const tq_planes& out, cudaStream_t s) {
+    const TcSide a = make_side(h, &tm_x, nullptr, 0, n_rows, out);
+    return launch_tc<D, BM, false>(a, nullptr, h.rot_passes, h.num_sms, s);
 }
 
 template <int D>
@@ -408,13 +467,25 @@ int launch_tc_d(const tq_ctx& h, const CUtensorMap& tm_x, int64_t n_rows, const 
 template <int D>
 int launch_tc_f32_d(const tq_ctx& h, const float* x, int64_t n_rows, int64_t stride, const tq_planes& out,
                     cudaStream_t s) {
-    const CUtensorMap& none = h.dp.tm_pi_hi;
+    const TcSide a = make_side(h, nullptr, x, stride, n_rows, out);
     switch (h.hp.b_mse) {
-        case 1: return launch_tc<D, 1, true>(h, none, n_rows, out, s, x, stride);
-        case 2: return launch_tc<D, 2, true>(h, none, n_rows, out, s, x, stride);
-        case 3: return launch_tc<D, 3, true>(h, none, n_rows, out, s, x, stride);
-        case 4: return launch_tc<D, 4, true>(h, none, n_rows, out, s, x, stride);
+        case 1: return launch_tc<D, 1, true>(a, nullptr, h.rot_passes, h.num_sms, s);
+        case 2: return launch_tc<D, 2, true>(a, nullptr, h.rot_passes, h.num_sms, s);
+        case 3: return launch_tc<D, 3, true>(a, nullptr, h.rot_passes, h.num_sms, s);
+        case 4: return launch_tc<D, 4, true>(a, nullptr, h.rot_passes, h.num_sms, s);
         default: return fail(TQ_EUNSUPPORTED, "b_m=%d", h.hp.b_mse);
+    }
+}
+
+// K and V sides in one launch (same D, b, row dtype and Π passes)
+template <int D, bool F32>
+int launch_tc_pair_d(int b_mse, const TcSide& a, const TcSide& b, int npass, int num_sms, cudaStream_t s) {
+    switch (b_mse) {
+        case 1: return launch_tc<D, 1, F32>(a, &b, npass, num_sms, s);
+        case 2: return launch_tc<D, 2, F32>(a, &b, npass, num_sms, s);
+        case 3: return launch_tc<D, 3, F32>(a, &b, npass, num_sms, s);
+        case 4: return launch_tc<D, 4, F32>(a, &b, npass, num_sms, s);
+        default: return fail(TQ_EUNSUPPORTED, "b_m=%d", b_mse);
     }
 }
 
@@ -1554,6 +1625,34 @@ bool quantize_tc_supported(const tq_ctx& h, int x_dtype, int64_t n_rows) {
     const bool dim = h.hp.d == 64 || h.hp.d == 128 || h.hp.d == 256;
     const bool f32 = x_dtype == TQ_F32 && h.hp.variant == TQ_MSE && (h.hp.d == 64 || h.hp.d == 128);
     return (x_dtype == TQ_BF16 || f32) && dim && params && h.num_sms > 0 && n_rows < ((int64_t)1 << 31) - kTile;
+}
+
+bool quantize_pair_tc_supported(const tq_ctx& ha, const tq_ctx& hb, int x_dtype, int64_t rows_a, int64_t rows_b) {
+    return ha.hp.variant == TQ_MSE && hb.hp.variant == TQ_MSE && ha.hp.d == hb.hp.d && (ha.hp.d == 64 || ha.hp.d == 128) &&
+           ha.hp.b_mse == hb.hp.b_mse && ha.rot_passes == hb.rot_passes && rows_a > 0 && rows_b > 0 &&
+           quantize_tc_supported(ha, x_dtype, rows_a) && quantize_tc_supported(hb, x_dtype, rows_b) &&
+           ha.num_sms == hb.num_sms;
+}
+
+int launch_quantize_pair_tc(const tq_ctx& ha, const void* xa, int64_t rows_a, int64_t stride_a, const tq_planes& out_a,
+                            const tq_ctx& hb, const void* xb, int64_t rows_b, int64_t stride_b, const tq_planes& out_b,
+                            int x_dtype, cudaStream_t s) {
+    const int d = ha.hp.d;
+    if (x_dtype == TQ_F32) {
+        const TcSide a = make_side(ha, nullptr, static_cast<const float*>(xa), stride_a, rows_a, out_a);
+        const TcSide b = make_side(hb, nullptr, static_cast<const float*>(xb), stride_b, rows_b, out_b);
+        return d == 64 ? launch_tc_pair_d<64, true>(ha.hp.b_mse, a, b, ha.rot_passes, ha.num_sms, s)
+                       : launch_tc_pair_d<128, true>(ha.hp.b_mse, a, b, ha.rot_passes, ha.num_sms, s);
+    }
+    CUtensorMap ma, mb;
+    int rc = encode_tmap_bf16_2d(&ma, xa, (uint64_t)d, (uint64_t)rows_a, (uint64_t)stride_a * 2, kKC, kTile);
+    if (rc != TQ_OK) return rc;
+    rc = encode_tmap_bf16_2d(&mb, xb, (uint64_t)d, (uint64_t)rows_b, (uint64_t)stride_b * 2, kKC, kTile);
+    if (rc != TQ_OK) return rc;
+    const TcSide a = make_side(ha, &ma, nullptr, 0, rows_a, out_a);
+    const TcSide b = make_side(hb, &mb, nullptr, 0, rows_b, out_b);
+    return d == 64 ? launch_tc_pair_d<64, false>(ha.hp.b_mse, a, b, ha.rot_passes, ha.num_sms, s)
+                   : launch_tc_pair_d<128, false>(ha.hp.b_mse, a, b, ha.rot_passes, ha.num_sms, s);
 }
 
 int launch_quantize_tc(const tq_ctx& h, const void* x, int x_dtype, int64_t n_rows, int64_t stride,

@@ -207,3 +207,52 @@ def test_tensor_core_path_fp32_rows(tq, d, bits, rotation):
     codes = planes["codes"].cpu().numpy()
     assert np.all(codes[5] == 0) and np.all(codes[n - 1] == 0)
     assert planes["norm"][5].item() == 0
+
+
+@pytest.mark.parametrize("case", [
+    # (d, bits K, variant K, bits V, variant V, rotation, dtype, K rows, V rows): one launch
+    (128, 3, "mse", 3, "mse", "qr", "bf16", 148 * 128 * 2 + 77, 148 * 128 * 2 + 77),
+    (64, 2, "mse", 2, "mse", "hadamard", "bf16", 5000, 300001),
+    (128, 4, "mse", 4, "mse", "qr", "f32", 20000, 777),
+    (128, 1, "mse", 1, "mse", "qr", "bf16", 1, 1),
+    (128, 3, "mse", 3, "mse", "qr", "bf16", 0, 4000),
+    # two launches: prod keys, d = 256, different bits
+    (128, 3, "prod", 3, "mse", "qr", "bf16", 3000, 3000),
+    (256, 2, "mse", 2, "mse", "qr", "bf16", 1000, 1000),
+    (128, 4, "mse", 2, "mse", "qr", "bf16", 2000, 2000),
+])
+def test_quantize_kv_matches_separate_calls(tq, case):
+    # tq_quantize_kv (K and V in one launch where the pair allows it) writes the
+    # same bytes as two tq_quantize calls; those are checked against the oracle
+    d, bk, vk, bv, vv, rot, dt, nk, nv = case
+    kq = tq.Quantizer(d, bk, vk, seed=101, rotation=rot)
+    vq = tq.Quantizer(d, bv, vv, seed=102, rotation=rot)
+    K = synthetic.gaussian((nk, d), seed=11, dtype=dt).cuda()
+    V = synthetic.student_t_unit_var((nv, d), seed=12, dtype=dt).cuda()
+    kc, vc = tq.quantize_kv(kq, vq, K, V)
+    ks, vs = kq.quantize(K), vq.quantize(V)
+    torch.cuda.synchronize()
+    assert kq.device_status() == 0 and vq.device_status() == 0
+    for got, ref in ((kc, ks), (vc, vs)):
+        for name in ref:
+            assert torch.equal(got[name], ref[name]), name
+    rows = np.unique(np.concatenate([np.arange(0, min(nv, 200)), np.arange(max(nv - 200, 0), nv)]))
+    if nv:
+        check_quantize(oracle_params(vq), f64(V), vc, rows=rows)
+
+
+def test_quantize_kv_rejects_bad_arguments(tq):
+    from kv_cache_vector_18_b300 import _lib
+    kq = tq.Quantizer(128, 3, "mse", seed=1)
+    vq = tq.Quantizer(128, 3, "mse", seed=2)
+    x = torch.zeros((16, 128), dtype=torch.bfloat16, device="cuda")
+    kp, vp = kq.empty_planes(16), vq.empty_planes(16)
+    L = _lib.lib()
+    ks, vs = kq.planes_struct(kp), vq.planes_struct(vp)
+    assert L.tq_quantize_kv(kq.handle, vq.handle, x.data_ptr(), x.data_ptr() + 2, 0, 16, 15, 128, 128, ks, vs,
+                            None) == _lib.TQ_EALIGN
+    assert L.tq_quantize_kv(kq.handle, None, x.data_ptr(), x.data_ptr(), 0, 16, 16, 128, 128, ks, vs,
+                            None) == _lib.TQ_EINVAL
+    assert L.tq_quantize_kv(kq.handle, vq.handle, x.data_ptr(), x.data_ptr(), 0, 16, 16, 128, 64, ks, vs,
+                            None) == _lib.TQ_EINVAL
+    torch.cuda.synchronize()
