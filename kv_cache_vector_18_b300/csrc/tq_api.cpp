@@ -102,7 +102,8 @@ void free_device(tq_ctx* h) {
         if (*p) cudaFree(*p);
         *p = nullptr;
     }
-    uint16_t** hl[] = {&h->dp.Pi_hi, &h->dp.Pi_lo, &h->dp.S_hi, &h->dp.S_lo, &h->dp.T_hi, &h->dp.T_lo, &h->dp.Pm};
+    uint16_t** hl[] = {&h->dp.Pi_hi,  &h->dp.Pi_lo,  &h->dp.S_hi,  &h->dp.S_lo, &h->dp.PiT_hi, &h->dp.PiT_lo,
+                       &h->dp.ST_hi,  &h->dp.ST_lo,  &h->dp.T_hi,  &h->dp.T_lo, &h->dp.Pm};
     for (uint16_t** p : hl) {
         if (*p) cudaFree(*p);
         *p = nullptr;
@@ -142,12 +143,22 @@ int upload_bf16_split(const std::vector<double>& m, uint16_t** dhi, uint16_t** d
     return rc;
 }
 
-// Π = Π_hi + Π_lo (and S = S_hi + S_lo) in bf16 for the tensor-core kernels, plus
-// the TMA maps over Π_hi / Π_lo.
+std::vector<double> transposed(const std::vector<double>& m, int d) {
+    std::vector<double> t(m.size());
+    for (int j = 0; j < d; ++j)
+        for (int i = 0; i < d; ++i) t[(size_t)i * d + j] = m[(size_t)j * d + i];
+    return t;
+}
+
+// Π = Π_hi + Π_lo (and S = S_hi + S_lo) in bf16 for the tensor-core kernels, their
+// transposes split the same way, plus the TMA maps over Π_hi / Π_lo.
 int upload_tensor_core_params(tq_ctx* h) {
     const int d = h->hp.d;
     int rc = upload_bf16_split(h->hp.Pi, &h->dp.Pi_hi, &h->dp.Pi_lo);
     if (rc == TQ_OK && h->hp.variant == TQ_PROD) rc = upload_bf16_split(h->hp.S, &h->dp.S_hi, &h->dp.S_lo);
+    if (rc == TQ_OK) rc = upload_bf16_split(transposed(h->hp.Pi, d), &h->dp.PiT_hi, &h->dp.PiT_lo);
+    if (rc == TQ_OK && h->hp.variant == TQ_PROD)
+        rc = upload_bf16_split(transposed(h->hp.S, d), &h->dp.ST_hi, &h->dp.ST_lo);
     if (rc != TQ_OK) return rc;
     if (d % 64 == 0) {
         rc = encode_tmap_bf16_2d(&h->dp.tm_pi_hi, h->dp.Pi_hi, d, d, (uint64_t)d * 2, 64, d);

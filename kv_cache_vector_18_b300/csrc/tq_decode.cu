@@ -297,6 +297,7 @@ int launch_d(const tq_ctx& hk, const tq_ctx& hv, const DecodeShape& p, const voi
     a.B = p.B; a.Hq = p.Hq; a.Hkv = p.Hkv; a.T_max = p.T_max; a.G = p.G;
     a.n_splits = p.n_splits; a.chunk = p.chunk;
     a.cnt = cnt; a.vPi = hv.dp.Pi; a.vS = hv.dp.S; a.out = out;
+    a.vPiT_hi = hv.dp.PiT_hi; a.vPiT_lo = hv.dp.PiT_lo; a.vST_hi = hv.dp.ST_hi; a.vST_lo = hv.dp.ST_lo;
     a.q = q; a.q_f32 = q_dtype == TQ_F32; a.kPi_hi = hk.dp.Pi_hi; a.kPi_lo = hk.dp.Pi_lo; a.kS_hi = hk.dp.S_hi; a.kS_lo = hk.dp.S_lo;
     a.status = hk.dp.status;
     if (use_mma_split(D)) {

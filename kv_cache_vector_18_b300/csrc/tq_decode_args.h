@@ -29,11 +29,17 @@ struct SplitArgs {
     float kgamma, vgamma, scale;
     int B, Hq, Hkv, T_max, G, n_splits, chunk, n_hblocks;
     // Fused merge (tensor-core path): one ticket counter per (batch, KV head,
-    // head block), zeroed by the query-prep launch; the last split CTA of a group
-    // combines the partials and writes out = Π_vᵀ·acc/l (+ S_vᵀ·acc2/l).
+    // head block), zeroed before the launch (a memset, or the decode-step append);
+    // the last split CTA of a group combines the partials and writes
+    // out = Π_vᵀ·acc/l (+ S_vᵀ·acc2/l).
     int* cnt;
     const float* vPi;  // Π_v row-major [d][d]
     const float* vS;   // S_v row-major [d][d] (prod values)
+    // Π_vᵀ = hi + lo and S_vᵀ = hi + lo, bf16 row-major [i][j]: the merge's matrix operands
+    const uint16_t* vPiT_hi;
+    const uint16_t* vPiT_lo;
+    const uint16_t* vST_hi;
+    const uint16_t* vST_lo;
     float* out;        // [B, Hq, d]
     // Query rotation inside the split kernel (tensor-core path): q′ = Π_k·q, q″ = S_k·q.
     const void* q;     // [B, Hq, d], bf16 or f32
@@ -55,6 +61,7 @@ constexpr int kHeadsPerCta = 8;
 constexpr int D128 = 128;
 constexpr int kMaxSplitsMerged = 256;  // splits the last CTA of a group can merge
 constexpr int kDecodeStageTimeout = 30;  // status code of an expired tile-staging wait
+constexpr int kDecodeMergeTimeout = 31;  // status code of an expired wait for the split partials
 // resident split CTAs per SM of the tensor-core decode kernel (one 16- or 8-warp CTA)
 constexpr int ctas_per_sm(bool /*vprod*/) { return 1; }
 template <int KB, bool KP>

@@ -115,6 +115,58 @@ constexpr int kQChunk = 36;
 constexpr int kQRow = 4 * kQChunk;
 __host__ __device__ constexpr int qidx(int h, int j) { return h * kQRow + (j >> 5) * kQChunk + (j & 31); }
 
+// ---- 8 heads × a d × d matrix on mma.sync with bf16 hi/lo operands ------------
+// r[h][i] = Σ_j M[i][j]·x[h][j] for a matrix held as M = M_hi + M_lo (bf16,
+// row-major [i][j]) and fp32 rows x.  The A operand is [x_hi; x_lo] (rows g and
+// g + 8 of the MMA), so the two halves of each output come out in rows g and g + 8
+// and their sum carries fp32-level accuracy.  The contraction order is permuted so
+// that in k16 blocks 2p and 2p + 1 lane (g, c) holds the eight consecutive dims
+// 32p + 8c … 32p + 8c + 7: its matrix operand is one 16-byte load of row i0 + g.
+// A fragments of head g from its fp32 row xg (dims contiguous).
+__device__ __forceinline__ void hilo_a(const float* xg, int c, uint32_t (&A)[kKB][4]) {
+#pragma unroll
+    for (int ks = 0; ks < kKB; ++ks)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const int d0 = 32 * (ks >> 1) + 8 * c + 4 * (ks & 1) + 2 * hh;
+            const float2 x = *reinterpret_cast<const float2*>(xg + d0);
+            const __nv_bfloat162 hi = __floats2bfloat162_rn(x.x, x.y);
+            const float2 hf = __bfloat1622float2(hi);
+            A[ks][2 * hh] = *reinterpret_cast<const uint32_t*>(&hi);
+            A[ks][2 * hh + 1] = pack_bf2(x.x - hf.x, x.y - hf.y);
+        }
+}
+// The same from a bf16 row: x is exact in bf16, so the low rows are zero.
+__device__ __forceinline__ void hilo_a(const __nv_bfloat16* xg, int c, uint32_t (&A)[kKB][4]) {
+#pragma unroll
+    for (int ks = 0; ks < kKB; ++ks)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const int d0 = 32 * (ks >> 1) + 8 * c + 4 * (ks & 1) + 2 * hh;
+            A[ks][2 * hh] = *reinterpret_cast<const uint32_t*>(xg + d0);
+            A[ks][2 * hh + 1] = 0u;
+        }
+}
+// this lane's 16-byte pieces of rows i0 + g of M_hi and M_lo
+__device__ __forceinline__ void hilo_b(const uint16_t* Mhi, const uint16_t* Mlo, int i0, int g, int c,
+                                       uint4 (&bh)[kKB / 2], uint4 (&bl)[kKB / 2]) {
+    const int row = ((i0 + g) * D + 8 * c) >> 3;  // 16-byte index of (i0 + g, 8c)
+#pragma unroll
+    for (int p2 = 0; p2 < kKB / 2; ++p2) {
+        bh[p2] = __ldg(reinterpret_cast<const uint4*>(Mhi) + row + 4 * p2);
+        bl[p2] = __ldg(reinterpret_cast<const uint4*>(Mlo) + row + 4 * p2);
+    }
+}
+__device__ __forceinline__ void hilo_mma(float (&acc)[4], const uint32_t (&A)[kKB][4], const uint4 (&bh)[kKB / 2],
+                                         const uint4 (&bl)[kKB / 2]) {
+#pragma unroll
+    for (int ks = 0; ks < kKB; ++ks) {
+        const uint4 h = bh[ks >> 1], l = bl[ks >> 1];
+        mma16816_bf16(acc, A[ks], (ks & 1) ? h.z : h.x, (ks & 1) ? h.w : h.y);
+        mma16816_bf16(acc, A[ks], (ks & 1) ? l.z : l.x, (ks & 1) ? l.w : l.y);
+    }
+}
+
 // Bits [bit, bit + NBITS) of the little-endian word run w, returned shifted
 // left by S0 (a byte offset into a table whose entries are 2^S0 bytes apart).
 template <int NBITS, int S0>
@@ -193,23 +245,31 @@ struct Table {
     static constexpr bool kPair = B >= 3;
     static constexpr size_t kBytes =
         kPair ? (size_t)(1 << (2 * B)) * 32 * 4 : (kQuad ? (size_t)256 * 16 * 8 : 0);
-    __device__ static void fill(unsigned char* tabp, const Codebook& cb) {
-        const float s = cb.lut_scale;
+    // Filled by nt threads (thread tid; nt and the entry counts multiples of 32, so
+    // whole warps take part in each round).  Lane k holds centroid k, and an
+    // entry's centroids come from shuffles: indexing the parameter codebook with
+    // per-lane indices would serialise constant-cache reads.
+    __device__ static void fill(unsigned char* tabp, const Codebook& cb, int tid, int nt) {
+        const int lane = tid & 31;
+        float cl = 0.f;
+#pragma unroll
+        for (int k = 0; k < (1 << B); ++k)
+            if (lane == k) cl = cb.c[k] * cb.lut_scale;
         if constexpr (kQuad) {
-            for (int i = threadIdx.x; i < 256 * 16; i += blockDim.x) {
+            for (int i = tid; i < 256 * 16; i += nt) {
                 const uint32_t e = (uint32_t)i >> 4, copy = (uint32_t)i & 15u;
-                uint2 v;
-                v.x = pack_h2(cb.c[e & 3] * s, cb.c[(e >> 2) & 3] * s);
-                v.y = pack_h2(cb.c[(e >> 4) & 3] * s, cb.c[(e >> 6) & 3] * s);
-                *reinterpret_cast<uint2*>(tabp + e * 128u + copy * 8u) = v;
+                const float c0 = __shfl_sync(0xffffffffu, cl, (int)(e & 3)), c1 = __shfl_sync(0xffffffffu, cl, (int)((e >> 2) & 3));
+                const float c2 = __shfl_sync(0xffffffffu, cl, (int)((e >> 4) & 3)), c3 = __shfl_sync(0xffffffffu, cl, (int)((e >> 6) & 3));
+                *reinterpret_cast<uint2*>(tabp + e * 128u + copy * 8u) = make_uint2(pack_h2(c0, c1), pack_h2(c2, c3));
             }
         }
         if constexpr (kPair) {
             constexpr uint32_t m = (1u << B) - 1u;
-            for (int i = threadIdx.x; i < (1 << (2 * B)) * 32; i += blockDim.x) {
+            for (int i = tid; i < (1 << (2 * B)) * 32; i += nt) {
                 const uint32_t e = (uint32_t)i >> 5, copy = (uint32_t)i & 31u;
-                *reinterpret_cast<uint32_t*>(tabp + e * 128u + copy * 4u) =
-                    pack_h2(cb.c[e & m] * s, cb.c[(e >> B) & m] * s);
+                const float c0 = __shfl_sync(0xffffffffu, cl, (int)(e & m));
+                const float c1 = __shfl_sync(0xffffffffu, cl, (int)((e >> B) & m));
+                *reinterpret_cast<uint32_t*>(tabp + e * 128u + copy * 4u) = pack_h2(c0, c1);
             }
         }
     }
@@ -262,8 +322,8 @@ struct KDecoder {
 // quarter-warp's loads apart.  Block kb covers dims 32c + 4kb … 32c + 4kb + 3.
 struct KSignTable {
     static constexpr size_t kBytes = (size_t)256 * 8 * 16;
-    __device__ static void fill(unsigned char* tabp) {
-        for (int i = threadIdx.x; i < 256 * 8; i += blockDim.x) {
+    __device__ static void fill(unsigned char* tabp, int tid, int nt) {
+        for (int i = tid; i < 256 * 8; i += nt) {
             const uint32_t e = (uint32_t)i >> 3, copy = (uint32_t)i & 7u;
             uint32_t v[4];
 #pragma unroll
@@ -532,10 +592,12 @@ struct Smem {
     static constexpr int kMaxSplits = kMaxSplitsMerged;
     static constexpr size_t kMW = 0;                                      // [kHeads][kMaxSplits] weights
     static constexpr size_t kML = kMW + (size_t)kHeads * kMaxSplits * 4;  // [kHeads] 1/l
-    static constexpr size_t kMO = kML + kHeads * 4;                       // [2][D][kHeads] merged acc
-    static constexpr size_t kMP = (kMO + 2 * (size_t)kHeads * D * 4 + 15) & ~(size_t)15;  // [D][D] Π_v, then S_v
-    static constexpr size_t kMQ = kMP + (VP ? 2 : 1) * (size_t)D * D * 4;  // [4][kHeads][D] mat-vec partials
-    static constexpr size_t kMerge = kMQ + 4 * (size_t)kHeads * D * 4;
+    static constexpr int kMRow = D + 8;                                   // padded row: 2-way LDS.64 conflicts
+    static constexpr size_t kMO = (kML + kHeads * 4 + 15) & ~(size_t)15;  // [2][kHeads][kMRow] merged acc
+    static constexpr int kMC = VP ? 16 : 32;                              // splits staged per round
+    static constexpr size_t kMS = kMO + 2 * (size_t)kHeads * kMRow * 4;   // [VP ? 2 : 1][kHeads][kMC][D] partials
+    static constexpr size_t kMerge = kMS + (VP ? 2 : 1) * (size_t)kMC * kHeads * D * 4;
+    static_assert(kQin % 16 == 0 && kMS % 16 == 0, "cp.async destinations must be 16-byte aligned");
     static constexpr size_t kBytes0 = kMain + kAlignSlack > kCombine ? kMain + kAlignSlack : kCombine;
     static constexpr size_t kBytes = kBytes0 > kMerge ? kBytes0 : kMerge;
 };
@@ -700,107 +762,132 @@ __device__ __forceinline__ void step(Acc<VP>& st, const unsigned char* stp, int 
 template <int KB, bool KP, int VB, bool VP>
 __device__ __forceinline__ void merge_group(const SplitArgs& a, unsigned char* smem, size_t head0, int G) {
     using SM = Smem<KB, KP, VB, VP>;
-    constexpr int NT = SM::kThreads;
+    constexpr int NT = SM::kThreads, NW = NT / 32, MR = SM::kMRow;
     float* wts = reinterpret_cast<float*>(smem + SM::kMW);   // [kHeads][kMaxSplits]
     float* linv = reinterpret_cast<float*>(smem + SM::kML);  // [kHeads]
-    float* mo = reinterpret_cast<float*>(smem + SM::kMO);    // [2][D][kHeads]
-    float* pis = reinterpret_cast<float*>(smem + SM::kMP);   // [D][D] Π_v, then [D][D] S_v
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float* mo = reinterpret_cast<float*>(smem + SM::kMO);    // [2][kHeads][MR]: acc/l, acc2/l
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
     const int ns = a.n_splits;
-    // stage Π_v (and S_v) with asynchronous copies that land while the split
-    // weights and the split sum are formed
-    {
-        const uint32_t dst = smem_addr(pis);
-        for (int i = threadIdx.x; i < D * D / 4; i += NT) cp_async16(dst + 16u * i, a.vPi + 4 * i, 16u);
-        if constexpr (VP)
-            for (int i = threadIdx.x; i < D * D / 4; i += NT)
-                cp_async16(dst + 16u * (D * D / 4 + i), a.vS + 4 * i, 16u);
-        cp_async_commit();
+    // out = Π_vᵀ·(acc/l) (+ S_vᵀ·(acc2/l)) on the tensor cores: warp w takes the 8
+    // output dims 8·job for job = w, w + NW, …; with mse values its Π_vᵀ operand is
+    // loaded now, so that the load overlaps the split sums
+    constexpr int kJobs = D / 8, kPer = (kJobs + NW - 1) / NW;
+    constexpr bool kEarly = !VP;  // prod values: two matrices, loaded per job (registers)
+    uint4 bh[kEarly ? kPer : 1][kKB / 2], bl[kEarly ? kPer : 1][kKB / 2];
+    if constexpr (kEarly) {
+#pragma unroll
+        for (int u = 0; u < kPer; ++u)
+            if (warp + u * NW < kJobs) hilo_b(a.vPiT_hi, a.vPiT_lo, 8 * (warp + u * NW), g, c, bh[u], bl[u]);
     }
+    // the split partials, kMC splits per round, brought into shared memory by one
+    // bulk copy per head (a head's splits are contiguous rows) while the split
+    // weights are formed
+    __shared__ __align__(8) uint64_t s_mbar;
+    float* stg = reinterpret_cast<float*>(smem + SM::kMS);
+    constexpr int kMC = SM::kMC;
+    if (threadIdx.x == 0) {
+        sm100::mbar_init(&s_mbar, 1);
+        sm100::fence_barrier_init();
+    }
+    __syncthreads();
+    auto stage_round = [&](int s0) {  // thread 0; the previous contents have been read
+        if (threadIdx.x == 0) {
+            const uint32_t bytes = (uint32_t)min(kMC, ns - s0) * D * 4;
+            asm volatile("fence.proxy.async;" ::: "memory");
+            sm100::mbar_arrive_expect_tx(&s_mbar, (VP ? 2 : 1) * G * bytes);
+#pragma unroll
+            for (int mtx = 0; mtx < (VP ? 2 : 1); ++mtx)
+                for (int h = 0; h < G; ++h)
+                    bulk_g2s(smem_addr(stg + (size_t)(mtx * kHeads + h) * kMC * D),
+                             (mtx ? a.pacc2 : a.pacc) + ((head0 + h) * ns + s0) * D, bytes, smem_addr(&s_mbar));
+        }
+    };
+    stage_round(0);
     if (warp < G) {
+        // split weights of head `warp`: every pm and pl load of the head in flight at once
+        constexpr int kR = SM::kMaxSplits / 32;
         const size_t hs = (head0 + warp) * ns;
+        float pmv[kR], plv[kR];
+#pragma unroll
+        for (int k = 0; k < kR; ++k) {
+            const int sp = lane + 32 * k;
+            pmv[k] = sp < ns ? __ldcg(a.pm + hs + sp) : -INFINITY;
+            plv[k] = sp < ns ? __ldcg(a.pl + hs + sp) : 0.f;
+        }
         float mx = -INFINITY;
-        for (int s = lane; s < ns; s += 32) mx = fmaxf(mx, __ldcg(a.pm + hs + s));
+#pragma unroll
+        for (int k = 0; k < kR; ++k) mx = fmaxf(mx, pmv[k]);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
         float l = 0.f;
-        for (int s = lane; s < ns; s += 32) {
-            const float f = mx == -INFINITY ? 0.f : ex2((__ldcg(a.pm + hs + s) - mx) * kLog2e);
-            wts[warp * SM::kMaxSplits + s] = f;
-            l = fmaf(f, __ldcg(a.pl + hs + s), l);
+#pragma unroll
+        for (int k = 0; k < kR; ++k) {
+            const int sp = lane + 32 * k;
+            if (sp < ns) {
+                const float f = mx == -INFINITY ? 0.f : ex2((pmv[k] - mx) * kLog2e);
+                wts[warp * SM::kMaxSplits + sp] = f;
+                l = fmaf(f, plv[k], l);
+            }
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
         if (lane == 0) linv[warp] = l > 0.f ? 1.f / l : 0.f;
     }
-    __syncthreads();
-    // Σ over splits, coalesced over dims (up to 32 splits' loads in flight per
-    // round); stored dim-major so the mat-vec reads the 8 heads of a dim at once
-    for (int i = threadIdx.x; i < G * D; i += NT) {
-        const int h = i / D, j = i % D;
-        const size_t hs = (head0 + h) * ns;
-        const float* w = wts + h * SM::kMaxSplits;
-        float o = 0.f, o2 = 0.f;
-        for (int s0 = 0; s0 < ns; s0 += 32) {
-            float v[32], v2[VP ? 32 : 1];
-#pragma unroll
-            for (int k = 0; k < 32; ++k) {
-                const bool in = s0 + k < ns;
-                v[k] = in ? __ldcg(a.pacc + (hs + s0 + k) * D + j) : 0.f;
-                if constexpr (VP) v2[k] = in ? __ldcg(a.pacc2 + (hs + s0 + k) * D + j) : 0.f;
-            }
-#pragma unroll
-            for (int k = 0; k < 32; ++k) {
-                const float wk = s0 + k < ns ? w[s0 + k] : 0.f;
-                o = fmaf(wk, v[k], o);
-                if constexpr (VP) o2 = fmaf(wk, v2[k], o2);
-            }
-        }
-        mo[j * kHeads + h] = o * linv[h];
-        if constexpr (VP) mo[kHeads * D + j * kHeads + h] = o2 * linv[h];
-    }
-    for (int i = G * D + threadIdx.x; i < kHeads * D; i += NT) {  // heads past G: zero
-        mo[(i % D) * kHeads + i / D] = 0.f;
-        if constexpr (VP) mo[kHeads * D + (i % D) * kHeads + i / D] = 0.f;
-    }
-    cp_async_wait<0>();  // this thread's part of Π_v has landed
-    __syncthreads();
-    // out[h][col] = Σ_j Π_v[j][col]·o[j][h] (+ S_v[j][col]·o2[j][h]): thread (col, quarter)
-    // sums its quarter of j for all 8 heads (one matrix load feeds 8 FMAs), then
-    // the four quarters are added
-    float* part = reinterpret_cast<float*>(smem + SM::kMQ);  // [4][kHeads][D]
-    for (int t2 = threadIdx.x; t2 < 4 * D; t2 += NT) {
-        const int col = t2 % D, jq = t2 / D;
-        float r[kHeads];
-#pragma unroll
-        for (int k = 0; k < kHeads; ++k) r[k] = 0.f;
-#pragma unroll
-        for (int mtx = 0; mtx < (VP ? 2 : 1); ++mtx) {
-            const float* P = pis + mtx * D * D;
-            const float* Mo = mo + mtx * kHeads * D;
-#pragma unroll 4
-            for (int j = 32 * jq; j < 32 * jq + 32; ++j) {
-                const float p = P[j * D + col];
-                const float4 m0 = *reinterpret_cast<const float4*>(Mo + j * kHeads);
-                const float4 m1 = *reinterpret_cast<const float4*>(Mo + j * kHeads + 4);
-                r[0] = fmaf(p, m0.x, r[0]);
-                r[1] = fmaf(p, m0.y, r[1]);
-                r[2] = fmaf(p, m0.z, r[2]);
-                r[3] = fmaf(p, m0.w, r[3]);
-                r[4] = fmaf(p, m1.x, r[4]);
-                r[5] = fmaf(p, m1.y, r[5]);
-                r[6] = fmaf(p, m1.z, r[6]);
-                r[7] = fmaf(p, m1.w, r[7]);
+    // Σ over splits from shared memory: thread t < kHeads·D/4 sums four dims of one head
+    const int th = threadIdx.x / (D / 4), tj = threadIdx.x % (D / 4);
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f), o2 = o;
+    for (int s0 = 0, round = 0; s0 < ns; s0 += kMC, ++round) {
+        const bool ok = sm100::mbar_wait(&s_mbar, (uint32_t)(round & 1), a.status, kDecodeMergeTimeout);
+        __syncthreads();  // this round's partials (and, first time, the weights) are visible
+        const int nsc = min(kMC, ns - s0);
+        if (ok && th < G) {
+            const float* w = wts + th * SM::kMaxSplits + s0;
+            const float4* x = reinterpret_cast<const float4*>(stg) + (size_t)th * kMC * (D / 4) + tj;
+            const float4* x2 = x + (size_t)kHeads * kMC * (D / 4);
+            for (int sp = 0; sp < nsc; ++sp) {
+                const float ws = w[sp];
+                const float4 v = x[sp * (D / 4)];
+                o = make_float4(fmaf(ws, v.x, o.x), fmaf(ws, v.y, o.y), fmaf(ws, v.z, o.z), fmaf(ws, v.w, o.w));
+                if constexpr (VP) {
+                    const float4 v2 = x2[sp * (D / 4)];
+                    o2 = make_float4(fmaf(ws, v2.x, o2.x), fmaf(ws, v2.y, o2.y), fmaf(ws, v2.z, o2.z),
+                                     fmaf(ws, v2.w, o2.w));
+                }
             }
         }
-#pragma unroll
-        for (int k = 0; k < kHeads; ++k) part[(jq * kHeads + k) * D + col] = r[k];
+        if (s0 + kMC < ns) {
+            __syncthreads();  // the staged round has been read
+            stage_round(s0 + kMC);
+        }
+    }
+    if (th < kHeads) {  // heads past G: zero
+        const float li = th < G ? linv[th] : 0.f;
+        *reinterpret_cast<float4*>(mo + th * MR + 4 * tj) = make_float4(o.x * li, o.y * li, o.z * li, o.w * li);
+        if constexpr (VP)
+            *reinterpret_cast<float4*>(mo + kHeads * MR + th * MR + 4 * tj) =
+                make_float4(o2.x * li, o2.y * li, o2.z * li, o2.w * li);
     }
     __syncthreads();
-    for (int i = threadIdx.x; i < G * D; i += NT) {
-        const int h = i / D, col = i % D;
-        a.out[(head0 + h) * D + col] = (part[(0 * kHeads + h) * D + col] + part[(1 * kHeads + h) * D + col]) +
-                                       (part[(2 * kHeads + h) * D + col] + part[(3 * kHeads + h) * D + col]);
+    uint32_t A[kKB][4], A2[VP ? kKB : 1][4];
+    hilo_a(mo + g * MR, c, A);
+    if constexpr (VP) hilo_a(mo + kHeads * MR + g * MR, c, A2);
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+        const int job = warp + u * NW;
+        if (job >= kJobs) break;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        if constexpr (kEarly) {
+            hilo_mma(acc, A, bh[u], bl[u]);
+        } else {
+            uint4 ph[kKB / 2], pl[kKB / 2], sh[kKB / 2], sl[kKB / 2];
+            hilo_b(a.vPiT_hi, a.vPiT_lo, 8 * job, g, c, ph, pl);
+            hilo_b(a.vST_hi, a.vST_lo, 8 * job, g, c, sh, sl);
+            hilo_mma(acc, A, ph, pl);
+            hilo_mma(acc, A2, sh, sl);
+        }
+        if (g < G)
+            *reinterpret_cast<float2*>(a.out + (head0 + g) * D + 8 * job + 2 * c) =
+                make_float2(acc[0] + acc[2], acc[1] + acc[3]);
     }
 }
 
@@ -828,16 +915,21 @@ __global__ void __launch_bounds__((Warps<VP>::value + 1) * 32, 1) decode_split_m
     const size_t head0 = (size_t)b * a.Hq + (size_t)kvh * a.G + (size_t)hb * kHeads;
     const int64_t rowbase = ((int64_t)b * a.Hkv + kvh) * a.T_max;
 
-    // Π_v (and S_v) of the final merge: one L2 prefetch per 128-byte line, spread
+    // the bf16 hi/lo matrices every CTA reads (Π_k, S_k for the query rotation) or
+    // the merging CTAs read (Π_vᵀ, S_vᵀ): one L2 prefetch per 128-byte line, spread
     // over the CTAs of the grid, kept with the evict-last priority
     {
         const int nct = gridDim.x * gridDim.y * gridDim.z;
         const int cta = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
-        constexpr int kLines = D * D * 4 / 128;
+        constexpr int kLines = D * D * 2 / 128;  // lines of one bf16 matrix
+        constexpr int kMats = 4 + (KP ? 2 : 0) + (VP ? 2 : 0);
         const int l = cta + nct * (int)threadIdx.x;
-        if (l < (VP ? 2 : 1) * kLines) {
-            const float* p = l < kLines ? a.vPi + 32 * l : a.vS + 32 * (l - kLines);
-            asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(p));
+        if (l < kMats * kLines) {
+            int m = l / kLines;
+            if (!KP && m >= 4) m += 2;  // skip S_k
+            const uint16_t* base = m == 0 ? a.kPi_hi : m == 1 ? a.kPi_lo : m == 2 ? a.vPiT_hi : m == 3 ? a.vPiT_lo
+                                 : m == 4 ? a.kS_hi : m == 5 ? a.kS_lo : m == 6 ? a.vST_hi : a.vST_lo;
+            asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(base + 64 * (l % kLines)));
         }
     }
 
@@ -858,8 +950,6 @@ __global__ void __launch_bounds__((Warps<VP>::value + 1) * 32, 1) decode_split_m
     const uint32_t ring = smem_addr(mp + SM::kStage);
     __shared__ __align__(8) uint64_t s_full[SM::kStages], s_empty[SM::kStages];
     const bool producer = warp == W;
-    // the producer fills the first stages before the prologue, so that they land
-    // while the tables and queries are prepared
     // bulk staging when every slab's norm rows start on a 16-byte boundary:
     // one lane, one copy per plane and stage
     const bool bulk = (a.T_max & 3) == 0;
@@ -876,115 +966,18 @@ __global__ void __launch_bounds__((Warps<VP>::value + 1) * 32, 1) decode_split_m
             asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
         }
     };
-    if (producer) {
-        if (lane == 0) {
-            for (int i = 0; i < SM::kStages; ++i) {
-                sm100::mbar_init(&s_full[i], bulk ? 1 : 32);
-                sm100::mbar_init(&s_empty[i], kStageRows / kTile);
-            }
-            sm100::fence_barrier_init();
+    // the stage barriers exist before anyone waits on them; from here on the
+    // producer streams stages and the consumers prepare tables and queries
+    // without waiting for it (their barriers are named barrier 1, W warps)
+    if (producer && lane == 0) {
+        for (int i = 0; i < SM::kStages; ++i) {
+            sm100::mbar_init(&s_full[i], bulk ? 1 : 32);
+            sm100::mbar_init(&s_empty[i], kStageRows / kTile);
         }
-        __syncwarp();
-        for (int i = 0; i < min(nstages, SM::kStages); ++i) produce(i);
-    }
-
-    // ---- prologue: decode tables, queries, query scales
-    // raw queries of this head block: loads issued before the table fill, stored after
-    constexpr int NT = SM::kThreads, kQPer = (kHeads * D + NT - 1) / NT;
-    float qv[kQPer];
-#pragma unroll
-    for (int r = 0; r < kQPer; ++r) {
-        const int i = threadIdx.x + r * NT, h = i / D;
-        const size_t gi = (head0 + h) * D + (i % D);
-        qv[r] = (i < kHeads * D && h < G) ? (a.q_f32 ? __ldg(static_cast<const float*>(a.q) + gi)
-                                                     : __bfloat162float(static_cast<const __nv_bfloat16*>(a.q)[gi]))
-                                          : 0.f;
-    }
-    Table<KB>::fill(mp + SM::kTabK, a.kcb);
-    Table<VB>::fill(mp + SM::kTabV, a.vcb);
-    if constexpr (KP) KSignTable::fill(mp + SM::kTabS);
-    float* qin = reinterpret_cast<float*>(mp + SM::kQin);  // [kHeads][D]
-#pragma unroll
-    for (int r = 0; r < kQPer; ++r)
-        if (threadIdx.x + r * NT < kHeads * D) qin[threadIdx.x + r * NT] = qv[r];
-    __syncthreads();
-    // q′ = Π_k·q and q″ = S_k·q on the tensor cores: D[16 × 8 dims] = A·B with
-    // A = [bf16 hi of the 8 heads' q; bf16 lo] and B = a bf16 half of the matrix,
-    // so q_hi·M + q_lo·M is the sum of rows g and g + 8; hi and lo halves of M
-    // accumulate in the same tile (fp32-level accuracy).  The contraction order
-    // is permuted so that in k16 blocks 2p and 2p + 1 lane (g, c) holds the eight
-    // consecutive input dims 32p + 8c … 32p + 8c + 7: its matrix operand is one
-    // 16-byte load of row j0 + g.  Each warp takes its 8-dim tiles with all of
-    // their loads in flight at once.
-    {
-        uint32_t A[kKB][4];
-#pragma unroll
-        for (int ks = 0; ks < kKB; ++ks) {
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const int d0 = 32 * (ks >> 1) + 8 * c + 4 * (ks & 1) + 2 * hh;
-                const float2 x = *reinterpret_cast<const float2*>(qin + g * D + d0);
-                const __nv_bfloat162 hi = __floats2bfloat162_rn(x.x, x.y);
-                const float2 hf = __bfloat1622float2(hi);
-                A[ks][2 * hh] = *reinterpret_cast<const uint32_t*>(&hi);
-                A[ks][2 * hh + 1] = pack_bf2(x.x - hf.x, x.y - hf.y);
-            }
-        }
-        constexpr int kJobs = (KP ? 2 : 1) * (D / 8), kAll = W + 1;
-        constexpr int kPer = (kJobs + kAll - 1) / kAll;  // tiles per warp
-        uint4 bh[kPer][kKB / 2], bl[kPer][kKB / 2];  // bf16 dims 32p + 8c … + 7 of row j0 + g
-#pragma unroll
-        for (int u = 0; u < kPer; ++u) {
-            const int job = warp + u * kAll;
-            if (job < kJobs) {
-                const int second = job >= D / 8, j0 = 8 * (job % (D / 8));
-                const uint4* Mh = reinterpret_cast<const uint4*>(second ? a.kS_hi : a.kPi_hi);
-                const uint4* Ml = reinterpret_cast<const uint4*>(second ? a.kS_lo : a.kPi_lo);
-                const int row = ((j0 + g) * D + 8 * c) >> 3;  // 16-byte index of (j0 + g, 8c)
-#pragma unroll
-                for (int p2 = 0; p2 < kKB / 2; ++p2) {
-                    bh[u][p2] = __ldg(Mh + row + 4 * p2);
-                    bl[u][p2] = __ldg(Ml + row + 4 * p2);
-                }
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < kPer; ++u) {
-            const int job = warp + u * kAll;
-            if (job < kJobs) {
-                const int second = job >= D / 8, j0 = 8 * (job % (D / 8));
-                float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int ks = 0; ks < kKB; ++ks) {
-                    const uint4 h = bh[u][ks >> 1], l = bl[u][ks >> 1];
-                    mma16816_bf16(acc, A[ks], (ks & 1) ? h.z : h.x, (ks & 1) ? h.w : h.y);
-                    mma16816_bf16(acc, A[ks], (ks & 1) ? l.z : l.x, (ks & 1) ? l.w : l.y);
-                }
-                float* o = qsh + (second ? kHeads * kQRow : 0) + qidx(g, j0 + 2 * c);
-                o[0] = acc[0] + acc[2];
-                o[1] = acc[1] + acc[3];
-            }
-        }
+        sm100::fence_barrier_init();
     }
     __syncthreads();
-    if (warp < kHeads) {
-        // warp w finds max|q′| (and max|q″|) of head w
-        float m1 = 0.f, m2 = 0.f;
-        for (int j = lane; j < D; j += 32) {
-            m1 = fmaxf(m1, fabsf(qsh[qidx(warp, j)]));
-            if constexpr (KP) m2 = fmaxf(m2, fabsf(qsh[kHeads * kQRow + qidx(warp, j)]));
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
-            m2 = fmaxf(m2, __shfl_xor_sync(0xffffffffu, m2, o));
-        }
-        if (lane == 0) {
-            qsc[warp] = m1 > 0.f ? m1 : 1.f;
-            qsc[kHeads + warp] = m2 > 0.f ? m2 : 1.f;
-        }
-    }
-    __syncthreads();
+    auto consumers_sync = [] { asm volatile("bar.sync 1, %0;" ::"n"(W * 32) : "memory"); };
 
     Acc<VP> st;
 #pragma unroll
@@ -999,7 +992,9 @@ __global__ void __launch_bounds__((Warps<VP>::value + 1) * 32, 1) decode_split_m
     st.l = 0.f;
 
     if (producer) {
-        // ---- producer: refill each stage once its four tiles have been consumed
+        // ---- producer: the first stages, then each stage again once its four
+        // tiles have been consumed
+        for (int i = 0; i < min(nstages, SM::kStages); ++i) produce(i);
         for (int i = SM::kStages; i < nstages; ++i) {
             const bool ok = sm100::mbar_wait(&s_empty[i % SM::kStages], (uint32_t)((i / SM::kStages - 1) & 1), a.status,
                                              kDecodeStageTimeout);
@@ -1008,6 +1003,80 @@ __global__ void __launch_bounds__((Warps<VP>::value + 1) * 32, 1) decode_split_m
         }
         cp_async_wait<0>();  // every copy this warp issued has landed
     } else {
+        // ---- prologue (consumer warps): decode tables, queries, query scales
+        constexpr int NC = W * 32;
+        // q′ = Π_k·q and q″ = S_k·q on the tensor cores (hilo_*): warp w takes the
+        // 8-dim tiles w, w + W, … of the two products; the matrix loads and the raw
+        // query loads are issued before the table fill so that their latency
+        // overlaps it
+        constexpr int kJobs = (KP ? 2 : 1) * (D / 8);
+        constexpr int kPer = (kJobs + W - 1) / W;
+        uint4 bh[kPer][kKB / 2], bl[kPer][kKB / 2];
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+            const int job = warp + u * W;
+            if (job < kJobs) {
+                const bool second = job >= D / 8;
+                hilo_b(second ? a.kS_hi : a.kPi_hi, second ? a.kS_lo : a.kPi_lo, 8 * (job % (D / 8)), g, c, bh[u],
+                       bl[u]);
+            }
+        }
+        // the raw queries of this head block (rows as stored, bf16 or fp32; heads
+        // past G zero) copied into shared memory while the tables are filled
+        unsigned char* qin = mp + SM::kQin;  // [kHeads][D] elements of the query dtype
+        {
+            const int rowq = a.q_f32 ? D / 4 : D / 8;  // 16-byte pieces per head row
+            const unsigned char* qb = static_cast<const unsigned char*>(a.q) + head0 * D * (a.q_f32 ? 4 : 2);
+            for (int idx = threadIdx.x; idx < kHeads * rowq; idx += NC) {
+                const bool live = idx / rowq < G;
+                cp_async16(smem_addr(qin) + 16u * (uint32_t)idx, live ? qb + 16 * idx : qb, live ? 16u : 0u);
+            }
+            cp_async_commit();
+        }
+        Table<KB>::fill(mp + SM::kTabK, a.kcb, threadIdx.x, NC);
+        Table<VB>::fill(mp + SM::kTabV, a.vcb, threadIdx.x, NC);
+        if constexpr (KP) KSignTable::fill(mp + SM::kTabS, threadIdx.x, NC);
+        cp_async_wait<0>();
+        consumers_sync();
+        {
+            uint32_t A[kKB][4];
+            if (a.q_f32)
+                hilo_a(reinterpret_cast<const float*>(qin) + g * D, c, A);
+            else
+                hilo_a(reinterpret_cast<const __nv_bfloat16*>(qin) + g * D, c, A);
+#pragma unroll
+            for (int u = 0; u < kPer; ++u) {
+                const int job = warp + u * W;
+                if (job < kJobs) {
+                    const int second = job >= D / 8, j0 = 8 * (job % (D / 8));
+                    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                    hilo_mma(acc, A, bh[u], bl[u]);
+                    float* o = qsh + (second ? kHeads * kQRow : 0) + qidx(g, j0 + 2 * c);
+                    o[0] = acc[0] + acc[2];
+                    o[1] = acc[1] + acc[3];
+                }
+            }
+        }
+        consumers_sync();
+        for (int h = warp; h < kHeads; h += W) {  // W may be below kHeads (prod values)
+            // max|q′| (and max|q″|) of head h
+            float m1 = 0.f, m2 = 0.f;
+            for (int j = lane; j < D; j += 32) {
+                m1 = fmaxf(m1, fabsf(qsh[qidx(h, j)]));
+                if constexpr (KP) m2 = fmaxf(m2, fabsf(qsh[kHeads * kQRow + qidx(h, j)]));
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
+                m2 = fmaxf(m2, __shfl_xor_sync(0xffffffffu, m2, o));
+            }
+            if (lane == 0) {
+                qsc[h] = m1 > 0.f ? m1 : 1.f;
+                qsc[kHeads + h] = m2 > 0.f ? m2 : 1.f;
+            }
+        }
+        consumers_sync();
+
         // A fragments of head g: [Q′_hi; Q′_lo] for the codes and [Q″_hi; Q″_lo] for
         // the QJL signs, k order following the key decoders' dims
         uint32_t AQ[kKB][4], AS[kKB][4];
@@ -1147,16 +1216,18 @@ __global__ void __launch_bounds__((Warps<VP>::value + 1) * 32, 1) decode_split_m
         if constexpr (VP) a.pacc2[ps * D + sign_dim(fg >> 1, tau, fg & 1)] = o2;
     }
 
-    // ---- the last CTA of this group to finish merges all of its splits
-    __threadfence();
+    // ---- the last CTA of this group to finish merges all of its splits: the
+    // barrier orders every thread's partial stores before thread 0's ticket, whose
+    // acquire-release add publishes them and, in the last CTA, acquires the others'
     __syncthreads();
     if (threadIdx.x == 0) {
         const int group = (b * a.Hkv + kvh) * a.n_hblocks + hb;
-        s_last = atomicAdd(a.cnt + group, 1) == a.n_splits - 1;
+        int old;
+        asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(a.cnt + group) : "memory");
+        s_last = old == a.n_splits - 1;
     }
     __syncthreads();
     if (!s_last) return;
-    __threadfence();
     merge_group<KB, KP, VB, VP>(a, smem, head0, G);
 }
 

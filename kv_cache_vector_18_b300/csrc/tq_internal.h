@@ -49,6 +49,11 @@ struct DeviceParams {
     uint16_t* Pi_lo = nullptr;
     uint16_t* S_hi = nullptr;  // S = S_hi + S_lo, bf16 row-major [j][i] (prod)
     uint16_t* S_lo = nullptr;
+    // Πᵀ and Sᵀ split the same way, row-major [i][j] (the decode merge's x = Πᵀ·y)
+    uint16_t* PiT_hi = nullptr;
+    uint16_t* PiT_lo = nullptr;
+    uint16_t* ST_hi = nullptr;  // (prod)
+    uint16_t* ST_lo = nullptr;
     CUtensorMap tm_pi_hi;   // TMA maps over Pi_hi / Pi_lo, box {64, d}, 128-byte swizzle
     CUtensorMap tm_pi_lo;
     // Hadamard rotation: √d·Π = H·diag(σ) has entries ±1, exact in bf16, so the
