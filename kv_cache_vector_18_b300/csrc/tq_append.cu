@@ -110,6 +110,10 @@ append_rows_kernel(AppendSide k_side, AppendSide v_side, int32_t* __restrict__ l
     __shared__ float part[kAppendThreads<D>];
     __shared__ uint32_t words[D / 8];  // up to 4 bits per coordinate
     __shared__ int s_last;
+    // the decode launched after this kernel as its programmatic dependent may start
+    // its prologue now; it reads what this kernel writes only after
+    // griddepcontrol.wait, i.e. after this grid has completed
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int j = threadIdx.x;
     const int64_t r = blockIdx.x;
     if (j == 0) s = blockIdx.y == 0 ? k_side : v_side;

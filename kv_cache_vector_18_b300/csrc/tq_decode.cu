@@ -249,22 +249,22 @@ __global__ void decode_merge_kernel(const float* __restrict__ pm, const float* _
 // The tensor-core split kernel is written for d = 128 (the head dimension of
 // every workload this library is tuned for).
 
-int launch_split_mma_any(const SplitArgs& a, dim3 grid, int kb, bool kp, int vb, bool vp, cudaStream_t s) {
+int launch_split_mma_any(const SplitArgs& a, dim3 grid, int kb, bool kp, int vb, bool vp, bool pdl, cudaStream_t s) {
     using namespace mmadec;
     if (kp) {
         switch (kb) {
-            case 0: return launch_for_k<0, true>(a, grid, vb, vp, s);
-            case 1: return launch_for_k<1, true>(a, grid, vb, vp, s);
-            case 2: return launch_for_k<2, true>(a, grid, vb, vp, s);
-            case 3: return launch_for_k<3, true>(a, grid, vb, vp, s);
+            case 0: return launch_for_k<0, true>(a, grid, vb, vp, pdl, s);
+            case 1: return launch_for_k<1, true>(a, grid, vb, vp, pdl, s);
+            case 2: return launch_for_k<2, true>(a, grid, vb, vp, pdl, s);
+            case 3: return launch_for_k<3, true>(a, grid, vb, vp, pdl, s);
             default: break;
         }
     } else {
         switch (kb) {
-            case 1: return launch_for_k<1, false>(a, grid, vb, vp, s);
-            case 2: return launch_for_k<2, false>(a, grid, vb, vp, s);
-            case 3: return launch_for_k<3, false>(a, grid, vb, vp, s);
-            case 4: return launch_for_k<4, false>(a, grid, vb, vp, s);
+            case 1: return launch_for_k<1, false>(a, grid, vb, vp, pdl, s);
+            case 2: return launch_for_k<2, false>(a, grid, vb, vp, pdl, s);
+            case 3: return launch_for_k<3, false>(a, grid, vb, vp, pdl, s);
+            case 4: return launch_for_k<4, false>(a, grid, vb, vp, pdl, s);
             default: break;
         }
     }
@@ -307,8 +307,10 @@ int launch_d(const tq_ctx& hk, const tq_ctx& hv, const DecodeShape& p, const voi
             e = cudaMemsetAsync(cnt, 0, (size_t)p.B * p.Hq * sizeof(int), s);
             if (e != cudaSuccess) return cuda_fail(e, "clearing the split tickets");
         }
+        // after the decode-step append (which cleared the tickets) the kernel is its
+        // programmatic dependent: its prologue overlaps the append
         return launch_split_mma_any(a, dim3(p.n_splits, p.Hkv * a.n_hblocks, p.B), hk.hp.b_mse, kprod, hv.hp.b_mse,
-                                    vprod, s);
+                                    vprod, tickets_zeroed, s);
     }
 
     // CUDA-core path: query prep (which also clears the tickets), split, merge

@@ -65,7 +65,7 @@ constexpr int kDecodeMergeTimeout = 31;  // status code of an expired wait for t
 // resident split CTAs per SM of the tensor-core decode kernel (one 16- or 8-warp CTA)
 constexpr int ctas_per_sm(bool /*vprod*/) { return 1; }
 template <int KB, bool KP>
-int launch_for_k(const SplitArgs& a, dim3 grid, int vb, bool vp, cudaStream_t s);
+int launch_for_k(const SplitArgs& a, dim3 grid, int vb, bool vp, bool pdl, cudaStream_t s);
 }  // namespace mmadec
 
 }  // namespace tq

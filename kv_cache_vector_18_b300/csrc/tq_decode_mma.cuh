@@ -908,10 +908,20 @@ __global__ void __launch_bounds__((Warps<VP>::value + 1) * 32, 1) decode_split_m
     const int G = min(kHeads, a.G - hb * kHeads);
     const int split = blockIdx.x, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
-    int L = a.seq_lens[b];
-    L = L < 0 ? 0 : (L > a.T_max ? a.T_max : L);
     const int t0 = split * a.chunk;
-    const int t1 = min(t0 + a.chunk, L);
+    // Lengths, cache planes and merge tickets may come from the kernel launched
+    // just before this one (the decode-step append, launched as its programmatic
+    // dependent): each branch reads them only after griddepcontrol.wait, which
+    // returns at once for an ordinary launch.
+    int t1 = t0, ntiles = 0, nstages = 0;
+    auto read_length = [&]() {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        int L = a.seq_lens[b];
+        L = L < 0 ? 0 : (L > a.T_max ? a.T_max : L);
+        t1 = min(t0 + a.chunk, L);
+        ntiles = t1 > t0 ? (t1 - t0 + kTile - 1) / kTile : 0;
+        nstages = (ntiles + kStageRows / kTile - 1) / (kStageRows / kTile);
+    };
     const size_t head0 = (size_t)b * a.Hq + (size_t)kvh * a.G + (size_t)hb * kHeads;
     const int64_t rowbase = ((int64_t)b * a.Hkv + kvh) * a.T_max;
 
@@ -945,8 +955,6 @@ __global__ void __launch_bounds__((Warps<VP>::value + 1) * 32, 1) decode_split_m
     sl.vrn = a.vrnorm + rowbase;
 
     // ---- staging ring: warp W produces, warps 0 … W − 1 consume 16-token tiles
-    const int ntiles = t1 > t0 ? (t1 - t0 + kTile - 1) / kTile : 0;
-    const int nstages = (ntiles + kStageRows / kTile - 1) / (kStageRows / kTile);
     const uint32_t ring = smem_addr(mp + SM::kStage);
     __shared__ __align__(8) uint64_t s_full[SM::kStages], s_empty[SM::kStages];
     const bool producer = warp == W;
@@ -994,6 +1002,7 @@ __global__ void __launch_bounds__((Warps<VP>::value + 1) * 32, 1) decode_split_m
     if (producer) {
         // ---- producer: the first stages, then each stage again once its four
         // tiles have been consumed
+        read_length();
         for (int i = 0; i < min(nstages, SM::kStages); ++i) produce(i);
         for (int i = SM::kStages; i < nstages; ++i) {
             const bool ok = sm100::mbar_wait(&s_empty[i % SM::kStages], (uint32_t)((i / SM::kStages - 1) & 1), a.status,
@@ -1077,6 +1086,7 @@ __global__ void __launch_bounds__((Warps<VP>::value + 1) * 32, 1) decode_split_m
         }
         consumers_sync();
 
+        read_length();
         // A fragments of head g: [Q′_hi; Q′_lo] for the codes and [Q″_hi; Q″_lo] for
         // the QJL signs, k order following the key decoders' dims
         uint32_t AQ[kKB][4], AS[kKB][4];
@@ -1231,36 +1241,48 @@ __global__ void __launch_bounds__((Warps<VP>::value + 1) * 32, 1) decode_split_m
     merge_group<KB, KP, VB, VP>(a, smem, head0, G);
 }
 
+// pdl: launched as the programmatic dependent of the kernel before it in the
+// stream (which must then be the decode-step append, the only producer of the
+// inputs the kernel reads before griddepcontrol.wait being its caller's q)
 template <int KB, bool KP, int VB, bool VP>
-int launch_split_mma(const SplitArgs& a, dim3 grid, cudaStream_t s) {
+int launch_split_mma(const SplitArgs& a, dim3 grid, bool pdl, cudaStream_t s) {
     using SM = Smem<KB, KP, VB, VP>;
     static_assert(SM::kBytes <= 232448 - 1024, "decode shared memory above the per-CTA limit");
     auto fn = decode_split_mma_kernel<KB, KP, VB, VP>;
     static std::atomic<uint64_t> smem_set{0};
     const int rc = ensure_smem_attr(smem_set, (const void*)fn, (int)SM::kBytes, "decode (tensor-core) smem attribute");
     if (rc != TQ_OK) return rc;
-    fn<<<grid, SM::kThreads, SM::kBytes, s>>>(a);
-    const cudaError_t e = cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(SM::kThreads);
+    cfg.dynamicSmemBytes = SM::kBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, fn, a);
     return e == cudaSuccess ? TQ_OK : cuda_fail(e, "decode (tensor-core) split launch");
 }
 
 // Values dispatched at run time for one key configuration (see tq_decode_args.h).
 template <int KB, bool KP>
-int launch_for_k(const SplitArgs& a, dim3 grid, int vb, bool vp, cudaStream_t s) {
+int launch_for_k(const SplitArgs& a, dim3 grid, int vb, bool vp, bool pdl, cudaStream_t s) {
     if (vp) {
         switch (vb) {
-            case 0: return launch_split_mma<KB, KP, 0, true>(a, grid, s);
-            case 1: return launch_split_mma<KB, KP, 1, true>(a, grid, s);
-            case 2: return launch_split_mma<KB, KP, 2, true>(a, grid, s);
-            case 3: return launch_split_mma<KB, KP, 3, true>(a, grid, s);
+            case 0: return launch_split_mma<KB, KP, 0, true>(a, grid, pdl, s);
+            case 1: return launch_split_mma<KB, KP, 1, true>(a, grid, pdl, s);
+            case 2: return launch_split_mma<KB, KP, 2, true>(a, grid, pdl, s);
+            case 3: return launch_split_mma<KB, KP, 3, true>(a, grid, pdl, s);
             default: break;
         }
     } else {
         switch (vb) {
-            case 1: return launch_split_mma<KB, KP, 1, false>(a, grid, s);
-            case 2: return launch_split_mma<KB, KP, 2, false>(a, grid, s);
-            case 3: return launch_split_mma<KB, KP, 3, false>(a, grid, s);
-            case 4: return launch_split_mma<KB, KP, 4, false>(a, grid, s);
+            case 1: return launch_split_mma<KB, KP, 1, false>(a, grid, pdl, s);
+            case 2: return launch_split_mma<KB, KP, 2, false>(a, grid, pdl, s);
+            case 3: return launch_split_mma<KB, KP, 3, false>(a, grid, pdl, s);
+            case 4: return launch_split_mma<KB, KP, 4, false>(a, grid, pdl, s);
             default: break;
         }
     }

@@ -4,6 +4,6 @@
 
 namespace tq {
 namespace mmadec {
-template int launch_for_k<2, false>(const SplitArgs&, dim3, int, bool, cudaStream_t);
+template int launch_for_k<2, false>(const SplitArgs&, dim3, int, bool, bool, cudaStream_t);
 }  // namespace mmadec
 }  // namespace tq
