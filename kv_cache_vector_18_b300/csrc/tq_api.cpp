@@ -591,7 +591,8 @@ int mixed_shape(tq_handle hko, tq_handle hkn, tq_handle hvo, tq_handle hvn, int 
     const int d = hko->hp.d + hkn->hp.d;
     if (hvo->hp.d + hvn->hp.d != d) return fail(TQ_EINVAL, "key d=%d and value d=%d differ", d,
                                                 hvo->hp.d + hvn->hp.d);
-    return mixed_plan(d, hko->num_sms, hvo->hp.variant == TQ_PROD, B, Hq, Hkv, T_max, plan, bytes);
+    const bool tc = mixed_decode_tc_supported(*hko, *hkn, *hvo, *hvn, T_max);
+    return mixed_plan(d, hko->num_sms, hvo->hp.variant == TQ_PROD, tc, B, Hq, Hkv, T_max, plan, bytes);
 }
 }  // namespace
 

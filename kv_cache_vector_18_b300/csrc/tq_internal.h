@@ -139,6 +139,7 @@ int launch_mixed_quantize_tc(const tq_ctx& ho, const tq_ctx& hn, const int32_t* 
                              cudaStream_t s);
 struct MixedShape {
     int B = 0, Hq = 0, Hkv = 0, T_max = 0, d = 0, G = 0, n_splits = 1, chunk = 64;
+    bool tc = false;  // the tensor-core mixed decode (tq_decode_mixed_mma.cu) runs it
 };
 struct MixedDecode {
     const tq_ctx* hk[2];  // key parts: outlier channels, the rest
@@ -154,7 +155,12 @@ struct MixedDecode {
     float* scores;
     void* workspace;
 };
-int mixed_plan(int d, int sms, bool vprod, int B, int Hq, int Hkv, int T_max, MixedShape* plan, size_t* ws_bytes);
+int mixed_plan(int d, int sms, bool vprod, bool tc, int B, int Hq, int Hkv, int T_max, MixedShape* plan,
+               size_t* ws_bytes);
+// Whether the tensor-core mixed decode serves these handles and T_max: d = 128,
+// outlier parts of 32 channels, mse parts, instantiated bit pairs, T_max % 4 == 0.
+bool mixed_decode_tc_supported(const tq_ctx& hko, const tq_ctx& hkn, const tq_ctx& hvo, const tq_ctx& hvn,
+                               int T_max);
 int launch_mixed_decode(const MixedDecode& m, const MixedShape& p, cudaStream_t s);
 int launch_select_outlier_channels(const void* x, int x_dtype, int64_t n_rows, int64_t stride, int d, int d_o,
                                    double* energy, int32_t* perm, cudaStream_t s);

@@ -13,6 +13,8 @@
 #include <math.h>
 
 #include "tq_common.cuh"
+#include "tq_decode_args.h"
+#include "tq_mixed_decode.h"
 
 namespace tq {
 namespace {
@@ -390,17 +392,20 @@ __global__ void mixed_merge_kernel(const float* __restrict__ pm, const float* __
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct MixedLayout {
-    size_t qr, qs, pm, pl, pacc, pacc2, total;
+    size_t qr, qs, pm, pl, pacc, pacc2, cnt, total;
 };
 
-MixedLayout mixed_layout(int B, int Hq, int d, int n_splits, bool vprod) {
+// The CUDA-core path keeps rotated queries (qr, qs) and separate merge
+// partials for prod values; the tensor-core path needs split maxima, sums,
+// value sums and one merge ticket per head (cnt).
+MixedLayout mixed_layout(int B, int Hq, int d, int n_splits, bool vprod, bool tc = false) {
     MixedLayout w;
     const size_t heads = (size_t)B * Hq;
     size_t off = 0;
     w.qr = off;
-    off = align256(off + heads * d * 4);
+    if (!tc) off = align256(off + heads * d * 4);
     w.qs = off;
-    off = align256(off + heads * d * 4);
+    if (!tc) off = align256(off + heads * d * 4);
     w.pm = off;
     off = align256(off + heads * n_splits * 4);
     w.pl = off;
@@ -409,8 +414,48 @@ MixedLayout mixed_layout(int B, int Hq, int d, int n_splits, bool vprod) {
     off = align256(off + heads * n_splits * d * 4);
     w.pacc2 = off;
     if (vprod) off = align256(off + heads * n_splits * d * 4);
+    w.cnt = off;
+    if (tc) off = align256(off + heads * 4);
     w.total = off > 0 ? off : 256;
     return w;
+}
+
+int launch_mixed_tc_path(const MixedDecode& m, const MixedShape& p, cudaStream_t s) {
+    const MixedLayout w = mixed_layout(p.B, p.Hq, p.d, p.n_splits, false, true);
+    char* ws = static_cast<char*>(m.workspace);
+    MixedTcArgs a;
+    for (int i = 0; i < 2; ++i) {
+        a.kc[i] = m.kc[i].codes;
+        a.kn[i] = m.kc[i].norm;
+        a.vc[i] = m.vc[i].codes;
+        a.vn[i] = m.vc[i].norm;
+        a.kcb[i] = m.hk[i]->cb;
+        a.vcb[i] = m.hv[i]->cb;
+        a.kPi_hi[i] = m.hk[i]->dp.Pi_hi;
+        a.kPi_lo[i] = m.hk[i]->dp.Pi_lo;
+        a.vPiT_hi[i] = m.hv[i]->dp.PiT_hi;
+        a.vPiT_lo[i] = m.hv[i]->dp.PiT_lo;
+    }
+    a.seq_lens = m.seq_lens;
+    a.perm_k = m.perm_k;
+    a.perm_v = m.perm_v;
+    a.pm = reinterpret_cast<float*>(ws + w.pm);
+    a.pl = reinterpret_cast<float*>(ws + w.pl);
+    a.pacc = reinterpret_cast<float*>(ws + w.pacc);
+    a.cnt = reinterpret_cast<int*>(ws + w.cnt);
+    a.out = m.out;
+    a.scores = m.scores;
+    a.scale = m.scale;
+    a.B = p.B; a.Hq = p.Hq; a.Hkv = p.Hkv; a.T_max = p.T_max; a.G = p.G;
+    a.n_splits = p.n_splits; a.chunk = p.chunk;
+    a.n_hblocks = (p.G + mmadec::kHeadsPerCta - 1) / mmadec::kHeadsPerCta;
+    a.q = m.q;
+    a.q_f32 = m.q_dtype == TQ_F32;
+    a.status = m.hk[0]->dp.status;
+    cudaError_t e = cudaMemsetAsync(a.cnt, 0, (size_t)p.B * p.Hq * sizeof(int), s);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the mixed merge tickets");
+    return launch_mixed_decode_tc(a, dim3(p.n_splits, p.Hkv * a.n_hblocks, p.B), m.hk[0]->hp.b_mse,
+                                  m.hk[1]->hp.b_mse, s);
 }
 
 void fill_part(Part* p, const tq_ctx& h, const tq_planes& pl) {
@@ -495,33 +540,55 @@ int launch_mixed_d(const MixedDecode& m, const MixedShape& p, cudaStream_t s) {
 
 }  // namespace
 
-int mixed_plan(int d, int sms, bool vprod, int B, int Hq, int Hkv, int T_max, MixedShape* plan, size_t* ws_bytes) {
+bool mixed_decode_tc_supported(const tq_ctx& hko, const tq_ctx& hkn, const tq_ctx& hvo, const tq_ctx& hvn,
+                               int T_max) {
+    const tq_ctx* hs[4] = {&hko, &hkn, &hvo, &hvn};
+    for (const tq_ctx* h : hs)
+        if (h->hp.variant != TQ_MSE || h->dp.Pi_hi == nullptr || h->dp.PiT_hi == nullptr) return false;
+    return hko.hp.d == 32 && hkn.hp.d == 96 && hvo.hp.d == 32 && hvn.hp.d == 96 && T_max % 4 == 0 &&
+           hko.num_sms > 0 && mixed_tc_bits_supported(hko.hp.b_mse, hkn.hp.b_mse, hvo.hp.b_mse, hvn.hp.b_mse);
+}
+
+int mixed_plan(int d, int sms, bool vprod, bool tc, int B, int Hq, int Hkv, int T_max, MixedShape* plan,
+               size_t* ws_bytes) {
     if (B < 0 || Hq < 0 || Hkv <= 0 || T_max < 0) return fail(TQ_EINVAL, "negative or zero shape");
     if (Hq % Hkv != 0) return fail(TQ_EINVAL, "Hq=%d is not a multiple of Hkv=%d", Hq, Hkv);
     if (Hq > 4096) return fail(TQ_EUNSUPPORTED, "Hq=%d > 4096", Hq);
     if ((int64_t)B * Hkv * T_max > (int64_t)1 << 40) return fail(TQ_EINVAL, "cache too large");
     MixedShape p;
     p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.T_max = T_max; p.d = d; p.G = Hq / Hkv;
-    const int hb = heads_per_cta(d);
+    p.tc = tc;
+    const int hb = tc ? mmadec::kHeadsPerCta : heads_per_cta(d);
     const int64_t units = (int64_t)(B > 0 ? B : 1) * Hkv * ((p.G + hb - 1) / hb);
-    // two waves of two resident 4-warp CTAs per SM
-    int64_t want = (4 * (int64_t)(sms > 0 ? sms : 148) + units - 1) / units;
+    const int64_t nsm = sms > 0 ? sms : 148;
+    // CUDA-core path: two waves of two resident 4-warp CTAs per SM; tensor-core
+    // path: one CTA per SM in one wave, at most kMaxChunk tokens per CTA and no
+    // more splits than the last CTA of a group merges
+    int64_t want = tc ? nsm / units : (4 * nsm + units - 1) / units;
     int64_t max_splits = (T_max + kMinChunk - 1) / kMinChunk;
     if (max_splits < 1) max_splits = 1;
+    if (tc && want > mmadec::kMaxSplitsMerged) want = mmadec::kMaxSplitsMerged;
     if (want > max_splits) want = max_splits;
     if (want < 1) want = 1;
     int64_t chunk = (T_max + want - 1) / want;
     chunk = (chunk + kMinChunk - 1) / kMinChunk * kMinChunk;
     if (chunk < kMinChunk) chunk = kMinChunk;
+    constexpr int64_t kMaxChunkTc = 8192;
+    if (tc && chunk > kMaxChunkTc) {
+        const int64_t floor_chunk =
+            ((T_max + mmadec::kMaxSplitsMerged - 1) / mmadec::kMaxSplitsMerged + kMinChunk - 1) / kMinChunk * kMinChunk;
+        chunk = kMaxChunkTc > floor_chunk ? kMaxChunkTc : floor_chunk;
+    }
     p.chunk = (int)chunk;
     p.n_splits = (int)((T_max + chunk - 1) / chunk);
     if (p.n_splits < 1) p.n_splits = 1;
     *plan = p;
-    *ws_bytes = mixed_layout(B, Hq, d, p.n_splits, vprod).total;
+    *ws_bytes = mixed_layout(B, Hq, d, p.n_splits, vprod, tc).total;
     return TQ_OK;
 }
 
 int launch_mixed_decode(const MixedDecode& m, const MixedShape& p, cudaStream_t s) {
+    if (p.tc) return launch_mixed_tc_path(m, p, s);
     switch (p.d) {
         case 64: return launch_mixed_d<64>(m, p, s);
         case 96: return launch_mixed_d<96>(m, p, s);

@@ -195,3 +195,65 @@ def test_mixed_rejects_bad_arguments(tq):
     assert L.tq_select_outlier_channels(x.data_ptr(), 0, 8, 128, 128, 100, e.data_ptr(), perm.data_ptr(),
                                         None) == _lib.TQ_EINVAL
     torch.cuda.synchronize()
+
+
+def _mixed_case(tq, B, Hq, Hkv, T, bo, bn, seed, q_dtype="bf16"):
+    d = 128
+    rng = np.random.default_rng(seed)
+    hot_k = rng.choice(d, 32, replace=False)
+    hot_v = rng.choice(d, 32, replace=False)
+    K = _hot_rows(B * Hkv * T, d, hot_k, seed=seed + 1)
+    V = _hot_rows(B * Hkv * T, d, hot_v, seed=seed + 2)
+    q = synthetic.gaussian((B, Hq, d), seed=seed + 3, dtype=q_dtype)
+    pk, _ = tq.select_outlier_channels(K.cuda(), 32)
+    pv, _ = tq.select_outlier_channels(V.cuda(), 32)
+    mk = tq.MixedQuantizer(pk, 32, bo, bn, "mse", seed_o=seed + 21, seed_n=seed + 22)
+    mv = tq.MixedQuantizer(pv, 32, bo, bn, "mse", seed_o=seed + 23, seed_n=seed + 24)
+    kc, vc = mk.quantize(K.cuda()), mv.quantize(V.cuda())
+    return mk, mv, q, kc, vc
+
+
+def _mixed_ref(mk, mv, q, kc, vc, lens, Hkv, T):
+    a, b = _mixed_params(mk), _mixed_params(mv)
+    return O.mixed_decode_attention(
+        a, b, f64(q), planes_to_oracle_rows(a.po, kc["o"]), planes_to_oracle_rows(a.pn, kc["n"]),
+        planes_to_oracle_rows(b.po, vc["o"]), planes_to_oracle_rows(b.pn, vc["n"]), lens, Hkv, T)
+
+
+@pytest.mark.parametrize("bo,bn,B,Hq,Hkv,T,lens,q_dtype", [
+    (3, 2, 3, 16, 2, 1028, [1028, 17, 1], "bf16"),      # the page's split; two head blocks; ragged tails
+    (3, 2, 2, 8, 1, 700, [0, 699], "f32"),               # an empty sequence, an fp32 query
+    (4, 3, 2, 12, 3, 512, [512, 300], "bf16"),           # G = 4: a partial head block
+    (4, 2, 1, 8, 1, 8192, [8191], "bf16"),               # 128 splits: several merge rounds
+])
+def test_mixed_decode_tensor_core_path(tq, bo, bn, B, Hq, Hkv, T, lens, q_dtype):
+    # T_max % 4 == 0, 32 outlier channels, mse parts: the tensor-core mixed decode
+    mk, mv, q, kc, vc = _mixed_case(tq, B, Hq, Hkv, T, bo, bn, seed=bo * 10 + bn + T, q_dtype=q_dtype)
+    sl = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    out, sc = tq.mixed_decode_attention(mk, mv, q.cuda(), kc, vc, sl, Hkv, T, return_scores=True)
+    torch.cuda.synchronize()
+    assert mk.qo.device_status() == 0
+    ref, ref_sc = _mixed_ref(mk, mv, q, kc, vc, lens, Hkv, T)
+    check_attention(f64(out), ref)
+    g = f64(sc)
+    mask = ~np.isnan(ref_sc)
+    assert np.array_equal(np.isnan(g), ~mask)
+    assert np.max(np.abs(g[mask] - ref_sc[mask])) <= 1e-3 * max(1.0, np.max(np.abs(ref_sc[mask])))
+    if 0 in lens:
+        assert np.all(f64(out)[lens.index(0)] == 0)
+
+
+def test_mixed_decode_tensor_core_bad_channel_flagged(tq):
+    # a permutation entry outside [0, d) in the decode's key or value map is read
+    # as channel 0 and recorded in the outlier key handle's status word
+    from kv_cache_vector_18_b300 import _lib
+    mk, mv, q, kc, vc = _mixed_case(tq, 1, 8, 1, 256, 3, 2, seed=5)
+    sl = torch.tensor([256], dtype=torch.int32, device="cuda")
+    pk_bad = mk.perm.clone()
+    pk_bad[77] = -3
+    mk.perm = pk_bad
+    out = tq.mixed_decode_attention(mk, mv, q.cuda(), kc, vc, sl, 1, 256)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out).all()
+    assert mk.qo.device_status(clear=True) == _lib.TQ_STATUS_BAD_CHANNEL
+    assert mk.qo.device_status() == 0
