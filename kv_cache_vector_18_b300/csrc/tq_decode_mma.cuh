@@ -35,12 +35,14 @@
 // amplified by the softmax — nearly vanishes.
 //
 // Data movement: one producer warp streams the chunk's packed planes into a
-// ring of shared-memory stages of 64 tokens with cp.async, each stage
-// completing on a "full" mbarrier; the consumer warps take 16-token tiles of
-// the stages round-robin, read their operands with short shared-memory loads
-// and release each stage on an "empty" mbarrier (every wait is bounded).  The
-// last CTA of each (batch, KV head, head block) to finish merges every split's
-// partial and applies Π_vᵀ (no merge launch).
+// ring of shared-memory stages of 64 tokens (one bulk copy per plane and stage,
+// or per-lane cp.async when the slab's norm rows are not 16-byte aligned), each
+// stage completing on a "full" mbarrier; the consumer warps prepare tables and
+// queries meanwhile (synchronising among themselves only), then take 16-token
+// tiles of the stages round-robin, read their operands with short shared-memory
+// loads and release each stage on an "empty" mbarrier (every wait is bounded).
+// The last CTA of each (batch, KV head, head block) to finish merges every
+// split's partial and applies Π_vᵀ on the tensor cores (no merge launch).
 #pragma once
 
 #include <math.h>
