@@ -34,8 +34,17 @@ def _ptr(t: torch.Tensor | None) -> int | None:
     return None if t is None else t.data_ptr()
 
 
+try:  # the raw current-stream handle without building a torch.cuda.Stream object
+    _raw_stream = torch._C._cuda_getCurrentRawStream
+    _cur_device = torch._C._cuda_getDevice
+except AttributeError:  # pragma: no cover - older torch
+    _raw_stream = None
+
+
 def _stream(stream) -> int | None:
     if stream is None:
+        if _raw_stream is not None:
+            return _raw_stream(_cur_device())
         stream = torch.cuda.current_stream()
     return stream.cuda_stream
 

@@ -5,6 +5,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <mutex>
 #include <new>
 
 #include <cuda_fp16.h>
@@ -28,12 +29,54 @@ int cuda_fail(cudaError_t e, const char* what) {
     return fail(TQ_ECUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
 }
 
+namespace {
+
+// Device allocations this thread has already validated: [base, end) on a device.
+// A pointer inside one of them needs no attribute query (the query costs about
+// a microsecond, and a call validates up to a dozen pointers).  Ranges come from
+// the driver's allocation lookup; only plain device memory is remembered.
+struct DevRange {
+    uintptr_t base = 0, end = 0;
+    int dev = -1;
+};
+constexpr int kRangeCache = 16;
+thread_local DevRange g_ranges[kRangeCache];
+thread_local int g_range_next = 0;
+
+bool allocation_range(const void* p, uintptr_t* base, uintptr_t* end) {
+    static PFN_cuMemGetAddressRange_v3020 get_range = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuMemGetAddressRange", &fn, 3020, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_range = reinterpret_cast<PFN_cuMemGetAddressRange_v3020>(fn);
+        cudaGetLastError();
+    });
+    if (get_range == nullptr) return false;
+    CUdeviceptr b = 0;
+    size_t n = 0;
+    if (get_range(&b, &n, (CUdeviceptr)(uintptr_t)p) != CUDA_SUCCESS || n == 0) return false;
+    *base = (uintptr_t)b;
+    *end = (uintptr_t)b + n;
+    return true;
+}
+
+}  // namespace
+
 int check_device_ptr(const void* p, const char* name, bool required) {
     if (p == nullptr) {
         if (required) return fail(TQ_EINVAL, "%s is NULL", name);
         return TQ_OK;
     }
     if (((uintptr_t)p & 15u) != 0) return fail(TQ_EALIGN, "%s is not 16-byte aligned", name);
+    int dev = -1;
+    cudaGetDevice(&dev);
+    const uintptr_t a = (uintptr_t)p;
+    for (const DevRange& r : g_ranges)
+        if (r.dev == dev && a >= r.base && a < r.end) return TQ_OK;
     cudaPointerAttributes attr;
     cudaError_t e = cudaPointerGetAttributes(&attr, p);
     if (e != cudaSuccess) {
@@ -42,9 +85,12 @@ int check_device_ptr(const void* p, const char* name, bool required) {
     }
     if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged)
         return fail(TQ_EINVAL, "%s is not device memory", name);
-    int dev = -1;
-    cudaGetDevice(&dev);
     if (attr.device != dev) return fail(TQ_EINVAL, "%s lives on device %d, current is %d", name, attr.device, dev);
+    uintptr_t b = 0, end = 0;
+    if (attr.type == cudaMemoryTypeDevice && allocation_range(p, &b, &end)) {
+        g_ranges[g_range_next] = DevRange{b, end, dev};
+        g_range_next = (g_range_next + 1) % kRangeCache;
+    }
     return TQ_OK;
 }
 
