@@ -640,6 +640,8 @@ def run_ours(args, spec):
                                         qsrc, tm["n_rows"])
         rl["quantize_k"]["tensor"] = tensor_info(spec["k_bits"], spec["k_variant"], tm["n_rows"], col["quantize_k"])
         rl["quantize_v"]["tensor"] = tensor_info(spec["v_bits"], spec["v_variant"], tm["n_rows"], col["quantize_v"])
+    for k in rl:  # the binding roofline of each quantize call (HBM or executed tensor flops)
+        rl[k]["binding"] = "tensor" if rl[k]["tensor"].get("frac_executed_sustained", 0) > rl[k]["frac"] else "hbm"
     rl["decode"] = hbm_roofline("tq_decode_attention", dc, tm["decode"],
                                 f"decode_{spec['k_variant']}_b{spec['k_bits']}_{spec['v_variant']}_b{spec['v_bits']}_d{d}",
                                 dsrc, tm["ctx_rows"])
