@@ -625,11 +625,13 @@ __device__ __forceinline__ void step(Acc<VP>& st, const unsigned char* stp, int 
     using ST = Stage<KB, KP, VB, VP>;
     // ---- scores of head g: S1 = [Q′_hi; Q′_lo]·K̃ᵀ (codes), S2 = [Q″_hi; Q″_lo]·Zᵀ (QJL signs)
     // accumulator of group n: [0] (hi, token 2c) [1] (hi, 2c + 1) [2] (lo, 2c) [3] (lo, 2c + 1)
-    float S1[2][4], S2[2][4];
+    // Each score sums its k16 blocks in two independent accumulator chains (even
+    // and odd blocks), so that an MMA need not wait for the one before it.
+    float S1[2][4], S2[2][4], S1x[2][4], S2x[2][4];
 #pragma unroll
     for (int n = 0; n < 2; ++n) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) S1[n][i] = S2[n][i] = 0.f;
+        for (int i = 0; i < 4; ++i) S1[n][i] = S2[n][i] = S1x[n][i] = S2x[n][i] = 0.f;
         if constexpr (KB > 0) {
             uint32_t w[KB];
             read_words<KB>(w, stp + ST::kKC + (r0 + 8 * n + g) * ST::kRK + c * (KB * 4));
@@ -637,7 +639,7 @@ __device__ __forceinline__ void step(Acc<VP>& st, const unsigned char* stp, int 
             for (int kb = 0; kb < kKB; ++kb) {
                 uint32_t b0, b1;
                 dk.frag(w, kb, b0, b1);
-                mma16816(S1[n], AQ[kb][0], AQ[kb][1], AQ[kb][2], AQ[kb][3], b0, b1);
+                mma16816((kb & 1) ? S1x[n] : S1[n], AQ[kb][0], AQ[kb][1], AQ[kb][2], AQ[kb][3], b0, b1);
             }
         }
         if constexpr (KP) {
@@ -646,8 +648,13 @@ __device__ __forceinline__ void step(Acc<VP>& st, const unsigned char* stp, int 
             for (int j = 0; j < kKB / 2; ++j) {
                 const uint4 f = lds128(field_off<8, 7>(&ws, 8 * j) | stab);
                 mma16816(S2[n], AS[2 * j][0], AS[2 * j][1], AS[2 * j][2], AS[2 * j][3], f.x, f.y);
-                mma16816(S2[n], AS[2 * j + 1][0], AS[2 * j + 1][1], AS[2 * j + 1][2], AS[2 * j + 1][3], f.z, f.w);
+                mma16816(S2x[n], AS[2 * j + 1][0], AS[2 * j + 1][1], AS[2 * j + 1][2], AS[2 * j + 1][3], f.z, f.w);
             }
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            S1[n][i] += S1x[n][i];
+            S2[n][i] += S2x[n][i];
         }
     }
     // this lane's tokens: i = 0, 1 → 2c, 2c + 1; i = 2, 3 → 8 + 2c, 9 + 2c
