@@ -206,8 +206,9 @@ int tq_decode_workspace_bytes(tq_handle hk, tq_handle hv, int B, int Hq, int Hkv
  * workspace: device buffer of at least tq_decode_workspace_bytes(...) bytes.
  * Rows of a slab past seq_lens[b] (up to T_max) may be read and are masked;
  * nothing past a slab's T_max rows is read.  A staging wait of the d = 128
- * tensor-core kernel that expires records code 30 in hk's status word
- * (tq_device_status); the outputs of that call are then undefined.
+ * tensor-core kernel that expires records code 30 in hk's status word, and the
+ * merging CTA's wait for the split partials code 31 (tq_device_status); the
+ * outputs of that call are then undefined.
  */
 int tq_decode_attention(tq_handle hk, tq_handle hv, const void* q, int q_dtype,
                         tq_planes kc, tq_planes vc, const int32_t* seq_lens,
@@ -282,6 +283,12 @@ int tq_mixed_decode_workspace_bytes(tq_handle hko, tq_handle hkn, tq_handle hvo,
  * must have the same total d (64..256).  Planes kc_o, kc_n, vc_o, vc_n hold
  * B·Hkv·T_max records each, ordered [B][Hkv][T_max].  Other arguments as
  * tq_decode_attention; bad perm entries are recorded in hko's status word.
+ * The split of the page's experiment — d = 128, 32 outlier channels for keys
+ * and for values, mse parts with (b_o, b_n) ∈ {(3, 2), (4, 3), (4, 2)} alike for
+ * keys and values — and T_max % 4 == 0 run on a tensor-core kernel (staging and
+ * merge waits record codes 30 and 31 in hko's status word); every other split on
+ * CUDA-core kernels.  The workspace size depends on which (the size query
+ * answers for the same handles and T_max).
  */
 int tq_mixed_decode_attention(tq_handle hko, tq_handle hkn, tq_handle hvo, tq_handle hvn,
                               const int32_t* perm_k, const int32_t* perm_v, const void* q, int q_dtype,
@@ -305,9 +312,11 @@ int tq_mixed_decode_attention(tq_handle hko, tq_handle hkn, tq_handle hvo, tq_ha
  * Attention then covers the updated lengths; q, q_dtype, kc, vc, B, Hq, Hkv,
  * T_max, scale, out and the workspace are as in tq_decode_attention.  Launches
  * on `stream`: one append (K and V rows together; its last block to finish
- * updates the lengths and clears the decode's merge tickets), then the decode.
- * The append counts its finished blocks in a device word of hk, so calls that
- * share hk must not overlap on the GPU.
+ * updates the lengths and clears the decode's merge tickets), then the decode
+ * (at d = 128 as the append's programmatic dependent: its setup overlaps the
+ * append, and it reads lengths, planes and tickets only once the append grid
+ * has completed).  The append counts its finished blocks in a device word of
+ * hk, so calls that share hk must not overlap on the GPU.
  */
 int tq_decode_append_attention(tq_handle hk, tq_handle hv, const void* q, int q_dtype,
                                const void* k_new, const void* v_new, int kv_dtype,
