@@ -598,11 +598,12 @@ __global__ void __launch_bounds__((kMW + 1) * 32, 1) decode_mixed_mma_kernel(con
         dvo.init(a.vcb[0], mp + SM::kTabVO, lane);
         dvn.init(a.vcb[1], mp + SM::kTabVN, lane);
         for (int tile = warp; tile < ntiles; tile += W) {
-            const int stage = tile >> 2, slot = stage % SM::kStages;
+            constexpr int kTilesPerStage = kStageRows / kTile;
+            const int stage = tile / kTilesPerStage, slot = stage % SM::kStages;
             const bool ok = sm100::mbar_wait(&s_full[slot], (uint32_t)((stage / SM::kStages) & 1), a.status,
                                              kDecodeStageTimeout);
             if (!__all_sync(0xffffffffu, ok)) break;
-            const int tb = t0 + tile * kTile, r0 = (tile & 3) * kTile;
+            const int tb = t0 + tile * kTile, r0 = (tile % kTilesPerStage) * kTile;
             const unsigned char* stp = mp + SM::kStage + (size_t)slot * ST::kBytes;
             if (tb + kTile <= t1)
                 mixed_step<KO, KN, VO, VN, true>(st, stp, r0, tb, t1, dko, dkn, dvo, dvn, AQ, fKo, fKn, a, head0, G, g,

@@ -35,7 +35,7 @@
 // amplified by the softmax — nearly vanishes.
 //
 // Data movement: one producer warp streams the chunk's packed planes into a
-// ring of shared-memory stages of 64 tokens (one bulk copy per plane and stage,
+// ring of shared-memory stages of 64 or 128 tokens (one bulk copy per plane and stage,
 // or per-lane cp.async when the slab's norm rows are not 16-byte aligned), each
 // stage completing on a "full" mbarrier; the consumer warps prepare tables and
 // queries meanwhile (synchronising among themselves only), then take 16-token
@@ -399,13 +399,17 @@ __host__ __device__ constexpr int sign_dim(int c, int tau, int e) { return SignD
 // Tokens per stage of the CTA's staging ring (four 16-token tiles), and the
 // most stages a ring holds (it takes what shared memory the tables leave).
 constexpr int kStageRows = 64;
+// With QJL planes (six or eight bulk copies per stage) stages are 128 tokens, so
+// that the producer's one issuing lane keeps ahead of the consumers.
+template <bool KP, bool VP>
+constexpr int stage_rows() { return KP || VP ? 2 * kStageRows : kStageRows; }
 constexpr int kMaxStages = 12;
 
-// Byte layout of one stage (kStageRows tokens) of every plane: plane by plane,
+// Byte layout of one stage (R tokens) of every plane: plane by plane,
 // rows in token order, so a 16-token tile of a plane is one contiguous run.
 template <int KB, bool KP, int VB, bool VP>
 struct Stage {
-    static constexpr int R = kStageRows;
+    static constexpr int R = stage_rows<KP, VP>();
     static constexpr int kRK = KB * 16, kRV = VB * 16;  // code bytes per row
     static constexpr int kKC = 0;
     static constexpr int kKS = kKC + R * kRK;
@@ -433,10 +437,10 @@ struct Slab {
 
 // The producer warp's copy of one stage: rows [tb, tb + valid) of every plane of
 // the slab into the stage at dst with per-lane cp.async; rows from `valid` to
-// kStageRows are zero-filled and nothing past the chunk's last token is read.
-template <int RB>  // bytes per row, a multiple of 16
+// the stage's R are zero-filled and nothing past the chunk's last token is read.
+template <int RB, int R>  // bytes per row (a multiple of 16), rows per stage
 __device__ __forceinline__ void copy_rows16(uint32_t dst, const uint8_t* src, int valid, int lane) {
-    constexpr int kChunks = kStageRows * RB / 16, kPerRow = RB / 16;
+    constexpr int kChunks = R * RB / 16, kPerRow = RB / 16;
 #pragma unroll
     for (int r = 0; r < (kChunks + 31) / 32; ++r) {
         const int q = lane + 32 * r;
@@ -448,22 +452,24 @@ __device__ __forceinline__ void copy_rows16(uint32_t dst, const uint8_t* src, in
 }
 // fp32 norms: 16-byte chunks of four rows when the plane's rows start on a
 // 16-byte boundary (a16), else one 4-byte copy per row
+template <int R>
 __device__ __forceinline__ void copy_norms(uint32_t dst, const float* src, bool a16, int valid, int lane) {
     if (a16) {
-        if (lane < kStageRows / 4) {
-            const int n = min(4, max(0, valid - 4 * lane));
-            cp_async16(dst + 16 * lane, n > 0 ? src + 4 * lane : src, 4u * (uint32_t)n);
+#pragma unroll
+        for (int q = lane; q < R / 4; q += 32) {
+            const int n = min(4, max(0, valid - 4 * q));
+            cp_async16(dst + 16 * q, n > 0 ? src + 4 * q : src, 4u * (uint32_t)n);
         }
     } else {
 #pragma unroll
-        for (int i = lane; i < kStageRows; i += 32) {
+        for (int i = lane; i < R; i += 32) {
             const bool ok = i < valid;
             cp_async4(dst + 4 * i, ok ? src + i : src, ok ? 4u : 0u);
         }
     }
 }
 
-// Bulk variant (T_max % 4 == 0): rows [tb, tb + min(kStageRows, T_max − tb)) of
+// Bulk variant (T_max % 4 == 0): rows [tb, tb + min(R, T_max − tb)) of
 // every plane with one untiled bulk copy each, completing on the stage's full
 // mbarrier.  The row count is a multiple of 4, so every copy is a multiple of 16
 // bytes and starts on a 16-byte boundary; rows past the chunk's end are masked
@@ -480,8 +486,8 @@ __device__ __forceinline__ void produce_stage_bulk(uint32_t dst, uint32_t bar, c
     using ST = Stage<KB, KP, VB, VP>;
     // bytes of one row over all planes: codes, norms (keys and values), signs and residual norms
     constexpr uint32_t kRowBytes = ST::kRK + ST::kRV + 8 + (KP ? 20 : 0) + (VP ? 20 : 0);
-    static_assert(kRowBytes * kStageRows == ST::kBytes, "bulk staging must fill the whole stage layout");
-    const uint32_t rows = (uint32_t)min(kStageRows, T_max - tb);
+    static_assert(kRowBytes * ST::R == ST::kBytes, "bulk staging must fill the whole stage layout");
+    const uint32_t rows = (uint32_t)min(ST::R, T_max - tb);
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the consumers' reads of the slot come first
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(rows * kRowBytes)
                  : "memory");
@@ -502,18 +508,19 @@ __device__ __forceinline__ void produce_stage_bulk(uint32_t dst, uint32_t bar, c
 template <int KB, bool KP, int VB, bool VP>
 __device__ __forceinline__ void produce_stage(uint32_t dst, const Slab& s, int tb, int valid, int lane) {
     using ST = Stage<KB, KP, VB, VP>;
-    if constexpr (KB > 0) copy_rows16<ST::kRK>(dst + ST::kKC, s.kc + (size_t)tb * ST::kRK, valid, lane);
+    constexpr int R = ST::R;
+    if constexpr (KB > 0) copy_rows16<ST::kRK, R>(dst + ST::kKC, s.kc + (size_t)tb * ST::kRK, valid, lane);
     if constexpr (KP) {
-        copy_rows16<16>(dst + ST::kKS, s.ks + (size_t)tb * 16, valid, lane);
-        copy_norms(dst + ST::kKR, s.krn + tb, s.a16, valid, lane);
+        copy_rows16<16, R>(dst + ST::kKS, s.ks + (size_t)tb * 16, valid, lane);
+        copy_norms<R>(dst + ST::kKR, s.krn + tb, s.a16, valid, lane);
     }
-    copy_norms(dst + ST::kKN, s.kn + tb, s.a16, valid, lane);
-    if constexpr (VB > 0) copy_rows16<ST::kRV>(dst + ST::kVC, s.vc + (size_t)tb * ST::kRV, valid, lane);
+    copy_norms<R>(dst + ST::kKN, s.kn + tb, s.a16, valid, lane);
+    if constexpr (VB > 0) copy_rows16<ST::kRV, R>(dst + ST::kVC, s.vc + (size_t)tb * ST::kRV, valid, lane);
     if constexpr (VP) {
-        copy_rows16<16>(dst + ST::kVS, s.vs + (size_t)tb * 16, valid, lane);
-        copy_norms(dst + ST::kVR, s.vrn + tb, s.a16, valid, lane);
+        copy_rows16<16, R>(dst + ST::kVS, s.vs + (size_t)tb * 16, valid, lane);
+        copy_norms<R>(dst + ST::kVR, s.vrn + tb, s.a16, valid, lane);
     }
-    copy_norms(dst + ST::kVN, s.vn + tb, s.a16, valid, lane);
+    copy_norms<R>(dst + ST::kVN, s.vn + tb, s.a16, valid, lane);
 }
 
 template <int NW>
@@ -929,7 +936,7 @@ __global__ void __launch_bounds__((Warps<VP>::value + 1) * 32, 1) decode_split_m
         L = L < 0 ? 0 : (L > a.T_max ? a.T_max : L);
         t1 = min(t0 + a.chunk, L);
         ntiles = t1 > t0 ? (t1 - t0 + kTile - 1) / kTile : 0;
-        nstages = (ntiles + kStageRows / kTile - 1) / (kStageRows / kTile);
+        nstages = (ntiles + ST::R / kTile - 1) / (ST::R / kTile);
     };
     const size_t head0 = (size_t)b * a.Hq + (size_t)kvh * a.G + (size_t)hb * kHeads;
     const int64_t rowbase = ((int64_t)b * a.Hkv + kvh) * a.T_max;
@@ -971,7 +978,7 @@ __global__ void __launch_bounds__((Warps<VP>::value + 1) * 32, 1) decode_split_m
     // one lane, one copy per plane and stage
     const bool bulk = (a.T_max & 3) == 0;
     auto produce = [&](int i) {
-        const int tb = t0 + i * kStageRows;
+        const int tb = t0 + i * ST::R;
         const uint32_t dst = ring + (uint32_t)((i % SM::kStages) * ST::kBytes);
         const uint32_t bar = smem_addr(&s_full[i % SM::kStages]);
         if (bulk) {
@@ -989,7 +996,7 @@ __global__ void __launch_bounds__((Warps<VP>::value + 1) * 32, 1) decode_split_m
     if (producer && lane == 0) {
         for (int i = 0; i < SM::kStages; ++i) {
             sm100::mbar_init(&s_full[i], bulk ? 1 : 32);
-            sm100::mbar_init(&s_empty[i], kStageRows / kTile);
+            sm100::mbar_init(&s_empty[i], ST::R / kTile);
         }
         sm100::fence_barrier_init();
     }
@@ -1153,13 +1160,14 @@ __global__ void __launch_bounds__((Warps<VP>::value + 1) * 32, 1) decode_split_m
         SignDecoder ds;
         const uint32_t stab = KP ? KSignTable::lane_base(mp + SM::kTabS, lane) : 0u;
 
-        // ---- consumers: tile t is rows 16·(t mod 4) … of stage t / 4
+        // ---- consumers: tile t is rows 16·(t mod n) … of stage t / n (n tiles per stage)
         for (int tile = warp; tile < ntiles; tile += W) {
-            const int stage = tile >> 2, slot = stage % SM::kStages;
+            constexpr int kTilesPerStage = ST::R / kTile;
+            const int stage = tile / kTilesPerStage, slot = stage % SM::kStages;
             const bool ok = sm100::mbar_wait(&s_full[slot], (uint32_t)((stage / SM::kStages) & 1), a.status,
                                              kDecodeStageTimeout);
             if (!__all_sync(0xffffffffu, ok)) break;  // the warp gives up together
-            const int tb = t0 + tile * kTile, r0 = (tile & 3) * kTile;
+            const int tb = t0 + tile * kTile, r0 = (tile % kTilesPerStage) * kTile;
             const unsigned char* stp = mp + SM::kStage + (size_t)slot * ST::kBytes;
             if (tb + kTile <= t1)
                 step<KB, KP, VB, VP, true>(st, stp, r0, tb, t1, dk, dv, ds, stab, AQ, AS, fK, fS, a, head0, G, g, c);
