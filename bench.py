@@ -953,14 +953,20 @@ def run_mixed(args) -> int:
     ws = torch.empty(tq.mixed_decode_workspace_bytes(mk, mv, B, Hq, Hkv, T), dtype=torch.uint8, device=dev)
     out = torch.empty((B, Hq, d), dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    def step():
+        tq.mixed_quantize_kv(mk, mv, Kd, Vd, kc, vc)
+        tq.mixed_decode_attention(mk, mv, qd, kc, vc, ld, Hkv, T, workspace=ws, out=out)
     calls = {"quantize_k": lambda: mk.quantize(Kd, out=kc), "quantize_v": lambda: mv.quantize(Vd, out=vc),
-             "decode": lambda: tq.mixed_decode_attention(mk, mv, qd, kc, vc, ld, Hkv, T, workspace=ws, out=out)}
+             "quantize_kv": lambda: tq.mixed_quantize_kv(mk, mv, Kd, Vd, kc, vc),
+             "decode": lambda: tq.mixed_decode_attention(mk, mv, qd, kc, vc, ld, Hkv, T, workspace=ws, out=out),
+             "step": step}
     for fn in calls.values():
         fn()
     torch.cuda.synchronize()
     rec = (bo * d_o // 8 + 4) + (bn * (d - d_o) // 8 + 4)  # record bytes of both parts
     nbytes = {"quantize_k": n * (2 * d + rec), "quantize_v": n * (2 * d + rec),
-              "decode": int(lens.sum()) * Hkv * 2 * rec + B * Hq * d * 6}
+              "quantize_kv": 2 * n * (2 * d + rec), "decode": int(lens.sum()) * Hkv * 2 * rec + B * Hq * d * 6}
+    nbytes["step"] = nbytes["quantize_kv"] + nbytes["decode"]
     peaks = load_peaks()
     res = {}
     for name, fn in calls.items():

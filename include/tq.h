@@ -262,6 +262,27 @@ int tq_mixed_quantize(tq_handle ho, tq_handle hn, const int32_t* perm, const voi
                       void* scratch, size_t scratch_bytes, void* stream);
 
 /*
+ * tq_mixed_quantize_kv — the keys k (k_rows rows: parts hko, hkn, split perm_k)
+ * and the values v (v_rows rows: hvo, hvn, perm_v) of one decode step in one
+ * call, each side's planes written exactly as tq_mixed_quantize writes them.
+ * k and v share x_dtype; each has its own row stride (rules as
+ * tq_mixed_quantize).  k_rows or v_rows may be 0: that side's pointers are then
+ * not read.  When both sides would take the tensor-core path on their own, have
+ * the same d_o and the same (b_o, b_n), and scratch holds at least
+ * 2·tq_mixed_quantize_scratch_bytes() (keys' operand first, values' second),
+ * one launch builds both operands and one launch quantizes both sides (the
+ * grid's CTAs divided between them in proportion to their rows); otherwise the
+ * sides are quantized one after the other on `stream`, sharing the scratch.
+ * Argument errors name the side ("key" / "value"); bad perm entries are
+ * recorded in that side's hko / hvo status word.
+ */
+int tq_mixed_quantize_kv(tq_handle hko, tq_handle hkn, tq_handle hvo, tq_handle hvn,
+                         const int32_t* perm_k, const int32_t* perm_v, const void* k, const void* v,
+                         int x_dtype, int64_t k_rows, int64_t v_rows, int64_t k_row_stride,
+                         int64_t v_row_stride, tq_planes k_out_o, tq_planes k_out_n, tq_planes v_out_o,
+                         tq_planes v_out_n, void* scratch, size_t scratch_bytes, void* stream);
+
+/*
  * tq_mixed_dequantize — both parts dequantized (as tq_dequantize) and written to
  * their channels of y: device [n_rows, d] of y_dtype, contiguous.
  */

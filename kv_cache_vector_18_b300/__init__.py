@@ -17,7 +17,7 @@ import torch
 from . import _lib
 from ._lib import TQ_BF16, TQ_F32, TQ_MSE, TQ_PROD, TQError, check
 
-__all__ = ["Quantizer", "MixedQuantizer", "quantize_kv", "decode_attention", "decode_append_attention", "mixed_decode_attention",
+__all__ = ["Quantizer", "MixedQuantizer", "quantize_kv", "mixed_quantize_kv", "decode_attention", "decode_append_attention", "mixed_decode_attention",
            "mixed_decode_workspace_bytes", "select_outlier_channels", "decode_workspace_bytes", "build_params_host", "TQError",
            "library_path"]
 
@@ -269,8 +269,9 @@ class MixedQuantizer:
         self.qo = Quantizer(d_o, bits_o, variant, seed=seed_o, rotation=rotation)
         self.qn = Quantizer(self.d - d_o, bits_n, variant, seed=seed_n, rotation=rotation)
         self.d_o, self.variant = d_o, variant
-        # scratch for the combined rotation operand of the tensor-core path
-        self.scratch = torch.empty(_lib.lib().tq_mixed_quantize_scratch_bytes(), dtype=torch.uint8,
+        # scratch for the combined rotation operand of the tensor-core path (room
+        # for two, so mixed_quantize_kv can put keys and values in one launch)
+        self.scratch = torch.empty(2 * _lib.lib().tq_mixed_quantize_scratch_bytes(), dtype=torch.uint8,
                                    device=self.perm.device)
 
     def empty_planes(self, n_rows: int) -> dict:
@@ -294,6 +295,28 @@ class MixedQuantizer:
                                              Quantizer.planes_struct(planes["o"]), Quantizer.planes_struct(planes["n"]),
                                              n, _ptr(y), _DTYPES[dtype], _stream(stream)))
         return y
+
+
+def mixed_quantize_kv(mk: MixedQuantizer, mv: MixedQuantizer, k: torch.Tensor, v: torch.Tensor,
+                      k_out: dict | None = None, v_out: dict | None = None, stream=None) -> tuple[dict, dict]:
+    """tq_mixed_quantize_kv: k with mk and v with mv in one call (one launch on the
+    tensor cores when both splits have the same d_o and bits); the scratch is mk's.
+    k and v are [n, d] with unit stride along channels and the same dtype."""
+    if k.dtype != v.dtype:
+        raise ValueError("k and v must have the same dtype")
+    for x, m in ((k, mk), (v, mv)):
+        if x.dim() != 2 or x.shape[1] != m.d or (x.shape[0] and x.stride(1) != 1):
+            raise ValueError("k and v must be [n, d] with unit stride along channels")
+    nk, nv = k.shape[0], v.shape[0]
+    k_out = mk.empty_planes(nk) if k_out is None else k_out
+    v_out = mv.empty_planes(nv) if v_out is None else v_out
+    P = Quantizer.planes_struct
+    check(_lib.lib().tq_mixed_quantize_kv(
+        mk.qo.handle, mk.qn.handle, mv.qo.handle, mv.qn.handle, _ptr(mk.perm), _ptr(mv.perm),
+        _ptr(k) if nk else None, _ptr(v) if nv else None, _DTYPES[k.dtype], nk, nv, k.stride(0) if nk else mk.d,
+        v.stride(0) if nv else mv.d, P(k_out["o"]), P(k_out["n"]), P(v_out["o"]), P(v_out["n"]), _ptr(mk.scratch),
+        mk.scratch.numel(), _stream(stream)))
+    return k_out, v_out
 
 
 def mixed_decode_workspace_bytes(mk: MixedQuantizer, mv: MixedQuantizer, B: int, Hq: int, Hkv: int, T_max: int) -> int:

@@ -27,7 +27,7 @@ EXPORTED = ["tq_init", "tq_init_ex", "tq_destroy", "tq_row_bytes", "tq_build_par
             "tq_build_params_host_ex", "tq_get_params",
             "tq_quantize", "tq_quantize_kv", "tq_dequantize", "tq_decode_workspace_bytes", "tq_decode_attention",
             "tq_decode_attention_noalloc", "tq_decode_append_attention", "tq_select_outlier_channels",
-            "tq_mixed_quantize_scratch_bytes", "tq_mixed_quantize", "tq_mixed_dequantize", "tq_mixed_decode_workspace_bytes",
+            "tq_mixed_quantize_scratch_bytes", "tq_mixed_quantize", "tq_mixed_quantize_kv", "tq_mixed_dequantize", "tq_mixed_decode_workspace_bytes",
             "tq_mixed_decode_attention", "tq_device_status", "tq_check_wait_timeout", "tq_last_error"]
 NOALLOC_WORKSPACE_BYTES = 4 << 20
 
@@ -75,6 +75,8 @@ def lib() -> ctypes.CDLL:
                                              ctypes.c_float, vp, vp, sz, vp]
     L.tq_select_outlier_channels.argtypes = [vp, i32, i64, i64, i32, i32, vp, vp, vp]
     L.tq_mixed_quantize.argtypes = [vp, vp, vp, vp, i32, i64, i64, Planes, Planes, vp, sz, vp]
+    L.tq_mixed_quantize_kv.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i64, i64, i64, i64, Planes, Planes,
+                                       Planes, Planes, vp, sz, vp]
     L.tq_mixed_quantize_scratch_bytes.argtypes = []
     L.tq_mixed_dequantize.argtypes = [vp, vp, vp, Planes, Planes, i64, vp, i32, vp]
     L.tq_mixed_decode_workspace_bytes.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, ctypes.POINTER(sz)]

@@ -585,28 +585,75 @@ int validate_split(tq_handle ho, tq_handle hn, const char* what) {
 
 size_t tq_mixed_quantize_scratch_bytes(void) { return mixed_tc_scratch_bytes(); }
 
-int tq_mixed_quantize(tq_handle ho, tq_handle hn, const int32_t* perm, const void* x, int x_dtype, int64_t n_rows,
-                      int64_t x_row_stride, tq_planes out_o, tq_planes out_n, void* scratch, size_t scratch_bytes,
-                      void* stream) {
-    int rc = validate_split(ho, hn, "quantizer");
+namespace {
+// The argument checks of one mixed quantize side (rows, perm, planes); n_rows = 0
+// checks only the handles and the dtype.
+int check_mixed_quantize_args(tq_handle ho, tq_handle hn, const int32_t* perm, const void* x, int x_dtype,
+                              int64_t n_rows, int64_t x_row_stride, const tq_planes& out_o, const tq_planes& out_n,
+                              const char* what) {
+    int rc = validate_split(ho, hn, what);
     if (rc != TQ_OK) return rc;
-    if (n_rows < 0) return fail(TQ_EINVAL, "n_rows=%lld is negative", (long long)n_rows);
+    if (n_rows < 0) return fail(TQ_EINVAL, "%s: n_rows=%lld is negative", what, (long long)n_rows);
     if (x_dtype != TQ_BF16 && x_dtype != TQ_F32) return fail(TQ_EINVAL, "x_dtype=%d invalid", x_dtype);
     if (n_rows == 0) return TQ_OK;
     const int d = ho->hp.d + hn->hp.d;
     const int es = x_dtype == TQ_BF16 ? 2 : 4;
-    if (x_row_stride < d) return fail(TQ_EINVAL, "x_row_stride=%lld < d=%d", (long long)x_row_stride, d);
-    if ((x_row_stride * es) % 16 != 0) return fail(TQ_EALIGN, "x_row_stride*elem_size must be a multiple of 16 bytes");
+    if (x_row_stride < d)
+        return fail(TQ_EINVAL, "%s: x_row_stride=%lld < d=%d", what, (long long)x_row_stride, d);
+    if ((x_row_stride * es) % 16 != 0)
+        return fail(TQ_EALIGN, "%s: x_row_stride*elem_size must be a multiple of 16 bytes", what);
     if ((rc = check_device_ptr(perm, "perm", true)) != TQ_OK) return rc;
     if ((rc = check_device_ptr(x, "x", true)) != TQ_OK) return rc;
     if ((rc = check_planes(*ho, out_o, "out_o")) != TQ_OK) return rc;
-    if ((rc = check_planes(*hn, out_n, "out_n")) != TQ_OK) return rc;
-    if ((rc = check_device_ptr(scratch, "scratch", false)) != TQ_OK) return rc;
-    const cudaStream_t s = (cudaStream_t)stream;
+    return check_planes(*hn, out_n, "out_n");
+}
+
+// One side after its checks (n_rows > 0).
+int mixed_quantize_side(tq_handle ho, tq_handle hn, const int32_t* perm, const void* x, int x_dtype, int64_t n_rows,
+                        int64_t x_row_stride, const tq_planes& out_o, const tq_planes& out_n, void* scratch,
+                        size_t scratch_bytes, cudaStream_t s) {
     if (mixed_quantize_tc_supported(*ho, *hn, x_dtype, n_rows, x_row_stride, scratch, scratch_bytes))
         return launch_mixed_quantize_tc(*ho, *hn, perm, x, n_rows, x_row_stride, out_o, out_n, scratch, s);
-    rc = launch_quantize_part(*ho, x, x_dtype, n_rows, x_row_stride, perm, d, out_o, s);
+    const int d = ho->hp.d + hn->hp.d;
+    int rc = launch_quantize_part(*ho, x, x_dtype, n_rows, x_row_stride, perm, d, out_o, s);
     if (rc == TQ_OK) rc = launch_quantize_part(*hn, x, x_dtype, n_rows, x_row_stride, perm + ho->hp.d, d, out_n, s);
+    return rc;
+}
+}  // namespace
+
+int tq_mixed_quantize(tq_handle ho, tq_handle hn, const int32_t* perm, const void* x, int x_dtype, int64_t n_rows,
+                      int64_t x_row_stride, tq_planes out_o, tq_planes out_n, void* scratch, size_t scratch_bytes,
+                      void* stream) {
+    int rc = check_mixed_quantize_args(ho, hn, perm, x, x_dtype, n_rows, x_row_stride, out_o, out_n, "quantizer");
+    if (rc != TQ_OK || n_rows == 0) return rc;
+    if ((rc = check_device_ptr(scratch, "scratch", false)) != TQ_OK) return rc;
+    return mixed_quantize_side(ho, hn, perm, x, x_dtype, n_rows, x_row_stride, out_o, out_n, scratch, scratch_bytes,
+                               (cudaStream_t)stream);
+}
+
+int tq_mixed_quantize_kv(tq_handle hko, tq_handle hkn, tq_handle hvo, tq_handle hvn, const int32_t* perm_k,
+                         const int32_t* perm_v, const void* k, const void* v, int x_dtype, int64_t k_rows,
+                         int64_t v_rows, int64_t k_row_stride, int64_t v_row_stride, tq_planes k_out_o,
+                         tq_planes k_out_n, tq_planes v_out_o, tq_planes v_out_n, void* scratch,
+                         size_t scratch_bytes, void* stream) {
+    int rc = check_mixed_quantize_args(hko, hkn, perm_k, k, x_dtype, k_rows, k_row_stride, k_out_o, k_out_n, "key");
+    if (rc != TQ_OK) return rc;
+    rc = check_mixed_quantize_args(hvo, hvn, perm_v, v, x_dtype, v_rows, v_row_stride, v_out_o, v_out_n, "value");
+    if (rc != TQ_OK) return rc;
+    if ((rc = check_device_ptr(scratch, "scratch", false)) != TQ_OK) return rc;
+    const cudaStream_t s = (cudaStream_t)stream;
+    if (k_rows > 0 && v_rows > 0 &&
+        mixed_quantize_pair_tc_supported(*hko, *hkn, *hvo, *hvn, x_dtype, k_rows, k_row_stride, v_rows, v_row_stride,
+                                         scratch, scratch_bytes))
+        return launch_mixed_quantize_pair_tc(*hko, *hkn, *hvo, *hvn, perm_k, perm_v, k, v, k_rows, k_row_stride,
+                                             v_rows, v_row_stride, k_out_o, k_out_n, v_out_o, v_out_n, scratch, s);
+    // two calls in stream order, so they may share the scratch
+    if (k_rows > 0 && (rc = mixed_quantize_side(hko, hkn, perm_k, k, x_dtype, k_rows, k_row_stride, k_out_o, k_out_n,
+                                                scratch, scratch_bytes, s)) != TQ_OK)
+        return rc;
+    if (v_rows > 0)
+        rc = mixed_quantize_side(hvo, hvn, perm_v, v, x_dtype, v_rows, v_row_stride, v_out_o, v_out_n, scratch,
+                                 scratch_bytes, s);
     return rc;
 }
 

@@ -137,6 +137,16 @@ bool mixed_quantize_tc_supported(const tq_ctx& ho, const tq_ctx& hn, int x_dtype
 int launch_mixed_quantize_tc(const tq_ctx& ho, const tq_ctx& hn, const int32_t* perm, const void* x, int64_t n_rows,
                              int64_t stride, const tq_planes& out_o, const tq_planes& out_n, void* scratch,
                              cudaStream_t s);
+// Keys and values in one launch (both sides supported alone, the same d_o and
+// bits, scratch of two operands: keys' first, values' second).
+bool mixed_quantize_pair_tc_supported(const tq_ctx& hko, const tq_ctx& hkn, const tq_ctx& hvo, const tq_ctx& hvn,
+                                      int x_dtype, int64_t k_rows, int64_t k_stride, int64_t v_rows,
+                                      int64_t v_stride, const void* scratch, size_t scratch_bytes);
+int launch_mixed_quantize_pair_tc(const tq_ctx& hko, const tq_ctx& hkn, const tq_ctx& hvo, const tq_ctx& hvn,
+                                  const int32_t* perm_k, const int32_t* perm_v, const void* k, const void* v,
+                                  int64_t k_rows, int64_t k_stride, int64_t v_rows, int64_t v_stride,
+                                  const tq_planes& k_out_o, const tq_planes& k_out_n, const tq_planes& v_out_o,
+                                  const tq_planes& v_out_n, void* scratch, cudaStream_t s);
 struct MixedShape {
     int B = 0, Hq = 0, Hkv = 0, T_max = 0, d = 0, G = 0, n_splits = 1, chunk = 64;
     bool tc = false;  // the tensor-core mixed decode (tq_decode_mixed_mma.cu) runs it

@@ -10,7 +10,9 @@
 // producer warp, one thread issuing tcgen05.mma (hi then lo) into one of three
 // TMEM accumulators, three epilogue warpgroups.  The epilogue differs: it keeps
 // one norm per part, bucketizes each part's columns against that part's codebook
-// and writes each part's codes and norm to that part's planes.
+// and writes each part's codes and norm to that part's planes.  The keys and
+// values of one step can share a launch: the grid's CTAs are divided between
+// two parameter blocks (each with its own operand M, rows and planes).
 #include "tq_common.cuh"
 #include "tq_sm100.cuh"
 
@@ -60,11 +62,22 @@ constexpr size_t kSmemBytes = kBarOffset + 256 + 1024;
 
 // M_hi / M_lo [j][c]: row j < d_o is row j of Π_o placed at the outlier
 // channels, row j ≥ d_o row j − d_o of Π_n at the other channels, zero elsewhere.
-__global__ void build_mixed_operand_kernel(const uint16_t* __restrict__ po_hi, const uint16_t* __restrict__ po_lo,
-                                           const uint16_t* __restrict__ pn_hi, const uint16_t* __restrict__ pn_lo,
-                                           const int32_t* __restrict__ perm, int d_o, uint16_t* __restrict__ m_hi,
-                                           uint16_t* __restrict__ m_lo, int* __restrict__ status_o,
-                                           int* __restrict__ status_n) {
+struct OperandSrc {
+    const uint16_t *po_hi, *po_lo, *pn_hi, *pn_lo;
+    const int32_t* perm;
+    int d_o;
+    uint16_t *m_hi, *m_lo;
+    int *status_o, *status_n;
+};
+
+// blockIdx.y picks the side (a single side launches one row of blocks).
+__global__ void build_mixed_operand_kernel(const OperandSrc src_a, const OperandSrc src_b) {
+    const OperandSrc& sr = blockIdx.y == 0 ? src_a : src_b;
+    const uint16_t *po_hi = sr.po_hi, *po_lo = sr.po_lo, *pn_hi = sr.pn_hi, *pn_lo = sr.pn_lo;
+    const int32_t* perm = sr.perm;
+    const int d_o = sr.d_o;
+    uint16_t *m_hi = sr.m_hi, *m_lo = sr.m_lo;
+    int *status_o = sr.status_o, *status_n = sr.status_n;
     const int j = blockIdx.x, c = threadIdx.x;
     m_hi[(size_t)j * kD + c] = 0;
     m_lo[(size_t)j * kD + c] = 0;
@@ -138,12 +151,39 @@ __device__ __forceinline__ void store_words(uint8_t* cd, const uint32_t (&cw)[BM
     }
 }
 
+// Everything one side of a launch reads and writes: its rows (tm_x), its operand
+// M (tm_m_hi, tm_m_lo), both parts' codebooks and planes, its status word.
+struct MixSide {
+    CUtensorMap tm_x, tm_m_hi, tm_m_lo;
+    int64_t n_rows;
+    Codebook cbo, cbn;
+    uint8_t* codes_o;
+    float* norm_o;
+    uint8_t* codes_n;
+    float* norm_n;
+    int* status;
+};
+
+// CTAs [0, split) quantize side a, CTAs [split, gridDim.x) side b; a single side
+// passes split = gridDim.x.
 template <int DO, int BMO, int BMN>
 __global__ void __launch_bounds__(kThreads, 1)
-quantize_mixed_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_m_hi,
-                         const __grid_constant__ CUtensorMap tm_m_lo, int64_t n_rows, Codebook cbo, Codebook cbn,
-                         uint8_t* __restrict__ codes_o, float* __restrict__ norm_o, uint8_t* __restrict__ codes_n,
-                         float* __restrict__ norm_n, int* __restrict__ status) {
+quantize_mixed_tc_kernel(const __grid_constant__ MixSide side_a, const __grid_constant__ MixSide side_b, int split) {
+    const bool on_b = (int)blockIdx.x >= split;
+    const MixSide& sd = on_b ? side_b : side_a;
+    const int cta = on_b ? (int)blockIdx.x - split : (int)blockIdx.x;
+    const int ncta = on_b ? (int)gridDim.x - split : split;
+    const CUtensorMap& tm_x = sd.tm_x;
+    const CUtensorMap& tm_m_hi = sd.tm_m_hi;
+    const CUtensorMap& tm_m_lo = sd.tm_m_lo;
+    const int64_t n_rows = sd.n_rows;
+    const Codebook& cbo = sd.cbo;
+    const Codebook& cbn = sd.cbn;
+    uint8_t* __restrict__ codes_o = sd.codes_o;
+    float* __restrict__ norm_o = sd.norm_o;
+    uint8_t* __restrict__ codes_n = sd.codes_n;
+    float* __restrict__ norm_n = sd.norm_n;
+    int* __restrict__ status = sd.status;
     constexpr int DN = kD - DO;
     constexpr int CO = DO / 32;                       // 32-column chunks of the outlier part
     constexpr int PO = (1 << BMO) / 2 - 1, PN = (1 << BMN) / 2 - 1;
@@ -195,7 +235,7 @@ quantize_mixed_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_
             tma_load_2d(m_lo + c * kChunkBytesB, &tm_m_lo, mat_full, c * kKC, 0);
         }
         int64_t i = 0;
-        for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++i) {
+        for (int64_t tile = cta; tile < ntiles; tile += ncta, ++i) {
             const int s = (int)(i % kStages);
             const int64_t u = i / kStages;
             if (u > 0 && !mbar_wait(&empty[s], (uint32_t)((u - 1) & 1), status, 21)) break;
@@ -216,7 +256,7 @@ quantize_mixed_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_
         tc_fence_after();
         const uint32_t a_base = smem_u32(stages), hi_base = smem_u32(m_hi), lo_base = smem_u32(m_lo);
         int64_t i = 0;
-        for (int64_t tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x, ++i) {
+        for (int64_t tile = cta; ok && tile < ntiles; tile += ncta, ++i) {
             const int s = (int)(i % kStages);
             const int acc = (int)(i % kAcc);
             const int64_t ua = i / kAcc;
@@ -255,8 +295,7 @@ quantize_mixed_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_
         for (int p = 0; p < PN; ++p) t2n[p] = cbn.t[LN / 2 + p] * cbn.t[LN / 2 + p];
         const uint32_t taddr0 = tmem_base + (uint32_t)(wg * kD) + ((uint32_t)(quad * 32) << 16);
         int64_t j = 0;
-        for (int64_t tile = blockIdx.x + (int64_t)wg * gridDim.x; tile < ntiles;
-             tile += (int64_t)kAcc * gridDim.x, ++j) {
+        for (int64_t tile = cta + (int64_t)wg * ncta; tile < ntiles; tile += (int64_t)kAcc * ncta, ++j) {
             if (!mbar_wait(&tfull[wg], (uint32_t)(j & 1), status, 27)) break;
             tc_fence_after();
             // pass 1: ‖y_o‖² and ‖y_n‖² (the chunk index fixes the part at compile time)
@@ -329,30 +368,74 @@ quantize_mixed_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_
     }
 }
 
+// One launch over one side, or over two (b != nullptr, both holding rows): the
+// grid's CTAs are divided between the sides in proportion to their tiles.
 template <int DO, int BMO, int BMN>
-int launch_mixed_tc(const CUtensorMap& tm_x, const CUtensorMap& tm_hi, const CUtensorMap& tm_lo, int64_t n_rows,
-                    const tq_ctx& ho, const tq_ctx& hn, const tq_planes& out_o, const tq_planes& out_n, int grid,
-                    cudaStream_t s) {
+int launch_mixed_tc(const MixSide& a, const MixSide* b, int num_sms, cudaStream_t s) {
     auto fn = quantize_mixed_tc_kernel<DO, BMO, BMN>;
     static std::atomic<uint64_t> smem_set{0};
     const int rc = ensure_smem_attr(smem_set, (const void*)fn, (int)kSmemBytes, "mixed quantize smem attribute");
     if (rc != TQ_OK) return rc;
-    fn<<<grid, kThreads, kSmemBytes, s>>>(tm_x, tm_hi, tm_lo, n_rows, ho.cb, hn.cb, out_o.codes, out_o.norm,
-                                          out_n.codes, out_n.norm, ho.dp.status);
+    const int64_t ta = (a.n_rows + kTile - 1) / kTile;
+    const int64_t tb = b ? (b->n_rows + kTile - 1) / kTile : 0;
+    const int64_t tiles = ta + tb;
+    const int grid = (int)(tiles < num_sms ? tiles : num_sms);
+    int split = grid;
+    if (b) {  // both sides hold ≥ 1 tile, so grid ≥ 2
+        const int64_t want = (ta * grid + tiles / 2) / tiles;
+        split = (int)(want < 1 ? 1 : (want > grid - 1 ? grid - 1 : want));
+    }
+    fn<<<grid, kThreads, kSmemBytes, s>>>(a, b ? *b : a, split);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? TQ_OK : cuda_fail(e, "mixed tensor-core quantize launch");
 }
 
 template <int DO>
-int dispatch_bits(int bo, int bn, const CUtensorMap& tm_x, const CUtensorMap& tm_hi, const CUtensorMap& tm_lo,
-                  int64_t n_rows, const tq_ctx& ho, const tq_ctx& hn, const tq_planes& oo, const tq_planes& on,
-                  int grid, cudaStream_t s) {
+int dispatch_bits(int bo, int bn, const MixSide& a, const MixSide* b, int num_sms, cudaStream_t s) {
 #define TQ_MB(BO, BN) \
-    if (bo == BO && bn == BN) return launch_mixed_tc<DO, BO, BN>(tm_x, tm_hi, tm_lo, n_rows, ho, hn, oo, on, grid, s)
+    if (bo == BO && bn == BN) return launch_mixed_tc<DO, BO, BN>(a, b, num_sms, s)
     TQ_MB(1, 1); TQ_MB(2, 1); TQ_MB(2, 2); TQ_MB(3, 1); TQ_MB(3, 2);
     TQ_MB(3, 3); TQ_MB(4, 1); TQ_MB(4, 2); TQ_MB(4, 3); TQ_MB(4, 4);
 #undef TQ_MB
     return fail(TQ_EUNSUPPORTED, "mixed tensor-core quantize: bits %d/%d", bo, bn);
+}
+
+// The operand source of one side, its M halves at scratch (2·kMatBytes).
+OperandSrc operand_src(const tq_ctx& ho, const tq_ctx& hn, const int32_t* perm, void* scratch) {
+    OperandSrc o;
+    o.po_hi = ho.dp.Pi_hi;
+    o.po_lo = ho.dp.Pi_lo;
+    o.pn_hi = hn.dp.Pi_hi;
+    o.pn_lo = hn.dp.Pi_lo;
+    o.perm = perm;
+    o.d_o = ho.hp.d;
+    o.m_hi = static_cast<uint16_t*>(scratch);
+    o.m_lo = o.m_hi + kD * kD;
+    o.status_o = ho.dp.status;
+    o.status_n = hn.dp.status;
+    return o;
+}
+
+int make_mix_side(const tq_ctx& ho, const tq_ctx& hn, const OperandSrc& src, const void* x, int64_t n_rows,
+                  int64_t stride, const tq_planes& out_o, const tq_planes& out_n, MixSide* sd) {
+    int rc = encode_tmap_bf16_2d(&sd->tm_x, x, (uint64_t)kD, (uint64_t)n_rows, (uint64_t)stride * 2, kKC, kTile);
+    if (rc == TQ_OK) rc = encode_tmap_bf16_2d(&sd->tm_m_hi, src.m_hi, kD, kD, (uint64_t)kD * 2, kKC, kD);
+    if (rc == TQ_OK) rc = encode_tmap_bf16_2d(&sd->tm_m_lo, src.m_lo, kD, kD, (uint64_t)kD * 2, kKC, kD);
+    sd->n_rows = n_rows;
+    sd->cbo = ho.cb;
+    sd->cbn = hn.cb;
+    sd->codes_o = out_o.codes;
+    sd->norm_o = out_o.norm;
+    sd->codes_n = out_n.codes;
+    sd->norm_n = out_n.norm;
+    sd->status = ho.dp.status;
+    return rc;
+}
+
+int launch_operands(const OperandSrc& a, const OperandSrc* b, cudaStream_t s) {
+    build_mixed_operand_kernel<<<dim3(kD, b ? 2 : 1), kD, 0, s>>>(a, b ? *b : a);
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? TQ_OK : cuda_fail(e, "mixed operand launch");
 }
 
 }  // namespace
@@ -372,22 +455,38 @@ bool mixed_quantize_tc_supported(const tq_ctx& ho, const tq_ctx& hn, int x_dtype
 int launch_mixed_quantize_tc(const tq_ctx& ho, const tq_ctx& hn, const int32_t* perm, const void* x, int64_t n_rows,
                              int64_t stride, const tq_planes& out_o, const tq_planes& out_n, void* scratch,
                              cudaStream_t s) {
-    uint16_t* m_hi = static_cast<uint16_t*>(scratch);
-    uint16_t* m_lo = m_hi + kD * kD;
-    build_mixed_operand_kernel<<<kD, kD, 0, s>>>(ho.dp.Pi_hi, ho.dp.Pi_lo, hn.dp.Pi_hi, hn.dp.Pi_lo, perm, ho.hp.d,
-                                                 m_hi, m_lo, ho.dp.status, hn.dp.status);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_fail(e, "mixed operand launch");
-    CUtensorMap tm_x, tm_hi, tm_lo;
-    int rc = encode_tmap_bf16_2d(&tm_x, x, (uint64_t)kD, (uint64_t)n_rows, (uint64_t)stride * 2, kKC, kTile);
-    if (rc == TQ_OK) rc = encode_tmap_bf16_2d(&tm_hi, m_hi, kD, kD, (uint64_t)kD * 2, kKC, kD);
-    if (rc == TQ_OK) rc = encode_tmap_bf16_2d(&tm_lo, m_lo, kD, kD, (uint64_t)kD * 2, kKC, kD);
+    const OperandSrc src = operand_src(ho, hn, perm, scratch);
+    int rc = launch_operands(src, nullptr, s);
+    MixSide a;
+    if (rc == TQ_OK) rc = make_mix_side(ho, hn, src, x, n_rows, stride, out_o, out_n, &a);
     if (rc != TQ_OK) return rc;
-    const int64_t ntiles = (n_rows + kTile - 1) / kTile;
-    const int grid = (int)(ntiles < ho.num_sms ? ntiles : ho.num_sms);
-    const int bo = ho.hp.b_mse, bn = hn.hp.b_mse;
-    if (ho.hp.d == 32) return dispatch_bits<32>(bo, bn, tm_x, tm_hi, tm_lo, n_rows, ho, hn, out_o, out_n, grid, s);
-    return dispatch_bits<64>(bo, bn, tm_x, tm_hi, tm_lo, n_rows, ho, hn, out_o, out_n, grid, s);
+    if (ho.hp.d == 32) return dispatch_bits<32>(ho.hp.b_mse, hn.hp.b_mse, a, nullptr, ho.num_sms, s);
+    return dispatch_bits<64>(ho.hp.b_mse, hn.hp.b_mse, a, nullptr, ho.num_sms, s);
+}
+
+bool mixed_quantize_pair_tc_supported(const tq_ctx& hko, const tq_ctx& hkn, const tq_ctx& hvo, const tq_ctx& hvn,
+                                      int x_dtype, int64_t k_rows, int64_t k_stride, int64_t v_rows,
+                                      int64_t v_stride, const void* scratch, size_t scratch_bytes) {
+    return mixed_quantize_tc_supported(hko, hkn, x_dtype, k_rows, k_stride, scratch, scratch_bytes) &&
+           mixed_quantize_tc_supported(hvo, hvn, x_dtype, v_rows, v_stride, scratch, scratch_bytes) &&
+           scratch_bytes >= 2 * mixed_tc_scratch_bytes() && hko.hp.d == hvo.hp.d &&
+           hko.hp.b_mse == hvo.hp.b_mse && hkn.hp.b_mse == hvn.hp.b_mse && hko.num_sms == hvo.num_sms;
+}
+
+int launch_mixed_quantize_pair_tc(const tq_ctx& hko, const tq_ctx& hkn, const tq_ctx& hvo, const tq_ctx& hvn,
+                                  const int32_t* perm_k, const int32_t* perm_v, const void* k, const void* v,
+                                  int64_t k_rows, int64_t k_stride, int64_t v_rows, int64_t v_stride,
+                                  const tq_planes& k_out_o, const tq_planes& k_out_n, const tq_planes& v_out_o,
+                                  const tq_planes& v_out_n, void* scratch, cudaStream_t s) {
+    const OperandSrc sk = operand_src(hko, hkn, perm_k, scratch);
+    const OperandSrc sv = operand_src(hvo, hvn, perm_v, static_cast<uint8_t*>(scratch) + mixed_tc_scratch_bytes());
+    int rc = launch_operands(sk, &sv, s);
+    MixSide a, b;
+    if (rc == TQ_OK) rc = make_mix_side(hko, hkn, sk, k, k_rows, k_stride, k_out_o, k_out_n, &a);
+    if (rc == TQ_OK) rc = make_mix_side(hvo, hvn, sv, v, v_rows, v_stride, v_out_o, v_out_n, &b);
+    if (rc != TQ_OK) return rc;
+    if (hko.hp.d == 32) return dispatch_bits<32>(hko.hp.b_mse, hkn.hp.b_mse, a, &b, hko.num_sms, s);
+    return dispatch_bits<64>(hko.hp.b_mse, hkn.hp.b_mse, a, &b, hko.num_sms, s);
 }
 
 }  // namespace tq

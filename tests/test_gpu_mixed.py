@@ -257,3 +257,70 @@ def test_mixed_decode_tensor_core_bad_channel_flagged(tq):
     assert torch.isfinite(out).all()
     assert mk.qo.device_status(clear=True) == _lib.TQ_STATUS_BAD_CHANNEL
     assert mk.qo.device_status() == 0
+
+
+@pytest.mark.parametrize("case", [
+    # (key d_o, key bits, value d_o, value bits, key rows, value rows, dtype)
+    (32, (3, 2), 32, (3, 2), 148 * 128 + 77, 2 * 148 * 128 + 5, "bf16"),   # one launch, ragged tails
+    (64, (4, 2), 64, (4, 2), 3000, 1, "bf16"),                            # one launch, 1-row side
+    (32, (4, 3), 32, (4, 3), 1, 129, "bf16"),                              # one launch on two CTAs
+    (32, (3, 2), 64, (3, 2), 900, 700, "bf16"),                            # d_o differs: two launches
+    (32, (3, 2), 32, (4, 2), 900, 700, "bf16"),                            # bits differ: two launches
+    (32, (3, 2), 32, (3, 2), 0, 500, "bf16"),                              # no keys
+    (32, (3, 2), 32, (3, 2), 500, 0, "bf16"),                              # no values
+    (32, (3, 2), 32, (3, 2), 400, 300, "f32"),                             # CUDA-core parts
+])
+def test_mixed_quantize_kv_matches_separate_calls(tq, case):
+    # tq_mixed_quantize_kv writes the bytes the two tq_mixed_quantize calls write
+    # (each checked against the oracle elsewhere); the value side is also checked
+    # against the oracle directly on sampled rows
+    kdo, kb, vdo, vb, nk, nv, dt = case
+    d = 128
+    K = _hot_rows(max(nk, 1), d, np.arange(0, 128, 4)[:kdo], seed=21, dtype=dt)[:nk]
+    V = _hot_rows(max(nv, 1), d, np.arange(1, 128, 4)[:vdo], seed=22, dtype=dt)[:nv]
+    pk = torch.as_tensor(np.random.default_rng(5).permutation(d), dtype=torch.int32, device="cuda")
+    pv = torch.as_tensor(np.random.default_rng(6).permutation(d), dtype=torch.int32, device="cuda")
+    mk = tq.MixedQuantizer(pk, kdo, kb[0], kb[1], "mse", seed_o=51, seed_n=52)
+    mv = tq.MixedQuantizer(pv, vdo, vb[0], vb[1], "mse", seed_o=53, seed_n=54)
+    kd, vd = K.cuda().contiguous(), V.cuda().contiguous()
+    kc, vc = tq.mixed_quantize_kv(mk, mv, kd, vd)
+    ks = mk.quantize(kd) if nk else mk.empty_planes(0)
+    vs = mv.quantize(vd) if nv else mv.empty_planes(0)
+    torch.cuda.synchronize()
+    for m in (mk, mv):
+        assert m.qo.device_status() == 0 and m.qn.device_status() == 0
+    for got, ref in ((kc, ks), (vc, vs)):
+        for part in ("o", "n"):
+            for name in ref[part]:
+                assert torch.equal(got[part][name], ref[part][name]), (part, name)
+    if nv:
+        mp = _mixed_params(mv)
+        Xf = f64(V)
+        rows = np.unique(np.concatenate([np.arange(min(nv, 150)), np.arange(max(nv - 150, 0), nv)]))
+        check_quantize(mp.po, Xf[:, mp.out], vc["o"], rows=rows)
+        check_quantize(mp.pn, Xf[:, mp.rest], vc["n"], rows=rows)
+
+
+def test_mixed_quantize_kv_rejects_bad_arguments(tq):
+    from kv_cache_vector_18_b300 import _lib
+    perm = torch.arange(128, dtype=torch.int32, device="cuda")
+    mk = tq.MixedQuantizer(perm, 32, 3, 2, "mse", seed_o=1, seed_n=2)
+    mv = tq.MixedQuantizer(perm, 32, 3, 2, "mse", seed_o=3, seed_n=4)
+    x = torch.zeros((16, 128), dtype=torch.bfloat16, device="cuda")
+    kp, vp = mk.empty_planes(16), mv.empty_planes(16)
+    P = tq.Quantizer.planes_struct
+    L = _lib.lib()
+
+    def call(hvo=mv.qo.handle, v_stride=128, scratch_bytes=mk.scratch.numel()):
+        return L.tq_mixed_quantize_kv(mk.qo.handle, mk.qn.handle, hvo, mv.qn.handle, perm.data_ptr(),
+                                      perm.data_ptr(), x.data_ptr(), x.data_ptr(), 0, 16, 16, 128, v_stride,
+                                      P(kp["o"]), P(kp["n"]), P(vp["o"]), P(vp["n"]), mk.scratch.data_ptr(),
+                                      scratch_bytes, None)
+    assert call(hvo=None) == _lib.TQ_EINVAL
+    assert call(v_stride=100) == _lib.TQ_EINVAL
+    assert call(v_stride=132) == _lib.TQ_EALIGN
+    assert "value" in L.tq_last_error().decode()
+    # one operand's worth of scratch: the sides run one after the other, same bytes
+    assert call(scratch_bytes=L.tq_mixed_quantize_scratch_bytes()) == 0
+    torch.cuda.synchronize()
+    assert mk.qo.device_status() == 0 and mv.qo.device_status() == 0
