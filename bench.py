@@ -35,10 +35,11 @@ import synthetic  # noqa: E402
 
 L2_FLUSH_BYTES = 256 << 20
 WARM_SECONDS = 1.0
-# Kernel launches per library call at d = 128 (quantize: 1; decode: the split
-# kernel, which rotates the queries and merges its splits itself, after a
-# memset node that clears its tickets).
-LAUNCHES = {"quantize": 1, "decode": 1}
+# Kernel launches per library call at d = 128 (quantize: 1; decode: the kernel
+# that clears the split tickets, then the split kernel, which rotates the
+# queries and merges its splits itself; the decode-step append's decode: the
+# split kernel alone, the append having cleared the tickets).
+LAUNCHES = {"quantize": 1, "decode": 2, "append_decode": 1}
 
 
 def kv_one_launch(spec) -> bool:
@@ -519,25 +520,34 @@ def run_ours(args, spec):
             assert fn() == 0
         abi_us.append((time.perf_counter() - t) / 20 * 1e6)
         torch.cuda.synchronize()
-    # One CUDA graph per step holding the three library calls back to back (as a
-    # serving loop replays them), captured from the same public API, with event
-    # record nodes between the calls: the replay issues exactly the library's
-    # kernels with no host work in between, the inner events give the per-call
-    # device times and events around each replay the step time.  If event nodes
-    # cannot be captured, one graph per call with events between the replays.
+    # One CUDA graph per step holding the library calls back to back (as a
+    # serving loop replays them), captured from the same public API: the replay
+    # issues exactly the library's kernels with no host work in between, and
+    # events around each replay give the step time.  Each call's kernels may
+    # start their prologues while the previous call's kernel finishes
+    # (programmatic dependent launch), which an event node between the calls
+    # would stop; so the per-call device times come from a second graph of the
+    # same calls with event record nodes between them, replayed K times right
+    # after the timed loop.  If event nodes cannot be captured, one graph per
+    # call with events between the replays serves both.
     cap_ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(calls) + 1)]
-    step_graph, graphs, graph_note = None, [], ""
+    step_graph, inst_graph, graphs, graph_note = None, None, [], ""
     try:
         sg = torch.cuda.CUDAGraph()
         with torch.cuda.graph(sg):
+            for fn in calls:
+                fn()
+        ig = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(ig):
             cap_ev[0].record()
             for i, fn in enumerate(calls):
                 fn()
                 cap_ev[i + 1].record()
         sg.replay()
+        ig.replay()
         torch.cuda.synchronize()
         _ = cap_ev[0].elapsed_time(cap_ev[-1])
-        step_graph = sg
+        step_graph, inst_graph = sg, ig
     except Exception as exc:  # fall back to one graph per call
         graph_note = f"step graph unavailable ({type(exc).__name__}); "
         torch.cuda.synchronize()
@@ -571,8 +581,6 @@ def run_ours(args, spec):
                 ev[0].record()
                 step_graph.replay()
                 ev[-1].record()
-                torch.cuda.synchronize()  # the in-graph events are read before the next replay
-                per_call.append([cap_ev[k].elapsed_time(cap_ev[k + 1]) for k in range(len(calls))])
             else:
                 ev[0].record()
                 for k, g in enumerate(graphs):
@@ -580,6 +588,12 @@ def run_ours(args, spec):
                     ev[k + 1].record()
         torch.cuda.synchronize()
         wall = time.perf_counter() - wall0
+        if inst_graph is not None:  # per-call device times
+            for i in range(args.steps):
+                flush.zero_()
+                inst_graph.replay()
+                torch.cuda.synchronize()  # the in-graph events are read before the next replay
+                per_call.append([cap_ev[k].elapsed_time(cap_ev[k + 1]) for k in range(len(calls))])
     barrier(world)
     if step_graph is None:
         per_call = [[e[k].elapsed_time(e[k + 1]) for k in range(len(calls))] for e in evs]
@@ -654,14 +668,14 @@ def run_ours(args, spec):
     for k, v in rl.items():
         groups.setdefault(v["kernel"], []).append(k)
     dom = max(groups, key=lambda kern: sum(rl[k]["launch_ms"] for k in groups[kern]))
-    calls = groups[dom]
-    if len(calls) == 1:
-        roofline = dict(rl[calls[0]], call=calls[0])
+    dcalls = groups[dom]
+    if len(dcalls) == 1:
+        roofline = dict(rl[dcalls[0]], call=dcalls[0])
     else:
-        nbytes = sum(rl[k]["bytes_per_launch"] for k in calls) / len(calls)
-        ms = sum(rl[k]["launch_ms"] for k in calls) / len(calls)
+        nbytes = sum(rl[k]["bytes_per_launch"] for k in dcalls) / len(dcalls)
+        ms = sum(rl[k]["launch_ms"] for k in dcalls) / len(dcalls)
         achieved = nbytes / (ms / 1e3) / 1e9
-        roofline = dict(rl[calls[0]], call="+".join(calls), achieved=achieved, frac=achieved / peaks["hbm_gbs"],
+        roofline = dict(rl[dcalls[0]], call="+".join(dcalls), achieved=achieved, frac=achieved / peaks["hbm_gbs"],
                         bytes_per_launch=nbytes, launch_ms=ms)
     roofline_decode = rl["decode"]
 
@@ -684,8 +698,10 @@ def run_ours(args, spec):
             "clocks": sampler.summary(), "wall_s_timed_loop": wall, "roofline": roofline,
             "roofline_decode": roofline_decode, "roofline_per_call": rl, "e2e": e2e, "append_step": append,
             "timing": graph_note + (f"one CUDA graph per step holding the {len(calls)} library calls (captured through "
-                                    "the public API); step time from CUDA events around each replay, per-call "
-                                    "times from event nodes inside the graph" if step_graph is not None else
+                                    "the public API); step time from CUDA events around each replay; per-call "
+                                    "times from event nodes between the calls of a second graph of the same calls, "
+                                    "replayed K times after the timed loop (the event nodes stop the calls' "
+                                    "programmatic overlap)" if step_graph is not None else
                                     "CUDA events around CUDA-graph replays of each library call (one graph per call)")
                       + "; L2 flushed before every step; after >= %.1f s of back-to-back warm-up (%d steps)"
                       % (args.warm_seconds, warm_steps),
@@ -887,7 +903,7 @@ def measure_append(tq, kq, vq, qd, kc, vc, ld, spec, ws, out, flush, dev, reps: 
         e1.record()
     torch.cuda.synchronize()
     us = [e0.elapsed_time(e1) * 1e3 for e0, e1 in evs]
-    return {"us": statistics.mean(us), "reps": reps, "library_launches": 1 + LAUNCHES["decode"],
+    return {"us": statistics.mean(us), "reps": reps, "library_launches": 1 + LAUNCHES["append_decode"],
             "what": "append of K and V (whose last block bumps the lengths and clears the decode's tickets) + "
                     "decode launched as its programmatic dependent, one graph; lengths reset and L2 flushed "
                     "before each replay, outside the timed region"}

@@ -271,6 +271,36 @@ int launch_split_mma_any(const SplitArgs& a, dim3 grid, int kb, bool kp, int vb,
     return fail(TQ_EUNSUPPORTED, "tensor-core decode: key b_m=%d", kb);
 }
 
+// Zeroes the split-merge tickets of the decode launched after it, which is its
+// programmatic dependent and may start right away; this grid completes only once
+// every kernel before it has, so the decode's griddepcontrol.wait covers them
+// all.  Launched itself as a programmatic dependent, its zeroing may overlap the
+// kernel before it, which therefore must not use this workspace (the quantize
+// kernels do not; a decode never lets its dependents start early).
+__global__ void clear_tickets_kernel(int* __restrict__ tickets, int n) {
+    for (int i = threadIdx.x; i < n; i += blockDim.x) tickets[i] = 0;
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+}  // namespace
+
+int launch_clear_tickets(int* tickets, int n, cudaStream_t s) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1);
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, clear_tickets_kernel, tickets, n);
+    return e == cudaSuccess ? TQ_OK : cuda_fail(e, "clearing the split tickets");
+}
+
+namespace {
+
 template <int D>
 int launch_d(const tq_ctx& hk, const tq_ctx& hv, const DecodeShape& p, const void* q, int q_dtype,
              const tq_planes& kc, const tq_planes& vc, const int32_t* seq_lens, float scale, float* out,
@@ -303,14 +333,16 @@ int launch_d(const tq_ctx& hk, const tq_ctx& hv, const DecodeShape& p, const voi
     if (use_mma_split(D)) {
         // query rotation, split and merge all happen in the split kernel
         a.n_hblocks = (p.G + mmadec::kHeadsPerCta - 1) / mmadec::kHeadsPerCta;
+        // the kernel is the programmatic dependent of the decode-step append (which
+        // cleared the tickets and does not write q) or of the ticket clearing
+        // kernel: its prologue overlaps the kernels before it
+        a.q_early = tickets_zeroed ? 1 : 0;
         if (!tickets_zeroed) {
-            e = cudaMemsetAsync(cnt, 0, (size_t)p.B * p.Hq * sizeof(int), s);
-            if (e != cudaSuccess) return cuda_fail(e, "clearing the split tickets");
+            const int rc = launch_clear_tickets(cnt, p.B * p.Hq, s);
+            if (rc != TQ_OK) return rc;
         }
-        // after the decode-step append (which cleared the tickets) the kernel is its
-        // programmatic dependent: its prologue overlaps the append
         return launch_split_mma_any(a, dim3(p.n_splits, p.Hkv * a.n_hblocks, p.B), hk.hp.b_mse, kprod, hv.hp.b_mse,
-                                    vprod, tickets_zeroed, s);
+                                    vprod, true, s);
     }
 
     // CUDA-core path: query prep (which also clears the tickets), split, merge

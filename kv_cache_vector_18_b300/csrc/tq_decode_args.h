@@ -44,6 +44,9 @@ struct SplitArgs {
     // Query rotation inside the split kernel (tensor-core path): q′ = Π_k·q, q″ = S_k·q.
     const void* q;     // [B, Hq, d], bf16 or f32
     int q_f32;
+    // 1: q may be read before griddepcontrol.wait (no kernel the launch may
+    // overlap writes it); 0: only after it
+    int q_early;
     // the rotation on the tensor cores: Π_k = hi + lo, S_k = hi + lo, bf16 row-major [j][i]
     const uint16_t* kPi_hi;
     const uint16_t* kPi_lo;

@@ -417,7 +417,11 @@ __global__ void __launch_bounds__((kMW + 1) * 32, 1) decode_mixed_mma_kernel(con
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
     const int t0 = split * a.chunk;
     int t1 = t0, ntiles = 0, nstages = 0;
+    // The kernel is the programmatic dependent of the ticket clearing kernel, so
+    // the kernels before that one may still run: lengths, cache planes, queries,
+    // permutations and tickets are read only after griddepcontrol.wait.
     auto read_length = [&]() {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
         int L = a.seq_lens[b];
         L = L < 0 ? 0 : (L > a.T_max ? a.T_max : L);
         t1 = min(t0 + a.chunk, L);
@@ -516,6 +520,11 @@ __global__ void __launch_bounds__((kMW + 1) * 32, 1) decode_mixed_mma_kernel(con
                             bl[u]);
         unsigned char* qin = mp + SM::kQin;
         int* pk = reinterpret_cast<int*>(mp + SM::kPerm);
+        Table<KO>::fill(mp + SM::kTabKO, a.kcb[0], threadIdx.x, NC);
+        Table<KN>::fill(mp + SM::kTabKN, a.kcb[1], threadIdx.x, NC);
+        Table<VO>::fill(mp + SM::kTabVO, a.vcb[0], threadIdx.x, NC);
+        Table<VN>::fill(mp + SM::kTabVN, a.vcb[1], threadIdx.x, NC);
+        asm volatile("griddepcontrol.wait;" ::: "memory");
         {
             const int rowq = a.q_f32 ? D / 4 : D / 8;
             const unsigned char* qb = static_cast<const unsigned char*>(a.q) + head0 * D * (a.q_f32 ? 4 : 2);
@@ -527,10 +536,6 @@ __global__ void __launch_bounds__((kMW + 1) * 32, 1) decode_mixed_mma_kernel(con
                 cp_async16(smem_addr(pk) + 16u * (uint32_t)idx, a.perm_k + 4 * idx, 16u);
             cp_async_commit();
         }
-        Table<KO>::fill(mp + SM::kTabKO, a.kcb[0], threadIdx.x, NC);
-        Table<KN>::fill(mp + SM::kTabKN, a.kcb[1], threadIdx.x, NC);
-        Table<VO>::fill(mp + SM::kTabVO, a.vcb[0], threadIdx.x, NC);
-        Table<VN>::fill(mp + SM::kTabVN, a.vcb[1], threadIdx.x, NC);
         cp_async_wait<0>();
         consumers_sync();
         // q gathered into the frame's channel order: qg[h][i] = q[h][perm_k[i]]
@@ -690,8 +695,18 @@ int launch_mixed_tc(const MixedTcArgs& a, dim3 grid, cudaStream_t s) {
     static std::atomic<uint64_t> smem_set{0};
     const int rc = ensure_smem_attr(smem_set, (const void*)fn, (int)SM::kBytes, "mixed decode smem attribute");
     if (rc != TQ_OK) return rc;
-    fn<<<grid, SM::kThreads, SM::kBytes, s>>>(a);
-    const cudaError_t e = cudaGetLastError();
+    // the programmatic dependent of the ticket clearing kernel launched before it
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(SM::kThreads);
+    cfg.dynamicSmemBytes = SM::kBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, fn, a);
     return e == cudaSuccess ? TQ_OK : cuda_fail(e, "mixed decode (tensor-core) launch");
 }
 

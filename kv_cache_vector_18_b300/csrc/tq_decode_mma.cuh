@@ -925,10 +925,10 @@ __global__ void __launch_bounds__((Warps<VP>::value + 1) * 32, 1) decode_split_m
     const int split = blockIdx.x, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
     const int t0 = split * a.chunk;
-    // Lengths, cache planes and merge tickets may come from the kernel launched
-    // just before this one (the decode-step append, launched as its programmatic
-    // dependent): each branch reads them only after griddepcontrol.wait, which
-    // returns at once for an ordinary launch.
+    // Lengths, cache planes, merge tickets and (unless a.q_early) the queries may
+    // come from the kernels launched before this one, whose tails this grid may
+    // overlap as a programmatic dependent: each branch reads them only after
+    // griddepcontrol.wait, which returns at once for an ordinary launch.
     int t1 = t0, ntiles = 0, nstages = 0;
     auto read_length = [&]() {
         asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -1047,9 +1047,10 @@ __global__ void __launch_bounds__((Warps<VP>::value + 1) * 32, 1) decode_split_m
             }
         }
         // the raw queries of this head block (rows as stored, bf16 or fp32; heads
-        // past G zero) copied into shared memory while the tables are filled
+        // past G zero) copied into shared memory: while the tables are filled when
+        // they may be read early, else after the tables and griddepcontrol.wait
         unsigned char* qin = mp + SM::kQin;  // [kHeads][D] elements of the query dtype
-        {
+        auto load_q = [&]() {
             const int rowq = a.q_f32 ? D / 4 : D / 8;  // 16-byte pieces per head row
             const unsigned char* qb = static_cast<const unsigned char*>(a.q) + head0 * D * (a.q_f32 ? 4 : 2);
             for (int idx = threadIdx.x; idx < kHeads * rowq; idx += NC) {
@@ -1057,10 +1058,15 @@ __global__ void __launch_bounds__((Warps<VP>::value + 1) * 32, 1) decode_split_m
                 cp_async16(smem_addr(qin) + 16u * (uint32_t)idx, live ? qb + 16 * idx : qb, live ? 16u : 0u);
             }
             cp_async_commit();
-        }
+        };
+        if (a.q_early) load_q();
         Table<KB>::fill(mp + SM::kTabK, a.kcb, threadIdx.x, NC);
         Table<VB>::fill(mp + SM::kTabV, a.vcb, threadIdx.x, NC);
         if constexpr (KP) KSignTable::fill(mp + SM::kTabS, threadIdx.x, NC);
+        if (!a.q_early) {
+            asm volatile("griddepcontrol.wait;" ::: "memory");
+            load_q();
+        }
         cp_async_wait<0>();
         consumers_sync();
         {
@@ -1259,8 +1265,9 @@ __global__ void __launch_bounds__((Warps<VP>::value + 1) * 32, 1) decode_split_m
 }
 
 // pdl: launched as the programmatic dependent of the kernel before it in the
-// stream (which must then be the decode-step append, the only producer of the
-// inputs the kernel reads before griddepcontrol.wait being its caller's q)
+// stream.  That kernel must not write the workspace; with a.q_early it must not
+// write q either (the decode-step append), else it may be anything (the ticket
+// clearing kernel, which completes only after the kernels before it).
 template <int KB, bool KP, int VB, bool VP>
 int launch_split_mma(const SplitArgs& a, dim3 grid, bool pdl, cudaStream_t s) {
     using SM = Smem<KB, KP, VB, VP>;

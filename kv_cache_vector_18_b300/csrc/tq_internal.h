@@ -169,6 +169,11 @@ int mixed_plan(int d, int sms, bool vprod, bool tc, int B, int Hq, int Hkv, int 
                size_t* ws_bytes);
 // Whether the tensor-core mixed decode serves these handles and T_max: d = 128,
 // outlier parts of 32 channels, mse parts, instantiated bit pairs, T_max % 4 == 0.
+// Zeroes n merge tickets in a kernel launched as a programmatic dependent,
+// which lets the decode launched right after it (as its programmatic dependent)
+// start while the kernels before finish; the decode's griddepcontrol.wait then
+// covers every kernel before the clearing one (tq_decode.cu).
+int launch_clear_tickets(int* tickets, int n, cudaStream_t s);
 bool mixed_decode_tc_supported(const tq_ctx& hko, const tq_ctx& hkn, const tq_ctx& hvo, const tq_ctx& hvn,
                                int T_max);
 int launch_mixed_decode(const MixedDecode& m, const MixedShape& p, cudaStream_t s);

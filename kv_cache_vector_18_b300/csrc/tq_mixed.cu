@@ -452,8 +452,8 @@ int launch_mixed_tc_path(const MixedDecode& m, const MixedShape& p, cudaStream_t
     a.q = m.q;
     a.q_f32 = m.q_dtype == TQ_F32;
     a.status = m.hk[0]->dp.status;
-    cudaError_t e = cudaMemsetAsync(a.cnt, 0, (size_t)p.B * p.Hq * sizeof(int), s);
-    if (e != cudaSuccess) return cuda_fail(e, "clearing the mixed merge tickets");
+    const int rc = launch_clear_tickets(a.cnt, p.B * p.Hq, s);
+    if (rc != TQ_OK) return rc;
     return launch_mixed_decode_tc(a, dim3(p.n_splits, p.Hkv * a.n_hblocks, p.B), m.hk[0]->hp.b_mse,
                                   m.hk[1]->hp.b_mse, s);
 }

@@ -189,6 +189,7 @@ quantize_mixed_tc_kernel(const __grid_constant__ MixSide side_a, const __grid_co
     constexpr int PO = (1 << BMO) / 2 - 1, PN = (1 << BMN) / 2 - 1;
     constexpr int RO = BMO * DO / 8, RN = BMN * DN / 8;  // record bytes of the two code planes
     extern __shared__ __align__(1024) uint8_t smem_raw[];
+    allow_dependents();
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* m_hi = smem;
     uint8_t* m_lo = smem + kMatBytes;

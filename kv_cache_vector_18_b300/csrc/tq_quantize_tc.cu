@@ -117,6 +117,7 @@ quantize_mse_tc_kernel(const __grid_constant__ TcSide side_a, const __grid_const
     constexpr int P = L / 2 - 1;          // positive decision boundaries
     constexpr int WORDS = BM * D / 32;    // packed 32-bit words per row
     extern __shared__ __align__(1024) uint8_t smem_raw[];
+    allow_dependents();
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* pi_hi = smem;
     uint8_t* pi_lo = smem + C::kPiBytes;
@@ -527,6 +528,7 @@ quantize_mse_tc256_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid
     constexpr int P = L / 2 - 1;          // positive decision boundaries
     constexpr int WORDS = BM * D / 32;    // packed 32-bit words per row
     extern __shared__ __align__(1024) uint8_t smem_raw[];
+    allow_dependents();
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* stages = smem;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
@@ -855,6 +857,7 @@ quantize_prod_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_c
     constexpr int P = BM >= 1 ? L / 2 - 1 : 0;  // positive decision boundaries
     constexpr int WORDS = BM * D / 32;          // packed code words per row
     extern __shared__ __align__(1024) uint8_t smem_raw[];
+    allow_dependents();
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* pi_hi = smem;
     uint8_t* pi_lo = smem + C::kMatBytes;
@@ -1255,6 +1258,7 @@ quantize_prod_tc256_kernel(const __grid_constant__ CUtensorMap tm_x, const __gri
     constexpr int P = BM >= 1 ? L / 2 - 1 : 0;  // positive decision boundaries
     constexpr int WORDS = BM * D / 32;          // packed code words per row
     extern __shared__ __align__(1024) uint8_t smem_raw[];
+    allow_dependents();
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* stages = smem;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);

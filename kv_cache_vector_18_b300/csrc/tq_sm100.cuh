@@ -29,6 +29,14 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
 }
 
+// Let the kernel launched after this one in the stream start now if it was
+// launched as a programmatic dependent: it reads what this grid writes only
+// after its griddepcontrol.wait, which returns once this grid has completed and
+// its writes are visible.  Without such a dependent it changes nothing.
+__device__ __forceinline__ void allow_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Make barrier initialisation visible to the async (TMA / tensor core) proxy.
 __device__ __forceinline__ void fence_barrier_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
