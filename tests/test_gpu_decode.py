@@ -170,3 +170,64 @@ def test_end_to_end_against_oracle_codes(tq):
           f"(rel-L2 {l2_own:.2e}) against the oracle on its own codes; rows whose codes differ: K {k_rows}, "
           f"K signs {s_rows}, V {v_rows} of {K.shape[0] * K.shape[1] * K.shape[2]}")
     assert e_own <= 5e-2 and l2_own <= 5e-2
+
+
+def test_decode_launched_behind_quantize_reads_its_codes(tq):
+    # The decode is a programmatic dependent (through the ticket clearing kernel)
+    # of the quantize launched just before it, so its prologue overlaps the
+    # quantize; it must still read only what that quantize wrote.  Outputs of
+    # unsynchronised quantize → decode sequences equal those of the same calls
+    # with a synchronisation in between, bit for bit (the decode's arithmetic and
+    # merge order are fixed).
+    B, Hq, Hkv, T, d = 1, 64, 8, 32768, 128
+    kq = tq.Quantizer(d, 3, "mse", seed=91)
+    vq = tq.Quantizer(d, 3, "mse", seed=92)
+    X = [synthetic.gaussian((B * Hkv * T, d), seed=s).cuda() for s in (1, 2, 3, 4)]
+    q = synthetic.gaussian((B, Hq, d), seed=5).cuda()
+    sl = torch.tensor([T], dtype=torch.int32, device="cuda")
+    kc, vc = kq.empty_planes(B * Hkv * T), vq.empty_planes(B * Hkv * T)
+
+    def step(k, v, sync):
+        tq.quantize_kv(kq, vq, k, v, k_out=kc, v_out=vc)
+        if sync:
+            torch.cuda.synchronize()
+        return tq.decode_attention(kq, vq, q, kc, vc, sl, Hkv, T)
+
+    ref_a = step(X[0], X[1], True)
+    ref_b = step(X[2], X[3], True)
+    torch.cuda.synchronize()
+    outs = [step(X[2 * (i % 2)], X[2 * (i % 2) + 1], False) for i in range(6)]
+    torch.cuda.synchronize()
+    assert kq.device_status() == 0 and vq.device_status() == 0
+    assert not torch.equal(ref_a, ref_b)
+    for i, o in enumerate(outs):
+        assert torch.equal(o, ref_a if i % 2 == 0 else ref_b), i
+
+
+def test_mixed_decode_launched_behind_quantize_reads_its_codes(tq):
+    # as above for the mixed-precision pair (one-launch K+V quantize, tensor-core decode)
+    B, Hq, Hkv, T, d = 1, 64, 8, 32768, 128
+    X = [synthetic.gaussian((B * Hkv * T, d), seed=s).cuda() for s in (11, 12, 13, 14)]
+    pk = torch.as_tensor(np.random.default_rng(1).permutation(d), dtype=torch.int32, device="cuda")
+    pv = torch.as_tensor(np.random.default_rng(2).permutation(d), dtype=torch.int32, device="cuda")
+    mk = tq.MixedQuantizer(pk, 32, 3, 2, "mse", seed_o=1, seed_n=2)
+    mv = tq.MixedQuantizer(pv, 32, 3, 2, "mse", seed_o=3, seed_n=4)
+    q = synthetic.gaussian((B, Hq, d), seed=15).cuda()
+    sl = torch.tensor([T], dtype=torch.int32, device="cuda")
+    kc, vc = mk.empty_planes(B * Hkv * T), mv.empty_planes(B * Hkv * T)
+
+    def step(k, v, sync):
+        tq.mixed_quantize_kv(mk, mv, k, v, kc, vc)
+        if sync:
+            torch.cuda.synchronize()
+        return tq.mixed_decode_attention(mk, mv, q, kc, vc, sl, Hkv, T)
+
+    ref_a = step(X[0], X[1], True)
+    ref_b = step(X[2], X[3], True)
+    torch.cuda.synchronize()
+    outs = [step(X[2 * (i % 2)], X[2 * (i % 2) + 1], False) for i in range(6)]
+    torch.cuda.synchronize()
+    assert mk.qo.device_status() == 0 and mv.qo.device_status() == 0
+    assert not torch.equal(ref_a, ref_b)
+    for i, o in enumerate(outs):
+        assert torch.equal(o, ref_a if i % 2 == 0 else ref_b), i
