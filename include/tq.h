@@ -209,6 +209,13 @@ int tq_decode_workspace_bytes(tq_handle hk, tq_handle hv, int B, int Hq, int Hkv
  * tensor-core kernel that expires records code 30 in hk's status word, and the
  * merging CTA's wait for the split partials code 31 (tq_device_status); the
  * outputs of that call are then undefined.
+ * Stream order is kept: at d = 128 the call launches a kernel that zeroes the
+ * workspace's merge tickets and then the decode kernel, each as the
+ * programmatic dependent of the kernel before it, and the decode reads none of
+ * its inputs before every kernel enqueued ahead of the call has completed.  The
+ * decode's prologue then overlaps the tail of a library quantize kernel
+ * launched just before it; an event or copy enqueued in between, or a kernel
+ * that does not release its dependents early, simply ends that overlap.
  */
 int tq_decode_attention(tq_handle hk, tq_handle hv, const void* q, int q_dtype,
                         tq_planes kc, tq_planes vc, const int32_t* seq_lens,

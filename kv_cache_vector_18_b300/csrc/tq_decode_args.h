@@ -29,7 +29,8 @@ struct SplitArgs {
     float kgamma, vgamma, scale;
     int B, Hq, Hkv, T_max, G, n_splits, chunk, n_hblocks;
     // Fused merge (tensor-core path): one ticket counter per (batch, KV head,
-    // head block), zeroed before the launch (a memset, or the decode-step append);
+    // head block), zeroed before the launch (by the ticket clearing kernel, or by
+    // the decode-step append);
     // the last split CTA of a group combines the partials and writes
     // out = Π_vᵀ·acc/l (+ S_vᵀ·acc2/l).
     int* cnt;
