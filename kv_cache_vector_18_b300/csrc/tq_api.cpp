@@ -759,7 +759,7 @@ int tq_decode_append_attention(tq_handle hk, tq_handle hv, const void* q, int q_
     int n_tickets = 0;
     int* tickets = decode_tickets(*hv, plan, workspace, &n_tickets);
     if ((rc = launch_append(*hk, *hv, k_new, v_new, kv_dtype, B, Hkv, T_max, seq_lens, kc, vc, tickets, n_tickets,
-                            s)) != TQ_OK)
+                            decode_split_ctas(plan), plan.chunk, s)) != TQ_OK)
         return rc;
     return launch_decode(*hk, *hv, plan, q, q_dtype, kc, vc, seq_lens, scale, out, nullptr, workspace, s, true);
 }

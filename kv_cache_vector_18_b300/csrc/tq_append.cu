@@ -6,7 +6,9 @@
 // then — and zeroes the merge tickets of the decode that follows.
 //
 // A step appends only B·Hkv rows per side, so the work is latency-bound, not
-// bandwidth-bound: one block per (row, side) with four threads per coordinate.
+// bandwidth-bound: one block per (row, side) with four threads per coordinate,
+// or, behind a decode with long chunks whose grid leaves SMs free, that many
+// blocks looping over the pairs (up to four each).
 // Coordinate j forms y_j = Σ_i Π_ji x_i reading Πᵀ down a column (consecutive j
 // across a warp, so every load is coalesced), each of its four threads a quarter
 // of the sum with all of its loads in flight; the sketch s_i = Σ_j T_ij e_j reads
@@ -99,10 +101,14 @@ __device__ __forceinline__ void append_row(const AppendSide& s, int64_t r, int64
     }
 }
 
-template <int D, typename TIn>
+// LOOP = false: one block per (row, side) pair, grid (rows, 2).  LOOP = true: a
+// 1-D grid whose blocks take pairs p = blockIdx.x, blockIdx.x + gridDim.x, …
+// (keys for p < rows, values after).
+template <int D, typename TIn, bool LOOP>
 __global__ void __launch_bounds__(kAppendThreads<D>)
 append_rows_kernel(AppendSide k_side, AppendSide v_side, int32_t* __restrict__ lens, int B, int Hkv, int T_max,
-                   int* __restrict__ status, int* __restrict__ done, int* __restrict__ tickets, int n_tickets) {
+                   int rows, int* __restrict__ status, int* __restrict__ done, int* __restrict__ tickets,
+                   int n_tickets) {
     __shared__ AppendSide s;
     __shared__ float xs[D];
     __shared__ float es[D];
@@ -115,15 +121,32 @@ append_rows_kernel(AppendSide k_side, AppendSide v_side, int32_t* __restrict__ l
     // griddepcontrol.wait, i.e. after this grid has completed
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int j = threadIdx.x;
-    const int64_t r = blockIdx.x;
-    if (j == 0) s = blockIdx.y == 0 ? k_side : v_side;
-    if (j < D / 8) words[j] = 0u;
-    const int L = lens[r / Hkv];
-    if (L >= 0 && L < T_max) {  // block-uniform
-        __syncthreads();
-        append_row<D, TIn>(s, r, r * T_max + L, xs, es, red, part, words);
-    } else if (j == 0 && blockIdx.y == 0) {
-        atomicExch(status, TQ_STATUS_APPEND_FULL);  // a full slab: the row is not written
+    if constexpr (LOOP) {
+        for (int64_t p = blockIdx.x; p < 2 * (int64_t)rows; p += gridDim.x) {
+            const bool vside = p >= rows;
+            const int64_t r = vside ? p - rows : p;
+            __syncthreads();  // the previous pair is done with the shared buffers
+            if (j == 0) s = vside ? v_side : k_side;
+            if (j < D / 8) words[j] = 0u;
+            const int L = lens[r / Hkv];
+            if (L >= 0 && L < T_max) {  // block-uniform
+                __syncthreads();
+                append_row<D, TIn>(s, r, r * T_max + L, xs, es, red, part, words);
+            } else if (j == 0 && !vside) {
+                atomicExch(status, TQ_STATUS_APPEND_FULL);  // a full slab: the row is not written
+            }
+        }
+    } else {
+        const int64_t r = blockIdx.x;
+        if (j == 0) s = blockIdx.y == 0 ? k_side : v_side;
+        if (j < D / 8) words[j] = 0u;
+        const int L = lens[r / Hkv];
+        if (L >= 0 && L < T_max) {  // block-uniform
+            __syncthreads();
+            append_row<D, TIn>(s, r, r * T_max + L, xs, es, red, part, words);
+        } else if (j == 0 && blockIdx.y == 0) {
+            atomicExch(status, TQ_STATUS_APPEND_FULL);  // a full slab: the row is not written
+        }
     }
     // the last block to finish (all blocks have read their lengths by then)
     // bumps every slab that had room and prepares the decode's tickets
@@ -157,13 +180,24 @@ AppendSide side_of(const tq_ctx& h, const void* x, const tq_planes& out) {
 
 template <int D>
 int launch_append_d(const AppendSide& k, const AppendSide& v, int x_dtype, int rows, int B, int Hkv, int T_max,
-                    int32_t* lens, int* status, int* done, int* tickets, int n_tickets, cudaStream_t st) {
-    const dim3 grid((unsigned)rows, 2);
-    if (x_dtype == TQ_BF16)
-        append_rows_kernel<D, __nv_bfloat16><<<grid, kAppendThreads<D>, 0, st>>>(k, v, lens, B, Hkv, T_max, status, done, tickets,
-                                                                 n_tickets);
-    else
-        append_rows_kernel<D, float><<<grid, kAppendThreads<D>, 0, st>>>(k, v, lens, B, Hkv, T_max, status, done, tickets, n_tickets);
+                    int32_t* lens, int* status, int* done, int* tickets, int n_tickets, int blocks, cudaStream_t st) {
+    constexpr int NT = kAppendThreads<D>;
+    if (blocks < 2 * rows) {
+        if (x_dtype == TQ_BF16)
+            append_rows_kernel<D, __nv_bfloat16, true><<<blocks, NT, 0, st>>>(k, v, lens, B, Hkv, T_max, rows, status,
+                                                                              done, tickets, n_tickets);
+        else
+            append_rows_kernel<D, float, true><<<blocks, NT, 0, st>>>(k, v, lens, B, Hkv, T_max, rows, status, done,
+                                                                      tickets, n_tickets);
+    } else {
+        const dim3 grid((unsigned)rows, 2);
+        if (x_dtype == TQ_BF16)
+            append_rows_kernel<D, __nv_bfloat16, false><<<grid, NT, 0, st>>>(k, v, lens, B, Hkv, T_max, rows, status,
+                                                                             done, tickets, n_tickets);
+        else
+            append_rows_kernel<D, float, false><<<grid, NT, 0, st>>>(k, v, lens, B, Hkv, T_max, rows, status, done,
+                                                                     tickets, n_tickets);
+    }
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? TQ_OK : cuda_fail(e, "append launch");
 }
@@ -172,13 +206,23 @@ int launch_append_d(const AppendSide& k, const AppendSide& v, int x_dtype, int r
 
 int launch_append(const tq_ctx& hk, const tq_ctx& hv, const void* k_new, const void* v_new, int x_dtype, int B,
                   int Hkv, int T_max, int32_t* lens, const tq_planes& kc, const tq_planes& vc, int* tickets,
-                  int n_tickets, cudaStream_t s) {
+                  int n_tickets, int64_t decode_ctas, int decode_chunk, cudaStream_t s) {
     const int64_t rows = (int64_t)B * Hkv;
-    if (rows > 0x7fffffffLL) return fail(TQ_EINVAL, "B·Hkv too large");
+    if (rows > 0x3fffffffLL) return fail(TQ_EINVAL, "B·Hkv too large");
+    // One block per (row, side) pair.  But when the decode's CTAs have long
+    // chunks (tens of microseconds of rows below the old length to stream before
+    // they need the append) and the SMs the decode grid leaves free can take the
+    // pairs at up to four per block, the append runs on those SMs alone and
+    // delays no decode CTA.
+    const int64_t pairs = 2 * rows, spare = (int64_t)hk.num_sms - decode_ctas;
+    const int64_t want = (pairs + 3) / 4;
+    const int blocks =
+        (int)(decode_chunk >= kAppendStreamChunk && spare >= want && spare < pairs ? spare : pairs);
     const AppendSide k = side_of(hk, k_new, kc), v = side_of(hv, v_new, vc);
     int* done = hk.dp.append_done;
 #define TQ_APPEND(DD) \
-    return launch_append_d<DD>(k, v, x_dtype, (int)rows, B, Hkv, T_max, lens, hk.dp.status, done, tickets, n_tickets, s)
+    return launch_append_d<DD>(k, v, x_dtype, (int)rows, B, Hkv, T_max, lens, hk.dp.status, done, tickets, n_tickets, \
+                               blocks, s)
     switch (hk.hp.d) {
         case 32: TQ_APPEND(32);
         case 64: TQ_APPEND(64);

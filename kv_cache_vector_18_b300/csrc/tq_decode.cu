@@ -336,7 +336,7 @@ int launch_d(const tq_ctx& hk, const tq_ctx& hv, const DecodeShape& p, const voi
         // the kernel is the programmatic dependent of the decode-step append (which
         // cleared the tickets and does not write q) or of the ticket clearing
         // kernel: its prologue overlaps the kernels before it
-        a.q_early = tickets_zeroed ? 1 : 0;
+        a.after_append = tickets_zeroed ? 1 : 0;
         if (!tickets_zeroed) {
             const int rc = launch_clear_tickets(cnt, p.B * p.Hq, s);
             if (rc != TQ_OK) return rc;
@@ -431,6 +431,11 @@ int decode_plan(const tq_ctx& hk, const tq_ctx& hv, int B, int Hq, int Hkv, int 
     *plan = p;
     *ws_bytes = ws_layout(p, hv.hp.variant == TQ_PROD).total;
     return TQ_OK;
+}
+
+int64_t decode_split_ctas(const DecodeShape& plan) {
+    const int hper = use_mma_split(plan.d) ? mmadec::kHeadsPerCta : kMaxGroup;
+    return (int64_t)plan.n_splits * plan.Hkv * ((plan.G + hper - 1) / hper) * plan.B;
 }
 
 int* decode_tickets(const tq_ctx& hv, const DecodeShape& plan, void* workspace, int* count) {

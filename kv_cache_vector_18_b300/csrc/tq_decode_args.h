@@ -45,9 +45,11 @@ struct SplitArgs {
     // Query rotation inside the split kernel (tensor-core path): q′ = Π_k·q, q″ = S_k·q.
     const void* q;     // [B, Hq, d], bf16 or f32
     int q_f32;
-    // 1: q may be read before griddepcontrol.wait (no kernel the launch may
-    // overlap writes it); 0: only after it
-    int q_early;
+    // 1: launched as the programmatic dependent of the decode-step append, which
+    // writes neither q nor any cache row below the length it starts from (it
+    // writes row seq_lens[b] of each slab, then bumps the lengths): q and those
+    // rows may be read before griddepcontrol.wait.  0: nothing before it.
+    int after_append;
     // the rotation on the tensor cores: Π_k = hi + lo, S_k = hi + lo, bf16 row-major [j][i]
     const uint16_t* kPi_hi;
     const uint16_t* kPi_lo;

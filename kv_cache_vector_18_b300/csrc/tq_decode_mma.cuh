@@ -907,7 +907,10 @@ __device__ __forceinline__ void merge_group(const SplitArgs& a, unsigned char* s
     }
 }
 
-template <int KB, bool KP, int VB, bool VP>
+// AA: launched behind the decode-step append (a.after_append), which writes no
+// cache row below the length it starts from: the stages wholly below that
+// length are streamed and consumed before griddepcontrol.wait.
+template <int KB, bool KP, int VB, bool VP, bool AA>
 __global__ void __launch_bounds__((Warps<VP>::value + 1) * 32, 1) decode_split_mma_kernel(const SplitArgs a) {
     using SM = Smem<KB, KP, VB, VP>;
     using ST = Stage<KB, KP, VB, VP>;
@@ -925,7 +928,7 @@ __global__ void __launch_bounds__((Warps<VP>::value + 1) * 32, 1) decode_split_m
     const int split = blockIdx.x, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
     const int t0 = split * a.chunk;
-    // Lengths, cache planes, merge tickets and (unless a.q_early) the queries may
+    // Lengths, cache planes, merge tickets and (unless a.after_append) the queries may
     // come from the kernels launched before this one, whose tails this grid may
     // overlap as a programmatic dependent: each branch reads them only after
     // griddepcontrol.wait, which returns at once for an ordinary launch.
@@ -977,6 +980,19 @@ __global__ void __launch_bounds__((Warps<VP>::value + 1) * 32, 1) decode_split_m
     // bulk staging when every slab's norm rows start on a 16-byte boundary:
     // one lane, one copy per plane and stage
     const bool bulk = (a.T_max & 3) == 0;
+    // AA: stages of this chunk wholly below L_pre − 1 (L_pre: the length read
+    // before the wait, the append's starting length or that plus one, so every
+    // row below L_pre − 1 was complete before the append started)
+    int ns_safe = 0;
+    if constexpr (AA) {
+        if (bulk) {
+            int Lp;
+            asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(Lp) : "l"(a.seq_lens + b) : "memory");
+            Lp = Lp > a.T_max ? a.T_max : Lp;
+            const int safe = min(t0 + a.chunk, Lp - 1) - t0;
+            ns_safe = safe > 0 ? safe / ST::R : 0;
+        }
+    }
     auto produce = [&](int i) {
         const int tb = t0 + i * ST::R;
         const uint32_t dst = ring + (uint32_t)((i % SM::kStages) * ST::kBytes);
@@ -1018,13 +1034,27 @@ __global__ void __launch_bounds__((Warps<VP>::value + 1) * 32, 1) decode_split_m
     if (producer) {
         // ---- producer: the first stages, then each stage again once its four
         // tiles have been consumed
+        bool live = true;
+        if constexpr (AA) {  // the stages below ns_safe before the wait
+            for (int i = 0; i < ns_safe; ++i) {
+                if (i >= SM::kStages) {
+                    live = __all_sync(0xffffffffu, sm100::mbar_wait(&s_empty[i % SM::kStages],
+                                                                    (uint32_t)((i / SM::kStages - 1) & 1), a.status,
+                                                                    kDecodeStageTimeout));
+                    if (!live) break;
+                }
+                produce(i);
+            }
+        }
         read_length();
-        for (int i = 0; i < min(nstages, SM::kStages); ++i) produce(i);
-        for (int i = SM::kStages; i < nstages; ++i) {
-            const bool ok = sm100::mbar_wait(&s_empty[i % SM::kStages], (uint32_t)((i / SM::kStages - 1) & 1), a.status,
-                                             kDecodeStageTimeout);
-            if (!__all_sync(0xffffffffu, ok)) break;
-            produce(i);
+        if (live) {
+            for (int i = ns_safe; i < min(nstages, SM::kStages); ++i) produce(i);
+            for (int i = max(SM::kStages, ns_safe); i < nstages; ++i) {
+                const bool ok = sm100::mbar_wait(&s_empty[i % SM::kStages], (uint32_t)((i / SM::kStages - 1) & 1),
+                                                 a.status, kDecodeStageTimeout);
+                if (!__all_sync(0xffffffffu, ok)) break;
+                produce(i);
+            }
         }
         cp_async_wait<0>();  // every copy this warp issued has landed
     } else {
@@ -1059,11 +1089,11 @@ __global__ void __launch_bounds__((Warps<VP>::value + 1) * 32, 1) decode_split_m
             }
             cp_async_commit();
         };
-        if (a.q_early) load_q();
+        if (a.after_append) load_q();
         Table<KB>::fill(mp + SM::kTabK, a.kcb, threadIdx.x, NC);
         Table<VB>::fill(mp + SM::kTabV, a.vcb, threadIdx.x, NC);
         if constexpr (KP) KSignTable::fill(mp + SM::kTabS, threadIdx.x, NC);
-        if (!a.q_early) {
+        if (!a.after_append) {
             asm volatile("griddepcontrol.wait;" ::: "memory");
             load_q();
         }
@@ -1108,7 +1138,7 @@ __global__ void __launch_bounds__((Warps<VP>::value + 1) * 32, 1) decode_split_m
         }
         consumers_sync();
 
-        read_length();
+        if constexpr (!AA) read_length();
         // A fragments of head g: [Q′_hi; Q′_lo] for the codes and [Q″_hi; Q″_lo] for
         // the QJL signs, k order following the key decoders' dims
         uint32_t AQ[kKB][4], AS[kKB][4];
@@ -1167,7 +1197,27 @@ __global__ void __launch_bounds__((Warps<VP>::value + 1) * 32, 1) decode_split_m
         const uint32_t stab = KP ? KSignTable::lane_base(mp + SM::kTabS, lane) : 0u;
 
         // ---- consumers: tile t is rows 16·(t mod n) … of stage t / n (n tiles per stage)
-        for (int tile = warp; tile < ntiles; tile += W) {
+        int tile = warp;
+        if constexpr (AA) {  // the tiles of the first ns_safe stages (all full) before the wait
+            constexpr int kTilesPerStage = ST::R / kTile;
+            const int tlim = t0 + ns_safe * ST::R;
+            for (; tile < ns_safe * kTilesPerStage; tile += W) {
+                const int stage = tile / kTilesPerStage, slot = stage % SM::kStages;
+                const bool ok = sm100::mbar_wait(&s_full[slot], (uint32_t)((stage / SM::kStages) & 1), a.status,
+                                                 kDecodeStageTimeout);
+                if (!__all_sync(0xffffffffu, ok)) {
+                    tile = 1 << 30;  // gave up: no further tiles
+                    break;
+                }
+                const int tb = t0 + tile * kTile, r0 = (tile % kTilesPerStage) * kTile;
+                const unsigned char* stp = mp + SM::kStage + (size_t)slot * ST::kBytes;
+                step<KB, KP, VB, VP, true>(st, stp, r0, tb, tlim, dk, dv, ds, stab, AQ, AS, fK, fS, a, head0, G, g, c);
+                __syncwarp();
+                if (lane == 0) sm100::mbar_arrive(&s_empty[slot]);
+            }
+            read_length();
+        }
+        for (; tile < ntiles; tile += W) {
             constexpr int kTilesPerStage = ST::R / kTile;
             const int stage = tile / kTilesPerStage, slot = stage % SM::kStages;
             const bool ok = sm100::mbar_wait(&s_full[slot], (uint32_t)((stage / SM::kStages) & 1), a.status,
@@ -1265,14 +1315,14 @@ __global__ void __launch_bounds__((Warps<VP>::value + 1) * 32, 1) decode_split_m
 }
 
 // pdl: launched as the programmatic dependent of the kernel before it in the
-// stream.  That kernel must not write the workspace; with a.q_early it must not
+// stream.  That kernel must not write the workspace; with a.after_append it must not
 // write q either (the decode-step append), else it may be anything (the ticket
 // clearing kernel, which completes only after the kernels before it).
-template <int KB, bool KP, int VB, bool VP>
-int launch_split_mma(const SplitArgs& a, dim3 grid, bool pdl, cudaStream_t s) {
+template <int KB, bool KP, int VB, bool VP, bool AA>
+int launch_split_mma_aa(const SplitArgs& a, dim3 grid, bool pdl, cudaStream_t s) {
     using SM = Smem<KB, KP, VB, VP>;
     static_assert(SM::kBytes <= 232448 - 1024, "decode shared memory above the per-CTA limit");
-    auto fn = decode_split_mma_kernel<KB, KP, VB, VP>;
+    auto fn = decode_split_mma_kernel<KB, KP, VB, VP, AA>;
     static std::atomic<uint64_t> smem_set{0};
     const int rc = ensure_smem_attr(smem_set, (const void*)fn, (int)SM::kBytes, "decode (tensor-core) smem attribute");
     if (rc != TQ_OK) return rc;
@@ -1288,6 +1338,13 @@ int launch_split_mma(const SplitArgs& a, dim3 grid, bool pdl, cudaStream_t s) {
     cfg.numAttrs = pdl ? 1 : 0;
     const cudaError_t e = cudaLaunchKernelEx(&cfg, fn, a);
     return e == cudaSuccess ? TQ_OK : cuda_fail(e, "decode (tensor-core) split launch");
+}
+
+template <int KB, bool KP, int VB, bool VP>
+int launch_split_mma(const SplitArgs& a, dim3 grid, bool pdl, cudaStream_t s) {
+    if (a.after_append && (a.T_max & 3) == 0 && a.chunk >= kAppendStreamChunk)
+        return launch_split_mma_aa<KB, KP, VB, VP, true>(a, grid, pdl, s);
+    return launch_split_mma_aa<KB, KP, VB, VP, false>(a, grid, pdl, s);
 }
 
 // Values dispatched at run time for one key configuration (see tq_decode_args.h).

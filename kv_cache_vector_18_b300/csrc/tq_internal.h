@@ -183,9 +183,17 @@ int launch_select_outlier_channels(const void* x, int x_dtype, int64_t n_rows, i
 // Decode-step append (tq_append.cu): quantize the new K and V rows [B·Hkv, d] into
 // the next free token of each (batch, KV head) slab; the launch's last block then
 // bumps the lengths and zeroes the decode's n_tickets merge tickets (if any).
+// Behind the decode-step append, decode CTAs of at least this many tokens stream
+// their rows below the pre-append length before waiting for the append, and the
+// append runs on the SMs the decode grid leaves free when they suffice.  With
+// shorter chunks the append would still be running when the CTAs finish that
+// prefix, and the streaming only slows it down.
+constexpr int kAppendStreamChunk = 4096;
+// decode_ctas, decode_chunk: CTAs and tokens per CTA of the decode launched after
+// the append (decode_split_ctas, the plan's chunk), which choose the append's grid.
 int launch_append(const tq_ctx& hk, const tq_ctx& hv, const void* k_new, const void* v_new, int x_dtype, int B,
                   int Hkv, int T_max, int32_t* lens, const tq_planes& kc, const tq_planes& vc, int* tickets,
-                  int n_tickets, cudaStream_t s);
+                  int n_tickets, int64_t decode_ctas, int decode_chunk, cudaStream_t s);
 int launch_quantize_tc(const tq_ctx& h, const void* x, int x_dtype, int64_t n_rows, int64_t x_row_stride,
                        const tq_planes& out, cudaStream_t s);
 // Two mse quantizers (same d ∈ {64, 128}, b, rotation kind) in one tensor-core launch.
@@ -211,5 +219,7 @@ int launch_decode(const tq_ctx& hk, const tq_ctx& hv, const DecodeShape& plan, c
                   void* workspace, cudaStream_t s, bool tickets_zeroed = false);
 // The merge tickets of a decode workspace: where they lie and how many there are.
 int* decode_tickets(const tq_ctx& hv, const DecodeShape& plan, void* workspace, int* count);
+// CTAs of the split kernel of this plan.
+int64_t decode_split_ctas(const DecodeShape& plan);
 
 }  // namespace tq

@@ -87,6 +87,48 @@ def test_append_step(tq, kv, kb, vv, vb):
     assert kq.device_status() == 0
 
 
+@pytest.mark.parametrize("kv,kb,vv,vb", [("prod", 3, "mse", 3), ("mse", 3, "mse", 3)])
+def test_append_long_context_streams_stable_prefix(tq, kv, kb, vv, vb):
+    # 131072-token slabs: the decode's CTAs take chunks long enough to stream
+    # their rows below the pre-append length before waiting for the append, and
+    # the append runs on the SMs the decode grid leaves free.  Checked: the
+    # appended rows against the oracle, the output bit for bit against the plain
+    # decode over the updated cache (same plan, same arithmetic), and five steps
+    # enqueued without synchronisation against the same steps synchronised one
+    # by one.
+    B, Hq, Hkv, T, d = 1, 64, 8, 131072, 128
+    kq = tq.Quantizer(d, kb, kv, seed=31)
+    vq = tq.Quantizer(d, vb, vv, seed=32)
+    kc = kq.quantize(synthetic.gaussian_cuda((B * Hkv * T, d), seed=33))
+    vc = vq.quantize(synthetic.gaussian_cuda((B * Hkv * T, d), seed=34))
+    sl = torch.tensor([T - 100], dtype=torch.int32, device="cuda")
+    new = [(synthetic.gaussian((B, Hkv, d), seed=200 + i), synthetic.gaussian((B, Hkv, d), seed=300 + i),
+            synthetic.gaussian((B, Hq, d), seed=400 + i)) for i in range(6)]
+    kn, vn, qn = new[0]
+    out = tq.decode_append_attention(kq, vq, qn.cuda(), kn.cuda(), vn.cuda(), kc, vc, sl, Hkv, T)
+    plain = tq.decode_attention(kq, vq, qn.cuda(), kc, vc, sl, Hkv, T)
+    torch.cuda.synchronize()
+    assert sl.tolist() == [T - 99]
+    assert torch.equal(out, plain)
+    dst = [h * T + T - 100 for h in range(Hkv)]
+    check_quantize(oracle_params(kq), f64(kn.reshape(-1, d)), _rows(kc, dst))
+    check_quantize(oracle_params(vq), f64(vn.reshape(-1, d)), _rows(vc, dst))
+    kc0, vc0, sl0 = _clone(kc), _clone(vc), sl.clone()
+    dev = [(k.cuda(), v.cuda(), q.cuda()) for k, v, q in new[1:]]
+    torch.cuda.synchronize()
+    free = [tq.decode_append_attention(kq, vq, q, k, v, kc, vc, sl, Hkv, T) for k, v, q in dev]
+    torch.cuda.synchronize()
+    for i, (k, v, q) in enumerate(dev):
+        ref = tq.decode_append_attention(kq, vq, q, k, v, kc0, vc0, sl0, Hkv, T)
+        torch.cuda.synchronize()
+        assert torch.equal(free[i], ref), i
+    assert torch.equal(sl, sl0) and sl.tolist() == [T - 94]
+    for a_, b_ in ((kc, kc0), (vc, vc0)):
+        for name in a_:
+            assert torch.equal(a_[name], b_[name]), name
+    assert kq.device_status() == 0
+
+
 @pytest.mark.parametrize("d", [64, 256])
 def test_append_other_head_dims_and_fp32_rows(tq, d):
     B, Hq, Hkv, T = 2, 8, 2, 200
