@@ -129,6 +129,31 @@ def test_append_long_context_streams_stable_prefix(tq, kv, kb, vv, vb):
     assert kq.device_status() == 0
 
 
+def test_append_long_context_ragged_and_full(tq):
+    # as above with two ragged slabs and a full one in the batch: chunks that end
+    # before a slab's length, one that holds it, ones past it, and a slab that
+    # takes no row (its status flagged, its length unchanged)
+    B, Hq, Hkv, T, d = 3, 64, 8, 65536, 128
+    kq = tq.Quantizer(d, 3, "prod", seed=41)
+    vq = tq.Quantizer(d, 3, "mse", seed=42)
+    kc = kq.quantize(synthetic.gaussian_cuda((B * Hkv * T, d), seed=43))
+    vc = vq.quantize(synthetic.gaussian_cuda((B * Hkv * T, d), seed=44))
+    lens0 = [65000, 30001, T]
+    sl = torch.tensor(lens0, dtype=torch.int32, device="cuda")
+    kn, vn, qn = (synthetic.gaussian((B, Hkv, d), seed=45), synthetic.gaussian((B, Hkv, d), seed=46),
+                  synthetic.gaussian((B, Hq, d), seed=47))
+    out = tq.decode_append_attention(kq, vq, qn.cuda(), kn.cuda(), vn.cuda(), kc, vc, sl, Hkv, T)
+    plain = tq.decode_attention(kq, vq, qn.cuda(), kc, vc, sl, Hkv, T)
+    torch.cuda.synchronize()
+    assert sl.tolist() == [65001, 30002, T]
+    assert torch.equal(out, plain)
+    assert kq.device_status(clear=True) == _lib_status()
+    src = [b * Hkv + h for b in range(2) for h in range(Hkv)]
+    dst = [(b * Hkv + h) * T + lens0[b] for b in range(2) for h in range(Hkv)]
+    check_quantize(oracle_params(kq), f64(kn.reshape(-1, d))[src], _rows(kc, dst))
+    check_quantize(oracle_params(vq), f64(vn.reshape(-1, d))[src], _rows(vc, dst))
+
+
 @pytest.mark.parametrize("d", [64, 256])
 def test_append_other_head_dims_and_fp32_rows(tq, d):
     B, Hq, Hkv, T = 2, 8, 2, 200
