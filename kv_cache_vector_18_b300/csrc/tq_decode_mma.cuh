@@ -773,6 +773,167 @@ __device__ __forceinline__ void step(Acc<VP>& st, const unsigned char* stp, int 
     }
 }
 
+// The step for at most four query heads per KV head (G4).  With [Q′_hi; Q′_lo] as
+// the A operand, four heads would fill only half of the MMA's 16 rows; here the
+// keys (and the QJL signs) are the A operand instead, 16 tokens × 16 dims, and
+// the queries the B operand, 8 columns (head h: Q′_hi in column 2h, Q′_lo in
+// 2h + 1), so each k16 block is one MMA for the whole tile instead of two.  Lane
+// (g, c) ends with head c's scores of tokens g and g + 8 (the two columns of head
+// c are the lane's accumulator pair).  The softmax weights are gathered into the
+// token × head tile that movmatrix transposes into the B fragment of the value
+// MMA, which is unchanged.  BQ[kb], BS[kb]: this lane's B fragments (column g).
+template <int KB, bool KP, int VB, bool VP, bool FULL>
+__device__ __forceinline__ void step4(Acc<VP>& st, const unsigned char* stp, int r0, int tb, int t1,
+                                      const KDecoder<KB>& dk, const Decoder<VB>& dv, const SignDecoder& ds,
+                                      uint32_t stab, const uint32_t (&BQ)[kKB][2], const uint32_t (&BS)[kKB][2],
+                                      float fK, float fS, const SplitArgs& a, size_t head0, int G, int g, int c) {
+    using ST = Stage<KB, KP, VB, VP>;
+    // accumulators: [0] token g column 2c (hi), [1] token g column 2c + 1 (lo),
+    // [2], [3] the same for token g + 8; even and odd k16 blocks in two chains
+    float S1[4] = {0.f, 0.f, 0.f, 0.f}, S1x[4] = {0.f, 0.f, 0.f, 0.f};
+    float S2[4] = {0.f, 0.f, 0.f, 0.f}, S2x[4] = {0.f, 0.f, 0.f, 0.f};
+    if constexpr (KB > 0) {
+        uint32_t w0[KB], w1[KB];
+        read_words<KB>(w0, stp + ST::kKC + (r0 + g) * ST::kRK + c * (KB * 4));
+        read_words<KB>(w1, stp + ST::kKC + (r0 + 8 + g) * ST::kRK + c * (KB * 4));
+#pragma unroll
+        for (int kb = 0; kb < kKB; ++kb) {
+            // a token's B fragment of the other orientation is its row of the A fragment
+            uint32_t a0, a1, a2, a3;
+            dk.frag(w0, kb, a0, a2);
+            dk.frag(w1, kb, a1, a3);
+            mma16816((kb & 1) ? S1x : S1, a0, a1, a2, a3, BQ[kb][0], BQ[kb][1]);
+        }
+    }
+    if constexpr (KP) {
+        const uint32_t ws0 = *reinterpret_cast<const uint32_t*>(stp + ST::kKS + (r0 + g) * 16 + c * 4);
+        const uint32_t ws1 = *reinterpret_cast<const uint32_t*>(stp + ST::kKS + (r0 + 8 + g) * 16 + c * 4);
+#pragma unroll
+        for (int j = 0; j < kKB / 2; ++j) {
+            const uint4 f0 = lds128(field_off<8, 7>(&ws0, 8 * j) | stab);
+            const uint4 f1 = lds128(field_off<8, 7>(&ws1, 8 * j) | stab);
+            mma16816(S2, f0.x, f1.x, f0.y, f1.y, BS[2 * j][0], BS[2 * j][1]);
+            mma16816(S2x, f0.z, f1.z, f0.w, f1.w, BS[2 * j + 1][0], BS[2 * j + 1][1]);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        S1[i] += S1x[i];
+        S2[i] += S2x[i];
+    }
+    // this lane's tokens: i = 0 → g, i = 1 → g + 8
+    auto norm2 = [&](int off, float (&v)[2]) {
+        v[0] = *reinterpret_cast<const float*>(stp + off + 4 * (r0 + g));
+        v[1] = *reinterpret_cast<const float*>(stp + off + 4 * (r0 + 8 + g));
+    };
+    float kn[2], vn[2], kr[2];
+    norm2(ST::kKN, kn);
+    norm2(ST::kVN, vn);
+    if constexpr (KP) norm2(ST::kKR, kr);
+    float z[2], lv[2], rv[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const float vv = fmaxf(vn[i], 1e-30f);
+        lv[i] = lg2(vv);
+        rv[i] = rcp(vv);
+        float v = fK * (S1[2 * i] + S1[2 * i + 1]);
+        if constexpr (KP) v = fmaf(fS * kr[i], S2[2 * i] + S2[2 * i + 1], v);
+        z[i] = fmaf(kn[i], v, lv[i]);
+        if constexpr (!FULL)
+            if (tb + g + 8 * i >= t1) z[i] = -INFINITY;
+    }
+    if (a.scores != nullptr && c < G) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int t = tb + g + 8 * i;
+            if (FULL || t < t1) a.scores[(head0 + c) * a.T_max + t] = (z[i] - lv[i]) * kLn2;
+        }
+    }
+
+    // ---- online softmax of head c (shared by the eight lanes with this c)
+    const float zm = fmaxf(z[0], z[1]);
+    if (__any_sync(0xffffffffu, zm > st.Mt)) {
+        float mx = fmaxf(zm, __shfl_xor_sync(0xffffffffu, zm, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        const float Mn = fmaxf(st.M, mx);
+        const float corr = Mn == -INFINITY ? 1.f : ex2(st.M - Mn);  // 0 on the first raise (M = −∞)
+        st.M = Mn;
+        st.Mt = Mn + kSlack;
+        st.l *= corr;
+        // the value accumulators hold heads 2c and 2c + 1 (lanes 2c and 2c + 1 keep their
+        // state); for c ≥ 2 they hold no head and stay zero
+        const float cA = __shfl_sync(0xffffffffu, corr, 2 * c), cB = __shfl_sync(0xffffffffu, corr, 2 * c + 1);
+#pragma unroll
+        for (int m = 0; m < kMT; ++m) {
+            st.O[m][0] *= cA;
+            st.O[m][1] *= cB;
+            st.O[m][2] *= cA;
+            st.O[m][3] *= cB;
+            if constexpr (VP) {
+                st.O2[m][0] *= cA;
+                st.O2[m][1] *= cB;
+                st.O2[m][2] *= cA;
+                st.O2[m][3] *= cB;
+            }
+        }
+    }
+    float pv[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        pv[i] = ex2(z[i] - st.M);
+        st.l = fmaf(pv[i], rv[i], st.l);
+    }
+    // token × head tile X (block 0: tokens 0–7, block 1: 8–15): lane (g, c) holds
+    // X[g][2c], X[g][2c + 1], the weights of heads 2c and 2c + 1 for token g (lanes
+    // (g, 2c) and (g, 2c + 1)), zero for c ≥ 2; its transpose gives lane (g, c) head
+    // g's weights of tokens 2c, 2c + 1 — the value MMA's B fragment
+    const int srcA = 4 * g + ((2 * c) & 3), srcB = 4 * g + ((2 * c + 1) & 3);
+    auto to_b = [&](float x) -> uint32_t {
+        const float xa = __shfl_sync(0xffffffffu, x, srcA), xb = __shfl_sync(0xffffffffu, x, srcB);
+        return mov_trans(c < 2 ? pack_h2(xa, xb) : 0u);
+    };
+    const uint32_t PB0 = to_b(pv[0]);
+    const uint32_t PB1 = to_b(pv[1]);
+
+    // ---- values: Oᵀ += Ṽᵀ·P′ᵀ in the rotated frame (as in step)
+    if constexpr (VB > 0) {
+        uint32_t vwA[VB], vwB[VB];
+        read_words<VB>(vwA, stp + ST::kVC + (r0 + g) * ST::kRV + c * (VB * 4));
+        read_words<VB>(vwB, stp + ST::kVC + (r0 + g + 8) * ST::kRV + c * (VB * 4));
+#pragma unroll
+        for (int m = 0; m < kMT; ++m) {
+            uint32_t x0, x1, y0, y1;
+            dv.pairs(vwA, m, x0, x1);
+            dv.pairs(vwB, m, y0, y1);
+            mma16816(st.O[m], mov_trans(x0), mov_trans(x1), mov_trans(y0), mov_trans(y1), PB0, PB1);
+        }
+    }
+    if constexpr (VP) {
+        float vr[2];
+        norm2(ST::kVR, vr);
+        if constexpr (!FULL) {
+            // rows past the chunk may hold anything (bulk staging copies whole tiles)
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+                if (tb + g + 8 * i >= t1) vr[i] = 0.f;
+        }
+        const uint32_t QB0 = to_b(pv[0] * a.vgamma * vr[0]);
+        const uint32_t QB1 = to_b(pv[1] * a.vgamma * vr[1]);
+        const uint32_t vsA = *reinterpret_cast<const uint32_t*>(stp + ST::kVS + (r0 + g) * 16 + c * 4);
+        const uint32_t vsB = *reinterpret_cast<const uint32_t*>(stp + ST::kVS + (r0 + g + 8) * 16 + c * 4);
+#pragma unroll
+        for (int m = 0; m < kMT / 2; ++m) {
+            uint32_t pa[4], pb[4];
+            ds.quad(vsA, m, pa);
+            ds.quad(vsB, m, pb);
+            mma16816(st.O2[2 * m], mov_trans(pa[0]), mov_trans(pa[1]), mov_trans(pb[0]), mov_trans(pb[1]), QB0, QB1);
+            mma16816(st.O2[2 * m + 1], mov_trans(pa[2]), mov_trans(pa[3]), mov_trans(pb[2]), mov_trans(pb[3]), QB0,
+                     QB1);
+        }
+    }
+}
+
 // Last CTA of a (batch, KV head, head block) group: combine the n_splits
 // partials of its G heads and write out = Π_vᵀ·acc/l (+ S_vᵀ·acc2/l).
 template <int KB, bool KP, int VB, bool VP>
@@ -910,7 +1071,8 @@ __device__ __forceinline__ void merge_group(const SplitArgs& a, unsigned char* s
 // AA: launched behind the decode-step append (a.after_append), which writes no
 // cache row below the length it starts from: the stages wholly below that
 // length are streamed and consumed before griddepcontrol.wait.
-template <int KB, bool KP, int VB, bool VP, bool AA>
+// G4: at most four query heads per KV head, stepped by step4.
+template <int KB, bool KP, int VB, bool VP, bool AA, bool G4>
 __global__ void __launch_bounds__((Warps<VP>::value + 1) * 32, 1) decode_split_mma_kernel(const SplitArgs a) {
     using SM = Smem<KB, KP, VB, VP>;
     using ST = Stage<KB, KP, VB, VP>;
@@ -1139,22 +1301,25 @@ __global__ void __launch_bounds__((Warps<VP>::value + 1) * 32, 1) decode_split_m
         consumers_sync();
 
         if constexpr (!AA) read_length();
-        // A fragments of head g: [Q′_hi; Q′_lo] for the codes and [Q″_hi; Q″_lo] for
-        // the QJL signs, k order following the key decoders' dims
+        // A fragments of head hq = g: [Q′_hi; Q′_lo] for the codes and [Q″_hi; Q″_lo]
+        // for the QJL signs, k order following the key decoders' dims.  G4: the same
+        // pairs of head hq = g / 2, of which column g of step4's B operand takes the
+        // high (g even) or low (g odd) halves.
+        const int hq = G4 ? (g >> 1) : g;
         uint32_t AQ[kKB][4], AS[kKB][4];
         {
-            const float i1 = 1.f / qsc[g], i2 = 1.f / qsc[kHeads + g];
-            // this lane's 32 dims of q′ (and q″): chunk c of head g, eight 16-byte loads
+            const float i1 = 1.f / qsc[hq], i2 = 1.f / qsc[kHeads + hq];
+            // this lane's 32 dims of q′ (and q″): chunk c of head hq, eight 16-byte loads
             float q1[32], q2[32];
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
-                const float4 u = *reinterpret_cast<const float4*>(qsh + qidx(g, 32 * c) + 4 * k);
+                const float4 u = *reinterpret_cast<const float4*>(qsh + qidx(hq, 32 * c) + 4 * k);
                 q1[4 * k] = u.x;
                 q1[4 * k + 1] = u.y;
                 q1[4 * k + 2] = u.z;
                 q1[4 * k + 3] = u.w;
                 if constexpr (KP) {
-                    const float4 v = *reinterpret_cast<const float4*>(qsh + kHeads * kQRow + qidx(g, 32 * c) + 4 * k);
+                    const float4 v = *reinterpret_cast<const float4*>(qsh + kHeads * kQRow + qidx(hq, 32 * c) + 4 * k);
                     q2[4 * k] = v.x;
                     q2[4 * k + 1] = v.y;
                     q2[4 * k + 2] = v.z;
@@ -1185,10 +1350,22 @@ __global__ void __launch_bounds__((Warps<VP>::value + 1) * 32, 1) decode_split_m
                 }
             }
         }
-        // score factors of head g, log2 units
+        uint32_t BQ[G4 ? kKB : 1][2], BS[G4 ? kKB : 1][2];
+        if constexpr (G4) {
+            const bool lo = g & 1;
+#pragma unroll
+            for (int kb = 0; kb < kKB; ++kb) {
+                BQ[kb][0] = lo ? AQ[kb][1] : AQ[kb][0];
+                BQ[kb][1] = lo ? AQ[kb][3] : AQ[kb][2];
+                BS[kb][0] = lo ? AS[kb][1] : AS[kb][0];
+                BS[kb][1] = lo ? AS[kb][3] : AS[kb][2];
+            }
+        }
+        // score factors of this lane's head (g; G4: c), log2 units
+        const int hs = G4 ? c : g;
         const float scale2 = a.scale * kLog2e;
-        const float fK = scale2 * qsc[g] / a.kcb.lut_scale;
-        const float fS = scale2 * a.kgamma * qsc[kHeads + g];
+        const float fK = scale2 * qsc[hs] / a.kcb.lut_scale;
+        const float fS = scale2 * a.kgamma * qsc[kHeads + hs];
         KDecoder<KB> dk;
         Decoder<VB> dv;
         dk.init(a.kcb, mp + SM::kTabK, lane);
@@ -1211,7 +1388,12 @@ __global__ void __launch_bounds__((Warps<VP>::value + 1) * 32, 1) decode_split_m
                 }
                 const int tb = t0 + tile * kTile, r0 = (tile % kTilesPerStage) * kTile;
                 const unsigned char* stp = mp + SM::kStage + (size_t)slot * ST::kBytes;
-                step<KB, KP, VB, VP, true>(st, stp, r0, tb, tlim, dk, dv, ds, stab, AQ, AS, fK, fS, a, head0, G, g, c);
+                if constexpr (G4)
+                    step4<KB, KP, VB, VP, true>(st, stp, r0, tb, tlim, dk, dv, ds, stab, BQ, BS, fK, fS, a, head0, G, g,
+                                                c);
+                else
+                    step<KB, KP, VB, VP, true>(st, stp, r0, tb, tlim, dk, dv, ds, stab, AQ, AS, fK, fS, a, head0, G, g,
+                                               c);
                 __syncwarp();
                 if (lane == 0) sm100::mbar_arrive(&s_empty[slot]);
             }
@@ -1225,18 +1407,33 @@ __global__ void __launch_bounds__((Warps<VP>::value + 1) * 32, 1) decode_split_m
             if (!__all_sync(0xffffffffu, ok)) break;  // the warp gives up together
             const int tb = t0 + tile * kTile, r0 = (tile % kTilesPerStage) * kTile;
             const unsigned char* stp = mp + SM::kStage + (size_t)slot * ST::kBytes;
-            if (tb + kTile <= t1)
-                step<KB, KP, VB, VP, true>(st, stp, r0, tb, t1, dk, dv, ds, stab, AQ, AS, fK, fS, a, head0, G, g, c);
-            else
-                step<KB, KP, VB, VP, false>(st, stp, r0, tb, t1, dk, dv, ds, stab, AQ, AS, fK, fS, a, head0, G, g, c);
+            if constexpr (G4) {
+                if (tb + kTile <= t1)
+                    step4<KB, KP, VB, VP, true>(st, stp, r0, tb, t1, dk, dv, ds, stab, BQ, BS, fK, fS, a, head0, G, g, c);
+                else
+                    step4<KB, KP, VB, VP, false>(st, stp, r0, tb, t1, dk, dv, ds, stab, BQ, BS, fK, fS, a, head0, G, g,
+                                                 c);
+            } else {
+                if (tb + kTile <= t1)
+                    step<KB, KP, VB, VP, true>(st, stp, r0, tb, t1, dk, dv, ds, stab, AQ, AS, fK, fS, a, head0, G, g, c);
+                else
+                    step<KB, KP, VB, VP, false>(st, stp, r0, tb, t1, dk, dv, ds, stab, AQ, AS, fK, fS, a, head0, G, g, c);
+            }
             __syncwarp();  // every lane has read the tile before the stage is released
             if (lane == 0) sm100::mbar_arrive(&s_empty[slot]);
         }
     }
 
-    // ---- combine the warps of this CTA into one split partial per head
-    st.l += __shfl_xor_sync(0xffffffffu, st.l, 1);
-    st.l += __shfl_xor_sync(0xffffffffu, st.l, 2);
+    // ---- combine the warps of this CTA into one split partial per head (the lanes
+    // holding a head's sum: the quad g, or with G4 the eight lanes of one c)
+    if constexpr (G4) {
+        st.l += __shfl_xor_sync(0xffffffffu, st.l, 4);
+        st.l += __shfl_xor_sync(0xffffffffu, st.l, 8);
+        st.l += __shfl_xor_sync(0xffffffffu, st.l, 16);
+    } else {
+        st.l += __shfl_xor_sync(0xffffffffu, st.l, 1);
+        st.l += __shfl_xor_sync(0xffffffffu, st.l, 2);
+    }
     __syncthreads();  // tables, queries and rings are dead from here on
     float* wM = reinterpret_cast<float*>(smem + SM::kWM);    // [warp][head] running maxima
     float* wL = reinterpret_cast<float*>(smem + SM::kWL);    // [warp][head] sums
@@ -1246,7 +1443,12 @@ __global__ void __launch_bounds__((Warps<VP>::value + 1) * 32, 1) decode_split_m
     // accumulators in fragment order: each store is 32 consecutive words
     constexpr int kFrag = kMT * 4 * 32;
     if (!producer) {
-        if (c == 0) {
+        if constexpr (G4) {  // heads c from lanes g = 0; heads 4–7 (none) from lanes g = 1
+            if (g < 2) {
+                wM[warp * kHeads + 4 * g + c] = g == 0 ? st.M : -INFINITY;
+                wL[warp * kHeads + 4 * g + c] = g == 0 ? st.l : 0.f;
+            }
+        } else if (c == 0) {
             wM[warp * kHeads + g] = st.M;
             wL[warp * kHeads + g] = st.l;
         }
@@ -1318,11 +1520,11 @@ __global__ void __launch_bounds__((Warps<VP>::value + 1) * 32, 1) decode_split_m
 // stream.  That kernel must not write the workspace; with a.after_append it must not
 // write q either (the decode-step append), else it may be anything (the ticket
 // clearing kernel, which completes only after the kernels before it).
-template <int KB, bool KP, int VB, bool VP, bool AA>
-int launch_split_mma_aa(const SplitArgs& a, dim3 grid, bool pdl, cudaStream_t s) {
+template <int KB, bool KP, int VB, bool VP, bool AA, bool G4>
+int launch_split_mma_v(const SplitArgs& a, dim3 grid, bool pdl, cudaStream_t s) {
     using SM = Smem<KB, KP, VB, VP>;
     static_assert(SM::kBytes <= 232448 - 1024, "decode shared memory above the per-CTA limit");
-    auto fn = decode_split_mma_kernel<KB, KP, VB, VP, AA>;
+    auto fn = decode_split_mma_kernel<KB, KP, VB, VP, AA, G4>;
     static std::atomic<uint64_t> smem_set{0};
     const int rc = ensure_smem_attr(smem_set, (const void*)fn, (int)SM::kBytes, "decode (tensor-core) smem attribute");
     if (rc != TQ_OK) return rc;
@@ -1342,9 +1544,11 @@ int launch_split_mma_aa(const SplitArgs& a, dim3 grid, bool pdl, cudaStream_t s)
 
 template <int KB, bool KP, int VB, bool VP>
 int launch_split_mma(const SplitArgs& a, dim3 grid, bool pdl, cudaStream_t s) {
-    if (a.after_append && (a.T_max & 3) == 0 && a.chunk >= kAppendStreamChunk)
-        return launch_split_mma_aa<KB, KP, VB, VP, true>(a, grid, pdl, s);
-    return launch_split_mma_aa<KB, KP, VB, VP, false>(a, grid, pdl, s);
+    const bool aa = a.after_append && (a.T_max & 3) == 0 && a.chunk >= kAppendStreamChunk, g4 = a.G <= 4;
+    if (g4) return aa ? launch_split_mma_v<KB, KP, VB, VP, true, true>(a, grid, pdl, s)
+                      : launch_split_mma_v<KB, KP, VB, VP, false, true>(a, grid, pdl, s);
+    return aa ? launch_split_mma_v<KB, KP, VB, VP, true, false>(a, grid, pdl, s)
+              : launch_split_mma_v<KB, KP, VB, VP, false, false>(a, grid, pdl, s);
 }
 
 // Values dispatched at run time for one key configuration (see tq_decode_args.h).
