@@ -129,11 +129,12 @@ def test_append_long_context_streams_stable_prefix(tq, kv, kb, vv, vb):
     assert kq.device_status() == 0
 
 
-def test_append_long_context_ragged_and_full(tq):
+@pytest.mark.parametrize("Hq", [64, 32])  # 8 query heads per KV head, and 4 (the keys-as-A step)
+def test_append_long_context_ragged_and_full(tq, Hq):
     # as above with two ragged slabs and a full one in the batch: chunks that end
     # before a slab's length, one that holds it, ones past it, and a slab that
     # takes no row (its status flagged, its length unchanged)
-    B, Hq, Hkv, T, d = 3, 64, 8, 65536, 128
+    B, Hkv, T, d = 3, 8, 65536, 128
     kq = tq.Quantizer(d, 3, "prod", seed=41)
     vq = tq.Quantizer(d, 3, "mse", seed=42)
     kc = kq.quantize(synthetic.gaussian_cuda((B * Hkv * T, d), seed=43))
