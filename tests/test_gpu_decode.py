@@ -112,6 +112,21 @@ def test_scores_output_small_config(tq):
     assert np.max(np.abs(gs - rs)) <= 1e-3 * max(1.0, np.max(np.abs(rs)))
 
 
+@pytest.mark.parametrize("Hq,Hkv,T,lens,vv", [
+    (8, 2, 1002, [1002, 517], "mse"),    # four query heads per KV head, per-lane staging (T % 4 != 0)
+    (6, 2, 1000, [999, 20], "prod"),      # three, bulk staging, prod values
+    (2, 2, 701, [701, 1], "mse"),         # one
+])
+def test_scores_output_small_groups(tq, Hq, Hkv, T, lens, vv):
+    # pre-softmax scores and outputs of the keys-as-A step (at most four query heads
+    # per KV head), fp32 queries, ragged tails
+    g, r, gs, rs = _run(tq, B=2, Hq=Hq, Hkv=Hkv, T=T, d=128, kb=3, kv="prod", vb=3, vv=vv, lens=lens,
+                        q_dtype="f32", return_scores=True, seed=Hq + T)
+    check_attention(g, r)
+    for b, L in enumerate(lens):
+        assert np.max(np.abs(gs[b, :, :L] - rs[b, :, :L])) <= 1e-3 * max(1.0, np.max(np.abs(rs[b, :, :L])))
+
+
 def test_decode_workspace_too_small(tq):
     from kv_cache_vector_18_b300 import _lib
     kq = tq.Quantizer(128, 3, "prod", seed=1)
