@@ -312,10 +312,10 @@ int tq_mixed_decode_workspace_bytes(tq_handle hko, tq_handle hkn, tq_handle hvo,
  * B·Hkv·T_max records each, ordered [B][Hkv][T_max].  Other arguments as
  * tq_decode_attention; bad perm entries are recorded in hko's status word.
  * The split of the page's experiment — d = 128, 32 outlier channels for keys
- * and for values, mse parts with (b_o, b_n) ∈ {(3, 2), (4, 3), (4, 2)} alike for
- * keys and values — and T_max % 4 == 0 run on a tensor-core kernel (staging and
- * merge waits record codes 30 and 31 in hko's status word); every other split on
- * CUDA-core kernels.  The workspace size depends on which (the size query
+ * and for values, mse value parts with (b_o, b_n) ∈ {(3, 2), (4, 3), (4, 2)} and
+ * key parts of the same bits, both mse or both prod — and T_max % 4 == 0 run on a
+ * tensor-core kernel (staging and merge waits record codes 30 and 31 in hko's
+ * status word); every other split on CUDA-core kernels.  The workspace size depends on which (the size query
  * answers for the same handles and T_max).
  */
 int tq_mixed_decode_attention(tq_handle hko, tq_handle hkn, tq_handle hvo, tq_handle hvn,

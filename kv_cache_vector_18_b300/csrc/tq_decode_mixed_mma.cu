@@ -20,6 +20,12 @@
 // outlier part and tiles 2–7 the rest, each weighted by its own value norm.
 // The softmax exponent carries log2 of the larger of a token's two value norms,
 // so both parts' f16 weights stay below 2^kSlack.
+//
+// Prod key parts (KP) add each part's QJL term to its score,
+// √(π/2)/d_p·‖k_p‖·‖r_p‖·⟨q″_p, z_p⟩ with q″ = blockdiag(S_o, S_n)·P·q: the signs are
+// the B operand of a second set of MMAs over the same k16 blocks (lane c takes
+// signs 8c … 8c + 7 of the outlier part, one byte, and 24c … 24c + 23 of the rest,
+// three bytes, the same dims as its codes), with [Q″_hi; Q″_lo] as A.
 #include "tq_decode_mma.cuh"
 #include "tq_mixed_decode.h"
 
@@ -30,6 +36,7 @@ namespace {
 constexpr int kDO = 32;        // outlier dims of the frame
 constexpr int kDN = D - kDO;   // the rest
 constexpr int kMW = 11;        // consumer warps (plus one producer warp)
+constexpr int kMWP = 7;        // with prod key parts (more registers per lane)
 
 // Bits [c·NB·8·LEN/8 …) of a row: lane c's run of LEN codes of NB bits, returned
 // as NW words (LSB first).  The row starts on a 4-byte boundary; the read may run
@@ -50,7 +57,7 @@ __device__ __forceinline__ void lane_run(const unsigned char* row, int c, uint32
 
 // Byte layout of one 64-token stage: code planes, then norm planes, of keys then
 // values (each plane's rows contiguous).
-template <int KO, int KN, int VO, int VN>
+template <int KO, int KN, int VO, int VN, bool KP = false>
 struct MStage {
     static constexpr int R = kStageRows;
     static constexpr int kRKo = kDO * KO / 8, kRKn = kDN * KN / 8, kRVo = kDO * VO / 8, kRVn = kDN * VN / 8;
@@ -62,8 +69,13 @@ struct MStage {
     static constexpr int kVNC = kVOC + R * kRVo;
     static constexpr int kVON = kVNC + R * kRVn;
     static constexpr int kVNN = kVON + R * 4;
-    static constexpr int kBytes = kVNN + R * 4;
-    static constexpr int kRowBytes = kRKo + kRKn + kRVo + kRVn + 16;
+    // prod keys: the parts' sign rows (32 and 96 signs) and residual norms
+    static constexpr int kKOS = kVNN + R * 4;
+    static constexpr int kKNS = kKOS + (KP ? R * 4 : 0);
+    static constexpr int kKOR = kKNS + (KP ? R * 12 : 0);
+    static constexpr int kKNR = kKOR + (KP ? R * 4 : 0);
+    static constexpr int kBytes = kKNR + (KP ? R * 4 : 0);
+    static constexpr int kRowBytes = kRKo + kRKn + kRVo + kRVn + 16 + (KP ? 24 : 0);
     static_assert(kRowBytes * R == kBytes, "stage layout");
     static_assert(kRKo % 4 == 0 && kRKn % 4 == 0 && kRVo % 4 == 0 && kRVn % 4 == 0, "code rows of whole words");
 };
@@ -71,14 +83,17 @@ struct MStage {
 // Shared memory: four decode tables (each at a multiple of its power-of-two
 // size), rotated and raw queries, the staging ring; then the combine and merge
 // phases reuse the bytes.
-template <int KO, int KN, int VO, int VN>
+template <int KO, int KN, int VO, int VN, bool KP = false>
 struct MSmem {
-    static constexpr int W = kMW;
+    static constexpr int W = KP ? kMWP : kMW;
     static constexpr int kThreads = (W + 1) * 32;
     static constexpr size_t kSz[4] = {Table<KO>::kBytes, Table<KN>::kBytes, Table<VO>::kBytes, Table<VN>::kBytes};
     static constexpr size_t kBig = 32768;
+    static constexpr size_t kTabS = 0;  // the QJL sign table (prod keys, 32 KB) comes first
+    static constexpr size_t kSgn = KP ? KSignTable::kBytes : 0;
+    static_assert(KSignTable::kBytes == kBig, "sign table size");
     static constexpr size_t table_offset(int which) {  // the 32 KB tables first, then the others
-        size_t off = 0;
+        size_t off = kSgn;
         for (int pass = 0; pass < 2; ++pass)
             for (int i = 0; i < 4; ++i)
                 if ((pass == 0) == (kSz[i] == kBig)) {
@@ -89,18 +104,20 @@ struct MSmem {
     }
     static constexpr size_t kTabKO = table_offset(0), kTabKN = table_offset(1), kTabVO = table_offset(2),
                             kTabVN = table_offset(3);
-    static constexpr size_t kQ = kSz[0] + kSz[1] + kSz[2] + kSz[3];  // [kHeads][D] q′ (fp32)
+    static constexpr size_t kQ = kSgn + kSz[0] + kSz[1] + kSz[2] + kSz[3];  // [kHeads][D] q′ (fp32)
     static constexpr size_t kQsc = kQ + (size_t)kHeads * D * 4;     // [kHeads]
     static constexpr size_t kQin = kQsc + kHeads * 4 + 16;          // [kHeads][D] raw q (query dtype)
     static constexpr size_t kQg = kQin + (size_t)kHeads * D * 4;    // [kHeads][D] permuted q (fp32)
     static constexpr size_t kPerm = kQg + (size_t)kHeads * D * 4;   // [D] perm_k
-    static constexpr size_t kStage = (kPerm + D * 4 + 127) & ~(size_t)127;
+    static constexpr size_t kQ2 = kPerm + D * 4;                    // [kHeads][D] q″ (prod keys)
+    static constexpr size_t kQsc2 = kQ2 + (KP ? (size_t)kHeads * D * 4 : 0);  // [kHeads]
+    static constexpr size_t kStage = (kQsc2 + (KP ? kHeads * 4 : 0) + 127) & ~(size_t)127;
     static constexpr size_t kAlignSlack = kBig - 16;
     static constexpr size_t kLimit = 232448 - 2048;
-    static constexpr int kStagesFit = (int)((kLimit - kAlignSlack - kStage) / MStage<KO, KN, VO, VN>::kBytes);
+    static constexpr int kStagesFit = (int)((kLimit - kAlignSlack - kStage) / MStage<KO, KN, VO, VN, KP>::kBytes);
     static constexpr int kStages = kStagesFit < kMaxStages ? kStagesFit : kMaxStages;
     static_assert(kStages >= 4, "too few staging stages fit in shared memory");
-    static constexpr size_t kMain = kStage + (size_t)kStages * MStage<KO, KN, VO, VN>::kBytes;
+    static constexpr size_t kMain = kStage + (size_t)kStages * MStage<KO, KN, VO, VN, KP>::kBytes;
     // combine phase
     static constexpr size_t kWM = 0;
     static constexpr size_t kWL = kWM + W * kHeads * 4;
@@ -168,19 +185,40 @@ struct MixedAcc {
     float M, Mt, l;
 };
 
-template <int KO, int KN, int VO, int VN, bool FULL>
+// QJL terms (KP): AS = [Q″_hi; Q″_lo] fragments, stab the lane's sign-table base,
+// fSo, fSn the parts' score factors of the sign sums.
+template <int KO, int KN, int VO, int VN, bool KP, bool FULL>
 __device__ __forceinline__ void mixed_step(MixedAcc& st, const unsigned char* stp, int r0, int tb, int t1,
                                            const KDecoder<KO>& dko, const KDecoder<KN>& dkn, const Decoder<VO>& dvo,
-                                           const Decoder<VN>& dvn, const uint32_t (&AQ)[kKB][4], float fKo, float fKn,
-                                           const MixedTcArgs& a, size_t head0, int G, int g, int c) {
-    using ST = MStage<KO, KN, VO, VN>;
+                                           const Decoder<VN>& dvn, const uint32_t (&AQ)[kKB][4],
+                                           const uint32_t (&AS)[KP ? kKB : 1][4], uint32_t stab, float fKo, float fKn,
+                                           float fSo, float fSn, const MixedTcArgs& a, size_t head0, int G, int g,
+                                           int c) {
+    using ST = MStage<KO, KN, VO, VN, KP>;
     constexpr int NWKN = (24 * KN + 31) / 32;
-    // ---- scores of head g, outlier part (k blocks 0–1) and the rest (2–7)
-    float So[2][4], Sn[2][4];
+    // ---- scores of head g, outlier part (k blocks 0–1) and the rest (2–7); with
+    // prod keys the sign sums of the two parts as well
+    float So[2][4], Sn[2][4], Qo[KP ? 2 : 1][4], Qn[KP ? 2 : 1][4];
 #pragma unroll
     for (int n = 0; n < 2; ++n) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) So[n][i] = Sn[n][i] = 0.f;
+        if constexpr (KP) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) Qo[n][i] = Qn[n][i] = 0.f;
+            // the lane's sign bytes: outlier byte c, then the rest's bytes 3c … 3c + 2
+            const int row = r0 + 8 * n + g;
+            uint32_t sw[1];
+            lane_run<1, 24, 1>(stp + ST::kKNS + row * 12, c, sw);
+            const uint32_t ws = (uint32_t)stp[ST::kKOS + row * 4 + c] | (sw[0] << 8);
+#pragma unroll
+            for (int j = 0; j < kKB / 2; ++j) {  // byte j: k blocks 2j, 2j + 1
+                const uint4 f = lds128(field_off<8, 7>(&ws, 8 * j) | stab);
+                float (&acc)[4] = j == 0 ? Qo[n] : Qn[n];
+                mma16816(acc, AS[2 * j][0], AS[2 * j][1], AS[2 * j][2], AS[2 * j][3], f.x, f.y);
+                mma16816(acc, AS[2 * j + 1][0], AS[2 * j + 1][1], AS[2 * j + 1][2], AS[2 * j + 1][3], f.z, f.w);
+            }
+        }
         const int row = r0 + 8 * n + g;
         uint32_t wo[1], wn[NWKN];
         lane_run<KO, 8, 1>(stp + ST::kKOC + row * ST::kRKo, c, wo);
@@ -191,11 +229,23 @@ __device__ __forceinline__ void mixed_step(MixedAcc& st, const unsigned char* st
             dko.frag(wo, kb, b0, b1);
             mma16816(So[n], AQ[kb][0], AQ[kb][1], AQ[kb][2], AQ[kb][3], b0, b1);
         }
+        if constexpr (KN == 1) {
+            // 1-bit codes are ±c₁: the ±1 sign table gives their fragments over the
+            // run's contiguous dims (c₁ is folded into fKn)
+            static_assert(!(KN == 1) || KP, "1-bit codes of the rest need the sign table");
 #pragma unroll
-        for (int kb = 2; kb < kKB; ++kb) {
-            uint32_t b0, b1;
-            dkn.frag(wn, kb - 2, b0, b1);
-            mma16816(Sn[n], AQ[kb][0], AQ[kb][1], AQ[kb][2], AQ[kb][3], b0, b1);
+            for (int j = 0; j < 3; ++j) {
+                const uint4 f = lds128(field_off<8, 7>(wn, 8 * j) | stab);
+                mma16816(Sn[n], AQ[2 + 2 * j][0], AQ[2 + 2 * j][1], AQ[2 + 2 * j][2], AQ[2 + 2 * j][3], f.x, f.y);
+                mma16816(Sn[n], AQ[3 + 2 * j][0], AQ[3 + 2 * j][1], AQ[3 + 2 * j][2], AQ[3 + 2 * j][3], f.z, f.w);
+            }
+        } else {
+#pragma unroll
+            for (int kb = 2; kb < kKB; ++kb) {
+                uint32_t b0, b1;
+                dkn.frag(wn, kb - 2, b0, b1);
+                mma16816(Sn[n], AQ[kb][0], AQ[kb][1], AQ[kb][2], AQ[kb][3], b0, b1);
+            }
         }
     }
     // this lane's tokens: i = 0, 1 → 2c, 2c + 1; i = 2, 3 → 8 + 2c, 9 + 2c
@@ -207,11 +257,15 @@ __device__ __forceinline__ void mixed_step(MixedAcc& st, const unsigned char* st
         v[2] = y.x;
         v[3] = y.y;
     };
-    float kno[4], knn[4], vno[4], vnn[4];
+    float kno[4], knn[4], vno[4], vnn[4], kro[KP ? 4 : 1], krn[KP ? 4 : 1];
     norms(ST::kKON, kno);
     norms(ST::kKNN, knn);
     norms(ST::kVON, vno);
     norms(ST::kVNN, vnn);
+    if constexpr (KP) {
+        norms(ST::kKOR, kro);
+        norms(ST::kKNR, krn);
+    }
     // z = s·log2e + log2 max(‖v_o‖, ‖v_n‖), −∞ past the chunk
     // rows past the chunk may hold anything (whole stages are copied): their
     // exponents are −∞ and their norm ratios 0
@@ -225,7 +279,11 @@ __device__ __forceinline__ void mixed_step(MixedAcc& st, const unsigned char* st
         rv[i] = rcp(vm);
         ro[i] = live ? vno[i] * rv[i] : 0.f;  // ≤ 1
         rn[i] = live ? vnn[i] * rv[i] : 0.f;
-        const float s = fmaf(fKo * kno[i], So[n][j] + So[n][2 + j], fKn * knn[i] * (Sn[n][j] + Sn[n][2 + j]));
+        float s = fmaf(fKo * kno[i], So[n][j] + So[n][2 + j], fKn * knn[i] * (Sn[n][j] + Sn[n][2 + j]));
+        if constexpr (KP) {
+            s = fmaf(fSo * kno[i] * kro[i], Qo[n][j] + Qo[n][2 + j], s);
+            s = fmaf(fSn * knn[i] * krn[i], Qn[n][j] + Qn[n][2 + j], s);
+        }
         z[i] = live ? s + lv[i] : -INFINITY;
     }
     if (a.scores != nullptr && g < G) {
@@ -290,9 +348,9 @@ __device__ __forceinline__ void mixed_step(MixedAcc& st, const unsigned char* st
     }
 }
 
-template <int KO, int KN, int VO, int VN>
+template <int KO, int KN, int VO, int VN, bool KP>
 __device__ __forceinline__ void merge_mixed(const MixedTcArgs& a, unsigned char* smem, size_t head0, int G) {
-    using SM = MSmem<KO, KN, VO, VN>;
+    using SM = MSmem<KO, KN, VO, VN, KP>;
     constexpr int NT = SM::kThreads, NW = NT / 32, MR = SM::kMRow;
     float* wts = reinterpret_cast<float*>(smem + SM::kMWt);
     float* linv = reinterpret_cast<float*>(smem + SM::kML);
@@ -399,10 +457,11 @@ __device__ __forceinline__ void merge_mixed(const MixedTcArgs& a, unsigned char*
     }
 }
 
-template <int KO, int KN, int VO, int VN>
-__global__ void __launch_bounds__((kMW + 1) * 32, 1) decode_mixed_mma_kernel(const __grid_constant__ MixedTcArgs a) {
-    using SM = MSmem<KO, KN, VO, VN>;
-    using ST = MStage<KO, KN, VO, VN>;
+template <int KO, int KN, int VO, int VN, bool KP>
+__global__ void __launch_bounds__(MSmem<KO, KN, VO, VN, KP>::kThreads, 1)
+    decode_mixed_mma_kernel(const __grid_constant__ MixedTcArgs a) {
+    using SM = MSmem<KO, KN, VO, VN, KP>;
+    using ST = MStage<KO, KN, VO, VN, KP>;
     constexpr int W = SM::W;
     extern __shared__ __align__(128) unsigned char smem[];
     const uint32_t sbase = smem_addr(smem);
@@ -457,6 +516,10 @@ __global__ void __launch_bounds__((kMW + 1) * 32, 1) decode_mixed_mma_kernel(con
     const uint8_t* vcn = a.vc[1] + (size_t)rowbase * ST::kRVn;
     const float* vno = a.vn[0] + rowbase;
     const float* vnn = a.vn[1] + rowbase;
+    const uint8_t* kso = KP ? a.ks[0] + (size_t)rowbase * 4 : nullptr;
+    const uint8_t* ksn = KP ? a.ks[1] + (size_t)rowbase * 12 : nullptr;
+    const float* kro = KP ? a.kr[0] + rowbase : nullptr;
+    const float* krn = KP ? a.kr[1] + rowbase : nullptr;
 
     const uint32_t ring = smem_addr(mp + SM::kStage);
     __shared__ __align__(8) uint64_t s_full[SM::kStages], s_empty[SM::kStages];
@@ -478,6 +541,12 @@ __global__ void __launch_bounds__((kMW + 1) * 32, 1) decode_mixed_mma_kernel(con
         bulk_g2s(dst + ST::kVNC, vcn + (size_t)tb * ST::kRVn, rows * ST::kRVn, bar);
         bulk_g2s(dst + ST::kVON, vno + tb, rows * 4, bar);
         bulk_g2s(dst + ST::kVNN, vnn + tb, rows * 4, bar);
+        if constexpr (KP) {
+            bulk_g2s(dst + ST::kKOS, kso + (size_t)tb * 4, rows * 4, bar);
+            bulk_g2s(dst + ST::kKNS, ksn + (size_t)tb * 12, rows * 12, bar);
+            bulk_g2s(dst + ST::kKOR, kro + tb, rows * 4, bar);
+            bulk_g2s(dst + ST::kKNR, krn + tb, rows * 4, bar);
+        }
     };
     if (producer && lane == 0) {
         for (int i = 0; i < SM::kStages; ++i) {
@@ -524,6 +593,7 @@ __global__ void __launch_bounds__((kMW + 1) * 32, 1) decode_mixed_mma_kernel(con
         Table<KN>::fill(mp + SM::kTabKN, a.kcb[1], threadIdx.x, NC);
         Table<VO>::fill(mp + SM::kTabVO, a.vcb[0], threadIdx.x, NC);
         Table<VN>::fill(mp + SM::kTabVN, a.vcb[1], threadIdx.x, NC);
+        if constexpr (KP) KSignTable::fill(mp + SM::kTabS, threadIdx.x, NC);
         asm volatile("griddepcontrol.wait;" ::: "memory");
         {
             const int rowq = a.q_f32 ? D / 4 : D / 8;
@@ -560,14 +630,38 @@ __global__ void __launch_bounds__((kMW + 1) * 32, 1) decode_mixed_mma_kernel(con
                     qsh[g * D + 8 * job + 2 * c + 1] = acc[1] + acc[3];
                 }
             }
+            if constexpr (KP) {  // q″ = blockdiag(S_o, S_n)·(P q), the same way
+                float* qsh2 = reinterpret_cast<float*>(mp + SM::kQ2);
+#pragma unroll
+                for (int u = 0; u < kPer; ++u) {
+                    const int job = warp + u * W;
+                    if (job < kJobs) {
+                        uint4 sh[kKB / 2], sl[kKB / 2];
+                        blockdiag_b(a.kS_hi[0], a.kS_lo[0], a.kS_hi[1], a.kS_lo[1], 8 * job, g, c, sh, sl);
+                        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                        hilo_mma(acc, A, sh, sl);
+                        qsh2[g * D + 8 * job + 2 * c] = acc[0] + acc[2];
+                        qsh2[g * D + 8 * job + 2 * c + 1] = acc[1] + acc[3];
+                    }
+                }
+            }
         }
         consumers_sync();
         for (int h = warp; h < kHeads; h += W) {
-            float m1 = 0.f;
-            for (int j = lane; j < D; j += 32) m1 = fmaxf(m1, fabsf(qsh[h * D + j]));
+            float m1 = 0.f, m2 = 0.f;
+            for (int j = lane; j < D; j += 32) {
+                m1 = fmaxf(m1, fabsf(qsh[h * D + j]));
+                if constexpr (KP) m2 = fmaxf(m2, fabsf(reinterpret_cast<const float*>(mp + SM::kQ2)[h * D + j]));
+            }
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
-            if (lane == 0) qsc[h] = m1 > 0.f ? m1 : 1.f;
+            for (int o = 16; o > 0; o >>= 1) {
+                m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
+                m2 = fmaxf(m2, __shfl_xor_sync(0xffffffffu, m2, o));
+            }
+            if (lane == 0) {
+                qsc[h] = m1 > 0.f ? m1 : 1.f;
+                if constexpr (KP) reinterpret_cast<float*>(mp + SM::kQsc2)[h] = m2 > 0.f ? m2 : 1.f;
+            }
         }
         consumers_sync();
         read_length();
@@ -591,9 +685,36 @@ __global__ void __launch_bounds__((kMW + 1) * 32, 1) decode_mixed_mma_kernel(con
                     AQ[kb][2 * h + 1] = pack_h2(x0 - hf.x, x1 - hf.y);
                 }
         }
+        // [Q″_hi; Q″_lo] fragments of head g over the same dims (prod keys)
+        uint32_t AS[KP ? kKB : 1][4];
+        float fSo = 0.f, fSn = 0.f;
         const float scale2 = a.scale * kLog2e;
+        if constexpr (KP) {
+            const float* qsh2 = reinterpret_cast<const float*>(mp + SM::kQ2);
+            const float qs2 = reinterpret_cast<const float*>(mp + SM::kQsc2)[g], i2 = 1.f / qs2;
+            float q2[32];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) q2[k] = qsh2[g * D + 8 * c + k];
+#pragma unroll
+            for (int k = 0; k < 24; ++k) q2[8 + k] = qsh2[g * D + kDO + 24 * c + k];
+#pragma unroll
+            for (int kb = 0; kb < kKB; ++kb)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const float x0 = q2[4 * kb + 2 * h] * i2, x1 = q2[4 * kb + 2 * h + 1] * i2;
+                    const __half2 hh = __floats2half2_rn(x0, x1);
+                    const float2 hf = __half22float2(hh);
+                    AS[kb][2 * h] = *reinterpret_cast<const uint32_t*>(&hh);
+                    AS[kb][2 * h + 1] = pack_h2(x0 - hf.x, x1 - hf.y);
+                }
+            fSo = scale2 * a.kgamma[0] * qs2;
+            fSn = scale2 * a.kgamma[1] * qs2;
+        }
+        const uint32_t stab = KP ? KSignTable::lane_base(mp + SM::kTabS, lane) : 0u;
+        static_assert(KO >= 2, "outlier codes of at least two bits");
         const float fKo = scale2 * qsc[g] / a.kcb[0].lut_scale;
-        const float fKn = scale2 * qsc[g] / a.kcb[1].lut_scale;
+        // 1-bit codes of the rest go through the ±1 sign table: scale by c₁
+        const float fKn = KN == 1 ? scale2 * qsc[g] * a.kcb[1].c[1] : scale2 * qsc[g] / a.kcb[1].lut_scale;
         KDecoder<KO> dko;
         KDecoder<KN> dkn;
         Decoder<VO> dvo;
@@ -611,11 +732,11 @@ __global__ void __launch_bounds__((kMW + 1) * 32, 1) decode_mixed_mma_kernel(con
             const int tb = t0 + tile * kTile, r0 = (tile % kTilesPerStage) * kTile;
             const unsigned char* stp = mp + SM::kStage + (size_t)slot * ST::kBytes;
             if (tb + kTile <= t1)
-                mixed_step<KO, KN, VO, VN, true>(st, stp, r0, tb, t1, dko, dkn, dvo, dvn, AQ, fKo, fKn, a, head0, G, g,
-                                                 c);
+                mixed_step<KO, KN, VO, VN, KP, true>(st, stp, r0, tb, t1, dko, dkn, dvo, dvn, AQ, AS, stab, fKo, fKn,
+                                                     fSo, fSn, a, head0, G, g, c);
             else
-                mixed_step<KO, KN, VO, VN, false>(st, stp, r0, tb, t1, dko, dkn, dvo, dvn, AQ, fKo, fKn, a, head0, G,
-                                                  g, c);
+                mixed_step<KO, KN, VO, VN, KP, false>(st, stp, r0, tb, t1, dko, dkn, dvo, dvn, AQ, AS, stab, fKo,
+                                                      fKn, fSo, fSn, a, head0, G, g, c);
             __syncwarp();
             if (lane == 0) sm100::mbar_arrive(&s_empty[slot]);
         }
@@ -684,14 +805,14 @@ __global__ void __launch_bounds__((kMW + 1) * 32, 1) decode_mixed_mma_kernel(con
     }
     __syncthreads();
     if (!s_last) return;
-    merge_mixed<KO, KN, VO, VN>(a, smem, head0, G);
+    merge_mixed<KO, KN, VO, VN, KP>(a, smem, head0, G);
 }
 
-template <int KO, int KN, int VO, int VN>
+template <int KO, int KN, int VO, int VN, bool KP>
 int launch_mixed_tc(const MixedTcArgs& a, dim3 grid, cudaStream_t s) {
-    using SM = MSmem<KO, KN, VO, VN>;
+    using SM = MSmem<KO, KN, VO, VN, KP>;
     static_assert(SM::kBytes <= 232448 - 1024, "mixed decode shared memory above the per-CTA limit");
-    auto fn = decode_mixed_mma_kernel<KO, KN, VO, VN>;
+    auto fn = decode_mixed_mma_kernel<KO, KN, VO, VN, KP>;
     static std::atomic<uint64_t> smem_set{0};
     const int rc = ensure_smem_attr(smem_set, (const void*)fn, (int)SM::kBytes, "mixed decode smem attribute");
     if (rc != TQ_OK) return rc;
@@ -713,17 +834,24 @@ int launch_mixed_tc(const MixedTcArgs& a, dim3 grid, cudaStream_t s) {
 }  // namespace
 }  // namespace mmadec
 
-// (b_o, b_n) of keys and values: the instantiated pairs
-bool mixed_tc_bits_supported(int ko, int kn, int vo, int vn) {
+// code bits (b_o, b_n) of keys and values: the instantiated combinations
+bool mixed_tc_bits_supported(int ko, int kn, int vo, int vn, bool kp) {
     auto ok = [](int o, int n) { return (o == 3 && n == 2) || (o == 4 && n == 3) || (o == 4 && n == 2); };
+    if (kp) return ok(ko + 1, kn + 1) && vo == ko + 1 && vn == kn + 1;
     return ok(ko, kn) && ko == vo && kn == vn;
 }
 
 int launch_mixed_decode_tc(const MixedTcArgs& a, dim3 grid, int ko, int kn, cudaStream_t s) {
     using namespace mmadec;
-    if (ko == 3 && kn == 2) return launch_mixed_tc<3, 2, 3, 2>(a, grid, s);
-    if (ko == 4 && kn == 3) return launch_mixed_tc<4, 3, 4, 3>(a, grid, s);
-    if (ko == 4 && kn == 2) return launch_mixed_tc<4, 2, 4, 2>(a, grid, s);
+    if (a.kp) {
+        if (ko == 2 && kn == 1) return launch_mixed_tc<2, 1, 3, 2, true>(a, grid, s);
+        if (ko == 3 && kn == 2) return launch_mixed_tc<3, 2, 4, 3, true>(a, grid, s);
+        if (ko == 3 && kn == 1) return launch_mixed_tc<3, 1, 4, 2, true>(a, grid, s);
+    } else {
+        if (ko == 3 && kn == 2) return launch_mixed_tc<3, 2, 3, 2, false>(a, grid, s);
+        if (ko == 4 && kn == 3) return launch_mixed_tc<4, 3, 4, 3, false>(a, grid, s);
+        if (ko == 4 && kn == 2) return launch_mixed_tc<4, 2, 4, 2, false>(a, grid, s);
+    }
     return fail(TQ_EUNSUPPORTED, "tensor-core mixed decode: bits (%d, %d)", ko, kn);
 }
 

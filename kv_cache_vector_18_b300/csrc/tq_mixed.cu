@@ -435,7 +435,13 @@ int launch_mixed_tc_path(const MixedDecode& m, const MixedShape& p, cudaStream_t
         a.kPi_lo[i] = m.hk[i]->dp.Pi_lo;
         a.vPiT_hi[i] = m.hv[i]->dp.PiT_hi;
         a.vPiT_lo[i] = m.hv[i]->dp.PiT_lo;
+        a.ks[i] = m.kc[i].signs;
+        a.kr[i] = m.kc[i].rnorm;
+        a.kS_hi[i] = m.hk[i]->dp.S_hi;
+        a.kS_lo[i] = m.hk[i]->dp.S_lo;
+        a.kgamma[i] = m.hk[i]->gamma;
     }
+    a.kp = m.hk[0]->hp.variant == TQ_PROD;
     a.seq_lens = m.seq_lens;
     a.perm_k = m.perm_k;
     a.perm_v = m.perm_v;
@@ -544,9 +550,13 @@ bool mixed_decode_tc_supported(const tq_ctx& hko, const tq_ctx& hkn, const tq_ct
                                int T_max) {
     const tq_ctx* hs[4] = {&hko, &hkn, &hvo, &hvn};
     for (const tq_ctx* h : hs)
-        if (h->hp.variant != TQ_MSE || h->dp.Pi_hi == nullptr || h->dp.PiT_hi == nullptr) return false;
+        if (h->dp.Pi_hi == nullptr || h->dp.PiT_hi == nullptr) return false;
+    // values mse; keys both mse, or both prod with their S in bf16 hi/lo
+    const bool kp = hko.hp.variant == TQ_PROD;
+    if (hvo.hp.variant != TQ_MSE || hvn.hp.variant != TQ_MSE || hkn.hp.variant != hko.hp.variant) return false;
+    if (kp && (hko.dp.S_hi == nullptr || hkn.dp.S_hi == nullptr)) return false;
     return hko.hp.d == 32 && hkn.hp.d == 96 && hvo.hp.d == 32 && hvn.hp.d == 96 && T_max % 4 == 0 &&
-           hko.num_sms > 0 && mixed_tc_bits_supported(hko.hp.b_mse, hkn.hp.b_mse, hvo.hp.b_mse, hvn.hp.b_mse);
+           hko.num_sms > 0 && mixed_tc_bits_supported(hko.hp.b_mse, hkn.hp.b_mse, hvo.hp.b_mse, hvn.hp.b_mse, kp);
 }
 
 int mixed_plan(int d, int sms, bool vprod, bool tc, int B, int Hq, int Hkv, int T_max, MixedShape* plan,

@@ -1,6 +1,7 @@
 // Arguments of the tensor-core mixed-precision decode (tq_decode_mixed_mma.cu):
 // keys and values each split into an outlier part (index 0: 32 channels) and the
-// rest (index 1: 96 channels) of d = 128, every part an mse quantizer.
+// rest (index 1: 96 channels) of d = 128; value parts mse quantizers, key parts
+// both mse or both prod (kp).
 #pragma once
 
 #include <cstdint>
@@ -36,10 +37,21 @@ struct MixedTcArgs {
     const uint16_t* vPiT_hi[2];
     const uint16_t* vPiT_lo[2];
     int* status;  // the outlier key handle's status word
+    // prod key parts: QJL sign planes (4 and 12 bytes per row), residual norms,
+    // S of each part (bf16 hi/lo, row-major) and √(π/2)/d_p
+    int kp;
+    const uint8_t* ks[2];
+    const float* kr[2];
+    const uint16_t* kS_hi[2];
+    const uint16_t* kS_lo[2];
+    float kgamma[2];
 };
 
-// The (b_o, b_n) pairs with a tensor-core kernel (keys and values alike).
-bool mixed_tc_bits_supported(int ko, int kn, int vo, int vn);
+// The code bits (b_o, b_n) of the key and value parts with a tensor-core kernel:
+// mse keys (3, 2), (4, 3), (4, 2) with values alike; prod keys (codes (2, 1),
+// (3, 2), (3, 1), i.e. 3/2, 4/3, 4/2 bits with the sign) with mse values of the
+// keys' total bits.
+bool mixed_tc_bits_supported(int ko, int kn, int vo, int vn, bool kp);
 int launch_mixed_decode_tc(const MixedTcArgs& a, dim3 grid, int ko, int kn, cudaStream_t s);
 
 }  // namespace tq

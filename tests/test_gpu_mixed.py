@@ -197,7 +197,7 @@ def test_mixed_rejects_bad_arguments(tq):
     torch.cuda.synchronize()
 
 
-def _mixed_case(tq, B, Hq, Hkv, T, bo, bn, seed, q_dtype="bf16"):
+def _mixed_case(tq, B, Hq, Hkv, T, bo, bn, seed, q_dtype="bf16", kv="mse"):
     d = 128
     rng = np.random.default_rng(seed)
     hot_k = rng.choice(d, 32, replace=False)
@@ -207,7 +207,7 @@ def _mixed_case(tq, B, Hq, Hkv, T, bo, bn, seed, q_dtype="bf16"):
     q = synthetic.gaussian((B, Hq, d), seed=seed + 3, dtype=q_dtype)
     pk, _ = tq.select_outlier_channels(K.cuda(), 32)
     pv, _ = tq.select_outlier_channels(V.cuda(), 32)
-    mk = tq.MixedQuantizer(pk, 32, bo, bn, "mse", seed_o=seed + 21, seed_n=seed + 22)
+    mk = tq.MixedQuantizer(pk, 32, bo, bn, kv, seed_o=seed + 21, seed_n=seed + 22)
     mv = tq.MixedQuantizer(pv, 32, bo, bn, "mse", seed_o=seed + 23, seed_n=seed + 24)
     kc, vc = mk.quantize(K.cuda()), mv.quantize(V.cuda())
     return mk, mv, q, kc, vc
@@ -229,6 +229,34 @@ def _mixed_ref(mk, mv, q, kc, vc, lens, Hkv, T):
 def test_mixed_decode_tensor_core_path(tq, bo, bn, B, Hq, Hkv, T, lens, q_dtype):
     # T_max % 4 == 0, 32 outlier channels, mse parts: the tensor-core mixed decode
     mk, mv, q, kc, vc = _mixed_case(tq, B, Hq, Hkv, T, bo, bn, seed=bo * 10 + bn + T, q_dtype=q_dtype)
+    sl = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    out, sc = tq.mixed_decode_attention(mk, mv, q.cuda(), kc, vc, sl, Hkv, T, return_scores=True)
+    torch.cuda.synchronize()
+    assert mk.qo.device_status() == 0
+    ref, ref_sc = _mixed_ref(mk, mv, q, kc, vc, lens, Hkv, T)
+    check_attention(f64(out), ref)
+    g = f64(sc)
+    mask = ~np.isnan(ref_sc)
+    assert np.array_equal(np.isnan(g), ~mask)
+    assert np.max(np.abs(g[mask] - ref_sc[mask])) <= 1e-3 * max(1.0, np.max(np.abs(ref_sc[mask])))
+    if 0 in lens:
+        assert np.all(f64(out)[lens.index(0)] == 0)
+
+
+@pytest.mark.parametrize("bo,bn,B,Hq,Hkv,T,lens,q_dtype", [
+    (3, 2, 3, 16, 2, 1028, [1028, 17, 1], "bf16"),      # the page's split; two head blocks; ragged tails
+    (4, 3, 2, 8, 1, 700 + 32, [0, 731], "f32"),          # an empty sequence, an fp32 query
+    (4, 2, 1, 8, 1, 8192, [8191], "bf16"),               # many splits: several merge rounds
+])
+def test_mixed_decode_tensor_core_prod_keys(tq, bo, bn, B, Hq, Hkv, T, lens, q_dtype):
+    # prod key parts (codes of b − 1 bits and QJL signs per part) with mse values of
+    # the same bits: the tensor-core mixed decode (its workspace is the one the mse
+    # keys of the same shape take, not the CUDA-core path's)
+    mk, mv, q, kc, vc = _mixed_case(tq, B, Hq, Hkv, T, bo, bn, seed=bo * 10 + bn + T + 1, q_dtype=q_dtype,
+                                    kv="prod")
+    mse_k = tq.MixedQuantizer(mk.perm, 32, bo, bn, "mse", seed_o=1, seed_n=2)
+    assert tq.mixed_decode_workspace_bytes(mk, mv, B, Hq, Hkv, T) == \
+        tq.mixed_decode_workspace_bytes(mse_k, mv, B, Hq, Hkv, T)
     sl = torch.tensor(lens, dtype=torch.int32, device="cuda")
     out, sc = tq.mixed_decode_attention(mk, mv, q.cuda(), kc, vc, sl, Hkv, T, return_scores=True)
     torch.cuda.synchronize()
