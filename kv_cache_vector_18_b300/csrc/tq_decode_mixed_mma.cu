@@ -36,7 +36,6 @@ namespace {
 constexpr int kDO = 32;        // outlier dims of the frame
 constexpr int kDN = D - kDO;   // the rest
 constexpr int kMW = 11;        // consumer warps (plus one producer warp)
-constexpr int kMWP = 7;        // with prod key parts (more registers per lane)
 
 // Bits [c·NB·8·LEN/8 …) of a row: lane c's run of LEN codes of NB bits, returned
 // as NW words (LSB first).  The row starts on a 4-byte boundary; the read may run
@@ -85,7 +84,7 @@ struct MStage {
 // phases reuse the bytes.
 template <int KO, int KN, int VO, int VN, bool KP = false>
 struct MSmem {
-    static constexpr int W = KP ? kMWP : kMW;
+    static constexpr int W = kMW;
     static constexpr int kThreads = (W + 1) * 32;
     static constexpr size_t kSz[4] = {Table<KO>::kBytes, Table<KN>::kBytes, Table<VO>::kBytes, Table<VN>::kBytes};
     static constexpr size_t kBig = 32768;
