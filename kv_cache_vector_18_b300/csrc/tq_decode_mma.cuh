@@ -630,15 +630,15 @@ __device__ __forceinline__ void step(Acc<VP>& st, const unsigned char* stp, int 
                                      uint32_t stab, const uint32_t (&AQ)[kKB][4], const uint32_t (&AS)[kKB][4],
                                      float fK, float fS, const SplitArgs& a, size_t head0, int G, int g, int c) {
     using ST = Stage<KB, KP, VB, VP>;
-    // ---- scores of head g: S1 = [Q′_hi; Q′_lo]·K̃ᵀ (codes)
+    // ---- scores of head g: S1 = [Q′_hi; Q′_lo]·K̃ᵀ (codes), S2 = [Q″_hi; Q″_lo]·Zᵀ (QJL signs)
     // accumulator of group n: [0] (hi, token 2c) [1] (hi, 2c + 1) [2] (lo, 2c) [3] (lo, 2c + 1)
     // Each score sums its k16 blocks in two independent accumulator chains (even
     // and odd blocks), so that an MMA need not wait for the one before it.
-    float S1[2][4], S1x[2][4];
+    float S1[2][4], S2[2][4], S1x[2][4], S2x[2][4];
 #pragma unroll
     for (int n = 0; n < 2; ++n) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) S1[n][i] = S1x[n][i] = 0.f;
+        for (int i = 0; i < 4; ++i) S1[n][i] = S2[n][i] = S1x[n][i] = S2x[n][i] = 0.f;
         if constexpr (KB > 0) {
             uint32_t w[KB];
             read_words<KB>(w, stp + ST::kKC + (r0 + 8 * n + g) * ST::kRK + c * (KB * 4));
@@ -649,36 +649,20 @@ __device__ __forceinline__ void step(Acc<VP>& st, const unsigned char* stp, int 
                 mma16816((kb & 1) ? S1x[n] : S1[n], AQ[kb][0], AQ[kb][1], AQ[kb][2], AQ[kb][3], b0, b1);
             }
         }
+        if constexpr (KP) {
+            const uint32_t ws = *reinterpret_cast<const uint32_t*>(stp + ST::kKS + (r0 + 8 * n + g) * 16 + c * 4);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) S1[n][i] += S1x[n][i];
-    }
-    // ---- QJL sums Zᵀ-side: the signs are the A operand (16 tokens × 16 dims; a
-    // token's B fragment of the other orientation is its row of the A fragment)
-    // and Q″_hi the B operand (column g: head g), so one MMA per k16 block covers
-    // the tile.  The 16 × 8 token × head result is rounded to f16 and transposed
-    // (movmatrix) into this lane's layout: head g, tokens 2c, 2c + 1, 8 + 2c, 9 + 2c.
-    // The QJL term is a small correction (γ = √(π/2)/d times ‖r‖): Q″ without its
-    // low half and an f16 sum keep it to ~2⁻¹¹ of itself.
-    float q2v[4] = {0.f, 0.f, 0.f, 0.f};
-    if constexpr (KP) {
-        float Q[4] = {0.f, 0.f, 0.f, 0.f}, Qx[4] = {0.f, 0.f, 0.f, 0.f};
-        const uint32_t ws0 = *reinterpret_cast<const uint32_t*>(stp + ST::kKS + (r0 + g) * 16 + c * 4);
-        const uint32_t ws1 = *reinterpret_cast<const uint32_t*>(stp + ST::kKS + (r0 + 8 + g) * 16 + c * 4);
-#pragma unroll
-        for (int j = 0; j < kKB / 2; ++j) {
-            const uint4 f0 = lds128(field_off<8, 7>(&ws0, 8 * j) | stab);
-            const uint4 f1 = lds128(field_off<8, 7>(&ws1, 8 * j) | stab);
-            mma16816(Q, f0.x, f1.x, f0.y, f1.y, AS[2 * j][0], AS[2 * j][2]);
-            mma16816(Qx, f0.z, f1.z, f0.w, f1.w, AS[2 * j + 1][0], AS[2 * j + 1][2]);
+            for (int j = 0; j < kKB / 2; ++j) {
+                const uint4 f = lds128(field_off<8, 7>(&ws, 8 * j) | stab);
+                mma16816(S2[n], AS[2 * j][0], AS[2 * j][1], AS[2 * j][2], AS[2 * j][3], f.x, f.y);
+                mma16816(S2x[n], AS[2 * j + 1][0], AS[2 * j + 1][1], AS[2 * j + 1][2], AS[2 * j + 1][3], f.z, f.w);
+            }
         }
-        const uint32_t t0 = mov_trans(pack_h2(Q[0] + Qx[0], Q[1] + Qx[1]));
-        const uint32_t t1 = mov_trans(pack_h2(Q[2] + Qx[2], Q[3] + Qx[3]));
-        const float2 u0 = __half22float2(*reinterpret_cast<const __half2*>(&t0));
-        const float2 u1 = __half22float2(*reinterpret_cast<const __half2*>(&t1));
-        q2v[0] = u0.x;
-        q2v[1] = u0.y;
-        q2v[2] = u1.x;
-        q2v[3] = u1.y;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            S1[n][i] += S1x[n][i];
+            S2[n][i] += S2x[n][i];
+        }
     }
     // this lane's tokens: i = 0, 1 → 2c, 2c + 1; i = 2, 3 → 8 + 2c, 9 + 2c
     auto norms = [&](int off, float (&v)[4]) {
@@ -702,7 +686,7 @@ __device__ __forceinline__ void step(Acc<VP>& st, const unsigned char* stp, int 
         lv[i] = lg2(vv);
         rv[i] = rcp(vv);
         float v = fK * (S1[n][j] + S1[n][2 + j]);
-        if constexpr (KP) v = fmaf(fS * kr[i], q2v[i], v);
+        if constexpr (KP) v = fmaf(fS * kr[i], S2[n][j] + S2[n][2 + j], v);
         z[i] = fmaf(kn[i], v, lv[i]);
         if constexpr (!FULL)
             if (tb + 8 * n + 2 * c + j >= t1) z[i] = -INFINITY;
