@@ -127,6 +127,16 @@ def test_scores_output_small_groups(tq, Hq, Hkv, T, lens, vv):
         assert np.max(np.abs(gs[b, :, :L] - rs[b, :, :L])) <= 1e-3 * max(1.0, np.max(np.abs(rs[b, :, :L])))
 
 
+@pytest.mark.parametrize("kb", [1, 2])
+def test_decode_low_bit_prod_keys_heavy_tailed(tq, kb):
+    # prod keys of 1 and 2 bits, where the QJL term is all or most of the score,
+    # on heavy-tailed rows with eight query heads per KV head: the score path's
+    # precision (Q″ as f16 hi + lo) is what keeps these inside the bound
+    g, r = _run(tq, B=2, Hq=16, Hkv=2, T=2000, d=128, kb=kb, kv="prod", vb=3, vv="mse", lens=[2000, 1500],
+                dist="t", seed=kb * 10)
+    check_attention(g, r)
+
+
 def test_decode_workspace_too_small(tq):
     from kv_cache_vector_18_b300 import _lib
     kq = tq.Quantizer(128, 3, "prod", seed=1)
