@@ -972,10 +972,16 @@ def run_mixed(args) -> int:
     def step():
         tq.mixed_quantize_kv(mk, mv, Kd, Vd, kc, vc)
         tq.mixed_decode_attention(mk, mv, qd, kc, vc, ld, Hkv, T, workspace=ws, out=out)
+    # the same split with prod key parts (codes of one bit fewer + QJL signs per part)
+    mkp = tq.MixedQuantizer(pk, d_o, bo, bn, "prod", seed_o=10, seed_n=12)
+    kcp = mkp.quantize(Kd)
+    wsp = torch.empty(tq.mixed_decode_workspace_bytes(mkp, mv, B, Hq, Hkv, T), dtype=torch.uint8, device=dev)
     calls = {"quantize_k": lambda: mk.quantize(Kd, out=kc), "quantize_v": lambda: mv.quantize(Vd, out=vc),
              "quantize_kv": lambda: tq.mixed_quantize_kv(mk, mv, Kd, Vd, kc, vc),
              "decode": lambda: tq.mixed_decode_attention(mk, mv, qd, kc, vc, ld, Hkv, T, workspace=ws, out=out),
-             "step": step}
+             "step": step,
+             "decode_prod_keys": lambda: tq.mixed_decode_attention(mkp, mv, qd, kcp, vc, ld, Hkv, T, workspace=wsp,
+                                                                   out=out)}
     for fn in calls.values():
         fn()
     torch.cuda.synchronize()
@@ -983,6 +989,9 @@ def run_mixed(args) -> int:
     nbytes = {"quantize_k": n * (2 * d + rec), "quantize_v": n * (2 * d + rec),
               "quantize_kv": 2 * n * (2 * d + rec), "decode": int(lens.sum()) * Hkv * 2 * rec + B * Hq * d * 6}
     nbytes["step"] = nbytes["quantize_kv"] + nbytes["decode"]
+    # prod key parts: codes of one bit fewer plus 32 + 96 sign bits and two residual norms
+    rec_kp = ((bo - 1) * d_o // 8 + 4 + d_o // 8 + 4) + ((bn - 1) * (d - d_o) // 8 + 4 + (d - d_o) // 8 + 4)
+    nbytes["decode_prod_keys"] = int(lens.sum()) * Hkv * (rec_kp + rec) + B * Hq * d * 6
     peaks = load_peaks()
     res = {}
     for name, fn in calls.items():
@@ -1011,7 +1020,8 @@ def run_mixed(args) -> int:
     dm = dist(mk.dequantize(mk.quantize(xs)))
     u2, u3 = tq.Quantizer(d, 2, "mse", seed=10), tq.Quantizer(d, 3, "mse", seed=10)
     d2, d3 = dist(u2.dequantize(u2.quantize(xs))), dist(u3.dequantize(u3.quantize(xs)))
-    print(json.dumps({"mixed": "outlier channels 32 x 3 bits + 96 x 2 bits, mse, K and V",
+    print(json.dumps({"mixed": "outlier channels 32 x 3 bits + 96 x 2 bits, mse, K and V (decode_prod_keys: prod "
+                               "key parts of the same bits)",
                       "workload": spec["name"], "code_bits_per_channel": (d_o * bo + (d - d_o) * bn) / d,
                       "record_bytes": rec, "calls": res, "peak_gbs": peaks["hbm_gbs"],
                       "distortion": {"mixed": dm, "uniform_b2": d2, "uniform_b3": d3},
