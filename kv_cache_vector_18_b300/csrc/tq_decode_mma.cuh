@@ -1178,7 +1178,33 @@ __global__ void __launch_bounds__((Warps<VP>::value + 1) * 32, 1) decode_split_m
         }
         sm100::fence_barrier_init();
     }
+    // A CTA whose chunk starts at or past its sequence's length has no tokens: it
+    // skips the staging and the prologue and contributes an empty partial (M = −∞,
+    // l = 0) to the merge.  Thread 0 reads the length before griddepcontrol.wait as
+    // a hint and, when it says "empty", waits and reads it again before deciding
+    // for the CTA (a chunk that the hint wrongly calls empty takes the ordinary
+    // path, only without its prologue overlap); the ragged batched workload has
+    // about one such CTA per sequence in four.  Only the small-group variant (G4,
+    // the batched workload's) has this path: in the eight-head variant the extra
+    // branch changed the register allocation and cost 3 % of the 131072-token
+    // decode.
+    constexpr bool kSkip = !AA && G4;
+    __shared__ int s_skip;
+    if constexpr (kSkip) {
+        if (threadIdx.x == 0) {
+            int Lh;
+            asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(Lh) : "l"(a.seq_lens + b) : "memory");
+            int skip = 0;
+            if (t0 >= Lh) {
+                asm volatile("griddepcontrol.wait;" ::: "memory");
+                const int L = a.seq_lens[b];
+                skip = t0 >= L;
+            }
+            s_skip = skip;
+        }
+    }
     __syncthreads();
+    const bool skip = kSkip && s_skip != 0;
     auto consumers_sync = [] { asm volatile("bar.sync 1, %0;" ::"n"(W * 32) : "memory"); };
 
     Acc<VP> st;
@@ -1193,7 +1219,9 @@ __global__ void __launch_bounds__((Warps<VP>::value + 1) * 32, 1) decode_split_m
     st.Mt = -INFINITY;
     st.l = 0.f;
 
-    if (producer) {
+    if (skip) {
+        // no tokens: straight to the combine (the partial is M = −∞, l = 0, O = 0)
+    } else if (producer) {
         // ---- producer: the first stages, then each stage again once its four
         // tiles have been consumed
         bool live = true;
