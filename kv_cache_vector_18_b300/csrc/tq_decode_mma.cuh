@@ -43,6 +43,13 @@
 // loads and release each stage on an "empty" mbarrier (every wait is bounded).
 // The last CTA of each (batch, KV head, head block) to finish merges every
 // split's partial and applies Π_vᵀ on the tensor cores (no merge launch).
+//
+// Variants (kernel template flags): with at most four query heads per KV head
+// (G4) the scores and QJL sums take the keys and signs as the A operand instead
+// (step4: one MMA per k16 block for the 16 tokens), and a CTA whose chunk lies
+// past its sequence's length skips its staging and prologue; behind the
+// decode-step append with long chunks (AA) the CTA streams the rows below the
+// pre-append length before waiting for the append.
 #pragma once
 
 #include <math.h>
