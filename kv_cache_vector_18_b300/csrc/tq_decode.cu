@@ -341,7 +341,7 @@ int launch_d(const tq_ctx& hk, const tq_ctx& hv, const DecodeShape& p, const voi
             const int rc = launch_clear_tickets(cnt, p.B * p.Hq, s);
             if (rc != TQ_OK) return rc;
         }
-        return launch_split_mma_any(a, dim3(p.n_splits, p.Hkv * a.n_hblocks, p.B), hk.hp.b_mse, kprod, hv.hp.b_mse,
+        return launch_split_mma_any(a, dim3(p.B, p.Hkv * a.n_hblocks, p.n_splits), hk.hp.b_mse, kprod, hv.hp.b_mse,
                                     vprod, true, s);
     }
 

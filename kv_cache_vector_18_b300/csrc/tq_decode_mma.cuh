@@ -1094,7 +1094,10 @@ __global__ void __launch_bounds__((Warps<VP>::value + 1) * 32, 1) decode_split_m
 
     const int hb = blockIdx.y % a.n_hblocks, kvh = blockIdx.y / a.n_hblocks;
     const int G = min(kHeads, a.G - hb * kHeads);
-    const int split = blockIdx.x, b = blockIdx.z;
+    // the grid is (batch, KV head × head block, split): CTAs start split by split,
+    // so with ragged lengths the full chunks go first and the partial and empty
+    // ones (the later splits of short sequences) last
+    const int split = blockIdx.z, b = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
     const int t0 = split * a.chunk;
     // Lengths, cache planes, merge tickets and (unless a.after_append) the queries may
