@@ -1197,8 +1197,9 @@ __global__ void __launch_bounds__((Warps<VP>::value + 1) * 32, 1) decode_split_m
     // about one such CTA per sequence in four.  Only the small-group variant (G4,
     // the batched workload's) has this path: in the eight-head variant the extra
     // branch changed the register allocation and cost 3 % of the 131072-token
-    // decode.
-    constexpr bool kSkip = !AA && G4;
+    // decode.  Behind the decode-step append the length read after the wait is
+    // the bumped one, so a chunk that starts at the new row is not skipped.
+    constexpr bool kSkip = G4;
     __shared__ int s_skip;
     if constexpr (kSkip) {
         if (threadIdx.x == 0) {
